@@ -1,0 +1,190 @@
+"""CPU oracle (fp64) for the sampled-token logprob path -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
+may import this package.  The product path (``bit_consistent_logprob_gb300``)
+never imports it and has no CPU fallback.  The arithmetic lives in
+``oracle/oracle.c`` (plain C, fp64, OpenMP over rows); this module only builds
+it with gcc and marshals numpy arrays through ctypes.
+
+Functions and the passages they follow are listed in the header of
+``oracle.c``.  Parity status: every function is pinned by the ``not gpu`` tests
+in ``tests/test_oracle.py`` (exact rational arithmetic, closed forms, golden
+values under ``tests/golden/``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_CFLAGS = ["-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared", "-std=c11"]
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into oracle/_build/liboracle.so (gcc, no -march flags)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"])
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        i64, i32 = ctypes.c_int64, ctypes.c_int32
+        p = ctypes.c_void_p
+        lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_logits.argtypes = [p, i64, p, i64, i64, p, i64, p]
+        lib.oracle_logprobs.argtypes = [p, i64, p, p, i64, i64, p, i64, p, p]
+        lib.oracle_log_softmax.argtypes = [p, i64, p, i64, i64, p, i64, p]
+        lib.oracle_leaf_sums.argtypes = [p, p, i64, i32, p]
+        lib.oracle_tree_fp32.argtypes = [p, i32]
+        lib.oracle_tree_fp32.restype = ctypes.c_float
+        lib.oracle_tree_fp32_many.argtypes = [p, i32, i64, p]
+        lib.oracle_importance_weights.argtypes = [p, p, p, i64, p, p, p, p]
+        for f in (lib.oracle_logits, lib.oracle_logprobs, lib.oracle_log_softmax,
+                  lib.oracle_leaf_sums, lib.oracle_tree_fp32_many,
+                  lib.oracle_importance_weights):
+            f.restype = None
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray) -> ctypes.c_void_p:
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _u16_2d(a) -> np.ndarray:
+    """Accept a numpy uint16/int16 array or a torch bf16 tensor; return uint16 [rows, cols]."""
+    if hasattr(a, "dtype") and str(a.dtype) == "torch.bfloat16":
+        import torch  # local: only the bf16 view needs torch
+
+        a = a.detach().to("cpu").contiguous().view(torch.int16).numpy()
+    a = np.asarray(a)
+    if a.dtype == np.int16:
+        a = a.view(np.uint16)
+    if a.dtype != np.uint16 or a.ndim != 2:
+        raise TypeError("expected a 2-D bf16 bit array")
+    return a
+
+
+def _rows_arg(rows, T: int) -> np.ndarray:
+    if rows is None:
+        return np.arange(T, dtype=np.int64)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    if rows.size and (rows.min() < 0 or rows.max() >= T):
+        raise IndexError("row index out of range")
+    return rows
+
+
+def num_threads() -> int:
+    """Number of OpenMP threads the oracle uses."""
+    return int(_load().oracle_num_threads())
+
+
+def logits(X, W, rows=None) -> np.ndarray:
+    """fp64 logits z[r, v] = sum_k X[rows[r], k] W[v, k]."""
+    X, W = _u16_2d(X), _u16_2d(W)
+    Xc = np.ascontiguousarray(X)
+    Wc = np.ascontiguousarray(W)
+    T, H = Xc.shape
+    V = Wc.shape[0]
+    assert Wc.shape[1] == H
+    r = _rows_arg(rows, T)
+    out = np.empty((r.size, V), dtype=np.float64)
+    _load().oracle_logits(_ptr(Xc), H, _ptr(Wc), H, V, _ptr(r), r.size, _ptr(out))
+    return out
+
+
+def logprobs(X, W, ids, rows=None):
+    """Sampled-token logprob and log-partition for the listed rows (fp64).
+
+    Returns (logp[nrows], logZ[nrows]).  ids is indexed by row number."""
+    X, W = _u16_2d(X), _u16_2d(W)
+    Xc = np.ascontiguousarray(X)
+    Wc = np.ascontiguousarray(W)
+    T, H = Xc.shape
+    V = Wc.shape[0]
+    assert Wc.shape[1] == H
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    assert ids.shape == (T,)
+    r = _rows_arg(rows, T)
+    logp = np.empty(r.size, dtype=np.float64)
+    logZ = np.empty(r.size, dtype=np.float64)
+    _load().oracle_logprobs(_ptr(Xc), H, _ptr(Wc), _ptr(ids), H, V, _ptr(r), r.size,
+                            _ptr(logp), _ptr(logZ))
+    return logp, logZ
+
+
+def log_softmax(X, W, rows=None) -> np.ndarray:
+    """Full fp64 log-softmax over the vocabulary for the listed rows: [nrows, V]."""
+    X, W = _u16_2d(X), _u16_2d(W)
+    Xc = np.ascontiguousarray(X)
+    Wc = np.ascontiguousarray(W)
+    T, H = Xc.shape
+    V = Wc.shape[0]
+    r = _rows_arg(rows, T)
+    out = np.empty((r.size, V), dtype=np.float64)
+    _load().oracle_log_softmax(_ptr(Xc), H, _ptr(Wc), H, V, _ptr(r), r.size, _ptr(out))
+    return out
+
+
+def leaf_sums(xrow, wrow, n_leaves: int) -> np.ndarray:
+    """fp64 sums over each of the n_leaves contiguous K leaves of one (row, vocab) pair."""
+    x = _u16_2d(xrow.reshape(1, -1))[0]
+    w = _u16_2d(wrow.reshape(1, -1))[0]
+    H = x.shape[0]
+    if H % n_leaves or w.shape[0] != H:
+        raise ValueError("H must be a multiple of n_leaves and the rows must match")
+    out = np.empty(n_leaves, dtype=np.float64)
+    xc, wc = np.ascontiguousarray(x), np.ascontiguousarray(w)
+    _load().oracle_leaf_sums(_ptr(xc), _ptr(wc), H, n_leaves, _ptr(out))
+    return out
+
+
+def tree_fp32(P) -> np.ndarray:
+    """Fixed pairwise fp32 tree over the last axis of P ([..., N], N a power of two)."""
+    P = np.ascontiguousarray(np.asarray(P, dtype=np.float32))
+    N = P.shape[-1]
+    flat = P.reshape(-1, N)
+    out = np.empty(flat.shape[0], dtype=np.float32)
+    _load().oracle_tree_fp32_many(_ptr(flat), N, flat.shape[0], _ptr(out))
+    return out.reshape(P.shape[:-1])
+
+
+def importance_weights(logp_pi, logp_mu, mask=None):
+    """w = exp(log pi - log mu), term = w - 1 - log w, D3 = mean term over valid tokens.
+
+    Returns (w f64[T], term f64[T], d3 float, n_valid int)."""
+    a = np.ascontiguousarray(np.asarray(logp_pi, dtype=np.float32))
+    b = np.ascontiguousarray(np.asarray(logp_mu, dtype=np.float32))
+    assert a.shape == b.shape and a.ndim == 1
+    T = a.size
+    m = None
+    if mask is not None:
+        m = np.ascontiguousarray(np.asarray(mask).astype(np.uint8))
+        assert m.shape == (T,)
+    w = np.empty(T, dtype=np.float64)
+    term = np.empty(T, dtype=np.float64)
+    d3 = np.zeros(1, dtype=np.float64)
+    nv = np.zeros(1, dtype=np.int64)
+    _load().oracle_importance_weights(_ptr(a), _ptr(b), None if m is None else _ptr(m), T,
+                                      _ptr(w), _ptr(term), _ptr(d3), _ptr(nv))
+    return w, term, float(d3[0]), int(nv[0])

@@ -1,0 +1,191 @@
+/*
+ * oracle.c -- plain, slow, obviously correct CPU oracle (fp64) for the
+ * sampled-token logprob path.  TEST INFRASTRUCTURE ONLY: the product path
+ * (the CUDA library and its Python binding) never links, loads or calls this
+ * file.  Only the tests, the smoke check and the benchmark's CPU-baseline leg
+ * use it.  It shares no code, header, table or helper with the CUDA sources.
+ *
+ * What it computes, and the passage each function follows:
+ *
+ *  - oracle_logits / oracle_logprobs / oracle_log_softmax:
+ *      z[t,v] = sum_k X[t,k] * W[v,k] over ALL k in one plain fp64 loop (the
+ *      products of two bf16 numbers are exact in fp64), then
+ *      logZ = max_v z + log(sum_v exp(z - max)), logp = z[t, y_t] - logZ.
+ *      The pages name "the final logprob" as a fused-kernel output (vLLM blog
+ *      "Finish RL training faster: bit-consistent, high-throughput,
+ *      agent-driven", section 3.1) and define diff over the logprob of every
+ *      sampled token (same page, section 2); they print no formula, so this is
+ *      the standard log-softmax definition.  The leaf split of K is a rounding
+ *      schedule, not a change of the mathematical result, so the exact value
+ *      is the plain sum.
+ *
+ *  - oracle_leaf_sums: the per-leaf sums P_j = sum_{k in leaf j} X[t,k]W[v,k]
+ *      for K cut into N contiguous leaves (IsoExec blog summary, section
+ *      "Parallelism-invariant kernels"; the contract example pins
+ *      leaves = 8, leaf_dtype = fp32).
+ *
+ *  - oracle_tree_fp32: the fixed binary tree that combines N leaf partials in
+ *      fp32: adjacent pairs first, level by level, e.g. for N = 8
+ *      ((P0+P1)+(P2+P3))+((P4+P5)+(P6+P7)).  Same IsoExec section ("a fixed
+ *      binary arithmetic schedule"); the pairing of adjacent leaves is the
+ *      reading taken where the page only says "fixed binary tree".
+ *      Compiled with -ffp-contract=off; every add is one IEEE binary32 add.
+ *
+ *  - oracle_importance_weights: w = pi/mu = exp(log pi - log mu), unclipped
+ *      (REINFORCE Zero summary, sections 2 and 4), per-token term
+ *      w - 1 - log w (the k3 form r - 1 - log r, vLLM blog section 3.2) and
+ *      D3 = mean of the term over valid tokens (REINFORCE Zero summary,
+ *      section 3).  log w is taken as exactly d = log pi - log mu, so the term
+ *      is expm1(d) - d; it is 0 at w = 1.  No valid token gives D3 = 0.
+ *
+ * Every function is single-threaded per output element; rows are spread over
+ * OpenMP threads, which changes no result (each row is computed alone).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 bit pattern -> exact double (bf16 is the top half of a binary32). */
+static double bf16_to_f64(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* One logit: plain fp64 dot product of row t of X with row v of W. */
+static double logit_f64(const uint16_t* xrow, const uint16_t* wrow, int64_t H) {
+    double acc = 0.0;
+    for (int64_t k = 0; k < H; ++k) acc += bf16_to_f64(xrow[k]) * bf16_to_f64(wrow[k]);
+    return acc;
+}
+
+/* z[r, v] for the rows listed in `rows` (nrows of them); z is [nrows, V]. */
+void oracle_logits(const uint16_t* X, int64_t ldx, const uint16_t* W, int64_t H, int64_t V,
+                   const int64_t* rows, int64_t nrows, double* z) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        const uint16_t* xrow = X + rows[r] * ldx;
+        for (int64_t v = 0; v < V; ++v) z[r * V + v] = logit_f64(xrow, W + v * H, H);
+    }
+}
+
+/* log of the partition function of one row of logits: max + log sum exp(z - max). */
+static double log_partition(const double* z, int64_t V) {
+    double m = -INFINITY;
+    for (int64_t v = 0; v < V; ++v)
+        if (z[v] > m || isnan(z[v])) m = z[v];
+    if (isnan(m)) return NAN;
+    if (isinf(m) && m < 0) return -INFINITY;
+    double s = 0.0;
+    for (int64_t v = 0; v < V; ++v) s += exp(z[v] - m);
+    return m + log(s);
+}
+
+/*
+ * Sampled-token logprob for the listed rows.  ids is indexed by the row number
+ * (ids[rows[r]]); an id outside [0, V) gives NaN.  logp, logZ are [nrows].
+ */
+void oracle_logprobs(const uint16_t* X, int64_t ldx, const uint16_t* W, const int32_t* ids,
+                     int64_t H, int64_t V, const int64_t* rows, int64_t nrows, double* logp,
+                     double* logZ) {
+#pragma omp parallel
+    {
+        double* z = (double*)malloc((size_t)V * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < nrows; ++r) {
+            const uint16_t* xrow = X + rows[r] * ldx;
+            int32_t y = ids[rows[r]];
+            for (int64_t v = 0; v < V; ++v) z[v] = logit_f64(xrow, W + v * H, H);
+            double lz = log_partition(z, V);
+            logZ[r] = lz;
+            logp[r] = (y >= 0 && (int64_t)y < V) ? z[y] - lz : NAN;
+        }
+        free(z);
+    }
+}
+
+/* Full log-softmax of the listed rows: out[r, v] = z[r,v] - logZ[r]. */
+void oracle_log_softmax(const uint16_t* X, int64_t ldx, const uint16_t* W, int64_t H, int64_t V,
+                        const int64_t* rows, int64_t nrows, double* out) {
+    oracle_logits(X, ldx, W, H, V, rows, nrows, out);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        double lz = log_partition(out + r * V, V);
+        for (int64_t v = 0; v < V; ++v) out[r * V + v] -= lz;
+    }
+}
+
+/*
+ * Leaf sums for one (row t, vocab v): leaf j covers k in [j*H/N, (j+1)*H/N).
+ * out is [N].  Requires H % N == 0.
+ */
+void oracle_leaf_sums(const uint16_t* xrow, const uint16_t* wrow, int64_t H, int32_t N,
+                      double* out) {
+    int64_t L = H / N;
+    for (int32_t j = 0; j < N; ++j) {
+        double acc = 0.0;
+        for (int64_t k = (int64_t)j * L; k < (int64_t)(j + 1) * L; ++k)
+            acc += bf16_to_f64(xrow[k]) * bf16_to_f64(wrow[k]);
+        out[j] = acc;
+    }
+}
+
+/*
+ * Fixed binary tree over N fp32 partials (N a power of two, N <= 64):
+ * level by level, node i of the next level = node 2i + node 2i+1.
+ * Returns NaN bits for an unsupported N.
+ */
+float oracle_tree_fp32(const float* P, int32_t N) {
+    float buf[64];
+    if (N < 1 || N > 64 || (N & (N - 1)) != 0) return NAN;
+    for (int32_t i = 0; i < N; ++i) buf[i] = P[i];
+    for (int32_t n = N; n > 1; n /= 2) {
+        for (int32_t i = 0; i < n / 2; ++i) {
+            volatile float a = buf[2 * i], b = buf[2 * i + 1];
+            buf[i] = a + b; /* one binary32 add, round to nearest even */
+        }
+    }
+    return buf[0];
+}
+
+/* Apply oracle_tree_fp32 to `count` independent groups of N partials: P is [count, N]. */
+void oracle_tree_fp32_many(const float* P, int32_t N, int64_t count, float* out) {
+    for (int64_t i = 0; i < count; ++i) out[i] = oracle_tree_fp32(P + i * N, N);
+}
+
+/*
+ * Importance weights and D3.  mask may be NULL (all tokens valid); a token is
+ * valid when mask[t] != 0.  w and term are written for every token (term of an
+ * invalid token is still computed but not counted).  d3 = sum(term over valid)
+ * / n_valid, or 0 when n_valid == 0.
+ */
+void oracle_importance_weights(const float* logp_pi, const float* logp_mu, const uint8_t* mask,
+                               int64_t T, double* w, double* term, double* d3,
+                               int64_t* n_valid) {
+    double sum = 0.0;
+    int64_t n = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        double d = (double)logp_pi[t] - (double)logp_mu[t];
+        w[t] = exp(d);
+        term[t] = expm1(d) - d;
+        if (mask == NULL || mask[t] != 0) {
+            sum += term[t];
+            ++n;
+        }
+    }
+    *n_valid = n;
+    *d3 = n > 0 ? sum / (double)n : 0.0;
+}

@@ -1,0 +1,317 @@
+"""Pins for the fp64 CPU oracle (runs without a GPU).
+
+Each check ties the oracle to something other than itself: exact rational
+arithmetic on bf16 inputs (Fraction), a high-precision log-sum-exp written
+independently with ``decimal``, closed forms (two-token vocabulary, uniform
+logits, shift invariance, one dominant logit), invariants (probabilities sum to
+one, D3 = 0 at w = 1, term >= 0) and hand-derived golden values under
+``tests/golden/``.  The mutation tests at the end plant plausible mistakes in a
+copy of the oracle source and check that the pins catch them.
+"""
+import math
+import os
+import shutil
+import subprocess
+from decimal import Decimal, getcontext
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+
+getcontext().prec = 60
+
+
+# ----------------------------------------------------------------- helpers
+def f32_to_bf16_bits(a) -> np.ndarray:
+    """Round fp32 values to bf16 (round to nearest even) and return the uint16 bit patterns."""
+    u = np.ascontiguousarray(np.asarray(a, dtype=np.float32)).view(np.uint32).astype(np.uint64)
+    rounding = ((u >> 16) & 1) + 0x7FFF
+    return ((u + rounding) >> 16).astype(np.uint16)
+
+
+def bits_to_fraction(b) -> Fraction:
+    f = np.array([int(b) << 16], dtype=np.uint32).view(np.float32)[0]
+    return Fraction(float(f))
+
+
+def rand_bf16(shape, seed, scale=1.0):
+    rng = np.random.default_rng(seed)
+    return f32_to_bf16_bits(rng.standard_normal(shape).astype(np.float32) * scale)
+
+
+def exact_logits(X, W):
+    T, H = X.shape
+    V = W.shape[0]
+    Xf = [[bits_to_fraction(X[t, k]) for k in range(H)] for t in range(T)]
+    Wf = [[bits_to_fraction(W[v, k]) for k in range(H)] for v in range(V)]
+    return [[sum(Xf[t][k] * Wf[v][k] for k in range(H)) for v in range(V)] for t in range(T)]
+
+
+def dec(fr: Fraction) -> Decimal:
+    return Decimal(fr.numerator) / Decimal(fr.denominator)
+
+
+def decimal_logprob(zrow, y):
+    """log softmax(z)[y] from exact logits, by the unshifted definition in 60-digit decimal."""
+    total = sum((dec(z).exp() for z in zrow), Decimal(0))
+    return float(dec(zrow[y]) - total.ln()), float(total.ln())
+
+
+# ----------------------------------------------------------------- logits
+def test_logits_exact_rational():
+    X = rand_bf16((3, 16), 1)
+    W = rand_bf16((5, 16), 2, 0.3)
+    z = oracle.logits(X, W)
+    ex = exact_logits(X, W)
+    for t in range(3):
+        for v in range(5):
+            assert z[t, v] == pytest.approx(float(ex[t][v]), rel=1e-15, abs=1e-300)
+
+
+def test_logits_rows_subset_and_orientation():
+    # Non-square shapes catch a transposed operand; the row subset must index X rows.
+    X = rand_bf16((6, 12), 3)
+    W = rand_bf16((4, 12), 4)
+    full = oracle.logits(X, W)
+    sub = oracle.logits(X, W, rows=[5, 0, 3])
+    assert full.shape == (6, 4)
+    np.testing.assert_array_equal(sub, full[[5, 0, 3]])
+    ex = exact_logits(X, W)
+    assert full[5, 2] == pytest.approx(float(ex[5][2]), rel=1e-15)
+
+
+# ----------------------------------------------------------------- logprobs
+def test_logprobs_brute_force_decimal():
+    X = rand_bf16((4, 8), 5)
+    W = rand_bf16((7, 8), 6, 0.8)
+    ids = np.array([0, 6, 3, 1], dtype=np.int32)
+    logp, logZ = oracle.logprobs(X, W, ids)
+    ex = exact_logits(X, W)
+    for t in range(4):
+        lp, lz = decimal_logprob(ex[t], int(ids[t]))
+        assert logp[t] == pytest.approx(lp, abs=1e-13)
+        assert logZ[t] == pytest.approx(lz, abs=1e-13)
+
+
+def test_two_token_vocab_closed_form():
+    # V = 2: log p_y = -log1p(exp(z_other - z_y)).
+    X = rand_bf16((5, 6), 7)
+    W = rand_bf16((2, 6), 8, 2.0)
+    ex = exact_logits(X, W)
+    for y in (0, 1):
+        ids = np.full(5, y, dtype=np.int32)
+        logp, _ = oracle.logprobs(X, W, ids)
+        for t in range(5):
+            d = float(ex[t][1 - y] - ex[t][y])
+            assert logp[t] == pytest.approx(-math.log1p(math.exp(d)), abs=1e-14)
+
+
+def test_uniform_logits_give_minus_log_v():
+    V, H = 4096, 32
+    X = rand_bf16((9, H), 9)
+    row = rand_bf16((1, H), 10)
+    W = np.repeat(row, V, axis=0)
+    ids = np.random.default_rng(11).integers(0, V, 9).astype(np.int32)
+    logp, _ = oracle.logprobs(X, W, ids)
+    np.testing.assert_allclose(logp, -math.log(V), rtol=0, atol=1e-12)
+
+
+def test_shift_invariance_through_a_constant_column():
+    # Append a hidden column with x = 1 and w = c for every token: every logit moves by c,
+    # so logZ moves by c and every logprob is unchanged.
+    X = rand_bf16((4, 10), 12)
+    W = rand_bf16((9, 10), 13)
+    ids = np.array([1, 8, 0, 4], dtype=np.int32)
+    c = 3.5
+    X2 = np.concatenate([X, f32_to_bf16_bits(np.ones((4, 1)))], axis=1)
+    W2 = np.concatenate([W, f32_to_bf16_bits(np.full((9, 1), c))], axis=1)
+    lp1, lz1 = oracle.logprobs(X, W, ids)
+    lp2, lz2 = oracle.logprobs(X2, W2, ids)
+    np.testing.assert_allclose(lp2, lp1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lz2, lz1 + c, rtol=0, atol=1e-12)
+
+
+def test_dominant_logit():
+    X = f32_to_bf16_bits(np.ones((1, 1)))
+    W = f32_to_bf16_bits(np.array([[40.0], [0.0], [0.0], [0.0]]))
+    for y, want in ((0, -math.log1p(3 * math.exp(-40.0))),
+                    (2, -40.0 - math.log1p(3 * math.exp(-40.0)))):
+        logp, logZ = oracle.logprobs(X, W, np.array([y], dtype=np.int32))
+        assert logp[0] == pytest.approx(want, abs=1e-13)
+    assert logZ[0] == pytest.approx(40.0, abs=1e-13)
+
+
+def test_log_softmax_normalised_and_consistent():
+    X = rand_bf16((6, 24), 14)
+    W = rand_bf16((300, 24), 15, 0.5)
+    ls = oracle.log_softmax(X, W)
+    np.testing.assert_allclose(np.exp(ls).sum(axis=1), 1.0, rtol=0, atol=1e-12)
+    ids = np.random.default_rng(16).integers(0, 300, 6).astype(np.int32)
+    logp, _ = oracle.logprobs(X, W, ids)
+    np.testing.assert_allclose(logp, ls[np.arange(6), ids], rtol=0, atol=1e-12)
+
+
+def test_bad_id_gives_nan():
+    X = rand_bf16((3, 8), 17)
+    W = rand_bf16((5, 8), 18)
+    logp, logZ = oracle.logprobs(X, W, np.array([-1, 5, 2], dtype=np.int32))
+    assert math.isnan(logp[0]) and math.isnan(logp[1]) and not math.isnan(logp[2])
+    assert np.all(np.isfinite(logZ))
+
+
+# ----------------------------------------------------------------- leaves and tree
+@pytest.mark.parametrize("n_leaves", [1, 2, 4, 8])
+def test_leaf_sums_exact(n_leaves):
+    H = 64
+    x = rand_bf16((H,), 19)
+    w = rand_bf16((H,), 20)
+    got = oracle.leaf_sums(x, w, n_leaves)
+    L = H // n_leaves
+    xf = [bits_to_fraction(b) for b in x]
+    wf = [bits_to_fraction(b) for b in w]
+    for j in range(n_leaves):
+        exact = sum(xf[k] * wf[k] for k in range(j * L, (j + 1) * L))
+        assert got[j] == pytest.approx(float(exact), rel=1e-15, abs=1e-300)
+    total = sum(xf[k] * wf[k] for k in range(H))
+    assert math.fsum(got) == pytest.approx(float(total), rel=1e-14)
+
+
+def _golden_tree(golden_dir):
+    cases = []
+    with open(os.path.join(golden_dir, "tree_fp32.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            n, ps, want, note = [s.strip() for s in line.split("|")]
+            P = [float.fromhex(s) for s in ps.split()]
+            assert len(P) == int(n)
+            cases.append((int(n), P, float.fromhex(want), note))
+    return cases
+
+
+def test_tree_fp32_golden(golden_dir):
+    cases = _golden_tree(golden_dir)
+    assert len(cases) >= 6
+    for n, P, want, note in cases:
+        got = float(oracle.tree_fp32(np.array([P], dtype=np.float32))[0])
+        assert got == want, (n, P, note)
+
+
+def test_tree_fp32_rejects_non_power_of_two():
+    assert math.isnan(float(oracle.tree_fp32(np.ones((1, 3), np.float32))[0]))
+
+
+# ----------------------------------------------------------------- importance weights / D3
+def _golden_is(golden_dir):
+    rows, d3 = [], None
+    with open(os.path.join(golden_dir, "importance_weights.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            parts = [s.strip() for s in line.split("|")]
+            if parts[0] == "D3":
+                d3 = (float(parts[1]), int(parts[3]))
+            else:
+                rows.append(tuple(float(p) for p in parts))
+    return rows, d3
+
+
+def test_importance_weights_golden(golden_dir):
+    rows, (d3_want, nv_want) = _golden_is(golden_dir)
+    lp = np.array([r[0] for r in rows], np.float32)
+    lm = np.array([r[1] for r in rows], np.float32)
+    mask = np.array([int(r[2]) for r in rows], np.uint8)
+    w, term, d3, nv = oracle.importance_weights(lp, lm, mask)
+    for i, r in enumerate(rows):
+        assert w[i] == pytest.approx(r[3], rel=1e-15)
+        assert term[i] == pytest.approx(r[4], rel=1e-14, abs=1e-300)
+    assert nv == nv_want
+    assert d3 == pytest.approx(d3_want, rel=1e-15)
+
+
+def test_d3_zero_when_weights_are_one():
+    rng = np.random.default_rng(21)
+    lp = rng.standard_normal(1000).astype(np.float32) * 3 - 5
+    w, term, d3, nv = oracle.importance_weights(lp, lp.copy())
+    assert np.all(w == 1.0) and np.all(term == 0.0)
+    assert d3 == 0.0 and nv == 1000
+
+
+def test_d3_small_gap_series():
+    # e^d - 1 - d = d^2/2 + d^3/6 + d^4/24 + ...: the term must not lose digits near w = 1.
+    d = np.array([1e-3, -1e-3, 2.0 ** -12, -(2.0 ** -20)], np.float32)
+    w, term, _, _ = oracle.importance_weights(d, np.zeros_like(d))
+    for di, ti in zip(d.astype(np.float64), term):
+        series = di * di / 2 + di ** 3 / 6 + di ** 4 / 24 + di ** 5 / 120
+        assert ti == pytest.approx(series, rel=1e-12)
+
+
+def test_d3_mask_and_empty():
+    lp = np.array([0.5, -1.0], np.float32)
+    lm = np.zeros(2, np.float32)
+    _, _, d3, nv = oracle.importance_weights(lp, lm, np.zeros(2, np.uint8))
+    assert d3 == 0.0 and nv == 0
+    _, _, d3, nv = oracle.importance_weights(np.zeros(0, np.float32), np.zeros(0, np.float32))
+    assert d3 == 0.0 and nv == 0
+
+
+def test_term_nonnegative_and_w_positive():
+    rng = np.random.default_rng(22)
+    lp = rng.uniform(-20, 0, 5000).astype(np.float32)
+    lm = rng.uniform(-20, 0, 5000).astype(np.float32)
+    w, term, d3, nv = oracle.importance_weights(lp, lm)
+    assert np.all(w > 0) and np.all(term >= 0) and d3 > 0 and nv == 5000
+
+
+# ----------------------------------------------------------------- planted mistakes
+MUTATIONS = [
+    # (description, original text, mutated text)
+    ("sign of the logprob", "? z[y] - lz : NAN", "? lz - z[y] : NAN"),
+    ("log-sum-exp without the max term", "return m + log(s);", "return log(s);"),
+    ("transposed row index", "z[r * V + v] = logit_f64(xrow, W + v * H, H);",
+     "z[r * V + v] = logit_f64(X + v * ldx, W + rows[r] * H, H);"),
+    ("interleaved tree pairing", "buf[i] = a + b;", "buf[i] = buf[i] + buf[i + n / 2];"),
+    ("ratio inverted", "double d = (double)logp_pi[t] - (double)logp_mu[t];",
+     "double d = (double)logp_mu[t] - (double)logp_pi[t];"),
+    ("term drops the -d", "term[t] = expm1(d) - d;", "term[t] = expm1(d);"),
+    ("leaf boundary off by one", "k < (int64_t)(j + 1) * L; ++k", "k <= (int64_t)(j + 1) * L && k < H; ++k"),
+]
+
+
+def _build_mutant(tmp_path, original, mutated):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")).read()
+    assert original in src, original
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(original, mutated))
+    lib = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
+                           "-std=c11", "-o", str(lib), str(path), "-lm"])
+    return str(lib)
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+@pytest.mark.parametrize("desc,original,mutated", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_planted_mistake(tmp_path, monkeypatch, golden_dir, desc, original, mutated):
+    """Swap the oracle library for a mutated build; at least one pin above must fail."""
+    lib_path = _build_mutant(tmp_path, original, mutated)
+    monkeypatch.setattr(oracle, "_lib", None)
+    monkeypatch.setattr(oracle, "build", lambda force=False: lib_path)
+    pins = [test_logits_exact_rational, test_logits_rows_subset_and_orientation,
+            test_logprobs_brute_force_decimal, test_two_token_vocab_closed_form,
+            test_uniform_logits_give_minus_log_v, test_dominant_logit,
+            lambda: test_tree_fp32_golden(golden_dir),
+            lambda: test_importance_weights_golden(golden_dir),
+            lambda: [test_leaf_sums_exact(n) for n in (2, 4, 8)],
+            test_d3_small_gap_series]
+    failed = 0
+    for pin in pins:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            failed += 1
+    monkeypatch.setattr(oracle, "_lib", None)
+    assert failed > 0, f"no pin caught the planted mistake: {desc}"
