@@ -1,0 +1,91 @@
+"""ctypes binding of ``liblp.so`` (the C ABI in ``include/lp.h``).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind these entry points.  There is no fallback: if the library has
+not been built, loading fails with an error that says how to build it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+LP_OK, LP_ERR_INVALID_ARG, LP_ERR_UNSUPPORTED, LP_ERR_CUDA, LP_ERR_OOM, LP_ERR_TIMEOUT = range(6)
+STATUS_NAMES = {
+    LP_OK: "LP_OK", LP_ERR_INVALID_ARG: "LP_ERR_INVALID_ARG",
+    LP_ERR_UNSUPPORTED: "LP_ERR_UNSUPPORTED", LP_ERR_CUDA: "LP_ERR_CUDA",
+    LP_ERR_OOM: "LP_ERR_OOM", LP_ERR_TIMEOUT: "LP_ERR_TIMEOUT",
+}
+LP_PHASE_AUTO, LP_PHASE_PREFILL, LP_PHASE_DECODE = 0, 1, 2
+
+# Every symbol include/lp.h declares, with its ctypes signature.
+_p = ctypes.c_void_p
+_i32, _i64 = ctypes.c_int32, ctypes.c_int64
+
+
+class LpConfig(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int32), ("V", ctypes.c_int32), ("n_leaves", ctypes.c_int32),
+                ("tp_slices", ctypes.c_int32), ("max_tokens", ctypes.c_int64)]
+
+
+SIGNATURES = {
+    "lp_init": (ctypes.c_int, [ctypes.POINTER(LpConfig), _p, _p, ctypes.POINTER(_p)]),
+    "lp_logprobs": (ctypes.c_int, [_p, _p, _i64, _p, _i64, _p, _p, ctypes.c_int, _p]),
+    "lp_logprobs_host": (ctypes.c_int, [_p, _p, _i64, _p, _i64, _p, _p, _p]),
+    "lp_logits_partial": (ctypes.c_int, [_p, _p, _i64, _i64, _i32, _i32, _p, _i64, _p]),
+    "lp_logprobs_from_partials": (ctypes.c_int, [_p, _p, _i32, _i64, _i64, _p, _i64, _p, _p, _p]),
+    "lp_importance_weights": (ctypes.c_int, [_p, _p, _p, _p, _i64, _p, _p, _p, _p]),
+    "lp_check": (ctypes.c_int, [_p]),
+    "lp_clear_status": (ctypes.c_int, [_p, _p]),
+    "lp_last_error": (ctypes.c_char_p, []),
+    "lp_workspace_bytes": (ctypes.c_int64, [_p]),
+    "lp_last_launch_count": (ctypes.c_int32, [_p]),
+    "lp_version": (ctypes.c_int, []),
+    "lp_free": (None, [_p]),
+}
+
+
+class LpError(RuntimeError):
+    """A non-zero lp_status returned by the native library."""
+
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(code, code)}: {message}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = False):
+    """Load liblp.so (optionally building it first).  Raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if build_if_missing:
+            path = _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"native library {path} is missing; build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` "
+                "(there is no CPU or PyTorch fallback)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def check(rc: int) -> None:
+    if rc != LP_OK:
+        msg = load().lp_last_error()
+        raise LpError(rc, msg.decode() if msg else "")

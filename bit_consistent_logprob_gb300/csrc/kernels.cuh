@@ -1,0 +1,559 @@
+// kernels.cuh -- sm_103a kernels of the logprob path.
+//
+//  leaf_gemm_kernel<kFused>   persistent, warp-specialised tcgen05 GEMM over 128x128
+//                             (token x vocab) tiles: TMA -> smem ring -> tcgen05.mma into
+//                             TMEM, one accumulator per K leaf, the fixed leaf tree in
+//                             the epilogue, then either the per-tile log-sum-exp partial
+//                             and the sampled logit (fused path) or the tree node written
+//                             to global memory (tensor-parallel slice / leaf export).
+//  partials_lse_kernel        upper levels of the leaf tree over gathered slice partials,
+//                             then the same per-tile log-sum-exp (emulated TP path).
+//  lse_combine_kernel         fixed pairwise tree over the vocabulary tiles of each row,
+//                             logZ and the sampled-token logprob.
+//  is_block_kernel /
+//  is_final_kernel            importance weight per token and D3 over a fixed tree of
+//                             1024-token blocks (fp64 sums).
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+#include "numerics.cuh"
+#include "ptx.cuh"
+
+namespace lp {
+
+constexpr int kGemmThreads = 192;                 // 6 warps: TMA, MMA, 4 x epilogue
+constexpr int kTileBytes = kBM * kBK * 2;         // 16 KB per operand tile per stage
+constexpr int kTmemCols = 512;                    // buf0 | buf1 | S0 | S1 (128 columns each)
+constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kVT);
+
+struct GemmParams {
+    int32_t T;                // rows of this launch
+    int32_t V;
+    int32_t leaf_len;         // H / N, a multiple of kBK
+    int32_t leaf_begin;       // first leaf of the range (global leaf index)
+    int32_t leaf_count;       // leaves in the range: 1, 2, 4 or 8
+    int32_t num_row_tiles;    // ceil(T / 128)
+    int32_t num_vocab_tiles;  // ceil(V / 128)
+    int32_t band;             // vocabulary tiles per scheduling band
+    const int32_t* ids;       // [T] sampled ids (fused path)
+    float2* ws_ms;            // [num_vocab_tiles][ws_ld] (max, sum-exp) per tile (fused path)
+    int64_t ws_ld;
+    float* zy;                // [T] sampled logit (fused path)
+    float* out;               // [T][ldo] tree node (partial path)
+    int64_t ldo;
+    int* status;              // sticky device status word
+    uint64_t timeout_ns;      // bound on every mbarrier wait
+};
+
+__host__ __device__ constexpr int gemm_smem_bytes(int stages) {
+    return 1024 /* alignment slack */ + stages * 2 * kTileBytes +
+           (2 * stages + 5) * 8 /* barriers */ + 16;
+}
+
+// Tile schedule: the vocabulary is cut into bands of `band` tiles; within a band the
+// tiles run row tile by row tile, vocabulary fastest.  Concurrent CTAs therefore share
+// the band's W tiles and a few X row tiles in L2.  The schedule decides only which
+// CTA computes a tile, never how.
+__device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& rt, int& vt) {
+    const int per_band = p.num_row_tiles * p.band;
+    const int b = tile / per_band;
+    const int r = tile - b * per_band;
+    const int vt0 = b * p.band;
+    const int width = min(p.band, p.num_vocab_tiles - vt0);
+    rt = r / width;
+    vt = vt0 + (r - rt * width);
+}
+
+__device__ __forceinline__ void raise_timeout(const GemmParams& p, volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicOr(p.status, kStatusTimeout);
+}
+
+// Number of trailing one bits of x.
+__device__ __forceinline__ int trailing_ones(int x) { return __ffs(~x) - 1; }
+
+template <bool kFused, int kStages>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    leaf_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
+                     const __grid_constant__ CUtensorMap tmW, const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;                                  // X tiles   [kStages][128 x 64] bf16
+    uint8_t* sB = smem + kStages * kTileBytes;           // W tiles   [kStages][128 x 64] bf16
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kStages * kTileBytes);
+    uint64_t* full = bars;                               // TMA -> MMA, per stage
+    uint64_t* empty = bars + kStages;                    // MMA -> TMA, per stage
+    uint64_t* acc_full = bars + 2 * kStages;             // MMA -> epilogue, per TMEM buffer
+    uint64_t* acc_empty = acc_full + 2;                  // epilogue -> MMA, per TMEM buffer
+    uint64_t* drain = acc_empty + 2;                     // MMA drain on abort
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);  // one arrive per epilogue warp
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmW);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const int num_tiles = p.num_row_tiles * p.num_vocab_tiles;
+    const int nkb = p.leaf_len / kBK;
+    const int n = p.leaf_count;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            uint64_t issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                int rt, vt;
+                tile_coords(tile, p, rt, vt);
+                const int row0 = rt * kBM, v0 = vt * kVT;
+                for (int jj = 0; ok && jj < n; ++jj) {
+                    const int kbase = (p.leaf_begin + jj) * p.leaf_len;
+                    for (int kb = 0; kb < nkb; ++kb) {
+                        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns)) {
+                            raise_timeout(p, abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes);
+                        tma_load_2d(&tmX, &full[stage], sA + stage * kTileBytes, kbase + kb * kBK,
+                                    row0);
+                        tma_load_2d(&tmW, &full[stage], sB + stage * kTileBytes, kbase + kb * kBK,
+                                    v0);
+                        ++issued;
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+            if (!ok) {
+                // Let the copies already in flight land before the CTA exits.
+                const uint64_t first = issued > kStages ? issued - kStages : 0;
+                for (uint64_t i = first; i < issued; ++i) {
+                    volatile int never = 0;
+                    mbar_wait(&full[i % kStages], static_cast<uint32_t>((i / kStages) & 1u),
+                              &never, p.timeout_ns);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, g = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                for (int jj = 0; ok && jj < n; ++jj, ++g) {
+                    const uint32_t buf = g & 1u, use = g >> 1;
+                    if (!mbar_wait(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.timeout_ns)) {
+                        raise_timeout(p, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t d_tmem = tmem_base + buf * kVT;
+                    for (int kb = 0; kb < nkb; ++kb) {
+                        if (!mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns)) {
+                            raise_timeout(p, abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const uint64_t a0 = sw128_kmajor_desc(smem_u32(sA + stage * kTileBytes));
+                        const uint64_t b0 = sw128_kmajor_desc(smem_u32(sB + stage * kTileBytes));
+#pragma unroll
+                        for (int k = 0; k < kBK / 16; ++k) {
+                            // +32 bytes per K step of 16 bf16 inside the swizzled row
+                            umma_bf16(d_tmem, a0 + 2u * k, b0 + 2u * k, kIdesc,
+                                      (kb | k) != 0 ? 1u : 0u);
+                        }
+                        umma_commit(&empty[stage]);
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (ok) umma_commit(&acc_full[buf]);
+                }
+            }
+            if (!ok) {
+                // Wait for every MMA already issued before TMEM is released.
+                volatile int never = 0;
+                umma_commit(drain);
+                mbar_wait(drain, 0, &never, p.timeout_ns);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (4 warps)
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        const uint32_t colS0 = 2 * kVT, colS1 = 3 * kVT;
+        uint32_t g = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            int rt, vt;
+            tile_coords(tile, p, rt, vt);
+            const int row = rt * kBM + q * 32 + lane;
+            const int v0 = vt * kVT;
+            const bool row_ok = row < p.T;
+            int ycol = -1;
+            if (kFused && row_ok) {
+                const int y = p.ids[row];
+                if (y >= 0 && y < p.V) ycol = y - v0;
+            }
+            int sc = 0;  // entries on the partial-sum stack (S0, S1)
+            for (int jj = 0; jj < n; ++jj, ++g) {
+                const uint32_t buf = g & 1u, use = g >> 1;
+                bool got = mbar_wait(&acc_full[buf], use & 1u, abort_flag, p.timeout_ns);
+                got = __all_sync(0xffffffffu, got);
+                if (!got) {
+                    if (lane == 0) raise_timeout(p, abort_flag);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t colB = buf * kVT;
+                const bool last = (jj == n - 1);
+                if (!last && jj == n - 2) continue;  // P_{n-2} waits in its buffer for P_{n-1}
+                float v[32], u[32];
+                if (!last) {
+                    if ((jj & 1) == 0) {
+                        // push P_jj
+                        const uint32_t colS = sc == 0 ? colS0 : colS1;
+#pragma unroll 1
+                        for (int c = 0; c < kChunks; ++c) {
+                            tmem_ld32(lane_base + colB + c * 32, v);
+                            tmem_st32(lane_base + colS + c * 32, v);
+                        }
+                        ++sc;
+                    } else {
+                        // complete the subtrees that end at leaf jj
+                        const int t = trailing_ones(jj);
+                        const int dst = sc - t;
+#pragma unroll 1
+                        for (int c = 0; c < kChunks; ++c) {
+                            tmem_ld32(lane_base + colB + c * 32, v);
+                            for (int l = 0; l < t; ++l) {
+                                const uint32_t colS = (sc - 1 - l) == 0 ? colS0 : colS1;
+                                tmem_ld32(lane_base + colS + c * 32, u);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) v[i] = __fadd_rn(u[i], v[i]);
+                            }
+                            tmem_st32(lane_base + (dst == 0 ? colS0 : colS1) + c * 32, v);
+                        }
+                        sc = dst + 1;
+                    }
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                    continue;
+                }
+                // last leaf of the range: finish the tree node
+                const uint32_t colPrev = (buf ^ 1u) * kVT;
+#pragma unroll 1
+                for (int c = 0; c < kChunks; ++c) {
+                    tmem_ld32(lane_base + colB + c * 32, v);
+                    if (n > 1) {
+                        tmem_ld32(lane_base + colPrev + c * 32, u);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __fadd_rn(u[i], v[i]);
+                        for (int l = 0; l < sc; ++l) {
+                            const uint32_t colS = (sc - 1 - l) == 0 ? colS0 : colS1;
+                            tmem_ld32(lane_base + colS + c * 32, u);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = __fadd_rn(u[i], v[i]);
+                        }
+                    }
+                    if (kFused) {
+                        tmem_st32(lane_base + colS0 + c * 32, v);  // z of this tile -> S0
+                    } else if (row_ok) {
+                        const int col0 = v0 + c * 32;
+                        float* dst = p.out + static_cast<int64_t>(row) * p.ldo + col0;
+                        if (col0 + 32 <= p.V) {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4)
+                                *reinterpret_cast<float4*>(dst + i) =
+                                    make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (col0 + i < p.V) dst[i] = v[i];
+                        }
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&acc_empty[buf]);
+                    if (n > 1) mbar_arrive(&acc_empty[buf ^ 1u]);
+                }
+                if (kFused) {
+                    float m, s, zy = 0.0f;
+                    const int nvalid = min(kVT, p.V - v0);
+                    tile_lse(
+                        [&](int c, float(&z)[32]) { tmem_ld32(lane_base + colS0 + c * 32, z); },
+                        nvalid, ycol, m, s, zy);
+                    if (row_ok) {
+                        p.ws_ms[static_cast<int64_t>(vt) * p.ws_ld + row] = make_float2(m, s);
+                        if (ycol >= 0 && ycol < kVT) p.zy[row] = zy;
+                    }
+                }
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// Upper levels of the leaf tree over gathered partials (one per slice), then the
+// per-tile log-sum-exp and sampled logit, exactly as the fused epilogue does.
+// grid: (num_vocab_tiles, ceil(T/128)); block: 128 threads, one row each.
+struct PartialsParams {
+    const float* parts;      // [n_parts] x [T][ldp]
+    int64_t part_stride;
+    int64_t ldp;
+    int32_t n_parts;         // 1, 2, 4, 8
+    int32_t T;
+    int32_t V;
+    const int32_t* ids;
+    float2* ws_ms;
+    int64_t ws_ld;
+    float* zy;
+};
+
+template <int kParts>
+__global__ void __launch_bounds__(128) partials_lse_kernel(const PartialsParams p) {
+    const int vt = blockIdx.x;
+    const int row = blockIdx.y * 128 + threadIdx.x;
+    if (row >= p.T) return;
+    const int v0 = vt * kVT;
+    const int nvalid = min(kVT, p.V - v0);
+    int ycol = -1;
+    const int y = p.ids[row];
+    if (y >= 0 && y < p.V) ycol = y - v0;
+    const float* base = p.parts + static_cast<int64_t>(row) * p.ldp + v0;
+    auto load = [&](int c, float(&z)[32]) {
+#pragma unroll 4
+        for (int i = 0; i < 32; ++i) {
+            const int col = c * 32 + i;
+            float node[kParts];
+#pragma unroll
+            for (int k = 0; k < kParts; ++k)
+                node[k] = col < nvalid ? base[k * p.part_stride + col] : 0.0f;
+#pragma unroll
+            for (int w = kParts >> 1; w >= 1; w >>= 1)
+#pragma unroll
+                for (int k = 0; k < w; ++k) node[k] = __fadd_rn(node[2 * k], node[2 * k + 1]);
+            z[i] = node[0];
+        }
+    };
+    float m, s, zy = 0.0f;
+    tile_lse(load, nvalid, ycol, m, s, zy);
+    p.ws_ms[static_cast<int64_t>(vt) * p.ws_ld + row] = make_float2(m, s);
+    if (ycol >= 0 && ycol < kVT) p.zy[row] = zy;
+}
+
+// Fixed pairwise tree over the vocabulary tiles of each row (adjacent pairs first,
+// level by level; an odd last entry moves up a level unchanged), logZ and logp.
+// block: 4 warps, one row per warp; dynamic smem: 4 x num_vocab_tiles float2.
+struct CombineParams {
+    const float2* ws_ms;
+    int64_t ws_ld;
+    const float* zy;
+    const int32_t* ids;
+    int32_t T;
+    int32_t V;
+    int32_t num_vocab_tiles;
+    float* out_logp;
+    float* out_logZ;          // may be null
+    int* status;
+};
+
+__global__ void __launch_bounds__(128) lse_combine_kernel(const CombineParams p) {
+    extern __shared__ float2 cmb_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * 4 + warp;
+    if (row >= p.T) return;
+    float2* a = cmb_smem + warp * p.num_vocab_tiles;
+    for (int b = lane; b < p.num_vocab_tiles; b += 32) a[b] = p.ws_ms[b * p.ws_ld + row];
+    __syncwarp();
+    int cnt = p.num_vocab_tiles;
+    while (cnt > 1) {
+        const int half = cnt >> 1;
+        for (int base = 0; base < half; base += 32) {
+            const int i = base + lane;
+            float2 r = make_float2(0.0f, 0.0f);
+            if (i < half) r = lse_merge(a[2 * i], a[2 * i + 1]);
+            __syncwarp();
+            if (i < half) a[i] = r;
+            __syncwarp();
+        }
+        if (cnt & 1) {
+            if (lane == 0) a[half] = a[cnt - 1];
+            __syncwarp();
+        }
+        cnt = half + (cnt & 1);
+    }
+    if (lane == 0) {
+        const float lz = lse_finish(a[0]);
+        const int y = p.ids[row];
+        float lp;
+        if (y >= 0 && y < p.V) {
+            lp = __fsub_rn(p.zy[row], lz);
+        } else {
+            lp = __int_as_float(0x7fc00000);
+            atomicOr(p.status, kStatusBadId);
+        }
+        p.out_logp[row] = lp;
+        if (p.out_logZ) p.out_logZ[row] = lz;
+    }
+}
+
+// ---------------------------------------------------------------------- IS / D3
+constexpr int kIsBlock = 1024;       // tokens per D3 block (fixed; the tree is over blocks)
+constexpr int kIsThreads = 256;      // 4 tokens per thread
+constexpr int kIsChunk = 2048;       // block partials per level-wise pass of the final kernel
+
+struct IsParams {
+    const float* logp_pi;
+    const float* logp_mu;
+    const uint8_t* mask;     // may be null
+    int64_t T;
+    float* out_w;
+    double* blk_sum;         // [num_blocks]
+    long long* blk_cnt;      // [num_blocks]
+};
+
+// Per token: d = log pi - log mu, w = e^d, term = e^d - 1 - d.  Per block of 1024
+// tokens: fp64 sum of the valid terms, each thread adding its 4 tokens in order, then
+// a fixed xor-butterfly over the 32 lanes and a pairwise tree over the 8 warps.
+__global__ void __launch_bounds__(kIsThreads) is_block_kernel(const IsParams p) {
+    __shared__ double wsum[kIsThreads / 32];
+    __shared__ long long wcnt[kIsThreads / 32];
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kIsBlock + threadIdx.x * 4;
+    double acc = 0.0;
+    long long cnt = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t t = t0 + i;
+        if (t < p.T) {
+            const float d = __fsub_rn(p.logp_pi[t], p.logp_mu[t]);
+            p.out_w[t] = expf(d);
+            const bool valid = p.mask == nullptr || p.mask[t] != 0;
+            if (valid) {
+                acc = __dadd_rn(acc, static_cast<double>(d3_term(d)));
+                ++cnt;
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        acc = __dadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+    }
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        wsum[warp] = acc;
+        wcnt[warp] = cnt;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const double s01 = __dadd_rn(wsum[0], wsum[1]), s23 = __dadd_rn(wsum[2], wsum[3]);
+        const double s45 = __dadd_rn(wsum[4], wsum[5]), s67 = __dadd_rn(wsum[6], wsum[7]);
+        p.blk_sum[blockIdx.x] = __dadd_rn(__dadd_rn(s01, s23), __dadd_rn(s45, s67));
+        long long c = 0;
+        for (int w = 0; w < kIsThreads / 32; ++w) c += wcnt[w];
+        p.blk_cnt[blockIdx.x] = c;
+    }
+}
+
+// Level-wise pairwise fp64 tree over n values in shared memory (in place), using the
+// whole block.  Result in a[0].
+__device__ __forceinline__ void block_tree_f64(double* a, int n) {
+    while (n > 1) {
+        const int half = n >> 1;
+        for (int base = 0; base < half; base += blockDim.x) {
+            const int i = base + threadIdx.x;
+            double r = 0.0;
+            if (i < half) r = __dadd_rn(a[2 * i], a[2 * i + 1]);
+            __syncthreads();
+            if (i < half) a[i] = r;
+            __syncthreads();
+        }
+        if (n & 1) {
+            if (threadIdx.x == 0) a[half] = a[n - 1];
+            __syncthreads();
+        }
+        n = half + (n & 1);
+    }
+}
+
+// One block: the tree over all block partials, taken in aligned chunks of kIsChunk
+// (each chunk is a whole subtree of the level-wise tree, so the result is the same
+// as one tree over every block), then D3 = sum / n_valid.
+__global__ void __launch_bounds__(1024) is_final_kernel(const double* blk_sum,
+                                                        const long long* blk_cnt, int num_blocks,
+                                                        double* out_d3, int64_t* out_nvalid) {
+    __shared__ double a[kIsChunk];
+    __shared__ double chunk_res[kIsChunk];
+    __shared__ long long cnt_part[1024];
+    long long cnt = 0;
+    for (int i = threadIdx.x; i < num_blocks; i += blockDim.x) cnt += blk_cnt[i];
+    cnt_part[threadIdx.x] = cnt;
+    const int num_chunks = (num_blocks + kIsChunk - 1) / kIsChunk;
+    for (int ch = 0; ch < num_chunks; ++ch) {
+        const int lo = ch * kIsChunk;
+        const int len = min(kIsChunk, num_blocks - lo);
+        for (int i = threadIdx.x; i < len; i += blockDim.x) a[i] = blk_sum[lo + i];
+        __syncthreads();
+        block_tree_f64(a, len);
+        if (threadIdx.x == 0) chunk_res[ch] = a[0];
+        __syncthreads();
+    }
+    if (num_chunks > 0) block_tree_f64(chunk_res, num_chunks);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        long long total = 0;
+        for (int i = 0; i < 1024; ++i) total += cnt_part[i];
+        const double sum = num_chunks > 0 ? chunk_res[0] : 0.0;
+        *out_d3 = total > 0 ? __ddiv_rn(sum, static_cast<double>(total)) : 0.0;
+        if (out_nvalid) *out_nvalid = total;
+    }
+}
+
+}  // namespace lp

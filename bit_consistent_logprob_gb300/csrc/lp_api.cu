@@ -1,0 +1,540 @@
+// lp_api.cu -- host side of the C ABI declared in include/lp.h: argument checks, the
+// fixed launch plan, workspace ownership, TMA descriptors and kernel launches.
+//
+// The plan depends only on (H, V, N, tp_slices, max_tokens) and on how many rows a
+// call carries; the per-element arithmetic never depends on T, the SM count or the
+// phase, so every row is bit-identical however it is batched.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+
+#include "kernels.cuh"
+#include "lp.h"
+
+namespace {
+
+constexpr int kStagesGemm = 6;
+constexpr int kBand = 16;                       // vocabulary tiles per scheduling band
+constexpr int64_t kMaxIsTokens = (1LL << 31) - 1;
+constexpr int64_t kTpRows = 1024;               // rows per pass of the emulated TP path
+
+thread_local std::string g_last_error = "no error";
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    cudaGetLastError();  // clear the non-sticky error
+    return fail(e == cudaErrorMemoryAllocation ? LP_ERR_OOM : LP_ERR_CUDA, "%s: %s (%s)", what,
+                cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define LP_CUDA(call, what)                          \
+    do {                                             \
+        cudaError_t e_ = (call);                     \
+        if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+    } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// K-major bf16 matrix [rows, K] with a row stride of `ld` elements, read in 128 x 64
+// boxes with 128-byte swizzling (the layout the tcgen05 descriptors expect).  Rows past
+// `rows` read as zero.
+int encode_kmajor(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K, uint64_t ld) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return fail(LP_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t dims[2] = {K, rows};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(lp::kBK), static_cast<cuuint32_t>(lp::kBM)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(LP_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return LP_OK;
+}
+
+}  // namespace
+
+struct lp_handle {
+    lp_config cfg{};
+    const void* W = nullptr;
+    int device = 0;
+    int num_sms = 0;
+    int num_vocab_tiles = 0;
+    int leaf_len = 0;
+    uint64_t timeout_ns = 0;
+    CUtensorMap tmW{};
+    // workspace (device)
+    float2* ws_ms = nullptr;      // [num_vocab_tiles][max_tokens]
+    float* zy = nullptr;          // [max_tokens]
+    int* status = nullptr;        // sticky status word
+    double* blk_sum = nullptr;    // [max_is_blocks]
+    long long* blk_cnt = nullptr; // [max_is_blocks]
+    int64_t max_is_blocks = 0;
+    float* tp_parts = nullptr;    // [tp_slices][max_tokens][ldp] slice outputs
+    float* tp_gather = nullptr;   // same shape: the "transported" copy
+    int64_t tp_ldp = 0;
+    int64_t chunk_rows = 0;       // rows per pass: max_tokens, or the TP sub-chunk
+    // staging for lp_logprobs_host (device)
+    void* x_stage = nullptr;
+    int32_t* ids_stage = nullptr;
+    float* logp_stage = nullptr;
+    float* logz_stage = nullptr;
+    cudaStream_t last_stream = nullptr;
+    int64_t ws_bytes = 0;
+    int32_t last_launches = 0;
+};
+
+namespace {
+
+int validate_config(const lp_config* c) {
+    if (c == nullptr) return fail(LP_ERR_INVALID_ARG, "config is NULL");
+    if (c->H <= 0 || c->V <= 0) return fail(LP_ERR_INVALID_ARG, "H and V must be positive");
+    if (c->max_tokens <= 0 || c->max_tokens > (1LL << 31) - 1)
+        return fail(LP_ERR_INVALID_ARG, "max_tokens must be in [1, 2^31)");
+    if (!(c->n_leaves == 1 || c->n_leaves == 2 || c->n_leaves == 4 || c->n_leaves == 8))
+        return fail(LP_ERR_UNSUPPORTED, "n_leaves must be 1, 2, 4 or 8 (got %d)", c->n_leaves);
+    if (c->H % (lp::kBK * c->n_leaves) != 0)
+        return fail(LP_ERR_UNSUPPORTED, "H (%d) must be a multiple of 64 * n_leaves (%d)", c->H,
+                    lp::kBK * c->n_leaves);
+    if (!(c->tp_slices == 1 || c->tp_slices == 2 || c->tp_slices == 4 || c->tp_slices == 8) ||
+        c->n_leaves % c->tp_slices != 0)
+        return fail(LP_ERR_UNSUPPORTED, "tp_slices must be 1, 2, 4 or 8 and divide n_leaves");
+    return LP_OK;
+}
+
+template <bool kFused>
+int launch_leaf_gemm(lp_handle* h, const CUtensorMap& tmX, int rows, int leaf_begin,
+                     int leaf_count, const int32_t* ids, float* out, int64_t ldo,
+                     cudaStream_t st) {
+    lp::GemmParams p{};
+    p.T = rows;
+    p.V = h->cfg.V;
+    p.leaf_len = h->leaf_len;
+    p.leaf_begin = leaf_begin;
+    p.leaf_count = leaf_count;
+    p.num_row_tiles = static_cast<int32_t>(ceil_div(rows, lp::kBM));
+    p.num_vocab_tiles = h->num_vocab_tiles;
+    p.band = kBand;
+    p.ids = ids;
+    p.ws_ms = h->ws_ms;
+    p.ws_ld = h->cfg.max_tokens;
+    p.zy = h->zy;
+    p.out = out;
+    p.ldo = ldo;
+    p.status = h->status;
+    p.timeout_ns = h->timeout_ns;
+    const int64_t tiles = static_cast<int64_t>(p.num_row_tiles) * p.num_vocab_tiles;
+    if (tiles > 0x7fffffff) return fail(LP_ERR_UNSUPPORTED, "too many tiles in one launch");
+    const int grid = static_cast<int>(tiles < h->num_sms ? tiles : h->num_sms);
+    lp::leaf_gemm_kernel<kFused, kStagesGemm>
+        <<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(kStagesGemm), st>>>(tmX, h->tmW, p);
+    LP_CUDA(cudaGetLastError(), "leaf_gemm_kernel launch");
+    ++h->last_launches;
+    return LP_OK;
+}
+
+int launch_combine(lp_handle* h, const int32_t* ids, int rows, float* out_logp, float* out_logZ,
+                   cudaStream_t st) {
+    lp::CombineParams c{};
+    c.ws_ms = h->ws_ms;
+    c.ws_ld = h->cfg.max_tokens;
+    c.zy = h->zy;
+    c.ids = ids;
+    c.T = rows;
+    c.V = h->cfg.V;
+    c.num_vocab_tiles = h->num_vocab_tiles;
+    c.out_logp = out_logp;
+    c.out_logZ = out_logZ;
+    c.status = h->status;
+    const size_t smem = 4 * sizeof(float2) * static_cast<size_t>(h->num_vocab_tiles);
+    lp::lse_combine_kernel<<<static_cast<unsigned>(ceil_div(rows, 4)), 128, smem, st>>>(c);
+    LP_CUDA(cudaGetLastError(), "lse_combine_kernel launch");
+    ++h->last_launches;
+    return LP_OK;
+}
+
+int launch_partials_lse(lp_handle* h, const float* parts, int n_parts, int64_t part_stride,
+                        int64_t ldp, const int32_t* ids, int rows, cudaStream_t st) {
+    lp::PartialsParams q{};
+    q.parts = parts;
+    q.part_stride = part_stride;
+    q.ldp = ldp;
+    q.n_parts = n_parts;
+    q.T = rows;
+    q.V = h->cfg.V;
+    q.ids = ids;
+    q.ws_ms = h->ws_ms;
+    q.ws_ld = h->cfg.max_tokens;
+    q.zy = h->zy;
+    dim3 grid(static_cast<unsigned>(h->num_vocab_tiles), static_cast<unsigned>(ceil_div(rows, 128)));
+    switch (n_parts) {
+        case 1: lp::partials_lse_kernel<1><<<grid, 128, 0, st>>>(q); break;
+        case 2: lp::partials_lse_kernel<2><<<grid, 128, 0, st>>>(q); break;
+        case 4: lp::partials_lse_kernel<4><<<grid, 128, 0, st>>>(q); break;
+        default: lp::partials_lse_kernel<8><<<grid, 128, 0, st>>>(q); break;
+    }
+    LP_CUDA(cudaGetLastError(), "partials_lse_kernel launch");
+    ++h->last_launches;
+    return LP_OK;
+}
+
+// Fused path or emulated tensor-parallel path for one chunk of rows (rows <= max_tokens).
+int logprobs_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int rows,
+                   float* out_logp, float* out_logZ, cudaStream_t st) {
+    CUtensorMap tmX;
+    int rc = encode_kmajor(&tmX, X, static_cast<uint64_t>(rows), h->cfg.H, ldx);
+    if (rc != LP_OK) return rc;
+    const int s = h->cfg.tp_slices;
+    if (s == 1) {
+        rc = launch_leaf_gemm<true>(h, tmX, rows, 0, h->cfg.n_leaves, ids, nullptr, 0, st);
+        if (rc != LP_OK) return rc;
+    } else {
+        // Slice r owns leaves [r*N/s, (r+1)*N/s) and produces that node of the leaf tree;
+        // the partials are then moved (a plain copy: data only, no arithmetic) into the
+        // gathered buffer, where the upper levels of the same tree are applied.
+        const int per = h->cfg.n_leaves / s;
+        const int64_t part_stride = h->chunk_rows * h->tp_ldp;
+        for (int r = 0; r < s; ++r) {
+            rc = launch_leaf_gemm<false>(h, tmX, rows, r * per, per, nullptr,
+                                         h->tp_parts + r * part_stride, h->tp_ldp, st);
+            if (rc != LP_OK) return rc;
+        }
+        for (int r = 0; r < s; ++r) {
+            LP_CUDA(cudaMemcpyAsync(h->tp_gather + r * part_stride, h->tp_parts + r * part_stride,
+                                    sizeof(float) * static_cast<size_t>(rows) * h->tp_ldp,
+                                    cudaMemcpyDeviceToDevice, st),
+                    "slice transport copy");
+        }
+        rc = launch_partials_lse(h, h->tp_gather, s, part_stride, h->tp_ldp, ids, rows, st);
+        if (rc != LP_OK) return rc;
+    }
+    return launch_combine(h, ids, rows, out_logp, out_logZ, st);
+}
+
+int check_x(const lp_handle* h, const void* X, int64_t ldx, int64_t T) {
+    if (T < 0) return fail(LP_ERR_INVALID_ARG, "T must be >= 0");
+    if (T == 0) return LP_OK;
+    if (X == nullptr) return fail(LP_ERR_INVALID_ARG, "X is NULL");
+    if (!aligned16(X)) return fail(LP_ERR_INVALID_ARG, "X must be 16-byte aligned");
+    if (ldx < h->cfg.H || ldx % 8 != 0)
+        return fail(LP_ERR_INVALID_ARG, "ldx must be >= H and a multiple of 8 (got %lld)",
+                    (long long)ldx);
+    return LP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lp_version(void) { return 100; }
+
+const char* lp_last_error(void) { return g_last_error.c_str(); }
+
+int64_t lp_workspace_bytes(const lp_handle* h) { return h ? h->ws_bytes : 0; }
+
+int32_t lp_last_launch_count(const lp_handle* h) { return h ? h->last_launches : 0; }
+
+void lp_free(lp_handle* h) {
+    if (h == nullptr) return;
+    cudaDeviceSynchronize();
+    cudaFree(h->ws_ms);
+    cudaFree(h->zy);
+    cudaFree(h->status);
+    cudaFree(h->blk_sum);
+    cudaFree(h->blk_cnt);
+    cudaFree(h->tp_parts);
+    cudaFree(h->tp_gather);
+    cudaFree(h->x_stage);
+    cudaFree(h->ids_stage);
+    cudaFree(h->logp_stage);
+    cudaFree(h->logz_stage);
+    delete h;
+}
+
+int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out) {
+    if (out == nullptr) return fail(LP_ERR_INVALID_ARG, "out handle pointer is NULL");
+    *out = nullptr;
+    int rc = validate_config(cfg);
+    if (rc != LP_OK) return rc;
+    if (W == nullptr) return fail(LP_ERR_INVALID_ARG, "W is NULL");
+    if (!aligned16(W)) return fail(LP_ERR_INVALID_ARG, "W must be 16-byte aligned");
+
+    int dev = 0;
+    LP_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+    cudaDeviceProp prop;
+    LP_CUDA(cudaGetDeviceProperties(&prop, dev), "cudaGetDeviceProperties");
+    if (!(prop.major == 10 && prop.minor == 3))
+        return fail(LP_ERR_UNSUPPORTED, "this library is built for sm_103a (GB300); device is sm_%d%d",
+                    prop.major, prop.minor);
+
+    lp_handle* h = new lp_handle();
+    h->cfg = *cfg;
+    h->W = W;
+    h->device = dev;
+    h->num_sms = prop.multiProcessorCount;
+    h->num_vocab_tiles = static_cast<int>(ceil_div(cfg->V, lp::kVT));
+    h->leaf_len = cfg->H / cfg->n_leaves;
+    uint64_t timeout_ms = 2000;
+    if (const char* e = std::getenv("LP_WAIT_TIMEOUT_MS")) {
+        long long v = std::atoll(e);
+        if (v > 0) timeout_ms = static_cast<uint64_t>(v);
+    }
+    h->timeout_ns = timeout_ms * 1000000ull;
+
+    auto cleanup = [&](int code) {
+        lp_free(h);
+        return code;
+    };
+    rc = encode_kmajor(&h->tmW, W, static_cast<uint64_t>(cfg->V), cfg->H, cfg->H);
+    if (rc != LP_OK) return cleanup(rc);
+
+    const int64_t mt = cfg->max_tokens;
+    auto alloc = [&](void** p, size_t bytes, const char* what) -> int {
+        cudaError_t e = cudaMalloc(p, bytes);
+        if (e != cudaSuccess) return cuda_fail(e, what);
+        h->ws_bytes += static_cast<int64_t>(bytes);
+        return LP_OK;
+    };
+    h->max_is_blocks = ceil_div(kMaxIsTokens, lp::kIsBlock);
+    if ((rc = alloc(reinterpret_cast<void**>(&h->ws_ms),
+                    sizeof(float2) * static_cast<size_t>(h->num_vocab_tiles) * mt, "ws_ms")) ||
+        (rc = alloc(reinterpret_cast<void**>(&h->zy), sizeof(float) * mt, "zy")) ||
+        (rc = alloc(reinterpret_cast<void**>(&h->status), sizeof(int), "status")) ||
+        (rc = alloc(reinterpret_cast<void**>(&h->blk_sum), sizeof(double) * h->max_is_blocks,
+                    "blk_sum")) ||
+        (rc = alloc(reinterpret_cast<void**>(&h->blk_cnt), sizeof(long long) * h->max_is_blocks,
+                    "blk_cnt")) ||
+        (rc = alloc(&h->x_stage, sizeof(uint16_t) * static_cast<size_t>(mt) * cfg->H, "x_stage")) ||
+        (rc = alloc(reinterpret_cast<void**>(&h->ids_stage), sizeof(int32_t) * mt, "ids_stage")) ||
+        (rc = alloc(reinterpret_cast<void**>(&h->logp_stage), sizeof(float) * mt, "logp_stage")) ||
+        (rc = alloc(reinterpret_cast<void**>(&h->logz_stage), sizeof(float) * mt, "logz_stage")))
+        return cleanup(rc);
+    h->chunk_rows = mt;
+    if (cfg->tp_slices > 1) {
+        h->chunk_rows = mt < kTpRows ? mt : kTpRows;
+        h->tp_ldp = ceil_div(cfg->V, 4) * 4;
+        const size_t bytes =
+            sizeof(float) * static_cast<size_t>(cfg->tp_slices) * h->chunk_rows * h->tp_ldp;
+        if ((rc = alloc(reinterpret_cast<void**>(&h->tp_parts), bytes, "tp_parts")) ||
+            (rc = alloc(reinterpret_cast<void**>(&h->tp_gather), bytes, "tp_gather")))
+            return cleanup(rc);
+    }
+
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<true, kStagesGemm>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  lp::gemm_smem_bytes(kStagesGemm))) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<false, kStagesGemm>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  lp::gemm_smem_bytes(kStagesGemm))) != cudaSuccess)
+        return cleanup(cuda_fail(e, "cudaFuncSetAttribute(leaf_gemm_kernel)"));
+    const int combine_smem = static_cast<int>(4 * sizeof(float2) * h->num_vocab_tiles);
+    if (combine_smem > 48 * 1024) {
+        if (combine_smem > 227 * 1024) return cleanup(fail(LP_ERR_UNSUPPORTED, "V too large"));
+        if ((e = cudaFuncSetAttribute(lp::lse_combine_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      combine_smem)) != cudaSuccess)
+            return cleanup(cuda_fail(e, "cudaFuncSetAttribute(lse_combine_kernel)"));
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((e = cudaMemsetAsync(h->status, 0, sizeof(int), st)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(st)) != cudaSuccess)
+        return cleanup(cuda_fail(e, "status init"));
+    h->last_stream = st;
+    *out = h;
+    return LP_OK;
+}
+
+int lp_logprobs(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int64_t T,
+                float* out_logp, float* out_logZ, int phase, void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    int rc = check_x(h, X, ldx, T);
+    if (rc != LP_OK) return rc;
+    if (phase < LP_PHASE_AUTO || phase > LP_PHASE_DECODE)
+        return fail(LP_ERR_INVALID_ARG, "unknown phase %d", phase);
+    h->last_launches = 0;
+    if (T == 0) return LP_OK;
+    if (ids == nullptr || out_logp == nullptr)
+        return fail(LP_ERR_INVALID_ARG, "ids and out_logp must not be NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    h->last_stream = st;
+    const int64_t chunk = h->chunk_rows;
+    const uint8_t* xb = static_cast<const uint8_t*>(X);
+    for (int64_t r0 = 0; r0 < T; r0 += chunk) {
+        const int rows = static_cast<int>(T - r0 < chunk ? T - r0 : chunk);
+        rc = logprobs_chunk(h, xb + r0 * ldx * 2, ldx, ids + r0, rows, out_logp + r0,
+                            out_logZ ? out_logZ + r0 : nullptr, st);
+        if (rc != LP_OK) return rc;
+    }
+    return LP_OK;
+}
+
+int lp_logprobs_host(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int64_t T,
+                     float* out_logp, float* out_logZ, void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    if (T < 0) return fail(LP_ERR_INVALID_ARG, "T must be >= 0");
+    h->last_launches = 0;
+    if (T == 0) return LP_OK;
+    if (X == nullptr || ids == nullptr || out_logp == nullptr)
+        return fail(LP_ERR_INVALID_ARG, "X, ids and out_logp must not be NULL");
+    if (ldx < h->cfg.H) return fail(LP_ERR_INVALID_ARG, "ldx must be >= H");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    h->last_stream = st;
+    const int64_t chunk = h->chunk_rows;
+    const int H = h->cfg.H;
+    const uint8_t* xb = static_cast<const uint8_t*>(X);
+    int32_t launches = 0;
+    for (int64_t r0 = 0; r0 < T; r0 += chunk) {
+        const int rows = static_cast<int>(T - r0 < chunk ? T - r0 : chunk);
+        LP_CUDA(cudaMemcpy2DAsync(h->x_stage, static_cast<size_t>(H) * 2, xb + r0 * ldx * 2,
+                                  static_cast<size_t>(ldx) * 2, static_cast<size_t>(H) * 2, rows,
+                                  cudaMemcpyHostToDevice, st),
+                "X host-to-device copy");
+        LP_CUDA(cudaMemcpyAsync(h->ids_stage, ids + r0, sizeof(int32_t) * rows,
+                                cudaMemcpyHostToDevice, st),
+                "ids host-to-device copy");
+        int rc = logprobs_chunk(h, h->x_stage, H, h->ids_stage, rows, h->logp_stage,
+                                h->logz_stage, st);
+        if (rc != LP_OK) return rc;
+        launches += h->last_launches;
+        h->last_launches = 0;
+        LP_CUDA(cudaMemcpyAsync(out_logp + r0, h->logp_stage, sizeof(float) * rows,
+                                cudaMemcpyDeviceToHost, st),
+                "logp device-to-host copy");
+        if (out_logZ)
+            LP_CUDA(cudaMemcpyAsync(out_logZ + r0, h->logz_stage, sizeof(float) * rows,
+                                    cudaMemcpyDeviceToHost, st),
+                    "logZ device-to-host copy");
+    }
+    h->last_launches = launches;
+    LP_CUDA(cudaStreamSynchronize(st), "stream synchronize");
+    return LP_OK;
+}
+
+int lp_logits_partial(lp_handle* h, const void* X, int64_t ldx, int64_t T, int32_t leaf_begin,
+                      int32_t leaf_count, float* out, int64_t ldo, void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    int rc = check_x(h, X, ldx, T);
+    if (rc != LP_OK) return rc;
+    if (!is_pow2(leaf_count) || leaf_begin < 0 || leaf_begin % leaf_count != 0 ||
+        leaf_begin + leaf_count > h->cfg.n_leaves)
+        return fail(LP_ERR_UNSUPPORTED,
+                    "leaf range [%d, %d) is not an aligned node of the %d-leaf tree", leaf_begin,
+                    leaf_begin + leaf_count, h->cfg.n_leaves);
+    h->last_launches = 0;
+    if (T == 0) return LP_OK;
+    if (out == nullptr || !aligned16(out) || ldo < h->cfg.V || ldo % 4 != 0)
+        return fail(LP_ERR_INVALID_ARG, "out must be 16-byte aligned with ldo >= V, ldo %% 4 == 0");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    h->last_stream = st;
+    const int64_t chunk = h->cfg.max_tokens;
+    const uint8_t* xb = static_cast<const uint8_t*>(X);
+    for (int64_t r0 = 0; r0 < T; r0 += chunk) {
+        const int rows = static_cast<int>(T - r0 < chunk ? T - r0 : chunk);
+        CUtensorMap tmX;
+        rc = encode_kmajor(&tmX, xb + r0 * ldx * 2, static_cast<uint64_t>(rows), h->cfg.H, ldx);
+        if (rc != LP_OK) return rc;
+        rc = launch_leaf_gemm<false>(h, tmX, rows, leaf_begin, leaf_count, nullptr,
+                                     out + r0 * ldo, ldo, st);
+        if (rc != LP_OK) return rc;
+    }
+    return LP_OK;
+}
+
+int lp_logprobs_from_partials(lp_handle* h, const float* partials, int32_t n_parts,
+                              int64_t part_stride, int64_t ldp, const int32_t* ids, int64_t T,
+                              float* out_logp, float* out_logZ, void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    if (!(n_parts == 1 || n_parts == 2 || n_parts == 4 || n_parts == 8) ||
+        h->cfg.n_leaves % n_parts != 0)
+        return fail(LP_ERR_UNSUPPORTED, "n_parts must be 1, 2, 4 or 8 and divide n_leaves");
+    if (T < 0 || T > h->cfg.max_tokens)
+        return fail(LP_ERR_INVALID_ARG, "T must be in [0, max_tokens]");
+    h->last_launches = 0;
+    if (T == 0) return LP_OK;
+    if (partials == nullptr || ids == nullptr || out_logp == nullptr)
+        return fail(LP_ERR_INVALID_ARG, "partials, ids and out_logp must not be NULL");
+    if (ldp < h->cfg.V || part_stride < ldp * T)
+        return fail(LP_ERR_INVALID_ARG, "need ldp >= V and part_stride >= ldp * T");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    h->last_stream = st;
+    int rc = launch_partials_lse(h, partials, n_parts, part_stride, ldp, ids, static_cast<int>(T), st);
+    if (rc != LP_OK) return rc;
+    return launch_combine(h, ids, static_cast<int>(T), out_logp, out_logZ, st);
+}
+
+int lp_importance_weights(lp_handle* h, const float* logp_pi, const float* logp_mu,
+                          const uint8_t* mask, int64_t T, float* out_w, double* out_d3,
+                          int64_t* out_nvalid, void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    if (T < 0 || T > kMaxIsTokens) return fail(LP_ERR_INVALID_ARG, "T must be in [0, 2^31)");
+    if (out_d3 == nullptr) return fail(LP_ERR_INVALID_ARG, "out_d3 must not be NULL");
+    if (T > 0 && (logp_pi == nullptr || logp_mu == nullptr || out_w == nullptr))
+        return fail(LP_ERR_INVALID_ARG, "logp_pi, logp_mu and out_w must not be NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    h->last_stream = st;
+    h->last_launches = 0;
+    const int64_t nblk = ceil_div(T, lp::kIsBlock);
+    if (nblk > 0) {
+        lp::IsParams p{logp_pi, logp_mu, mask, T, out_w, h->blk_sum, h->blk_cnt};
+        lp::is_block_kernel<<<static_cast<unsigned>(nblk), lp::kIsThreads, 0, st>>>(p);
+        LP_CUDA(cudaGetLastError(), "is_block_kernel launch");
+        ++h->last_launches;
+    }
+    lp::is_final_kernel<<<1, 1024, 0, st>>>(h->blk_sum, h->blk_cnt, static_cast<int>(nblk),
+                                            out_d3, out_nvalid);
+    LP_CUDA(cudaGetLastError(), "is_final_kernel launch");
+    ++h->last_launches;
+    return LP_OK;
+}
+
+int lp_check(lp_handle* h) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    LP_CUDA(cudaStreamSynchronize(h->last_stream), "stream synchronize");
+    int st = 0;
+    LP_CUDA(cudaMemcpy(&st, h->status, sizeof(int), cudaMemcpyDeviceToHost), "status read");
+    if (st & lp::kStatusTimeout)
+        return fail(LP_ERR_TIMEOUT, "a device-side bounded wait expired; the kernel returned early");
+    if (st & lp::kStatusBadId)
+        return fail(LP_ERR_INVALID_ARG, "a sampled id was outside [0, V); its logprob is NaN");
+    return LP_OK;
+}
+
+int lp_clear_status(lp_handle* h, void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    LP_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), static_cast<cudaStream_t>(stream)),
+            "status clear");
+    return LP_OK;
+}
+
+}  // extern "C"

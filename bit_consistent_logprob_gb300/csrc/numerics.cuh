@@ -1,0 +1,105 @@
+// numerics.cuh -- the pinned per-element arithmetic shared by every kernel.
+//
+// Bit-identity across batch size, row position, prefill/decode and the emulated
+// tensor-parallel split holds because every path applies exactly these
+// functions, in this order, to exactly the same fp32 values.  Every operation
+// is an explicit IEEE binary32 operation (__fadd_rn / __fsub_rn / __fmul_rn /
+// __fmaf_rn, fmaxf, and CUDA's expf / expm1f / logf), so no compiler
+// contraction can differ between kernels.
+#pragma once
+
+#include <cstdint>
+
+namespace lp {
+
+constexpr int kVT = 128;     // vocabulary tile: MMA N and the log-sum-exp granularity
+constexpr int kBM = 128;     // token rows per tile: MMA M
+constexpr int kBK = 64;      // K elements per pipeline stage (128 bytes of bf16)
+constexpr int kChunk = 32;   // columns per TMEM load
+constexpr int kChunks = kVT / kChunk;
+constexpr int kMaxLeaves = 8;
+
+// Sticky device status bits (mapped to lp_status by the host).
+constexpr int kStatusBadId = 1;
+constexpr int kStatusTimeout = 2;
+
+// Pairwise sum of 32 values, adjacent pairs first, level by level.  Destroys v.
+__device__ __forceinline__ float tree_sum32(float (&v)[32]) {
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+#pragma unroll
+        for (int i = 0; i < w; ++i) v[i] = __fadd_rn(v[2 * i], v[2 * i + 1]);
+    }
+    return v[0];
+}
+
+// Log-sum-exp partial of one 128-column vocabulary tile of one row:
+//   m  = max of the valid columns' logits
+//   s  = sum over valid columns of exp(z - m): each 32-column chunk is summed by
+//        the pairwise tree above, then the four chunk sums as (c0+c1)+(c2+c3)
+//   zy = the logit in column `ycol` (untouched when ycol is outside the tile)
+// `load(c, v)` fills v with the 32 logits of chunk c; it is called twice per
+// chunk (max pass, then sum pass) and must return the same values both times.
+// Columns at or beyond `nvalid` (vocab entries >= V) are excluded.
+template <class Load>
+__device__ __forceinline__ void tile_lse(Load&& load, int nvalid, int ycol, float& m_out,
+                                         float& s_out, float& zy) {
+    float v[32];
+    float m = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+        load(c, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (c * 32 + i < nvalid) m = fmaxf(m, v[i]);
+    }
+    float cs[kChunks];
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+        load(c, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int col = c * 32 + i;
+            if (col == ycol) zy = v[i];
+            v[i] = (col < nvalid) ? expf(__fsub_rn(v[i], m)) : 0.0f;
+        }
+        cs[c] = tree_sum32(v);
+    }
+    m_out = m;
+    s_out = __fadd_rn(__fadd_rn(cs[0], cs[1]), __fadd_rn(cs[2], cs[3]));
+}
+
+// Merge two (max, sum-exp) pairs: m = max(m1, m2), s = s1 e^(m1-m) + s2 e^(m2-m).
+// Two -inf maxima give (-inf, 0); a NaN propagates through s.
+__device__ __forceinline__ float2 lse_merge(float2 a, float2 b) {
+    const float m = fmaxf(a.x, b.x);
+    if (m == -INFINITY) return make_float2(-INFINITY, 0.0f);
+    const float s = __fadd_rn(__fmul_rn(a.y, expf(__fsub_rn(a.x, m))),
+                              __fmul_rn(b.y, expf(__fsub_rn(b.x, m))));
+    return make_float2(m, s);
+}
+
+// logZ of a fully merged pair.
+__device__ __forceinline__ float lse_finish(float2 ms) { return __fadd_rn(ms.x, logf(ms.y)); }
+
+// Per-token term of D3, e^d - 1 - d with d = log pi - log mu (w = e^d, log w = d).
+// |d| < 1/4: its Taylor series d^2 (1/2! + d/3! + ... + d^7/9!) by Horner's rule
+// (the next term is below 1e-11 relative); otherwise expm1f(d) - d, where the
+// cancellation is at most ~9x.  Overflows to +inf above d ~ 88.7 (fp32 range).
+__device__ __forceinline__ float d3_term(float d) {
+    if (fabsf(d) < 0.25f) {
+        float p = 1.0f / 362880.0f;                 // 1/9!
+        p = __fmaf_rn(p, d, 1.0f / 40320.0f);       // 1/8!
+        p = __fmaf_rn(p, d, 1.0f / 5040.0f);        // 1/7!
+        p = __fmaf_rn(p, d, 1.0f / 720.0f);         // 1/6!
+        p = __fmaf_rn(p, d, 1.0f / 120.0f);         // 1/5!
+        p = __fmaf_rn(p, d, 1.0f / 24.0f);          // 1/4!
+        p = __fmaf_rn(p, d, 1.0f / 6.0f);           // 1/3!
+        p = __fmaf_rn(p, d, 0.5f);                  // 1/2!
+        return __fmul_rn(__fmul_rn(d, d), p);
+    }
+    if (d == INFINITY) return INFINITY;
+    return __fsub_rn(expm1f(d), d);
+}
+
+}  // namespace lp

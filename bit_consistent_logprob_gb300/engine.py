@@ -1,0 +1,191 @@
+"""PyTorch-facing wrapper of the C ABI: device memory and streams come from torch,
+every computation runs in the library's CUDA kernels."""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _native
+from ._native import LP_PHASE_AUTO, LP_PHASE_DECODE, LP_PHASE_PREFILL, LpConfig, LpError
+
+__all__ = ["Engine", "LpError", "LP_PHASE_AUTO", "LP_PHASE_PREFILL", "LP_PHASE_DECODE"]
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _require(t: torch.Tensor, name: str, dtype, ndim: int, device_type="cuda"):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must be {ndim}-D, got shape {tuple(t.shape)}")
+    if t.device.type != device_type:
+        raise ValueError(f"{name} must live on {device_type}, got {t.device}")
+
+
+class Engine:
+    """Bit-consistent sampled-token logprob engine for one lm_head.
+
+    W: bf16 [V, H] CUDA tensor (referenced, not copied: in-place updates are seen).
+    n_leaves: N contiguous K leaves combined by the fixed pairwise tree (1, 2, 4, 8).
+    tp_slices: emulated tensor-parallel split of K for ``logprobs`` (1 = fused path).
+    max_tokens: rows per pass; sizes the workspace.
+    """
+
+    def __init__(self, W: torch.Tensor, n_leaves: int = 8, tp_slices: int = 1,
+                 max_tokens: int = 16384, stream=None):
+        _require(W, "W", torch.bfloat16, 2)
+        if not W.is_contiguous():
+            raise ValueError("W must be contiguous")
+        self._lib = _native.load()
+        self.V, self.H = int(W.shape[0]), int(W.shape[1])
+        self.n_leaves, self.tp_slices, self.max_tokens = int(n_leaves), int(tp_slices), int(max_tokens)
+        self._W = W
+        cfg = LpConfig(self.H, self.V, self.n_leaves, self.tp_slices, self.max_tokens)
+        h = ctypes.c_void_p()
+        with torch.cuda.device(W.device):
+            _native.check(self._lib.lp_init(ctypes.byref(cfg), _ptr(W), _stream_ptr(stream),
+                                            ctypes.byref(h)))
+        self._h = h
+        self.device = W.device
+
+    # ------------------------------------------------------------------ logprobs
+    def logprobs(self, X: torch.Tensor, ids: torch.Tensor, out: torch.Tensor = None,
+                 out_logZ: torch.Tensor = None, return_logZ: bool = False,
+                 phase: int = LP_PHASE_AUTO, stream=None):
+        """logp[t] = z[t, ids[t]] - logZ[t] for X bf16 [T, H] (row stride may exceed H)."""
+        _require(X, "X", torch.bfloat16, 2)
+        _require(ids, "ids", torch.int32, 1)
+        T = int(X.shape[0])
+        if X.shape[1] != self.H or X.stride(1) != 1:
+            raise ValueError("X must be [T, H] with unit column stride")
+        if ids.shape[0] != T or not ids.is_contiguous():
+            raise ValueError("ids must be a contiguous [T] tensor")
+        if out is None:
+            out = torch.empty(T, dtype=torch.float32, device=X.device)
+        if return_logZ and out_logZ is None:
+            out_logZ = torch.empty(T, dtype=torch.float32, device=X.device)
+        ldx = X.stride(0) if T > 1 else self.H
+        _native.check(self._lib.lp_logprobs(self._h, _ptr(X), ldx, _ptr(ids), T, _ptr(out),
+                                            _ptr(out_logZ), int(phase), _stream_ptr(stream)))
+        return (out, out_logZ) if (return_logZ or out_logZ is not None) else out
+
+    def logprobs_host(self, X: torch.Tensor, ids: torch.Tensor, out: torch.Tensor = None,
+                      out_logZ: torch.Tensor = None, stream=None):
+        """Host-memory variant: X, ids, out live in (preferably pinned) CPU memory."""
+        _require(X, "X", torch.bfloat16, 2, "cpu")
+        _require(ids, "ids", torch.int32, 1, "cpu")
+        T = int(X.shape[0])
+        if X.shape[1] != self.H or X.stride(1) != 1 or ids.shape[0] != T:
+            raise ValueError("X must be [T, H] with unit column stride; ids [T]")
+        if out is None:
+            out = torch.empty(T, dtype=torch.float32, pin_memory=True)
+        ldx = X.stride(0) if T > 1 else self.H
+        with torch.cuda.device(self.device):
+            _native.check(self._lib.lp_logprobs_host(self._h, _ptr(X), ldx, _ptr(ids), T,
+                                                     _ptr(out), _ptr(out_logZ),
+                                                     _stream_ptr(stream)))
+        return out
+
+    def logits_partial(self, X: torch.Tensor, leaf_begin: int, leaf_count: int,
+                       out: torch.Tensor = None, stream=None) -> torch.Tensor:
+        """fp32 [T, V] tree node over leaves [leaf_begin, leaf_begin + leaf_count)."""
+        _require(X, "X", torch.bfloat16, 2)
+        T = int(X.shape[0])
+        if out is None:
+            ldo = (self.V + 3) // 4 * 4
+            out = torch.empty(T, ldo, dtype=torch.float32, device=X.device)[:, : self.V]
+        ldx = X.stride(0) if T > 1 else self.H
+        ldo = out.stride(0) if T > 1 else (self.V + 3) // 4 * 4
+        _native.check(self._lib.lp_logits_partial(self._h, _ptr(X), ldx, T, int(leaf_begin),
+                                                  int(leaf_count), _ptr(out), ldo,
+                                                  _stream_ptr(stream)))
+        return out
+
+    def logprobs_from_partials(self, partials: torch.Tensor, ids: torch.Tensor,
+                               out: torch.Tensor = None, out_logZ: torch.Tensor = None,
+                               return_logZ: bool = False, stream=None):
+        """Finish from gathered tree nodes: partials fp32 [n_parts, T, ldp] (ldp >= V)."""
+        _require(partials, "partials", torch.float32, 3)
+        _require(ids, "ids", torch.int32, 1)
+        n_parts, T = int(partials.shape[0]), int(partials.shape[1])
+        if partials.stride(2) != 1:
+            raise ValueError("partials must have unit stride in the vocabulary axis")
+        if out is None:
+            out = torch.empty(T, dtype=torch.float32, device=partials.device)
+        if return_logZ and out_logZ is None:
+            out_logZ = torch.empty(T, dtype=torch.float32, device=partials.device)
+        _native.check(self._lib.lp_logprobs_from_partials(
+            self._h, _ptr(partials), n_parts, partials.stride(0), partials.stride(1), _ptr(ids), T,
+            _ptr(out), _ptr(out_logZ), _stream_ptr(stream)))
+        return (out, out_logZ) if (return_logZ or out_logZ is not None) else out
+
+    # ------------------------------------------------------------------ IS / D3
+    def importance_weights(self, logp_pi: torch.Tensor, logp_mu: torch.Tensor,
+                           mask: torch.Tensor = None, out_w: torch.Tensor = None,
+                           out_d3: torch.Tensor = None, out_nvalid: torch.Tensor = None,
+                           stream=None):
+        """(w fp32 [T], D3 fp64 [1], n_valid int64 [1]) -- all on the device, no sync."""
+        _require(logp_pi, "logp_pi", torch.float32, 1)
+        _require(logp_mu, "logp_mu", torch.float32, 1)
+        T = int(logp_pi.shape[0])
+        if logp_mu.shape[0] != T:
+            raise ValueError("logp_pi and logp_mu must have the same length")
+        if mask is not None:
+            _require(mask, "mask", torch.uint8, 1)
+            if mask.shape[0] != T:
+                raise ValueError("mask must have length T")
+        dev = logp_pi.device
+        if out_w is None:
+            out_w = torch.empty(T, dtype=torch.float32, device=dev)
+        if out_d3 is None:
+            out_d3 = torch.empty(1, dtype=torch.float64, device=dev)
+        if out_nvalid is None:
+            out_nvalid = torch.empty(1, dtype=torch.int64, device=dev)
+        _native.check(self._lib.lp_importance_weights(
+            self._h, _ptr(logp_pi), _ptr(logp_mu), _ptr(mask), T, _ptr(out_w), _ptr(out_d3),
+            _ptr(out_nvalid), _stream_ptr(stream)))
+        return out_w, out_d3, out_nvalid
+
+    # ------------------------------------------------------------------ status
+    def check(self) -> None:
+        """Synchronise and raise LpError if a kernel flagged a bad id or a wait timeout."""
+        _native.check(self._lib.lp_check(self._h))
+
+    def clear_status(self, stream=None) -> None:
+        _native.check(self._lib.lp_clear_status(self._h, _stream_ptr(stream)))
+
+    @property
+    def workspace_bytes(self) -> int:
+        return int(self._lib.lp_workspace_bytes(self._h))
+
+    @property
+    def last_launch_count(self) -> int:
+        return int(self._lib.lp_last_launch_count(self._h))
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            self._lib.lp_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()

@@ -1,0 +1,200 @@
+/*
+ * lp.h -- C ABI of the bit-consistent sampled-token logprob engine (GB300, sm_103a).
+ *
+ * The engine turns final hidden states X[T,H] (bf16) into the logprob of each
+ * sampled token under an lm_head W[V,H] (bf16):
+ *
+ *   P_j[t,v] = sum_{k in leaf j} X[t,k] W[v,k]      fp32 accumulation, K cut into
+ *                                                   N contiguous leaves of H/N
+ *   z[t,v]   = fixed pairwise tree over P_0..P_{N-1} (adjacent pairs first)
+ *   logZ[t]  = fixed-order log-sum-exp of z[t,:] over the vocabulary
+ *   logp[t]  = z[t, y_t] - logZ[t]
+ *
+ * and, from a learner logprob log pi and a rollout logprob log mu, the unclipped
+ * importance weight w = exp(log pi - log mu) and D3 = mean over valid tokens of
+ * w - 1 - log w.
+ *
+ * Sources (the pages the method comes from):
+ *  - diff = 0: the rollout logprob of every valid sampled token must equal the
+ *    trainer's recomputed one exactly, with the same weights and prefix; results
+ *    must not depend on batch composition, prefill versus decode, or the
+ *    parallel layout (vLLM blog "Finish RL training faster: bit-consistent,
+ *    high-throughput, agent-driven", section 2).
+ *  - K cut into N contiguous FP32 leaves combined by a fixed binary tree, with a
+ *    fixed rank->leaf map and partials only transported between ranks
+ *    (IsoExec, SkyRL blog summary, section "Parallelism-invariant kernels";
+ *    contract example: leaves = 8, leaf_dtype = fp32).  Unproven parallel sizes
+ *    are rejected (same page, "Claims").
+ *  - w = pi / mu, unclipped, per sampled token (REINFORCE Zero summary,
+ *    sections 2 and 4); D3 = per-update token mean of w - 1 - log w (same page,
+ *    section 3).
+ *  - workspaces sized by static limits before any CUDA-graph capture, no host
+ *    synchronisation inside a step, weights updated in place (vLLM blog,
+ *    section 4.6).
+ *
+ * Every call is asynchronous on the caller's CUDA stream (cudaStream_t passed as
+ * void*; NULL = legacy default stream), performs no host synchronisation and no
+ * allocation (except lp_init, lp_free, lp_check and the *_host variants, which
+ * are documented as synchronous), and can be captured in a CUDA graph.
+ *
+ * Errors: every function returns an lp_status.  Argument errors are detected on
+ * the host and returned before anything is enqueued; lp_last_error() gives a
+ * thread-local message.  Problems found on the device (a sampled id outside
+ * [0, V), a bounded wait that expired) set a sticky status word in the handle;
+ * lp_check() synchronises and reports it.
+ */
+#ifndef LP_H_
+#define LP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LP_API __attribute__((visibility("default")))
+#else
+#define LP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum lp_status {
+    LP_OK = 0,
+    LP_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, sampled id outside [0,V) */
+    LP_ERR_UNSUPPORTED = 2, /* configuration outside the proven set (see lp_config) */
+    LP_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+    LP_ERR_OOM = 4,         /* workspace allocation failed */
+    LP_ERR_TIMEOUT = 5      /* a device-side bounded wait expired (kernel returned early) */
+} lp_status;
+
+/* Phase hint of lp_logprobs.  It selects a launch schedule only: every phase runs
+ * the same per-element arithmetic, so results are bit-identical across phases. */
+enum { LP_PHASE_AUTO = 0, LP_PHASE_PREFILL = 1, LP_PHASE_DECODE = 2 };
+
+/*
+ * Static configuration, fixed for the lifetime of a handle.
+ *   H           hidden size (K of the lm_head GEMM); H % (64 * n_leaves) == 0.
+ *   V           vocabulary size, 1 <= V < 2^31.
+ *   n_leaves    N, number of contiguous K leaves: 1, 2, 4 or 8 (the proven set).
+ *   tp_slices   emulated tensor-parallel split of K used by lp_logprobs: 1 (fused
+ *               path), or 2, 4, 8 with tp_slices dividing n_leaves.  Slice r owns
+ *               leaves [r*N/s, (r+1)*N/s) and produces that node of the leaf tree.
+ *   max_tokens  row chunk: lp_logprobs processes at most this many rows per pass
+ *               (larger T is split into chunks, which changes no bits because every
+ *               row is computed alone).  The workspace is sized by it.
+ */
+typedef struct lp_config {
+    int32_t H;
+    int32_t V;
+    int32_t n_leaves;
+    int32_t tp_slices;
+    int64_t max_tokens;
+} lp_config;
+
+typedef struct lp_handle lp_handle; /* opaque, owned by the library */
+
+/*
+ * Create a handle.  W: device pointer to the lm_head, bf16 [V, H] row-major
+ * (row v = token v), 16-byte aligned, owned by the caller, referenced (not
+ * copied): in-place updates of W are seen by later calls.  stream: used for the
+ * one-time workspace initialisation (synchronised before return).  Allocates the
+ * workspace (device memory sized by max_tokens and V, plus pinned staging for the
+ * *_host call).  Returns LP_ERR_UNSUPPORTED for a configuration outside the
+ * proven set or a device that is not sm_103.
+ */
+LP_API int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out);
+
+/*
+ * Sampled-token logprobs.
+ *   X         device, bf16 [T, ldx] row-major (row t = hidden state of token t),
+ *             16-byte aligned, ldx >= H and ldx % 8 == 0.
+ *   ids       device, int32 [T], sampled token of each row.
+ *   out_logp  device, fp32 [T]: z[t, ids[t]] - logZ[t]; NaN for an id outside
+ *             [0, V) (which also sets the sticky LP_ERR_INVALID_ARG status).
+ *   out_logZ  device, fp32 [T], or NULL: the log-partition logZ[t].
+ *   phase     LP_PHASE_*; a schedule hint only (see above).
+ * T == 0 is a no-op.  All buffers are caller-owned.
+ */
+LP_API int lp_logprobs(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int64_t T,
+                float* out_logp, float* out_logZ, int phase, void* stream);
+
+/*
+ * Same as lp_logprobs with HOST buffers (X: bf16 [T, ldx]; ids, out_logp,
+ * out_logZ as above but in host memory; pinned memory is fastest).  Rows are
+ * staged through the handle's device workspace chunk by chunk; the call
+ * returns after the results are in host memory (it synchronises `stream`).
+ */
+LP_API int lp_logprobs_host(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int64_t T,
+                     float* out_logp, float* out_logZ, void* stream);
+
+/*
+ * One node of the leaf tree: the fp32 tree over leaves
+ * [leaf_begin, leaf_begin + leaf_count) of every logit (what tensor-parallel
+ * rank r contributes when it owns those leaves).  leaf_count must be a power of
+ * two and leaf_begin a multiple of it (an aligned subtree), leaf_begin +
+ * leaf_count <= N.  With leaf_count == 1 this exports the raw leaf partials P_j.
+ *   X, ldx, T  as in lp_logprobs.
+ *   out        device, fp32 [T, ldo] row-major, ldo >= V, 16-byte aligned rows.
+ */
+LP_API int lp_logits_partial(lp_handle* h, const void* X, int64_t ldx, int64_t T, int32_t leaf_begin,
+                      int32_t leaf_count, float* out, int64_t ldo, void* stream);
+
+/*
+ * Finish the logprob from n_parts tree nodes that together cover the N leaves
+ * in order (the partials gathered from all ranks): the upper levels of the same
+ * fixed tree, then the same log-sum-exp and gather as lp_logprobs.
+ *   partials    device, fp32; part p of row t, vocab v at
+ *               partials[p * part_stride + t * ldp + v]; ldp >= V.
+ *   n_parts     1, 2, 4 or 8, dividing N.
+ *   ids, T, out_logp, out_logZ as in lp_logprobs (T <= max_tokens).
+ * Bit-identical to lp_logprobs when the parts come from lp_logits_partial with
+ * leaf_count = N / n_parts.
+ */
+LP_API int lp_logprobs_from_partials(lp_handle* h, const float* partials, int32_t n_parts,
+                              int64_t part_stride, int64_t ldp, const int32_t* ids, int64_t T,
+                              float* out_logp, float* out_logZ, void* stream);
+
+/*
+ * Importance weights and D3.
+ *   logp_pi, logp_mu  device, fp32 [T]: learner and rollout logprobs.
+ *   mask              device, uint8 [T] (nonzero = valid token), or NULL (all valid).
+ *   out_w             device, fp32 [T]: exp(logp_pi - logp_mu) for every token.
+ *   out_d3            device, one double: sum over valid tokens of
+ *                     (w - 1 - log w) / n_valid, 0 when n_valid == 0.  The sum is
+ *                     fp64 over a fixed tree of 1024-token blocks, independent of
+ *                     the launch.
+ *   out_nvalid        device, one int64: number of valid tokens (may be NULL).
+ * T may exceed max_tokens (no row-chunk limit) up to 2^31 - 1.
+ */
+LP_API int lp_importance_weights(lp_handle* h, const float* logp_pi, const float* logp_mu,
+                          const uint8_t* mask, int64_t T, float* out_w, double* out_d3,
+                          int64_t* out_nvalid, void* stream);
+
+/* Synchronise the stream last used with the handle and return the sticky device
+ * status (LP_OK, LP_ERR_INVALID_ARG for a bad id, LP_ERR_TIMEOUT). */
+LP_API int lp_check(lp_handle* h);
+
+/* Clear the sticky device status (asynchronous on `stream`). */
+LP_API int lp_clear_status(lp_handle* h, void* stream);
+
+/* Thread-local message describing the last error returned on this thread. */
+LP_API const char* lp_last_error(void);
+
+/* Workspace bytes held by the handle (device), for capacity planning. */
+LP_API int64_t lp_workspace_bytes(const lp_handle* h);
+
+/* Number of kernel launches the last lp_* compute call on this handle enqueued. */
+LP_API int32_t lp_last_launch_count(const lp_handle* h);
+
+/* ABI version (major * 100 + minor). */
+LP_API int lp_version(void);
+
+/* Synchronise and release the handle and its workspace.  NULL is a no-op. */
+LP_API void lp_free(lp_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LP_H_ */
