@@ -1,0 +1,432 @@
+#!/usr/bin/env python3
+"""Benchmark: sampled-token logprobs/sec of the bit-consistent engine on one GB300.
+
+One step = one pass of the whole hot path over one batch: the lm_head GEMM with its
+leaf tree and vocabulary-tile log-sum-exp, the combine and sampled-token gather
+(``lp_logprobs``), then the importance weights and D3 against a rollout logprob from
+a lagged weight copy (``lp_importance_weights``).  Inputs are seeded synthetic data
+already resident in HBM; W alone is larger than L2, so every step streams it from HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle on the
+host cores on a bounded row sample of the same workload.  With N > 1 (torchrun) every
+rank runs an independent replica of the workload (weak scaling, no collective on the
+data path; the ranks only meet at the timing barriers).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sampled-token logprobs/sec (prefill & decode) at diff=0; % of roofline"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+KERNEL_SOURCES = ["bit_consistent_logprob_gb300/csrc/kernels.cuh",
+                  "bit_consistent_logprob_gb300/csrc/numerics.cuh",
+                  "bit_consistent_logprob_gb300/csrc/ptx.cuh",
+                  "bit_consistent_logprob_gb300/csrc/lp_api.cu"]
+
+
+# ----------------------------------------------------------------------------- setup
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg, device=None):
+    if pg is not None:
+        if device is not None:
+            pg.barrier(device_ids=[device.index])
+        else:
+            pg.barrier()
+
+
+def max_over_ranks(pg, value: float, device) -> float:
+    if pg is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if it
+    was taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    def __init__(self, index: int, period_ms: int = 100):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(period_ms), "-i", str(index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- workloads
+def make_workload(name: str, device, seed_offset: int = 0, batch: int = 128):
+    import torch
+
+    from bit_consistent_logprob_gb300 import inputs
+
+    wl = inputs.WORKLOADS[name]
+    seed = wl.seed + seed_offset
+    if name in ("qwen_prefill", "is_d3"):
+        lengths = inputs.packed_lengths(wl.n_seqs, wl.len_lo, wl.len_hi, wl.seed)
+        T = sum(lengths)
+    elif name == "ds_decode":
+        lengths = [1] * batch
+        T = batch
+    else:
+        T = wl.T
+        lengths = [T]
+    X = inputs.hidden_states(T, wl.H, seed, device=device)
+    W = inputs.lm_head(wl.V, wl.H, seed, device=device)
+    ids = inputs.uniform_ids(T, wl.V, seed, device=device)
+    return wl, lengths, X, W, ids
+
+
+def rollout_logprobs(W, X, ids, wl, seed, max_tokens):
+    """The rollout side's logprob mu, from a weight copy a few updates behind (data prep)."""
+    from bit_consistent_logprob_gb300 import Engine, inputs
+
+    W_lag = inputs.lagged_lm_head(W, seed)
+    with Engine(W_lag, n_leaves=wl.n_leaves, max_tokens=max_tokens) as eng:
+        mu = eng.logprobs(X, ids)
+        eng.check()
+    del W_lag
+    return mu
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local, pg):
+    import torch
+
+    from bit_consistent_logprob_gb300 import Engine, LP_PHASE_DECODE, LP_PHASE_PREFILL
+
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl, lengths, X, W, ids = make_workload(args.workload, dev, seed_offset=rank, batch=args.batch)
+    T, H, V, N = X.shape[0], wl.H, wl.V, wl.n_leaves
+    max_tokens = min(T, args.max_tokens)
+    mu = rollout_logprobs(W, X, ids, wl, wl.seed + rank, max_tokens)
+    eng = Engine(W, n_leaves=N, max_tokens=max_tokens)
+    phase = LP_PHASE_DECODE if args.workload == "ds_decode" else LP_PHASE_PREFILL
+    logp = torch.empty(T, dtype=torch.float32, device=dev)
+    w = torch.empty(T, dtype=torch.float32, device=dev)
+    d3 = torch.empty(1, dtype=torch.float64, device=dev)
+    nv = torch.empty(1, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream()
+    launches = [0]
+
+    def step():
+        eng.logprobs(X, ids, out=logp, phase=phase)
+        launches[0] += eng.last_launch_count
+        eng.importance_weights(logp, mu, out_w=w, out_d3=d3, out_nvalid=nv)
+        launches[0] += eng.last_launch_count
+
+    for _ in range(args.warmup):
+        step()
+    eng.check()
+    torch.cuda.synchronize()
+    launches[0] = 0
+    eng.profile_enable(True)
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    barrier(pg, dev)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg, dev)
+    clocks = sampler.stop()
+    gemm_ms, gemm_n = eng.profile_read()
+    eng.profile_enable(False)
+    eng.check()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(pg, ms, dev)
+    gpu_launches = launches[0]
+
+    # end to end through the public API with host buffers (pinned), copies in the region
+    e2e = None
+    if not args.no_e2e:
+        Xh = X.cpu().pin_memory()
+        idsh = ids.cpu().pin_memory()
+        muh = mu.cpu().pin_memory()
+        logph = torch.empty(T, dtype=torch.float32).pin_memory()
+        wh = torch.empty(T, dtype=torch.float32).pin_memory()
+
+        def step_e2e():
+            eng.logprobs_host(Xh, idsh, out=logph)
+            return eng.importance_weights_host(logph, muh, out_w=wh)
+
+        for _ in range(max(1, args.warmup)):
+            step_e2e()
+        torch.cuda.synchronize()
+        barrier(pg, dev)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step_e2e()
+        t1 = time.perf_counter()
+        barrier(pg, dev)
+        e2e_ms = max_over_ranks(pg, (t1 - t0) * 1000.0 / args.steps, dev)
+        bi = T * H * 2 + T * 4 + T * 4 + T * 4
+        bo = T * 4 + T * 4 + 16
+        e2e = {"value": world * T / (e2e_ms / 1000.0), "unit": UNIT, "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+    peaks, peak_src = load_peaks()
+    gemm_avg_ms = gemm_ms / max(1, gemm_n)
+    launches_per_step = gemm_n / max(1, args.steps)
+    if args.workload == "ds_decode":
+        # HBM-bound: W streamed once per step plus X and the per-tile partials.
+        nb = (V + 127) // 128
+        algo = (2 * H * V + 2 * T * H + 8 * T * nb + 8 * T) / launches_per_step
+        achieved = algo / (gemm_avg_ms / 1000.0) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": f"{peak_src} hbm_gbs"}
+    else:
+        algo = 2.0 * T * H * V / launches_per_step
+        achieved = algo / (gemm_avg_ms / 1000.0) / 1e12
+        peak = float(peaks["bf16_tflops_sustained"])
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a "
+                               f"back-to-back step loop)"}
+    roof["traffic"] = recorded_traffic(args.workload)
+    roof["kernel"] = "leaf_gemm_kernel<fused>"
+    roof["kernel_ms"] = gemm_avg_ms
+    roof["algorithmic_per_launch"] = algo
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(X, W, ids, mu, wl, rows=args.cpu_rows)
+    eng.close()
+
+    if rank != 0:
+        return None
+    value = world * T / (ms_max / 1000.0)
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "T": T, "H": H, "V": V, "n_leaves": N,
+                   "n_seqs": len(lengths), "phase": "decode" if phase == LP_PHASE_DECODE else "prefill",
+                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                   "l2": f"inputs larger than L2 (W {2 * H * V / 1e6:.0f} MB streamed every step)",
+                   "step": "lp_logprobs + lp_importance_weights"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
+        "clocks": clocks,
+    }
+
+
+def cpu_baseline(X, W, ids, mu, wl, rows: int):
+    """The fp64 oracle, as it stands, on a seeded row sample of the same workload."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    T = X.shape[0]
+    rng = np.random.default_rng(wl.seed)
+    sample = np.sort(rng.choice(T, size=min(rows, T), replace=False))
+    Xh, Wh = X.cpu(), W.cpu()
+    idsh = ids.cpu().numpy()
+    oracle.build()
+    t0 = time.perf_counter()
+    logp, _ = oracle.logprobs(Xh, Wh, idsh, rows=sample)
+    oracle.importance_weights(logp.astype(np.float32), mu.cpu().numpy()[sample])
+    dt = time.perf_counter() - t0
+    del torch
+    return {"value": len(sample) / dt, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"{len(sample)} seeded rows of the {wl.name} batch (full vocabulary each), "
+                      f"logprob + importance weight"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference implementation, on a bounded row sample per step."""
+    if rank != 0:
+        return None
+    import numpy as np
+
+    import oracle
+    from bit_consistent_logprob_gb300 import inputs
+
+    wl = inputs.WORKLOADS[args.workload]
+    if args.workload in ("qwen_prefill", "is_d3"):
+        T = sum(inputs.packed_lengths(wl.n_seqs, wl.len_lo, wl.len_hi, wl.seed))
+    elif args.workload == "ds_decode":
+        T = args.batch
+    else:
+        T = wl.T
+    oracle.build()
+    # Rows generated on the host are a stand-in sample of the batch: the oracle cost per
+    # row is H * V fp64 products whatever the row holds.
+    W = inputs.lm_head(wl.V, wl.H, wl.seed)
+    rng = np.random.default_rng(wl.seed)
+    probe_rows = 2
+    Xp = inputs.hidden_states(probe_rows, wl.H, wl.seed)
+    idsp = inputs.uniform_ids(probe_rows, wl.V, wl.seed)
+    t0 = time.perf_counter()
+    oracle.logprobs(Xp, W, idsp.numpy())
+    per_row = (time.perf_counter() - t0) / probe_rows
+    rows = int(max(1, min(T, round(args.ref_step_seconds / max(per_row, 1e-9)))))
+    Xs = inputs.hidden_states(rows, wl.H, wl.seed + 1)
+    idss = inputs.uniform_ids(rows, wl.V, wl.seed + 1).numpy()
+    mus = rng.standard_normal(rows).astype(np.float32) - 5.0
+
+    def step():
+        lp, _ = oracle.logprobs(Xs, W, idss)
+        oracle.importance_weights(lp.astype(np.float32), mus)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = rows / dt
+    sample = (f"{rows} rows per step of the {wl.name} workload (H={wl.H}, V={wl.V}), full "
+              f"vocabulary per row, fp64 oracle")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1000.0,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "T": T, "H": wl.H, "V": wl.V, "n_leaves": wl.n_leaves,
+                   "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="qwen_prefill",
+                    choices=("tiny", "qwen_prefill", "ds_prefill", "ds_decode", "is_d3"))
+    ap.add_argument("--batch", type=int, default=128, help="rows of the decode workload")
+    ap.add_argument("--max-tokens", type=int, default=32768, help="row chunk of the engine")
+    ap.add_argument("--cpu-rows", type=int, default=128, help="rows of the CPU-baseline sample")
+    ap.add_argument("--ref-step-seconds", type=float, default=1.5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return args
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local, pg = dist_setup()
+    if args.gpus != world and world > 1:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_ours(args, world, rank, local, pg)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -13,6 +13,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <string>
+#include <vector>
 
 #include "kernels.cuh"
 #include "lp.h"
@@ -23,6 +24,8 @@ constexpr int kStagesGemm = 6;
 constexpr int kBand = 16;                       // vocabulary tiles per scheduling band
 constexpr int64_t kMaxIsTokens = (1LL << 31) - 1;
 constexpr int64_t kTpRows = 1024;               // rows per pass of the emulated TP path
+constexpr int kProfPairs = 4096;
+constexpr int64_t kIsStage = 1 << 20;            // tokens per pass of the host IS call
 
 thread_local std::string g_last_error = "no error";
 
@@ -109,9 +112,16 @@ struct lp_handle {
     int32_t* ids_stage = nullptr;
     float* logp_stage = nullptr;
     float* logz_stage = nullptr;
+    float* is_stage = nullptr;      // [3][kIsStage]: log pi, log mu, w of one pass
+    uint8_t* is_mask_stage = nullptr;
+    double* scalars = nullptr;      // [2]: D3 and n_valid of the host IS call
     cudaStream_t last_stream = nullptr;
     int64_t ws_bytes = 0;
     int32_t last_launches = 0;
+    // profiling: event pairs around leaf-GEMM launches
+    bool profiling = false;
+    std::vector<cudaEvent_t> prof_events;  // 2 * kProfPairs, created on enable
+    int prof_used = 0;                     // pairs recorded since the last read
 };
 
 namespace {
@@ -156,9 +166,15 @@ int launch_leaf_gemm(lp_handle* h, const CUtensorMap& tmX, int rows, int leaf_be
     const int64_t tiles = static_cast<int64_t>(p.num_row_tiles) * p.num_vocab_tiles;
     if (tiles > 0x7fffffff) return fail(LP_ERR_UNSUPPORTED, "too many tiles in one launch");
     const int grid = static_cast<int>(tiles < h->num_sms ? tiles : h->num_sms);
+    const bool prof = h->profiling && h->prof_used < kProfPairs;
+    if (prof) LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used], st), "profile event");
     lp::leaf_gemm_kernel<kFused, kStagesGemm>
         <<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(kStagesGemm), st>>>(tmX, h->tmW, p);
     LP_CUDA(cudaGetLastError(), "leaf_gemm_kernel launch");
+    if (prof) {
+        LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used + 1], st), "profile event");
+        ++h->prof_used;
+    }
     ++h->last_launches;
     return LP_OK;
 }
@@ -267,6 +283,7 @@ int32_t lp_last_launch_count(const lp_handle* h) { return h ? h->last_launches :
 void lp_free(lp_handle* h) {
     if (h == nullptr) return;
     cudaDeviceSynchronize();
+    for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
     cudaFree(h->ws_ms);
     cudaFree(h->zy);
     cudaFree(h->status);
@@ -278,6 +295,9 @@ void lp_free(lp_handle* h) {
     cudaFree(h->ids_stage);
     cudaFree(h->logp_stage);
     cudaFree(h->logz_stage);
+    cudaFree(h->is_stage);
+    cudaFree(h->is_mask_stage);
+    cudaFree(h->scalars);
     delete h;
 }
 
@@ -337,7 +357,11 @@ int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out) 
         (rc = alloc(&h->x_stage, sizeof(uint16_t) * static_cast<size_t>(mt) * cfg->H, "x_stage")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->ids_stage), sizeof(int32_t) * mt, "ids_stage")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->logp_stage), sizeof(float) * mt, "logp_stage")) ||
-        (rc = alloc(reinterpret_cast<void**>(&h->logz_stage), sizeof(float) * mt, "logz_stage")))
+        (rc = alloc(reinterpret_cast<void**>(&h->logz_stage), sizeof(float) * mt, "logz_stage")) ||
+        (rc = alloc(reinterpret_cast<void**>(&h->is_stage), sizeof(float) * 3 * kIsStage,
+                    "is_stage")) ||
+        (rc = alloc(reinterpret_cast<void**>(&h->is_mask_stage), kIsStage, "is_mask_stage")) ||
+        (rc = alloc(reinterpret_cast<void**>(&h->scalars), 2 * sizeof(double), "scalars")))
         return cleanup(rc);
     h->chunk_rows = mt;
     if (cfg->tp_slices > 1) {
@@ -515,6 +539,84 @@ int lp_importance_weights(lp_handle* h, const float* logp_pi, const float* logp_
                                             out_d3, out_nvalid);
     LP_CUDA(cudaGetLastError(), "is_final_kernel launch");
     ++h->last_launches;
+    return LP_OK;
+}
+
+int lp_importance_weights_host(lp_handle* h, const float* logp_pi, const float* logp_mu,
+                               const uint8_t* mask, int64_t T, float* out_w, double* out_d3,
+                               int64_t* out_nvalid, void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    if (T < 0 || T > kMaxIsTokens) return fail(LP_ERR_INVALID_ARG, "T must be in [0, 2^31)");
+    if (out_d3 == nullptr) return fail(LP_ERR_INVALID_ARG, "out_d3 must not be NULL");
+    if (T > 0 && (logp_pi == nullptr || logp_mu == nullptr || out_w == nullptr))
+        return fail(LP_ERR_INVALID_ARG, "logp_pi, logp_mu and out_w must not be NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    h->last_stream = st;
+    h->last_launches = 0;
+    // Stage in passes of kIsStage tokens (whole 1024-token blocks), so the block
+    // partials and the tree over them are those of one device call.
+    const int64_t chunk = kIsStage;
+    float* a = h->is_stage;
+    float* b = h->is_stage + kIsStage;
+    float* wbuf = h->is_stage + 2 * kIsStage;
+    uint8_t* mbuf = h->is_mask_stage;
+    const int64_t nblk = ceil_div(T, lp::kIsBlock);
+    for (int64_t t0 = 0; t0 < T; t0 += chunk) {
+        const int64_t n = T - t0 < chunk ? T - t0 : chunk;
+        LP_CUDA(cudaMemcpyAsync(a, logp_pi + t0, sizeof(float) * n, cudaMemcpyHostToDevice, st),
+                "logp_pi host-to-device copy");
+        LP_CUDA(cudaMemcpyAsync(b, logp_mu + t0, sizeof(float) * n, cudaMemcpyHostToDevice, st),
+                "logp_mu host-to-device copy");
+        if (mask)
+            LP_CUDA(cudaMemcpyAsync(mbuf, mask + t0, n, cudaMemcpyHostToDevice, st),
+                    "mask host-to-device copy");
+        lp::IsParams p{a, b, mask ? mbuf : nullptr, n, wbuf, h->blk_sum + t0 / lp::kIsBlock,
+                       h->blk_cnt + t0 / lp::kIsBlock};
+        lp::is_block_kernel<<<static_cast<unsigned>(ceil_div(n, lp::kIsBlock)), lp::kIsThreads, 0,
+                              st>>>(p);
+        LP_CUDA(cudaGetLastError(), "is_block_kernel launch");
+        ++h->last_launches;
+        LP_CUDA(cudaMemcpyAsync(out_w + t0, wbuf, sizeof(float) * n, cudaMemcpyDeviceToHost, st),
+                "w device-to-host copy");
+    }
+    double* d3_dev = h->scalars;
+    lp::is_final_kernel<<<1, 1024, 0, st>>>(h->blk_sum, h->blk_cnt, static_cast<int>(nblk), d3_dev,
+                                            reinterpret_cast<int64_t*>(d3_dev + 1));
+    LP_CUDA(cudaGetLastError(), "is_final_kernel launch");
+    ++h->last_launches;
+    double res[2];
+    LP_CUDA(cudaMemcpyAsync(res, d3_dev, sizeof res, cudaMemcpyDeviceToHost, st), "D3 copy");
+    LP_CUDA(cudaStreamSynchronize(st), "stream synchronize");
+    *out_d3 = res[0];
+    if (out_nvalid) std::memcpy(out_nvalid, &res[1], sizeof(int64_t));
+    return LP_OK;
+}
+
+int lp_profile_enable(lp_handle* h, int enable) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    if (enable && h->prof_events.empty()) {
+        h->prof_events.resize(2 * kProfPairs);
+        for (auto& e : h->prof_events) LP_CUDA(cudaEventCreate(&e), "cudaEventCreate");
+    }
+    h->profiling = enable != 0;
+    h->prof_used = 0;
+    return LP_OK;
+}
+
+int lp_profile_read(lp_handle* h, double* gemm_ms_total, int32_t* gemm_launches) {
+    if (h == nullptr || gemm_ms_total == nullptr)
+        return fail(LP_ERR_INVALID_ARG, "handle and gemm_ms_total must not be NULL");
+    double total = 0.0;
+    for (int i = 0; i < h->prof_used; ++i) {
+        LP_CUDA(cudaEventSynchronize(h->prof_events[2 * i + 1]), "cudaEventSynchronize");
+        float ms = 0.0f;
+        LP_CUDA(cudaEventElapsedTime(&ms, h->prof_events[2 * i], h->prof_events[2 * i + 1]),
+                "cudaEventElapsedTime");
+        total += ms;
+    }
+    *gemm_ms_total = total;
+    if (gemm_launches) *gemm_launches = h->prof_used;
+    h->prof_used = 0;
     return LP_OK;
 }
 

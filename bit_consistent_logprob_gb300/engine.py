@@ -157,6 +157,37 @@ class Engine:
             _ptr(out_nvalid), _stream_ptr(stream)))
         return out_w, out_d3, out_nvalid
 
+    def importance_weights_host(self, logp_pi: torch.Tensor, logp_mu: torch.Tensor,
+                                mask: torch.Tensor = None, out_w: torch.Tensor = None,
+                                stream=None):
+        """Host-memory variant: returns (w fp32 [T] on the host, D3 float, n_valid int)."""
+        _require(logp_pi, "logp_pi", torch.float32, 1, "cpu")
+        _require(logp_mu, "logp_mu", torch.float32, 1, "cpu")
+        T = int(logp_pi.shape[0])
+        if mask is not None:
+            _require(mask, "mask", torch.uint8, 1, "cpu")
+        if out_w is None:
+            out_w = torch.empty(T, dtype=torch.float32, pin_memory=True)
+        d3 = ctypes.c_double()
+        nv = ctypes.c_int64()
+        with torch.cuda.device(self.device):
+            _native.check(self._lib.lp_importance_weights_host(
+                self._h, _ptr(logp_pi), _ptr(logp_mu), _ptr(mask), T, _ptr(out_w),
+                ctypes.byref(d3), ctypes.byref(nv), _stream_ptr(stream)))
+        return out_w, d3.value, nv.value
+
+    # ------------------------------------------------------------------ profiling
+    def profile_enable(self, enable: bool = True) -> None:
+        """Bracket every leaf-GEMM launch with CUDA events on its stream."""
+        _native.check(self._lib.lp_profile_enable(self._h, int(bool(enable))))
+
+    def profile_read(self):
+        """(total leaf-GEMM milliseconds, launches) since the last read; synchronises."""
+        ms = ctypes.c_double()
+        n = ctypes.c_int32()
+        _native.check(self._lib.lp_profile_read(self._h, ctypes.byref(ms), ctypes.byref(n)))
+        return ms.value, n.value
+
     # ------------------------------------------------------------------ status
     def check(self) -> None:
         """Synchronise and raise LpError if a kernel flagged a bad id or a wait timeout."""

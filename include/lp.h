@@ -171,6 +171,26 @@ LP_API int lp_importance_weights(lp_handle* h, const float* logp_pi, const float
                           const uint8_t* mask, int64_t T, float* out_w, double* out_d3,
                           int64_t* out_nvalid, void* stream);
 
+/*
+ * Same as lp_importance_weights with HOST buffers (logp_pi, logp_mu, mask, out_w in
+ * host memory; out_d3 and out_nvalid are host scalars).  Tokens are staged through
+ * the device workspace in chunks of whole 1024-token blocks, so D3 is the same tree
+ * as the device call.  Synchronises `stream` before returning.
+ */
+LP_API int lp_importance_weights_host(lp_handle* h, const float* logp_pi, const float* logp_mu,
+                                      const uint8_t* mask, int64_t T, float* out_w,
+                                      double* out_d3, int64_t* out_nvalid, void* stream);
+
+/*
+ * Kernel timing for profiling.  While enabled, every leaf-GEMM launch (the dominant
+ * kernel) is bracketed by a pair of CUDA events recorded on the launch stream (at
+ * most 4096 pairs are kept).  lp_profile_read synchronises, returns the summed
+ * duration in milliseconds and the number of launches recorded since the last
+ * read, and clears the record.  Enabling creates the events (not graph-capturable).
+ */
+LP_API int lp_profile_enable(lp_handle* h, int enable);
+LP_API int lp_profile_read(lp_handle* h, double* gemm_ms_total, int32_t* gemm_launches);
+
 /* Synchronise the stream last used with the handle and return the sticky device
  * status (LP_OK, LP_ERR_INVALID_ARG for a bad id, LP_ERR_TIMEOUT). */
 LP_API int lp_check(lp_handle* h);
