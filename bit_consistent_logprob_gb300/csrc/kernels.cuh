@@ -23,9 +23,12 @@
 
 namespace lp {
 
-constexpr int kGemmThreads = 192;                 // 6 warps: TMA, MMA, 4 x epilogue
+constexpr int kEpiWarps = 8;                      // 2 per TMEM lane quarter, 64 columns each
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps; // TMA warp, MMA warp, 8 epilogue warps
 constexpr int kTileBytes = kBM * kBK * 2;         // 16 KB per operand tile per stage
-constexpr int kTmemCols = 512;                    // buf0 | buf1 | S0 | S1 (128 columns each)
+constexpr int kAccBufs = 3;                       // rotating TMEM leaf accumulators
+constexpr int kTmemCols = 512;                    // buf0 | buf1 | buf2 | S0 (128 columns each)
+constexpr uint32_t kColS0 = kAccBufs * kVT;       // TMEM slot of the deeper partial sum
 constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kVT);
 
 struct GemmParams {
@@ -37,6 +40,7 @@ struct GemmParams {
     int32_t num_row_tiles;    // ceil(T / 128)
     int32_t num_vocab_tiles;  // ceil(V / 128)
     int32_t band;             // vocabulary tiles per scheduling band
+    int32_t x_box_rows;       // rows per X TMA box (128, or T rounded up to 8 when T < 128)
     const int32_t* ids;       // [T] sampled ids (fused path)
     float2* ws_ms;            // [num_vocab_tiles][ws_ld] (max, sum-exp) per tile (fused path)
     int64_t ws_ld;
@@ -47,9 +51,11 @@ struct GemmParams {
     uint64_t timeout_ns;      // bound on every mbarrier wait
 };
 
+__host__ __device__ constexpr int kNumBars(int stages) { return 2 * stages + 2 * kAccBufs + 1 + 4; }
+
 __host__ __device__ constexpr int gemm_smem_bytes(int stages) {
-    return 1024 /* alignment slack */ + stages * 2 * kTileBytes +
-           (2 * stages + 5) * 8 /* barriers */ + 16;
+    return 1024 /* alignment slack */ + stages * 2 * kTileBytes + kNumBars(stages) * 8 +
+           16 /* TMEM address, abort flag */ + 2 * 2 * kBM * 4 /* pair exchange */;
 }
 
 // Tile schedule: the vocabulary is cut into bands of `band` tiles; within a band the
@@ -74,6 +80,33 @@ __device__ __forceinline__ void raise_timeout(const GemmParams& p, volatile int*
 // Number of trailing one bits of x.
 __device__ __forceinline__ int trailing_ones(int x) { return __ffs(~x) - 1; }
 
+template <int N>
+__device__ __forceinline__ void add_into(float (&acc)[N], const float (&v)[N]) {
+    // acc = acc + v elementwise (the left operand is the earlier leaf/subtree)
+#pragma unroll
+    for (int i = 0; i < N; ++i) acc[i] = __fadd_rn(acc[i], v[i]);
+}
+
+__device__ __forceinline__ float (&chunk_of(float (&a)[64], int c))[32] {
+    return *reinterpret_cast<float(*)[32]>(&a[c * 32]);
+}
+
+// Warp-uniform bounded wait; on failure raises the abort flag (lane 0) and returns false.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const GemmParams& p,
+                                          volatile int* abort_flag) {
+    bool got = mbar_wait(bar, parity, abort_flag, p.timeout_ns);
+    got = __all_sync(0xffffffffu, got);
+    if (!got && (threadIdx.x & 31) == 0) raise_timeout(p, abort_flag);
+    return got;
+}
+
+// Release a TMEM buffer to the MMA warp: this warp's loads from it have completed.
+__device__ __forceinline__ void release_buf(uint64_t* bar) {
+    tc_fence_before_sync();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 template <bool kFused, int kStages>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     leaf_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
@@ -87,10 +120,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* full = bars;                               // TMA -> MMA, per stage
     uint64_t* empty = bars + kStages;                    // MMA -> TMA, per stage
     uint64_t* acc_full = bars + 2 * kStages;             // MMA -> epilogue, per TMEM buffer
-    uint64_t* acc_empty = acc_full + 2;                  // epilogue -> MMA, per TMEM buffer
-    uint64_t* drain = acc_empty + 2;                     // MMA drain on abort
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* acc_empty = acc_full + kAccBufs;           // epilogue -> MMA, per TMEM buffer
+    uint64_t* drain = acc_empty + kAccBufs;              // MMA drain on abort
+    uint64_t* xbar = drain + 1;                          // epilogue pair exchange, per quarter
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(xbar + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    float* xch = reinterpret_cast<float*>(tmem_holder + 4);  // [2 kinds][2 halves][128 rows]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -100,11 +135,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 4);  // one arrive per epilogue warp
+            mbar_init(&acc_empty[b], kEpiWarps);  // every epilogue warp reads every buffer
         }
         mbar_init(drain, 1);
+        for (int q = 0; q < 4; ++q) mbar_init(&xbar[q], 2);  // the two warps of a lane quarter
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -128,6 +164,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
+            const uint32_t tx_bytes = static_cast<uint32_t>(p.x_box_rows * kBK * 2 + kTileBytes);
             uint32_t stage = 0, phase = 0;
             uint64_t issued = 0;
             bool ok = true;
@@ -143,7 +180,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes);
+                        mbar_arrive_expect_tx(&full[stage], tx_bytes);
                         tma_load_2d(&tmX, &full[stage], sA + stage * kTileBytes, kbase + kb * kBK,
                                     row0);
                         tma_load_2d(&tmW, &full[stage], sB + stage * kTileBytes, kbase + kb * kBK,
@@ -173,7 +210,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 for (int jj = 0; ok && jj < n; ++jj, ++g) {
-                    const uint32_t buf = g & 1u, use = g >> 1;
+                    const uint32_t buf = g % kAccBufs, use = g / kAccBufs;
                     if (!mbar_wait(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.timeout_ns)) {
                         raise_timeout(p, abort_flag);
                         ok = false;
@@ -213,16 +250,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
         }
     } else {
-        // ------------------------------------------------------------ epilogue (4 warps)
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        const uint32_t colS0 = 2 * kVT, colS1 = 3 * kVT;
-        uint32_t g = 0;
+        // ------------------------------------------------------------ epilogue (8 warps)
+        // Warp w may read TMEM lanes 32*(w%4)..+31; warps 2-5 take columns 0-63 of each
+        // 128-column buffer, warps 6-9 columns 64-127.
+        const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
+        const int r_in_tile = q * 32 + lane;
+        const uint32_t lane_base =
+            tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * 64);
+        uint32_t g = 0, xphase = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
             int rt, vt;
             tile_coords(tile, p, rt, vt);
-            const int row = rt * kBM + q * 32 + lane;
+            const int row = rt * kBM + r_in_tile;
             const int v0 = vt * kVT;
             const bool row_ok = row < p.T;
             int ycol = -1;
@@ -230,101 +271,124 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int y = p.ids[row];
                 if (y >= 0 && y < p.V) ycol = y - v0;
             }
-            int sc = 0;  // entries on the partial-sum stack (S0, S1)
+            // Leaf tree in post-order: the newest partial lives in registers (R), the one
+            // below it in TMEM slot S0; P_{n-2} waits in its buffer for P_{n-1}.
+            float R[64];
+            int depth = 0;
             for (int jj = 0; jj < n; ++jj, ++g) {
-                const uint32_t buf = g & 1u, use = g >> 1;
-                bool got = mbar_wait(&acc_full[buf], use & 1u, abort_flag, p.timeout_ns);
-                got = __all_sync(0xffffffffu, got);
-                if (!got) {
-                    if (lane == 0) raise_timeout(p, abort_flag);
+                const uint32_t buf = g % kAccBufs, use = g / kAccBufs;
+                if (!warp_wait(&acc_full[buf], use & 1u, p, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t colB = buf * kVT;
                 const bool last = (jj == n - 1);
-                if (!last && jj == n - 2) continue;  // P_{n-2} waits in its buffer for P_{n-1}
-                float v[32], u[32];
+                if (!last && jj == n - 2) continue;
+                const uint32_t colB = buf * kVT;
                 if (!last) {
                     if ((jj & 1) == 0) {
-                        // push P_jj
-                        const uint32_t colS = sc == 0 ? colS0 : colS1;
-#pragma unroll 1
-                        for (int c = 0; c < kChunks; ++c) {
-                            tmem_ld32(lane_base + colB + c * 32, v);
-                            tmem_st32(lane_base + colS + c * 32, v);
+                        // push P_jj (spilling the current top to S0)
+                        if (depth == 1) tmem_st64(lane_base + kColS0, R);
+                        tmem_ld64(lane_base + colB, R);
+                        ++depth;
+                    } else if (trailing_ones(jj) == 1) {
+                        // close the pair (P_{jj-1}, P_jj)
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            float a[32];
+                            tmem_ld32(lane_base + colB + c * 32, a);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) R[c * 32 + i] = __fadd_rn(R[c * 32 + i], a[i]);
                         }
-                        ++sc;
                     } else {
-                        // complete the subtrees that end at leaf jj
-                        const int t = trailing_ones(jj);
-                        const int dst = sc - t;
-#pragma unroll 1
-                        for (int c = 0; c < kChunks; ++c) {
-                            tmem_ld32(lane_base + colB + c * 32, v);
-                            for (int l = 0; l < t; ++l) {
-                                const uint32_t colS = (sc - 1 - l) == 0 ? colS0 : colS1;
-                                tmem_ld32(lane_base + colS + c * 32, u);
+                        // close the pair, then the four-leaf subtree below it in S0
 #pragma unroll
-                                for (int i = 0; i < 32; ++i) v[i] = __fadd_rn(u[i], v[i]);
-                            }
-                            tmem_st32(lane_base + (dst == 0 ? colS0 : colS1) + c * 32, v);
-                        }
-                        sc = dst + 1;
-                    }
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&acc_empty[buf]);
-                    continue;
-                }
-                // last leaf of the range: finish the tree node
-                const uint32_t colPrev = (buf ^ 1u) * kVT;
-#pragma unroll 1
-                for (int c = 0; c < kChunks; ++c) {
-                    tmem_ld32(lane_base + colB + c * 32, v);
-                    if (n > 1) {
-                        tmem_ld32(lane_base + colPrev + c * 32, u);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = __fadd_rn(u[i], v[i]);
-                        for (int l = 0; l < sc; ++l) {
-                            const uint32_t colS = (sc - 1 - l) == 0 ? colS0 : colS1;
-                            tmem_ld32(lane_base + colS + c * 32, u);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = __fadd_rn(u[i], v[i]);
-                        }
-                    }
-                    if (kFused) {
-                        tmem_st32(lane_base + colS0 + c * 32, v);  // z of this tile -> S0
-                    } else if (row_ok) {
-                        const int col0 = v0 + c * 32;
-                        float* dst = p.out + static_cast<int64_t>(row) * p.ldo + col0;
-                        if (col0 + 32 <= p.V) {
-#pragma unroll
-                            for (int i = 0; i < 32; i += 4)
-                                *reinterpret_cast<float4*>(dst + i) =
-                                    make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-                        } else {
+                        for (int c = 0; c < 2; ++c) {
+                            float a[32], b[32];
+                            tmem_ld32x2(lane_base + colB + c * 32, a, lane_base + kColS0 + c * 32, b);
 #pragma unroll
                             for (int i = 0; i < 32; ++i)
-                                if (col0 + i < p.V) dst[i] = v[i];
+                                R[c * 32 + i] = __fadd_rn(b[i], __fadd_rn(R[c * 32 + i], a[i]));
                         }
+                        --depth;
                     }
+                    release_buf(&acc_empty[buf]);
+                    continue;
                 }
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&acc_empty[buf]);
-                    if (n > 1) mbar_arrive(&acc_empty[buf ^ 1u]);
+                // last leaf of the range: finish the tree node into R
+                const uint32_t colPrev = ((g + kAccBufs - 1) % kAccBufs) * kVT;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    float a[32], b[32];
+                    if (n >= 2) {
+                        tmem_ld32x2(lane_base + colB + c * 32, a, lane_base + colPrev + c * 32, b);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) a[i] = __fadd_rn(b[i], a[i]);
+                    } else {
+                        tmem_ld32(lane_base + colB + c * 32, a);
+                    }
+                    if (depth >= 1) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) a[i] = __fadd_rn(R[c * 32 + i], a[i]);
+                    }
+                    if (depth == 2) {
+                        tmem_ld32(lane_base + kColS0 + c * 32, b);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) a[i] = __fadd_rn(b[i], a[i]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) R[c * 32 + i] = a[i];
                 }
+                release_buf(&acc_empty[buf]);
+                if (n >= 2) release_buf(&acc_empty[(g + kAccBufs - 1) % kAccBufs]);
+
+                const int col0 = v0 + h * 64;
                 if (kFused) {
-                    float m, s, zy = 0.0f;
-                    const int nvalid = min(kVT, p.V - v0);
-                    tile_lse(
-                        [&](int c, float(&z)[32]) { tmem_ld32(lane_base + colS0 + c * 32, z); },
-                        nvalid, ycol, m, s, zy);
+                    // per-tile log-sum-exp: this warp holds chunks 2h and 2h+1 of the row,
+                    // its partner (same lane quarter) the other two
+                    const int nv = min(kVT, p.V - v0) - h * 64;
+                    const float mh = fmaxf(chunk_max(chunk_of(R, 0), nv),
+                                           chunk_max(chunk_of(R, 1), nv - 32));
+                    xch[h * kBM + r_in_tile] = mh;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&xbar[q]);
+                    if (!warp_wait(&xbar[q], xphase, p, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    xphase ^= 1u;
+                    const float m = fmaxf(xch[r_in_tile], xch[kBM + r_in_tile]);
+                    float zy = 0.0f;
+                    const int yc = ycol - h * 64;
+                    const float cs0 = chunk_expsum(chunk_of(R, 0), nv, m, yc, zy);
+                    const float cs1 = chunk_expsum(chunk_of(R, 1), nv - 32, m, yc - 32, zy);
+                    const float ph = __fadd_rn(cs0, cs1);
+                    xch[2 * kBM + h * kBM + r_in_tile] = ph;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&xbar[q]);
+                    if (!warp_wait(&xbar[q], xphase, p, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    xphase ^= 1u;
                     if (row_ok) {
-                        p.ws_ms[static_cast<int64_t>(vt) * p.ws_ld + row] = make_float2(m, s);
-                        if (ycol >= 0 && ycol < kVT) p.zy[row] = zy;
+                        if (h == 0) {
+                            const float s = __fadd_rn(ph, xch[3 * kBM + r_in_tile]);
+                            p.ws_ms[static_cast<int64_t>(vt) * p.ws_ld + row] = make_float2(m, s);
+                        }
+                        if (yc >= 0 && yc < 64) p.zy[row] = zy;
+                    }
+                } else if (row_ok) {
+                    float* dst = p.out + static_cast<int64_t>(row) * p.ldo + col0;
+                    if (col0 + 64 <= p.V) {
+#pragma unroll
+                        for (int i = 0; i < 64; i += 4)
+                            *reinterpret_cast<float4*>(dst + i) =
+                                make_float4(R[i], R[i + 1], R[i + 2], R[i + 3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i)
+                            if (col0 + i < p.V) dst[i] = R[i];
                     }
                 }
             }

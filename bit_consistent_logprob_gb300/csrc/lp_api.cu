@@ -21,7 +21,7 @@
 namespace {
 
 constexpr int kStagesGemm = 6;
-constexpr int kBand = 16;                       // vocabulary tiles per scheduling band
+constexpr int kBand = 32;                       // vocabulary tiles per scheduling band
 constexpr int64_t kMaxIsTokens = (1LL << 31) - 1;
 constexpr int64_t kTpRows = 1024;               // rows per pass of the emulated TP path
 constexpr int kProfPairs = 4096;
@@ -71,12 +71,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // K-major bf16 matrix [rows, K] with a row stride of `ld` elements, read in 128 x 64
 // boxes with 128-byte swizzling (the layout the tcgen05 descriptors expect).  Rows past
 // `rows` read as zero.
-int encode_kmajor(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K, uint64_t ld) {
+int encode_kmajor(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K, uint64_t ld,
+                  uint32_t box_rows = lp::kBM) {
     auto enc = tensor_map_encoder();
     if (enc == nullptr) return fail(LP_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
     cuuint64_t dims[2] = {K, rows};
     cuuint64_t strides[1] = {ld * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(lp::kBK), static_cast<cuuint32_t>(lp::kBM)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(lp::kBK), box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -142,6 +143,13 @@ int validate_config(const lp_config* c) {
     return LP_OK;
 }
 
+// Rows per X TMA box: a full 128-row tile, or for a batch smaller than one tile just its
+// rows rounded up to 8 (the rows of the shared-memory tile past the box are never written;
+// they only feed accumulator rows that are never read back).
+uint32_t x_box_rows(int rows) {
+    return rows >= lp::kBM ? lp::kBM : static_cast<uint32_t>((rows + 7) / 8 * 8);
+}
+
 template <bool kFused>
 int launch_leaf_gemm(lp_handle* h, const CUtensorMap& tmX, int rows, int leaf_begin,
                      int leaf_count, const int32_t* ids, float* out, int64_t ldo,
@@ -155,6 +163,7 @@ int launch_leaf_gemm(lp_handle* h, const CUtensorMap& tmX, int rows, int leaf_be
     p.num_row_tiles = static_cast<int32_t>(ceil_div(rows, lp::kBM));
     p.num_vocab_tiles = h->num_vocab_tiles;
     p.band = kBand;
+    p.x_box_rows = static_cast<int32_t>(x_box_rows(rows));
     p.ids = ids;
     p.ws_ms = h->ws_ms;
     p.ws_ld = h->cfg.max_tokens;
@@ -228,7 +237,7 @@ int launch_partials_lse(lp_handle* h, const float* parts, int n_parts, int64_t p
 int logprobs_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int rows,
                    float* out_logp, float* out_logZ, cudaStream_t st) {
     CUtensorMap tmX;
-    int rc = encode_kmajor(&tmX, X, static_cast<uint64_t>(rows), h->cfg.H, ldx);
+    int rc = encode_kmajor(&tmX, X, static_cast<uint64_t>(rows), h->cfg.H, ldx, x_box_rows(rows));
     if (rc != LP_OK) return rc;
     const int s = h->cfg.tp_slices;
     if (s == 1) {
@@ -486,7 +495,8 @@ int lp_logits_partial(lp_handle* h, const void* X, int64_t ldx, int64_t T, int32
     for (int64_t r0 = 0; r0 < T; r0 += chunk) {
         const int rows = static_cast<int>(T - r0 < chunk ? T - r0 : chunk);
         CUtensorMap tmX;
-        rc = encode_kmajor(&tmX, xb + r0 * ldx * 2, static_cast<uint64_t>(rows), h->cfg.H, ldx);
+        rc = encode_kmajor(&tmX, xb + r0 * ldx * 2, static_cast<uint64_t>(rows), h->cfg.H, ldx,
+                           x_box_rows(rows));
         if (rc != LP_OK) return rc;
         rc = launch_leaf_gemm<false>(h, tmX, rows, leaf_begin, leaf_count, nullptr,
                                      out + r0 * ldo, ldo, st);

@@ -33,37 +33,54 @@ __device__ __forceinline__ float tree_sum32(float (&v)[32]) {
     return v[0];
 }
 
-// Log-sum-exp partial of one 128-column vocabulary tile of one row:
-//   m  = max of the valid columns' logits
-//   s  = sum over valid columns of exp(z - m): each 32-column chunk is summed by
-//        the pairwise tree above, then the four chunk sums as (c0+c1)+(c2+c3)
-//   zy = the logit in column `ycol` (untouched when ycol is outside the tile)
-// `load(c, v)` fills v with the 32 logits of chunk c; it is called twice per
-// chunk (max pass, then sum pass) and must return the same values both times.
-// Columns at or beyond `nvalid` (vocab entries >= V) are excluded.
+// Log-sum-exp partial of one 128-column vocabulary tile of one row, defined on its four
+// 32-column chunks c = 0..3 (columns at or beyond `nvalid`, i.e. vocabulary entries >= V,
+// are excluded):
+//   m_c = max of the chunk's valid logits, taken left to right from -inf
+//   m   = max(max(m_0, m_1), max(m_2, m_3))
+//   e_i = exp(z_i - m) for valid columns, 0 otherwise
+//   s_c = pairwise tree sum of the chunk's 32 e_i (chunk_expsum)
+//   s   = (s_0 + s_1) + (s_2 + s_3)
+// The fused GEMM epilogue splits the chunks over two warps and the tensor-parallel
+// kernel runs them in one thread; both apply exactly these operations in this order.
+__device__ __forceinline__ float chunk_max(const float (&v)[32], int nvalid) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        if (i < nvalid) m = fmaxf(m, v[i]);
+    return m;
+}
+
+// Sum of exp(z - m) over the chunk's valid columns (pairwise tree); captures the logit in
+// column `ycol` (chunk-relative) into zy.  Destroys v.
+__device__ __forceinline__ float chunk_expsum(float (&v)[32], int nvalid, float m, int ycol,
+                                              float& zy) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        if (i == ycol) zy = v[i];
+        v[i] = (i < nvalid) ? expf(__fsub_rn(v[i], m)) : 0.0f;
+    }
+    return tree_sum32(v);
+}
+
+// The whole tile in one thread.  `load(c, v)` fills v with the 32 logits of chunk c; it is
+// called twice per chunk (max pass, then sum pass).
 template <class Load>
 __device__ __forceinline__ void tile_lse(Load&& load, int nvalid, int ycol, float& m_out,
                                          float& s_out, float& zy) {
     float v[32];
-    float m = -INFINITY;
+    float mc[kChunks];
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
         load(c, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (c * 32 + i < nvalid) m = fmaxf(m, v[i]);
+        mc[c] = chunk_max(v, nvalid - c * 32);
     }
+    const float m = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
     float cs[kChunks];
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
         load(c, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int col = c * 32 + i;
-            if (col == ycol) zy = v[i];
-            v[i] = (col < nvalid) ? expf(__fsub_rn(v[i], m)) : 0.0f;
-        }
-        cs[c] = tree_sum32(v);
+        cs[c] = chunk_expsum(v, nvalid - c * 32, m, ycol - c * 32, zy);
     }
     m_out = m;
     s_out = __fadd_rn(__fadd_rn(cs[0], cs[1]), __fadd_rn(cs[2], cs[3]));
