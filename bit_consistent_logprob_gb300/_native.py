@@ -44,6 +44,8 @@ SIGNATURES = {
     "lp_profile_enable": (ctypes.c_int, [_p, ctypes.c_int]),
     "lp_profile_read": (ctypes.c_int, [_p, ctypes.POINTER(ctypes.c_double),
                                        ctypes.POINTER(ctypes.c_int32)]),
+    "lp_logprobs_noalloc": (ctypes.c_int, [_p, _i32, _i32, _i32, _p, _i64, _p, _i64, _p, _p, _p]),
+    "lp_noalloc_last_error": (ctypes.c_char_p, []),
     "lp_check": (ctypes.c_int, [_p]),
     "lp_clear_status": (ctypes.c_int, [_p, _p]),
     "lp_last_error": (ctypes.c_char_p, []),

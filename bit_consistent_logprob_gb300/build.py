@@ -1,7 +1,8 @@
 """Build the native library (``_build/liblp.so``) with nvcc for sm_103a only.
 
-One translation unit (``csrc/lp_api.cu``) holds the C ABI and every kernel, so
-all kernels share one compilation of the pinned numerics.  The library links
+``csrc/lp_api.cu`` holds the handle-based C ABI and ``csrc/lp_noalloc.cu`` the
+no-allocation entry point; both instantiate the same kernel templates from
+``csrc/kernels.cuh`` with the same flags, so they share the pinned numerics.  The library links
 the shared CUDA runtime and resolves the driver's tensor-map encoder at run
 time (no link against libcuda).
 """
@@ -18,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "liblp.so")
-SOURCES = [os.path.join(CSRC, "lp_api.cu")]
+SOURCES = [os.path.join(CSRC, "lp_api.cu"), os.path.join(CSRC, "lp_noalloc.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("kernels.cuh", "numerics.cuh", "ptx.cuh")] + [
     os.path.join(INCLUDE, "lp.h")]
 

@@ -15,6 +15,9 @@
 //                             1024-token blocks (fp64 sums).
 #pragma once
 
+// Non-template kernels are `static` (internal linkage): each translation unit that
+// includes this header gets its own copy, compiled from the same source.
+
 #include <cuda.h>
 #include <cstdint>
 
@@ -468,7 +471,7 @@ struct CombineParams {
     int* status;
 };
 
-__global__ void __launch_bounds__(128) lse_combine_kernel(const CombineParams p) {
+static __global__ void __launch_bounds__(128) lse_combine_kernel(const CombineParams p) {
     extern __shared__ float2 cmb_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = blockIdx.x * 4 + warp;
@@ -526,7 +529,7 @@ struct IsParams {
 // Per token: d = log pi - log mu, w = e^d, term = e^d - 1 - d.  Per block of 1024
 // tokens: fp64 sum of the valid terms, each thread adding its 4 tokens in order, then
 // a fixed xor-butterfly over the 32 lanes and a pairwise tree over the 8 warps.
-__global__ void __launch_bounds__(kIsThreads) is_block_kernel(const IsParams p) {
+static __global__ void __launch_bounds__(kIsThreads) is_block_kernel(const IsParams p) {
     __shared__ double wsum[kIsThreads / 32];
     __shared__ long long wcnt[kIsThreads / 32];
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kIsBlock + threadIdx.x * 4;
@@ -590,7 +593,7 @@ __device__ __forceinline__ void block_tree_f64(double* a, int n) {
 // One block: the tree over all block partials, taken in aligned chunks of kIsChunk
 // (each chunk is a whole subtree of the level-wise tree, so the result is the same
 // as one tree over every block), then D3 = sum / n_valid.
-__global__ void __launch_bounds__(1024) is_final_kernel(const double* blk_sum,
+static __global__ void __launch_bounds__(1024) is_final_kernel(const double* blk_sum,
                                                         const long long* blk_cnt, int num_blocks,
                                                         double* out_d3, int64_t* out_nvalid) {
     __shared__ double a[kIsChunk];

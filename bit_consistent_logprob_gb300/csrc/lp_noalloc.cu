@@ -1,0 +1,228 @@
+// lp_noalloc.cu -- lp_logprobs_noalloc: the fused sampled-token logprob path for callers
+// that must not allocate device memory.
+//
+// Some callers cannot call cudaMalloc: code that runs while a CUDA graph is being
+// captured, runtimes whose memory is planned ahead by their own allocator (which must not
+// see allocations behind its back), or hosts that forbid allocation after start-up.  For
+// them this entry point needs no handle and no workspace: the per-tile (max, sum-exp)
+// partials, the sampled logits and the status word live in one file-scope device array
+// of fixed size, g_lp_noalloc_scratch, which every GPU that loads the library holds until
+// the process exits.  The caller still passes the inputs and the outputs.
+//
+// The kernels are the same templates as the handle-based path (same per-element
+// arithmetic, so the results are bit-identical to lp_logprobs with tp_slices = 1).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "kernels.cuh"
+#include "lp.h"
+
+namespace {
+
+constexpr int kStages = 6;
+constexpr int kBand = 32;
+// Capacity of the static scratch (stated in include/lp.h):
+constexpr int64_t kNoallocMaxTileRows = int64_t(1) << 19;  // T * ceil(V/128) (max, sum) pairs
+constexpr int64_t kNoallocMaxRows = int64_t(1) << 15;      // T per call
+constexpr size_t kMsBytes = static_cast<size_t>(kNoallocMaxTileRows) * sizeof(float2);  // 4 MiB
+constexpr size_t kZyBytes = static_cast<size_t>(kNoallocMaxRows) * sizeof(float);       // 128 KiB
+constexpr size_t kStatusBytes = 256;
+constexpr size_t kScratchBytes = kMsBytes + kZyBytes + kStatusBytes;
+constexpr int kMaxDevices = 64;
+
+}  // namespace
+
+// The scratch.  In host code this name is only a host-side stand-in for the device array:
+// its address must come from cudaGetSymbolAddress (done once per device below).
+static __device__ __align__(256) unsigned char g_lp_noalloc_scratch[kScratchBytes];
+
+namespace {
+
+thread_local std::string g_noalloc_error = "no error";
+
+int nfail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_noalloc_error = buf;
+    return code;
+}
+
+struct DeviceSetup {
+    std::once_flag once;
+    int status = LP_OK;
+    std::string message;
+    unsigned char* scratch = nullptr;  // device address of g_lp_noalloc_scratch on this device
+    int num_sms = 0;
+};
+DeviceSetup g_setup[kMaxDevices];
+
+// Once per device, with that device current: resolve the scratch array's device address,
+// check the architecture and raise the kernels' dynamic shared-memory limits.  Nothing here
+// allocates.
+void setup_device(int dev, DeviceSetup& s) {
+    cudaDeviceProp prop;
+    cudaError_t e = cudaGetDeviceProperties(&prop, dev);
+    if (e == cudaSuccess && !(prop.major == 10 && prop.minor == 3)) {
+        s.status = LP_ERR_UNSUPPORTED;
+        s.message = "lp_logprobs_noalloc is built for sm_103a (GB300)";
+        return;
+    }
+    void* ptr = nullptr;
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&ptr, g_lp_noalloc_scratch);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<true, kStages>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 lp::gemm_smem_bytes(kStages));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(lp::lse_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 227 * 1024);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        s.status = LP_ERR_CUDA;
+        s.message = std::string("no-alloc set-up failed: ") + cudaGetErrorString(e);
+        return;
+    }
+    s.scratch = static_cast<unsigned char*>(ptr);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+int encode(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K, uint64_t ld,
+           uint32_t box_rows) {
+    auto enc = encoder();
+    if (enc == nullptr) return nfail(LP_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t dims[2] = {K, rows};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(lp::kBK), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return nfail(LP_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return LP_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+LP_API const char* lp_noalloc_last_error(void) { return g_noalloc_error.c_str(); }
+
+LP_API int lp_logprobs_noalloc(const void* W, int32_t H, int32_t V, int32_t n_leaves, const void* X,
+                        int64_t ldx, const int32_t* ids, int64_t T, float* out_logp,
+                        float* out_logZ, void* stream) {
+    // ---- host-side checks (before any CUDA call)
+    if (!(n_leaves == 1 || n_leaves == 2 || n_leaves == 4 || n_leaves == 8))
+        return nfail(LP_ERR_UNSUPPORTED, "n_leaves must be 1, 2, 4 or 8 (got %d)", n_leaves);
+    if (H <= 0 || V <= 0 || H % (lp::kBK * n_leaves) != 0)
+        return nfail(LP_ERR_UNSUPPORTED, "need H > 0, V > 0 and H %% (64 * n_leaves) == 0");
+    if (T < 0) return nfail(LP_ERR_INVALID_ARG, "T must be >= 0");
+    const int64_t nb = (static_cast<int64_t>(V) + lp::kVT - 1) / lp::kVT;
+    if (T > kNoallocMaxRows || T * nb > kNoallocMaxTileRows)
+        return nfail(LP_ERR_INVALID_ARG,
+                     "T = %lld rows x %lld vocabulary tiles exceeds the static scratch "
+                     "(at most %lld rows and %lld row-tiles; use lp_logprobs with a handle)",
+                     (long long)T, (long long)nb, (long long)kNoallocMaxRows,
+                     (long long)kNoallocMaxTileRows);
+    if (T == 0) return LP_OK;
+    if (W == nullptr || X == nullptr || ids == nullptr || out_logp == nullptr)
+        return nfail(LP_ERR_INVALID_ARG, "W, X, ids and out_logp must not be NULL");
+    if (!aligned16(W) || !aligned16(X) || ldx < H || ldx % 8 != 0)
+        return nfail(LP_ERR_INVALID_ARG, "W and X must be 16-byte aligned, ldx >= H, ldx %% 8 == 0");
+    if (static_cast<int64_t>(nb) * 4 * sizeof(float2) > 227 * 1024)
+        return nfail(LP_ERR_UNSUPPORTED, "V too large");
+
+    // ---- once-per-device set-up (the first call on a device; it must precede any capture)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return nfail(LP_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return nfail(LP_ERR_UNSUPPORTED, "device index too large");
+    DeviceSetup& s = g_setup[dev];
+    std::call_once(s.once, setup_device, dev, std::ref(s));
+    if (s.status != LP_OK) return nfail(s.status, "%s", s.message.c_str());
+
+    float2* ws_ms = reinterpret_cast<float2*>(s.scratch);
+    float* zy = reinterpret_cast<float*>(s.scratch + kMsBytes);
+    int* status = reinterpret_cast<int*>(s.scratch + kMsBytes + kZyBytes);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    CUtensorMap tmW, tmX;
+    const int rows = static_cast<int>(T);
+    const uint32_t box = rows >= lp::kBM ? lp::kBM : static_cast<uint32_t>((rows + 7) / 8 * 8);
+    int rc = encode(&tmW, W, static_cast<uint64_t>(V), H, H, lp::kBM);
+    if (rc == LP_OK) rc = encode(&tmX, X, static_cast<uint64_t>(rows), H, ldx, box);
+    if (rc != LP_OK) return rc;
+
+    // the status word starts at zero for every call (the array keeps the last call's data)
+    e = cudaMemsetAsync(status, 0, sizeof(int), st);
+    if (e != cudaSuccess) return nfail(LP_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
+
+    lp::GemmParams p{};
+    p.T = rows;
+    p.V = V;
+    p.leaf_len = H / n_leaves;
+    p.leaf_begin = 0;
+    p.leaf_count = n_leaves;
+    p.num_row_tiles = (rows + lp::kBM - 1) / lp::kBM;
+    p.num_vocab_tiles = static_cast<int32_t>(nb);
+    p.band = kBand;
+    p.x_box_rows = static_cast<int32_t>(box);
+    p.ids = ids;
+    p.ws_ms = ws_ms;
+    p.ws_ld = T;
+    p.zy = zy;
+    p.out = nullptr;
+    p.ldo = 0;
+    p.status = status;
+    p.timeout_ns = 2000000000ull;
+    const int64_t tiles = static_cast<int64_t>(p.num_row_tiles) * nb;
+    const int grid = static_cast<int>(tiles < s.num_sms ? tiles : s.num_sms);
+    lp::leaf_gemm_kernel<true, kStages>
+        <<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(kStages), st>>>(tmX, tmW, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return nfail(LP_ERR_CUDA, "leaf_gemm_kernel launch: %s", cudaGetErrorString(e));
+
+    lp::CombineParams c{};
+    c.ws_ms = ws_ms;
+    c.ws_ld = T;
+    c.zy = zy;
+    c.ids = ids;
+    c.T = rows;
+    c.V = V;
+    c.num_vocab_tiles = static_cast<int32_t>(nb);
+    c.out_logp = out_logp;
+    c.out_logZ = out_logZ;
+    c.status = status;
+    lp::lse_combine_kernel<<<static_cast<unsigned>((rows + 3) / 4), 128,
+                             4 * sizeof(float2) * static_cast<size_t>(nb), st>>>(c);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return nfail(LP_ERR_CUDA, "lse_combine_kernel launch: %s", cudaGetErrorString(e));
+    return LP_OK;
+}
+
+}  // extern "C"

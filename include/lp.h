@@ -191,6 +191,29 @@ LP_API int lp_importance_weights_host(lp_handle* h, const float* logp_pi, const 
 LP_API int lp_profile_enable(lp_handle* h, int enable);
 LP_API int lp_profile_read(lp_handle* h, double* gemm_ms_total, int32_t* gemm_launches);
 
+/*
+ * lp_logprobs without a handle and without any device allocation.  (The pages have no
+ * counterpart; this is a deployment entry point.)  For callers that cannot call
+ * cudaMalloc -- code running while a CUDA graph is captured, runtimes whose device memory
+ * is planned ahead by their own allocator, hosts that forbid allocation after start-up.
+ * The scratch (per-tile max/sum-exp pairs, sampled logits, a status word) is a fixed
+ * 4.25 MiB file-scope device array that every GPU loading the library holds until exit.
+ *   W, H, V, n_leaves  as in lp_config / lp_init (W referenced, bf16 [V, H]).
+ *   X, ldx, ids, T, out_logp, out_logZ  as in lp_logprobs.
+ * Limits: T <= 32768 and T * ceil(V / 128) <= 524288 (e.g. 441 rows at V = 151936);
+ * larger calls return LP_ERR_INVALID_ARG and must use lp_logprobs with a handle.
+ * The first call on a device resolves the array's device address and sets kernel
+ * attributes (no allocation); make that first call before any stream capture.
+ * Every call shares the array: calls whose kernels may overlap on the GPU (other streams,
+ * other threads) race and must be serialised by the caller.  An id outside [0, V) gives
+ * NaN (there is no sticky status for this entry point).  Bit-identical to lp_logprobs
+ * with tp_slices = 1.  Errors are described by lp_noalloc_last_error().
+ */
+LP_API int lp_logprobs_noalloc(const void* W, int32_t H, int32_t V, int32_t n_leaves,
+                               const void* X, int64_t ldx, const int32_t* ids, int64_t T,
+                               float* out_logp, float* out_logZ, void* stream);
+LP_API const char* lp_noalloc_last_error(void);
+
 /* Synchronise the stream last used with the handle and return the sticky device
  * status (LP_OK, LP_ERR_INVALID_ARG for a bad id, LP_ERR_TIMEOUT). */
 LP_API int lp_check(lp_handle* h);
