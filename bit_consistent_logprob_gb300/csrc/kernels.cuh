@@ -56,9 +56,15 @@ struct GemmParams {
 
 __host__ __device__ constexpr int kNumBars(int stages) { return 2 * stages + 2 * kAccBufs + 1 + 4; }
 
-__host__ __device__ constexpr int gemm_smem_bytes(int stages) {
-    return 1024 /* alignment slack */ + stages * 2 * kTileBytes + kNumBars(stages) * 8 +
-           16 /* TMEM address, abort flag */ + 2 * 2 * kBM * 4 /* pair exchange */;
+// A pipeline stage holds kSub 64-wide K sub-blocks of X and of W (4 MMAs of K = 16 per
+// sub-block).  More MMAs per stage means fewer barrier synchronisations per MMA in the
+// issuing thread; the MMA sequence of a leaf is the same for every kSub.
+__host__ __device__ constexpr int gemm_stages(int sub) { return 6 / sub; }
+
+__host__ __device__ constexpr int gemm_smem_bytes(int sub) {
+    return 1024 /* alignment slack */ + gemm_stages(sub) * sub * 2 * kTileBytes +
+           kNumBars(gemm_stages(sub)) * 8 + 16 /* TMEM address, abort flag */ +
+           2 * 2 * kBM * 4 /* pair exchange */;
 }
 
 // Tile schedule: the vocabulary is cut into bands of `band` tiles; within a band the
@@ -83,17 +89,6 @@ __device__ __forceinline__ void raise_timeout(const GemmParams& p, volatile int*
 // Number of trailing one bits of x.
 __device__ __forceinline__ int trailing_ones(int x) { return __ffs(~x) - 1; }
 
-template <int N>
-__device__ __forceinline__ void add_into(float (&acc)[N], const float (&v)[N]) {
-    // acc = acc + v elementwise (the left operand is the earlier leaf/subtree)
-#pragma unroll
-    for (int i = 0; i < N; ++i) acc[i] = __fadd_rn(acc[i], v[i]);
-}
-
-__device__ __forceinline__ float (&chunk_of(float (&a)[64], int c))[32] {
-    return *reinterpret_cast<float(*)[32]>(&a[c * 32]);
-}
-
 // Warp-uniform bounded wait; on failure raises the abort flag (lane 0) and returns false.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const GemmParams& p,
                                           volatile int* abort_flag) {
@@ -110,16 +105,18 @@ __device__ __forceinline__ void release_buf(uint64_t* bar) {
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
-template <bool kFused, int kStages>
+template <bool kFused, int kSub>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     leaf_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmW, const GemmParams p) {
+    constexpr int kStages = gemm_stages(kSub);
+    constexpr int kStageBytes = kSub * kTileBytes;       // one operand, one stage
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sA = smem;                                  // X tiles   [kStages][128 x 64] bf16
-    uint8_t* sB = smem + kStages * kTileBytes;           // W tiles   [kStages][128 x 64] bf16
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kStages * kTileBytes);
+    uint8_t* sA = smem;                                  // X  [kStages][kSub][128 x 64] bf16
+    uint8_t* sB = smem + kStages * kStageBytes;          // W  [kStages][kSub][128 x 64] bf16
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kStages * kStageBytes);
     uint64_t* full = bars;                               // TMA -> MMA, per stage
     uint64_t* empty = bars + kStages;                    // MMA -> TMA, per stage
     uint64_t* acc_full = bars + 2 * kStages;             // MMA -> epilogue, per TMEM buffer
@@ -161,13 +158,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t tmem_base = *tmem_holder;
 
     const int num_tiles = p.num_row_tiles * p.num_vocab_tiles;
-    const int nkb = p.leaf_len / kBK;
+    const int nkb = p.leaf_len / (kBK * kSub);   // stages per leaf
     const int n = p.leaf_count;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            const uint32_t tx_bytes = static_cast<uint32_t>(p.x_box_rows * kBK * 2 + kTileBytes);
+            const uint32_t tx_bytes =
+                static_cast<uint32_t>(kSub * (p.x_box_rows * kBK * 2 + kTileBytes));
             uint32_t stage = 0, phase = 0;
             uint64_t issued = 0;
             bool ok = true;
@@ -184,10 +182,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             break;
                         }
                         mbar_arrive_expect_tx(&full[stage], tx_bytes);
-                        tma_load_2d(&tmX, &full[stage], sA + stage * kTileBytes, kbase + kb * kBK,
-                                    row0);
-                        tma_load_2d(&tmW, &full[stage], sB + stage * kTileBytes, kbase + kb * kBK,
-                                    v0);
+#pragma unroll
+                        for (int u = 0; u < kSub; ++u) {
+                            const int k0 = kbase + (kb * kSub + u) * kBK;
+                            tma_load_2d(&tmX, &full[stage], sA + stage * kStageBytes + u * kTileBytes,
+                                        k0, row0);
+                            tma_load_2d(&tmW, &full[stage], sB + stage * kStageBytes + u * kTileBytes,
+                                        k0, v0);
+                        }
                         ++issued;
                         if (++stage == kStages) {
                             stage = 0;
@@ -208,41 +210,61 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // The tensor core's instruction queue is shallow, so this thread does as little as
+        // possible between MMAs: descriptors are precomputed, buffer/stage indices advance
+        // incrementally, and the barriers of the next stage and the next leaf's buffer are
+        // probed (non-blocking) before the current stage's MMAs are issued.
         if (lane == 0) {
-            uint32_t stage = 0, phase = 0, g = 0;
+            const uint64_t descA = sw128_kmajor_desc(smem_u32(sA));
+            const uint64_t descB = sw128_kmajor_desc(smem_u32(sB));
+            constexpr uint32_t kStageDesc = kStageBytes >> 4;  // descriptor units per stage
+            constexpr uint32_t kSubDesc = kTileBytes >> 4;     // ... per 64-K sub-block
+            uint32_t stage = 0, phase = 0;
+            uint32_t buf = 0, bphase = 0;  // TMEM buffer of the current leaf, its use parity
             bool ok = true;
+            bool ready = mbar_test_wait(&full[0], 0);
+            bool acc_ready = true;  // the first uses of every buffer find it free
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                for (int jj = 0; ok && jj < n; ++jj, ++g) {
-                    const uint32_t buf = g % kAccBufs, use = g / kAccBufs;
-                    if (!mbar_wait(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.timeout_ns)) {
+                for (int jj = 0; ok && jj < n; ++jj) {
+                    if (!acc_ready &&
+                        !mbar_wait(&acc_empty[buf], bphase ^ 1u, abort_flag, p.timeout_ns)) {
                         raise_timeout(p, abort_flag);
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t d_tmem = tmem_base + buf * kVT;
+                    const uint32_t d_tmem = tmem_base + (buf << 7);
+                    const uint32_t nbuf = buf + 1 == kAccBufs ? 0u : buf + 1;
+                    const uint32_t nbphase = buf + 1 == kAccBufs ? bphase ^ 1u : bphase;
                     for (int kb = 0; kb < nkb; ++kb) {
-                        if (!mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns)) {
+                        if (!ready && !mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns)) {
                             raise_timeout(p, abort_flag);
                             ok = false;
                             break;
                         }
                         tc_fence_after_sync();
-                        const uint64_t a0 = sw128_kmajor_desc(smem_u32(sA + stage * kTileBytes));
-                        const uint64_t b0 = sw128_kmajor_desc(smem_u32(sB + stage * kTileBytes));
+                        const uint32_t nstage = stage + 1 == kStages ? 0u : stage + 1;
+                        const uint32_t nphase = stage + 1 == kStages ? phase ^ 1u : phase;
+                        ready = mbar_test_wait(&full[nstage], nphase);
+                        if (kb == nkb - 1) acc_ready = mbar_test_wait(&acc_empty[nbuf], nbphase ^ 1u);
+                        const uint64_t a = descA + stage * kStageDesc;
+                        const uint64_t b = descB + stage * kStageDesc;
+                        // +32 bytes (2 descriptor units) per K step of 16 bf16 inside a row;
+                        // only the leaf's very first MMA starts a fresh accumulator
+                        umma_bf16(d_tmem, a, b, kIdesc, kb != 0 ? 1u : 0u);
 #pragma unroll
-                        for (int k = 0; k < kBK / 16; ++k) {
-                            // +32 bytes per K step of 16 bf16 inside the swizzled row
-                            umma_bf16(d_tmem, a0 + 2u * k, b0 + 2u * k, kIdesc,
-                                      (kb | k) != 0 ? 1u : 0u);
+                        for (int i = 1; i < kSub * (kBK / 16); ++i) {
+                            const uint32_t off = (i >> 2) * kSubDesc + 2u * (i & 3);
+                            umma_bf16(d_tmem, a + off, b + off, kIdesc, 1u);
                         }
                         umma_commit(&empty[stage]);
-                        if (++stage == kStages) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
+                        stage = nstage;
+                        phase = nphase;
                     }
-                    if (ok) umma_commit(&acc_full[buf]);
+                    if (!ok) break;
+                    umma_commit(&acc_full[buf]);
+                    buf = nbuf;
+                    bphase = nbphase;
                 }
             }
             if (!ok) {
@@ -297,21 +319,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     } else if (trailing_ones(jj) == 1) {
                         // close the pair (P_{jj-1}, P_jj)
 #pragma unroll
-                        for (int c = 0; c < 2; ++c) {
+                        for (int cc = 0; cc < 2; ++cc) {
                             float a[32];
-                            tmem_ld32(lane_base + colB + c * 32, a);
+                            tmem_ld32(lane_base + colB + cc * 32, a);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) R[c * 32 + i] = __fadd_rn(R[c * 32 + i], a[i]);
+                            for (int i = 0; i < 32; ++i) R[cc * 32 + i] = __fadd_rn(R[cc * 32 + i], a[i]);
                         }
                     } else {
                         // close the pair, then the four-leaf subtree below it in S0
 #pragma unroll
-                        for (int c = 0; c < 2; ++c) {
+                        for (int cc = 0; cc < 2; ++cc) {
                             float a[32], b[32];
-                            tmem_ld32x2(lane_base + colB + c * 32, a, lane_base + kColS0 + c * 32, b);
+                            tmem_ld32x2(lane_base + colB + cc * 32, a, lane_base + kColS0 + cc * 32, b);
 #pragma unroll
                             for (int i = 0; i < 32; ++i)
-                                R[c * 32 + i] = __fadd_rn(b[i], __fadd_rn(R[c * 32 + i], a[i]));
+                                R[cc * 32 + i] = __fadd_rn(b[i], __fadd_rn(R[cc * 32 + i], a[i]));
                         }
                         --depth;
                     }
@@ -321,26 +343,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 // last leaf of the range: finish the tree node into R
                 const uint32_t colPrev = ((g + kAccBufs - 1) % kAccBufs) * kVT;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int cc = 0; cc < 2; ++cc) {
                     float a[32], b[32];
                     if (n >= 2) {
-                        tmem_ld32x2(lane_base + colB + c * 32, a, lane_base + colPrev + c * 32, b);
+                        tmem_ld32x2(lane_base + colB + cc * 32, a, lane_base + colPrev + cc * 32, b);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) a[i] = __fadd_rn(b[i], a[i]);
                     } else {
-                        tmem_ld32(lane_base + colB + c * 32, a);
+                        tmem_ld32(lane_base + colB + cc * 32, a);
                     }
                     if (depth >= 1) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) a[i] = __fadd_rn(R[c * 32 + i], a[i]);
+                        for (int i = 0; i < 32; ++i) a[i] = __fadd_rn(R[cc * 32 + i], a[i]);
                     }
                     if (depth == 2) {
-                        tmem_ld32(lane_base + kColS0 + c * 32, b);
+                        tmem_ld32(lane_base + kColS0 + cc * 32, b);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) a[i] = __fadd_rn(b[i], a[i]);
                     }
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) R[c * 32 + i] = a[i];
+                    for (int i = 0; i < 32; ++i) R[cc * 32 + i] = a[i];
                 }
                 release_buf(&acc_empty[buf]);
                 if (n >= 2) release_buf(&acc_empty[(g + kAccBufs - 1) % kAccBufs]);
@@ -349,10 +371,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (kFused) {
                     // per-tile log-sum-exp: this warp holds chunks 2h and 2h+1 of the row,
                     // its partner (same lane quarter) the other two
+                    float(&R0)[32] = *reinterpret_cast<float(*)[32]>(&R[0]);
+                    float(&R1)[32] = *reinterpret_cast<float(*)[32]>(&R[32]);
                     const int nv = min(kVT, p.V - v0) - h * 64;
-                    const float mh = fmaxf(chunk_max(chunk_of(R, 0), nv),
-                                           chunk_max(chunk_of(R, 1), nv - 32));
-                    xch[h * kBM + r_in_tile] = mh;
+                    xch[h * kBM + r_in_tile] = fmaxf(chunk_max(R0, nv), chunk_max(R1, nv - 32));
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&xbar[q]);
                     if (!warp_wait(&xbar[q], xphase, p, abort_flag)) {
@@ -363,8 +385,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const float m = fmaxf(xch[r_in_tile], xch[kBM + r_in_tile]);
                     float zy = 0.0f;
                     const int yc = ycol - h * 64;
-                    const float cs0 = chunk_expsum(chunk_of(R, 0), nv, m, yc, zy);
-                    const float cs1 = chunk_expsum(chunk_of(R, 1), nv - 32, m, yc - 32, zy);
+                    const float cs0 = chunk_expsum(R0, nv, m, yc, zy);
+                    const float cs1 = chunk_expsum(R1, nv - 32, m, yc - 32, zy);
                     const float ph = __fadd_rn(cs0, cs1);
                     xch[2 * kBM + h * kBM + r_in_tile] = ph;
                     __syncwarp();
@@ -374,7 +396,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     xphase ^= 1u;
-                    if (row_ok) {
+                    if (row_ok && vt < p.num_vocab_tiles) {
                         if (h == 0) {
                             const float s = __fadd_rn(ph, xch[3 * kBM + r_in_tile]);
                             p.ws_ms[static_cast<int64_t>(vt) * p.ws_ld + row] = make_float2(m, s);

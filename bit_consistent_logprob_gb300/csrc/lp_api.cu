@@ -20,7 +20,6 @@
 
 namespace {
 
-constexpr int kStagesGemm = 6;
 constexpr int kBand = 32;                       // vocabulary tiles per scheduling band
 constexpr int64_t kMaxIsTokens = (1LL << 31) - 1;
 constexpr int64_t kTpRows = 1024;               // rows per pass of the emulated TP path
@@ -177,8 +176,13 @@ int launch_leaf_gemm(lp_handle* h, const CUtensorMap& tmX, int rows, int leaf_be
     const int grid = static_cast<int>(tiles < h->num_sms ? tiles : h->num_sms);
     const bool prof = h->profiling && h->prof_used < kProfPairs;
     if (prof) LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used], st), "profile event");
-    lp::leaf_gemm_kernel<kFused, kStagesGemm>
-        <<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(kStagesGemm), st>>>(tmX, h->tmW, p);
+    // Stages of 128 K (8 MMAs per synchronisation) when the leaf length allows, else 64.
+    if (h->leaf_len % (2 * lp::kBK) == 0)
+        lp::leaf_gemm_kernel<kFused, 2>
+            <<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(2), st>>>(tmX, h->tmW, p);
+    else
+        lp::leaf_gemm_kernel<kFused, 1>
+            <<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(1), st>>>(tmX, h->tmW, p);
     LP_CUDA(cudaGetLastError(), "leaf_gemm_kernel launch");
     if (prof) {
         LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used + 1], st), "profile event");
@@ -384,12 +388,18 @@ int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out) 
     }
 
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<true, kStagesGemm>,
+    if ((e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<true, 1>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  lp::gemm_smem_bytes(kStagesGemm))) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<false, kStagesGemm>,
+                                  lp::gemm_smem_bytes(1))) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<false, 1>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  lp::gemm_smem_bytes(kStagesGemm))) != cudaSuccess)
+                                  lp::gemm_smem_bytes(1))) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<true, 2>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  lp::gemm_smem_bytes(2))) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<false, 2>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  lp::gemm_smem_bytes(2))) != cudaSuccess)
         return cleanup(cuda_fail(e, "cudaFuncSetAttribute(leaf_gemm_kernel)"));
     const int combine_smem = static_cast<int>(4 * sizeof(float2) * h->num_vocab_tiles);
     if (combine_smem > 48 * 1024) {
