@@ -356,13 +356,16 @@ def run_reference(args, world, rank):
     # row is H * V fp64 products whatever the row holds.
     W = inputs.lm_head(wl.V, wl.H, wl.seed)
     rng = np.random.default_rng(wl.seed)
-    probe_rows = 2
-    Xp = inputs.hidden_states(probe_rows, wl.H, wl.seed)
-    idsp = inputs.uniform_ids(probe_rows, wl.V, wl.seed)
+    threads = oracle.num_threads()
+    # calibrate on one row per thread (the oracle spreads rows over its OpenMP threads)
+    Xp = inputs.hidden_states(threads, wl.H, wl.seed)
+    idsp = inputs.uniform_ids(threads, wl.V, wl.seed)
+    oracle.logprobs(Xp[:1], W, idsp[:1].numpy())  # start the thread pool
     t0 = time.perf_counter()
     oracle.logprobs(Xp, W, idsp.numpy())
-    per_row = (time.perf_counter() - t0) / probe_rows
-    rows = int(max(1, min(T, round(args.ref_step_seconds / max(per_row, 1e-9)))))
+    per_round = time.perf_counter() - t0
+    rounds = max(1, round(args.ref_step_seconds / max(per_round, 1e-9)))
+    rows = int(min(T, rounds * threads))
     Xs = inputs.hidden_states(rows, wl.H, wl.seed + 1)
     idss = inputs.uniform_ids(rows, wl.V, wl.seed + 1).numpy()
     mus = rng.standard_normal(rows).astype(np.float32) - 5.0
