@@ -296,10 +296,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int y = p.ids[row];
                 if (y >= 0 && y < p.V) ycol = y - v0;
             }
-            // Leaf tree in post-order: the newest partial lives in registers (R), the one
-            // below it in TMEM slot S0; P_{n-2} waits in its buffer for P_{n-1}.
+            // Leaf tree: every even leaf waits in its TMEM buffer for its odd partner, the
+            // pair sum P_{2i} + P_{2i+1} is read from the two buffers, and the pair sums are
+            // combined in post-order (the newest partial in registers R, the one below it in
+            // TMEM slot S0) -- the same adds, in the same tree, as level-by-level pairing.
             float R[64];
             int depth = 0;
+            const int npairs = n >> 1;
             for (int jj = 0; jj < n; ++jj, ++g) {
                 const uint32_t buf = g % kAccBufs, use = g / kAccBufs;
                 if (!warp_wait(&acc_full[buf], use & 1u, p, abort_flag)) {
@@ -307,66 +310,54 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const bool last = (jj == n - 1);
-                if (!last && jj == n - 2) continue;
                 const uint32_t colB = buf * kVT;
-                if (!last) {
-                    if ((jj & 1) == 0) {
-                        // push P_jj (spilling the current top to S0)
-                        if (depth == 1) tmem_st64(lane_base + kColS0, R);
-                        tmem_ld64(lane_base + colB, R);
-                        ++depth;
-                    } else if (trailing_ones(jj) == 1) {
-                        // close the pair (P_{jj-1}, P_jj)
-#pragma unroll
-                        for (int cc = 0; cc < 2; ++cc) {
-                            float a[32];
-                            tmem_ld32(lane_base + colB + cc * 32, a);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) R[cc * 32 + i] = __fadd_rn(R[cc * 32 + i], a[i]);
-                        }
-                    } else {
-                        // close the pair, then the four-leaf subtree below it in S0
-#pragma unroll
-                        for (int cc = 0; cc < 2; ++cc) {
-                            float a[32], b[32];
-                            tmem_ld32x2(lane_base + colB + cc * 32, a, lane_base + kColS0 + cc * 32, b);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                R[cc * 32 + i] = __fadd_rn(b[i], __fadd_rn(R[cc * 32 + i], a[i]));
-                        }
-                        --depth;
-                    }
+                if (n == 1) {
+                    tmem_ld64(lane_base + colB, R);
                     release_buf(&acc_empty[buf]);
                     continue;
                 }
-                // last leaf of the range: finish the tree node into R
-                const uint32_t colPrev = ((g + kAccBufs - 1) % kAccBufs) * kVT;
+                if ((jj & 1) == 0) continue;  // wait for the partner leaf
+                const uint32_t pbuf = (g + kAccBufs - 1) % kAccBufs;
+                const uint32_t colP = pbuf * kVT;
+                const int i = jj >> 1;  // pair index
+                if ((i & 1) == 0 && i != npairs - 1) {
+                    // push the pair sum (spilling the current top to S0): R is free, so both
+                    // leaves load in one round trip
+                    if (depth == 1) tmem_st64(lane_base + kColS0, R);
+                    float b[64];
+                    tmem_ld64x2(lane_base + colP, R, lane_base + colB, b);
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    float a[32], b[32];
-                    if (n >= 2) {
-                        tmem_ld32x2(lane_base + colB + cc * 32, a, lane_base + colPrev + cc * 32, b);
+                    for (int k = 0; k < 64; ++k) R[k] = __fadd_rn(R[k], b[k]);
+                    ++depth;
+                } else if (npairs == 1) {
+                    // single pair: the node is P0 + P1
+                    float b[64];
+                    tmem_ld64x2(lane_base + colP, R, lane_base + colB, b);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) a[i] = __fadd_rn(b[i], a[i]);
-                    } else {
-                        tmem_ld32(lane_base + colB + cc * 32, a);
+                    for (int k = 0; k < 64; ++k) R[k] = __fadd_rn(R[k], b[k]);
+                } else {
+                    // odd pair index: close the subtrees that end at this pair
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        float a[32], b[32];
+                        tmem_ld32x2(lane_base + colP + cc * 32, a, lane_base + colB + cc * 32, b);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            R[cc * 32 + k] = __fadd_rn(R[cc * 32 + k], __fadd_rn(a[k], b[k]));
                     }
-                    if (depth >= 1) {
+                    if (trailing_ones(i) >= 2) {
+                        float b[64];
+                        tmem_ld64(lane_base + kColS0, b);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) a[i] = __fadd_rn(R[cc * 32 + i], a[i]);
+                        for (int k = 0; k < 64; ++k) R[k] = __fadd_rn(b[k], R[k]);
+                        --depth;
                     }
-                    if (depth == 2) {
-                        tmem_ld32(lane_base + kColS0 + cc * 32, b);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) a[i] = __fadd_rn(b[i], a[i]);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) R[cc * 32 + i] = a[i];
                 }
+                release_buf(&acc_empty[pbuf]);
                 release_buf(&acc_empty[buf]);
-                if (n >= 2) release_buf(&acc_empty[(g + kAccBufs - 1) % kAccBufs]);
-
+            }
+            if (!ok) break;
+            {
                 const int col0 = v0 + h * 64;
                 if (kFused) {
                     // per-tile log-sum-exp: this warp holds chunks 2h and 2h+1 of the row,

@@ -4,7 +4,7 @@
 // tensor-parallel split holds because every path applies exactly these
 // functions, in this order, to exactly the same fp32 values.  Every operation
 // is an explicit IEEE binary32 operation (__fadd_rn / __fsub_rn / __fmul_rn /
-// __fmaf_rn, fmaxf, and CUDA's expf / expm1f / logf), so no compiler
+// __fmaf_rn, fmaxf, and CUDA's __expf / expf / expm1f / logf), so no compiler
 // contraction can differ between kernels.
 #pragma once
 
@@ -52,13 +52,15 @@ __device__ __forceinline__ float chunk_max(const float (&v)[32], int nvalid) {
 }
 
 // Sum of exp(z - m) over the chunk's valid columns (pairwise tree); captures the logit in
-// column `ycol` (chunk-relative) into zy.  Destroys v.
+// column `ycol` (chunk-relative) into zy.  Destroys v.  The exponential is CUDA's __expf
+// intrinsic (argument <= 0 here; a few units in the last place, far inside the logprob
+// tolerance), used identically by every kernel that forms a tile partial.
 __device__ __forceinline__ float chunk_expsum(float (&v)[32], int nvalid, float m, int ycol,
                                               float& zy) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         if (i == ycol) zy = v[i];
-        v[i] = (i < nvalid) ? expf(__fsub_rn(v[i], m)) : 0.0f;
+        v[i] = (i < nvalid) ? __expf(__fsub_rn(v[i], m)) : 0.0f;
     }
     return tree_sum32(v);
 }
