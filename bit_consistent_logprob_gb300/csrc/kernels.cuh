@@ -161,118 +161,123 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int nkb = p.leaf_len / (kBK * kSub);   // stages per leaf
     const int n = p.leaf_count;
 
+    constexpr uint32_t kFull = 0xffffffffu;
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            const uint32_t tx_bytes =
-                static_cast<uint32_t>(kSub * (p.x_box_rows * kBK * 2 + kTileBytes));
-            uint32_t stage = 0, phase = 0;
-            uint64_t issued = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                int rt, vt;
-                tile_coords(tile, p, rt, vt);
-                const int row0 = rt * kBM, v0 = vt * kVT;
-                for (int jj = 0; ok && jj < n; ++jj) {
-                    const int kbase = (p.leaf_begin + jj) * p.leaf_len;
-                    for (int kb = 0; kb < nkb; ++kb) {
-                        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns)) {
-                            raise_timeout(p, abort_flag);
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&full[stage], tx_bytes);
-#pragma unroll
-                        for (int u = 0; u < kSub; ++u) {
-                            const int k0 = kbase + (kb * kSub + u) * kBK;
-                            tma_load_2d(&tmX, &full[stage], sA + stage * kStageBytes + u * kTileBytes,
-                                        k0, row0);
-                            tma_load_2d(&tmW, &full[stage], sB + stage * kStageBytes + u * kTileBytes,
-                                        k0, v0);
-                        }
-                        ++issued;
-                        if (++stage == kStages) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
+        // ------------------------------------------------------------ TMA producer (warp)
+        const uint32_t tx_bytes =
+            static_cast<uint32_t>(kSub * (p.x_box_rows * kBK * 2 + kTileBytes));
+        uint32_t stage = 0, phase = 0;
+        uint64_t issued = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            int rt, vt;
+            tile_coords(tile, p, rt, vt);
+            const int row0 = rt * kBM, v0 = vt * kVT;
+            for (int jj = 0; ok && jj < n; ++jj) {
+                const int kbase = (p.leaf_begin + jj) * p.leaf_len;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    ok = __all_sync(kFull,
+                                    mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns));
+                    if (!ok) {
+                        if (lane == 0) raise_timeout(p, abort_flag);
+                        break;
                     }
-                }
-            }
-            if (!ok) {
-                // Let the copies already in flight land before the CTA exits.
-                const uint64_t first = issued > kStages ? issued - kStages : 0;
-                for (uint64_t i = first; i < issued; ++i) {
-                    volatile int never = 0;
-                    mbar_wait(&full[i % kStages], static_cast<uint32_t>((i / kStages) & 1u),
-                              &never, p.timeout_ns);
+                    mbar_arrive_expect_tx_elect(&full[stage], tx_bytes);
+#pragma unroll
+                    for (int u = 0; u < kSub; ++u) {
+                        const int k0 = kbase + (kb * kSub + u) * kBK;
+                        tma_load_2d_elect(&tmX, &full[stage],
+                                          sA + stage * kStageBytes + u * kTileBytes, k0, row0);
+                        tma_load_2d_elect(&tmW, &full[stage],
+                                          sB + stage * kStageBytes + u * kTileBytes, k0, v0);
+                    }
+                    ++issued;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
         }
+        if (!ok) {
+            // Let the copies already in flight land before the CTA exits.
+            const uint64_t first = issued > kStages ? issued - kStages : 0;
+            for (uint64_t i = first; i < issued; ++i) {
+                volatile int never = 0;
+                mbar_wait(&full[i % kStages], static_cast<uint32_t>((i / kStages) & 1u), &never,
+                          p.timeout_ns);
+            }
+        }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // The tensor core's instruction queue is shallow, so this thread does as little as
-        // possible between MMAs: descriptors are precomputed, buffer/stage indices advance
-        // incrementally, and the barriers of the next stage and the next leaf's buffer are
-        // probed (non-blocking) before the current stage's MMAs are issued.
-        if (lane == 0) {
-            const uint64_t descA = sw128_kmajor_desc(smem_u32(sA));
-            const uint64_t descB = sw128_kmajor_desc(smem_u32(sB));
-            constexpr uint32_t kStageDesc = kStageBytes >> 4;  // descriptor units per stage
-            constexpr uint32_t kSubDesc = kTileBytes >> 4;     // ... per 64-K sub-block
-            uint32_t stage = 0, phase = 0;
-            uint32_t buf = 0, bphase = 0;  // TMEM buffer of the current leaf, its use parity
-            bool ok = true;
-            bool ready = mbar_test_wait(&full[0], 0);
-            bool acc_ready = true;  // the first uses of every buffer find it free
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                for (int jj = 0; ok && jj < n; ++jj) {
-                    if (!acc_ready &&
-                        !mbar_wait(&acc_empty[buf], bphase ^ 1u, abort_flag, p.timeout_ns)) {
-                        raise_timeout(p, abort_flag);
-                        ok = false;
+        // ------------------------------------------------------------ MMA issuer (warp)
+        // The tensor core's instruction queue is shallow, so the issuing loop does as little
+        // as possible between MMAs: descriptors are precomputed, buffer/stage indices advance
+        // incrementally, every value is warp-uniform, and the barriers of the next stage and
+        // of the next leaf's buffer are probed (non-blocking) before this stage's MMAs issue.
+        const uint64_t descA = sw128_kmajor_desc(smem_u32(sA));
+        const uint64_t descB = sw128_kmajor_desc(smem_u32(sB));
+        constexpr uint32_t kStageDesc = kStageBytes >> 4;  // descriptor units per stage
+        constexpr uint32_t kSubDesc = kTileBytes >> 4;     // ... per 64-K sub-block
+        uint32_t stage = 0, phase = 0;
+        uint32_t buf = 0, bphase = 0;  // TMEM buffer of the current leaf, its use parity
+        bool ok = true;
+        bool ready = __all_sync(kFull, mbar_test_wait(&full[0], 0));
+        bool acc_ready = true;  // the first uses of every buffer find it free
+        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int jj = 0; ok && jj < n; ++jj) {
+                if (!acc_ready) {
+                    ok = __all_sync(kFull, mbar_wait(&acc_empty[buf], bphase ^ 1u, abort_flag,
+                                                     p.timeout_ns));
+                    if (!ok) {
+                        if (lane == 0) raise_timeout(p, abort_flag);
                         break;
                     }
-                    tc_fence_after_sync();
-                    const uint32_t d_tmem = tmem_base + (buf << 7);
-                    const uint32_t nbuf = buf + 1 == kAccBufs ? 0u : buf + 1;
-                    const uint32_t nbphase = buf + 1 == kAccBufs ? bphase ^ 1u : bphase;
-                    for (int kb = 0; kb < nkb; ++kb) {
-                        if (!ready && !mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns)) {
-                            raise_timeout(p, abort_flag);
-                            ok = false;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + (buf << 7);
+                const uint32_t nbuf = buf + 1 == kAccBufs ? 0u : buf + 1;
+                const uint32_t nbphase = buf + 1 == kAccBufs ? bphase ^ 1u : bphase;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!ready) {
+                        ok = __all_sync(kFull,
+                                        mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns));
+                        if (!ok) {
+                            if (lane == 0) raise_timeout(p, abort_flag);
                             break;
                         }
-                        tc_fence_after_sync();
-                        const uint32_t nstage = stage + 1 == kStages ? 0u : stage + 1;
-                        const uint32_t nphase = stage + 1 == kStages ? phase ^ 1u : phase;
-                        ready = mbar_test_wait(&full[nstage], nphase);
-                        if (kb == nkb - 1) acc_ready = mbar_test_wait(&acc_empty[nbuf], nbphase ^ 1u);
-                        const uint64_t a = descA + stage * kStageDesc;
-                        const uint64_t b = descB + stage * kStageDesc;
-                        // +32 bytes (2 descriptor units) per K step of 16 bf16 inside a row;
-                        // only the leaf's very first MMA starts a fresh accumulator
-                        umma_bf16(d_tmem, a, b, kIdesc, kb != 0 ? 1u : 0u);
-#pragma unroll
-                        for (int i = 1; i < kSub * (kBK / 16); ++i) {
-                            const uint32_t off = (i >> 2) * kSubDesc + 2u * (i & 3);
-                            umma_bf16(d_tmem, a + off, b + off, kIdesc, 1u);
-                        }
-                        umma_commit(&empty[stage]);
-                        stage = nstage;
-                        phase = nphase;
                     }
-                    if (!ok) break;
-                    umma_commit(&acc_full[buf]);
-                    buf = nbuf;
-                    bphase = nbphase;
+                    tc_fence_after_sync();
+                    const uint32_t nstage = stage + 1 == kStages ? 0u : stage + 1;
+                    const uint32_t nphase = stage + 1 == kStages ? phase ^ 1u : phase;
+                    ready = __all_sync(kFull, mbar_test_wait(&full[nstage], nphase));
+                    if (kb == nkb - 1)
+                        acc_ready =
+                            __all_sync(kFull, mbar_test_wait(&acc_empty[nbuf], nbphase ^ 1u));
+                    const uint64_t a = descA + stage * kStageDesc;
+                    const uint64_t b = descB + stage * kStageDesc;
+                    // +32 bytes (2 descriptor units) per K step of 16 bf16 inside a row;
+                    // only the leaf's very first MMA starts a fresh accumulator
+                    umma_bf16_elect(d_tmem, a, b, kIdesc, kb != 0 ? 1u : 0u);
+#pragma unroll
+                    for (int i = 1; i < kSub * (kBK / 16); ++i) {
+                        const uint32_t off = (i >> 2) * kSubDesc + 2u * (i & 3);
+                        umma_bf16_elect(d_tmem, a + off, b + off, kIdesc, 1u);
+                    }
+                    umma_commit_elect(&empty[stage]);
+                    stage = nstage;
+                    phase = nphase;
                 }
+                if (!ok) break;
+                umma_commit_elect(&acc_full[buf]);
+                buf = nbuf;
+                bphase = nbphase;
             }
-            if (!ok) {
-                // Wait for every MMA already issued before TMEM is released.
-                volatile int never = 0;
-                umma_commit(drain);
-                mbar_wait(drain, 0, &never, p.timeout_ns);
-            }
+        }
+        if (!ok) {
+            // Wait for every MMA already issued before TMEM is released.
+            volatile int never = 0;
+            umma_commit_elect(drain);
+            mbar_wait(drain, 0, &never, p.timeout_ns);
         }
     } else {
         // ------------------------------------------------------------ epilogue (8 warps)
