@@ -81,6 +81,22 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& 
     vt = vt0 + (r - rt * width);
 }
 
+// Cluster of two CTAs: they take vocabulary-adjacent tiles (2*vp, 2*vp + 1) of one row tile
+// and share its X tile.  Cluster tiles follow the same band schedule with bands of band/2
+// vocabulary pairs.  A CTA whose tile lies past the vocabulary still loads and computes
+// (its partner needs its half of X) but writes nothing.
+__device__ __forceinline__ void pair_tile_coords(int ct, const GemmParams& p, int num_pairs,
+                                                 uint32_t rank, int& rt, int& vt) {
+    const int band = p.band >> 1;
+    const int per_band = p.num_row_tiles * band;
+    const int b = ct / per_band;
+    const int r = ct - b * per_band;
+    const int vp0 = b * band;
+    const int width = min(band, num_pairs - vp0);
+    rt = r / width;
+    vt = 2 * (vp0 + (r - rt * width)) + static_cast<int>(rank);
+}
+
 __device__ __forceinline__ void raise_timeout(const GemmParams& p, volatile int* abort_flag) {
     *abort_flag = 1;
     atomicOr(p.status, kStatusTimeout);
@@ -105,7 +121,10 @@ __device__ __forceinline__ void release_buf(uint64_t* bar) {
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
-template <bool kFused, int kSub>
+// kCluster = 1: one CTA per tile.  kCluster = 2: clusters of two CTAs share the X tile of
+// vocabulary-adjacent tiles; each CTA loads 64 of its 128 rows and multicasts them to both
+// (tmX then has 64-row boxes).  The per-element arithmetic is identical in both modes.
+template <bool kFused, int kSub, int kCluster>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     leaf_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmW, const GemmParams p) {
@@ -130,10 +149,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    const uint32_t crank = kCluster == 2 ? cluster_ctarank() : 0u;
+    constexpr uint16_t kPairMask = 0x3;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], kCluster);  // one MMA commit from each CTA that reads the stage
         }
         for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -154,24 +175,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
+    if (kCluster == 2) cluster_sync_all();  // the partner's barriers exist before any multicast
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
 
-    const int num_tiles = p.num_row_tiles * p.num_vocab_tiles;
+    const int num_pairs = (p.num_vocab_tiles + 1) >> 1;
+    const int num_tiles =
+        kCluster == 2 ? p.num_row_tiles * num_pairs : p.num_row_tiles * p.num_vocab_tiles;
+    const int tile0 = kCluster == 2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int tile_step = kCluster == 2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
     const int nkb = p.leaf_len / (kBK * kSub);   // stages per leaf
     const int n = p.leaf_count;
 
     constexpr uint32_t kFull = 0xffffffffu;
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer (warp)
-        const uint32_t tx_bytes =
-            static_cast<uint32_t>(kSub * (p.x_box_rows * kBK * 2 + kTileBytes));
+        const uint32_t tx_bytes = static_cast<uint32_t>(
+            kSub * ((kCluster == 2 ? kBM : p.x_box_rows) * kBK * 2 + kTileBytes));
         uint32_t stage = 0, phase = 0;
         uint64_t issued = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
             int rt, vt;
-            tile_coords(tile, p, rt, vt);
+            if (kCluster == 2)
+                pair_tile_coords(tile, p, num_pairs, crank, rt, vt);
+            else
+                tile_coords(tile, p, rt, vt);
             const int row0 = rt * kBM, v0 = vt * kVT;
             for (int jj = 0; ok && jj < n; ++jj) {
                 const int kbase = (p.leaf_begin + jj) * p.leaf_len;
@@ -186,8 +215,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                     for (int u = 0; u < kSub; ++u) {
                         const int k0 = kbase + (kb * kSub + u) * kBK;
-                        tma_load_2d_elect(&tmX, &full[stage],
-                                          sA + stage * kStageBytes + u * kTileBytes, k0, row0);
+                        uint8_t* xdst = sA + stage * kStageBytes + u * kTileBytes;
+                        if (kCluster == 2)  // my 64 rows of the shared X tile, to both CTAs
+                            tma_load_2d_mc_elect(&tmX, &full[stage], xdst + crank * (kTileBytes / 2),
+                                                 k0, row0 + static_cast<int>(crank) * (kBM / 2),
+                                                 kPairMask);
+                        else
+                            tma_load_2d_elect(&tmX, &full[stage], xdst, k0, row0);
                         tma_load_2d_elect(&tmW, &full[stage],
                                           sB + stage * kStageBytes + u * kTileBytes, k0, v0);
                     }
@@ -223,7 +257,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         bool ok = true;
         bool ready = __all_sync(kFull, mbar_test_wait(&full[0], 0));
         bool acc_ready = true;  // the first uses of every buffer find it free
-        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
             for (int jj = 0; ok && jj < n; ++jj) {
                 if (!acc_ready) {
                     ok = __all_sync(kFull, mbar_wait(&acc_empty[buf], bphase ^ 1u, abort_flag,
@@ -263,7 +297,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const uint32_t off = (i >> 2) * kSubDesc + 2u * (i & 3);
                         umma_bf16_elect(d_tmem, a + off, b + off, kIdesc, 1u);
                     }
-                    umma_commit_elect(&empty[stage]);
+                    if (kCluster == 2)
+                        umma_commit_mc_elect(&empty[stage], kPairMask);  // both CTAs' stage freed
+                    else
+                        umma_commit_elect(&empty[stage]);
                     stage = nstage;
                     phase = nphase;
                 }
@@ -290,9 +327,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * 64);
         uint32_t g = 0, xphase = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
             int rt, vt;
-            tile_coords(tile, p, rt, vt);
+            if (kCluster == 2)
+                pair_tile_coords(tile, p, num_pairs, crank, rt, vt);
+            else
+                tile_coords(tile, p, rt, vt);
             const int row = rt * kBM + r_in_tile;
             const int v0 = vt * kVT;
             const bool row_ok = row < p.T;
@@ -419,6 +459,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ---------------------------------------------------------------- teardown
     tc_fence_before_sync();
     __syncthreads();
+    if (kCluster == 2) cluster_sync_all();  // no multicast or commit still targets this CTA
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, kTmemCols);

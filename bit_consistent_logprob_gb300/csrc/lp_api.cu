@@ -118,6 +118,11 @@ struct lp_handle {
     cudaStream_t last_stream = nullptr;
     int64_t ws_bytes = 0;
     int32_t last_launches = 0;
+    // launch-layout switches read from the environment at init (LP_FORCE_SINGLE_CTA,
+    // LP_FORCE_SHORT_STAGES); they change only the schedule, never the arithmetic, and let
+    // the tests prove that
+    bool force_single_cta = false;
+    bool force_sub1 = false;
     // profiling: event pairs around leaf-GEMM launches
     bool profiling = false;
     std::vector<cudaEvent_t> prof_events;  // 2 * kProfPairs, created on enable
@@ -149,8 +154,47 @@ uint32_t x_box_rows(int rows) {
     return rows >= lp::kBM ? lp::kBM : static_cast<uint32_t>((rows + 7) / 8 * 8);
 }
 
+template <bool kFused, int kSub, int kCluster>
+cudaError_t launch_gemm_variant(int grid, cudaStream_t st, const CUtensorMap& tmX,
+                                const CUtensorMap& tmW, const lp::GemmParams& p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(lp::kGemmThreads);
+    cfg.dynamicSmemBytes = lp::gemm_smem_bytes(kSub);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    if (kCluster > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kCluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, lp::leaf_gemm_kernel<kFused, kSub, kCluster>, tmX, tmW, p);
+}
+
 template <bool kFused>
-int launch_leaf_gemm(lp_handle* h, const CUtensorMap& tmX, int rows, int leaf_begin,
+int set_gemm_attributes() {
+    const auto set = [](auto fn, int sub) {
+        return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    lp::gemm_smem_bytes(sub));
+    };
+    cudaError_t e;
+    if ((e = set(lp::leaf_gemm_kernel<kFused, 1, 1>, 1)) != cudaSuccess ||
+        (e = set(lp::leaf_gemm_kernel<kFused, 2, 1>, 2)) != cudaSuccess ||
+        (e = set(lp::leaf_gemm_kernel<kFused, 1, 2>, 1)) != cudaSuccess ||
+        (e = set(lp::leaf_gemm_kernel<kFused, 2, 2>, 2)) != cudaSuccess)
+        return cuda_fail(e, "cudaFuncSetAttribute(leaf_gemm_kernel)");
+    return LP_OK;
+}
+
+// The leaf GEMM over `rows` rows of X starting at `X` (row stride ldx).  Calls with at least
+// one full 128-row tile run in clusters of two CTAs that share each X tile (multicast);
+// smaller (decode) calls run one CTA per tile with an X box cut to their rows.  Stages are
+// 128 K deep (8 MMAs per barrier synchronisation) when the leaf length allows, else 64.
+template <bool kFused>
+int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int leaf_begin,
                      int leaf_count, const int32_t* ids, float* out, int64_t ldo,
                      cudaStream_t st) {
     lp::GemmParams p{};
@@ -162,7 +206,6 @@ int launch_leaf_gemm(lp_handle* h, const CUtensorMap& tmX, int rows, int leaf_be
     p.num_row_tiles = static_cast<int32_t>(ceil_div(rows, lp::kBM));
     p.num_vocab_tiles = h->num_vocab_tiles;
     p.band = kBand;
-    p.x_box_rows = static_cast<int32_t>(x_box_rows(rows));
     p.ids = ids;
     p.ws_ms = h->ws_ms;
     p.ws_ld = h->cfg.max_tokens;
@@ -171,18 +214,28 @@ int launch_leaf_gemm(lp_handle* h, const CUtensorMap& tmX, int rows, int leaf_be
     p.ldo = ldo;
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
-    const int64_t tiles = static_cast<int64_t>(p.num_row_tiles) * p.num_vocab_tiles;
+    const bool cluster = rows >= lp::kBM && h->num_vocab_tiles >= 2 && !h->force_single_cta;
+    p.x_box_rows = static_cast<int32_t>(cluster ? lp::kBM / 2 : x_box_rows(rows));
+    CUtensorMap tmX;
+    int rc = encode_kmajor(&tmX, X, static_cast<uint64_t>(rows), h->cfg.H, ldx,
+                           static_cast<uint32_t>(p.x_box_rows));
+    if (rc != LP_OK) return rc;
+    const int64_t pairs = ceil_div(h->num_vocab_tiles, 2);
+    const int64_t tiles = static_cast<int64_t>(p.num_row_tiles) * (cluster ? pairs : h->num_vocab_tiles);
     if (tiles > 0x7fffffff) return fail(LP_ERR_UNSUPPORTED, "too many tiles in one launch");
-    const int grid = static_cast<int>(tiles < h->num_sms ? tiles : h->num_sms);
+    const int64_t slots = cluster ? h->num_sms / 2 : h->num_sms;
+    const int grid = static_cast<int>((tiles < slots ? tiles : slots) * (cluster ? 2 : 1));
+    const bool sub2 = h->leaf_len % (2 * lp::kBK) == 0 && !h->force_sub1;
     const bool prof = h->profiling && h->prof_used < kProfPairs;
     if (prof) LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used], st), "profile event");
-    // Stages of 128 K (8 MMAs per synchronisation) when the leaf length allows, else 64.
-    if (h->leaf_len % (2 * lp::kBK) == 0)
-        lp::leaf_gemm_kernel<kFused, 2>
-            <<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(2), st>>>(tmX, h->tmW, p);
+    cudaError_t e;
+    if (cluster)
+        e = sub2 ? launch_gemm_variant<kFused, 2, 2>(grid, st, tmX, h->tmW, p)
+                 : launch_gemm_variant<kFused, 1, 2>(grid, st, tmX, h->tmW, p);
     else
-        lp::leaf_gemm_kernel<kFused, 1>
-            <<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(1), st>>>(tmX, h->tmW, p);
+        e = sub2 ? launch_gemm_variant<kFused, 2, 1>(grid, st, tmX, h->tmW, p)
+                 : launch_gemm_variant<kFused, 1, 1>(grid, st, tmX, h->tmW, p);
+    LP_CUDA(e, "leaf_gemm_kernel launch");
     LP_CUDA(cudaGetLastError(), "leaf_gemm_kernel launch");
     if (prof) {
         LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used + 1], st), "profile event");
@@ -240,12 +293,10 @@ int launch_partials_lse(lp_handle* h, const float* parts, int n_parts, int64_t p
 // Fused path or emulated tensor-parallel path for one chunk of rows (rows <= max_tokens).
 int logprobs_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int rows,
                    float* out_logp, float* out_logZ, cudaStream_t st) {
-    CUtensorMap tmX;
-    int rc = encode_kmajor(&tmX, X, static_cast<uint64_t>(rows), h->cfg.H, ldx, x_box_rows(rows));
-    if (rc != LP_OK) return rc;
+    int rc;
     const int s = h->cfg.tp_slices;
     if (s == 1) {
-        rc = launch_leaf_gemm<true>(h, tmX, rows, 0, h->cfg.n_leaves, ids, nullptr, 0, st);
+        rc = launch_leaf_gemm<true>(h, X, ldx, rows, 0, h->cfg.n_leaves, ids, nullptr, 0, st);
         if (rc != LP_OK) return rc;
     } else {
         // Slice r owns leaves [r*N/s, (r+1)*N/s) and produces that node of the leaf tree;
@@ -254,7 +305,7 @@ int logprobs_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids,
         const int per = h->cfg.n_leaves / s;
         const int64_t part_stride = h->chunk_rows * h->tp_ldp;
         for (int r = 0; r < s; ++r) {
-            rc = launch_leaf_gemm<false>(h, tmX, rows, r * per, per, nullptr,
+            rc = launch_leaf_gemm<false>(h, X, ldx, rows, r * per, per, nullptr,
                                          h->tp_parts + r * part_stride, h->tp_ldp, st);
             if (rc != LP_OK) return rc;
         }
@@ -343,6 +394,8 @@ int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out) 
         if (v > 0) timeout_ms = static_cast<uint64_t>(v);
     }
     h->timeout_ns = timeout_ms * 1000000ull;
+    if (const char* e = std::getenv("LP_FORCE_SINGLE_CTA")) h->force_single_cta = e[0] == '1';
+    if (const char* e = std::getenv("LP_FORCE_SHORT_STAGES")) h->force_sub1 = e[0] == '1';
 
     auto cleanup = [&](int code) {
         lp_free(h);
@@ -387,20 +440,9 @@ int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out) 
             return cleanup(rc);
     }
 
+    if ((rc = set_gemm_attributes<true>()) != LP_OK || (rc = set_gemm_attributes<false>()) != LP_OK)
+        return cleanup(rc);
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<true, 1>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  lp::gemm_smem_bytes(1))) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<false, 1>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  lp::gemm_smem_bytes(1))) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<true, 2>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  lp::gemm_smem_bytes(2))) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<false, 2>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  lp::gemm_smem_bytes(2))) != cudaSuccess)
-        return cleanup(cuda_fail(e, "cudaFuncSetAttribute(leaf_gemm_kernel)"));
     const int combine_smem = static_cast<int>(4 * sizeof(float2) * h->num_vocab_tiles);
     if (combine_smem > 48 * 1024) {
         if (combine_smem > 227 * 1024) return cleanup(fail(LP_ERR_UNSUPPORTED, "V too large"));
@@ -504,12 +546,8 @@ int lp_logits_partial(lp_handle* h, const void* X, int64_t ldx, int64_t T, int32
     const uint8_t* xb = static_cast<const uint8_t*>(X);
     for (int64_t r0 = 0; r0 < T; r0 += chunk) {
         const int rows = static_cast<int>(T - r0 < chunk ? T - r0 : chunk);
-        CUtensorMap tmX;
-        rc = encode_kmajor(&tmX, xb + r0 * ldx * 2, static_cast<uint64_t>(rows), h->cfg.H, ldx,
-                           x_box_rows(rows));
-        if (rc != LP_OK) return rc;
-        rc = launch_leaf_gemm<false>(h, tmX, rows, leaf_begin, leaf_count, nullptr,
-                                     out + r0 * ldo, ldo, st);
+        rc = launch_leaf_gemm<false>(h, xb + r0 * ldx * 2, ldx, rows, leaf_begin, leaf_count,
+                                     nullptr, out + r0 * ldo, ldo, st);
         if (rc != LP_OK) return rc;
     }
     return LP_OK;

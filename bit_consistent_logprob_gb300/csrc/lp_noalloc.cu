@@ -79,11 +79,11 @@ void setup_device(int dev, DeviceSetup& s) {
     if (e == cudaSuccess) e = cudaGetSymbolAddress(&ptr, g_lp_noalloc_scratch);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<true, 1>,
+        e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<true, 1, 1>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  lp::gemm_smem_bytes(1));
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<true, 2>,
+        e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<true, 2, 1>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  lp::gemm_smem_bytes(2));
     if (e == cudaSuccess)
@@ -205,9 +205,9 @@ LP_API int lp_logprobs_noalloc(const void* W, int32_t H, int32_t V, int32_t n_le
     const int64_t tiles = static_cast<int64_t>(p.num_row_tiles) * nb;
     const int grid = static_cast<int>(tiles < s.num_sms ? tiles : s.num_sms);
     if (p.leaf_len % (2 * lp::kBK) == 0)
-        lp::leaf_gemm_kernel<true, 2><<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(2), st>>>(tmX, tmW, p);
+        lp::leaf_gemm_kernel<true, 2, 1><<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(2), st>>>(tmX, tmW, p);
     else
-        lp::leaf_gemm_kernel<true, 1><<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(1), st>>>(tmX, tmW, p);
+        lp::leaf_gemm_kernel<true, 1, 1><<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(1), st>>>(tmX, tmW, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return nfail(LP_ERR_CUDA, "leaf_gemm_kernel launch: %s", cudaGetErrorString(e));
 

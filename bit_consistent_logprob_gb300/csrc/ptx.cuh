@@ -146,6 +146,45 @@ __device__ __forceinline__ void tma_load_2d_elect(const CUtensorMap* map, uint64
         : "memory");
 }
 
+// Multicast variant: the box lands at the same shared-memory offset in every CTA of
+// `cta_mask` (this GPU's cluster), and each destination CTA's barrier at the same offset
+// receives the transaction bytes.
+__device__ __forceinline__ void tma_load_2d_mc_elect(const CUtensorMap* map, uint64_t* bar,
+                                                     void* dst, int32_t x, int32_t y,
+                                                     uint16_t cta_mask) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;\n\t}" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask)
+        : "memory");
+}
+
+// Arrive on the barrier at the same offset in every CTA of `cta_mask` when this thread's
+// tcgen05 operations so far complete.
+__device__ __forceinline__ void umma_commit_mc_elect(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster"
+        ".b64 [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA in the cluster arrives, then waits for all of them.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
 __device__ __forceinline__ void umma_bf16_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                 uint32_t idesc, uint32_t accumulate) {
     asm volatile(

@@ -237,3 +237,18 @@ def test_importance_weights_invariance(eng, dev):
         _, d3b, _ = eng.importance_weights(lp, lm, mask)
         assert d3b.item() == d3.item()
     eng.check()
+
+
+@pytest.mark.parametrize("env", ["LP_FORCE_SINGLE_CTA", "LP_FORCE_SHORT_STAGES"])
+def test_launch_layout_changes_no_bits(data, eng, env, monkeypatch):
+    # Two-CTA clusters sharing X versus one CTA per tile, and 128-K versus 64-K pipeline
+    # stages, change only how data moves and who computes a tile.
+    X, W, ids = data
+    T = 3000
+    base, baseZ = eng.logprobs(X[:T], ids[:T], return_logZ=True)
+    monkeypatch.setenv(env, "1")
+    with Engine(W, n_leaves=N, max_tokens=T) as e2:
+        other, otherZ = e2.logprobs(X[:T], ids[:T], return_logZ=True)
+        e2.check()
+    assert_bit_equal(other, base, env)
+    assert_bit_equal(otherZ, baseZ, env)
