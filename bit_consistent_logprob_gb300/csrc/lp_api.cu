@@ -20,7 +20,6 @@
 
 namespace {
 
-constexpr int kBand = 32;                       // vocabulary tiles per scheduling band
 constexpr int64_t kMaxIsTokens = (1LL << 31) - 1;
 constexpr int64_t kTpRows = 1024;               // rows per pass of the emulated TP path
 constexpr int kProfPairs = 4096;
@@ -123,6 +122,7 @@ struct lp_handle {
     // the tests prove that
     bool force_single_cta = false;
     bool force_sub1 = false;
+    int band = 0;  // vocabulary tiles per scheduling band (even); schedule only
     // profiling: event pairs around leaf-GEMM launches
     bool profiling = false;
     std::vector<cudaEvent_t> prof_events;  // 2 * kProfPairs, created on enable
@@ -205,7 +205,7 @@ int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int lea
     p.leaf_count = leaf_count;
     p.num_row_tiles = static_cast<int32_t>(ceil_div(rows, lp::kBM));
     p.num_vocab_tiles = h->num_vocab_tiles;
-    p.band = kBand;
+    p.band = h->band;
     p.ids = ids;
     p.ws_ms = h->ws_ms;
     p.ws_ld = h->cfg.max_tokens;
@@ -396,6 +396,19 @@ int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out) 
     h->timeout_ns = timeout_ms * 1000000ull;
     if (const char* e = std::getenv("LP_FORCE_SINGLE_CTA")) h->force_single_cta = e[0] == '1';
     if (const char* e = std::getenv("LP_FORCE_SHORT_STAGES")) h->force_sub1 = e[0] == '1';
+    // Scheduling band: enough vocabulary tiles for ~28 MiB of W, which stays L2-resident
+    // while every row tile of the batch sweeps across it (measured best on GB300: 16 tiles
+    // at H = 7168, 32-48 at H = 2048).  The band decides which CTA computes a tile, never how.
+    {
+        const int64_t per_tile = static_cast<int64_t>(lp::kVT) * cfg->H * 2;
+        int64_t b = (int64_t(28) << 20) / per_tile;
+        b = b < 8 ? 8 : (b > 64 ? 64 : b);
+        h->band = static_cast<int>(b) & ~1;
+    }
+    if (const char* e = std::getenv("LP_BAND")) {
+        const int b = std::atoi(e);
+        if (b >= 2 && b <= 1024) h->band = b & ~1;
+    }
 
     auto cleanup = [&](int code) {
         lp_free(h);
