@@ -42,10 +42,11 @@ struct GemmParams {
     int32_t leaf_count;       // leaves in the range: 1, 2, 4 or 8
     int32_t num_row_tiles;    // ceil(T / 128)
     int32_t num_vocab_tiles;  // ceil(V / 128)
+    int32_t num_lse_tiles;    // ceil(V / 64)
     int32_t band;             // vocabulary tiles per scheduling band
     int32_t x_box_rows;       // rows per X TMA box (128, or T rounded up to 8 when T < 128)
     const int32_t* ids;       // [T] sampled ids (fused path)
-    float2* ws_ms;            // [num_vocab_tiles][ws_ld] (max, sum-exp) per tile (fused path)
+    float2* ws_ms;            // [num_lse_tiles][ws_ld] (max, sum-exp) per 64-column tile (fused)
     int64_t ws_ld;
     float* zy;                // [T] sampled logit (fused path)
     float* out;               // [T][ldo] tree node (partial path)
@@ -54,7 +55,7 @@ struct GemmParams {
     uint64_t timeout_ns;      // bound on every mbarrier wait
 };
 
-__host__ __device__ constexpr int kNumBars(int stages) { return 2 * stages + 2 * kAccBufs + 1 + 4; }
+__host__ __device__ constexpr int kNumBars(int stages) { return 2 * stages + 2 * kAccBufs + 1; }
 
 // A pipeline stage holds kSub 64-wide K sub-blocks of X and of W (4 MMAs of K = 16 per
 // sub-block).  More MMAs per stage means fewer barrier synchronisations per MMA in the
@@ -63,8 +64,7 @@ __host__ __device__ constexpr int gemm_stages(int sub) { return 6 / sub; }
 
 __host__ __device__ constexpr int gemm_smem_bytes(int sub) {
     return 1024 /* alignment slack */ + gemm_stages(sub) * sub * 2 * kTileBytes +
-           kNumBars(gemm_stages(sub)) * 8 + 16 /* TMEM address, abort flag */ +
-           2 * 2 * kBM * 4 /* pair exchange */;
+           kNumBars(gemm_stages(sub)) * 8 + 16 /* TMEM address, abort flag */;
 }
 
 // Tile schedule: the vocabulary is cut into bands of `band` tiles; within a band the
@@ -141,10 +141,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* acc_full = bars + 2 * kStages;             // MMA -> epilogue, per TMEM buffer
     uint64_t* acc_empty = acc_full + kAccBufs;           // epilogue -> MMA, per TMEM buffer
     uint64_t* drain = acc_empty + kAccBufs;              // MMA drain on abort
-    uint64_t* xbar = drain + 1;                          // epilogue pair exchange, per quarter
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(xbar + 4);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-    float* xch = reinterpret_cast<float*>(tmem_holder + 4);  // [2 kinds][2 halves][128 rows]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -161,7 +159,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&acc_empty[b], kEpiWarps);  // every epilogue warp reads every buffer
         }
         mbar_init(drain, 1);
-        for (int q = 0; q < 4; ++q) mbar_init(&xbar[q], 2);  // the two warps of a lane quarter
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -325,7 +322,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int r_in_tile = q * 32 + lane;
         const uint32_t lane_base =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * 64);
-        uint32_t g = 0, xphase = 0;
+        uint32_t g = 0;
         bool ok = true;
         for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
             int rt, vt;
@@ -405,39 +402,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             {
                 const int col0 = v0 + h * 64;
                 if (kFused) {
-                    // per-tile log-sum-exp: this warp holds chunks 2h and 2h+1 of the row,
-                    // its partner (same lane quarter) the other two
-                    float(&R0)[32] = *reinterpret_cast<float(*)[32]>(&R[0]);
-                    float(&R1)[32] = *reinterpret_cast<float(*)[32]>(&R[32]);
-                    const int nv = min(kVT, p.V - v0) - h * 64;
-                    xch[h * kBM + r_in_tile] = fmaxf(chunk_max(R0, nv), chunk_max(R1, nv - 32));
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&xbar[q]);
-                    if (!warp_wait(&xbar[q], xphase, p, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    xphase ^= 1u;
-                    const float m = fmaxf(xch[r_in_tile], xch[kBM + r_in_tile]);
-                    float zy = 0.0f;
-                    const int yc = ycol - h * 64;
-                    const float cs0 = chunk_expsum(R0, nv, m, yc, zy);
-                    const float cs1 = chunk_expsum(R1, nv - 32, m, yc - 32, zy);
-                    const float ph = __fadd_rn(cs0, cs1);
-                    xch[2 * kBM + h * kBM + r_in_tile] = ph;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&xbar[q]);
-                    if (!warp_wait(&xbar[q], xphase, p, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    xphase ^= 1u;
-                    if (row_ok && vt < p.num_vocab_tiles) {
-                        if (h == 0) {
-                            const float s = __fadd_rn(ph, xch[3 * kBM + r_in_tile]);
-                            p.ws_ms[static_cast<int64_t>(vt) * p.ws_ld + row] = make_float2(m, s);
-                        }
-                        if (yc >= 0 && yc < 64) p.zy[row] = zy;
+                    // the 64-column log-sum-exp tile 2*vt + h of this row is entirely in R
+                    const int nv = p.V - col0;
+                    if (row_ok && nv > 0) {
+                        float zy = 0.0f;
+                        const int yc = ycol - h * 64;
+                        const float2 ms = tile_lse64(R, min(nv, kLT), yc, zy);
+                        p.ws_ms[static_cast<int64_t>(2 * vt + h) * p.ws_ld + row] = ms;
+                        if (yc >= 0 && yc < kLT) p.zy[row] = zy;
                     }
                 } else if (row_ok) {
                     float* dst = p.out + static_cast<int64_t>(row) * p.ldo + col0;
@@ -467,8 +439,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 // Upper levels of the leaf tree over gathered partials (one per slice), then the
-// per-tile log-sum-exp and sampled logit, exactly as the fused epilogue does.
-// grid: (num_vocab_tiles, ceil(T/128)); block: 128 threads, one row each.
+// log-sum-exp partials of the two 64-column tiles and the sampled logit, exactly as the fused
+// epilogue forms them.  grid: (num_vocab_tiles, ceil(T/128)); block: 128 threads, one row each.
 struct PartialsParams {
     const float* parts;      // [n_parts] x [T][ldp]
     int64_t part_stride;
@@ -487,36 +459,45 @@ __global__ void __launch_bounds__(128) partials_lse_kernel(const PartialsParams 
     const int vt = blockIdx.x;
     const int row = blockIdx.y * 128 + threadIdx.x;
     if (row >= p.T) return;
-    const int v0 = vt * kVT;
-    const int nvalid = min(kVT, p.V - v0);
-    int ycol = -1;
     const int y = p.ids[row];
-    if (y >= 0 && y < p.V) ycol = y - v0;
-    const float* base = p.parts + static_cast<int64_t>(row) * p.ldp + v0;
-    auto load = [&](int c, float(&z)[32]) {
-#pragma unroll 4
-        for (int i = 0; i < 32; ++i) {
-            const int col = c * 32 + i;
+    const float* base = p.parts + static_cast<int64_t>(row) * p.ldp;
+#pragma unroll 1
+    for (int h = 0; h < kVT / kLT; ++h) {
+        const int col0 = vt * kVT + h * kLT;
+        const int nv = p.V - col0;
+        if (nv <= 0) break;
+        float z[kLT];
+#pragma unroll
+        for (int i = 0; i < kLT; ++i) {
             float node[kParts];
 #pragma unroll
             for (int k = 0; k < kParts; ++k)
-                node[k] = col < nvalid ? base[k * p.part_stride + col] : 0.0f;
+                node[k] = i < nv ? base[k * p.part_stride + col0 + i] : 0.0f;
 #pragma unroll
             for (int w = kParts >> 1; w >= 1; w >>= 1)
 #pragma unroll
                 for (int k = 0; k < w; ++k) node[k] = __fadd_rn(node[2 * k], node[2 * k + 1]);
             z[i] = node[0];
         }
-    };
-    float m, s, zy = 0.0f;
-    tile_lse(load, nvalid, ycol, m, s, zy);
-    p.ws_ms[static_cast<int64_t>(vt) * p.ws_ld + row] = make_float2(m, s);
-    if (ycol >= 0 && ycol < kVT) p.zy[row] = zy;
+        const int ycol = (y >= 0 && y < p.V) ? y - col0 : -1;
+        float zy = 0.0f;
+        const float2 ms = tile_lse64(z, min(nv, kLT), ycol, zy);
+        p.ws_ms[static_cast<int64_t>(2 * vt + h) * p.ws_ld + row] = ms;
+        if (ycol >= 0 && ycol < kLT) p.zy[row] = zy;
+    }
 }
 
-// Fixed pairwise tree over the vocabulary tiles of each row (adjacent pairs first,
-// level by level; an odd last entry moves up a level unchanged), logZ and logp.
-// block: 4 warps, one row per warp; dynamic smem: 4 x num_vocab_tiles float2.
+// Fixed pairwise tree over the 64-column log-sum-exp tiles of each row (adjacent pairs
+// first, level by level; an odd last entry moves up a level unchanged), logZ and logp.
+//
+// Level l of that tree holds one node per aligned block [j 2^l, (j+1) 2^l) of tiles (cut
+// at the last tile), and two nodes merge exactly when their blocks are siblings.  So any
+// split of the tiles into aligned power-of-two segments gives the same nodes in the same
+// merge order: a thread folds one segment (8-tile rounds, each an in-register tree, joined
+// by a binary counter whose final fold runs from the smallest block up), and the segments
+// of a row meet in a shared-memory tree.  The split is chosen per launch for occupancy
+// and coalescing; the bits do not depend on it.
+// block: rows x nseg threads, thread (r, g) at g * rows + r; grid: ceil(T / rows).
 struct CombineParams {
     const float2* ws_ms;
     int64_t ws_ld;
@@ -524,39 +505,109 @@ struct CombineParams {
     const int32_t* ids;
     int32_t T;
     int32_t V;
-    int32_t num_vocab_tiles;
+    int32_t num_tiles;        // ceil(V / 64)
+    int32_t rows;             // rows per block (power of two, <= 16)
+    int32_t seg_log;          // tiles per segment = 2^seg_log, 3 <= seg_log <= kSegLogMax
+    int32_t nseg;             // ceil(num_tiles / 2^seg_log); rows * nseg <= 512
     float* out_logp;
     float* out_logZ;          // may be null
     int* status;
 };
 
-static __global__ void __launch_bounds__(128) lse_combine_kernel(const CombineParams p) {
-    extern __shared__ float2 cmb_smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * 4 + warp;
-    if (row >= p.T) return;
-    float2* a = cmb_smem + warp * p.num_vocab_tiles;
-    for (int b = lane; b < p.num_vocab_tiles; b += 32) a[b] = p.ws_ms[b * p.ws_ld + row];
-    __syncwarp();
-    int cnt = p.num_vocab_tiles;
-    while (cnt > 1) {
-        const int half = cnt >> 1;
-        for (int base = 0; base < half; base += 32) {
-            const int i = base + lane;
-            float2 r = make_float2(0.0f, 0.0f);
-            if (i < half) r = lse_merge(a[2 * i], a[2 * i + 1]);
-            __syncwarp();
-            if (i < half) a[i] = r;
-            __syncwarp();
-        }
-        if (cnt & 1) {
-            if (lane == 0) a[half] = a[cnt - 1];
-            __syncwarp();
-        }
-        cnt = half + (cnt & 1);
+constexpr int kCmbRound = 8;      // tiles per in-register tree
+constexpr int kSegLogMax = 11;    // up to 2^11 tiles per thread
+constexpr int kCmbMaxThreads = 512;
+
+struct CombineLayout {
+    int rows, seg_log, nseg;
+};
+
+// Rows per block: the largest power of two <= 16 that still gives every SM two blocks;
+// segment length: the shortest that fits the block in 512 threads and the grid in about
+// two waves of 2048 threads per SM.
+__host__ inline CombineLayout combine_layout(int64_t T, int num_tiles, int num_sms) {
+    CombineLayout c{1, 3, 0};
+    while (c.rows < 16 && static_cast<int64_t>(c.rows) * 2 * num_sms <= T) c.rows *= 2;
+    const int64_t groups = (T + c.rows - 1) / c.rows;
+    for (;;) {
+        c.nseg = (num_tiles + (1 << c.seg_log) - 1) >> c.seg_log;
+        const int64_t threads = groups * c.rows * c.nseg;
+        if (c.seg_log == kSegLogMax) break;
+        if (c.rows * c.nseg <= kCmbMaxThreads && threads <= int64_t(4096) * num_sms) break;
+        ++c.seg_log;
     }
-    if (lane == 0) {
-        const float lz = lse_finish(a[0]);
+    while (c.rows > 1 && c.rows * c.nseg > kCmbMaxThreads) c.rows /= 2;  // V beyond 2^21 only
+    return c;
+}
+
+static __global__ void __launch_bounds__(kCmbMaxThreads) lse_combine_kernel(const CombineParams p) {
+    extern __shared__ float2 cmb_smem[];  // [nseg][rows]
+    const int r = threadIdx.x % p.rows;
+    const int g = threadIdx.x / p.rows;
+    const int row = blockIdx.x * p.rows + r;
+    const bool row_ok = row < p.T;
+    if (row_ok) {
+        const int b_end = min((g + 1) << p.seg_log, p.num_tiles);
+        float2 stack[kSegLogMax - 2];  // counter levels: blocks of 8, 16, ..., 2^kSegLogMax
+        uint32_t k = 0;                // rounds folded so far
+        const int b_begin = g << p.seg_log;
+        float2 nxt[kCmbRound];         // the next round's tiles, loaded one round ahead
+#pragma unroll
+        for (int i = 0; i < kCmbRound; ++i)
+            nxt[i] = b_begin + i < b_end
+                         ? __ldg(p.ws_ms + static_cast<int64_t>(b_begin + i) * p.ws_ld + row)
+                         : make_float2(0.0f, 0.0f);
+        for (int b = b_begin; b < b_end; b += kCmbRound, ++k) {
+            const int nv = min(kCmbRound, b_end - b);
+            float2 v[kCmbRound];
+#pragma unroll
+            for (int i = 0; i < kCmbRound; ++i) v[i] = nxt[i];
+            const int bn = b + kCmbRound;
+#pragma unroll
+            for (int i = 0; i < kCmbRound; ++i)
+                nxt[i] = bn + i < b_end
+                             ? __ldg(p.ws_ms + static_cast<int64_t>(bn + i) * p.ws_ld + row)
+                             : make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int w = 1; w < kCmbRound; w <<= 1)
+#pragma unroll
+                for (int i = 0; i < kCmbRound; i += 2 * w)
+                    if (i + w < nv) v[i] = lse_merge(v[i], v[i + w]);
+            float2 carry = v[0];
+            bool open = true;  // carry not yet stored
+#pragma unroll
+            for (int j = 0; j < kSegLogMax - 2; ++j) {
+                if (open) {
+                    if ((k >> j) & 1u) {
+                        carry = lse_merge(stack[j], carry);
+                    } else {
+                        stack[j] = carry;
+                        open = false;
+                    }
+                }
+            }
+        }
+        // blocks still open, smallest (rightmost) first
+        float2 acc = make_float2(0.0f, 0.0f);
+        bool have = false;
+#pragma unroll
+        for (int j = 0; j < kSegLogMax - 2; ++j) {
+            if ((k >> j) & 1u) {
+                acc = have ? lse_merge(stack[j], acc) : stack[j];
+                have = true;
+            }
+        }
+        cmb_smem[g * p.rows + r] = acc;
+    }
+    __syncthreads();
+    for (int s = 1; s < p.nseg; s <<= 1) {
+        if (row_ok && (g & (2 * s - 1)) == 0 && g + s < p.nseg)
+            cmb_smem[g * p.rows + r] = lse_merge(cmb_smem[g * p.rows + r],
+                                                 cmb_smem[(g + s) * p.rows + r]);
+        __syncthreads();
+    }
+    if (row_ok && g == 0) {
+        const float lz = lse_finish(cmb_smem[r]);
         const int y = p.ids[row];
         float lp;
         if (y >= 0 && y < p.V) {

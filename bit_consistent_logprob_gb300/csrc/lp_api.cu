@@ -91,12 +91,13 @@ struct lp_handle {
     const void* W = nullptr;
     int device = 0;
     int num_sms = 0;
-    int num_vocab_tiles = 0;
+    int num_vocab_tiles = 0;  // ceil(V / 128): MMA tiles
+    int num_lse_tiles = 0;    // ceil(V / 64): log-sum-exp tiles
     int leaf_len = 0;
     uint64_t timeout_ns = 0;
     CUtensorMap tmW{};
     // workspace (device)
-    float2* ws_ms = nullptr;      // [num_vocab_tiles][max_tokens]
+    float2* ws_ms = nullptr;      // [num_lse_tiles][max_tokens]
     float* zy = nullptr;          // [max_tokens]
     int* status = nullptr;        // sticky status word
     double* blk_sum = nullptr;    // [max_is_blocks]
@@ -205,6 +206,7 @@ int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int lea
     p.leaf_count = leaf_count;
     p.num_row_tiles = static_cast<int32_t>(ceil_div(rows, lp::kBM));
     p.num_vocab_tiles = h->num_vocab_tiles;
+    p.num_lse_tiles = h->num_lse_tiles;
     p.band = h->band;
     p.ids = ids;
     p.ws_ms = h->ws_ms;
@@ -254,12 +256,17 @@ int launch_combine(lp_handle* h, const int32_t* ids, int rows, float* out_logp, 
     c.ids = ids;
     c.T = rows;
     c.V = h->cfg.V;
-    c.num_vocab_tiles = h->num_vocab_tiles;
+    c.num_tiles = h->num_lse_tiles;
+    const lp::CombineLayout lay = lp::combine_layout(rows, h->num_lse_tiles, h->num_sms);
+    c.rows = lay.rows;
+    c.seg_log = lay.seg_log;
+    c.nseg = lay.nseg;
     c.out_logp = out_logp;
     c.out_logZ = out_logZ;
     c.status = h->status;
-    const size_t smem = 4 * sizeof(float2) * static_cast<size_t>(h->num_vocab_tiles);
-    lp::lse_combine_kernel<<<static_cast<unsigned>(ceil_div(rows, 4)), 128, smem, st>>>(c);
+    const size_t smem = sizeof(float2) * static_cast<size_t>(lay.rows) * lay.nseg;
+    lp::lse_combine_kernel<<<static_cast<unsigned>(ceil_div(rows, lay.rows)),
+                             static_cast<unsigned>(lay.rows * lay.nseg), smem, st>>>(c);
     LP_CUDA(cudaGetLastError(), "lse_combine_kernel launch");
     ++h->last_launches;
     return LP_OK;
@@ -387,6 +394,7 @@ int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out) 
     h->device = dev;
     h->num_sms = prop.multiProcessorCount;
     h->num_vocab_tiles = static_cast<int>(ceil_div(cfg->V, lp::kVT));
+    h->num_lse_tiles = static_cast<int>(ceil_div(cfg->V, lp::kLT));
     h->leaf_len = cfg->H / cfg->n_leaves;
     uint64_t timeout_ms = 2000;
     if (const char* e = std::getenv("LP_WAIT_TIMEOUT_MS")) {
@@ -426,7 +434,7 @@ int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out) 
     };
     h->max_is_blocks = ceil_div(kMaxIsTokens, lp::kIsBlock);
     if ((rc = alloc(reinterpret_cast<void**>(&h->ws_ms),
-                    sizeof(float2) * static_cast<size_t>(h->num_vocab_tiles) * mt, "ws_ms")) ||
+                    sizeof(float2) * static_cast<size_t>(h->num_lse_tiles) * mt, "ws_ms")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->zy), sizeof(float) * mt, "zy")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->status), sizeof(int), "status")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->blk_sum), sizeof(double) * h->max_is_blocks,
@@ -456,14 +464,8 @@ int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out) 
     if ((rc = set_gemm_attributes<true>()) != LP_OK || (rc = set_gemm_attributes<false>()) != LP_OK)
         return cleanup(rc);
     cudaError_t e;
-    const int combine_smem = static_cast<int>(4 * sizeof(float2) * h->num_vocab_tiles);
-    if (combine_smem > 48 * 1024) {
-        if (combine_smem > 227 * 1024) return cleanup(fail(LP_ERR_UNSUPPORTED, "V too large"));
-        if ((e = cudaFuncSetAttribute(lp::lse_combine_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      combine_smem)) != cudaSuccess)
-            return cleanup(cuda_fail(e, "cudaFuncSetAttribute(lse_combine_kernel)"));
-    }
+    if (h->num_lse_tiles > (lp::kCmbMaxThreads << lp::kSegLogMax))
+        return cleanup(fail(LP_ERR_UNSUPPORTED, "V too large (at most 2^26 columns)"));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if ((e = cudaMemsetAsync(h->status, 0, sizeof(int), st)) != cudaSuccess ||
         (e = cudaStreamSynchronize(st)) != cudaSuccess)

@@ -27,9 +27,9 @@ namespace {
 
 constexpr int kBand = 32;
 // Capacity of the static scratch (stated in include/lp.h):
-constexpr int64_t kNoallocMaxTileRows = int64_t(1) << 19;  // T * ceil(V/128) (max, sum) pairs
+constexpr int64_t kNoallocMaxTileRows = int64_t(1) << 20;  // T * ceil(V/64) (max, sum) pairs
 constexpr int64_t kNoallocMaxRows = int64_t(1) << 15;      // T per call
-constexpr size_t kMsBytes = static_cast<size_t>(kNoallocMaxTileRows) * sizeof(float2);  // 4 MiB
+constexpr size_t kMsBytes = static_cast<size_t>(kNoallocMaxTileRows) * sizeof(float2);  // 8 MiB
 constexpr size_t kZyBytes = static_cast<size_t>(kNoallocMaxRows) * sizeof(float);       // 128 KiB
 constexpr size_t kStatusBytes = 256;
 constexpr size_t kScratchBytes = kMsBytes + kZyBytes + kStatusBytes;
@@ -86,9 +86,6 @@ void setup_device(int dev, DeviceSetup& s) {
         e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<true, 2, 1>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  lp::gemm_smem_bytes(2));
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(lp::lse_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 227 * 1024);
     if (e != cudaSuccess) {
         cudaGetLastError();
         s.status = LP_ERR_CUDA;
@@ -144,10 +141,10 @@ LP_API int lp_logprobs_noalloc(const void* W, int32_t H, int32_t V, int32_t n_le
     if (H <= 0 || V <= 0 || H % (lp::kBK * n_leaves) != 0)
         return nfail(LP_ERR_UNSUPPORTED, "need H > 0, V > 0 and H %% (64 * n_leaves) == 0");
     if (T < 0) return nfail(LP_ERR_INVALID_ARG, "T must be >= 0");
-    const int64_t nb = (static_cast<int64_t>(V) + lp::kVT - 1) / lp::kVT;
+    const int64_t nb = (static_cast<int64_t>(V) + lp::kLT - 1) / lp::kLT;  // log-sum-exp tiles
     if (T > kNoallocMaxRows || T * nb > kNoallocMaxTileRows)
         return nfail(LP_ERR_INVALID_ARG,
-                     "T = %lld rows x %lld vocabulary tiles exceeds the static scratch "
+                     "T = %lld rows x %lld log-sum-exp tiles exceeds the static scratch "
                      "(at most %lld rows and %lld row-tiles; use lp_logprobs with a handle)",
                      (long long)T, (long long)nb, (long long)kNoallocMaxRows,
                      (long long)kNoallocMaxTileRows);
@@ -156,8 +153,8 @@ LP_API int lp_logprobs_noalloc(const void* W, int32_t H, int32_t V, int32_t n_le
         return nfail(LP_ERR_INVALID_ARG, "W, X, ids and out_logp must not be NULL");
     if (!aligned16(W) || !aligned16(X) || ldx < H || ldx % 8 != 0)
         return nfail(LP_ERR_INVALID_ARG, "W and X must be 16-byte aligned, ldx >= H, ldx %% 8 == 0");
-    if (static_cast<int64_t>(nb) * 4 * sizeof(float2) > 227 * 1024)
-        return nfail(LP_ERR_UNSUPPORTED, "V too large");
+    if (nb > (int64_t(lp::kCmbMaxThreads) << lp::kSegLogMax))
+        return nfail(LP_ERR_UNSUPPORTED, "V too large (at most 2^26 columns)");
 
     // ---- once-per-device set-up (the first call on a device; it must precede any capture)
     int dev = 0;
@@ -191,7 +188,8 @@ LP_API int lp_logprobs_noalloc(const void* W, int32_t H, int32_t V, int32_t n_le
     p.leaf_begin = 0;
     p.leaf_count = n_leaves;
     p.num_row_tiles = (rows + lp::kBM - 1) / lp::kBM;
-    p.num_vocab_tiles = static_cast<int32_t>(nb);
+    p.num_vocab_tiles = static_cast<int32_t>((V + lp::kVT - 1) / lp::kVT);
+    p.num_lse_tiles = static_cast<int32_t>(nb);
     p.band = kBand;
     p.x_box_rows = static_cast<int32_t>(box);
     p.ids = ids;
@@ -202,7 +200,7 @@ LP_API int lp_logprobs_noalloc(const void* W, int32_t H, int32_t V, int32_t n_le
     p.ldo = 0;
     p.status = status;
     p.timeout_ns = 2000000000ull;
-    const int64_t tiles = static_cast<int64_t>(p.num_row_tiles) * nb;
+    const int64_t tiles = static_cast<int64_t>(p.num_row_tiles) * p.num_vocab_tiles;
     const int grid = static_cast<int>(tiles < s.num_sms ? tiles : s.num_sms);
     if (p.leaf_len % (2 * lp::kBK) == 0)
         lp::leaf_gemm_kernel<true, 2, 1><<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(2), st>>>(tmX, tmW, p);
@@ -218,12 +216,17 @@ LP_API int lp_logprobs_noalloc(const void* W, int32_t H, int32_t V, int32_t n_le
     c.ids = ids;
     c.T = rows;
     c.V = V;
-    c.num_vocab_tiles = static_cast<int32_t>(nb);
+    c.num_tiles = static_cast<int32_t>(nb);
+    const lp::CombineLayout lay = lp::combine_layout(rows, c.num_tiles, s.num_sms);
+    c.rows = lay.rows;
+    c.seg_log = lay.seg_log;
+    c.nseg = lay.nseg;
     c.out_logp = out_logp;
     c.out_logZ = out_logZ;
     c.status = status;
-    lp::lse_combine_kernel<<<static_cast<unsigned>((rows + 3) / 4), 128,
-                             4 * sizeof(float2) * static_cast<size_t>(nb), st>>>(c);
+    lp::lse_combine_kernel<<<static_cast<unsigned>((rows + lay.rows - 1) / lay.rows),
+                             static_cast<unsigned>(lay.rows * lay.nseg),
+                             sizeof(float2) * static_cast<size_t>(lay.rows) * lay.nseg, st>>>(c);
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return nfail(LP_ERR_CUDA, "lse_combine_kernel launch: %s", cudaGetErrorString(e));

@@ -12,7 +12,8 @@
 
 namespace lp {
 
-constexpr int kVT = 128;     // vocabulary tile: MMA N and the log-sum-exp granularity
+constexpr int kVT = 128;     // vocabulary tile: MMA N
+constexpr int kLT = 64;      // log-sum-exp tile: half a vocabulary tile
 constexpr int kBM = 128;     // token rows per tile: MMA M
 constexpr int kBK = 64;      // K elements per pipeline stage (128 bytes of bf16)
 constexpr int kChunk = 32;   // columns per TMEM load
@@ -33,16 +34,16 @@ __device__ __forceinline__ float tree_sum32(float (&v)[32]) {
     return v[0];
 }
 
-// Log-sum-exp partial of one 128-column vocabulary tile of one row, defined on its four
-// 32-column chunks c = 0..3 (columns at or beyond `nvalid`, i.e. vocabulary entries >= V,
+// Log-sum-exp partial of one 64-column log-sum-exp tile of one row, defined on its two
+// 32-column chunks c = 0, 1 (columns at or beyond `nvalid`, i.e. vocabulary entries >= V,
 // are excluded):
 //   m_c = max of the chunk's valid logits, taken left to right from -inf
-//   m   = max(max(m_0, m_1), max(m_2, m_3))
+//   m   = max(m_0, m_1)
 //   e_i = exp(z_i - m) for valid columns, 0 otherwise
 //   s_c = pairwise tree sum of the chunk's 32 e_i (chunk_expsum)
-//   s   = (s_0 + s_1) + (s_2 + s_3)
-// The fused GEMM epilogue splits the chunks over two warps and the tensor-parallel
-// kernel runs them in one thread; both apply exactly these operations in this order.
+//   s   = s_0 + s_1
+// The fused GEMM epilogue (one thread holds a whole 64-column tile of its row) and the
+// tensor-parallel kernel apply exactly these operations in this order.
 __device__ __forceinline__ float chunk_max(const float (&v)[32], int nvalid) {
     float m = -INFINITY;
 #pragma unroll
@@ -65,27 +66,16 @@ __device__ __forceinline__ float chunk_expsum(float (&v)[32], int nvalid, float 
     return tree_sum32(v);
 }
 
-// The whole tile in one thread.  `load(c, v)` fills v with the 32 logits of chunk c; it is
-// called twice per chunk (max pass, then sum pass).
-template <class Load>
-__device__ __forceinline__ void tile_lse(Load&& load, int nvalid, int ycol, float& m_out,
-                                         float& s_out, float& zy) {
-    float v[32];
-    float mc[kChunks];
-#pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-        load(c, v);
-        mc[c] = chunk_max(v, nvalid - c * 32);
-    }
-    const float m = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
-    float cs[kChunks];
-#pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-        load(c, v);
-        cs[c] = chunk_expsum(v, nvalid - c * 32, m, ycol - c * 32, zy);
-    }
-    m_out = m;
-    s_out = __fadd_rn(__fadd_rn(cs[0], cs[1]), __fadd_rn(cs[2], cs[3]));
+// One 64-column log-sum-exp tile held by one thread (z[0..63]); nvalid counts its valid
+// columns (> 0), ycol is the tile-relative column of the sampled token (or outside
+// [0, 64)).  Destroys z.
+__device__ __forceinline__ float2 tile_lse64(float (&z)[64], int nvalid, int ycol, float& zy) {
+    float(&z0)[32] = *reinterpret_cast<float(*)[32]>(&z[0]);
+    float(&z1)[32] = *reinterpret_cast<float(*)[32]>(&z[32]);
+    const float m = fmaxf(chunk_max(z0, nvalid), chunk_max(z1, nvalid - 32));
+    const float s0 = chunk_expsum(z0, nvalid, m, ycol, zy);
+    const float s1 = chunk_expsum(z1, nvalid - 32, m, ycol - 32, zy);
+    return make_float2(m, __fadd_rn(s0, s1));
 }
 
 // Merge two (max, sum-exp) pairs: m = max(m1, m2), s = s1 e^(m1-m) + s2 e^(m2-m).

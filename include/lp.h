@@ -7,7 +7,8 @@
  *   P_j[t,v] = sum_{k in leaf j} X[t,k] W[v,k]      fp32 accumulation, K cut into
  *                                                   N contiguous leaves of H/N
  *   z[t,v]   = fixed pairwise tree over P_0..P_{N-1} (adjacent pairs first)
- *   logZ[t]  = fixed-order log-sum-exp of z[t,:] over the vocabulary
+ *   logZ[t]  = fixed-order log-sum-exp of z[t,:]: (max, sum-exp) per 64-column tile, then a
+ *              fixed pairwise tree over the tiles
  *   logp[t]  = z[t, y_t] - logZ[t]
  *
  * and, from a learner logprob log pi and a rollout logprob log mu, the unclipped
@@ -197,10 +198,10 @@ LP_API int lp_profile_read(lp_handle* h, double* gemm_ms_total, int32_t* gemm_la
  * cudaMalloc -- code running while a CUDA graph is captured, runtimes whose device memory
  * is planned ahead by their own allocator, hosts that forbid allocation after start-up.
  * The scratch (per-tile max/sum-exp pairs, sampled logits, a status word) is a fixed
- * 4.25 MiB file-scope device array that every GPU loading the library holds until exit.
+ * 8.13 MiB file-scope device array that every GPU loading the library holds until exit.
  *   W, H, V, n_leaves  as in lp_config / lp_init (W referenced, bf16 [V, H]).
  *   X, ldx, ids, T, out_logp, out_logZ  as in lp_logprobs.
- * Limits: T <= 32768 and T * ceil(V / 128) <= 524288 (e.g. 441 rows at V = 151936);
+ * Limits: T <= 32768 and T * ceil(V / 64) <= 1048576 (e.g. 441 rows at V = 151936);
  * larger calls return LP_ERR_INVALID_ARG and must use lp_logprobs with a handle.
  * The first call on a device resolves the array's device address and sets kernel
  * attributes (no allocation); make that first call before any stream capture.

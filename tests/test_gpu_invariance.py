@@ -88,6 +88,25 @@ def test_token_count_sweep(eng, data, solo):
     eng.check()
 
 
+def test_combine_layouts_change_no_bits(data, eng, solo):
+    # The vocabulary combine picks rows per block (1 to 16) and the per-thread segment
+    # length from T; the pairwise tree it evaluates, and so every bit, stay the same.
+    X, W, ids = data
+    rng = np.random.default_rng(4)
+    targets = list(solo)[:4]
+    with Engine(W, n_leaves=N, max_tokens=10000) as e:
+        for T in (1, 2, 300, 600, 1300, 2500, 5000, 10000):
+            order = rng.choice(POOL, size=T, replace=True)
+            pos = rng.choice(T, size=min(T, len(targets)), replace=False)
+            order[pos] = targets[: len(pos)]
+            idx = torch.as_tensor(order, device=X.device)
+            lp, lz = e.logprobs(X[idx].contiguous(), ids[idx].contiguous(), return_logZ=True)
+            for p_, t in zip(pos, targets):
+                assert_bit_equal(lp[p_:p_ + 1], solo[t][0], f"row {t} at T={T}")
+                assert_bit_equal(lz[p_:p_ + 1], solo[t][1], f"logZ {t} at T={T}")
+        e.check()
+
+
 def test_chunking_changes_no_bits(data, dev):
     X, W, ids = data
     T = 4097

@@ -67,9 +67,9 @@ def test_noalloc_matches_handle_path_on_two_calls(T, H, V, N):
 def test_noalloc_refuses_calls_beyond_its_scratch():
     dev = require_cuda()
     lib = _native.load()
-    H, V = 256, 151936                      # 1187 vocabulary tiles
+    H, V = 256, 151936                      # 2374 log-sum-exp tiles of 64 columns
     W = inputs.lm_head(V, H, seed=1, device=dev)
-    T = 442                                 # 442 * 1187 > 2^19 row-tiles
+    T = 442                                 # 442 * 2374 > 2^20 row-tiles
     X = inputs.hidden_states(T, H, seed=1, device=dev)
     ids = inputs.uniform_ids(T, V, seed=1, device=dev)
     out = torch.empty(T, device=dev)
