@@ -58,6 +58,11 @@ def _load():
         lib.oracle_tree_fp32.argtypes = [p, i32]
         lib.oracle_tree_fp32.restype = ctypes.c_float
         lib.oracle_tree_fp32_many.argtypes = [p, i32, i64, p]
+        lib.oracle_acceptance_stats.argtypes = [p, p, p, i64, p]
+        lib.oracle_reinforce_zero.argtypes = [p, p, p, p, i64, p, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_double, ctypes.c_float, ctypes.c_float,
+                                              ctypes.c_double, ctypes.c_double,
+                                              p, p, p, p, p, p]
         lib.oracle_importance_weights.argtypes = [p, p, p, i64, p, p, p, p]
         for f in (lib.oracle_logits, lib.oracle_logprobs, lib.oracle_log_softmax,
                   lib.oracle_leaf_sums, lib.oracle_tree_fp32_many,
@@ -188,3 +193,60 @@ def importance_weights(logp_pi, logp_mu, mask=None):
     _load().oracle_importance_weights(_ptr(a), _ptr(b), None if m is None else _ptr(m), T,
                                       _ptr(w), _ptr(term), _ptr(d3), _ptr(nv))
     return w, term, float(d3[0]), int(nv[0])
+
+
+def _f32(x) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+
+
+def _mask_arg(mask, T):
+    if mask is None:
+        return None
+    m = np.ascontiguousarray(np.asarray(mask).astype(np.uint8))
+    assert m.shape == (T,)
+    return m
+
+
+def acceptance_stats(logp_a, logp_b, mask=None) -> dict:
+    """max, mean, std (population) of |a - b| and k3 = mean(r - 1 - log r), r = e^(a-b),
+    over valid tokens; n_valid."""
+    a, b = _f32(logp_a), _f32(logp_b)
+    assert a.shape == b.shape and a.ndim == 1
+    m = _mask_arg(mask, a.size)
+    out = np.zeros(5, dtype=np.float64)
+    _load().oracle_acceptance_stats(_ptr(a), _ptr(b), None if m is None else _ptr(m), a.size,
+                                    _ptr(out))
+    return dict(max=out[0], mean=out[1], std=out[2], k3=out[3], n_valid=int(out[4]))
+
+
+TIS, TOKEN_GATE, SEQ_GATE = 1, 2, 4
+
+
+def reinforce_zero(logp_pi, logp_mu, offsets, rewards, group_size, mask=None, flags=0,
+                   tis_cap=float("inf"), token_log_lo=-float("inf"),
+                   token_log_hi=float("inf"), seq_log_lo=-float("inf"),
+                   seq_log_hi=float("inf")) -> dict:
+    """REINFORCE Zero loss, weights and dL/dlog pi for responses packed at ``offsets``.
+
+    Returns dict(loss, w_hat[T], grad[T], adv[B], seq_logratio[B], kept[B]) in fp64."""
+    a, b = _f32(logp_pi), _f32(logp_mu)
+    T = a.size
+    offs = np.ascontiguousarray(np.asarray(offsets, dtype=np.int64))
+    B = offs.size - 1
+    assert B >= 0 and offs[0] == 0 and offs[-1] == T and np.all(np.diff(offs) >= 0)
+    r = _f32(rewards)
+    assert r.shape == (B,) and group_size >= 1 and B % group_size == 0
+    m = _mask_arg(mask, T)
+    w_hat = np.zeros(T, dtype=np.float64)
+    grad = np.zeros(T, dtype=np.float64)
+    adv = np.zeros(B, dtype=np.float64)
+    slr = np.zeros(B, dtype=np.float64)
+    kept = np.zeros(B, dtype=np.int32)
+    loss = np.zeros(1, dtype=np.float64)
+    _load().oracle_reinforce_zero(_ptr(a), _ptr(b), None if m is None else _ptr(m), _ptr(offs), B,
+                                  _ptr(r), int(group_size), int(flags), float(tis_cap),
+                                  float(token_log_lo), float(token_log_hi), float(seq_log_lo),
+                                  float(seq_log_hi), _ptr(w_hat), _ptr(grad), _ptr(adv), _ptr(slr),
+                                  _ptr(kept), _ptr(loss))
+    return dict(loss=float(loss[0]), w_hat=w_hat, grad=grad, adv=adv, seq_logratio=slr,
+                kept=kept.astype(bool))

@@ -38,6 +38,32 @@
  *      section 3).  log w is taken as exactly d = log pi - log mu, so the term
  *      is expm1(d) - d; it is 0 at w = 1.  No valid token gives D3 = 0.
  *
+ *  - oracle_acceptance_stats: over the valid tokens, the max, mean and
+ *      population standard deviation of |a - b| between two logprob vectors,
+ *      and the k3 KL estimate mean(r - 1 - log r) with r = exp(a - b) (vLLM
+ *      blog section 2: acceptance asks the max, mean and std of the per-token
+ *      difference to be 0 over every valid sampled token; section 3.2: the k3
+ *      estimator).  a is the learner's logprob, b the rollout's, so r = pi/mu
+ *      and k3 is the same per-token term as D3.  A NaN difference on a valid
+ *      token makes every statistic NaN; no valid token gives all zeros.
+ *
+ *  - oracle_reinforce_zero: the REINFORCE Zero loss (REINFORCE Zero summary,
+ *      section 4) for B responses packed back to back,
+ *        L = -(1/B) sum_i (1/T_i) sum_t A_i * w_it,
+ *      A_i = R_i - mean of R over the response's group (groups of G
+ *      consecutive responses), T_i = valid tokens of response i, w = pi/mu
+ *      unclipped at token level, and dL/dlog pi_it = -(1/B)(1/T_i) A_i w_it.
+ *      Options from the corrections the pages list beside it (vLLM blog
+ *      section 1; REINFORCE Zero summary, results table): TIS truncates
+ *      the weight at a cap, w_hat = min(w, C); a token gate zeroes tokens
+ *      whose d = log pi - log mu (rounded to fp32, the precision the gate is
+ *      decided in) lies outside [lo, hi]; a sequence gate (MIS) zeroes every
+ *      token of a response whose sequence log-ratio sum_t d_t lies outside
+ *      [lo, hi].  With any option the modified weight multiplies grad log pi
+ *      (it is held constant under differentiation), so the gradient is
+ *      -(1/B)(1/T_i) A_i w_hat_it and L uses w_hat in place of w.  Masked
+ *      tokens get w_hat = 0 and gradient 0; a response with T_i = 0 adds 0.
+ *
  * Every function is single-threaded per output element; rows are spread over
  * OpenMP threads, which changes no result (each row is computed alone).
  */
@@ -188,4 +214,89 @@ void oracle_importance_weights(const float* logp_pi, const float* logp_mu, const
     }
     *n_valid = n;
     *d3 = n > 0 ? sum / (double)n : 0.0;
+}
+
+/* Max, mean, population std of |a-b| and mean of expm1(d) - d over valid tokens. */
+void oracle_acceptance_stats(const float* a, const float* b, const uint8_t* mask, int64_t T,
+                             double* out /* [5]: max, mean, std, k3, n_valid */) {
+    int64_t n = 0;
+    double mx = 0.0, sum = 0.0, k3 = 0.0;
+    int any_nan = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        if (mask != NULL && mask[t] == 0) continue;
+        double d = (double)a[t] - (double)b[t];
+        double x = fabs(d);
+        if (isnan(x)) any_nan = 1;
+        else if (x > mx) mx = x;
+        sum += x;
+        k3 += expm1(d) - d;
+        ++n;
+    }
+    if (n == 0) {
+        for (int i = 0; i < 5; ++i) out[i] = 0.0;
+        return;
+    }
+    double mean = sum / (double)n;
+    double ss = 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+        if (mask != NULL && mask[t] == 0) continue;
+        double x = fabs((double)a[t] - (double)b[t]);
+        ss += (x - mean) * (x - mean);
+    }
+    out[0] = any_nan ? NAN : mx;
+    out[1] = mean;
+    out[2] = sqrt(ss / (double)n);
+    out[3] = k3 / (double)n;
+    out[4] = (double)n;
+}
+
+enum { ORC_TIS = 1, ORC_TOKEN_GATE = 2, ORC_SEQ_GATE = 4 };
+
+/* REINFORCE Zero loss with optional TIS / token gate / sequence gate.
+ * offs[B+1]: response i holds tokens [offs[i], offs[i+1]). */
+void oracle_reinforce_zero(const float* logp_pi, const float* logp_mu, const uint8_t* mask,
+                           const int64_t* offs, int64_t B, const float* rewards, int G,
+                           int flags, double tis_cap, float tok_lo, float tok_hi,
+                           double seq_lo, double seq_hi,
+                           double* w_hat, double* grad, double* adv, double* seq_logratio,
+                           int32_t* kept, double* loss) {
+    double total = 0.0;
+    for (int64_t i = 0; i < B; ++i) {
+        /* advantage: reward minus the mean reward of the response's group */
+        int64_t g0 = (i / G) * G;
+        double gsum = 0.0;
+        for (int64_t j = g0; j < g0 + G; ++j) gsum += (double)rewards[j];
+        double A = (double)rewards[i] - gsum / (double)G;
+        adv[i] = A;
+
+        int64_t n = 0;
+        double lr = 0.0;
+        for (int64_t t = offs[i]; t < offs[i + 1]; ++t) {
+            if (mask != NULL && mask[t] == 0) continue;
+            lr += (double)logp_pi[t] - (double)logp_mu[t];
+            ++n;
+        }
+        seq_logratio[i] = lr;
+        int keep = !(flags & ORC_SEQ_GATE) || (lr >= seq_lo && lr <= seq_hi);
+        kept[i] = keep;
+
+        double wsum = 0.0;
+        for (int64_t t = offs[i]; t < offs[i + 1]; ++t) {
+            int valid = mask == NULL || mask[t] != 0;
+            double d = (double)logp_pi[t] - (double)logp_mu[t];
+            double wh = exp(d);
+            if (flags & ORC_TOKEN_GATE) {
+                float d32 = (float)d;
+                if (!(d32 >= tok_lo && d32 <= tok_hi)) wh = 0.0;
+            }
+            if ((flags & ORC_TIS) && wh > tis_cap) wh = tis_cap;
+            if (!valid || !keep) wh = 0.0;
+            w_hat[t] = wh;
+            wsum += wh;
+        }
+        double coef = n > 0 ? -A / ((double)B * (double)n) : 0.0;
+        for (int64_t t = offs[i]; t < offs[i + 1]; ++t) grad[t] = coef * w_hat[t];
+        if (n > 0) total += A * wsum / (double)n;
+    }
+    *loss = B > 0 ? -total / (double)B : 0.0;
 }

@@ -267,6 +267,183 @@ def test_term_nonnegative_and_w_positive():
     assert np.all(w > 0) and np.all(term >= 0) and d3 > 0 and nv == 5000
 
 
+# ----------------------------------------------------------------- acceptance statistics
+def test_acceptance_stats_identical_inputs_all_zero():
+    rng = np.random.default_rng(30)
+    a = rng.uniform(-30, 0, 4000).astype(np.float32)
+    st = oracle.acceptance_stats(a, a.copy())
+    assert (st["max"], st["mean"], st["std"], st["k3"], st["n_valid"]) == (0.0, 0.0, 0.0, 0.0, 4000)
+
+
+def test_acceptance_stats_constant_gap_closed_form():
+    # a - b = 1/2 exactly on every token (b on a 1/8 grid): max = mean = 1/2, std = 0,
+    # k3 = e^(1/2) - 1 - 1/2.
+    b = (-np.arange(0, 640) / 8.0).astype(np.float32)
+    a = (b + 0.5).astype(np.float32)
+    st = oracle.acceptance_stats(a, b)
+    assert st["max"] == 0.5 and st["mean"] == 0.5 and st["std"] == 0.0
+    # (640 equal terms summed in fp64: relative error below 640 * 2^-53)
+    assert abs(st["k3"] - (math.exp(0.5) - 1.5)) < 1e-13 * st["k3"]
+    st = oracle.acceptance_stats(b, a)  # r = e^(-1/2)
+    assert abs(st["k3"] - (math.exp(-0.5) - 1 + 0.5)) < 1e-13 * st["k3"]
+
+
+def test_acceptance_stats_against_library_statistics():
+    import statistics
+
+    rng = np.random.default_rng(31)
+    a = rng.uniform(-12, 0, 3001).astype(np.float32)
+    b = (a + rng.normal(0, 0.05, a.size)).astype(np.float32)
+    mask = rng.random(a.size) < 0.7
+    st = oracle.acceptance_stats(a, b, mask)
+    gaps = [abs(Fraction(float(x)) - Fraction(float(y))) for x, y, m in zip(a, b, mask) if m]
+    assert st["n_valid"] == len(gaps)
+    assert st["max"] == float(max(gaps))
+    assert abs(st["mean"] - float(statistics.fmean(gaps))) < 1e-15
+    assert abs(st["std"] - statistics.pstdev([float(g) for g in gaps])) < 1e-14
+    # k3 is the D3 term on the same tokens
+    _, _, d3, nv = oracle.importance_weights(a, b, mask)
+    assert nv == st["n_valid"] and abs(st["k3"] - d3) < 1e-15
+
+
+def test_acceptance_stats_nan_mask_and_empty():
+    a = np.array([0.0, -1.0, np.nan, -2.0], dtype=np.float32)
+    b = np.array([0.0, -1.5, -3.0, -2.0], dtype=np.float32)
+    st = oracle.acceptance_stats(a, b, [1, 1, 0, 1])  # NaN token masked out
+    assert st["max"] == 0.5 and st["n_valid"] == 3
+    st = oracle.acceptance_stats(a, b)
+    assert all(math.isnan(st[k]) for k in ("max", "mean", "std", "k3"))
+    st = oracle.acceptance_stats(a, b, [0, 0, 0, 0])
+    assert st == dict(max=0.0, mean=0.0, std=0.0, k3=0.0, n_valid=0)
+
+
+# ----------------------------------------------------------------- REINFORCE Zero loss
+def test_reinforce_zero_worked_example():
+    # Two groups of two responses; rewards (1, 0 | 1/2, 1/2) give A = (1/2, -1/2, 0, 0).
+    # Response 0: tokens with w = 2 and 1 (mean 3/2); response 1: one token with w = 4.
+    # L = -(1/4) (1/2 * 3/2 - 1/2 * 4) = 5/16.  dL/dlog pi = -(1/4)(1/T_i) A_i w:
+    # -1/8, -1/16 | 1/2 | 0 0 0 | 0.
+    lp = np.array([math.log(2), 0, math.log(4), 0, 0, 0, 0], dtype=np.float32)
+    out = oracle.reinforce_zero(lp, np.zeros(7, np.float32), [0, 2, 3, 6, 7],
+                                [1, 0, 0.5, 0.5], 2)
+    assert abs(out["loss"] - 5 / 16) < 1e-6
+    assert np.allclose(out["grad"], [-1 / 8, -1 / 16, 1 / 2, 0, 0, 0, 0], rtol=1e-6, atol=0)
+    assert np.array_equal(out["adv"], [0.5, -0.5, 0.0, 0.0])
+    # masking response 0's second token makes its token mean 2: L = -(1/4)(1 - 2) = 1/4
+    out = oracle.reinforce_zero(lp, np.zeros(7, np.float32), [0, 2, 3, 6, 7],
+                                [1, 0, 0.5, 0.5], 2, mask=[1, 0, 1, 1, 1, 1, 1])
+    assert abs(out["loss"] - 1 / 4) < 1e-6 and out["grad"][1] == 0.0 and out["w_hat"][1] == 0.0
+
+
+def _rz_case(seed, B=8, G=4, lag=0.05):
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(1, 40, B)
+    offs = np.concatenate([[0], np.cumsum(lens)])
+    T = int(offs[-1])
+    # logprobs on a 2^-10 grid so that +-2^-12 perturbations are exact in fp32
+    lm = (np.round(rng.uniform(-6, -0.1, T) * 1024) / 1024).astype(np.float32)
+    lp = (lm + np.round(rng.normal(0, lag, T) * 1024) / 1024).astype(np.float32)
+    rewards = rng.integers(0, 2, B).astype(np.float32)
+    mask = rng.random(T) < 0.85
+    return lp, lm, offs, rewards, G, mask
+
+
+def test_reinforce_zero_equal_policies_give_zero_loss():
+    # w = 1 everywhere: L = -(1/B) sum_i A_i, and group-centred advantages sum to 0
+    lp, lm, offs, rewards, G, mask = _rz_case(40)
+    mask[offs[:-1]] = True  # every response keeps a valid token
+    out = oracle.reinforce_zero(lp, lp, offs, rewards, G, mask=mask)
+    assert abs(out["loss"]) < 1e-15
+    assert np.all(out["w_hat"][mask] == 1.0)
+
+
+@pytest.mark.parametrize("opts", [
+    dict(),
+    dict(flags=oracle.TIS, tis_cap=1.03),
+    dict(flags=oracle.TOKEN_GATE, token_log_lo=-0.06, token_log_hi=0.06),
+    dict(flags=oracle.SEQ_GATE, seq_log_lo=-0.3, seq_log_hi=0.3),
+], ids=["plain", "tis", "token_gate", "seq_gate"])
+def test_reinforce_zero_gradient_is_the_derivative_of_the_loss(opts):
+    lp, lm, offs, rewards, G, mask = _rz_case(41)
+    out = oracle.reinforce_zero(lp, lm, offs, rewards, G, mask=mask, **opts)
+    h = 2.0 ** -12
+    d = lp.astype(np.float64) - lm
+    checked = 0
+    for t in range(lp.size):
+        w = math.exp(d[t])
+        # stay inside one smooth piece: away from the cap and the gate edges
+        if "tis_cap" in opts and abs(w - opts["tis_cap"]) < 4 * h * w:
+            continue
+        if "token_log_lo" in opts and min(abs(d[t] - 0.06), abs(d[t] + 0.06)) < 2 * h:
+            continue
+        i = np.searchsorted(offs, t, side="right") - 1
+        if "seq_log_lo" in opts and min(abs(out["seq_logratio"][i] - 0.3),
+                                        abs(out["seq_logratio"][i] + 0.3)) < 2 * h:
+            continue
+        up, dn = lp.copy(), lp.copy()
+        up[t] += np.float32(h)
+        dn[t] -= np.float32(h)
+        lu = oracle.reinforce_zero(up, lm, offs, rewards, G, mask=mask, **opts)["loss"]
+        ld = oracle.reinforce_zero(dn, lm, offs, rewards, G, mask=mask, **opts)["loss"]
+        fd = (lu - ld) / (2 * h)
+        g = out["grad"][t]
+        if opts.get("flags", 0) & (oracle.TIS | oracle.TOKEN_GATE | oracle.SEQ_GATE):
+            # the modified weight is a coefficient of grad log pi: d/dlog pi of w_hat is
+            # w_hat where it tracks w, 0 where it is capped or gated
+            capped = "tis_cap" in opts and w > opts["tis_cap"]
+            if capped:
+                assert abs(fd) < 1e-9, (t, fd)
+                assert abs(g - out["grad"][t]) == 0.0
+                checked += 1
+                continue
+        assert abs(fd - g) <= 1e-6 * max(abs(g), 1e-3), (t, fd, g)
+        checked += 1
+    assert checked > lp.size // 2
+
+
+def test_reinforce_zero_tis_and_gate_limits():
+    lp, lm, offs, rewards, G, mask = _rz_case(42)
+    plain = oracle.reinforce_zero(lp, lm, offs, rewards, G, mask=mask)
+    big = oracle.reinforce_zero(lp, lm, offs, rewards, G, mask=mask, flags=oracle.TIS,
+                                tis_cap=1e30)
+    assert big["loss"] == plain["loss"] and np.array_equal(big["grad"], plain["grad"])
+    open_gates = oracle.reinforce_zero(lp, lm, offs, rewards, G, mask=mask,
+                                       flags=oracle.TOKEN_GATE | oracle.SEQ_GATE)
+    assert open_gates["loss"] == plain["loss"] and open_gates["kept"].all()
+    # a cap below every weight makes w_hat constant, so the centred advantages cancel
+    mask[offs[:-1]] = True
+    tiny = oracle.reinforce_zero(lp, lm, offs, rewards, G, mask=mask, flags=oracle.TIS,
+                                 tis_cap=1e-3)
+    assert np.all(tiny["w_hat"][mask] == 1e-3) and abs(tiny["loss"]) < 1e-15
+
+
+def test_reinforce_zero_sequence_gate_drops_whole_responses():
+    # response 0: four tokens with d = 1/4 (log-ratio 1); response 1: d = 1/8 twice (1/4)
+    lm = np.full(8, -2.0, dtype=np.float32)
+    lp = lm + np.array([0.25] * 4 + [0.125] * 2 + [0, 0], dtype=np.float32)
+    offs, rewards = [0, 4, 6, 7, 8], [1, 0, 1, 0]
+    out = oracle.reinforce_zero(lp, lm, offs, rewards, 2, flags=oracle.SEQ_GATE,
+                                seq_log_lo=-0.9, seq_log_hi=0.9)
+    assert out["kept"].tolist() == [False, True, True, True]
+    assert out["seq_logratio"][0] == 1.0 and out["seq_logratio"][1] == 0.25
+    assert np.all(out["w_hat"][:4] == 0) and np.all(out["grad"][:4] == 0)
+    # the same as a plain loss with response 0 masked out (T_0 = 0 adds nothing)
+    masked = oracle.reinforce_zero(lp, lm, offs, rewards, 2, mask=[0] * 4 + [1] * 4)
+    assert out["loss"] == masked["loss"]
+    assert abs(out["loss"] - (-(1 / 4) * (-0.5 * math.exp(0.125) + 0.5 - 0.5))) < 1e-7
+
+
+def test_reinforce_zero_token_gate_and_empty_response():
+    lm = np.full(6, -1.0, dtype=np.float32)
+    lp = lm + np.array([0.5, 0.0, -0.5, 0.0, 0.0, 0.0], dtype=np.float32)
+    out = oracle.reinforce_zero(lp, lm, [0, 3, 3, 6, 6], [1, 0, 0, 1], 2,
+                                flags=oracle.TOKEN_GATE, token_log_lo=-0.25, token_log_hi=0.25)
+    assert out["w_hat"].tolist() == [0.0, 1.0, 0.0, 1.0, 1.0, 1.0]
+    # responses 1 and 3 are empty: they add nothing and give no NaN
+    assert np.isfinite(out["loss"]) and np.isfinite(out["grad"]).all()
+    assert abs(out["loss"] - (-(1 / 4) * (0.5 * (1 / 3) - 0.5 * 1.0))) < 1e-15
+
+
 # ----------------------------------------------------------------- planted mistakes
 MUTATIONS = [
     # (description, original text, mutated text)
@@ -279,6 +456,17 @@ MUTATIONS = [
      "double d = (double)logp_mu[t] - (double)logp_pi[t];"),
     ("term drops the -d", "term[t] = expm1(d) - d;", "term[t] = expm1(d);"),
     ("leaf boundary off by one", "k < (int64_t)(j + 1) * L; ++k", "k <= (int64_t)(j + 1) * L && k < H; ++k"),
+    ("std with n - 1", "out[2] = sqrt(ss / (double)n);", "out[2] = sqrt(ss / (double)(n - 1));"),
+    ("k3 drops the -d", "k3 += expm1(d) - d;", "k3 += expm1(d);"),
+    ("advantage not centred", "double A = (double)rewards[i] - gsum / (double)G;",
+     "double A = (double)rewards[i];"),
+    ("groups strided", "int64_t g0 = (i / G) * G;", "int64_t g0 = (i % G) * G;"),
+    ("token mean over masked tokens too", "if (n > 0) total += A * wsum / (double)n;",
+     "if (n > 0) total += A * wsum / (double)(offs[i + 1] - offs[i]);"),
+    ("gradient sign", "double coef = n > 0 ? -A /", "double coef = n > 0 ? A /"),
+    ("TIS as a floor", "wh > tis_cap) wh = tis_cap;", "wh < tis_cap) wh = tis_cap;"),
+    ("sequence gate on the last token only", "lr += (double)logp_pi[t] - (double)logp_mu[t];",
+     "lr = (double)logp_pi[t] - (double)logp_mu[t];"),
 ]
 
 
@@ -306,7 +494,16 @@ def test_pins_catch_planted_mistake(tmp_path, monkeypatch, golden_dir, desc, ori
             lambda: test_tree_fp32_golden(golden_dir),
             lambda: test_importance_weights_golden(golden_dir),
             lambda: [test_leaf_sums_exact(n) for n in (2, 4, 8)],
-            test_d3_small_gap_series]
+            test_d3_small_gap_series,
+            test_acceptance_stats_constant_gap_closed_form,
+            test_acceptance_stats_against_library_statistics,
+            test_reinforce_zero_worked_example,
+            test_reinforce_zero_equal_policies_give_zero_loss,
+            lambda: [test_reinforce_zero_gradient_is_the_derivative_of_the_loss(o) for o in (
+                dict(), dict(flags=oracle.TIS, tis_cap=1.03))],
+            test_reinforce_zero_tis_and_gate_limits,
+            test_reinforce_zero_sequence_gate_drops_whole_responses,
+            test_reinforce_zero_token_gate_and_empty_response]
     failed = 0
     for pin in pins:
         try:
