@@ -33,6 +33,16 @@ class LpConfig(ctypes.Structure):
                 ("tp_slices", ctypes.c_int32), ("max_tokens", ctypes.c_int64)]
 
 
+class LpRzOptions(ctypes.Structure):
+    _fields_ = [("flags", ctypes.c_int32), ("tis_cap", ctypes.c_float),
+                ("token_log_lo", ctypes.c_float), ("token_log_hi", ctypes.c_float),
+                ("seq_log_lo", ctypes.c_double), ("seq_log_hi", ctypes.c_double)]
+
+
+LP_RZ_TIS, LP_RZ_TOKEN_GATE, LP_RZ_SEQ_GATE = 1, 2, 4
+LP_STAT_MAX_ABS, LP_STAT_MEAN_ABS, LP_STAT_STD_ABS, LP_STAT_K3, LP_STAT_N_VALID = range(5)
+LP_STAT_COUNT = 5
+
 SIGNATURES = {
     "lp_init": (ctypes.c_int, [ctypes.POINTER(LpConfig), _p, _p, ctypes.POINTER(_p)]),
     "lp_logprobs": (ctypes.c_int, [_p, _p, _i64, _p, _i64, _p, _p, ctypes.c_int, _p]),
@@ -41,6 +51,9 @@ SIGNATURES = {
     "lp_logprobs_from_partials": (ctypes.c_int, [_p, _p, _i32, _i64, _i64, _p, _i64, _p, _p, _p]),
     "lp_importance_weights": (ctypes.c_int, [_p, _p, _p, _p, _i64, _p, _p, _p, _p]),
     "lp_importance_weights_host": (ctypes.c_int, [_p, _p, _p, _p, _i64, _p, _p, _p, _p]),
+    "lp_acceptance_stats": (ctypes.c_int, [_p, _p, _p, _p, _i64, _p, _p]),
+    "lp_reinforce_zero": (ctypes.c_int, [_p, _p, _p, _p, _i64, _p, _i64, _p, _i32,
+                                         ctypes.POINTER(LpRzOptions), _p, _p, _p, _p, _p, _p]),
     "lp_profile_enable": (ctypes.c_int, [_p, ctypes.c_int]),
     "lp_profile_read": (ctypes.c_int, [_p, ctypes.POINTER(ctypes.c_double),
                                        ctypes.POINTER(ctypes.c_int32)]),

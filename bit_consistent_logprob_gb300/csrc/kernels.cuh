@@ -700,23 +700,18 @@ __device__ __forceinline__ void block_tree_f64(double* a, int n) {
     }
 }
 
-// One block: the tree over all block partials, taken in aligned chunks of kIsChunk
-// (each chunk is a whole subtree of the level-wise tree, so the result is the same
-// as one tree over every block), then D3 = sum / n_valid.
-static __global__ void __launch_bounds__(1024) is_final_kernel(const double* blk_sum,
-                                                        const long long* blk_cnt, int num_blocks,
-                                                        double* out_d3, int64_t* out_nvalid) {
-    __shared__ double a[kIsChunk];
-    __shared__ double chunk_res[kIsChunk];
-    __shared__ long long cnt_part[1024];
-    long long cnt = 0;
-    for (int i = threadIdx.x; i < num_blocks; i += blockDim.x) cnt += blk_cnt[i];
-    cnt_part[threadIdx.x] = cnt;
-    const int num_chunks = (num_blocks + kIsChunk - 1) / kIsChunk;
+// The level-wise pairwise tree over n <= 2^21 block partials, taken in aligned chunks of
+// kIsChunk (each chunk is a whole subtree of the level-wise tree, so the result is the
+// same as one tree over every partial).  Called by a whole block of 1024 threads; `a`
+// holds kIsChunk and `chunk_res` 1024 doubles of shared memory.  The result is returned
+// to every thread.
+__device__ __forceinline__ double tree_over_partials(const double* src, int n, double* a,
+                                                     double* chunk_res) {
+    const int num_chunks = (n + kIsChunk - 1) / kIsChunk;
     for (int ch = 0; ch < num_chunks; ++ch) {
         const int lo = ch * kIsChunk;
-        const int len = min(kIsChunk, num_blocks - lo);
-        for (int i = threadIdx.x; i < len; i += blockDim.x) a[i] = blk_sum[lo + i];
+        const int len = min(kIsChunk, n - lo);
+        for (int i = threadIdx.x; i < len; i += blockDim.x) a[i] = src[lo + i];
         __syncthreads();
         block_tree_f64(a, len);
         if (threadIdx.x == 0) chunk_res[ch] = a[0];
@@ -724,10 +719,37 @@ static __global__ void __launch_bounds__(1024) is_final_kernel(const double* blk
     }
     if (num_chunks > 0) block_tree_f64(chunk_res, num_chunks);
     __syncthreads();
+    const double r = num_chunks > 0 ? chunk_res[0] : 0.0;
+    __syncthreads();
+    return r;
+}
+
+// Exact sum of n counts (integer adds; the order does not matter).  Whole block of 1024.
+__device__ __forceinline__ long long block_count_sum(const long long* src, int n,
+                                                     long long* part) {
+    long long c = 0;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) c += src[i];
+    part[threadIdx.x] = c;
+    __syncthreads();
+    for (int w = blockDim.x >> 1; w >= 1; w >>= 1) {
+        if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+        __syncthreads();
+    }
+    const long long r = part[0];
+    __syncthreads();
+    return r;
+}
+
+// One block: D3 = (tree over the block sums) / n_valid.
+static __global__ void __launch_bounds__(1024) is_final_kernel(const double* blk_sum,
+                                                        const long long* blk_cnt, int num_blocks,
+                                                        double* out_d3, int64_t* out_nvalid) {
+    __shared__ double a[kIsChunk];
+    __shared__ double chunk_res[1024];
+    __shared__ long long cnt_part[1024];
+    const long long total = block_count_sum(blk_cnt, num_blocks, cnt_part);
+    const double sum = tree_over_partials(blk_sum, num_blocks, a, chunk_res);
     if (threadIdx.x == 0) {
-        long long total = 0;
-        for (int i = 0; i < 1024; ++i) total += cnt_part[i];
-        const double sum = num_chunks > 0 ? chunk_res[0] : 0.0;
         *out_d3 = total > 0 ? __ddiv_rn(sum, static_cast<double>(total)) : 0.0;
         if (out_nvalid) *out_nvalid = total;
     }

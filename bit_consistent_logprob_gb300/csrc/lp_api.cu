@@ -17,6 +17,7 @@
 
 #include "kernels.cuh"
 #include "lp.h"
+#include "rl_kernels.cuh"
 
 namespace {
 
@@ -102,6 +103,8 @@ struct lp_handle {
     int* status = nullptr;        // sticky status word
     double* blk_sum = nullptr;    // [max_is_blocks]
     long long* blk_cnt = nullptr; // [max_is_blocks]
+    double* stat_blk = nullptr;   // [2][max_is_blocks]: sum |d|^2 and sum k3 per block
+    float* stat_max = nullptr;    // [max_is_blocks]: max |d| per block
     int64_t max_is_blocks = 0;
     float* tp_parts = nullptr;    // [tp_slices][max_tokens][ldp] slice outputs
     float* tp_gather = nullptr;   // same shape: the "transported" copy
@@ -360,6 +363,8 @@ void lp_free(lp_handle* h) {
     cudaFree(h->status);
     cudaFree(h->blk_sum);
     cudaFree(h->blk_cnt);
+    cudaFree(h->stat_blk);
+    cudaFree(h->stat_max);
     cudaFree(h->tp_parts);
     cudaFree(h->tp_gather);
     cudaFree(h->x_stage);
@@ -441,6 +446,10 @@ int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out) 
                     "blk_sum")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->blk_cnt), sizeof(long long) * h->max_is_blocks,
                     "blk_cnt")) ||
+        (rc = alloc(reinterpret_cast<void**>(&h->stat_blk), 2 * sizeof(double) * h->max_is_blocks,
+                    "stat_blk")) ||
+        (rc = alloc(reinterpret_cast<void**>(&h->stat_max), sizeof(float) * h->max_is_blocks,
+                    "stat_max")) ||
         (rc = alloc(&h->x_stage, sizeof(uint16_t) * static_cast<size_t>(mt) * cfg->H, "x_stage")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->ids_stage), sizeof(int32_t) * mt, "ids_stage")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->logp_stage), sizeof(float) * mt, "logp_stage")) ||
@@ -615,6 +624,98 @@ int lp_importance_weights(lp_handle* h, const float* logp_pi, const float* logp_
     return LP_OK;
 }
 
+int lp_acceptance_stats(lp_handle* h, const float* logp_a, const float* logp_b,
+                        const uint8_t* mask, int64_t T, double* out_stats, void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    if (T < 0 || T > kMaxIsTokens) return fail(LP_ERR_INVALID_ARG, "T must be in [0, 2^31)");
+    if (out_stats == nullptr) return fail(LP_ERR_INVALID_ARG, "out_stats must not be NULL");
+    if (T > 0 && (logp_a == nullptr || logp_b == nullptr))
+        return fail(LP_ERR_INVALID_ARG, "logp_a and logp_b must not be NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    h->last_stream = st;
+    h->last_launches = 0;
+    const int64_t nblk = ceil_div(T, lp::kIsBlock);
+    lp::StatsParams p{logp_a, logp_b, mask, T, h->blk_sum, h->stat_blk,
+                      h->stat_blk + h->max_is_blocks, h->stat_max, h->blk_cnt};
+    if (nblk > 0) {
+        lp::stats_block_kernel<<<static_cast<unsigned>(nblk), lp::kIsThreads, 0, st>>>(p);
+        LP_CUDA(cudaGetLastError(), "stats_block_kernel launch");
+        ++h->last_launches;
+    }
+    lp::stats_final_kernel<<<1, 1024, 0, st>>>(p, static_cast<int>(nblk), out_stats);
+    LP_CUDA(cudaGetLastError(), "stats_final_kernel launch");
+    ++h->last_launches;
+    return LP_OK;
+}
+
+int lp_reinforce_zero(lp_handle* h, const float* logp_pi, const float* logp_mu,
+                      const uint8_t* mask, int64_t T, const int64_t* seq_offsets, int64_t B,
+                      const float* rewards, int32_t group_size, const lp_rz_options* opt,
+                      float* out_w_hat, float* out_grad, double* out_adv, double* out_loss,
+                      int64_t* out_n_kept, void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    if (T < 0 || T > kMaxIsTokens) return fail(LP_ERR_INVALID_ARG, "T must be in [0, 2^31)");
+    if (B < 0 || B > h->max_is_blocks)
+        return fail(LP_ERR_INVALID_ARG, "B must be in [0, %lld]", (long long)h->max_is_blocks);
+    if (group_size < 1 || (B > 0 && B % group_size != 0))
+        return fail(LP_ERR_INVALID_ARG, "group_size must be >= 1 and divide B");
+    if (out_loss == nullptr) return fail(LP_ERR_INVALID_ARG, "out_loss must not be NULL");
+    if (B > 0 && (seq_offsets == nullptr || rewards == nullptr))
+        return fail(LP_ERR_INVALID_ARG, "seq_offsets and rewards must not be NULL");
+    if (T > 0 && (logp_pi == nullptr || logp_mu == nullptr || out_grad == nullptr))
+        return fail(LP_ERR_INVALID_ARG, "logp_pi, logp_mu and out_grad must not be NULL");
+    lp::RzParams p{};
+    p.logp_pi = logp_pi;
+    p.logp_mu = logp_mu;
+    p.mask = mask;
+    p.T = T;
+    p.offs = seq_offsets;
+    p.B = B;
+    p.rewards = rewards;
+    p.G = group_size;
+    p.flags = 0;
+    p.tis_cap = INFINITY;
+    p.tok_lo = -INFINITY;
+    p.tok_hi = INFINITY;
+    p.seq_lo = -INFINITY;
+    p.seq_hi = INFINITY;
+    if (opt != nullptr) {
+        if (opt->flags & ~(LP_RZ_TIS | LP_RZ_TOKEN_GATE | LP_RZ_SEQ_GATE))
+            return fail(LP_ERR_INVALID_ARG, "unknown flag in lp_rz_options.flags");
+        if ((opt->flags & LP_RZ_TIS) && !(opt->tis_cap > 0.0f))
+            return fail(LP_ERR_INVALID_ARG, "tis_cap must be > 0");
+        if ((opt->flags & LP_RZ_TOKEN_GATE) && !(opt->token_log_lo <= opt->token_log_hi))
+            return fail(LP_ERR_INVALID_ARG, "token gate needs token_log_lo <= token_log_hi");
+        if ((opt->flags & LP_RZ_SEQ_GATE) && !(opt->seq_log_lo <= opt->seq_log_hi))
+            return fail(LP_ERR_INVALID_ARG, "sequence gate needs seq_log_lo <= seq_log_hi");
+        p.flags = opt->flags;
+        p.tis_cap = opt->tis_cap;
+        p.tok_lo = opt->token_log_lo;
+        p.tok_hi = opt->token_log_hi;
+        p.seq_lo = opt->seq_log_lo;
+        p.seq_hi = opt->seq_log_hi;
+    }
+    p.out_w_hat = out_w_hat;
+    p.out_grad = out_grad;
+    p.out_adv = out_adv;
+    p.seq_term = h->blk_sum;
+    p.seq_kept = h->blk_cnt;
+    p.status = h->status;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    h->last_stream = st;
+    h->last_launches = 0;
+    if (B > 0) {
+        lp::rz_seq_kernel<<<static_cast<unsigned>(B), lp::kRzThreads, 0, st>>>(p);
+        LP_CUDA(cudaGetLastError(), "rz_seq_kernel launch");
+        ++h->last_launches;
+    }
+    lp::rz_final_kernel<<<1, 1024, 0, st>>>(h->blk_sum, h->blk_cnt, static_cast<int>(B), out_loss,
+                                            out_n_kept);
+    LP_CUDA(cudaGetLastError(), "rz_final_kernel launch");
+    ++h->last_launches;
+    return LP_OK;
+}
+
 int lp_importance_weights_host(lp_handle* h, const float* logp_pi, const float* logp_mu,
                                const uint8_t* mask, int64_t T, float* out_w, double* out_d3,
                                int64_t* out_nvalid, void* stream) {
@@ -702,6 +803,9 @@ int lp_check(lp_handle* h) {
         return fail(LP_ERR_TIMEOUT, "a device-side bounded wait expired; the kernel returned early");
     if (st & lp::kStatusBadId)
         return fail(LP_ERR_INVALID_ARG, "a sampled id was outside [0, V); its logprob is NaN");
+    if (st & lp::kStatusBadOffsets)
+        return fail(LP_ERR_INVALID_ARG,
+                    "a response's token range [offs[i], offs[i+1]) was not inside [0, T)");
     return LP_OK;
 }
 

@@ -157,6 +157,73 @@ class Engine:
             _ptr(out_nvalid), _stream_ptr(stream)))
         return out_w, out_d3, out_nvalid
 
+    def acceptance_stats(self, logp_a: torch.Tensor, logp_b: torch.Tensor,
+                         mask: torch.Tensor = None, out: torch.Tensor = None, stream=None):
+        """fp64 [5] on the device: max, mean and std of |a - b|, k3, n_valid (no sync)."""
+        _require(logp_a, "logp_a", torch.float32, 1)
+        _require(logp_b, "logp_b", torch.float32, 1)
+        T = int(logp_a.shape[0])
+        if logp_b.shape[0] != T:
+            raise ValueError("logp_a and logp_b must have the same length")
+        if mask is not None:
+            _require(mask, "mask", torch.uint8, 1)
+            if mask.shape[0] != T:
+                raise ValueError("mask must have length T")
+        if out is None:
+            out = torch.empty(_native.LP_STAT_COUNT, dtype=torch.float64, device=logp_a.device)
+        _native.check(self._lib.lp_acceptance_stats(
+            self._h, _ptr(logp_a), _ptr(logp_b), _ptr(mask), T, _ptr(out), _stream_ptr(stream)))
+        return out
+
+    def reinforce_zero(self, logp_pi: torch.Tensor, logp_mu: torch.Tensor,
+                       seq_offsets: torch.Tensor, rewards: torch.Tensor, group_size: int,
+                       mask: torch.Tensor = None, tis_cap: float = None,
+                       token_gate: tuple = None, seq_gate: tuple = None,
+                       out_w_hat: torch.Tensor = None, out_grad: torch.Tensor = None,
+                       out_adv: torch.Tensor = None, stream=None):
+        """REINFORCE Zero loss over responses packed at ``seq_offsets`` ([B+1] int64).
+
+        tis_cap: TIS cap C (w_hat = min(w, C)); token_gate: (lo, hi) bounds on
+        d = log pi - log mu; seq_gate: (lo, hi) bounds on a response's sum of d.
+        Returns (loss fp64 [1], w_hat fp32 [T], grad fp32 [T] = dL/dlog pi,
+        adv fp64 [B], n_kept int64 [1]), all on the device, no sync."""
+        _require(logp_pi, "logp_pi", torch.float32, 1)
+        _require(logp_mu, "logp_mu", torch.float32, 1)
+        _require(seq_offsets, "seq_offsets", torch.int64, 1)
+        _require(rewards, "rewards", torch.float32, 1)
+        T = int(logp_pi.shape[0])
+        B = int(rewards.shape[0])
+        if logp_mu.shape[0] != T or seq_offsets.shape[0] != B + 1:
+            raise ValueError("need logp_mu of length T and seq_offsets of length B + 1")
+        if mask is not None:
+            _require(mask, "mask", torch.uint8, 1)
+            if mask.shape[0] != T:
+                raise ValueError("mask must have length T")
+        opt = _native.LpRzOptions()
+        if tis_cap is not None:
+            opt.flags |= _native.LP_RZ_TIS
+            opt.tis_cap = float(tis_cap)
+        if token_gate is not None:
+            opt.flags |= _native.LP_RZ_TOKEN_GATE
+            opt.token_log_lo, opt.token_log_hi = (float(v) for v in token_gate)
+        if seq_gate is not None:
+            opt.flags |= _native.LP_RZ_SEQ_GATE
+            opt.seq_log_lo, opt.seq_log_hi = (float(v) for v in seq_gate)
+        dev = logp_pi.device
+        if out_w_hat is None:
+            out_w_hat = torch.empty(T, dtype=torch.float32, device=dev)
+        if out_grad is None:
+            out_grad = torch.empty(T, dtype=torch.float32, device=dev)
+        if out_adv is None:
+            out_adv = torch.empty(B, dtype=torch.float64, device=dev)
+        loss = torch.empty(1, dtype=torch.float64, device=dev)
+        n_kept = torch.empty(1, dtype=torch.int64, device=dev)
+        _native.check(self._lib.lp_reinforce_zero(
+            self._h, _ptr(logp_pi), _ptr(logp_mu), _ptr(mask), T, _ptr(seq_offsets), B,
+            _ptr(rewards), int(group_size), ctypes.byref(opt), _ptr(out_w_hat), _ptr(out_grad),
+            _ptr(out_adv), _ptr(loss), _ptr(n_kept), _stream_ptr(stream)))
+        return loss, out_w_hat, out_grad, out_adv, n_kept
+
     def importance_weights_host(self, logp_pi: torch.Tensor, logp_mu: torch.Tensor,
                                 mask: torch.Tensor = None, out_w: torch.Tensor = None,
                                 stream=None):

@@ -130,3 +130,17 @@ def synthetic_is_inputs(T: int, seed: int, lag_std: float = 0.05, p_mask: float 
     logmu = logpi + torch.randn(T, generator=g, device=device, dtype=torch.float32) * lag_std
     mask = (torch.rand(T, generator=g, device=device) < p_mask).to(torch.uint8)
     return logpi.contiguous(), logmu.contiguous(), mask.contiguous()
+
+
+def response_batch(n_groups: int, group_size: int, lo: int, hi: int, seed: int,
+                   p_reward: float = 0.5):
+    """Packed responses for a group-sampled RL batch: lengths uniform in [lo, hi],
+    their int64 offsets [B+1] (response i holds tokens [offs[i], offs[i+1])), and 0/1
+    rewards drawn with probability p_reward.  CPU tensors."""
+    B = n_groups * group_size
+    lengths = packed_lengths(B, lo, hi, seed)
+    offs = torch.zeros(B + 1, dtype=torch.int64)
+    offs[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0)
+    g = generator(seed + 15485863, "cpu")
+    rewards = (torch.rand(B, generator=g) < p_reward).to(torch.float32)
+    return offs, rewards

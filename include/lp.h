@@ -183,6 +183,76 @@ LP_API int lp_importance_weights_host(lp_handle* h, const float* logp_pi, const 
                                       double* out_d3, int64_t* out_nvalid, void* stream);
 
 /*
+ * Acceptance statistics between two logprob vectors (vLLM blog "Finish RL training
+ * faster", section 2: acceptance asks the max, mean and std of the per-token difference
+ * over every valid sampled token to be 0; section 3.2: the k3 KL estimator r - 1 - log r).
+ *   logp_a, logp_b  device, fp32 [T]: learner (log pi) and rollout (log mu) logprobs.
+ *   mask            device, uint8 [T] (nonzero = valid), or NULL (all valid).
+ *   out_stats       device, double [LP_STAT_COUNT]:
+ *     [LP_STAT_MAX_ABS]   max |d| over valid tokens, d = fp32(logp_a - logp_b)
+ *     [LP_STAT_MEAN_ABS]  mean |d|
+ *     [LP_STAT_STD_ABS]   population std of |d|: sqrt(max(0, mean d^2 - mean^2))
+ *     [LP_STAT_K3]        mean of e^d - 1 - d (r = pi/mu); bit-equal to the D3 of
+ *                         lp_importance_weights on the same inputs
+ *     [LP_STAT_N_VALID]   number of valid tokens
+ *   Sums are fp64 over the same fixed tree of 1024-token blocks as D3.  A NaN |d| on a
+ *   valid token makes the max NaN (and the sums with it); no valid token gives all 0.
+ * T up to 2^31 - 1.  Uses the handle's block workspace: calls on one handle must be
+ * stream-ordered.
+ */
+enum { LP_STAT_MAX_ABS = 0, LP_STAT_MEAN_ABS, LP_STAT_STD_ABS, LP_STAT_K3, LP_STAT_N_VALID,
+       LP_STAT_COUNT };
+LP_API int lp_acceptance_stats(lp_handle* h, const float* logp_a, const float* logp_b,
+                               const uint8_t* mask, int64_t T, double* out_stats, void* stream);
+
+/*
+ * REINFORCE Zero loss (REINFORCE Zero summary, section 4) for B responses packed back to
+ * back, with the corrections the pages list beside it as options (vLLM blog, section 1:
+ * TIS truncates the ratio at an upper bound, MIS drops whole sequences whose ratio passes
+ * a threshold; REINFORCE Zero summary, results table: sequence and token gates):
+ *
+ *   L = -(1/B) sum_i (1/T_i) sum_t A_i w_hat_it,   dL/dlog pi_it = -(1/B)(1/T_i) A_i w_hat_it
+ *
+ *   w_it   = exp(d_it), d_it = fp32(logp_pi - logp_mu), unclipped (the plain recipe);
+ *   w_hat  = w, then 0 if LP_RZ_TOKEN_GATE and d is outside [token_log_lo, token_log_hi],
+ *            then min(., tis_cap) if LP_RZ_TIS, then 0 for the whole response if
+ *            LP_RZ_SEQ_GATE and its log-ratio sum_t d_it (fp64, valid tokens) is outside
+ *            [seq_log_lo, seq_log_hi]; masked tokens get w_hat = 0.  The modified weight
+ *            is the coefficient of grad log pi, so the gradient uses w_hat in every mode;
+ *   A_i    = R_i - mean of R over the response's group (groups of group_size consecutive
+ *            responses), fp64;
+ *   T_i    = valid tokens of response i; a response with T_i = 0 adds 0.
+ *
+ *   logp_pi, logp_mu  device, fp32 [T];   mask  device, uint8 [T] or NULL (all valid).
+ *   seq_offsets       device, int64 [B+1]: response i holds tokens [offs[i], offs[i+1]);
+ *                     expected offs[0] = 0 and offs[B] = T.  A range outside [0, T) sets
+ *                     the sticky status (lp_check: LP_ERR_INVALID_ARG) and is treated as
+ *                     empty; tokens outside every range are not written.
+ *   rewards           device, fp32 [B];  group_size >= 1 dividing B;  B <= 2^21.
+ *   opt               host, or NULL for the plain recipe.
+ *   out_w_hat         device, fp32 [T] or NULL;  out_grad  device, fp32 [T].
+ *   out_adv           device, double [B] or NULL: A_i.
+ *   out_loss          device, one double: L (sum over responses by a fixed fp64 tree).
+ *   out_n_kept        device, one int64 or NULL: responses that passed the sequence gate.
+ * Per-token outputs depend only on the token's response and its group, never on the
+ * rest of the batch or the launch.  Uses the handle's block workspace: calls on one handle
+ * must be stream-ordered.
+ */
+enum { LP_RZ_TIS = 1, LP_RZ_TOKEN_GATE = 2, LP_RZ_SEQ_GATE = 4 };
+typedef struct lp_rz_options {
+    int32_t flags;                    /* OR of LP_RZ_*; 0 = unclipped token-level IS */
+    float tis_cap;                    /* LP_RZ_TIS: cap C > 0 */
+    float token_log_lo, token_log_hi; /* LP_RZ_TOKEN_GATE: bounds on d (fp32) */
+    double seq_log_lo, seq_log_hi;    /* LP_RZ_SEQ_GATE: bounds on sum_t d (fp64) */
+} lp_rz_options;
+LP_API int lp_reinforce_zero(lp_handle* h, const float* logp_pi, const float* logp_mu,
+                             const uint8_t* mask, int64_t T, const int64_t* seq_offsets,
+                             int64_t B, const float* rewards, int32_t group_size,
+                             const lp_rz_options* opt, float* out_w_hat, float* out_grad,
+                             double* out_adv, double* out_loss, int64_t* out_n_kept,
+                             void* stream);
+
+/*
  * Kernel timing for profiling.  While enabled, every leaf-GEMM launch (the dominant
  * kernel) is bracketed by a pair of CUDA events recorded on the launch stream (at
  * most 4096 pairs are kept).  lp_profile_read synchronises, returns the summed
