@@ -59,6 +59,9 @@ def _load():
         lib.oracle_tree_fp32.restype = ctypes.c_float
         lib.oracle_tree_fp32_many.argtypes = [p, i32, i64, p]
         lib.oracle_acceptance_stats.argtypes = [p, p, p, i64, p]
+        lib.oracle_entropy.argtypes = [p, i64, p, i64, i64, p, i64, p]
+        lib.oracle_logprobs_f64.argtypes = [p, p, p, i64, i64, i64, p]
+        lib.oracle_logprob_grad.argtypes = [p, p, p, p, i64, i64, i64, p, p, p]
         lib.oracle_reinforce_zero.argtypes = [p, p, p, p, i64, p, ctypes.c_int, ctypes.c_int,
                                               ctypes.c_double, ctypes.c_float, ctypes.c_float,
                                               ctypes.c_double, ctypes.c_double,
@@ -250,3 +253,44 @@ def reinforce_zero(logp_pi, logp_mu, offsets, rewards, group_size, mask=None, fl
                                   _ptr(kept), _ptr(loss))
     return dict(loss=float(loss[0]), w_hat=w_hat, grad=grad, adv=adv, seq_logratio=slr,
                 kept=kept.astype(bool))
+
+
+def entropy(X, W, rows=None) -> np.ndarray:
+    """Softmax entropy -sum_v p log p of the listed rows (fp64)."""
+    X, W = _u16_2d(X), _u16_2d(W)
+    Xc, Wc = np.ascontiguousarray(X), np.ascontiguousarray(W)
+    T, H = Xc.shape
+    V = Wc.shape[0]
+    r = _rows_arg(rows, T)
+    out = np.empty(r.size, dtype=np.float64)
+    _load().oracle_entropy(_ptr(Xc), H, _ptr(Wc), H, V, _ptr(r), r.size, _ptr(out))
+    return out
+
+
+def logprobs_f64(X, W, ids) -> np.ndarray:
+    """Sampled-token logprobs of real-valued (fp64) X [T, H] and W [V, H]."""
+    Xd = np.ascontiguousarray(np.asarray(X, dtype=np.float64))
+    Wd = np.ascontiguousarray(np.asarray(W, dtype=np.float64))
+    T, H = Xd.shape
+    V = Wd.shape[0]
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    out = np.empty(T, dtype=np.float64)
+    _load().oracle_logprobs_f64(_ptr(Xd), _ptr(Wd), _ptr(ids), T, H, V, _ptr(out))
+    return out
+
+
+def logprob_grad(X, W, ids, g):
+    """Gradient of sum_t g_t logp_t: returns (dX [T,H], dW [V,H], dl [T,V]) in fp64."""
+    X, W = _u16_2d(X), _u16_2d(W)
+    Xc, Wc = np.ascontiguousarray(X), np.ascontiguousarray(W)
+    T, H = Xc.shape
+    V = Wc.shape[0]
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    g = np.ascontiguousarray(np.asarray(g, dtype=np.float64))
+    assert ids.shape == (T,) and g.shape == (T,)
+    dX = np.empty((T, H), dtype=np.float64)
+    dW = np.empty((V, H), dtype=np.float64)
+    dl = np.empty((T, V), dtype=np.float64)
+    _load().oracle_logprob_grad(_ptr(Xc), _ptr(Wc), _ptr(ids), _ptr(g), T, H, V, _ptr(dX),
+                                _ptr(dW), _ptr(dl))
+    return dX, dW, dl

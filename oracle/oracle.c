@@ -38,6 +38,18 @@
  *      section 3).  log w is taken as exactly d = log pi - log mu, so the term
  *      is expm1(d) - d; it is 0 at w = 1.  No valid token gives D3 = 0.
  *
+ *  - oracle_entropy: the entropy of each row's softmax, H = -sum_v p_v log p_v
+ *      with log p = z - logZ (the actor entropy the vLLM blog tracks beside the
+ *      train-inference KL, section 3.2 results).
+ *
+ *  - oracle_logprob_grad: the gradient of sum_t g_t logp_t with respect to X
+ *      and W, from d logp_t / d z_tv = 1[v = y_t] - p_tv (the standard
+ *      log-softmax derivative; the pages' recipe differentiates a training
+ *      graph beside the inference forward, vLLM blog section 3.1):
+ *        dl[t,v] = g_t (1[v = y_t] - p_tv), dX = dl W, dW = dl^T X.
+ *      oracle_logprobs_f64 is the logprob definition on real-valued (fp64)
+ *      inputs, used to check the gradient by finite differences.
+ *
  *  - oracle_acceptance_stats: over the valid tokens, the max, mean and
  *      population standard deviation of |a - b| between two logprob vectors,
  *      and the k3 KL estimate mean(r - 1 - log r) with r = exp(a - b) (vLLM
@@ -299,4 +311,77 @@ void oracle_reinforce_zero(const float* logp_pi, const float* logp_mu, const uin
         if (n > 0) total += A * wsum / (double)n;
     }
     *loss = B > 0 ? -total / (double)B : 0.0;
+}
+
+/* Entropy of the softmax of the listed rows: out[r] = -sum_v p log p, log p = z - logZ. */
+void oracle_entropy(const uint16_t* X, int64_t ldx, const uint16_t* W, int64_t H, int64_t V,
+                    const int64_t* rows, int64_t nrows, double* out) {
+#pragma omp parallel
+    {
+        double* z = (double*)malloc((size_t)V * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < nrows; ++r) {
+            const uint16_t* xrow = X + rows[r] * ldx;
+            for (int64_t v = 0; v < V; ++v) z[v] = logit_f64(xrow, W + v * H, H);
+            double lz = log_partition(z, V);
+            double h = 0.0;
+            for (int64_t v = 0; v < V; ++v) {
+                double lp = z[v] - lz;
+                double p = exp(lp);
+                if (p > 0.0) h -= p * lp;
+            }
+            out[r] = h;
+        }
+        free(z);
+    }
+}
+
+/* Sampled-token logprobs of fp64 inputs X [T, H], W [V, H] (plain definition). */
+void oracle_logprobs_f64(const double* X, const double* W, const int32_t* ids, int64_t T,
+                         int64_t H, int64_t V, double* logp) {
+    double* z = (double*)malloc((size_t)V * sizeof(double));
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t v = 0; v < V; ++v) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < H; ++k) acc += X[t * H + k] * W[v * H + k];
+            z[v] = acc;
+        }
+        double lz = log_partition(z, V);
+        int32_t y = ids[t];
+        logp[t] = (y >= 0 && (int64_t)y < V) ? z[y] - lz : NAN;
+    }
+    free(z);
+}
+
+/* Gradient of L = sum_t g_t logp_t: dX [T, H] and dW [V, H] (fp64; X, W bf16 bits). */
+void oracle_logprob_grad(const uint16_t* X, const uint16_t* W, const int32_t* ids,
+                         const double* g, int64_t T, int64_t H, int64_t V, double* dX,
+                         double* dW, double* dl /* [T, V] */) {
+#pragma omp parallel
+    {
+        double* z = (double*)malloc((size_t)V * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < T; ++t) {
+            for (int64_t v = 0; v < V; ++v) z[v] = logit_f64(X + t * H, W + v * H, H);
+            double lz = log_partition(z, V);
+            for (int64_t v = 0; v < V; ++v) {
+                double onehot = (v == (int64_t)ids[t]) ? 1.0 : 0.0;
+                dl[t * V + v] = g[t] * (onehot - exp(z[v] - lz));
+            }
+            for (int64_t k = 0; k < H; ++k) {
+                double acc = 0.0;
+                for (int64_t v = 0; v < V; ++v) acc += dl[t * V + v] * bf16_to_f64(W[v * H + k]);
+                dX[t * H + k] = acc;
+            }
+        }
+        free(z);
+    }
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t v = 0; v < V; ++v) {
+        for (int64_t k = 0; k < H; ++k) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < T; ++t) acc += dl[t * V + v] * bf16_to_f64(X[t * H + k]);
+            dW[v * H + k] = acc;
+        }
+    }
 }

@@ -444,6 +444,89 @@ def test_reinforce_zero_token_gate_and_empty_response():
     assert abs(out["loss"] - (-(1 / 4) * (0.5 * (1 / 3) - 0.5 * 1.0))) < 1e-15
 
 
+# ----------------------------------------------------------------- entropy
+def test_entropy_closed_forms():
+    # uniform logits: log V; two tokens: the binary entropy of sigmoid(z_1 - z_0)
+    V, H = 1000, 16
+    X = rand_bf16((3, H), 50)
+    W = np.repeat(rand_bf16((1, H), 51), V, axis=0)
+    np.testing.assert_allclose(oracle.entropy(X, W), math.log(V), rtol=0, atol=1e-12)
+    X = rand_bf16((5, 6), 52)
+    W = rand_bf16((2, 6), 53, 2.0)
+    ex = exact_logits(X, W)
+    ent = oracle.entropy(X, W)
+    for t in range(5):
+        p = 1.0 / (1.0 + math.exp(float(ex[t][0] - ex[t][1])))
+        want = -(p * math.log(p) + (1 - p) * math.log1p(-p))
+        assert ent[t] == pytest.approx(want, abs=1e-13)
+
+
+def test_entropy_bounds_and_decimal_brute_force():
+    X = rand_bf16((3, 8), 54)
+    W = rand_bf16((11, 8), 55, 3.0)
+    ent = oracle.entropy(X, W)
+    ex = exact_logits(X, W)
+    for t in range(3):
+        zs = [dec(z) for z in ex[t]]
+        total = sum((z.exp() for z in zs), Decimal(0))
+        lz = total.ln()
+        want = -sum(((z - lz).exp() * (z - lz) for z in zs), Decimal(0))
+        assert ent[t] == pytest.approx(float(want), abs=1e-14)
+        assert 0.0 <= ent[t] <= math.log(11) + 1e-15
+    # one dominant logit: the entropy vanishes like 40 * 3 e^-40
+    X1 = f32_to_bf16_bits(np.ones((1, 1)))
+    W1 = f32_to_bf16_bits(np.array([[40.0], [0.0], [0.0], [0.0]]))
+    assert oracle.entropy(X1, W1)[0] == pytest.approx(41 * 3 * math.exp(-40.0), rel=1e-6)
+
+
+# ----------------------------------------------------------------- logprob gradient
+def test_logprobs_f64_matches_the_bf16_path():
+    X = rand_bf16((6, 24), 56)
+    W = rand_bf16((37, 24), 57)
+    ids = np.random.default_rng(58).integers(0, 37, 6).astype(np.int32)
+    lp, _ = oracle.logprobs(X, W, ids)
+    Xd = np.array([[float(bits_to_fraction(b)) for b in row] for row in X])
+    Wd = np.array([[float(bits_to_fraction(b)) for b in row] for row in W])
+    np.testing.assert_allclose(oracle.logprobs_f64(Xd, Wd, ids), lp, rtol=0, atol=1e-13)
+
+
+def test_logprob_grad_is_the_derivative():
+    T, H, V = 3, 5, 7
+    X = rand_bf16((T, H), 59)
+    W = rand_bf16((V, H), 60, 1.5)
+    ids = np.array([0, 6, 3], dtype=np.int32)
+    g = np.array([0.7, -1.3, 2.0])
+    dX, dW, dl = oracle.logprob_grad(X, W, ids, g)
+    Xd = np.array([[float(bits_to_fraction(b)) for b in row] for row in X])
+    Wd = np.array([[float(bits_to_fraction(b)) for b in row] for row in W])
+    L = lambda Xv, Wv: float(np.dot(g, oracle.logprobs_f64(Xv, Wv, ids)))  # noqa: E731
+    h = 1e-6
+    for t in range(T):
+        for k in range(H):
+            up, dn = Xd.copy(), Xd.copy()
+            up[t, k] += h
+            dn[t, k] -= h
+            assert (L(up, Wd) - L(dn, Wd)) / (2 * h) == pytest.approx(dX[t, k], abs=1e-8)
+    for v in range(V):
+        for k in range(H):
+            up, dn = Wd.copy(), Wd.copy()
+            up[v, k] += h
+            dn[v, k] -= h
+            assert (L(Xd, up) - L(Xd, dn)) / (2 * h) == pytest.approx(dW[v, k], abs=1e-8)
+    # each row of dl sums to 0 (probabilities sum to 1), so the columns of dW sum to 0
+    np.testing.assert_allclose(dl.sum(axis=1), 0.0, atol=1e-14)
+    np.testing.assert_allclose(dW.sum(axis=0), 0.0, atol=1e-13)
+
+
+def test_logprob_grad_identical_rows_give_zero_dx():
+    V, H = 64, 12
+    X = rand_bf16((4, H), 61)
+    W = np.repeat(rand_bf16((1, H), 62), V, axis=0)
+    dX, _, dl = oracle.logprob_grad(X, W, np.array([3, 0, 63, 9], dtype=np.int32), np.ones(4))
+    np.testing.assert_allclose(dX, 0.0, atol=1e-14)
+    np.testing.assert_allclose(dl[0, 3], 1 - 1 / V, rtol=1e-14)
+
+
 # ----------------------------------------------------------------- planted mistakes
 MUTATIONS = [
     # (description, original text, mutated text)
@@ -465,6 +548,13 @@ MUTATIONS = [
      "if (n > 0) total += A * wsum / (double)(offs[i + 1] - offs[i]);"),
     ("gradient sign", "double coef = n > 0 ? -A /", "double coef = n > 0 ? A /"),
     ("TIS as a floor", "wh > tis_cap) wh = tis_cap;", "wh < tis_cap) wh = tis_cap;"),
+    ("entropy sign", "if (p > 0.0) h -= p * lp;", "if (p > 0.0) h += p * lp;"),
+    ("gradient without the one-hot term", "dl[t * V + v] = g[t] * (onehot - exp(z[v] - lz));",
+     "dl[t * V + v] = g[t] * (-exp(z[v] - lz));"),
+    ("gradient with unnormalised probabilities", "dl[t * V + v] = g[t] * (onehot - exp(z[v] - lz));",
+     "dl[t * V + v] = g[t] * (onehot - exp(z[v]));"),
+    ("dW with a transposed operand", "acc += dl[t * V + v] * bf16_to_f64(X[t * H + k]);",
+     "acc += dl[t * V + v] * bf16_to_f64(W[v * H + k]);"),
     ("sequence gate on the last token only", "lr += (double)logp_pi[t] - (double)logp_mu[t];",
      "lr = (double)logp_pi[t] - (double)logp_mu[t];"),
 ]
@@ -503,7 +593,9 @@ def test_pins_catch_planted_mistake(tmp_path, monkeypatch, golden_dir, desc, ori
                 dict(), dict(flags=oracle.TIS, tis_cap=1.03))],
             test_reinforce_zero_tis_and_gate_limits,
             test_reinforce_zero_sequence_gate_drops_whole_responses,
-            test_reinforce_zero_token_gate_and_empty_response]
+            test_reinforce_zero_token_gate_and_empty_response,
+            test_entropy_closed_forms, test_entropy_bounds_and_decimal_brute_force,
+            test_logprob_grad_is_the_derivative, test_logprob_grad_identical_rows_give_zero_dx]
     failed = 0
     for pin in pins:
         try:
