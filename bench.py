@@ -183,6 +183,145 @@ def rollout_logprobs(W, X, ids, wl, seed, max_tokens):
     return mu
 
 
+# ----------------------------------------------------------------------------- RL epilogues
+RL_BYTES_PER_TOKEN = {"stats": 9, "reinforce_zero": 17}  # reads a, b, mask; + writes w_hat, grad
+
+
+def rl_inputs(device, seed_offset: int = 0):
+    """The importance-weight workload's token stream: 512 responses of U[128, 8192] tokens in
+    groups of 8, learner / rollout logprobs, response mask, 0/1 rewards."""
+    from bit_consistent_logprob_gb300 import inputs
+
+    wl = inputs.WORKLOADS["is_d3"]
+    offs, rewards = inputs.response_batch(wl.n_seqs // 8, 8, wl.len_lo, wl.len_hi, wl.seed)
+    T = int(offs[-1])
+    lp, lm, mask = inputs.synthetic_is_inputs(T, seed=wl.seed + seed_offset, device=device)
+    return wl, offs, rewards, lp, lm, mask
+
+
+def run_rl_epilogue(args, world, rank, local, pg):
+    import torch
+
+    from bit_consistent_logprob_gb300 import Engine, inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl, offs_h, rewards_h, lp, lm, mask = rl_inputs(dev, seed_offset=rank)
+    T, B = lp.shape[0], rewards_h.shape[0]
+    offs, rewards = offs_h.to(dev), rewards_h.to(dev)
+    W = inputs.lm_head(1024, 256, wl.seed, device=dev)  # the handle's workspace only
+    eng = Engine(W, n_leaves=4, max_tokens=128)
+    stats = torch.empty(5, dtype=torch.float64, device=dev)
+    w_hat = torch.empty(T, dtype=torch.float32, device=dev)
+    grad = torch.empty(T, dtype=torch.float32, device=dev)
+    adv = torch.empty(B, dtype=torch.float64, device=dev)
+    stream = torch.cuda.current_stream()
+    launches = [0]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    timing = [False]
+
+    def step(k=None):
+        eng.acceptance_stats(lp, lm, mask, out=stats)
+        launches[0] += eng.last_launch_count
+        if k is not None:
+            ev[k][0].record(stream)
+        loss = eng.reinforce_zero(lp, lm, offs, rewards, 8, mask=mask, out_w_hat=w_hat,
+                                  out_grad=grad, out_adv=adv)[0]
+        if k is not None:
+            ev[k][1].record(stream)
+        launches[0] += eng.last_launch_count
+        return loss
+
+    for _ in range(args.warmup):
+        step()
+    eng.check()
+    torch.cuda.synchronize()
+    launches[0] = 0
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    barrier(pg, dev)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(args.steps):
+        step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg, dev)
+    clocks = sampler.stop()
+    eng.check()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(pg, ms, dev)
+    rz_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+
+    e2e = None
+    if not args.no_e2e:
+        lph, lmh, mh = (t.cpu().pin_memory() for t in (lp, lm, mask))
+        offh, rwh = offs_h.pin_memory(), rewards_h.pin_memory()
+        res = torch.empty(6, dtype=torch.float64).pin_memory()
+
+        def step_e2e():
+            a, b, m = (t.to(dev, non_blocking=True) for t in (lph, lmh, mh))
+            o, r = offh.to(dev, non_blocking=True), rwh.to(dev, non_blocking=True)
+            eng.acceptance_stats(a, b, m, out=stats)
+            loss = eng.reinforce_zero(a, b, o, r, 8, mask=m, out_w_hat=w_hat, out_grad=grad,
+                                      out_adv=adv)[0]
+            res[:5].copy_(stats, non_blocking=True)
+            res[5:].copy_(loss, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(max(1, args.warmup)):
+            step_e2e()
+        barrier(pg, dev)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step_e2e()
+        t1 = time.perf_counter()
+        barrier(pg, dev)
+        e2e_ms = max_over_ranks(pg, (t1 - t0) * 1000.0 / args.steps, dev)
+        e2e = {"value": world * T / (e2e_ms / 1000.0), "unit": UNIT, "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": T * 9 + offh.numel() * 8 + B * 4,
+               "d2h_bytes_per_step": 48}
+
+    peaks, peak_src = load_peaks()
+    algo = RL_BYTES_PER_TOKEN["reinforce_zero"] * T
+    achieved = algo / (rz_ms / 1000.0) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_source": f"{peak_src} hbm_gbs",
+            "traffic": None, "kernel": "lp_reinforce_zero (rz_seq_kernel + rz_final_kernel)",
+            "kernel_ms": rz_ms, "algorithmic_per_launch": algo}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        a, b, m = lp.cpu().numpy(), lm.cpu().numpy(), mask.cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.acceptance_stats(a, b, m)
+        oracle.reinforce_zero(a, b, offs_h.numpy(), rewards_h.numpy(), 8, mask=m)
+        dt = time.perf_counter() - t0
+        cpu = {"value": T / dt, "unit": UNIT, "cores": 1, "kind": "oracle", "seconds": dt,
+               "sample": f"the whole {T}-token stream: acceptance statistics + REINFORCE Zero"}
+    eng.close()
+    if rank != 0:
+        return None
+    return {
+        "metric": "RL-epilogue tokens/sec (acceptance statistics + REINFORCE Zero loss)",
+        "value": world * T / (ms_max / 1000.0), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32/f64",
+        "data": "synthetic",
+        "config": {"workload": "rl_epilogue", "T": T, "responses": B, "group_size": 8,
+                   "l2": "inputs smaller than L2 (19 MB); each step re-reads them",
+                   "step": "lp_acceptance_stats + lp_reinforce_zero"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches[0],
+        "clocks": clocks,
+    }
+
+
 # ----------------------------------------------------------------------------- our arm
 def run_ours(args, world, rank, local, pg):
     import torch
@@ -269,7 +408,7 @@ def run_ours(args, world, rank, local, pg):
     launches_per_step = gemm_n / max(1, args.steps)
     if args.workload == "ds_decode":
         # HBM-bound: W streamed once per step plus X and the per-tile partials.
-        nb = (V + 127) // 128
+        nb = (V + 63) // 64  # (max, sum-exp) partial per 64-column tile
         algo = (2 * H * V + 2 * T * H + 8 * T * nb + 8 * T) / launches_per_step
         achieved = algo / (gemm_avg_ms / 1000.0) / 1e9
         peak = float(peaks["hbm_gbs"])
@@ -335,10 +474,46 @@ def cpu_baseline(X, W, ids, mu, wl, rows: int):
 
 
 # ----------------------------------------------------------------------------- reference arm
+def run_reference_rl(args, world):
+    """The oracle's acceptance statistics + REINFORCE Zero loss over the whole token stream."""
+    import oracle
+
+    wl, offs, rewards, lp, lm, mask = rl_inputs("cpu")
+    a, b, m = lp.numpy(), lm.numpy(), mask.numpy()
+    T = a.shape[0]
+    oracle.build()
+
+    def step():
+        oracle.acceptance_stats(a, b, m)
+        oracle.reinforce_zero(a, b, offs.numpy(), rewards.numpy(), 8, mask=m)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = T / dt
+    return {
+        "impl": "reference", "metric": "RL-epilogue tokens/sec (acceptance statistics + "
+        "REINFORCE Zero loss)", "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1000.0,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "rl_epilogue", "T": T, "responses": int(rewards.numel()),
+                   "group_size": 8},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"the whole {T}-token stream per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args, world, rank):
     """The CPU oracle as the reference implementation, on a bounded row sample per step."""
     if rank != 0:
         return None
+    if args.workload == "rl_epilogue":
+        return run_reference_rl(args, world)
     import numpy as np
 
     import oracle
@@ -403,7 +578,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="qwen_prefill",
-                    choices=("tiny", "qwen_prefill", "ds_prefill", "ds_decode", "is_d3"))
+                    choices=("tiny", "qwen_prefill", "ds_prefill", "ds_decode", "is_d3",
+                             "rl_epilogue"))
     ap.add_argument("--batch", type=int, default=128, help="rows of the decode workload")
     ap.add_argument("--max-tokens", type=int, default=32768, help="row chunk of the engine")
     ap.add_argument("--cpu-rows", type=int, default=128, help="rows of the CPU-baseline sample")
@@ -423,6 +599,8 @@ def main(argv=None):
         raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
     if args.impl == "reference":
         line = run_reference(args, world, rank)
+    elif args.workload == "rl_epilogue":
+        line = run_rl_epilogue(args, world, rank, local, pg)
     else:
         line = run_ours(args, world, rank, local, pg)
     if rank == 0 and line is not None:

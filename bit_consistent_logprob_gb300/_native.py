@@ -52,6 +52,10 @@ SIGNATURES = {
     "lp_importance_weights": (ctypes.c_int, [_p, _p, _p, _p, _i64, _p, _p, _p, _p]),
     "lp_importance_weights_host": (ctypes.c_int, [_p, _p, _p, _p, _i64, _p, _p, _p, _p]),
     "lp_acceptance_stats": (ctypes.c_int, [_p, _p, _p, _p, _i64, _p, _p]),
+    "lp_logprobs_entropy": (ctypes.c_int, [_p, _p, _i64, _p, _i64, _p, _p, _p, ctypes.c_int, _p]),
+    "lp_logprobs_backward": (ctypes.c_int, [_p, _p, _i64, _p, _p, _p, _i64, _p, _p, ctypes.c_int,
+                                            _p]),
+    "lp_backward_reserve": (ctypes.c_int, [_p, _i64]),
     "lp_reinforce_zero": (ctypes.c_int, [_p, _p, _p, _p, _i64, _p, _i64, _p, _i32,
                                          ctypes.POINTER(LpRzOptions), _p, _p, _p, _p, _p, _p]),
     "lp_profile_enable": (ctypes.c_int, [_p, ctypes.c_int]),

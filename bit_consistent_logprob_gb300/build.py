@@ -3,8 +3,8 @@
 ``csrc/lp_api.cu`` holds the handle-based C ABI and ``csrc/lp_noalloc.cu`` the
 no-allocation entry point; both instantiate the same kernel templates from
 ``csrc/kernels.cuh`` with the same flags, so they share the pinned numerics.  The library links
-the shared CUDA runtime and resolves the driver's tensor-map encoder at run
-time (no link against libcuda).
+the shared CUDA runtime and cuBLAS (for the two plain GEMMs of the logprob backward) and
+resolves the driver's tensor-map encoder at run time (no link against libcuda).
 """
 from __future__ import annotations
 
@@ -20,13 +20,15 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "liblp.so")
 SOURCES = [os.path.join(CSRC, "lp_api.cu"), os.path.join(CSRC, "lp_noalloc.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("kernels.cuh", "numerics.cuh", "ptx.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("kernels.cuh", "numerics.cuh", "ptx.cuh",
+                                                  "rl_kernels.cuh")] + [
     os.path.join(INCLUDE, "lp.h")]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", *ARCH_FLAGS, "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-shared", "-cudart", "shared",
               "-I", INCLUDE, "-I", CSRC]
+LINK_FLAGS = ["-lcublas"]  # the backward's two plain GEMMs (dX = dl W, dW = dl^T X)
 
 
 def nvcc() -> str:
@@ -49,7 +51,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *NVCC_FLAGS, *(["-Xptxas", "-v"] if verbose else []), "-o", tmp, *SOURCES]
+    cmd = [nvcc(), *NVCC_FLAGS, *(["-Xptxas", "-v"] if verbose else []), "-o", tmp, *SOURCES, *LINK_FLAGS]
     proc = subprocess.run(cmd, capture_output=True, text=True)
     if proc.returncode != 0:
         raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + proc.stdout + proc.stderr)

@@ -1,11 +1,13 @@
 // kernels.cuh -- sm_103a kernels of the logprob path.
 //
-//  leaf_gemm_kernel<kFused>   persistent, warp-specialised tcgen05 GEMM over 128x128
+//  leaf_gemm_kernel<kMode>    persistent, warp-specialised tcgen05 GEMM over 128x128
 //                             (token x vocab) tiles: TMA -> smem ring -> tcgen05.mma into
 //                             TMEM, one accumulator per K leaf, the fixed leaf tree in
-//                             the epilogue, then either the per-tile log-sum-exp partial
-//                             and the sampled logit (fused path) or the tree node written
-//                             to global memory (tensor-parallel slice / leaf export).
+//                             the epilogue, then by mode: the per-tile log-sum-exp partial
+//                             and the sampled logit (fused path; optionally the entropy
+//                             partial too), the tree node written to global memory
+//                             (tensor-parallel slice / leaf export), or the logprob
+//                             gradient with respect to the logits (backward).
 //  partials_lse_kernel        upper levels of the leaf tree over gathered slice partials,
 //                             then the same per-tile log-sum-exp (emulated TP path).
 //  lse_combine_kernel         fixed pairwise tree over the vocabulary tiles of each row,
@@ -20,6 +22,7 @@
 
 #include <cuda.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "numerics.cuh"
 #include "ptx.cuh"
@@ -33,6 +36,12 @@ constexpr int kAccBufs = 3;                       // rotating TMEM leaf accumula
 constexpr int kTmemCols = 512;                    // buf0 | buf1 | buf2 | S0 (128 columns each)
 constexpr uint32_t kColS0 = kAccBufs * kVT;       // TMEM slot of the deeper partial sum
 constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kVT);
+
+// What the epilogue does with each finished 128x128 tile of logits z.
+constexpr int kModeNode = 0;     // write z (fp32) to out: a tree node of a leaf range
+constexpr int kModeLse = 1;      // (max, sum-exp) per 64-column tile + the sampled logit
+constexpr int kModeLseEnt = 2;   // kModeLse + sum e^(z-m)(z-m) per tile (row entropy)
+constexpr int kModeGrad = 3;     // dl = g (onehot(y) - e^(z - logZ)) as bf16 to dl
 
 struct GemmParams {
     int32_t T;                // rows of this launch
@@ -51,6 +60,11 @@ struct GemmParams {
     float* zy;                // [T] sampled logit (fused path)
     float* out;               // [T][ldo] tree node (partial path)
     int64_t ldo;
+    float* ws_u;              // [num_lse_tiles][ws_ld] entropy partial per tile (kModeLseEnt)
+    const float* logZ;        // [T] per-row logZ of the forward pass (kModeGrad)
+    const float* gout;        // [T] dLoss/dlogp per row (kModeGrad)
+    uint16_t* dl;             // [T][ldd] bf16 gradient with respect to the logits (kModeGrad)
+    int64_t ldd;
     int* status;              // sticky device status word
     uint64_t timeout_ns;      // bound on every mbarrier wait
 };
@@ -124,7 +138,7 @@ __device__ __forceinline__ void release_buf(uint64_t* bar) {
 // kCluster = 1: one CTA per tile.  kCluster = 2: clusters of two CTAs share the X tile of
 // vocabulary-adjacent tiles; each CTA loads 64 of its 128 rows and multicasts them to both
 // (tmX then has 64-row boxes).  The per-element arithmetic is identical in both modes.
-template <bool kFused, int kSub, int kCluster>
+template <int kMode, int kSub, int kCluster>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     leaf_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmW, const GemmParams p) {
@@ -334,7 +348,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int v0 = vt * kVT;
             const bool row_ok = row < p.T;
             int ycol = -1;
-            if (kFused && row_ok) {
+            if (kMode != kModeNode && row_ok) {
                 const int y = p.ids[row];
                 if (y >= 0 && y < p.V) ycol = y - v0;
             }
@@ -401,7 +415,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (!ok) break;
             {
                 const int col0 = v0 + h * 64;
-                if (kFused) {
+                if constexpr (kMode == kModeLse) {
                     // the 64-column log-sum-exp tile 2*vt + h of this row is entirely in R
                     const int nv = p.V - col0;
                     if (row_ok && nv > 0) {
@@ -410,6 +424,46 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const float2 ms = tile_lse64(R, min(nv, kLT), yc, zy);
                         p.ws_ms[static_cast<int64_t>(2 * vt + h) * p.ws_ld + row] = ms;
                         if (yc >= 0 && yc < kLT) p.zy[row] = zy;
+                    }
+                } else if constexpr (kMode == kModeLseEnt) {
+                    const int nv = p.V - col0;
+                    if (row_ok && nv > 0) {
+                        float zy = 0.0f, u;
+                        const int yc = ycol - h * 64;
+                        const int64_t wi = static_cast<int64_t>(2 * vt + h) * p.ws_ld + row;
+                        p.ws_ms[wi] = tile_lse64_ent(R, min(nv, kLT), yc, zy, u);
+                        p.ws_u[wi] = u;
+                        if (yc >= 0 && yc < kLT) p.zy[row] = zy;
+                    }
+                } else if constexpr (kMode == kModeGrad) {
+                    const int nv = p.V - col0;
+                    if (row_ok && nv > 0) {
+                        const float lz = p.logZ[row], gg = p.gout[row];
+                        const int yc = ycol - h * 64;
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int i = 0; i < 64; i += 2) {
+                            float d[2];
+#pragma unroll
+                            for (int k = 0; k < 2; ++k) {
+                                const float pr = __expf(__fsub_rn(R[i + k], lz));
+                                d[k] = __fmul_rn(gg, __fsub_rn(i + k == yc ? 1.0f : 0.0f, pr));
+                            }
+                            pk[i >> 1] = pack_bf16x2(d[0], d[1]);
+                        }
+                        uint16_t* dst = p.dl + static_cast<int64_t>(row) * p.ldd + col0;
+                        if (nv >= 64) {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4)
+                                *reinterpret_cast<uint4*>(dst + 2 * i) =
+                                    make_uint4(pk[i], pk[i + 1], pk[i + 2], pk[i + 3]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 64; ++i)
+                                if (i < nv)
+                                    dst[i] = static_cast<uint16_t>(
+                                        (i & 1) ? (pk[i >> 1] >> 16) : (pk[i >> 1] & 0xffffu));
+                        }
                     }
                 } else if (row_ok) {
                     float* dst = p.out + static_cast<int64_t>(row) * p.ldo + col0;
@@ -450,11 +504,12 @@ struct PartialsParams {
     int32_t V;
     const int32_t* ids;
     float2* ws_ms;
+    float* ws_u;             // entropy partials (kEnt)
     int64_t ws_ld;
     float* zy;
 };
 
-template <int kParts>
+template <int kParts, bool kEnt>
 __global__ void __launch_bounds__(128) partials_lse_kernel(const PartialsParams p) {
     const int vt = blockIdx.x;
     const int row = blockIdx.y * 128 + threadIdx.x;
@@ -481,8 +536,14 @@ __global__ void __launch_bounds__(128) partials_lse_kernel(const PartialsParams 
         }
         const int ycol = (y >= 0 && y < p.V) ? y - col0 : -1;
         float zy = 0.0f;
-        const float2 ms = tile_lse64(z, min(nv, kLT), ycol, zy);
-        p.ws_ms[static_cast<int64_t>(2 * vt + h) * p.ws_ld + row] = ms;
+        const int64_t wi = static_cast<int64_t>(2 * vt + h) * p.ws_ld + row;
+        if constexpr (kEnt) {
+            float u;
+            p.ws_ms[wi] = tile_lse64_ent(z, min(nv, kLT), ycol, zy, u);
+            p.ws_u[wi] = u;
+        } else {
+            p.ws_ms[wi] = tile_lse64(z, min(nv, kLT), ycol, zy);
+        }
         if (ycol >= 0 && ycol < kLT) p.zy[row] = zy;
     }
 }
@@ -500,6 +561,7 @@ __global__ void __launch_bounds__(128) partials_lse_kernel(const PartialsParams 
 // block: rows x nseg threads, thread (r, g) at g * rows + r; grid: ceil(T / rows).
 struct CombineParams {
     const float2* ws_ms;
+    const float* ws_u;        // entropy partials (entropy variant)
     int64_t ws_ld;
     const float* zy;
     const int32_t* ids;
@@ -511,6 +573,7 @@ struct CombineParams {
     int32_t nseg;             // ceil(num_tiles / 2^seg_log); rows * nseg <= 512
     float* out_logp;
     float* out_logZ;          // may be null
+    float* out_entropy;       // entropy variant only
     int* status;
 };
 
@@ -540,46 +603,56 @@ __host__ inline CombineLayout combine_layout(int64_t T, int num_tiles, int num_s
     return c;
 }
 
-static __global__ void __launch_bounds__(kCmbMaxThreads) lse_combine_kernel(const CombineParams p) {
-    extern __shared__ float2 cmb_smem[];  // [nseg][rows]
+template <bool kEnt>
+__global__ void __launch_bounds__(kCmbMaxThreads) lse_combine_kernel(const CombineParams p) {
+    // (m, s) per tile, or (m, s, u) with the entropy partial; merged by the same tree
+    using Acc = typename std::conditional<kEnt, float3, float2>::type;
+    extern __shared__ __align__(16) uint8_t cmb_raw[];
+    Acc* cmb = reinterpret_cast<Acc*>(cmb_raw);  // [nseg][rows]
+    const auto load = [&](int b, int row) -> Acc {
+        const int64_t i = static_cast<int64_t>(b) * p.ws_ld + row;
+        const float2 ms = __ldg(p.ws_ms + i);
+        if constexpr (kEnt) return make_float3(ms.x, ms.y, __ldg(p.ws_u + i));
+        else return ms;
+    };
+    const auto merge = [](Acc a, Acc b) -> Acc {
+        if constexpr (kEnt) return lse_merge_ent(a, b);
+        else return lse_merge(a, b);
+    };
     const int r = threadIdx.x % p.rows;
     const int g = threadIdx.x / p.rows;
     const int row = blockIdx.x * p.rows + r;
     const bool row_ok = row < p.T;
     if (row_ok) {
         const int b_end = min((g + 1) << p.seg_log, p.num_tiles);
-        float2 stack[kSegLogMax - 2];  // counter levels: blocks of 8, 16, ..., 2^kSegLogMax
+        Acc stack[kSegLogMax - 2];     // counter levels: blocks of 8, 16, ..., 2^kSegLogMax
         uint32_t k = 0;                // rounds folded so far
         const int b_begin = g << p.seg_log;
-        float2 nxt[kCmbRound];         // the next round's tiles, loaded one round ahead
+        Acc nxt[kCmbRound];            // the next round's tiles, loaded one round ahead
 #pragma unroll
         for (int i = 0; i < kCmbRound; ++i)
-            nxt[i] = b_begin + i < b_end
-                         ? __ldg(p.ws_ms + static_cast<int64_t>(b_begin + i) * p.ws_ld + row)
-                         : make_float2(0.0f, 0.0f);
+            if (b_begin + i < b_end) nxt[i] = load(b_begin + i, row);
         for (int b = b_begin; b < b_end; b += kCmbRound, ++k) {
             const int nv = min(kCmbRound, b_end - b);
-            float2 v[kCmbRound];
+            Acc v[kCmbRound];
 #pragma unroll
             for (int i = 0; i < kCmbRound; ++i) v[i] = nxt[i];
             const int bn = b + kCmbRound;
 #pragma unroll
             for (int i = 0; i < kCmbRound; ++i)
-                nxt[i] = bn + i < b_end
-                             ? __ldg(p.ws_ms + static_cast<int64_t>(bn + i) * p.ws_ld + row)
-                             : make_float2(0.0f, 0.0f);
+                if (bn + i < b_end) nxt[i] = load(bn + i, row);
 #pragma unroll
             for (int w = 1; w < kCmbRound; w <<= 1)
 #pragma unroll
                 for (int i = 0; i < kCmbRound; i += 2 * w)
-                    if (i + w < nv) v[i] = lse_merge(v[i], v[i + w]);
-            float2 carry = v[0];
+                    if (i + w < nv) v[i] = merge(v[i], v[i + w]);
+            Acc carry = v[0];
             bool open = true;  // carry not yet stored
 #pragma unroll
             for (int j = 0; j < kSegLogMax - 2; ++j) {
                 if (open) {
                     if ((k >> j) & 1u) {
-                        carry = lse_merge(stack[j], carry);
+                        carry = merge(stack[j], carry);
                     } else {
                         stack[j] = carry;
                         open = false;
@@ -588,26 +661,26 @@ static __global__ void __launch_bounds__(kCmbMaxThreads) lse_combine_kernel(cons
             }
         }
         // blocks still open, smallest (rightmost) first
-        float2 acc = make_float2(0.0f, 0.0f);
+        Acc acc{};
         bool have = false;
 #pragma unroll
         for (int j = 0; j < kSegLogMax - 2; ++j) {
             if ((k >> j) & 1u) {
-                acc = have ? lse_merge(stack[j], acc) : stack[j];
+                acc = have ? merge(stack[j], acc) : stack[j];
                 have = true;
             }
         }
-        cmb_smem[g * p.rows + r] = acc;
+        cmb[g * p.rows + r] = acc;
     }
     __syncthreads();
     for (int s = 1; s < p.nseg; s <<= 1) {
         if (row_ok && (g & (2 * s - 1)) == 0 && g + s < p.nseg)
-            cmb_smem[g * p.rows + r] = lse_merge(cmb_smem[g * p.rows + r],
-                                                 cmb_smem[(g + s) * p.rows + r]);
+            cmb[g * p.rows + r] = merge(cmb[g * p.rows + r], cmb[(g + s) * p.rows + r]);
         __syncthreads();
     }
     if (row_ok && g == 0) {
-        const float lz = lse_finish(cmb_smem[r]);
+        const Acc fin = cmb[r];
+        const float lz = lse_finish(make_float2(fin.x, fin.y));
         const int y = p.ids[row];
         float lp;
         if (y >= 0 && y < p.V) {
@@ -618,6 +691,7 @@ static __global__ void __launch_bounds__(kCmbMaxThreads) lse_combine_kernel(cons
         }
         p.out_logp[row] = lp;
         if (p.out_logZ) p.out_logZ[row] = lz;
+        if constexpr (kEnt) p.out_entropy[row] = entropy_finish(fin);
     }
 }
 

@@ -6,6 +6,7 @@
 // phase, so every row is bit-identical however it is batched.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cublas_v2.h>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -99,6 +100,13 @@ struct lp_handle {
     CUtensorMap tmW{};
     // workspace (device)
     float2* ws_ms = nullptr;      // [num_lse_tiles][max_tokens]
+    float* ws_u = nullptr;        // [num_lse_tiles][max_tokens] entropy partials
+    // backward (lp_backward_reserve)
+    uint16_t* dl = nullptr;       // [dl_rows][ldd] bf16 gradient with respect to the logits
+    int64_t dl_rows = 0;
+    int64_t ldd = 0;
+    cublasHandle_t cublas = nullptr;
+    void* cublas_ws = nullptr;
     float* zy = nullptr;          // [max_tokens]
     int* status = nullptr;        // sticky status word
     double* blk_sum = nullptr;    // [max_is_blocks]
@@ -158,7 +166,7 @@ uint32_t x_box_rows(int rows) {
     return rows >= lp::kBM ? lp::kBM : static_cast<uint32_t>((rows + 7) / 8 * 8);
 }
 
-template <bool kFused, int kSub, int kCluster>
+template <int kMode, int kSub, int kCluster>
 cudaError_t launch_gemm_variant(int grid, cudaStream_t st, const CUtensorMap& tmX,
                                 const CUtensorMap& tmW, const lp::GemmParams& p) {
     cudaLaunchConfig_t cfg = {};
@@ -175,20 +183,20 @@ cudaError_t launch_gemm_variant(int grid, cudaStream_t st, const CUtensorMap& tm
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, lp::leaf_gemm_kernel<kFused, kSub, kCluster>, tmX, tmW, p);
+    return cudaLaunchKernelEx(&cfg, lp::leaf_gemm_kernel<kMode, kSub, kCluster>, tmX, tmW, p);
 }
 
-template <bool kFused>
+template <int kMode>
 int set_gemm_attributes() {
     const auto set = [](auto fn, int sub) {
         return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     lp::gemm_smem_bytes(sub));
     };
     cudaError_t e;
-    if ((e = set(lp::leaf_gemm_kernel<kFused, 1, 1>, 1)) != cudaSuccess ||
-        (e = set(lp::leaf_gemm_kernel<kFused, 2, 1>, 2)) != cudaSuccess ||
-        (e = set(lp::leaf_gemm_kernel<kFused, 1, 2>, 1)) != cudaSuccess ||
-        (e = set(lp::leaf_gemm_kernel<kFused, 2, 2>, 2)) != cudaSuccess)
+    if ((e = set(lp::leaf_gemm_kernel<kMode, 1, 1>, 1)) != cudaSuccess ||
+        (e = set(lp::leaf_gemm_kernel<kMode, 2, 1>, 2)) != cudaSuccess ||
+        (e = set(lp::leaf_gemm_kernel<kMode, 1, 2>, 1)) != cudaSuccess ||
+        (e = set(lp::leaf_gemm_kernel<kMode, 2, 2>, 2)) != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute(leaf_gemm_kernel)");
     return LP_OK;
 }
@@ -197,10 +205,18 @@ int set_gemm_attributes() {
 // one full 128-row tile run in clusters of two CTAs that share each X tile (multicast);
 // smaller (decode) calls run one CTA per tile with an X box cut to their rows.  Stages are
 // 128 K deep (8 MMAs per barrier synchronisation) when the leaf length allows, else 64.
-template <bool kFused>
+// Extra per-mode operands of the leaf GEMM epilogue (kModeGrad).
+struct GradArgs {
+    const float* logZ = nullptr;
+    const float* gout = nullptr;
+    uint16_t* dl = nullptr;
+    int64_t ldd = 0;
+};
+
+template <int kMode>
 int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int leaf_begin,
                      int leaf_count, const int32_t* ids, float* out, int64_t ldo,
-                     cudaStream_t st) {
+                     cudaStream_t st, const GradArgs& ga = GradArgs()) {
     lp::GemmParams p{};
     p.T = rows;
     p.V = h->cfg.V;
@@ -217,6 +233,11 @@ int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int lea
     p.zy = h->zy;
     p.out = out;
     p.ldo = ldo;
+    p.ws_u = h->ws_u;
+    p.logZ = ga.logZ;
+    p.gout = ga.gout;
+    p.dl = ga.dl;
+    p.ldd = ga.ldd;
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
     const bool cluster = rows >= lp::kBM && h->num_vocab_tiles >= 2 && !h->force_single_cta;
@@ -235,11 +256,11 @@ int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int lea
     if (prof) LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used], st), "profile event");
     cudaError_t e;
     if (cluster)
-        e = sub2 ? launch_gemm_variant<kFused, 2, 2>(grid, st, tmX, h->tmW, p)
-                 : launch_gemm_variant<kFused, 1, 2>(grid, st, tmX, h->tmW, p);
+        e = sub2 ? launch_gemm_variant<kMode, 2, 2>(grid, st, tmX, h->tmW, p)
+                 : launch_gemm_variant<kMode, 1, 2>(grid, st, tmX, h->tmW, p);
     else
-        e = sub2 ? launch_gemm_variant<kFused, 2, 1>(grid, st, tmX, h->tmW, p)
-                 : launch_gemm_variant<kFused, 1, 1>(grid, st, tmX, h->tmW, p);
+        e = sub2 ? launch_gemm_variant<kMode, 2, 1>(grid, st, tmX, h->tmW, p)
+                 : launch_gemm_variant<kMode, 1, 1>(grid, st, tmX, h->tmW, p);
     LP_CUDA(e, "leaf_gemm_kernel launch");
     LP_CUDA(cudaGetLastError(), "leaf_gemm_kernel launch");
     if (prof) {
@@ -251,9 +272,11 @@ int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int lea
 }
 
 int launch_combine(lp_handle* h, const int32_t* ids, int rows, float* out_logp, float* out_logZ,
-                   cudaStream_t st) {
+                   float* out_entropy, cudaStream_t st) {
     lp::CombineParams c{};
     c.ws_ms = h->ws_ms;
+    c.ws_u = h->ws_u;
+    c.out_entropy = out_entropy;
     c.ws_ld = h->cfg.max_tokens;
     c.zy = h->zy;
     c.ids = ids;
@@ -267,16 +290,20 @@ int launch_combine(lp_handle* h, const int32_t* ids, int rows, float* out_logp, 
     c.out_logp = out_logp;
     c.out_logZ = out_logZ;
     c.status = h->status;
-    const size_t smem = sizeof(float2) * static_cast<size_t>(lay.rows) * lay.nseg;
-    lp::lse_combine_kernel<<<static_cast<unsigned>(ceil_div(rows, lay.rows)),
-                             static_cast<unsigned>(lay.rows * lay.nseg), smem, st>>>(c);
+    const size_t n = static_cast<size_t>(lay.rows) * lay.nseg;
+    const dim3 grid(static_cast<unsigned>(ceil_div(rows, lay.rows)));
+    const dim3 block(static_cast<unsigned>(lay.rows * lay.nseg));
+    if (out_entropy)
+        lp::lse_combine_kernel<true><<<grid, block, sizeof(float3) * n, st>>>(c);
+    else
+        lp::lse_combine_kernel<false><<<grid, block, sizeof(float2) * n, st>>>(c);
     LP_CUDA(cudaGetLastError(), "lse_combine_kernel launch");
     ++h->last_launches;
     return LP_OK;
 }
 
 int launch_partials_lse(lp_handle* h, const float* parts, int n_parts, int64_t part_stride,
-                        int64_t ldp, const int32_t* ids, int rows, cudaStream_t st) {
+                        int64_t ldp, const int32_t* ids, int rows, bool entropy, cudaStream_t st) {
     lp::PartialsParams q{};
     q.parts = parts;
     q.part_stride = part_stride;
@@ -286,14 +313,24 @@ int launch_partials_lse(lp_handle* h, const float* parts, int n_parts, int64_t p
     q.V = h->cfg.V;
     q.ids = ids;
     q.ws_ms = h->ws_ms;
+    q.ws_u = h->ws_u;
     q.ws_ld = h->cfg.max_tokens;
     q.zy = h->zy;
     dim3 grid(static_cast<unsigned>(h->num_vocab_tiles), static_cast<unsigned>(ceil_div(rows, 128)));
-    switch (n_parts) {
-        case 1: lp::partials_lse_kernel<1><<<grid, 128, 0, st>>>(q); break;
-        case 2: lp::partials_lse_kernel<2><<<grid, 128, 0, st>>>(q); break;
-        case 4: lp::partials_lse_kernel<4><<<grid, 128, 0, st>>>(q); break;
-        default: lp::partials_lse_kernel<8><<<grid, 128, 0, st>>>(q); break;
+    if (entropy) {
+        switch (n_parts) {
+            case 1: lp::partials_lse_kernel<1, true><<<grid, 128, 0, st>>>(q); break;
+            case 2: lp::partials_lse_kernel<2, true><<<grid, 128, 0, st>>>(q); break;
+            case 4: lp::partials_lse_kernel<4, true><<<grid, 128, 0, st>>>(q); break;
+            default: lp::partials_lse_kernel<8, true><<<grid, 128, 0, st>>>(q); break;
+        }
+    } else {
+        switch (n_parts) {
+            case 1: lp::partials_lse_kernel<1, false><<<grid, 128, 0, st>>>(q); break;
+            case 2: lp::partials_lse_kernel<2, false><<<grid, 128, 0, st>>>(q); break;
+            case 4: lp::partials_lse_kernel<4, false><<<grid, 128, 0, st>>>(q); break;
+            default: lp::partials_lse_kernel<8, false><<<grid, 128, 0, st>>>(q); break;
+        }
     }
     LP_CUDA(cudaGetLastError(), "partials_lse_kernel launch");
     ++h->last_launches;
@@ -302,11 +339,15 @@ int launch_partials_lse(lp_handle* h, const float* parts, int n_parts, int64_t p
 
 // Fused path or emulated tensor-parallel path for one chunk of rows (rows <= max_tokens).
 int logprobs_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int rows,
-                   float* out_logp, float* out_logZ, cudaStream_t st) {
+                   float* out_logp, float* out_logZ, float* out_entropy, cudaStream_t st) {
     int rc;
     const int s = h->cfg.tp_slices;
     if (s == 1) {
-        rc = launch_leaf_gemm<true>(h, X, ldx, rows, 0, h->cfg.n_leaves, ids, nullptr, 0, st);
+        rc = out_entropy
+                 ? launch_leaf_gemm<lp::kModeLseEnt>(h, X, ldx, rows, 0, h->cfg.n_leaves, ids,
+                                                     nullptr, 0, st)
+                 : launch_leaf_gemm<lp::kModeLse>(h, X, ldx, rows, 0, h->cfg.n_leaves, ids,
+                                                  nullptr, 0, st);
         if (rc != LP_OK) return rc;
     } else {
         // Slice r owns leaves [r*N/s, (r+1)*N/s) and produces that node of the leaf tree;
@@ -315,7 +356,7 @@ int logprobs_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids,
         const int per = h->cfg.n_leaves / s;
         const int64_t part_stride = h->chunk_rows * h->tp_ldp;
         for (int r = 0; r < s; ++r) {
-            rc = launch_leaf_gemm<false>(h, X, ldx, rows, r * per, per, nullptr,
+            rc = launch_leaf_gemm<lp::kModeNode>(h, X, ldx, rows, r * per, per, nullptr,
                                          h->tp_parts + r * part_stride, h->tp_ldp, st);
             if (rc != LP_OK) return rc;
         }
@@ -325,10 +366,11 @@ int logprobs_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids,
                                     cudaMemcpyDeviceToDevice, st),
                     "slice transport copy");
         }
-        rc = launch_partials_lse(h, h->tp_gather, s, part_stride, h->tp_ldp, ids, rows, st);
+        rc = launch_partials_lse(h, h->tp_gather, s, part_stride, h->tp_ldp, ids, rows,
+                                 out_entropy != nullptr, st);
         if (rc != LP_OK) return rc;
     }
-    return launch_combine(h, ids, rows, out_logp, out_logZ, st);
+    return launch_combine(h, ids, rows, out_logp, out_logZ, out_entropy, st);
 }
 
 int check_x(const lp_handle* h, const void* X, int64_t ldx, int64_t T) {
@@ -361,6 +403,10 @@ void lp_free(lp_handle* h) {
     cudaFree(h->ws_ms);
     cudaFree(h->zy);
     cudaFree(h->status);
+    cudaFree(h->ws_u);
+    cudaFree(h->dl);
+    cudaFree(h->cublas_ws);
+    if (h->cublas) cublasDestroy(h->cublas);
     cudaFree(h->blk_sum);
     cudaFree(h->blk_cnt);
     cudaFree(h->stat_blk);
@@ -440,6 +486,8 @@ int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out) 
     h->max_is_blocks = ceil_div(kMaxIsTokens, lp::kIsBlock);
     if ((rc = alloc(reinterpret_cast<void**>(&h->ws_ms),
                     sizeof(float2) * static_cast<size_t>(h->num_lse_tiles) * mt, "ws_ms")) ||
+        (rc = alloc(reinterpret_cast<void**>(&h->ws_u),
+                    sizeof(float) * static_cast<size_t>(h->num_lse_tiles) * mt, "ws_u")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->zy), sizeof(float) * mt, "zy")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->status), sizeof(int), "status")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->blk_sum), sizeof(double) * h->max_is_blocks,
@@ -470,7 +518,10 @@ int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out) 
             return cleanup(rc);
     }
 
-    if ((rc = set_gemm_attributes<true>()) != LP_OK || (rc = set_gemm_attributes<false>()) != LP_OK)
+    if ((rc = set_gemm_attributes<lp::kModeNode>()) != LP_OK ||
+        (rc = set_gemm_attributes<lp::kModeLse>()) != LP_OK ||
+        (rc = set_gemm_attributes<lp::kModeLseEnt>()) != LP_OK ||
+        (rc = set_gemm_attributes<lp::kModeGrad>()) != LP_OK)
         return cleanup(rc);
     cudaError_t e;
     if (h->num_lse_tiles > (lp::kCmbMaxThreads << lp::kSegLogMax))
@@ -484,8 +535,9 @@ int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out) 
     return LP_OK;
 }
 
-int lp_logprobs(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int64_t T,
-                float* out_logp, float* out_logZ, int phase, void* stream) {
+namespace {
+int logprobs_impl(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int64_t T,
+                  float* out_logp, float* out_logZ, float* out_entropy, int phase, void* stream) {
     if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
     int rc = check_x(h, X, ldx, T);
     if (rc != LP_OK) return rc;
@@ -502,8 +554,117 @@ int lp_logprobs(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, in
     for (int64_t r0 = 0; r0 < T; r0 += chunk) {
         const int rows = static_cast<int>(T - r0 < chunk ? T - r0 : chunk);
         rc = logprobs_chunk(h, xb + r0 * ldx * 2, ldx, ids + r0, rows, out_logp + r0,
-                            out_logZ ? out_logZ + r0 : nullptr, st);
+                            out_logZ ? out_logZ + r0 : nullptr,
+                            out_entropy ? out_entropy + r0 : nullptr, st);
         if (rc != LP_OK) return rc;
+    }
+    return LP_OK;
+}
+}  // namespace
+
+int lp_logprobs(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int64_t T,
+                float* out_logp, float* out_logZ, int phase, void* stream) {
+    return logprobs_impl(h, X, ldx, ids, T, out_logp, out_logZ, nullptr, phase, stream);
+}
+
+int lp_logprobs_entropy(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int64_t T,
+                        float* out_logp, float* out_logZ, float* out_entropy, int phase,
+                        void* stream) {
+    if (T > 0 && out_entropy == nullptr)
+        return fail(LP_ERR_INVALID_ARG, "out_entropy must not be NULL");
+    return logprobs_impl(h, X, ldx, ids, T, out_logp, out_logZ, out_entropy, phase, stream);
+}
+
+namespace {
+constexpr size_t kCublasWorkspace = size_t(32) << 20;
+
+int cublas_fail(cublasStatus_t s, const char* what) {
+    return fail(LP_ERR_CUDA, "%s: cuBLAS status %d", what, static_cast<int>(s));
+}
+}  // namespace
+
+int lp_backward_reserve(lp_handle* h, int64_t max_rows) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    if (max_rows < 1 || max_rows > (int64_t(1) << 31) - 1)
+        return fail(LP_ERR_INVALID_ARG, "max_rows must be in [1, 2^31)");
+    if (max_rows <= h->dl_rows) return LP_OK;
+    const int64_t ldd = ceil_div(h->cfg.V, 8) * 8;
+    void* p = nullptr;
+    const size_t bytes = sizeof(uint16_t) * static_cast<size_t>(max_rows) * ldd;
+    cudaError_t e = cudaMalloc(&p, bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(LP_ERR_OOM, "backward workspace (%zu bytes): %s", bytes, cudaGetErrorString(e));
+    }
+    if (h->dl) {
+        LP_CUDA(cudaDeviceSynchronize(), "device synchronize");
+        cudaFree(h->dl);
+        h->ws_bytes -= static_cast<int64_t>(sizeof(uint16_t)) * h->dl_rows * h->ldd;
+    }
+    h->dl = static_cast<uint16_t*>(p);
+    h->dl_rows = max_rows;
+    h->ldd = ldd;
+    h->ws_bytes += static_cast<int64_t>(bytes);
+    if (h->cublas == nullptr) {
+        cublasStatus_t cs = cublasCreate(&h->cublas);
+        if (cs != CUBLAS_STATUS_SUCCESS) {
+            h->cublas = nullptr;
+            return cublas_fail(cs, "cublasCreate");
+        }
+        LP_CUDA(cudaMalloc(&h->cublas_ws, kCublasWorkspace), "cuBLAS workspace");
+        h->ws_bytes += static_cast<int64_t>(kCublasWorkspace);
+    }
+    return LP_OK;
+}
+
+int lp_logprobs_backward(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids,
+                         const float* logZ, const float* grad_logp, int64_t T, float* dX,
+                         float* dW, int accumulate, void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    int rc = check_x(h, X, ldx, T);
+    if (rc != LP_OK) return rc;
+    if (h->dl == nullptr)
+        return fail(LP_ERR_INVALID_ARG, "call lp_backward_reserve before lp_logprobs_backward");
+    if (T > 0 && (ids == nullptr || logZ == nullptr || grad_logp == nullptr))
+        return fail(LP_ERR_INVALID_ARG, "ids, logZ and grad_logp must not be NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    h->last_stream = st;
+    h->last_launches = 0;
+    const int H = h->cfg.H, V = h->cfg.V;
+    if (dW != nullptr && !accumulate)
+        LP_CUDA(cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * H, st), "dW clear");
+    if (T == 0 || (dX == nullptr && dW == nullptr)) return LP_OK;
+    cublasStatus_t cs;
+    if ((cs = cublasSetStream(h->cublas, st)) != CUBLAS_STATUS_SUCCESS ||
+        (cs = cublasSetWorkspace(h->cublas, h->cublas_ws, kCublasWorkspace)) != CUBLAS_STATUS_SUCCESS)
+        return cublas_fail(cs, "cublasSetStream/cublasSetWorkspace");
+    const float one = 1.0f, zero = 0.0f;
+    const uint8_t* xb = static_cast<const uint8_t*>(X);
+    for (int64_t r0 = 0; r0 < T; r0 += h->dl_rows) {
+        const int rows = static_cast<int>(T - r0 < h->dl_rows ? T - r0 : h->dl_rows);
+        const void* Xc = xb + r0 * ldx * 2;
+        GradArgs ga;
+        ga.logZ = logZ + r0;
+        ga.gout = grad_logp + r0;
+        ga.dl = h->dl;
+        ga.ldd = h->ldd;
+        rc = launch_leaf_gemm<lp::kModeGrad>(h, Xc, ldx, rows, 0, h->cfg.n_leaves, ids + r0,
+                                             nullptr, 0, st, ga);
+        if (rc != LP_OK) return rc;
+        // row-major [r][c] buffers seen column-major: dX^T = W^T dl^T, dW^T = X^T dl
+        if (dX != nullptr) {
+            cs = cublasGemmEx(h->cublas, CUBLAS_OP_N, CUBLAS_OP_N, H, rows, V, &one, h->W,
+                              CUDA_R_16BF, H, h->dl, CUDA_R_16BF, static_cast<int>(h->ldd), &zero,
+                              dX + r0 * H, CUDA_R_32F, H, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+            if (cs != CUBLAS_STATUS_SUCCESS) return cublas_fail(cs, "dX GEMM");
+        }
+        if (dW != nullptr) {
+            cs = cublasGemmEx(h->cublas, CUBLAS_OP_N, CUBLAS_OP_T, H, V, rows, &one, Xc,
+                              CUDA_R_16BF, static_cast<int>(ldx), h->dl, CUDA_R_16BF,
+                              static_cast<int>(h->ldd), &one, dW, CUDA_R_32F, H,
+                              CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+            if (cs != CUBLAS_STATUS_SUCCESS) return cublas_fail(cs, "dW GEMM");
+        }
     }
     return LP_OK;
 }
@@ -533,7 +694,7 @@ int lp_logprobs_host(lp_handle* h, const void* X, int64_t ldx, const int32_t* id
                                 cudaMemcpyHostToDevice, st),
                 "ids host-to-device copy");
         int rc = logprobs_chunk(h, h->x_stage, H, h->ids_stage, rows, h->logp_stage,
-                                h->logz_stage, st);
+                                h->logz_stage, nullptr, st);
         if (rc != LP_OK) return rc;
         launches += h->last_launches;
         h->last_launches = 0;
@@ -570,7 +731,7 @@ int lp_logits_partial(lp_handle* h, const void* X, int64_t ldx, int64_t T, int32
     const uint8_t* xb = static_cast<const uint8_t*>(X);
     for (int64_t r0 = 0; r0 < T; r0 += chunk) {
         const int rows = static_cast<int>(T - r0 < chunk ? T - r0 : chunk);
-        rc = launch_leaf_gemm<false>(h, xb + r0 * ldx * 2, ldx, rows, leaf_begin, leaf_count,
+        rc = launch_leaf_gemm<lp::kModeNode>(h, xb + r0 * ldx * 2, ldx, rows, leaf_begin, leaf_count,
                                      nullptr, out + r0 * ldo, ldo, st);
         if (rc != LP_OK) return rc;
     }
@@ -594,9 +755,10 @@ int lp_logprobs_from_partials(lp_handle* h, const float* partials, int32_t n_par
         return fail(LP_ERR_INVALID_ARG, "need ldp >= V and part_stride >= ldp * T");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     h->last_stream = st;
-    int rc = launch_partials_lse(h, partials, n_parts, part_stride, ldp, ids, static_cast<int>(T), st);
+    int rc = launch_partials_lse(h, partials, n_parts, part_stride, ldp, ids, static_cast<int>(T),
+                                 false, st);
     if (rc != LP_OK) return rc;
-    return launch_combine(h, ids, static_cast<int>(T), out_logp, out_logZ, st);
+    return launch_combine(h, ids, static_cast<int>(T), out_logp, out_logZ, nullptr, st);
 }
 
 int lp_importance_weights(lp_handle* h, const float* logp_pi, const float* logp_mu,

@@ -79,11 +79,11 @@ void setup_device(int dev, DeviceSetup& s) {
     if (e == cudaSuccess) e = cudaGetSymbolAddress(&ptr, g_lp_noalloc_scratch);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<true, 1, 1>,
+        e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<lp::kModeLse, 1, 1>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  lp::gemm_smem_bytes(1));
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<true, 2, 1>,
+        e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<lp::kModeLse, 2, 1>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  lp::gemm_smem_bytes(2));
     if (e != cudaSuccess) {
@@ -203,9 +203,9 @@ LP_API int lp_logprobs_noalloc(const void* W, int32_t H, int32_t V, int32_t n_le
     const int64_t tiles = static_cast<int64_t>(p.num_row_tiles) * p.num_vocab_tiles;
     const int grid = static_cast<int>(tiles < s.num_sms ? tiles : s.num_sms);
     if (p.leaf_len % (2 * lp::kBK) == 0)
-        lp::leaf_gemm_kernel<true, 2, 1><<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(2), st>>>(tmX, tmW, p);
+        lp::leaf_gemm_kernel<lp::kModeLse, 2, 1><<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(2), st>>>(tmX, tmW, p);
     else
-        lp::leaf_gemm_kernel<true, 1, 1><<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(1), st>>>(tmX, tmW, p);
+        lp::leaf_gemm_kernel<lp::kModeLse, 1, 1><<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(1), st>>>(tmX, tmW, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return nfail(LP_ERR_CUDA, "leaf_gemm_kernel launch: %s", cudaGetErrorString(e));
 
@@ -224,7 +224,7 @@ LP_API int lp_logprobs_noalloc(const void* W, int32_t H, int32_t V, int32_t n_le
     c.out_logp = out_logp;
     c.out_logZ = out_logZ;
     c.status = status;
-    lp::lse_combine_kernel<<<static_cast<unsigned>((rows + lay.rows - 1) / lay.rows),
+    lp::lse_combine_kernel<false><<<static_cast<unsigned>((rows + lay.rows - 1) / lay.rows),
                              static_cast<unsigned>(lay.rows * lay.nseg),
                              sizeof(float2) * static_cast<size_t>(lay.rows) * lay.nseg, st>>>(c);
     e = cudaGetLastError();

@@ -8,6 +8,8 @@
 // contraction can differ between kernels.
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include <cstdint>
 
 namespace lp {
@@ -78,6 +80,48 @@ __device__ __forceinline__ float2 tile_lse64(float (&z)[64], int nvalid, int yco
     return make_float2(m, __fadd_rn(s0, s1));
 }
 
+// Entropy variant of tile_lse64: the same m and s (bit-equal: the same operations in the
+// same order), and u = sum over valid columns of e_i * (z_i - m), e_i = exp(z_i - m), as a
+// pairwise tree over each chunk's 32 products (level 0 formed pairwise on the fly), then
+// u = u_0 + u_1.  The row entropy is log s - u / s once the tiles are merged.
+__device__ __forceinline__ float chunk_expsum_ent(float (&v)[32], int nvalid, float m, int ycol,
+                                                  float& zy, float& u) {
+    float w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float t[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int c = 2 * i + k;
+            if (c == ycol) zy = v[c];
+            const float d = __fsub_rn(v[c], m);
+            const float e = (c < nvalid) ? __expf(d) : 0.0f;
+            t[k] = (c < nvalid) ? __fmul_rn(e, d) : 0.0f;
+            v[c] = e;
+        }
+        w[i] = __fadd_rn(t[0], t[1]);
+    }
+#pragma unroll
+    for (int l = 8; l >= 1; l >>= 1) {
+#pragma unroll
+        for (int i = 0; i < l; ++i) w[i] = __fadd_rn(w[2 * i], w[2 * i + 1]);
+    }
+    u = w[0];
+    return tree_sum32(v);
+}
+
+__device__ __forceinline__ float2 tile_lse64_ent(float (&z)[64], int nvalid, int ycol, float& zy,
+                                                 float& u) {
+    float(&z0)[32] = *reinterpret_cast<float(*)[32]>(&z[0]);
+    float(&z1)[32] = *reinterpret_cast<float(*)[32]>(&z[32]);
+    const float m = fmaxf(chunk_max(z0, nvalid), chunk_max(z1, nvalid - 32));
+    float u0, u1;
+    const float s0 = chunk_expsum_ent(z0, nvalid, m, ycol, zy, u0);
+    const float s1 = chunk_expsum_ent(z1, nvalid - 32, m, ycol - 32, zy, u1);
+    u = __fadd_rn(u0, u1);
+    return make_float2(m, __fadd_rn(s0, s1));
+}
+
 // Merge two (max, sum-exp) pairs: m = max(m1, m2), s = s1 e^(m1-m) + s2 e^(m2-m).
 // Two -inf maxima give (-inf, 0); a NaN propagates through s.
 __device__ __forceinline__ float2 lse_merge(float2 a, float2 b) {
@@ -86,6 +130,31 @@ __device__ __forceinline__ float2 lse_merge(float2 a, float2 b) {
     const float s = __fadd_rn(__fmul_rn(a.y, expf(__fsub_rn(a.x, m))),
                               __fmul_rn(b.y, expf(__fsub_rn(b.x, m))));
     return make_float2(m, s);
+}
+
+// Entropy-carrying merge of (m, s, u) triples: m and s exactly as lse_merge, and
+// u = (u1 + (m1 - m) s1) e^(m1-m) + (u2 + (m2 - m) s2) e^(m2-m), the sum of e^(z-m)(z-m)
+// rebased to the common maximum.
+__device__ __forceinline__ float3 lse_merge_ent(float3 a, float3 b) {
+    const float m = fmaxf(a.x, b.x);
+    if (m == -INFINITY) return make_float3(-INFINITY, 0.0f, 0.0f);
+    const float da = __fsub_rn(a.x, m), db = __fsub_rn(b.x, m);
+    const float ea = expf(da), eb = expf(db);
+    const float s = __fadd_rn(__fmul_rn(a.y, ea), __fmul_rn(b.y, eb));
+    const float ua = __fmul_rn(__fadd_rn(a.z, __fmul_rn(da, a.y)), ea);
+    const float ub = __fmul_rn(__fadd_rn(b.z, __fmul_rn(db, b.y)), eb);
+    return make_float3(m, s, __fadd_rn(ua, ub));
+}
+
+// Row entropy from the fully merged triple: log s - u / s.
+__device__ __forceinline__ float entropy_finish(float3 msu) {
+    return __fsub_rn(logf(msu.y), __fdiv_rn(msu.z, msu.y));
+}
+
+// Two fp32 values rounded to bf16 (nearest even), packed low then high.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
 }
 
 // logZ of a fully merged pair.

@@ -80,6 +80,62 @@ class Engine:
                                             _ptr(out_logZ), int(phase), _stream_ptr(stream)))
         return (out, out_logZ) if (return_logZ or out_logZ is not None) else out
 
+    def logprobs_entropy(self, X: torch.Tensor, ids: torch.Tensor, out: torch.Tensor = None,
+                         out_logZ: torch.Tensor = None, out_entropy: torch.Tensor = None,
+                         phase: int = LP_PHASE_AUTO, stream=None):
+        """(logp, logZ, entropy) fp32 [T]: logprobs plus each row's softmax entropy."""
+        _require(X, "X", torch.bfloat16, 2)
+        _require(ids, "ids", torch.int32, 1)
+        T = int(X.shape[0])
+        if X.shape[1] != self.H or X.stride(1) != 1:
+            raise ValueError("X must be [T, H] with unit column stride")
+        if ids.shape[0] != T or not ids.is_contiguous():
+            raise ValueError("ids must be a contiguous [T] tensor")
+        dev = X.device
+        out = torch.empty(T, dtype=torch.float32, device=dev) if out is None else out
+        out_logZ = torch.empty(T, dtype=torch.float32, device=dev) if out_logZ is None else out_logZ
+        if out_entropy is None:
+            out_entropy = torch.empty(T, dtype=torch.float32, device=dev)
+        ldx = X.stride(0) if T > 1 else self.H
+        _native.check(self._lib.lp_logprobs_entropy(
+            self._h, _ptr(X), ldx, _ptr(ids), T, _ptr(out), _ptr(out_logZ), _ptr(out_entropy),
+            int(phase), _stream_ptr(stream)))
+        return out, out_logZ, out_entropy
+
+    # ------------------------------------------------------------------ backward
+    def backward_reserve(self, max_rows: int) -> None:
+        """Allocate the backward's bf16 logit-gradient buffer for chunks of max_rows rows."""
+        with torch.cuda.device(self.device):
+            _native.check(self._lib.lp_backward_reserve(self._h, int(max_rows)))
+
+    def logprobs_backward(self, X: torch.Tensor, ids: torch.Tensor, logZ: torch.Tensor,
+                          grad_logp: torch.Tensor, need_dX: bool = True, need_dW: bool = True,
+                          dX: torch.Tensor = None, dW: torch.Tensor = None,
+                          accumulate: bool = False, stream=None):
+        """(dX fp32 [T, H], dW fp32 [V, H]) for upstream gradient grad_logp = dL/dlogp."""
+        _require(X, "X", torch.bfloat16, 2)
+        _require(ids, "ids", torch.int32, 1)
+        _require(logZ, "logZ", torch.float32, 1)
+        _require(grad_logp, "grad_logp", torch.float32, 1)
+        T = int(X.shape[0])
+        if X.shape[1] != self.H or X.stride(1) != 1:
+            raise ValueError("X must be [T, H] with unit column stride")
+        for t, name in ((ids, "ids"), (logZ, "logZ"), (grad_logp, "grad_logp")):
+            if t.shape[0] != T or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous [T] tensor")
+        dev = X.device
+        if need_dX and dX is None:
+            dX = torch.empty(T, self.H, dtype=torch.float32, device=dev)
+        if need_dW and dW is None:
+            dW = torch.empty(self.V, self.H, dtype=torch.float32, device=dev)
+            accumulate = False
+        ldx = X.stride(0) if T > 1 else self.H
+        _native.check(self._lib.lp_logprobs_backward(
+            self._h, _ptr(X), ldx, _ptr(ids), _ptr(logZ), _ptr(grad_logp), T,
+            _ptr(dX if need_dX else None), _ptr(dW if need_dW else None), int(bool(accumulate)),
+            _stream_ptr(stream)))
+        return (dX if need_dX else None), (dW if need_dW else None)
+
     def logprobs_host(self, X: torch.Tensor, ids: torch.Tensor, out: torch.Tensor = None,
                       out_logZ: torch.Tensor = None, stream=None):
         """Host-memory variant: X, ids, out live in (preferably pinned) CPU memory."""
@@ -287,3 +343,35 @@ class Engine:
 
     def __exit__(self, *exc):
         self.close()
+
+
+class _Logprobs(torch.autograd.Function):
+    """Forward values from the bit-consistent kernel; backward from lp_logprobs_backward."""
+
+    @staticmethod
+    def forward(ctx, X, W, ids, engine):
+        logp, logZ = engine.logprobs(X, ids, return_logZ=True)
+        ctx.engine = engine
+        ctx.save_for_backward(X, ids, logZ)
+        ctx.mark_non_differentiable(logZ)
+        return logp
+
+    @staticmethod
+    def backward(ctx, grad):
+        X, ids, logZ = ctx.saved_tensors
+        need_dX, need_dW = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+        dX, dW = ctx.engine.logprobs_backward(X, ids, logZ, grad.contiguous().float(),
+                                              need_dX=need_dX, need_dW=need_dW)
+        return (dX.to(X.dtype) if dX is not None else None,
+                dW.to(ctx.engine._W.dtype) if dW is not None else None, None, None)
+
+
+def logprobs_with_grad(engine: "Engine", X: torch.Tensor, W: torch.Tensor,
+                       ids: torch.Tensor) -> torch.Tensor:
+    """Differentiable sampled-token logprobs: the values are the engine's bit-consistent
+    forward; gradients with respect to X and W come from the engine's backward.  W must be
+    the tensor the engine was built on (it is referenced, not copied)."""
+    if W.data_ptr() != engine._W.data_ptr():
+        raise ValueError("W must be the engine's lm_head tensor")
+    engine.backward_reserve(min(int(X.shape[0]), engine.max_tokens) or 1)
+    return _Logprobs.apply(X, W, ids, engine)

@@ -121,6 +121,18 @@ LP_API int lp_logprobs(lp_handle* h, const void* X, int64_t ldx, const int32_t* 
                 float* out_logp, float* out_logZ, int phase, void* stream);
 
 /*
+ * lp_logprobs plus the entropy of each row's softmax, H[t] = -sum_v p log p = logZ - sum_v p z
+ * (the actor entropy the pages track beside the KL; vLLM blog "Finish RL training faster",
+ * section 3.2 results).  Per 64-column tile the epilogue also forms
+ * u = sum e^(z-m) (z - m), merged by the same tile tree with the (m, s) partials:
+ * H = log s - u / s.  logp and logZ are bit-equal to lp_logprobs's; H obeys the same
+ * invariance (batch, position, phase, TP split).  out_entropy: device, fp32 [T].
+ */
+LP_API int lp_logprobs_entropy(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids,
+                               int64_t T, float* out_logp, float* out_logZ, float* out_entropy,
+                               int phase, void* stream);
+
+/*
  * Same as lp_logprobs with HOST buffers (X: bf16 [T, ldx]; ids, out_logp,
  * out_logZ as above but in host memory; pinned memory is fastest).  Rows are
  * staged through the handle's device workspace chunk by chunk; the call
@@ -181,6 +193,33 @@ LP_API int lp_importance_weights(lp_handle* h, const float* logp_pi, const float
 LP_API int lp_importance_weights_host(lp_handle* h, const float* logp_pi, const float* logp_mu,
                                       const uint8_t* mask, int64_t T, float* out_w,
                                       double* out_d3, int64_t* out_nvalid, void* stream);
+
+/*
+ * Logprob backward.  For a loss L with upstream gradient g[t] = dL/dlogp[t] (fp32, device
+ * [T]), with logp = lp_logprobs(X, ids) and logZ its out_logZ (device [T]):
+ *   dl[t,v] = g[t] (1[v = y_t] - exp(z[t,v] - logZ[t]))      rounded to bf16, row chunks
+ *   dX[t,:] = sum_v dl[t,v] W[v,:]                            fp32 [T][H] (row stride H)
+ *   dW[v,:] = sum_t dl[t,v] X[t,:]  (added to dW if accumulate) fp32 [V][H]
+ * z is recomputed by the forward's leaf GEMM and tree (the same kernel, a third epilogue),
+ * so dl uses exactly the forward's logits.  The two products are plain GEMMs (cuBLAS, fp32
+ * accumulation).  The pages' recipe keeps forward values from the inference kernel and
+ * differentiates a separate training graph, whose backward need only be correct, not
+ * deterministic (vLLM blog "Finish RL training faster", section 3.1); this backward is
+ * deterministic for a given T and chunking but is not covered by the invariance guarantees.
+ *   dX or dW may be NULL (not computed).  Requires lp_backward_reserve.
+ * Uses the reserved gradient buffer: calls on one handle must be stream-ordered.
+ */
+LP_API int lp_logprobs_backward(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids,
+                                const float* logZ, const float* grad_logp, int64_t T, float* dX,
+                                float* dW, int accumulate, void* stream);
+
+/*
+ * Reserve the backward's workspace for row chunks of max_rows rows: a bf16 buffer
+ * [max_rows][ceil(V/8)*8] (e.g. 4096 rows at V = 151936: 1.24 GB) and a cuBLAS handle with
+ * a 32 MiB workspace.  Allocates and may synchronise the device: call it before any graph
+ * capture.  A smaller request than the current reservation is a no-op.
+ */
+LP_API int lp_backward_reserve(lp_handle* h, int64_t max_rows);
 
 /*
  * Acceptance statistics between two logprob vectors (vLLM blog "Finish RL training
