@@ -56,6 +56,11 @@ SIGNATURES = {
     "lp_logprobs_backward": (ctypes.c_int, [_p, _p, _i64, _p, _p, _p, _i64, _p, _p, ctypes.c_int,
                                             _p]),
     "lp_backward_reserve": (ctypes.c_int, [_p, _i64]),
+    "lp_contract": (ctypes.c_int, [ctypes.POINTER(LpConfig), _p, ctypes.c_size_t,
+                                   ctypes.POINTER(ctypes.c_size_t)]),
+    "lp_contract_digest": (ctypes.c_int, [ctypes.POINTER(LpConfig), ctypes.c_int, _p]),
+    "lp_contract_check": (ctypes.c_int, [ctypes.POINTER(LpConfig), _p, _p]),
+    "lp_sha256": (None, [_p, ctypes.c_size_t, _p]),
     "lp_reinforce_zero": (ctypes.c_int, [_p, _p, _p, _p, _i64, _p, _i64, _p, _i32,
                                          ctypes.POINTER(LpRzOptions), _p, _p, _p, _p, _p, _p]),
     "lp_profile_enable": (ctypes.c_int, [_p, ctypes.c_int]),

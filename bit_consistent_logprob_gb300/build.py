@@ -19,9 +19,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "liblp.so")
-SOURCES = [os.path.join(CSRC, "lp_api.cu"), os.path.join(CSRC, "lp_noalloc.cu")]
+SOURCES = [os.path.join(CSRC, "lp_api.cu"), os.path.join(CSRC, "lp_noalloc.cu"),
+           os.path.join(CSRC, "lp_contract.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("kernels.cuh", "numerics.cuh", "ptx.cuh",
-                                                  "rl_kernels.cuh")] + [
+                                                  "rl_kernels.cuh", "lp_internal.h")] + [
     os.path.join(INCLUDE, "lp.h")]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -18,6 +18,7 @@
 
 #include "kernels.cuh"
 #include "lp.h"
+#include "lp_internal.h"
 #include "rl_kernels.cuh"
 
 namespace {
@@ -385,6 +386,18 @@ int check_x(const lp_handle* h, const void* X, int64_t ldx, int64_t T) {
 }
 
 }  // namespace
+
+int lp_internal_validate_config(const lp_config* c) { return validate_config(c); }
+
+int lp_internal_fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
 
 extern "C" {
 

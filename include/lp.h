@@ -324,6 +324,32 @@ LP_API int lp_logprobs_noalloc(const void* W, int32_t H, int32_t V, int32_t n_le
                                float* out_logp, float* out_logZ, void* stream);
 LP_API const char* lp_noalloc_last_error(void);
 
+/*
+ * Execution contract (IsoExec, SkyRL blog summary, "unified execution contract"): a canonical
+ * JSON description of every execution choice that can change a bit, and SHA-256 identities
+ * of its three sections, so that two runtimes (a trainer and a rollout engine) can prove they
+ * run the same numerics by comparing digests.
+ *   semantic          the logical computation (op, lm_head shape, outputs);
+ *   numerical_policy  cases, composition (implementation ids and versions, pinned constants:
+ *                     leaves, leaf dtype, MMA shape and order, tree shapes, LSE tile and order,
+ *                     exp/log functions, D3 blocks) and claims (proven TP sizes, phases,
+ *                     tolerances);
+ *   deployment        settings proven not to change bits (max_tokens, tp_slices).
+ * Pure host code: no device, no handle.  The configuration is validated as by lp_init.
+ *
+ * lp_contract writes the JSON (NUL-terminated) into buf[cap]; with buf == NULL it only sets
+ * *len (the length without the NUL).  lp_contract_digest writes one 32-byte SHA-256 of the
+ * canonical section.  lp_contract_check compares this configuration's semantic and
+ * numerical_policy digests with a peer's and returns LP_ERR_UNSUPPORTED on a mismatch.
+ * lp_sha256 is the library's SHA-256 (FIPS 180-4), exported for verification.
+ */
+enum { LP_DIGEST_SEMANTIC = 0, LP_DIGEST_NUMERICAL_POLICY = 1, LP_DIGEST_DEPLOYMENT = 2 };
+LP_API int lp_contract(const lp_config* cfg, char* buf, size_t cap, size_t* len);
+LP_API int lp_contract_digest(const lp_config* cfg, int which, uint8_t out[32]);
+LP_API int lp_contract_check(const lp_config* cfg, const uint8_t peer_semantic[32],
+                             const uint8_t peer_numerical_policy[32]);
+LP_API void lp_sha256(const void* data, size_t n, uint8_t out[32]);
+
 /* Synchronise the stream last used with the handle and return the sticky device
  * status (LP_OK, LP_ERR_INVALID_ARG for a bad id, LP_ERR_TIMEOUT). */
 LP_API int lp_check(lp_handle* h);
