@@ -60,6 +60,12 @@ def _load():
         lib.oracle_tree_fp32_many.argtypes = [p, i32, i64, p]
         lib.oracle_acceptance_stats.argtypes = [p, p, p, i64, p]
         lib.oracle_entropy.argtypes = [p, i64, p, i64, i64, p, i64, p]
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = ctypes.c_double
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_quantize_blocks.argtypes = [p, i64, i64, i64, i64, p, p]
+        lib.oracle_logprobs_fp8.argtypes = [p, p, p, p, p, i64, i64, p, i64, p, p]
         lib.oracle_logprobs_f64.argtypes = [p, p, p, i64, i64, i64, p]
         lib.oracle_logprob_grad.argtypes = [p, p, p, p, i64, i64, i64, p, p, p]
         lib.oracle_reinforce_zero.argtypes = [p, p, p, p, i64, p, ctypes.c_int, ctypes.c_int,
@@ -294,3 +300,44 @@ def logprob_grad(X, W, ids, g):
     _load().oracle_logprob_grad(_ptr(Xc), _ptr(Wc), _ptr(ids), _ptr(g), T, H, V, _ptr(dX),
                                 _ptr(dW), _ptr(dl))
     return dX, dW, dl
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib.oracle_e4m3_decode(int(v)) for v in c], dtype=np.float64)
+
+
+def e4m3_encode(values) -> np.ndarray:
+    lib = _load()
+    x = np.asarray(values, dtype=np.float32).ravel()
+    return np.array([lib.oracle_e4m3_encode(float(v)) for v in x], dtype=np.uint8)
+
+
+def quantize_blocks(M, block_rows: int):
+    """Block-FP8 quantisation of a bf16 matrix [rows, cols]: (q uint8 [rows, cols],
+    scales float32 [ceil(rows / block_rows), cols / 128])."""
+    M = np.ascontiguousarray(_u16_2d(M))
+    rows, cols = M.shape
+    assert cols % 128 == 0
+    q = np.empty((rows, cols), dtype=np.uint8)
+    scales = np.empty(((rows + block_rows - 1) // block_rows, cols // 128), dtype=np.float32)
+    _load().oracle_quantize_blocks(_ptr(M), rows, cols, cols, block_rows, _ptr(q), _ptr(scales))
+    return q, scales
+
+
+def logprobs_fp8(xq, sx, wq, sw, ids, rows=None):
+    """Sampled-token logprob and logZ (fp64) from block-FP8 operands."""
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    wq = np.ascontiguousarray(wq, dtype=np.uint8)
+    sx = np.ascontiguousarray(sx, dtype=np.float32)
+    sw = np.ascontiguousarray(sw, dtype=np.float32)
+    T, H = xq.shape
+    V = wq.shape[0]
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    r = _rows_arg(rows, T)
+    logp = np.empty(r.size, dtype=np.float64)
+    logZ = np.empty(r.size, dtype=np.float64)
+    _load().oracle_logprobs_fp8(_ptr(xq), _ptr(sx), _ptr(wq), _ptr(sw), _ptr(ids), H, V, _ptr(r),
+                                r.size, _ptr(logp), _ptr(logZ))
+    return logp, logZ

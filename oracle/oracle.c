@@ -50,6 +50,17 @@
  *      oracle_logprobs_f64 is the logprob definition on real-valued (fp64)
  *      inputs, used to check the gradient by finite differences.
  *
+ *  - oracle_e4m3_encode / oracle_e4m3_decode / oracle_quantize_blocks /
+ *    oracle_logprobs_fp8: the block-FP8 (W8A8) variant the vLLM blog keeps for
+ *      DeepSeek-V4's deployment (section 4.1), with DeepSeek's block rule:
+ *      activation blocks 1 x 128, weight blocks 128 x 128, scale = amax / 448
+ *      in fp32 (1 for an all-zero block), q = e4m3(x / s) with x / s an fp32
+ *      division, rounded to nearest even and saturated to +-448 (the OCP
+ *      E4M3 format: bias 7, 3 mantissa bits, no infinities).  The quantised
+ *      bytes are an integer decision, so they are made in the same fp32
+ *      arithmetic the GPU uses.  The logits are the plain fp64 dot products
+ *      of the dequantised values q * s.
+ *
  *  - oracle_acceptance_stats: over the valid tokens, the max, mean and
  *      population standard deviation of |a - b| between two logprob vectors,
  *      and the k3 KL estimate mean(r - 1 - log r) with r = exp(a - b) (vLLM
@@ -383,5 +394,90 @@ void oracle_logprob_grad(const uint16_t* X, const uint16_t* W, const int32_t* id
             for (int64_t t = 0; t < T; ++t) acc += dl[t * V + v] * bf16_to_f64(X[t * H + k]);
             dW[v * H + k] = acc;
         }
+    }
+}
+
+/* OCP E4M3 (finite-only variant): value of one code. */
+double oracle_e4m3_decode(uint8_t c) {
+    int sgn = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sgn ? -v : v;
+}
+
+/* Nearest E4M3 code to x (ties to even mantissa), saturating to +-448; NaN -> 0x7F. */
+uint8_t oracle_e4m3_encode(float x) {
+    if (isnan(x)) return 0x7F;
+    uint8_t sgn = signbit(x) ? 0x80 : 0;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sgn | 0x7E;
+    if (a < ldexp(1.0, -6)) {                    /* subnormal spacing 2^-9; k = 8 is 2^-6 */
+        double k = nearbyint(a / ldexp(1.0, -9));
+        return sgn | (uint8_t)k;
+    }
+    int E;
+    frexp(a, &E);                                /* a = f 2^E, f in [0.5, 1) */
+    int e = E - 1;                               /* a in [2^e, 2^(e+1)) */
+    double m = nearbyint((a / ldexp(1.0, e) - 1.0) * 8.0);
+    if (m == 8.0) {
+        m = 0.0;
+        e += 1;
+    }
+    int code = ((e + 7) << 3) | (int)m;
+    if (code > 0x7E) code = 0x7E;
+    return sgn | (uint8_t)code;
+}
+
+/* Block quantisation of a bf16 matrix [rows, cols] (row stride ld): blocks of block_rows x 128,
+ * scales [ceil(rows / block_rows)][cols / 128]. */
+void oracle_quantize_blocks(const uint16_t* src, int64_t rows, int64_t cols, int64_t ld,
+                            int64_t block_rows, uint8_t* q, float* scales) {
+    int64_t nkb = cols / 128, nrb = (rows + block_rows - 1) / block_rows;
+    for (int64_t rb = 0; rb < nrb; ++rb) {
+        for (int64_t kb = 0; kb < nkb; ++kb) {
+            int64_t r0 = rb * block_rows, r1 = r0 + block_rows < rows ? r0 + block_rows : rows;
+            float amax = 0.0f;
+            for (int64_t r = r0; r < r1; ++r)
+                for (int64_t k = kb * 128; k < kb * 128 + 128; ++k) {
+                    float v = fabsf((float)bf16_to_f64(src[r * ld + k]));
+                    if (v > amax) amax = v;
+                }
+            float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+            scales[rb * nkb + kb] = s;
+            for (int64_t r = r0; r < r1; ++r)
+                for (int64_t k = kb * 128; k < kb * 128 + 128; ++k)
+                    q[r * cols + k] = oracle_e4m3_encode((float)bf16_to_f64(src[r * ld + k]) / s);
+        }
+    }
+}
+
+/* Sampled-token logprobs from quantised operands: z = sum_k (qx sx)(qw sw) in fp64. */
+void oracle_logprobs_fp8(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
+                         const int32_t* ids, int64_t H, int64_t V, const int64_t* rows,
+                         int64_t nrows, double* logp, double* logZ) {
+    int64_t nkb = H / 128;
+#pragma omp parallel
+    {
+        double* z = (double*)malloc((size_t)V * sizeof(double));
+        double* xd = (double*)malloc((size_t)H * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < nrows; ++r) {
+            int64_t t = rows[r];
+            for (int64_t k = 0; k < H; ++k)
+                xd[k] = oracle_e4m3_decode(xq[t * H + k]) * (double)sx[t * nkb + k / 128];
+            for (int64_t v = 0; v < V; ++v) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < H; ++k)
+                    acc += xd[k] * (oracle_e4m3_decode(wq[v * H + k]) *
+                                    (double)sw[(v / 128) * nkb + k / 128]);
+                z[v] = acc;
+            }
+            double lz = log_partition(z, V);
+            int32_t y = ids[t];
+            logZ[r] = lz;
+            logp[r] = (y >= 0 && (int64_t)y < V) ? z[y] - lz : NAN;
+        }
+        free(xd);
+        free(z);
     }
 }

@@ -527,6 +527,94 @@ def test_logprob_grad_identical_rows_give_zero_dx():
     np.testing.assert_allclose(dl[0, 3], 1 - 1 / V, rtol=1e-14)
 
 
+# ----------------------------------------------------------------- block FP8
+def _torch_e4m3():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("this torch has no float8_e4m3fn")
+    return torch
+
+
+def test_e4m3_codes_match_the_library_format():
+    torch = _torch_e4m3()
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().double().numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    assert np.array_equal(ours[~np.isnan(ours)], ref[~np.isnan(ref)])
+    assert ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9 and ours[0x08] == 2.0 ** -6
+
+
+def test_e4m3_rounding_matches_the_library_and_saturates():
+    torch = _torch_e4m3()
+    rng = np.random.default_rng(70)
+    x = np.concatenate([rng.uniform(-448, 448, 20000), rng.uniform(-0.03, 0.03, 20000),
+                        # exact ties between neighbours: 1 + 1/16 lies between 1 and 1.125
+                        [1.0625, -1.0625, 1.1875, 2.0 ** -10, 3 * 2.0 ** -10, 416.0, 432.0]])
+    x = x.astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(x), ref)
+    assert oracle.e4m3_encode([1.0625])[0] == 0x38          # tie to the even mantissa: 1.0
+    assert oracle.e4m3_encode([1.1875])[0] == 0x3A          # tie to even: 1.25
+    sat = oracle.e4m3_encode([449.0, 1e30, -500.0, 464.0])
+    assert sat.tolist() == [0x7E, 0x7E, 0xFE, 0x7E]         # saturate to +-448
+
+
+def test_block_quantisation_rule():
+    rng = np.random.default_rng(71)
+    M = f32_to_bf16_bits(rng.standard_normal((130, 256)).astype(np.float32) * 0.05)
+    M[7, 3:131] = 0  # an all-zero 1 x 128 block
+    for block_rows in (1, 128):
+        q, s = oracle.quantize_blocks(M, block_rows)
+        vals = np.array([[float(bits_to_fraction(b)) for b in row] for row in M], dtype=np.float32)
+        for rb in range(s.shape[0]):
+            for kb in range(2):
+                blk = vals[rb * block_rows:(rb + 1) * block_rows, kb * 128:(kb + 1) * 128]
+                amax = np.float32(np.abs(blk).max())
+                want = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+                assert s[rb, kb] == want
+                deq = oracle.e4m3_decode(q[rb * block_rows:(rb + 1) * block_rows,
+                                           kb * 128:(kb + 1) * 128]).reshape(blk.shape)
+                if amax > 0:
+                    assert np.abs(deq).max() == 448.0  # the block maximum maps to +-448
+                # every value within half a step of its e4m3 neighbour (relative 2^-4)
+                err = np.abs(deq - blk.astype(np.float64) / float(s[rb, kb]))
+                assert np.all(err <= np.maximum(np.abs(deq) * 2.0 ** -4, 2.0 ** -10))
+
+
+def test_logprobs_fp8_equals_the_bf16_oracle_on_representable_inputs():
+    # blocks whose maximum is 448 and whose values are e4m3 numbers quantise to themselves
+    # with scale 1, so the block-FP8 logprob must equal the bf16 logprob of the same values
+    rng = np.random.default_rng(72)
+    grid = oracle.e4m3_decode(np.arange(1, 0x7F, dtype=np.uint8))  # nonzero, so signs survive
+    grid = np.concatenate([grid, -grid])
+    def rep(shape):
+        v = rng.choice(grid[np.abs(grid) <= 2.0], size=shape)
+        v[:, ::128] = 448.0
+        return v.astype(np.float32)
+    X = f32_to_bf16_bits(rep((5, 256)) / 1.0)
+    W = f32_to_bf16_bits(np.concatenate([rep((128, 256)), rep((3, 256))]))
+    ids = np.array([0, 130, 7, 64, 129], dtype=np.int32)
+    xq, sx = oracle.quantize_blocks(X, 1)
+    wq, sw = oracle.quantize_blocks(W, 128)
+    assert np.all(sx == 1.0) and np.all(sw == 1.0)
+    lp8, lz8 = oracle.logprobs_fp8(xq, sx, wq, sw, ids)
+    lp, lz = oracle.logprobs(X, W, ids)
+    np.testing.assert_allclose(lp8, lp, rtol=0, atol=1e-9)
+    np.testing.assert_allclose(lz8, lz, rtol=1e-15, atol=0)
+    # and scaling a weight block by 2^-3 moves its scale, not its codes
+    W2 = W.copy()
+    W2[:128, 128:] = f32_to_bf16_bits(np.array([[float(bits_to_fraction(b)) for b in row]
+                                                 for row in W[:128, 128:]]) / 8.0)
+    wq2, sw2 = oracle.quantize_blocks(W2, 128)
+    assert np.array_equal(wq2, wq) and sw2[0, 1] == 0.125 and sw2[0, 0] == 1.0
+    # with unequal (power-of-two) block scales the dequantised values are still exact in bf16
+    lp8, lz8 = oracle.logprobs_fp8(xq, sx, wq2, sw2, ids)
+    lp, lz = oracle.logprobs(X, W2, ids)
+    np.testing.assert_allclose(lp8, lp, rtol=0, atol=1e-9)
+    np.testing.assert_allclose(lz8, lz, rtol=1e-15, atol=0)
+
+
 # ----------------------------------------------------------------- planted mistakes
 MUTATIONS = [
     # (description, original text, mutated text)
@@ -555,6 +643,13 @@ MUTATIONS = [
      "dl[t * V + v] = g[t] * (onehot - exp(z[v]));"),
     ("dW with a transposed operand", "acc += dl[t * V + v] * bf16_to_f64(X[t * H + k]);",
      "acc += dl[t * V + v] * bf16_to_f64(W[v * H + k]);"),
+    ("e4m3 ties away from zero", "double m = nearbyint((a / ldexp(1.0, e) - 1.0) * 8.0);",
+     "double m = floor((a / ldexp(1.0, e) - 1.0) * 8.0 + 0.5);"),
+    ("e4m3 without saturation", "if (a >= 448.0) return sgn | 0x7E;", "if (a >= 480.0) return sgn | 0x7F;"),
+    ("block scale against 224", "float s = amax > 0.0f ? amax / 448.0f : 1.0f;",
+     "float s = amax > 0.0f ? amax / 224.0f : 1.0f;"),
+    ("weight scale with a transposed block index", "(double)sw[(v / 128) * nkb + k / 128]",
+     "(double)sw[(k / 128) * nkb + v / 128]"),
     ("sequence gate on the last token only", "lr += (double)logp_pi[t] - (double)logp_mu[t];",
      "lr = (double)logp_pi[t] - (double)logp_mu[t];"),
 ]
@@ -595,7 +690,10 @@ def test_pins_catch_planted_mistake(tmp_path, monkeypatch, golden_dir, desc, ori
             test_reinforce_zero_sequence_gate_drops_whole_responses,
             test_reinforce_zero_token_gate_and_empty_response,
             test_entropy_closed_forms, test_entropy_bounds_and_decimal_brute_force,
-            test_logprob_grad_is_the_derivative, test_logprob_grad_identical_rows_give_zero_dx]
+            test_logprob_grad_is_the_derivative, test_logprob_grad_identical_rows_give_zero_dx,
+            test_e4m3_codes_match_the_library_format,
+            test_e4m3_rounding_matches_the_library_and_saturates, test_block_quantisation_rule,
+            test_logprobs_fp8_equals_the_bf16_oracle_on_representable_inputs]
     failed = 0
     for pin in pins:
         try:
