@@ -335,7 +335,7 @@ def run_ours(args, world, rank, local, pg):
     T, H, V, N = X.shape[0], wl.H, wl.V, wl.n_leaves
     max_tokens = min(T, args.max_tokens)
     mu = rollout_logprobs(W, X, ids, wl, wl.seed + rank, max_tokens)
-    eng = Engine(W, n_leaves=N, max_tokens=max_tokens)
+    eng = Engine(W, n_leaves=N, max_tokens=max_tokens, fp8=args.fp8)
     phase = LP_PHASE_DECODE if args.workload == "ds_decode" else LP_PHASE_PREFILL
     logp = torch.empty(T, dtype=torch.float32, device=dev)
     w = torch.empty(T, dtype=torch.float32, device=dev)
@@ -409,7 +409,9 @@ def run_ours(args, world, rank, local, pg):
     if args.workload == "ds_decode":
         # HBM-bound: W streamed once per step plus X and the per-tile partials.
         nb = (V + 63) // 64  # (max, sum-exp) partial per 64-column tile
-        algo = (2 * H * V + 2 * T * H + 8 * T * nb + 8 * T) / launches_per_step
+        wbytes = H * V + 4 * ((V + 127) // 128) * (H // 128) if args.fp8 else 2 * H * V
+        xbytes = T * H + 4 * T * (H // 128) if args.fp8 else 2 * T * H
+        algo = (wbytes + xbytes + 8 * T * nb + 8 * T) / launches_per_step
         achieved = algo / (gemm_avg_ms / 1000.0) / 1e9
         peak = float(peaks["hbm_gbs"])
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -418,17 +420,20 @@ def run_ours(args, world, rank, local, pg):
         algo = 2.0 * T * H * V / launches_per_step
         achieved = algo / (gemm_avg_ms / 1000.0) / 1e12
         peak = float(peaks["bf16_tflops_sustained"])
+        src = (f"{peak_src} bf16_tflops_sustained (kernel timed inside a back-to-back step "
+               f"loop)")
+        if args.fp8:  # dense fp8 = 2 x bf16 (nominal 4.5 / 2.25 PFLOP/s)
+            peak *= 2.0
+            src = f"{src} x 2, the nominal fp8/bf16 ratio"
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak,
-                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a "
-                               f"back-to-back step loop)"}
-    roof["traffic"] = recorded_traffic(args.workload)
-    roof["kernel"] = "leaf_gemm_kernel<fused>"
+                "frac": achieved / peak, "peak_source": src}
+    roof["traffic"] = recorded_traffic(args.workload + ("_fp8" if args.fp8 else ""))
+    roof["kernel"] = "leaf_gemm_fp8_kernel" if args.fp8 else "leaf_gemm_kernel<fused>"
     roof["kernel_ms"] = gemm_avg_ms
     roof["algorithmic_per_launch"] = algo
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.fp8:
         cpu = cpu_baseline(X, W, ids, mu, wl, rows=args.cpu_rows)
     eng.close()
 
@@ -438,8 +443,9 @@ def run_ours(args, world, rank, local, pg):
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "T": T, "H": H, "V": V, "n_leaves": N,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 block-FP8" if args.fp8 else "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.name + ("+fp8" if args.fp8 else ""), "T": T, "H": H, "V": V, "n_leaves": N,
                    "n_seqs": len(lengths), "phase": "decode" if phase == LP_PHASE_DECODE else "prefill",
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
                    "l2": f"inputs larger than L2 (W {2 * H * V / 1e6:.0f} MB streamed every step)",
@@ -586,6 +592,8 @@ def parse_args(argv=None):
     ap.add_argument("--ref-step-seconds", type=float, default=1.5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="block-FP8 (W8A8) handle: 1x128 activation, 128x128 weight blocks")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

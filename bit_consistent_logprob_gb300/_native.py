@@ -56,6 +56,10 @@ SIGNATURES = {
     "lp_logprobs_backward": (ctypes.c_int, [_p, _p, _i64, _p, _p, _p, _i64, _p, _p, ctypes.c_int,
                                             _p]),
     "lp_backward_reserve": (ctypes.c_int, [_p, _i64]),
+    "lp_init_fp8": (ctypes.c_int, [ctypes.POINTER(LpConfig), _p, _p, ctypes.POINTER(_p)]),
+    "lp_fp8_requantize": (ctypes.c_int, [_p, _p]),
+    "lp_fp8_weights": (ctypes.c_int, [_p, ctypes.POINTER(_p), ctypes.POINTER(_p)]),
+    "lp_fp8_quantize_x": (ctypes.c_int, [_p, _p, _i64, _i64, _p, _p, _p]),
     "lp_contract": (ctypes.c_int, [ctypes.POINTER(LpConfig), _p, ctypes.c_size_t,
                                    ctypes.POINTER(ctypes.c_size_t)]),
     "lp_contract_digest": (ctypes.c_int, [ctypes.POINTER(LpConfig), ctypes.c_int, _p]),

@@ -22,7 +22,8 @@ LIB_PATH = os.path.join(BUILD_DIR, "liblp.so")
 SOURCES = [os.path.join(CSRC, "lp_api.cu"), os.path.join(CSRC, "lp_noalloc.cu"),
            os.path.join(CSRC, "lp_contract.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("kernels.cuh", "numerics.cuh", "ptx.cuh",
-                                                  "rl_kernels.cuh", "lp_internal.h")] + [
+                                                  "rl_kernels.cuh", "lp_internal.h",
+                                                  "fp8_kernels.cuh")] + [
     os.path.join(INCLUDE, "lp.h")]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

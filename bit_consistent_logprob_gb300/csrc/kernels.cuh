@@ -65,6 +65,9 @@ struct GemmParams {
     const float* gout;        // [T] dLoss/dlogp per row (kModeGrad)
     uint16_t* dl;             // [T][ldd] bf16 gradient with respect to the logits (kModeGrad)
     int64_t ldd;
+    const float* sx;          // [T][nkb] activation block scales (block-FP8 kernel)
+    const float* sw;          // [num_vocab_tiles][nkb] weight block scales (block-FP8 kernel)
+    int32_t nkb;              // 128-K blocks over H (block-FP8 kernel)
     int* status;              // sticky device status word
     uint64_t timeout_ns;      // bound on every mbarrier wait
 };

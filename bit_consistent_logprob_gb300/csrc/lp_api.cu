@@ -18,6 +18,7 @@
 
 #include "kernels.cuh"
 #include "lp.h"
+#include "fp8_kernels.cuh"
 #include "lp_internal.h"
 #include "rl_kernels.cuh"
 
@@ -72,15 +73,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // K-major bf16 matrix [rows, K] with a row stride of `ld` elements, read in 128 x 64
 // boxes with 128-byte swizzling (the layout the tcgen05 descriptors expect).  Rows past
 // `rows` read as zero.
+// K-major 2-D tensor map with 128-byte-wide boxes (64 bf16 or 128 one-byte elements) and the
+// 128-byte swizzle the MMA descriptors expect.
 int encode_kmajor(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K, uint64_t ld,
-                  uint32_t box_rows = lp::kBM) {
+                  uint32_t box_rows = lp::kBM, bool bytes = false) {
     auto enc = tensor_map_encoder();
     if (enc == nullptr) return fail(LP_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    const uint64_t esize = bytes ? 1 : 2;
     cuuint64_t dims[2] = {K, rows};
-    cuuint64_t strides[1] = {ld * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(lp::kBK), box_rows};
+    cuuint64_t strides[1] = {ld * esize};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+    CUresult r = enc(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     2, const_cast<void*>(base), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(LP_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
@@ -127,6 +132,14 @@ struct lp_handle {
     float* is_stage = nullptr;      // [3][kIsStage]: log pi, log mu, w of one pass
     uint8_t* is_mask_stage = nullptr;
     double* scalars = nullptr;      // [2]: D3 and n_valid of the host IS call
+    // block-FP8 handles (lp_init_fp8)
+    bool fp8 = false;
+    uint8_t* wq = nullptr;          // [V][H] e4m3 lm_head
+    float* sw = nullptr;            // [num_vocab_tiles][H/128] weight block scales
+    uint8_t* xq = nullptr;          // [max_tokens][H] e4m3 activations of one chunk
+    float* sx = nullptr;            // [max_tokens][H/128] activation block scales
+    CUtensorMap tmWq{};
+    int band_fp8 = 0;
     cudaStream_t last_stream = nullptr;
     int64_t ws_bytes = 0;
     int32_t last_launches = 0;
@@ -338,12 +351,75 @@ int launch_partials_lse(lp_handle* h, const float* parts, int n_parts, int64_t p
     return LP_OK;
 }
 
+// Block-FP8 path for one chunk: quantise the rows (1 x 128 blocks), then the block-scaled leaf
+// GEMM with the fused tile log-sum-exp (one CTA per tile, X box cut to the rows when T < 128).
+int launch_fp8_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int rows,
+                     cudaStream_t st) {
+    const int H = h->cfg.H;
+    const int nkb = H / lp::kQBlock;
+    const int64_t warps = static_cast<int64_t>(rows) * nkb;
+    lp::quant_x_kernel<<<static_cast<unsigned>(ceil_div(warps, 8)), 256, 0, st>>>(
+        static_cast<const uint16_t*>(X), ldx, rows, H, h->xq, H, h->sx);
+    LP_CUDA(cudaGetLastError(), "quant_x_kernel launch");
+    ++h->last_launches;
+    lp::GemmParams p{};
+    p.T = rows;
+    p.V = h->cfg.V;
+    p.leaf_len = h->leaf_len;
+    p.leaf_begin = 0;
+    p.leaf_count = h->cfg.n_leaves;
+    p.num_row_tiles = static_cast<int32_t>(ceil_div(rows, lp::kBM));
+    p.num_vocab_tiles = h->num_vocab_tiles;
+    p.num_lse_tiles = h->num_lse_tiles;
+    p.band = h->band_fp8;
+    p.x_box_rows = static_cast<int32_t>(x_box_rows(rows));
+    p.ids = ids;
+    p.ws_ms = h->ws_ms;
+    p.ws_ld = h->cfg.max_tokens;
+    p.zy = h->zy;
+    p.sx = h->sx;
+    p.sw = h->sw;
+    p.nkb = nkb;
+    p.status = h->status;
+    p.timeout_ns = h->timeout_ns;
+    CUtensorMap tmX;
+    int rc = encode_kmajor(&tmX, h->xq, static_cast<uint64_t>(rows), H, H,
+                           static_cast<uint32_t>(p.x_box_rows), true);
+    if (rc != LP_OK) return rc;
+    const int64_t tiles = static_cast<int64_t>(p.num_row_tiles) * h->num_vocab_tiles;
+    if (tiles > 0x7fffffff) return fail(LP_ERR_UNSUPPORTED, "too many tiles in one launch");
+    const int grid = static_cast<int>(tiles < h->num_sms ? tiles : h->num_sms);
+    const bool prof = h->profiling && h->prof_used < kProfPairs;
+    if (prof) LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used], st), "profile event");
+    lp::leaf_gemm_fp8_kernel<<<grid, lp::kGemmThreads, lp::fp8_smem_bytes(), st>>>(tmX, h->tmWq, p);
+    LP_CUDA(cudaGetLastError(), "leaf_gemm_fp8_kernel launch");
+    if (prof) {
+        LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used + 1], st), "profile event");
+        ++h->prof_used;
+    }
+    ++h->last_launches;
+    return LP_OK;
+}
+
+// Quantise the referenced bf16 lm_head into the handle's e4m3 copy (128 x 128 blocks).
+int quantize_weights(lp_handle* h, cudaStream_t st) {
+    const dim3 grid(static_cast<unsigned>(h->cfg.H / lp::kQBlock),
+                    static_cast<unsigned>(h->num_vocab_tiles));
+    lp::quant_w_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(h->W), h->cfg.V,
+                                             h->cfg.H, h->wq, h->sw);
+    LP_CUDA(cudaGetLastError(), "quant_w_kernel launch");
+    return LP_OK;
+}
+
 // Fused path or emulated tensor-parallel path for one chunk of rows (rows <= max_tokens).
 int logprobs_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int rows,
                    float* out_logp, float* out_logZ, float* out_entropy, cudaStream_t st) {
     int rc;
     const int s = h->cfg.tp_slices;
-    if (s == 1) {
+    if (h->fp8) {
+        rc = launch_fp8_chunk(h, X, ldx, ids, rows, st);
+        if (rc != LP_OK) return rc;
+    } else if (s == 1) {
         rc = out_entropy
                  ? launch_leaf_gemm<lp::kModeLseEnt>(h, X, ldx, rows, 0, h->cfg.n_leaves, ids,
                                                      nullptr, 0, st)
@@ -417,6 +493,10 @@ void lp_free(lp_handle* h) {
     cudaFree(h->zy);
     cudaFree(h->status);
     cudaFree(h->ws_u);
+    cudaFree(h->wq);
+    cudaFree(h->sw);
+    cudaFree(h->xq);
+    cudaFree(h->sx);
     cudaFree(h->dl);
     cudaFree(h->cublas_ws);
     if (h->cublas) cublasDestroy(h->cublas);
@@ -436,11 +516,18 @@ void lp_free(lp_handle* h) {
     delete h;
 }
 
-int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out) {
+namespace {
+int init_impl(const lp_config* cfg, const void* W, void* stream, lp_handle** out, bool fp8) {
     if (out == nullptr) return fail(LP_ERR_INVALID_ARG, "out handle pointer is NULL");
     *out = nullptr;
     int rc = validate_config(cfg);
     if (rc != LP_OK) return rc;
+    if (fp8 && cfg->H % (lp::kQBlock * cfg->n_leaves) != 0)
+        return fail(LP_ERR_UNSUPPORTED,
+                    "block FP8 needs H (%d) to be a multiple of 128 * n_leaves (%d)", cfg->H,
+                    lp::kQBlock * cfg->n_leaves);
+    if (fp8 && cfg->tp_slices != 1)
+        return fail(LP_ERR_UNSUPPORTED, "block FP8 runs the fused path only (tp_slices = 1)");
     if (W == nullptr) return fail(LP_ERR_INVALID_ARG, "W is NULL");
     if (!aligned16(W)) return fail(LP_ERR_INVALID_ARG, "W must be 16-byte aligned");
 
@@ -481,6 +568,14 @@ int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out) 
         const int b = std::atoi(e);
         if (b >= 2 && b <= 1024) h->band = b & ~1;
     }
+    {
+        // e4m3 weights are one byte: twice the tiles fit the same L2 budget
+        const int64_t per_tile = static_cast<int64_t>(lp::kVT) * cfg->H;
+        int64_t b = (int64_t(28) << 20) / per_tile;
+        b = b < 8 ? 8 : (b > 128 ? 128 : b);
+        h->band_fp8 = static_cast<int>(b) & ~1;
+    }
+    h->fp8 = fp8;
 
     auto cleanup = [&](int code) {
         lp_free(h);
@@ -543,8 +638,77 @@ int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out) 
     if ((e = cudaMemsetAsync(h->status, 0, sizeof(int), st)) != cudaSuccess ||
         (e = cudaStreamSynchronize(st)) != cudaSuccess)
         return cleanup(cuda_fail(e, "status init"));
+    if (fp8) {
+        const int nkb = cfg->H / lp::kQBlock;
+        if ((rc = alloc(reinterpret_cast<void**>(&h->wq),
+                        static_cast<size_t>(cfg->V) * cfg->H, "wq")) ||
+            (rc = alloc(reinterpret_cast<void**>(&h->sw),
+                        sizeof(float) * static_cast<size_t>(h->num_vocab_tiles) * nkb, "sw")) ||
+            (rc = alloc(reinterpret_cast<void**>(&h->xq), static_cast<size_t>(mt) * cfg->H, "xq")) ||
+            (rc = alloc(reinterpret_cast<void**>(&h->sx), sizeof(float) * static_cast<size_t>(mt) * nkb,
+                        "sx")))
+            return cleanup(rc);
+        if ((e = cudaFuncSetAttribute(lp::leaf_gemm_fp8_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      lp::fp8_smem_bytes())) != cudaSuccess)
+            return cleanup(cuda_fail(e, "cudaFuncSetAttribute(leaf_gemm_fp8_kernel)"));
+        if ((rc = encode_kmajor(&h->tmWq, h->wq, static_cast<uint64_t>(cfg->V), cfg->H, cfg->H,
+                                lp::kBM, true)) != LP_OK ||
+            (rc = quantize_weights(h, st)) != LP_OK)
+            return cleanup(rc);
+        if ((e = cudaStreamSynchronize(st)) != cudaSuccess)
+            return cleanup(cuda_fail(e, "weight quantisation"));
+    }
     h->last_stream = st;
     *out = h;
+    return LP_OK;
+}
+}  // namespace
+
+int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out) {
+    return init_impl(cfg, W, stream, out, false);
+}
+
+int lp_init_fp8(const lp_config* cfg, const void* W, void* stream, lp_handle** out) {
+    return init_impl(cfg, W, stream, out, true);
+}
+
+int lp_fp8_requantize(lp_handle* h, void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    if (!h->fp8) return fail(LP_ERR_INVALID_ARG, "not a block-FP8 handle");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    h->last_stream = st;
+    h->last_launches = 1;
+    return quantize_weights(h, st);
+}
+
+int lp_fp8_quantize_x(lp_handle* h, const void* X, int64_t ldx, int64_t T, uint8_t* xq, float* sx,
+                      void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    int rc = check_x(h, X, ldx, T);
+    if (rc != LP_OK) return rc;
+    if (T > 0 && (xq == nullptr || sx == nullptr))
+        return fail(LP_ERR_INVALID_ARG, "xq and sx must not be NULL");
+    if (h->cfg.H % lp::kQBlock != 0) return fail(LP_ERR_UNSUPPORTED, "H must be a multiple of 128");
+    if (reinterpret_cast<uintptr_t>(xq) % 4 != 0)
+        return fail(LP_ERR_INVALID_ARG, "xq must be 4-byte aligned");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    h->last_stream = st;
+    h->last_launches = 0;
+    if (T == 0) return LP_OK;
+    const int64_t warps = T * (h->cfg.H / lp::kQBlock);
+    if (ceil_div(warps, 8) > 0x7fffffff) return fail(LP_ERR_UNSUPPORTED, "T too large");
+    lp::quant_x_kernel<<<static_cast<unsigned>(ceil_div(warps, 8)), 256, 0, st>>>(
+        static_cast<const uint16_t*>(X), ldx, T, h->cfg.H, xq, h->cfg.H, sx);
+    LP_CUDA(cudaGetLastError(), "quant_x_kernel launch");
+    h->last_launches = 1;
+    return LP_OK;
+}
+
+int lp_fp8_weights(const lp_handle* h, const uint8_t** wq, const float** sw) {
+    if (h == nullptr || !h->fp8) return fail(LP_ERR_INVALID_ARG, "not a block-FP8 handle");
+    if (wq) *wq = h->wq;
+    if (sw) *sw = h->sw;
     return LP_OK;
 }
 
@@ -583,6 +747,8 @@ int lp_logprobs(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, in
 int lp_logprobs_entropy(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int64_t T,
                         float* out_logp, float* out_logZ, float* out_entropy, int phase,
                         void* stream) {
+    if (h != nullptr && h->fp8)
+        return fail(LP_ERR_UNSUPPORTED, "entropy is not built for block-FP8 handles");
     if (T > 0 && out_entropy == nullptr)
         return fail(LP_ERR_INVALID_ARG, "out_entropy must not be NULL");
     return logprobs_impl(h, X, ldx, ids, T, out_logp, out_logZ, out_entropy, phase, stream);
@@ -636,6 +802,7 @@ int lp_logprobs_backward(lp_handle* h, const void* X, int64_t ldx, const int32_t
     if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
     int rc = check_x(h, X, ldx, T);
     if (rc != LP_OK) return rc;
+    if (h->fp8) return fail(LP_ERR_UNSUPPORTED, "the backward is not built for block-FP8 handles");
     if (h->dl == nullptr)
         return fail(LP_ERR_INVALID_ARG, "call lp_backward_reserve before lp_logprobs_backward");
     if (T > 0 && (ids == nullptr || logZ == nullptr || grad_logp == nullptr))
@@ -727,6 +894,7 @@ int lp_logprobs_host(lp_handle* h, const void* X, int64_t ldx, const int32_t* id
 int lp_logits_partial(lp_handle* h, const void* X, int64_t ldx, int64_t T, int32_t leaf_begin,
                       int32_t leaf_count, float* out, int64_t ldo, void* stream) {
     if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    if (h->fp8) return fail(LP_ERR_UNSUPPORTED, "tree nodes are not exported by block-FP8 handles");
     int rc = check_x(h, X, ldx, T);
     if (rc != LP_OK) return rc;
     if (!is_pow2(leaf_count) || leaf_begin < 0 || leaf_begin % leaf_count != 0 ||
@@ -755,6 +923,7 @@ int lp_logprobs_from_partials(lp_handle* h, const float* partials, int32_t n_par
                               int64_t part_stride, int64_t ldp, const int32_t* ids, int64_t T,
                               float* out_logp, float* out_logZ, void* stream) {
     if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    if (h->fp8) return fail(LP_ERR_UNSUPPORTED, "block-FP8 handles run the fused path only");
     if (!(n_parts == 1 || n_parts == 2 || n_parts == 4 || n_parts == 8) ||
         h->cfg.n_leaves % n_parts != 0)
         return fail(LP_ERR_UNSUPPORTED, "n_parts must be 1, 2, 4 or 8 and divide n_leaves");

@@ -22,6 +22,19 @@ def _ptr(t) -> ctypes.c_void_p:
     return ctypes.c_void_p(0 if t is None else t.data_ptr())
 
 
+class _DeviceArray:
+    """A borrowed device buffer described by the CUDA array interface (no copy)."""
+
+    def __init__(self, ptr, shape, typestr):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
+                                         "data": (int(ptr), False), "version": 3, "strides": None}
+
+
+def _device_view(ptr, shape, typestr, device):
+    with torch.cuda.device(device):
+        return torch.as_tensor(_DeviceArray(ptr, shape, typestr), device=device)
+
+
 def _require(t: torch.Tensor, name: str, dtype, ndim: int, device_type="cuda"):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -40,10 +53,12 @@ class Engine:
     n_leaves: N contiguous K leaves combined by the fixed pairwise tree (1, 2, 4, 8).
     tp_slices: emulated tensor-parallel split of K for ``logprobs`` (1 = fused path).
     max_tokens: rows per pass; sizes the workspace.
+    fp8: block-FP8 (W8A8) handle: W is quantised to e4m3 in 128 x 128 blocks at construction
+    (and by ``fp8_requantize``), each batch of X in 1 x 128 blocks per call.
     """
 
     def __init__(self, W: torch.Tensor, n_leaves: int = 8, tp_slices: int = 1,
-                 max_tokens: int = 16384, stream=None):
+                 max_tokens: int = 16384, stream=None, fp8: bool = False):
         _require(W, "W", torch.bfloat16, 2)
         if not W.is_contiguous():
             raise ValueError("W must be contiguous")
@@ -54,10 +69,11 @@ class Engine:
         cfg = LpConfig(self.H, self.V, self.n_leaves, self.tp_slices, self.max_tokens)
         h = ctypes.c_void_p()
         with torch.cuda.device(W.device):
-            _native.check(self._lib.lp_init(ctypes.byref(cfg), _ptr(W), _stream_ptr(stream),
-                                            ctypes.byref(h)))
+            init = self._lib.lp_init_fp8 if fp8 else self._lib.lp_init
+            _native.check(init(ctypes.byref(cfg), _ptr(W), _stream_ptr(stream), ctypes.byref(h)))
         self._h = h
         self.device = W.device
+        self.fp8 = bool(fp8)
 
     # ------------------------------------------------------------------ logprobs
     def logprobs(self, X: torch.Tensor, ids: torch.Tensor, out: torch.Tensor = None,
@@ -101,6 +117,30 @@ class Engine:
             self._h, _ptr(X), ldx, _ptr(ids), T, _ptr(out), _ptr(out_logZ), _ptr(out_entropy),
             int(phase), _stream_ptr(stream)))
         return out, out_logZ, out_entropy
+
+    # ------------------------------------------------------------------ block FP8
+    def fp8_requantize(self, stream=None) -> None:
+        """Re-quantise the referenced bf16 lm_head (after an in-place update)."""
+        _native.check(self._lib.lp_fp8_requantize(self._h, _stream_ptr(stream)))
+
+    def fp8_weights(self):
+        """(wq uint8 [V, H], sw fp32 [ceil(V/128), H/128]): copies of the handle's e4m3 lm_head."""
+        wq, sw = ctypes.c_void_p(), ctypes.c_void_p()
+        _native.check(self._lib.lp_fp8_weights(self._h, ctypes.byref(wq), ctypes.byref(sw)))
+        nvb, nkb = (self.V + 127) // 128, self.H // 128
+        return (_device_view(wq.value, (self.V, self.H), "|u1", self.device).clone(),
+                _device_view(sw.value, (nvb, nkb), "<f4", self.device).clone())
+
+    def fp8_quantize_x(self, X: torch.Tensor, stream=None):
+        """The activation rule alone: (xq uint8 [T, H], sx fp32 [T, H/128])."""
+        _require(X, "X", torch.bfloat16, 2)
+        T = int(X.shape[0])
+        xq = torch.empty(T, self.H, dtype=torch.uint8, device=X.device)
+        sx = torch.empty(T, self.H // 128, dtype=torch.float32, device=X.device)
+        ldx = X.stride(0) if T > 1 else self.H
+        _native.check(self._lib.lp_fp8_quantize_x(self._h, _ptr(X), ldx, T, _ptr(xq), _ptr(sx),
+                                                  _stream_ptr(stream)))
+        return xq, sx
 
     # ------------------------------------------------------------------ backward
     def backward_reserve(self, max_rows: int) -> None:

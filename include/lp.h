@@ -195,6 +195,35 @@ LP_API int lp_importance_weights_host(lp_handle* h, const float* logp_pi, const 
                                       double* out_d3, int64_t* out_nvalid, void* stream);
 
 /*
+ * Block-FP8 (W8A8) handle.  The deployment recipe keeps the lm_head GEMM in block FP8 on both
+ * sides: the trainer quantises its master bf16 weights by the deployment rule and calls the
+ * inference GEMM (vLLM blog "Finish RL training faster", section 4.1).  The rule (DeepSeek's
+ * block rule): activations in 1 x 128 blocks, weights in 128 x 128 blocks, scale
+ * s = amax / 448 (fp32; 1 for an all-zero block), q = e4m3(x / s) rounded to nearest even and
+ * saturated to +-448.  Then, per 128-K block kb, B_kb = sum qx qw (tcgen05 kind::f8f6f4, fp32);
+ * per leaf P_j = sum over its blocks, ascending, of (sx sw) B_kb (a product, then one fma
+ * per block); z = the same fixed pairwise leaf tree, and the same log-sum-exp and combine.
+ *
+ * lp_init_fp8 takes the same arguments as lp_init (W: the bf16 master lm_head, referenced) and
+ * additionally requires H % (128 * n_leaves) == 0 and tp_slices == 1.  It quantises W into
+ * a handle-owned e4m3 copy with its scales (synchronises `stream`).  lp_logprobs and
+ * lp_logprobs_host on such a handle quantise each chunk of X (1 x 128 blocks) and run the
+ * block-scaled GEMM; results obey the same invariance (batch, position, phase, chunking).
+ * lp_logprobs_entropy, lp_logits_partial, lp_logprobs_from_partials and lp_logprobs_backward
+ * return LP_ERR_UNSUPPORTED on a block-FP8 handle.
+ * lp_fp8_requantize re-quantises W after an in-place update (asynchronous on `stream`).
+ * lp_fp8_weights exposes the handle's e4m3 weights [V][H] and scales [ceil(V/128)][H/128]
+ * (device pointers owned by the handle) for verification.
+ */
+LP_API int lp_init_fp8(const lp_config* cfg, const void* W, void* stream, lp_handle** out);
+LP_API int lp_fp8_requantize(lp_handle* h, void* stream);
+LP_API int lp_fp8_weights(const lp_handle* h, const uint8_t** wq, const float** sw);
+/* The activation rule alone: X bf16 [T][ldx] -> xq e4m3 [T][H] (4-byte aligned) and
+ * sx fp32 [T][H/128], on `stream`.  Any handle with H % 128 == 0. */
+LP_API int lp_fp8_quantize_x(lp_handle* h, const void* X, int64_t ldx, int64_t T, uint8_t* xq,
+                             float* sx, void* stream);
+
+/*
  * Logprob backward.  For a loss L with upstream gradient g[t] = dL/dlogp[t] (fp32, device
  * [T]), with logp = lp_logprobs(X, ids) and logZ its out_logZ (device [T]):
  *   dl[t,v] = g[t] (1[v = y_t] - exp(z[t,v] - logZ[t]))      rounded to bf16, row chunks

@@ -1,0 +1,140 @@
+"""Block-FP8 (W8A8) handles on the GPU, against the oracle.
+
+The deployment recipe keeps the lm_head GEMM in block FP8 on both sides (vLLM blog "Finish
+RL training faster", section 4.1).  Checks:
+* the quantised bytes and scales of W (128 x 128 blocks) and X (1 x 128 blocks) are
+  bit-equal to the oracle's (both decide in IEEE fp32: amax / 448, x / s, E4M3 rounding);
+* logp within 2e-3 nats of the oracle's fp64 logprob of the dequantised operands, and within
+  1e-4 (fp32 block partials, at most 56 fma promotions and 3 tree adds per logit);
+* the same invariance as the bf16 path (row alone or in a batch, decode versus prefill,
+  chunking, graph replay), and in-place weight updates picked up by re-quantisation.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_consistent_logprob_gb300 import LP_PHASE_DECODE, LP_PHASE_PREFILL, Engine, LpError, inputs
+
+from gpu_util import LOGP_TOL, assert_bit_equal, require_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return require_cuda()
+
+
+def _bits(t):
+    return t.detach().cpu().contiguous().view(torch.uint8 if t.dtype == torch.uint8 else torch.int32)
+
+
+@pytest.mark.parametrize("T,H,V,N", [(300, 256, 4001, 2), (130, 1024, 32001, 8), (1, 512, 1000, 4)])
+def test_fp8_quantisation_and_logprobs_match_oracle(dev, T, H, V, N):
+    X = inputs.hidden_states(T, H, seed=T + 1, device=dev)
+    W = inputs.lm_head(V, H, seed=T + 1, device=dev)
+    ids = inputs.uniform_ids(T, V, seed=T + 1, device=dev)
+    with Engine(W, n_leaves=N, max_tokens=T, fp8=True) as eng:
+        wq, sw = eng.fp8_weights()
+        xq, sx = eng.fp8_quantize_x(X)
+        lp, lz = eng.logprobs(X, ids, return_logZ=True)
+        eng.check()
+    owq, osw = oracle.quantize_blocks(W.cpu(), 128)
+    oxq, osx = oracle.quantize_blocks(X.cpu(), 1)
+    assert np.array_equal(wq.cpu().numpy(), owq), "weight codes"
+    assert np.array_equal(sw.cpu().numpy().view(np.int32), osw.view(np.int32)), "weight scales"
+    assert np.array_equal(xq.cpu().numpy(), oxq), "activation codes"
+    assert np.array_equal(sx.cpu().numpy().view(np.int32), osx.view(np.int32)), "activation scales"
+    rows = np.unique(np.r_[0, T - 1, np.random.default_rng(T).choice(T, min(T, 48))])
+    want, wantZ = oracle.logprobs_fp8(oxq, osx, owq, osw, ids.cpu().numpy(), rows=rows)
+    err = np.abs(lp.cpu().double().numpy()[rows] - want).max()
+    errZ = np.abs(lz.cpu().double().numpy()[rows] - wantZ).max()
+    assert err <= LOGP_TOL and err <= 1e-4, err
+    assert errZ <= 1e-4, errZ
+
+
+def test_fp8_invariance(dev):
+    T, H, V, N = 2100, 1024, 32001, 8
+    X = inputs.hidden_states(T, H, seed=5, device=dev)
+    W = inputs.lm_head(V, H, seed=5, device=dev)
+    ids = inputs.uniform_ids(T, V, seed=5, device=dev)
+    with Engine(W, n_leaves=N, max_tokens=T, fp8=True) as eng:
+        ref, refZ = eng.logprobs(X, ids, return_logZ=True)
+        for r in (0, 1000, T - 1):
+            lp, lz = eng.logprobs(X[r:r + 1], ids[r:r + 1], return_logZ=True)
+            assert_bit_equal(lp, ref[r:r + 1], f"row {r} alone")
+            assert_bit_equal(lz, refZ[r:r + 1], f"logZ row {r} alone")
+        for B in (1, 7, 128, 256):
+            dec = eng.logprobs(X[500:500 + B], ids[500:500 + B], phase=LP_PHASE_DECODE)
+            assert_bit_equal(dec, ref[500:500 + B], f"decode B={B}")
+        idx = torch.randperm(T, generator=torch.Generator().manual_seed(1)).to(dev)
+        shuf = eng.logprobs(X[idx].contiguous(), ids[idx].contiguous(), phase=LP_PHASE_PREFILL)
+        assert_bit_equal(shuf, ref[idx], "shuffled batch")
+        # graph replay
+        out = torch.empty(T, device=dev)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            eng.logprobs(X, ids, out=out)
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            eng.logprobs(X, ids, out=out)
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert_bit_equal(out, ref, "graph replay")
+        eng.check()
+    for mt in (128, 1000):
+        with Engine(W, n_leaves=N, max_tokens=mt, fp8=True) as e2:
+            assert_bit_equal(e2.logprobs(X, ids), ref, f"max_tokens={mt}")
+            e2.check()
+
+
+def test_fp8_requantize_after_inplace_update_and_unsupported_calls(dev):
+    T, H, V, N = 400, 512, 8192, 4
+    X = inputs.hidden_states(T, H, seed=6, device=dev)
+    W = inputs.lm_head(V, H, seed=6, device=dev)
+    ids = inputs.uniform_ids(T, V, seed=6, device=dev)
+    W_new = inputs.lagged_lm_head(W, seed=7, std=1e-3)
+    with Engine(W, n_leaves=N, max_tokens=T, fp8=True) as eng, \
+            Engine(W_new, n_leaves=N, max_tokens=T, fp8=True) as fresh:
+        before = eng.logprobs(X, ids).clone()
+        W.copy_(W_new)
+        eng.fp8_requantize()
+        after = eng.logprobs(X, ids)
+        assert_bit_equal(after, fresh.logprobs(X, ids), "re-quantised vs fresh")
+        assert not torch.equal(before, after)
+        with pytest.raises(LpError):
+            eng.logprobs_entropy(X, ids)
+        with pytest.raises(LpError):
+            eng.logits_partial(X, 0, 2)
+        eng.check()
+        fresh.check()
+    with pytest.raises(LpError):
+        Engine(W, n_leaves=8, max_tokens=T, fp8=True)  # 512 is not a multiple of 128 * 8
+
+
+def test_fp8_ds_shape_rows(dev):
+    # DeepSeek-shape lm_head (H = 7168, V = 129280, N = 8): sampled rows against the oracle
+    T, H, V, N = 300, 7168, 129280, 8
+    X = inputs.hidden_states(T, H, seed=1002, device=dev)
+    W = inputs.lm_head(V, H, seed=1002, device=dev)
+    ids = inputs.uniform_ids(T, V, seed=1002, device=dev)
+    with Engine(W, n_leaves=N, max_tokens=T, fp8=True) as eng:
+        wq, sw = eng.fp8_weights()
+        xq, sx = eng.fp8_quantize_x(X)
+        lp = eng.logprobs(X, ids)
+        eng.check()
+    rows = np.array([0, 127, 128, 299])
+    want, _ = oracle.logprobs_fp8(xq.cpu().numpy(), sx.cpu().numpy(), wq.cpu().numpy(),
+                                  sw.cpu().numpy(), ids.cpu().numpy(), rows=rows)
+    err = np.abs(lp.cpu().double().numpy()[rows] - want).max()
+    assert err <= 1e-4, err
+    # the weight codes of the first and last 128-row blocks against the oracle's rule
+    for r0 in (0, (V - 1) // 128 * 128):
+        blk = W[r0:r0 + 128].cpu()
+        q, s = oracle.quantize_blocks(blk, 128)
+        assert np.array_equal(wq[r0:r0 + 128].cpu().numpy(), q)
+        assert np.array_equal(sw[r0 // 128].cpu().numpy(), s[0])
