@@ -60,10 +60,11 @@ SIGNATURES = {
     "lp_fp8_requantize": (ctypes.c_int, [_p, _p]),
     "lp_fp8_weights": (ctypes.c_int, [_p, ctypes.POINTER(_p), ctypes.POINTER(_p)]),
     "lp_fp8_quantize_x": (ctypes.c_int, [_p, _p, _i64, _i64, _p, _p, _p]),
-    "lp_contract": (ctypes.c_int, [ctypes.POINTER(LpConfig), _p, ctypes.c_size_t,
+    "lp_contract": (ctypes.c_int, [ctypes.POINTER(LpConfig), ctypes.c_int, _p, ctypes.c_size_t,
                                    ctypes.POINTER(ctypes.c_size_t)]),
-    "lp_contract_digest": (ctypes.c_int, [ctypes.POINTER(LpConfig), ctypes.c_int, _p]),
-    "lp_contract_check": (ctypes.c_int, [ctypes.POINTER(LpConfig), _p, _p]),
+    "lp_contract_digest": (ctypes.c_int, [ctypes.POINTER(LpConfig), ctypes.c_int, ctypes.c_int,
+                                          _p]),
+    "lp_contract_check": (ctypes.c_int, [ctypes.POINTER(LpConfig), ctypes.c_int, _p, _p]),
     "lp_sha256": (None, [_p, ctypes.c_size_t, _p]),
     "lp_reinforce_zero": (ctypes.c_int, [_p, _p, _p, _p, _i64, _p, _i64, _p, _i32,
                                          ctypes.POINTER(LpRzOptions), _p, _p, _p, _p, _p, _p]),

@@ -143,10 +143,27 @@ std::string semantic_json(const lp_config* c) {
     return b;
 }
 
-std::string policy_json(const lp_config* c) {
+std::string policy_json(const lp_config* c, int precision) {
+    const bool fp8 = precision == LP_PRECISION_FP8_BLOCK;
     std::string tp = "[1";
-    for (int s = 2; s <= c->n_leaves; s *= 2) tp += "," + std::to_string(s);
+    if (!fp8)
+        for (int s = 2; s <= c->n_leaves; s *= 2) tp += "," + std::to_string(s);
     tp += "]";
+    const char* lm_bf16 =
+        "\"impl\":{\"id\":\"leaf_gemm_tcgen05\",\"version\":%d,\"arch\":\"sm_103a\"},"
+        "\"constants\":{\"input_dtype\":\"bf16\",\"leaves\":%d,\"leaf_dtype\":\"fp32\","
+        "\"leaf_len\":%d,\"leaf_order\":\"k ascending, tcgen05.mma kind::f16 m128n128k16\",";
+    const char* lm_fp8 =
+        "\"impl\":{\"id\":\"leaf_gemm_tcgen05_block_fp8\",\"version\":%d,\"arch\":\"sm_103a\"},"
+        "\"constants\":{\"input_dtype\":\"e4m3\",\"quantization\":{\"activation_block\":"
+        "\"1x128\",\"weight_block\":\"128x128\",\"scale\":\"fp32 amax/448, 1 if amax=0\","
+        "\"rounding\":\"x/s in fp32, nearest even, saturate to 448\"},\"leaves\":%d,"
+        "\"leaf_dtype\":\"fp32\",\"leaf_len\":%d,\"leaf_order\":\"128-k blocks ascending: "
+        "tcgen05.mma kind::f8f6f4 m128n128k32 per block; (sx*sw)*B, first a product then one fma "
+        "per block\",";
+    char lm[1024];
+    std::snprintf(lm, sizeof lm, fp8 ? lm_fp8 : lm_bf16, lp_version(), c->n_leaves,
+                  c->H / c->n_leaves);
     char b[4096];
     std::snprintf(
         b, sizeof b,
@@ -154,10 +171,7 @@ std::string policy_json(const lp_config* c) {
         "\"composition\":["
         "{\"region\":[\"lm_head\",\"log_softmax\",\"sampled_logprob\"],"
         "\"cases\":[\"engine_prefill\",\"engine_decode\",\"trainer_fwd\",\"trainer_fwd_tp\"],"
-        "\"impl\":{\"id\":\"leaf_gemm_tcgen05\",\"version\":%d,\"arch\":\"sm_103a\"},"
-        "\"constants\":{\"input_dtype\":\"bf16\",\"leaves\":%d,\"leaf_dtype\":\"fp32\","
-        "\"leaf_len\":%d,\"leaf_order\":\"k ascending, tcgen05.mma kind::f16 m128n128k16\","
-        "\"leaf_tree\":\"adjacent pairs, level by level\",\"lse_tile\":64,"
+        "%s\"leaf_tree\":\"adjacent pairs, level by level\",\"lse_tile\":64,"
         "\"lse_tile_order\":\"2 chunks of 32: max left to right; sum of exp(z-m) by pairwise "
         "tree; s0+s1\",\"tile_exp\":\"__expf\",\"merge\":\"(m,s) with expf; aligned pairwise "
         "tree over tiles\",\"log\":\"logf\",\"logp\":\"z_y - (m + log s)\"}},"
@@ -168,7 +182,7 @@ std::string policy_json(const lp_config* c) {
         "\"term\":\"taylor to d^9/9! for |d|<1/4 else expm1f(d)-d\"}}],"
         "\"claims\":{\"topology\":{\"tp_slices\":%s},\"phases\":[\"prefill\",\"decode\"],"
         "\"batch_invariance\":\"bit_exact\",\"tolerances\":{\"oracle_logp_nats\":0.002}}}",
-        lp_version(), c->n_leaves, c->H / c->n_leaves, tp.c_str());
+        lm, tp.c_str());
     return b;
 }
 
@@ -179,10 +193,22 @@ std::string deployment_json(const lp_config* c) {
     return b;
 }
 
-std::string section(const lp_config* c, int which) {
+std::string section(const lp_config* c, int precision, int which) {
     return which == LP_DIGEST_SEMANTIC ? semantic_json(c)
-           : which == LP_DIGEST_NUMERICAL_POLICY ? policy_json(c)
+           : which == LP_DIGEST_NUMERICAL_POLICY ? policy_json(c, precision)
                                                  : deployment_json(c);
+}
+
+int check_args(const lp_config* cfg, int precision) {
+    int rc = lp_internal_validate_config(cfg);
+    if (rc != LP_OK) return rc;
+    if (precision != LP_PRECISION_BF16 && precision != LP_PRECISION_FP8_BLOCK)
+        return lp_internal_fail(LP_ERR_INVALID_ARG, "unknown precision %d", precision);
+    if (precision == LP_PRECISION_FP8_BLOCK &&
+        (cfg->H % (128 * cfg->n_leaves) != 0 || cfg->tp_slices != 1))
+        return lp_internal_fail(LP_ERR_UNSUPPORTED,
+                                "block FP8 needs H %% (128 * n_leaves) == 0 and tp_slices == 1");
+    return LP_OK;
 }
 
 }  // namespace
@@ -191,23 +217,23 @@ extern "C" {
 
 void lp_sha256(const void* data, size_t n, uint8_t out[32]) { sha256(data, n, out); }
 
-int lp_contract_digest(const lp_config* cfg, int which, uint8_t out[32]) {
-    int rc = lp_internal_validate_config(cfg);
+int lp_contract_digest(const lp_config* cfg, int precision, int which, uint8_t out[32]) {
+    int rc = check_args(cfg, precision);
     if (rc != LP_OK) return rc;
     if (which < LP_DIGEST_SEMANTIC || which > LP_DIGEST_DEPLOYMENT || out == nullptr)
         return lp_internal_fail(LP_ERR_INVALID_ARG, "bad digest selector or NULL output");
-    const std::string s = section(cfg, which);
+    const std::string s = section(cfg, precision, which);
     sha256(s.data(), s.size(), out);
     return LP_OK;
 }
 
-int lp_contract(const lp_config* cfg, char* buf, size_t cap, size_t* len) {
-    int rc = lp_internal_validate_config(cfg);
+int lp_contract(const lp_config* cfg, int precision, char* buf, size_t cap, size_t* len) {
+    int rc = check_args(cfg, precision);
     if (rc != LP_OK) return rc;
     uint8_t d[3][32];
     std::string parts[3];
     for (int i = 0; i < 3; ++i) {
-        parts[i] = section(cfg, i);
+        parts[i] = section(cfg, precision, i);
         sha256(parts[i].data(), parts[i].size(), d[i]);
     }
     const std::string json = "{\"semantic\":" + parts[0] + ",\"numerical_policy\":" + parts[1] +
@@ -223,16 +249,16 @@ int lp_contract(const lp_config* cfg, char* buf, size_t cap, size_t* len) {
     return LP_OK;
 }
 
-int lp_contract_check(const lp_config* cfg, const uint8_t peer_semantic[32],
+int lp_contract_check(const lp_config* cfg, int precision, const uint8_t peer_semantic[32],
                       const uint8_t peer_numerical_policy[32]) {
     uint8_t mine[32];
-    int rc = lp_contract_digest(cfg, LP_DIGEST_SEMANTIC, mine);
+    int rc = lp_contract_digest(cfg, precision, LP_DIGEST_SEMANTIC, mine);
     if (rc != LP_OK) return rc;
     if (peer_semantic == nullptr || peer_numerical_policy == nullptr)
         return lp_internal_fail(LP_ERR_INVALID_ARG, "peer digests must not be NULL");
     if (std::memcmp(mine, peer_semantic, 32) != 0)
         return lp_internal_fail(LP_ERR_UNSUPPORTED, "semantic digest differs from the peer's");
-    lp_contract_digest(cfg, LP_DIGEST_NUMERICAL_POLICY, mine);
+    lp_contract_digest(cfg, precision, LP_DIGEST_NUMERICAL_POLICY, mine);
     if (std::memcmp(mine, peer_numerical_policy, 32) != 0)
         return lp_internal_fail(LP_ERR_UNSUPPORTED,
                                 "numerical_policy digest differs from the peer's");

@@ -373,9 +373,11 @@ LP_API const char* lp_noalloc_last_error(void);
  * lp_sha256 is the library's SHA-256 (FIPS 180-4), exported for verification.
  */
 enum { LP_DIGEST_SEMANTIC = 0, LP_DIGEST_NUMERICAL_POLICY = 1, LP_DIGEST_DEPLOYMENT = 2 };
-LP_API int lp_contract(const lp_config* cfg, char* buf, size_t cap, size_t* len);
-LP_API int lp_contract_digest(const lp_config* cfg, int which, uint8_t out[32]);
-LP_API int lp_contract_check(const lp_config* cfg, const uint8_t peer_semantic[32],
+/* precision: the handle kind the contract describes (lp_init or lp_init_fp8). */
+enum { LP_PRECISION_BF16 = 0, LP_PRECISION_FP8_BLOCK = 1 };
+LP_API int lp_contract(const lp_config* cfg, int precision, char* buf, size_t cap, size_t* len);
+LP_API int lp_contract_digest(const lp_config* cfg, int precision, int which, uint8_t out[32]);
+LP_API int lp_contract_check(const lp_config* cfg, int precision, const uint8_t peer_semantic[32],
                              const uint8_t peer_numerical_policy[32]);
 LP_API void lp_sha256(const void* data, size_t n, uint8_t out[32]);
 

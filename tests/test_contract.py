@@ -55,6 +55,24 @@ def test_which_settings_move_which_digest():
     assert d(contract.SEMANTIC) == d(contract.SEMANTIC, n_leaves=4)
 
 
+def test_block_fp8_policy_differs_and_is_canonical():
+    kw = dict(H=7168, V=129280)
+    doc = contract.contract(precision=contract.FP8_BLOCK, **kw)
+    for key in ("semantic", "numerical_policy", "deployment"):
+        canon = json.dumps(doc[key], separators=(",", ":")).encode()
+        assert doc["identities"][key] == hashlib.sha256(canon).hexdigest(), key
+    lm = doc["numerical_policy"]["composition"][0]
+    assert lm["constants"]["input_dtype"] == "e4m3"
+    assert lm["constants"]["quantization"]["weight_block"] == "128x128"
+    assert doc["numerical_policy"]["claims"]["topology"]["tp_slices"] == [1]
+    pol = contract.NUMERICAL_POLICY
+    assert contract.digest(pol, precision=contract.FP8_BLOCK, **kw) != contract.digest(pol, **kw)
+    assert (contract.digest(contract.SEMANTIC, precision=contract.FP8_BLOCK, **kw)
+            == contract.digest(contract.SEMANTIC, **kw))
+    with pytest.raises(LpError):
+        contract.digest(pol, precision=contract.FP8_BLOCK, H=512, V=1000, n_leaves=8)
+
+
 def test_peer_check():
     kw = dict(H=2048, V=151936)
     sem, pol = contract.digest(contract.SEMANTIC, **kw), contract.digest(contract.NUMERICAL_POLICY, **kw)
