@@ -37,6 +37,8 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 KERNEL_SOURCES = ["bit_consistent_logprob_gb300/csrc/kernels.cuh",
                   "bit_consistent_logprob_gb300/csrc/numerics.cuh",
                   "bit_consistent_logprob_gb300/csrc/ptx.cuh",
+                  "bit_consistent_logprob_gb300/csrc/fp8_kernels.cuh",
+                  "bit_consistent_logprob_gb300/csrc/rl_kernels.cuh",
                   "bit_consistent_logprob_gb300/csrc/lp_api.cu"]
 
 

@@ -45,14 +45,26 @@ __host__ __device__ constexpr int fp8_smem_bytes() {
     return 1024 + kF8Stages * 2 * kTileBytes + kF8S1Bytes + kF8NumBars() * 8 + 16;
 }
 
-__device__ __forceinline__ void umma_f8_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate) {
+// One 128-K block from a single elected lane: 4 MMAs of K = 32 (+32 bytes each), the first
+// starting a fresh accumulator, then the commits that free the stage and hand the block's
+// TMEM buffer to the epilogue.
+__device__ __forceinline__ void umma_f8_block_elect(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                                    uint32_t idesc, uint64_t* stage_bar,
+                                                    uint64_t* acc_bar) {
     asm volatile(
-        "{\n\t.reg .pred e, p;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "{\n\t.reg .pred e, f, t;\n\t.reg .b64 a1, b1;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 f, 0, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, f;\n\t"
+        "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a1, b1, %3, t;\n\t"
+        "add.s64 a1, %1, 4;\n\tadd.s64 b1, %2, 4;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a1, b1, %3, t;\n\t"
+        "add.s64 a1, %1, 6;\n\tadd.s64 b1, %2, 6;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a1, b1, %3, t;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}" ::"r"(
+            d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(smem_u32(stage_bar)), "r"(smem_u32(acc_bar))
         : "memory");
 }
 
@@ -251,11 +263,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t d_tmem = tmem_base + buf * kVT;
                 const uint64_t a = descA + stage * kStageDesc;
                 const uint64_t b = descB + stage * kStageDesc;
-#pragma unroll
-                for (int i = 0; i < kQBlock / 32; ++i)
-                    umma_f8_elect(d_tmem, a + 2u * i, b + 2u * i, kIdescF8, i != 0 ? 1u : 0u);
-                umma_commit_elect(&empty[stage]);
-                umma_commit_elect(&acc_full[buf]);
+                umma_f8_block_elect(d_tmem, a, b, kIdescF8, &empty[stage], &acc_full[buf]);
                 ++used;
                 if (++stage == kF8Stages) {
                     stage = 0;

@@ -304,17 +304,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint64_t a = descA + stage * kStageDesc;
                     const uint64_t b = descB + stage * kStageDesc;
                     // +32 bytes (2 descriptor units) per K step of 16 bf16 inside a row;
-                    // only the leaf's very first MMA starts a fresh accumulator
-                    umma_bf16_elect(d_tmem, a, b, kIdesc, kb != 0 ? 1u : 0u);
-#pragma unroll
-                    for (int i = 1; i < kSub * (kBK / 16); ++i) {
-                        const uint32_t off = (i >> 2) * kSubDesc + 2u * (i & 3);
-                        umma_bf16_elect(d_tmem, a + off, b + off, kIdesc, 1u);
-                    }
-                    if (kCluster == 2)
-                        umma_commit_mc_elect(&empty[stage], kPairMask);  // both CTAs' stage freed
-                    else
-                        umma_commit_elect(&empty[stage]);
+                    // only the leaf's very first MMA starts a fresh accumulator; the stage is
+                    // freed for both CTAs of a pair (multicast commit) or for this CTA
+                    static_assert(kSubDesc == 1024, "sub-block stride assumed by the stage issue");
+                    umma_stage_elect<kSub, kCluster == 2>(d_tmem, a, b, kIdesc, kb != 0 ? 1u : 0u,
+                                                          &empty[stage], kPairMask);
                     stage = nstage;
                     phase = nphase;
                 }

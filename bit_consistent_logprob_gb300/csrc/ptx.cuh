@@ -196,6 +196,59 @@ __device__ __forceinline__ void umma_bf16_elect(uint32_t d_tmem, uint64_t a_desc
         : "memory");
 }
 
+// One pipeline stage of MMAs from a single elected lane: 4 * kSub MMAs (kind::f16, K = 16),
+// the descriptors advanced by +32 bytes per K step inside a 64-K sub-block and by 16 KB
+// (1024 descriptor units) per sub-block, the first MMA with the caller's accumulate flag and
+// the rest accumulating, then the commit that frees the stage (multicast to both CTAs of a
+// cluster pair when kMc).  The same instructions as one elected MMA at a time, with one
+// election per stage instead of one per instruction.
+#define LP_MMA_F16(A, B, P) "@e tcgen05.mma.cta_group::1.kind::f16 [%0], " A ", " B ", %3, " P ";\n\t"
+#define LP_ADV(OFF) "add.s64 a1, %1, " OFF ";\n\tadd.s64 b1, %2, " OFF ";\n\t"
+#define LP_STAGE_X4 \
+    LP_MMA_F16("%1", "%2", "p") LP_ADV("2") LP_MMA_F16("a1", "b1", "t") \
+    LP_ADV("4") LP_MMA_F16("a1", "b1", "t") LP_ADV("6") LP_MMA_F16("a1", "b1", "t")
+#define LP_STAGE_X8_TAIL \
+    LP_ADV("1024") LP_MMA_F16("a1", "b1", "t") LP_ADV("1026") LP_MMA_F16("a1", "b1", "t") \
+    LP_ADV("1028") LP_MMA_F16("a1", "b1", "t") LP_ADV("1030") LP_MMA_F16("a1", "b1", "t")
+#define LP_STAGE_HEAD \
+    "{\n\t.reg .pred e, p, t;\n\t.reg .b64 a1, b1;\n\t" \
+    "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+#define LP_COMMIT "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}"
+#define LP_COMMIT_MC                                                                            \
+    "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster" \
+    ".b64 [%5], %6;\n\t}"
+
+template <int kSub, bool kMc>
+__device__ __forceinline__ void umma_stage_elect(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                                 uint32_t idesc, uint32_t accumulate,
+                                                 uint64_t* bar, uint16_t mask) {
+    static_assert(kSub == 1 || kSub == 2, "stages hold one or two 64-K sub-blocks");
+    if constexpr (kSub == 2 && kMc) {
+        asm volatile(LP_STAGE_HEAD LP_STAGE_X4 LP_STAGE_X8_TAIL LP_COMMIT_MC ::"r"(d_tmem), "l"(a),
+                     "l"(b), "r"(idesc), "r"(accumulate), "r"(smem_u32(bar)), "h"(mask)
+                     : "memory");
+    } else if constexpr (kSub == 2) {
+        asm volatile(LP_STAGE_HEAD LP_STAGE_X4 LP_STAGE_X8_TAIL LP_COMMIT ::"r"(d_tmem), "l"(a),
+                     "l"(b), "r"(idesc), "r"(accumulate), "r"(smem_u32(bar))
+                     : "memory");
+    } else if constexpr (kMc) {
+        asm volatile(LP_STAGE_HEAD LP_STAGE_X4 LP_COMMIT_MC ::"r"(d_tmem), "l"(a), "l"(b),
+                     "r"(idesc), "r"(accumulate), "r"(smem_u32(bar)), "h"(mask)
+                     : "memory");
+    } else {
+        asm volatile(LP_STAGE_HEAD LP_STAGE_X4 LP_COMMIT ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc),
+                     "r"(accumulate), "r"(smem_u32(bar))
+                     : "memory");
+    }
+}
+#undef LP_MMA_F16
+#undef LP_ADV
+#undef LP_STAGE_X4
+#undef LP_STAGE_X8_TAIL
+#undef LP_STAGE_HEAD
+#undef LP_COMMIT
+#undef LP_COMMIT_MC
+
 __device__ __forceinline__ void umma_commit_elect(uint64_t* bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
