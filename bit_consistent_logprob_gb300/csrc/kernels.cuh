@@ -707,14 +707,23 @@ struct IsParams {
     long long* blk_cnt;      // [num_blocks]
 };
 
-// Per token: d = log pi - log mu, w = e^d, term = e^d - 1 - d.  Per block of 1024
-// tokens: fp64 sum of the valid terms, each thread adding its 4 tokens in order, then
-// a fixed xor-butterfly over the 32 lanes and a pairwise tree over the 8 warps.
+// Per token: d = log pi - log mu, w = e^d, term = e^d - 1 - d.  Per block of 1024 tokens:
+// each thread adds its 4 valid terms in order (double-float), a lane butterfly sums the warp
+// (double-float), and a pairwise fp64 tree sums the 8 warps.
+__device__ __forceinline__ double block_sum_8warps(df32 v, double* wsum) {
+    v = warp_sum_df(v);
+    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = df_to_f64(v);
+    __syncthreads();
+    const double s01 = __dadd_rn(wsum[0], wsum[1]), s23 = __dadd_rn(wsum[2], wsum[3]);
+    const double s45 = __dadd_rn(wsum[4], wsum[5]), s67 = __dadd_rn(wsum[6], wsum[7]);
+    return __dadd_rn(__dadd_rn(s01, s23), __dadd_rn(s45, s67));
+}
+
 static __global__ void __launch_bounds__(kIsThreads) is_block_kernel(const IsParams p) {
     __shared__ double wsum[kIsThreads / 32];
     __shared__ long long wcnt[kIsThreads / 32];
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kIsBlock + threadIdx.x * 4;
-    double acc = 0.0;
+    df32 acc{0.0f, 0.0f};
     long long cnt = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -724,26 +733,17 @@ static __global__ void __launch_bounds__(kIsThreads) is_block_kernel(const IsPar
             p.out_w[t] = expf(d);
             const bool valid = p.mask == nullptr || p.mask[t] != 0;
             if (valid) {
-                acc = __dadd_rn(acc, static_cast<double>(d3_term(d)));
+                acc = df_add(acc, d3_term(d));
                 ++cnt;
             }
         }
     }
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        acc = __dadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
-        cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
-    }
-    const int warp = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) {
-        wsum[warp] = acc;
-        wcnt[warp] = cnt;
-    }
-    __syncthreads();
+    for (int off = 16; off >= 1; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+    if ((threadIdx.x & 31) == 0) wcnt[threadIdx.x >> 5] = cnt;
+    const double total = block_sum_8warps(acc, wsum);
     if (threadIdx.x == 0) {
-        const double s01 = __dadd_rn(wsum[0], wsum[1]), s23 = __dadd_rn(wsum[2], wsum[3]);
-        const double s45 = __dadd_rn(wsum[4], wsum[5]), s67 = __dadd_rn(wsum[6], wsum[7]);
-        p.blk_sum[blockIdx.x] = __dadd_rn(__dadd_rn(s01, s23), __dadd_rn(s45, s67));
+        p.blk_sum[blockIdx.x] = total;
         long long c = 0;
         for (int w = 0; w < kIsThreads / 32; ++w) c += wcnt[w];
         p.blk_cnt[blockIdx.x] = c;

@@ -151,7 +151,58 @@ __device__ __forceinline__ float entropy_finish(float3 msu) {
     return __fsub_rn(logf(msu.y), __fdiv_rn(msu.z, msu.y));
 }
 
-// Two fp32 values rounded to bf16 (nearest even), packed low then high.
+// Double-float sums: a value hi + lo held as two non-overlapping fp32 numbers (about 48
+// significant bits), added with error-free transformations (Knuth's two-sum) on the fp32
+// pipes.  The GB300's fp64 rate is a small fraction of its fp32 rate, so per-token sums run in
+// double-float and only the few per-warp results are widened to fp64 (exactly: hi + lo fits
+// in a double).  Every operation is an explicit IEEE fp32 operation, so the result is the
+// same on every launch.
+struct df32 {
+    float hi, lo;
+};
+
+__device__ __forceinline__ df32 two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return {s, e};
+}
+
+__device__ __forceinline__ df32 df_add(df32 x, df32 y) {
+    const df32 s = two_sum(x.hi, y.hi);
+    const float lo = __fadd_rn(__fadd_rn(x.lo, y.lo), s.lo);
+    return two_sum(s.hi, lo);
+}
+
+__device__ __forceinline__ df32 df_add(df32 x, float v) { return df_add(x, df32{v, 0.0f}); }
+
+// x * x exactly, as a double-float (the rounding error of the product by an fma).
+__device__ __forceinline__ df32 square_exact(float x) {
+    const float p = __fmul_rn(x, x);
+    return {p, __fmaf_rn(x, x, -p)};
+}
+
+// a - b exactly, as a double-float.
+__device__ __forceinline__ df32 diff_exact(float a, float b) { return two_sum(a, -b); }
+
+__device__ __forceinline__ double df_to_f64(df32 x) {
+    return __dadd_rn(static_cast<double>(x.hi), static_cast<double>(x.lo));
+}
+
+// Lane butterfly over a warp (xor 16, 8, ..., 1); every lane ends with the same sum.
+__device__ __forceinline__ df32 warp_sum_df(df32 v) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const df32 o{__shfl_xor_sync(0xffffffffu, v.hi, off), __shfl_xor_sync(0xffffffffu, v.lo, off)};
+        // the lower lane adds (own, other), the upper (other, own): same operands in the same
+        // order on both lanes, so they stay equal
+        const bool low = (threadIdx.x & off) == 0;
+        v = low ? df_add(v, o) : df_add(o, v);
+    }
+    return v;
+}
+
+// Two fp32 values rounded to bf16 (nearest even), packed low then high.// Two fp32 values rounded to bf16 (nearest even), packed low then high.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);

@@ -12,7 +12,8 @@
 //                       TIS / token-gate / sequence-gate options (REINFORCE Zero summary,
 //                       section 4 and results table; vLLM blog, section 1).
 //
-// Every sum is fp64 in a fixed order that depends only on token positions (1024-token
+// Per-token sums are double-float (fp32 pairs, error-free additions) within a thread and a
+// warp and fp64 above, in a fixed order that depends only on token positions (1024-token
 // blocks) or on the response itself (one block per response), never on the launch.
 #pragma once
 
@@ -41,28 +42,16 @@ struct StatsParams {
 // max that keeps a NaN once seen (fmaxf would drop it); commutative for every input pair
 __device__ __forceinline__ float nan_max(float m, float x) { return (x > m || x != x) ? x : m; }
 
-__device__ __forceinline__ double warp_sum_f64(double v) {
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) v = __dadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
-    return v;
-}
-
-// pairwise tree over the 8 warps' values (the same shape as the D3 block sum)
-__device__ __forceinline__ double tree8_f64(const double* w) {
-    const double s01 = __dadd_rn(w[0], w[1]), s23 = __dadd_rn(w[2], w[3]);
-    const double s45 = __dadd_rn(w[4], w[5]), s67 = __dadd_rn(w[6], w[7]);
-    return __dadd_rn(__dadd_rn(s01, s23), __dadd_rn(s45, s67));
-}
-
-// Per block of 1024 tokens (4 per thread, in order): the three fp64 sums by the same
-// lane butterfly and 8-warp tree as the D3 block sum, so the k3 partials are bit-equal
-// to the D3 partials of the same tokens; max and count are exact in any order.
+// Per block of 1024 tokens (4 per thread, in order): three double-float sums reduced exactly
+// like the D3 block sum (is_block_kernel), so the k3 partials are bit-equal to the D3 partials
+// of the same tokens; |d|^2 enters exactly (an fma recovers the product's rounding error);
+// max and count are exact in any order.
 static __global__ void __launch_bounds__(kIsThreads) stats_block_kernel(const StatsParams p) {
-    __shared__ double s_abs[8], s_sq[8], s_k3[8];
+    __shared__ double s_w[8];
     __shared__ float s_max[8];
     __shared__ long long s_cnt[8];
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kIsBlock + threadIdx.x * 4;
-    double acc_abs = 0.0, acc_sq = 0.0, acc_k3 = 0.0;
+    df32 acc_abs{0.0f, 0.0f}, acc_sq{0.0f, 0.0f}, acc_k3{0.0f, 0.0f};
     float mx = 0.0f;
     long long cnt = 0;
 #pragma unroll
@@ -71,35 +60,31 @@ static __global__ void __launch_bounds__(kIsThreads) stats_block_kernel(const St
         if (t < p.T && (p.mask == nullptr || p.mask[t] != 0)) {
             const float d = __fsub_rn(p.a[t], p.b[t]);
             const float x = fabsf(d);
-            const double xd = static_cast<double>(x);
-            acc_abs = __dadd_rn(acc_abs, xd);
-            acc_sq = __dadd_rn(acc_sq, __dmul_rn(xd, xd));  // exact: 48-bit product
-            acc_k3 = __dadd_rn(acc_k3, static_cast<double>(d3_term(d)));
+            acc_abs = df_add(acc_abs, x);
+            acc_sq = df_add(acc_sq, square_exact(x));
+            acc_k3 = df_add(acc_k3, d3_term(d));
             mx = nan_max(mx, x);
             ++cnt;
         }
     }
-    acc_abs = warp_sum_f64(acc_abs);
-    acc_sq = warp_sum_f64(acc_sq);
-    acc_k3 = warp_sum_f64(acc_k3);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
         mx = nan_max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
         cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
     }
-    const int warp = threadIdx.x >> 5;
     if ((threadIdx.x & 31) == 0) {
-        s_abs[warp] = acc_abs;
-        s_sq[warp] = acc_sq;
-        s_k3[warp] = acc_k3;
-        s_max[warp] = mx;
-        s_cnt[warp] = cnt;
+        s_max[threadIdx.x >> 5] = mx;
+        s_cnt[threadIdx.x >> 5] = cnt;
     }
+    const double sum_abs = block_sum_8warps(acc_abs, s_w);
     __syncthreads();
+    const double sum_sq = block_sum_8warps(acc_sq, s_w);
+    __syncthreads();
+    const double sum_k3 = block_sum_8warps(acc_k3, s_w);
     if (threadIdx.x == 0) {
-        p.blk_abs[blockIdx.x] = tree8_f64(s_abs);
-        p.blk_sq[blockIdx.x] = tree8_f64(s_sq);
-        p.blk_k3[blockIdx.x] = tree8_f64(s_k3);
+        p.blk_abs[blockIdx.x] = sum_abs;
+        p.blk_sq[blockIdx.x] = sum_sq;
+        p.blk_k3[blockIdx.x] = sum_k3;
         float m = 0.0f;
         long long c = 0;
         for (int w = 0; w < 8; ++w) {
@@ -185,12 +170,13 @@ __device__ __forceinline__ float rz_token_weight(const RzParams& p, float d) {
 }
 
 // One block per response i.  Pass 1 (thread j takes tokens j, j + 256, ... in order): the
-// valid-token count, the sequence log-ratio sum d (fp64, d exact as a difference of the
-// two fp32 inputs) and sum w_hat (fp64), each reduced by the lane butterfly and 8-warp
-// tree.  Then the gate, A_i = R_i - mean of the group's rewards (fp64, in order), and
-// pass 2 writes w_hat and dL/dlog pi = -(A_i / (B T_i)) w_hat per token.
+// valid-token count, the sequence log-ratio sum d (d exact as a double-float difference of the
+// two fp32 inputs) and sum w_hat, each a double-float sum per thread, reduced by the lane
+// butterfly and the 8-warp fp64 tree.  Then the gate, A_i = R_i - mean of the group's rewards
+// (fp64, in order), and pass 2 writes w_hat and dL/dlog pi = -(A_i / (B T_i)) w_hat per token
+// (the coefficient rounded to fp32 once, then one fp32 product).
 static __global__ void __launch_bounds__(kRzThreads) rz_seq_kernel(const RzParams p) {
-    __shared__ double s_lr[8], s_w[8];
+    __shared__ double s_w[8];
     __shared__ long long s_n[8];
     const int64_t i = blockIdx.x;
     int64_t t_begin = p.offs[i], t_end = p.offs[i + 1];
@@ -198,31 +184,24 @@ static __global__ void __launch_bounds__(kRzThreads) rz_seq_kernel(const RzParam
         if (threadIdx.x == 0) atomicOr(p.status, kStatusBadOffsets);
         t_begin = t_end = 0;
     }
-    double lr = 0.0, ws = 0.0;
+    df32 lr{0.0f, 0.0f}, ws{0.0f, 0.0f};
     long long n = 0;
     for (int64_t t = t_begin + threadIdx.x; t < t_end; t += kRzThreads) {
         if (p.mask != nullptr && p.mask[t] == 0) continue;
         const float a = p.logp_pi[t], b = p.logp_mu[t];
-        lr = __dadd_rn(lr, __dsub_rn(static_cast<double>(a), static_cast<double>(b)));
-        ws = __dadd_rn(ws, static_cast<double>(rz_token_weight(p, __fsub_rn(a, b))));
+        lr = df_add(lr, diff_exact(a, b));
+        ws = df_add(ws, rz_token_weight(p, __fsub_rn(a, b)));
         ++n;
     }
-    lr = warp_sum_f64(lr);
-    ws = warp_sum_f64(ws);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
-    const int warp = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) {
-        s_lr[warp] = lr;
-        s_w[warp] = ws;
-        s_n[warp] = n;
-    }
+    if ((threadIdx.x & 31) == 0) s_n[threadIdx.x >> 5] = n;
+    const double lrd = block_sum_8warps(lr, s_w);
     __syncthreads();
-    lr = tree8_f64(s_lr);
-    ws = tree8_f64(s_w);
+    const double wsd = block_sum_8warps(ws, s_w);
     n = 0;
     for (int w = 0; w < 8; ++w) n += s_n[w];
-    const bool keep = !(p.flags & kRzFlagSeqGate) || (lr >= p.seq_lo && lr <= p.seq_hi);
+    const bool keep = !(p.flags & kRzFlagSeqGate) || (lrd >= p.seq_lo && lrd <= p.seq_hi);
 
     const int64_t g0 = (i / p.G) * p.G;
     double gsum = 0.0;
@@ -230,19 +209,19 @@ static __global__ void __launch_bounds__(kRzThreads) rz_seq_kernel(const RzParam
     const double A = __dsub_rn(static_cast<double>(p.rewards[i]),
                                __ddiv_rn(gsum, static_cast<double>(p.G)));
     const double bn = __dmul_rn(static_cast<double>(p.B), static_cast<double>(n));
-    const double coef = (n > 0 && keep) ? __ddiv_rn(-A, bn) : 0.0;
+    const float coef = (n > 0 && keep) ? __double2float_rn(__ddiv_rn(-A, bn)) : 0.0f;
 
     for (int64_t t = t_begin + threadIdx.x; t < t_end; t += kRzThreads) {
         float wh = 0.0f, g = 0.0f;
         if (keep && (p.mask == nullptr || p.mask[t] != 0)) {
             wh = rz_token_weight(p, __fsub_rn(p.logp_pi[t], p.logp_mu[t]));
-            g = static_cast<float>(__dmul_rn(coef, static_cast<double>(wh)));
+            g = __fmul_rn(coef, wh);
         }
         if (p.out_w_hat) p.out_w_hat[t] = wh;
         p.out_grad[t] = g;
     }
     if (threadIdx.x == 0) {
-        p.seq_term[i] = (n > 0 && keep) ? __ddiv_rn(__dmul_rn(A, ws), static_cast<double>(n)) : 0.0;
+        p.seq_term[i] = (n > 0 && keep) ? __ddiv_rn(__dmul_rn(A, wsd), static_cast<double>(n)) : 0.0;
         p.seq_kept[i] = keep ? 1 : 0;
         if (p.out_adv) p.out_adv[i] = A;
     }
