@@ -74,6 +74,7 @@ SIGNATURES = {
     "lp_logprobs_noalloc": (ctypes.c_int, [_p, _i32, _i32, _i32, _p, _i64, _p, _i64, _p, _p, _p]),
     "lp_noalloc_last_error": (ctypes.c_char_p, []),
     "lp_check": (ctypes.c_int, [_p]),
+    "lp_selftest_wait_timeout": (ctypes.c_int, [_p, _i64, _p]),
     "lp_clear_status": (ctypes.c_int, [_p, _p]),
     "lp_last_error": (ctypes.c_char_p, []),
     "lp_workspace_bytes": (ctypes.c_int64, [_p]),

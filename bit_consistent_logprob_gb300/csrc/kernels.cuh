@@ -692,6 +692,23 @@ __global__ void __launch_bounds__(kCmbMaxThreads) lse_combine_kernel(const Combi
     }
 }
 
+// Failure-detection self-test: one mbarrier that nothing ever arrives on (no copy, no MMA, no
+// TMEM in flight), waited on with the same bounded wait as every pipeline barrier.  The wait
+// must give up after timeout_ns, raise the sticky timeout bit and return, leaving the context
+// usable.  One block of 32 threads.
+static __global__ void __launch_bounds__(32) wait_selftest_kernel(int* status, uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const bool got = __all_sync(0xffffffffu, mbar_wait(&bar, 0, &abort_flag, timeout_ns));
+    if (!got && threadIdx.x == 0) atomicOr(status, kStatusTimeout);
+}
+
 // ---------------------------------------------------------------------- IS / D3
 constexpr int kIsBlock = 1024;       // tokens per D3 block (fixed; the tree is over blocks)
 constexpr int kIsThreads = 256;      // 4 tokens per thread

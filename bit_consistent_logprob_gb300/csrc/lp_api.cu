@@ -1138,6 +1138,18 @@ int lp_profile_read(lp_handle* h, double* gemm_ms_total, int32_t* gemm_launches)
     return LP_OK;
 }
 
+int lp_selftest_wait_timeout(lp_handle* h, int64_t timeout_us, void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    if (timeout_us < 1 || timeout_us > 2000000)
+        return fail(LP_ERR_INVALID_ARG, "timeout_us must be in [1, 2e6]");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    h->last_stream = st;
+    lp::wait_selftest_kernel<<<1, 32, 0, st>>>(h->status, static_cast<uint64_t>(timeout_us) * 1000u);
+    LP_CUDA(cudaGetLastError(), "wait_selftest_kernel launch");
+    h->last_launches = 1;
+    return LP_OK;
+}
+
 int lp_check(lp_handle* h) {
     if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
     LP_CUDA(cudaStreamSynchronize(h->last_stream), "stream synchronize");

@@ -356,6 +356,11 @@ class Engine:
         """Synchronise and raise LpError if a kernel flagged a bad id or a wait timeout."""
         _native.check(self._lib.lp_check(self._h))
 
+    def selftest_wait_timeout(self, timeout_us: int = 1000, stream=None) -> None:
+        """Run the bounded-wait self-test (raises the sticky timeout status; see lp.h)."""
+        _native.check(self._lib.lp_selftest_wait_timeout(self._h, int(timeout_us),
+                                                         _stream_ptr(stream)))
+
     def clear_status(self, stream=None) -> None:
         _native.check(self._lib.lp_clear_status(self._h, _stream_ptr(stream)))
 

@@ -381,6 +381,15 @@ LP_API int lp_contract_check(const lp_config* cfg, int precision, const uint8_t 
                              const uint8_t peer_numerical_policy[32]);
 LP_API void lp_sha256(const void* data, size_t n, uint8_t out[32]);
 
+/*
+ * Failure-detection self-test: launches a one-warp kernel that waits, with the same bounded
+ * wait as every pipeline barrier, on an mbarrier nothing ever arrives on.  After timeout_us
+ * (1 .. 2e6) it raises the sticky timeout status and returns; lp_check then reports
+ * LP_ERR_TIMEOUT and lp_clear_status resets it.  Nothing else is in flight in that kernel, so
+ * the context stays usable.
+ */
+LP_API int lp_selftest_wait_timeout(lp_handle* h, int64_t timeout_us, void* stream);
+
 /* Synchronise the stream last used with the handle and return the sticky device
  * status (LP_OK, LP_ERR_INVALID_ARG for a bad id, LP_ERR_TIMEOUT). */
 LP_API int lp_check(lp_handle* h);

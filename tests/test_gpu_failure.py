@@ -1,0 +1,62 @@
+"""Failure detection without a GPU fault.
+
+Every pipeline wait in the kernels is bounded (a %globaltimer budget).  The self-test kernel
+waits on an mbarrier that nothing ever arrives on -- a flag that nothing sets -- with that
+same bounded wait; it must give up, raise the sticky timeout status and return.  The host
+reads the status (LP_ERR_TIMEOUT), clears it, and the context keeps working bit-exactly.
+Bad sampled ids are the other device-side failure: NaN for that row and LP_ERR_INVALID_ARG.
+"""
+import time
+
+import pytest
+import torch
+
+from bit_consistent_logprob_gb300 import Engine, LpError, inputs
+from bit_consistent_logprob_gb300._native import LP_ERR_INVALID_ARG, LP_ERR_TIMEOUT
+
+from gpu_util import assert_bit_equal, require_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    dev = require_cuda()
+    X = inputs.hidden_states(300, 256, seed=2, device=dev)
+    W = inputs.lm_head(4096, 256, seed=2, device=dev)
+    ids = inputs.uniform_ids(300, 4096, seed=2, device=dev)
+    with Engine(W, n_leaves=4, max_tokens=300) as eng:
+        before = eng.logprobs(X, ids).clone()
+        eng.check()
+        t0 = time.perf_counter()
+        eng.selftest_wait_timeout(20_000)  # 20 ms budget
+        with pytest.raises(LpError) as err:
+            eng.check()
+        elapsed = time.perf_counter() - t0
+        assert err.value.code == LP_ERR_TIMEOUT
+        assert 0.015 < elapsed < 5.0, elapsed
+        eng.clear_status()
+        eng.check()
+        after = eng.logprobs(X, ids)
+        eng.check()
+    assert_bit_equal(after, before, "after a reported timeout")
+
+
+def test_bad_id_is_reported_and_isolated():
+    dev = require_cuda()
+    X = inputs.hidden_states(200, 256, seed=3, device=dev)
+    W = inputs.lm_head(4096, 256, seed=3, device=dev)
+    ids = inputs.uniform_ids(200, 4096, seed=3, device=dev)
+    with Engine(W, n_leaves=4, max_tokens=200) as eng:
+        good = eng.logprobs(X, ids).clone()
+        bad = ids.clone()
+        bad[17] = 4096
+        bad[150] = -1
+        lp = eng.logprobs(X, bad)
+        with pytest.raises(LpError) as err:
+            eng.check()
+        assert err.value.code == LP_ERR_INVALID_ARG
+        eng.clear_status()
+    assert torch.isnan(lp[17]) and torch.isnan(lp[150])
+    keep = torch.ones(200, dtype=torch.bool, device=dev)
+    keep[[17, 150]] = False
+    assert_bit_equal(lp[keep], good[keep], "rows with valid ids")
