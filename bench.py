@@ -429,7 +429,10 @@ def run_ours(args, world, rank, local, pg):
             src = f"{src} x 2, the nominal fp8/bf16 ratio"
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "peak_source": src}
-    roof["traffic"] = recorded_traffic(args.workload + ("_fp8" if args.fp8 else ""))
+    key = args.workload + ("_fp8" if args.fp8 else "")
+    if args.workload == "ds_decode":
+        key += f"_b{args.batch}"
+    roof["traffic"] = recorded_traffic(key)
     roof["kernel"] = "leaf_gemm_fp8_kernel" if args.fp8 else "leaf_gemm_kernel<fused>"
     roof["kernel_ms"] = gemm_avg_ms
     roof["algorithmic_per_launch"] = algo
