@@ -215,10 +215,6 @@ int set_gemm_attributes() {
     return LP_OK;
 }
 
-// The leaf GEMM over `rows` rows of X starting at `X` (row stride ldx).  Calls with at least
-// one full 128-row tile run in clusters of two CTAs that share each X tile (multicast);
-// smaller (decode) calls run one CTA per tile with an X box cut to their rows.  Stages are
-// 128 K deep (8 MMAs per barrier synchronisation) when the leaf length allows, else 64.
 // Extra per-mode operands of the leaf GEMM epilogue (kModeGrad).
 struct GradArgs {
     const float* logZ = nullptr;
@@ -227,6 +223,10 @@ struct GradArgs {
     int64_t ldd = 0;
 };
 
+// The leaf GEMM over `rows` rows of X starting at `X` (row stride ldx).  Calls with at least
+// one full 128-row tile run in clusters of two CTAs that share each X tile (multicast);
+// smaller (decode) calls run one CTA per tile with an X box cut to their rows.  Stages are
+// 128 K deep (8 MMAs per barrier synchronisation) when the leaf length allows, else 64.
 template <int kMode>
 int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int leaf_begin,
                      int leaf_count, const int32_t* ids, float* out, int64_t ldo,
