@@ -35,12 +35,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+# Sources that decide the dominant kernel's code and launch (the recorded DRAM traffic is
+# dropped when they change): the leaf GEMM and its host launch; plus the FP8 kernel for --fp8.
 KERNEL_SOURCES = ["bit_consistent_logprob_gb300/csrc/kernels.cuh",
                   "bit_consistent_logprob_gb300/csrc/numerics.cuh",
                   "bit_consistent_logprob_gb300/csrc/ptx.cuh",
-                  "bit_consistent_logprob_gb300/csrc/fp8_kernels.cuh",
-                  "bit_consistent_logprob_gb300/csrc/rl_kernels.cuh",
                   "bit_consistent_logprob_gb300/csrc/lp_api.cu"]
+FP8_SOURCES = ["bit_consistent_logprob_gb300/csrc/fp8_kernels.cuh"]
 
 
 # ----------------------------------------------------------------------------- setup
@@ -86,11 +87,11 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(fp8: bool = False) -> str:
     """SHA-256 (first 16 hex digits) of the kernel and launch sources with comments and
     whitespace removed, so that a recorded traffic figure survives edits to comments only."""
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES + (FP8_SOURCES if fp8 else []):
         with open(os.path.join(ROOT, rel)) as f:
             src = f.read()
         src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
@@ -108,7 +109,7 @@ def recorded_traffic(workload: str):
     with open(path) as f:
         d = json.load(f)
     e = d.get(workload)
-    if not e or e.get("kernel_source_sha") != kernel_source_hash():
+    if not e or e.get("kernel_source_sha") != kernel_source_hash(fp8=workload.endswith("_fp8")):
         return None
     return e.get("dram_bytes_per_launch")
 

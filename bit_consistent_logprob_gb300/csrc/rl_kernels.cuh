@@ -169,7 +169,8 @@ __device__ __forceinline__ float rz_token_weight(const RzParams& p, float d) {
     return w;
 }
 
-// One block per response i.  Pass 1 (thread j takes tokens j, j + 256, ... in order): the
+// One block per response i.  Pass 1 (thread j takes tokens j, j + 256, ... in order, four
+// loads in flight): the
 // valid-token count, the sequence log-ratio sum d (d exact as a double-float difference of the
 // two fp32 inputs) and sum w_hat, each a double-float sum per thread, reduced by the lane
 // butterfly and the 8-warp fp64 tree.  Then the gate, A_i = R_i - mean of the group's rewards
@@ -186,12 +187,25 @@ static __global__ void __launch_bounds__(kRzThreads) rz_seq_kernel(const RzParam
     }
     df32 lr{0.0f, 0.0f}, ws{0.0f, 0.0f};
     long long n = 0;
-    for (int64_t t = t_begin + threadIdx.x; t < t_end; t += kRzThreads) {
-        if (p.mask != nullptr && p.mask[t] == 0) continue;
-        const float a = p.logp_pi[t], b = p.logp_mu[t];
-        lr = df_add(lr, diff_exact(a, b));
-        ws = df_add(ws, rz_token_weight(p, __fsub_rn(a, b)));
-        ++n;
+    // four tokens per round: their loads are issued together, then folded in token order
+    constexpr int kU = 4;
+    for (int64_t t0 = t_begin + threadIdx.x; t0 < t_end; t0 += kU * kRzThreads) {
+        float a[kU], b[kU];
+        bool valid[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int64_t t = t0 + static_cast<int64_t>(u) * kRzThreads;
+            valid[u] = t < t_end && (p.mask == nullptr || p.mask[t] != 0);
+            a[u] = t < t_end ? p.logp_pi[t] : 0.0f;
+            b[u] = t < t_end ? p.logp_mu[t] : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            if (!valid[u]) continue;
+            lr = df_add(lr, diff_exact(a[u], b[u]));
+            ws = df_add(ws, rz_token_weight(p, __fsub_rn(a[u], b[u])));
+            ++n;
+        }
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
@@ -211,14 +225,23 @@ static __global__ void __launch_bounds__(kRzThreads) rz_seq_kernel(const RzParam
     const double bn = __dmul_rn(static_cast<double>(p.B), static_cast<double>(n));
     const float coef = (n > 0 && keep) ? __double2float_rn(__ddiv_rn(-A, bn)) : 0.0f;
 
-    for (int64_t t = t_begin + threadIdx.x; t < t_end; t += kRzThreads) {
-        float wh = 0.0f, g = 0.0f;
-        if (keep && (p.mask == nullptr || p.mask[t] != 0)) {
-            wh = rz_token_weight(p, __fsub_rn(p.logp_pi[t], p.logp_mu[t]));
-            g = __fmul_rn(coef, wh);
+    for (int64_t t0 = t_begin + threadIdx.x; t0 < t_end; t0 += kU * kRzThreads) {
+        float d[kU];
+        bool valid[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int64_t t = t0 + static_cast<int64_t>(u) * kRzThreads;
+            valid[u] = keep && t < t_end && (p.mask == nullptr || p.mask[t] != 0);
+            d[u] = valid[u] ? __fsub_rn(p.logp_pi[t], p.logp_mu[t]) : 0.0f;
         }
-        if (p.out_w_hat) p.out_w_hat[t] = wh;
-        p.out_grad[t] = g;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int64_t t = t0 + static_cast<int64_t>(u) * kRzThreads;
+            if (t >= t_end) break;
+            const float wh = valid[u] ? rz_token_weight(p, d[u]) : 0.0f;
+            if (p.out_w_hat) p.out_w_hat[t] = wh;
+            p.out_grad[t] = valid[u] ? __fmul_rn(coef, wh) : 0.0f;
+        }
     }
     if (threadIdx.x == 0) {
         p.seq_term[i] = (n > 0 && keep) ? __ddiv_rn(__dmul_rn(A, wsd), static_cast<double>(n)) : 0.0;
