@@ -331,6 +331,94 @@ def run_rl_epilogue(args, world, rank, local, pg):
     }
 
 
+# ----------------------------------------------------------------------------- backward
+def run_backward(args, world, rank, local, pg):
+    """The logprob backward over the workload's batch: dl = g (onehot - p) from the forward's
+    logits (the leaf GEMM's gradient epilogue), then dX = dl W and dW = dl^T X (cuBLAS)."""
+    import torch
+
+    from bit_consistent_logprob_gb300 import Engine
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl, lengths, X, W, ids = make_workload(args.workload, dev, seed_offset=rank, batch=args.batch)
+    T, H, V, N = X.shape[0], wl.H, wl.V, wl.n_leaves
+    eng = Engine(W, n_leaves=N, max_tokens=min(T, args.max_tokens))
+    _, logZ = eng.logprobs(X, ids, return_logZ=True)
+    g = torch.randn(T, generator=torch.Generator().manual_seed(wl.seed), dtype=torch.float32).to(dev)
+    chunk = min(T, 4096)
+    eng.backward_reserve(chunk)
+    dX = torch.empty(T, H, dtype=torch.float32, device=dev)
+    dW = torch.empty(V, H, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    launches = [0]
+
+    def step():
+        eng.logprobs_backward(X, ids, logZ, g, dX=dX, dW=dW)
+        launches[0] += eng.last_launch_count
+
+    for _ in range(args.warmup):
+        step()
+    eng.check()
+    torch.cuda.synchronize()
+    launches[0] = 0
+    eng.profile_enable(True)
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    barrier(pg, dev)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg, dev)
+    clocks = sampler.stop()
+    gemm_ms, gemm_n = eng.profile_read()
+    eng.profile_enable(False)
+    eng.check()
+    ms = max_over_ranks(pg, e0.elapsed_time(e1) / args.steps, dev)
+    peaks, peak_src = load_peaks()
+    grad_ms = gemm_ms / max(1, gemm_n)
+    per_launch = 2.0 * T * H * V / (gemm_n / max(1, args.steps))
+    achieved = per_launch / (grad_ms / 1000.0) / 1e12
+    peak = float(peaks["bf16_tflops_sustained"])
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "peak_source": f"{peak_src} bf16_tflops_sustained",
+            "traffic": None, "kernel": "leaf_gemm_kernel<gradient epilogue>",
+            "kernel_ms": grad_ms, "algorithmic_per_launch": per_launch}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import numpy as np
+
+        import oracle
+
+        oracle.build()
+        rows = np.array([0, T // 2, T - 1])
+        t0 = time.perf_counter()
+        oracle.logprob_grad(X[rows].cpu(), W.cpu(), ids.cpu().numpy()[rows],
+                            g.cpu().double().numpy()[rows])
+        dt = time.perf_counter() - t0
+        cpu = {"value": len(rows) / dt, "unit": UNIT, "cores": oracle.num_threads(),
+               "kind": "oracle", "seconds": dt,
+               "sample": f"{len(rows)} rows of the {wl.name} batch: their dX and dW terms"}
+    eng.close()
+    if rank != 0:
+        return None
+    return {
+        "metric": "logprob-backward tokens/sec (dX and dW)", "value": world * T / (ms / 1000.0),
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 (dl bf16, fp32 accumulation)", "data": "synthetic",
+        "config": {"workload": wl.name + "+backward", "T": T, "H": H, "V": V, "n_leaves": N,
+                   "row_chunk": chunk, "step": "lp_logprobs_backward (dX and dW)",
+                   "step_tflops": 3 * 2.0 * T * H * V / (ms / 1000.0) / 1e12},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches[0],
+        "clocks": clocks,
+    }
+
+
 # ----------------------------------------------------------------------------- our arm
 def run_ours(args, world, rank, local, pg):
     import torch
@@ -353,8 +441,14 @@ def run_ours(args, world, rank, local, pg):
     stream = torch.cuda.current_stream()
     launches = [0]
 
+    ent = torch.empty(T, dtype=torch.float32, device=dev) if args.entropy else None
+    logz = torch.empty(T, dtype=torch.float32, device=dev) if args.entropy else None
+
     def step():
-        eng.logprobs(X, ids, out=logp, phase=phase)
+        if args.entropy:
+            eng.logprobs_entropy(X, ids, out=logp, out_logZ=logz, out_entropy=ent, phase=phase)
+        else:
+            eng.logprobs(X, ids, out=logp, phase=phase)
         launches[0] += eng.last_launch_count
         eng.importance_weights(logp, mu, out_w=w, out_d3=d3, out_nvalid=nv)
         launches[0] += eng.last_launch_count
@@ -386,7 +480,7 @@ def run_ours(args, world, rank, local, pg):
 
     # end to end through the public API with host buffers (pinned), copies in the region
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.entropy:
         Xh = X.cpu().pin_memory()
         idsh = ids.cpu().pin_memory()
         muh = mu.cpu().pin_memory()
@@ -436,11 +530,12 @@ def run_ours(args, world, rank, local, pg):
             src = f"{src} x 2, the nominal fp8/bf16 ratio"
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "peak_source": src}
-    key = args.workload + ("_fp8" if args.fp8 else "")
+    key = args.workload + ("_fp8" if args.fp8 else "") + ("_entropy" if args.entropy else "")
     if args.workload == "ds_decode":
         key += f"_b{args.batch}"
     roof["traffic"] = recorded_traffic(key)
-    roof["kernel"] = "leaf_gemm_fp8_kernel" if args.fp8 else "leaf_gemm_kernel<fused>"
+    roof["kernel"] = ("leaf_gemm_fp8_kernel" if args.fp8 else
+                      "leaf_gemm_kernel<fused, entropy>" if args.entropy else "leaf_gemm_kernel<fused>")
     roof["kernel_ms"] = gemm_avg_ms
     roof["algorithmic_per_launch"] = algo
 
@@ -461,7 +556,8 @@ def run_ours(args, world, rank, local, pg):
                    "n_seqs": len(lengths), "phase": "decode" if phase == LP_PHASE_DECODE else "prefill",
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
                    "l2": f"inputs larger than L2 (W {2 * H * V / 1e6:.0f} MB streamed every step)",
-                   "step": "lp_logprobs + lp_importance_weights"},
+                   "step": ("lp_logprobs_entropy" if args.entropy else "lp_logprobs")
+                           + " + lp_importance_weights"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
         "clocks": clocks,
     }
@@ -604,6 +700,10 @@ def parse_args(argv=None):
     ap.add_argument("--ref-step-seconds", type=float, default=1.5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--entropy", action="store_true",
+                    help="the step also forms each row's softmax entropy (lp_logprobs_entropy)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the logprob backward (dX, dW) instead of the forward step")
     ap.add_argument("--fp8", action="store_true",
                     help="block-FP8 (W8A8) handle: 1x128 activation, 128x128 weight blocks")
     args = ap.parse_args(argv)
@@ -621,6 +721,8 @@ def main(argv=None):
         line = run_reference(args, world, rank)
     elif args.workload == "rl_epilogue":
         line = run_rl_epilogue(args, world, rank, local, pg)
+    elif args.backward:
+        line = run_backward(args, world, rank, local, pg)
     else:
         line = run_ours(args, world, rank, local, pg)
     if rank == 0 and line is not None:
