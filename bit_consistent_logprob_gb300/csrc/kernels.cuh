@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // The tensor core's instruction queue is shallow, so the issuing loop does as little
         // as possible between MMAs: descriptors are precomputed, buffer/stage indices advance
         // incrementally, every value is warp-uniform, and the barriers of the next stage and
-        // of the next leaf's buffer are probed (non-blocking) before this stage's MMAs issue.
+        // of the next leaf's buffer are probed (non-blocking) while this stage's MMAs run.
         const uint64_t descA = sw128_kmajor_desc(smem_u32(sA));
         const uint64_t descB = sw128_kmajor_desc(smem_u32(sB));
         constexpr uint32_t kStageDesc = kStageBytes >> 4;  // descriptor units per stage
@@ -297,10 +297,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tc_fence_after_sync();
                     const uint32_t nstage = stage + 1 == kStages ? 0u : stage + 1;
                     const uint32_t nphase = stage + 1 == kStages ? phase ^ 1u : phase;
-                    ready = __all_sync(kFull, mbar_test_wait(&full[nstage], nphase));
-                    if (kb == nkb - 1)
-                        acc_ready =
-                            __all_sync(kFull, mbar_test_wait(&acc_empty[nbuf], nbphase ^ 1u));
                     const uint64_t a = descA + stage * kStageDesc;
                     const uint64_t b = descB + stage * kStageDesc;
                     // +32 bytes (2 descriptor units) per K step of 16 bf16 inside a row;
@@ -309,6 +305,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     static_assert(kSubDesc == 1024, "sub-block stride assumed by the stage issue");
                     umma_stage_elect<kSub, kCluster == 2>(d_tmem, a, b, kIdesc, kb != 0 ? 1u : 0u,
                                                           &empty[stage], kPairMask);
+                    // probe the next stage (and the next leaf's buffer) while these MMAs run
+                    ready = __all_sync(kFull, mbar_test_wait(&full[nstage], nphase));
+                    if (kb == nkb - 1)
+                        acc_ready =
+                            __all_sync(kFull, mbar_test_wait(&acc_empty[nbuf], nbphase ^ 1u));
                     stage = nstage;
                     phase = nphase;
                 }
