@@ -240,13 +240,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint64_t descA = sw128_kmajor_desc(smem_u32(sA));
         const uint64_t descB = sw128_kmajor_desc(smem_u32(sB));
         constexpr uint32_t kStageDesc = kTileBytes >> 4;
+        // the next stage's and next buffer's barriers are probed while this block's MMAs run
         uint32_t stage = 0, phase = 0;
         uint32_t buf = 0, bphase = 0;
         uint64_t used = 0;
         bool ok = true;
+        bool ready = __all_sync(kFull, mbar_test_wait(&full[0], 0));
+        bool acc_ready = true;  // the first use of each buffer finds it free
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
             for (int kb = 0; ok && kb < nkb; ++kb) {
-                if (used >= kF8Bufs) {
+                if (!acc_ready) {
                     ok = __all_sync(kFull, mbar_wait(&acc_empty[buf], bphase ^ 1u, abort_flag,
                                                      p.timeout_ns));
                     if (!ok) {
@@ -254,10 +257,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                 }
-                ok = __all_sync(kFull, mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns));
-                if (!ok) {
-                    if (lane == 0) raise_timeout(p, abort_flag);
-                    break;
+                if (!ready) {
+                    ok = __all_sync(kFull, mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns));
+                    if (!ok) {
+                        if (lane == 0) raise_timeout(p, abort_flag);
+                        break;
+                    }
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + buf * kVT;
@@ -273,6 +278,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     buf = 0;
                     bphase ^= 1u;
                 }
+                ready = __all_sync(kFull, mbar_test_wait(&full[stage], phase));
+                acc_ready = used < kF8Bufs ||
+                            __all_sync(kFull, mbar_test_wait(&acc_empty[buf], bphase ^ 1u));
             }
         }
         if (!ok) {
