@@ -36,12 +36,30 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 # Sources that decide the dominant kernel's code and launch (the recorded DRAM traffic is
-# dropped when they change): the leaf GEMM and its host launch; plus the FP8 kernel for --fp8.
+# dropped when they change): the leaf GEMM, and from the host library only the functions
+# that encode its tensor maps, pick its launch shape and its scheduling band; plus the FP8
+# kernel and its launch for --fp8.
 KERNEL_SOURCES = ["bit_consistent_logprob_gb300/csrc/kernels.cuh",
                   "bit_consistent_logprob_gb300/csrc/numerics.cuh",
-                  "bit_consistent_logprob_gb300/csrc/ptx.cuh",
-                  "bit_consistent_logprob_gb300/csrc/lp_api.cu"]
+                  "bit_consistent_logprob_gb300/csrc/ptx.cuh"]
+HOST_LAUNCH = ("bit_consistent_logprob_gb300/csrc/lp_api.cu",
+               ["encode_kmajor", "scheduling_band", "x_box_rows", "launch_gemm_variant",
+                "launch_leaf_gemm"])
 FP8_SOURCES = ["bit_consistent_logprob_gb300/csrc/fp8_kernels.cuh"]
+FP8_HOST_LAUNCH = ["launch_fp8_chunk", "quantize_weights"]
+
+
+def _function_text(src: str, name: str) -> str:
+    """The definition of the first function called `name` (signature through its closing brace)."""
+    m = re.search(r"^[^\n;{}]*\b" + re.escape(name) + r"\([^;{]*\{", src, flags=re.M)
+    if m is None:
+        raise KeyError(name)
+    depth, i = 0, m.end() - 1
+    while True:
+        depth += {"{": 1, "}": -1}.get(src[i], 0)
+        i += 1
+        if depth == 0:
+            return src[m.start():i]
 
 
 # ----------------------------------------------------------------------------- setup
@@ -90,13 +108,21 @@ def load_peaks():
 def kernel_source_hash(fp8: bool = False) -> str:
     """SHA-256 (first 16 hex digits) of the kernel and launch sources with comments and
     whitespace removed, so that a recorded traffic figure survives edits to comments only."""
+    def strip_comments(src):
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        return re.sub(r"//[^\n]*", " ", src)
+
+    def canon(src):
+        return " ".join(src.split()).encode()
+
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES + (FP8_SOURCES if fp8 else []):
         with open(os.path.join(ROOT, rel)) as f:
-            src = f.read()
-        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
-        src = re.sub(r"//[^\n]*", " ", src)
-        h.update(" ".join(src.split()).encode())
+            h.update(canon(strip_comments(f.read())))
+    with open(os.path.join(ROOT, HOST_LAUNCH[0])) as f:
+        host = strip_comments(f.read())
+    for name in HOST_LAUNCH[1] + (FP8_HOST_LAUNCH if fp8 else []):
+        h.update(canon(_function_text(host, name)))
     return h.hexdigest()[:16]
 
 

@@ -180,6 +180,16 @@ uint32_t x_box_rows(int rows) {
     return rows >= lp::kBM ? lp::kBM : static_cast<uint32_t>((rows + 7) / 8 * 8);
 }
 
+// Scheduling band: enough vocabulary tiles for ~28 MiB of W, which stays L2-resident while
+// every row tile of the batch sweeps across it (measured best on GB300: 16 tiles at H = 7168,
+// 32-48 at H = 2048).  The band decides which CTA computes a tile, never how.
+int scheduling_band(int H, int bytes_per_weight, int max_tiles) {
+    const int64_t per_tile = static_cast<int64_t>(lp::kVT) * H * bytes_per_weight;
+    int64_t b = (int64_t(28) << 20) / per_tile;
+    b = b < 8 ? 8 : (b > max_tiles ? max_tiles : b);
+    return static_cast<int>(b) & ~1;
+}
+
 template <int kMode, int kSub, int kCluster>
 cudaError_t launch_gemm_variant(int grid, cudaStream_t st, const CUtensorMap& tmX,
                                 const CUtensorMap& tmW, const lp::GemmParams& p) {
@@ -555,26 +565,12 @@ int init_impl(const lp_config* cfg, const void* W, void* stream, lp_handle** out
     h->timeout_ns = timeout_ms * 1000000ull;
     if (const char* e = std::getenv("LP_FORCE_SINGLE_CTA")) h->force_single_cta = e[0] == '1';
     if (const char* e = std::getenv("LP_FORCE_SHORT_STAGES")) h->force_sub1 = e[0] == '1';
-    // Scheduling band: enough vocabulary tiles for ~28 MiB of W, which stays L2-resident
-    // while every row tile of the batch sweeps across it (measured best on GB300: 16 tiles
-    // at H = 7168, 32-48 at H = 2048).  The band decides which CTA computes a tile, never how.
-    {
-        const int64_t per_tile = static_cast<int64_t>(lp::kVT) * cfg->H * 2;
-        int64_t b = (int64_t(28) << 20) / per_tile;
-        b = b < 8 ? 8 : (b > 64 ? 64 : b);
-        h->band = static_cast<int>(b) & ~1;
-    }
+    h->band = scheduling_band(cfg->H, 2, 64);
     if (const char* e = std::getenv("LP_BAND")) {
         const int b = std::atoi(e);
         if (b >= 2 && b <= 1024) h->band = b & ~1;
     }
-    {
-        // e4m3 weights are one byte: twice the tiles fit the same L2 budget
-        const int64_t per_tile = static_cast<int64_t>(lp::kVT) * cfg->H;
-        int64_t b = (int64_t(28) << 20) / per_tile;
-        b = b < 8 ? 8 : (b > 128 ? 128 : b);
-        h->band_fp8 = static_cast<int>(b) & ~1;
-    }
+    h->band_fp8 = scheduling_band(cfg->H, 1, 128);  // e4m3 weights: twice the tiles per byte
     h->fp8 = fp8;
 
     auto cleanup = [&](int code) {
@@ -585,9 +581,14 @@ int init_impl(const lp_config* cfg, const void* W, void* stream, lp_handle** out
     if (rc != LP_OK) return cleanup(rc);
 
     const int64_t mt = cfg->max_tokens;
+    // LP_TEST_FAIL_ALLOC=<buffer name> reports that buffer's allocation as failed: a test hook
+    // for the clean-up path (every buffer allocated so far is freed, nothing leaks)
+    const char* fail_alloc = std::getenv("LP_TEST_FAIL_ALLOC");
     auto alloc = [&](void** p, size_t bytes, const char* what) -> int {
+        if (fail_alloc != nullptr && std::strcmp(fail_alloc, what) == 0)
+            return fail(LP_ERR_OOM, "%s: allocation of %zu bytes failed (test hook)", what, bytes);
         cudaError_t e = cudaMalloc(p, bytes);
-        if (e != cudaSuccess) return cuda_fail(e, what);
+        if (e != cudaSuccess) return cuda_fail(e, what);  // LP_ERR_OOM when out of memory
         h->ws_bytes += static_cast<int64_t>(bytes);
         return LP_OK;
     };

@@ -60,3 +60,27 @@ def test_bad_id_is_reported_and_isolated():
     keep = torch.ones(200, dtype=torch.bool, device=dev)
     keep[[17, 150]] = False
     assert_bit_equal(lp[keep], good[keep], "rows with valid ids")
+
+
+@pytest.mark.parametrize("buffer", ["ws_ms", "zy", "stat_max", "is_stage", "wq"])
+def test_allocation_failure_is_reported_and_cleaned_up(buffer, monkeypatch):
+    # the test hook fails one named workspace allocation; lp_init must return LP_ERR_OOM,
+    # free what it had allocated, and a later init must succeed
+    dev = require_cuda()
+    from bit_consistent_logprob_gb300._native import LP_ERR_OOM
+
+    W = inputs.lm_head(4096, 256, seed=4, device=dev)
+    free0 = torch.cuda.mem_get_info()[0]
+    monkeypatch.setenv("LP_TEST_FAIL_ALLOC", buffer)
+    for _ in range(3):
+        with pytest.raises(LpError) as err:
+            Engine(W, n_leaves=2, max_tokens=4096, fp8=True)
+        assert err.value.code == LP_ERR_OOM and buffer in str(err.value)
+    monkeypatch.delenv("LP_TEST_FAIL_ALLOC")
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] >= free0 - (64 << 20)  # nothing leaked
+    X = inputs.hidden_states(64, 256, seed=4, device=dev)
+    ids = inputs.uniform_ids(64, 4096, seed=4, device=dev)
+    with Engine(W, n_leaves=2, max_tokens=4096, fp8=True) as eng:
+        assert torch.isfinite(eng.logprobs(X, ids)).all()
+        eng.check()
