@@ -420,3 +420,14 @@ def logprobs_with_grad(engine: "Engine", X: torch.Tensor, W: torch.Tensor,
         raise ValueError("W must be the engine's lm_head tensor")
     engine.backward_reserve(min(int(X.shape[0]), engine.max_tokens) or 1)
     return _Logprobs.apply(X, W, ids, engine)
+
+
+def visible_with_graph_gradient(visible: torch.Tensor, graph: torch.Tensor) -> torch.Tensor:
+    """visible + (graph - graph.detach()): the value of ``visible`` (e.g. the bit-consistent
+    kernel's logprobs) with the gradient of ``graph`` (any differentiable computation of the
+    same quantity), the form the pages give for attaching a training graph's backward to an
+    inference kernel's forward values (vLLM blog "Finish RL training faster", section 3.1).
+    ``logprobs_with_grad`` does the same job with the engine's own backward."""
+    if visible.shape != graph.shape:
+        raise ValueError("visible and graph must have the same shape")
+    return visible.detach() + (graph - graph.detach())
