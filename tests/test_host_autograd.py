@@ -15,7 +15,7 @@ def test_value_is_visible_and_gradient_is_the_graphs():
     out = visible_with_graph_gradient(visible, graph)
     assert torch.equal(out.detach(), visible)
     g = torch.linspace(-1, 1, 5, dtype=torch.float64)
-    (out * g).sum().backward()
+    (out * g).sum().backward(retain_graph=True)
     gx, gw = X.grad.clone(), W.grad.clone()
     X.grad = None
     W.grad = None
