@@ -10,11 +10,13 @@
 //                             gradient with respect to the logits (backward).
 //  partials_lse_kernel        upper levels of the leaf tree over gathered slice partials,
 //                             then the same per-tile log-sum-exp (emulated TP path).
-//  lse_combine_kernel         fixed pairwise tree over the vocabulary tiles of each row,
-//                             logZ and the sampled-token logprob.
+//  lse_combine_kernel<ent>    fixed pairwise tree over the 64-column tiles of each row,
+//                             logZ and the sampled-token logprob (and the row entropy).
+//  wait_selftest_kernel       the bounded mbarrier wait on a barrier nothing arrives on
+//                             (failure-detection self-test).
 //  is_block_kernel /
 //  is_final_kernel            importance weight per token and D3 over a fixed tree of
-//                             1024-token blocks (fp64 sums).
+//                             1024-token blocks (double-float within a block, fp64 above).
 #pragma once
 
 // Non-template kernels are `static` (internal linkage): each translation unit that

@@ -1,5 +1,8 @@
 // lp_api.cu -- host side of the C ABI declared in include/lp.h: argument checks, the
-// fixed launch plan, workspace ownership, TMA descriptors and kernel launches.
+// fixed launch plan, workspace ownership, TMA descriptors and kernel launches for the
+// logprob path (bf16 and block-FP8 handles), the RL epilogues, the backward (whose two plain
+// GEMMs go to cuBLAS) and the failure-detection self-test.  The execution contract lives in
+// lp_contract.cu, the handle-free entry point in lp_noalloc.cu.
 //
 // The plan depends only on (H, V, N, tp_slices, max_tokens) and on how many rows a
 // call carries; the per-element arithmetic never depends on T, the SM count or the
