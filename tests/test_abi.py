@@ -94,3 +94,50 @@ def test_engine_requires_the_native_library(monkeypatch, tmp_path):
     monkeypatch.setattr(build, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no CPU or PyTorch fallback"):
         _native.load()
+
+
+C_CONSUMER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "lp.h"
+
+int main(void) {
+    lp_config cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.H = 7168; cfg.V = 129280; cfg.n_leaves = 8; cfg.tp_slices = 1; cfg.max_tokens = 2048;
+    unsigned char d[32];
+    if (lp_contract_digest(&cfg, LP_PRECISION_BF16, LP_DIGEST_NUMERICAL_POLICY, d) != LP_OK) {
+        fprintf(stderr, "%s\n", lp_last_error());
+        return 1;
+    }
+    printf("%d ", lp_version());
+    for (int i = 0; i < 32; ++i) printf("%02x", d[i]);
+    printf("\n");
+    cfg.n_leaves = 3;  /* outside the proven set */
+    return lp_contract_digest(&cfg, LP_PRECISION_BF16, 0, d) == LP_ERR_UNSUPPORTED ? 0 : 2;
+}
+"""
+
+
+def test_plain_c_program_compiles_and_links_against_the_library(lib, tmp_path):
+    # the header is C (not only C++), and a C program links liblp.so with no Python around it
+    import shutil
+    import subprocess
+
+    from bit_consistent_logprob_gb300 import contract
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("needs gcc")
+    src = tmp_path / "consumer.c"
+    src.write_text(C_CONSUMER)
+    exe = tmp_path / "consumer"
+    libdir = os.path.dirname(_native.library_path())
+    subprocess.check_call([gcc, "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                           str(src), "-o", str(exe), "-L", libdir, "-llp",
+                           f"-Wl,-rpath,{libdir}"])
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    assert int(out[0]) == lib.lp_version()
+    want = contract.digest(contract.NUMERICAL_POLICY, H=7168, V=129280, n_leaves=8,
+                           max_tokens=2048)
+    assert out[1] == want.hex()
