@@ -162,3 +162,20 @@ def test_backward_qwen_shape_rows(dev):
     bx = (2.0 ** -8) * (np.abs(dl) @ np.abs(_bf16_f64(W)))
     ex = np.abs(dX.cpu().double().numpy()[rows] - want_dX)
     assert np.all(ex <= bx + 1e-6 * np.abs(want_dX).max()), ex.max()
+
+
+def test_entropy_qwen_shape_rows(dev):
+    # Qwen-shape lm_head: entropy of sampled rows of a 2-row-tile batch against the oracle, and
+    # the entropy path's logp bits equal to the plain path's at full vocabulary width
+    T, H, V, N = 300, 2048, 151936, 8
+    X = inputs.hidden_states(T, H, seed=1003, device=dev)
+    W = inputs.lm_head(V, H, seed=1003, device=dev)
+    ids = inputs.uniform_ids(T, V, seed=1003, device=dev)
+    with Engine(W, n_leaves=N, max_tokens=T) as eng:
+        lp, lz, ent = eng.logprobs_entropy(X, ids)
+        assert_bit_equal(lp, eng.logprobs(X, ids), "logp with entropy at the Qwen shape")
+        eng.check()
+    rows = np.array([0, 127, 128, 299])
+    want = oracle.entropy(X.cpu(), W.cpu(), rows=rows)
+    err = np.abs(ent.cpu().double().numpy()[rows] - want).max()
+    assert err <= 1e-4, err
