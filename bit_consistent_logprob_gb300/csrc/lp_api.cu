@@ -31,6 +31,8 @@ constexpr int64_t kMaxIsTokens = (1LL << 31) - 1;
 constexpr int64_t kTpRows = 1024;               // rows per pass of the emulated TP path
 constexpr int kProfPairs = 4096;
 constexpr int64_t kIsStage = 1 << 20;            // tokens per pass of the host IS call
+constexpr int64_t kHostFirstPiece = 512;  // lp_logprobs_host: rows of the first piece
+constexpr int64_t kHostGrowth = 8;        // ... and the growth of each piece over the last
 
 thread_local std::string g_last_error = "no error";
 
@@ -132,6 +134,12 @@ struct lp_handle {
     int32_t* ids_stage = nullptr;
     float* logp_stage = nullptr;
     float* logz_stage = nullptr;
+    // lp_logprobs_host pipeline: pieces alternate between the two halves of the staging
+    // buffers; the copy of piece i+1 (on copy_stream) runs under the GEMM of piece i
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t stage_ready[2] = {nullptr, nullptr};  // half b holds its piece
+    cudaEvent_t stage_free[2] = {nullptr, nullptr};   // half b's kernels are done with it
+    cudaEvent_t host_entry = nullptr;                 // the caller's stream at entry
     float* is_stage = nullptr;      // [3][kIsStage]: log pi, log mu, w of one pass
     uint8_t* is_mask_stage = nullptr;
     double* scalars = nullptr;      // [2]: D3 and n_valid of the host IS call
@@ -502,6 +510,10 @@ void lp_free(lp_handle* h) {
     if (h == nullptr) return;
     cudaDeviceSynchronize();
     for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
+    for (cudaEvent_t e : {h->stage_ready[0], h->stage_ready[1], h->stage_free[0],
+                          h->stage_free[1], h->host_entry})
+        if (e) cudaEventDestroy(e);
+    if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
     cudaFree(h->ws_ms);
     cudaFree(h->zy);
     cudaFree(h->status);
@@ -628,6 +640,14 @@ int init_impl(const lp_config* cfg, const void* W, void* stream, lp_handle** out
         if ((rc = alloc(reinterpret_cast<void**>(&h->tp_parts), bytes, "tp_parts")) ||
             (rc = alloc(reinterpret_cast<void**>(&h->tp_gather), bytes, "tp_gather")))
             return cleanup(rc);
+    }
+
+    {
+        cudaError_t ce = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking);
+        for (cudaEvent_t* ev : {&h->stage_ready[0], &h->stage_ready[1], &h->stage_free[0],
+                                &h->stage_free[1], &h->host_entry})
+            if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+        if (ce != cudaSuccess) return cleanup(cuda_fail(ce, "host staging stream and events"));
     }
 
     if ((rc = set_gemm_attributes<lp::kModeNode>()) != LP_OK ||
@@ -864,29 +884,55 @@ int lp_logprobs_host(lp_handle* h, const void* X, int64_t ldx, const int32_t* id
     if (ldx < h->cfg.H) return fail(LP_ERR_INVALID_ARG, "ldx must be >= H");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     h->last_stream = st;
-    const int64_t chunk = h->chunk_rows;
     const int H = h->cfg.H;
+    // Pieces: a first piece of kHostFirstPiece rows, then each piece kHostGrowth times the
+    // one before, each within one half of the staging buffers (max_tokens rows) and within
+    // one pass (chunk_rows).  Only the first copy is exposed: the GEMM of a piece takes far
+    // longer than the copy of a piece kHostGrowth times its size at large vocabularies.  With
+    // max_tokens < 256 the halves are too small and pieces of max_tokens rows run one after
+    // the other in the whole buffer.  Pieces are row ranges: the results do not depend on
+    // the split.
+    const int64_t half = h->cfg.max_tokens / 2 / lp::kBM * lp::kBM;
+    const int nbuf = half > 0 ? 2 : 1;
+    const int64_t cap = nbuf == 2 ? (half < h->chunk_rows ? half : h->chunk_rows) : h->chunk_rows;
+    const int64_t slot = nbuf == 2 ? half : 0;  // rows between the two halves
     const uint8_t* xb = static_cast<const uint8_t*>(X);
+    uint16_t* xs = static_cast<uint16_t*>(h->x_stage);
+    // the copy stream starts after everything already queued on the caller's stream
+    LP_CUDA(cudaEventRecord(h->host_entry, st), "host entry event");
+    LP_CUDA(cudaStreamWaitEvent(h->copy_stream, h->host_entry, 0), "host entry wait");
     int32_t launches = 0;
-    for (int64_t r0 = 0; r0 < T; r0 += chunk) {
-        const int rows = static_cast<int>(T - r0 < chunk ? T - r0 : chunk);
-        LP_CUDA(cudaMemcpy2DAsync(h->x_stage, static_cast<size_t>(H) * 2, xb + r0 * ldx * 2,
+    int i = 0;
+    int64_t piece = nbuf == 2 && kHostFirstPiece < cap ? kHostFirstPiece : cap;
+    for (int64_t r0 = 0; r0 < T; r0 += piece, ++i) {
+        if (i > 0) piece = piece * kHostGrowth < cap ? piece * kHostGrowth : cap;
+        const int rows = static_cast<int>(T - r0 < piece ? T - r0 : piece);
+        const int b = i % nbuf;
+        const int64_t off = b * slot;
+        if (i >= nbuf)
+            LP_CUDA(cudaStreamWaitEvent(h->copy_stream, h->stage_free[b], 0), "stage free wait");
+        LP_CUDA(cudaMemcpy2DAsync(xs + off * H, static_cast<size_t>(H) * 2, xb + r0 * ldx * 2,
                                   static_cast<size_t>(ldx) * 2, static_cast<size_t>(H) * 2, rows,
-                                  cudaMemcpyHostToDevice, st),
+                                  cudaMemcpyHostToDevice, h->copy_stream),
                 "X host-to-device copy");
-        LP_CUDA(cudaMemcpyAsync(h->ids_stage, ids + r0, sizeof(int32_t) * rows,
-                                cudaMemcpyHostToDevice, st),
+        LP_CUDA(cudaMemcpyAsync(h->ids_stage + off, ids + r0, sizeof(int32_t) * rows,
+                                cudaMemcpyHostToDevice, h->copy_stream),
                 "ids host-to-device copy");
-        int rc = logprobs_chunk(h, h->x_stage, H, h->ids_stage, rows, h->logp_stage,
-                                h->logz_stage, nullptr, st);
+        LP_CUDA(cudaEventRecord(h->stage_ready[b], h->copy_stream), "stage ready event");
+        LP_CUDA(cudaStreamWaitEvent(st, h->stage_ready[b], 0), "stage ready wait");
+        int rc = logprobs_chunk(h, xs + off * H, H, h->ids_stage + off, rows, h->logp_stage + off,
+                                h->logz_stage + off, nullptr, st);
         if (rc != LP_OK) return rc;
         launches += h->last_launches;
         h->last_launches = 0;
-        LP_CUDA(cudaMemcpyAsync(out_logp + r0, h->logp_stage, sizeof(float) * rows,
+        LP_CUDA(cudaEventRecord(h->stage_free[b], st), "stage free event");
+        // the results of this piece leave on the caller's stream, before any later kernel
+        // there can overwrite them
+        LP_CUDA(cudaMemcpyAsync(out_logp + r0, h->logp_stage + off, sizeof(float) * rows,
                                 cudaMemcpyDeviceToHost, st),
                 "logp device-to-host copy");
         if (out_logZ)
-            LP_CUDA(cudaMemcpyAsync(out_logZ + r0, h->logz_stage, sizeof(float) * rows,
+            LP_CUDA(cudaMemcpyAsync(out_logZ + r0, h->logz_stage + off, sizeof(float) * rows,
                                     cudaMemcpyDeviceToHost, st),
                     "logZ device-to-host copy");
     }

@@ -135,8 +135,13 @@ LP_API int lp_logprobs_entropy(lp_handle* h, const void* X, int64_t ldx, const i
 /*
  * Same as lp_logprobs with HOST buffers (X: bf16 [T, ldx]; ids, out_logp,
  * out_logZ as above but in host memory; pinned memory is fastest).  Rows are
- * staged through the handle's device workspace chunk by chunk; the call
- * returns after the results are in host memory (it synchronises `stream`).
+ * staged through the handle's device workspace in pieces (512 rows, then 8
+ * times the previous piece, at most half of max_tokens, alternating between the
+ * two halves of the workspace when max_tokens >= 256): the host-to-device copy
+ * of the next piece runs on a stream the handle owns, under the kernels of the
+ * current piece on `stream`.
+ * Results do not depend on the split.  The call returns after the results are
+ * in host memory (it synchronises `stream`).
  */
 LP_API int lp_logprobs_host(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int64_t T,
                      float* out_logp, float* out_logZ, void* stream);
