@@ -78,8 +78,10 @@ __host__ __device__ constexpr int kNumBars(int stages) { return 2 * stages + 2 *
 
 // A pipeline stage holds kSub 64-wide K sub-blocks of X and of W (4 MMAs of K = 16 per
 // sub-block).  More MMAs per stage means fewer barrier synchronisations per MMA in the
-// issuing thread; the MMA sequence of a leaf is the same for every kSub.
-__host__ __device__ constexpr int gemm_stages(int sub) { return 6 / sub; }
+// issuing thread; the MMA sequence of a leaf is the same for every kSub.  kSub = 2: three
+// 128-K stages (192 KB); kSub = 1: seven 64-K stages (224 KB), the deeper ring for launches
+// that stream W from DRAM.
+__host__ __device__ constexpr int gemm_stages(int sub) { return sub == 1 ? 7 : 3; }
 
 __host__ __device__ constexpr int gemm_smem_bytes(int sub) {
     return 1024 /* alignment slack */ + gemm_stages(sub) * sub * 2 * kTileBytes +
