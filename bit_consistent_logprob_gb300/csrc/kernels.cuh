@@ -118,6 +118,17 @@ __device__ __forceinline__ void pair_tile_coords(int ct, const GemmParams& p, in
     vt = 2 * (vp0 + (r - rt * width)) + static_cast<int>(rank);
 }
 
+// W-sharing pair (two-row-tile decode launches): the two CTAs take row tiles 2*rp and
+// 2*rp + 1 of one vocabulary tile and share its W tile, each loading 64 of its 128 vocabulary
+// rows and multicasting them to both; each loads its own X tile.  A CTA whose row tile lies
+// past T still loads and computes (its partner needs its half of W) but writes nothing.
+__device__ __forceinline__ void wpair_tile_coords(int ct, const GemmParams& p, uint32_t rank,
+                                                  int& rt, int& vt) {
+    const int rp = ct / p.num_vocab_tiles;
+    vt = ct - rp * p.num_vocab_tiles;
+    rt = 2 * rp + static_cast<int>(rank);
+}
+
 __device__ __forceinline__ void raise_timeout(const GemmParams& p, volatile int* abort_flag) {
     *abort_flag = 1;
     atomicOr(p.status, kStatusTimeout);
@@ -144,13 +155,16 @@ __device__ __forceinline__ void release_buf(uint64_t* bar) {
 
 // kCluster = 1: one CTA per tile.  kCluster = 2: clusters of two CTAs share the X tile of
 // vocabulary-adjacent tiles; each CTA loads 64 of its 128 rows and multicasts them to both
-// (tmX then has 64-row boxes).  The per-element arithmetic is identical in both modes.
-template <int kMode, int kSub, int kCluster>
+// (tmX then has 64-row boxes).  kCluster = 2 with kShareW: the pair shares the W tile of two
+// row tiles instead (tmW then has 64-row boxes).  The per-element arithmetic is identical in
+// every mode.
+template <int kMode, int kSub, int kCluster, bool kShareW = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     leaf_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmW, const GemmParams p) {
     constexpr int kStages = gemm_stages(kSub);
     constexpr int kStageBytes = kSub * kTileBytes;       // one operand, one stage
+    static_assert(!kShareW || kCluster == 2, "W is shared within a two-CTA cluster");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -198,8 +212,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t tmem_base = *tmem_holder;
 
     const int num_pairs = (p.num_vocab_tiles + 1) >> 1;
-    const int num_tiles =
-        kCluster == 2 ? p.num_row_tiles * num_pairs : p.num_row_tiles * p.num_vocab_tiles;
+    const int num_tiles = kShareW       ? ((p.num_row_tiles + 1) >> 1) * p.num_vocab_tiles
+                          : kCluster == 2 ? p.num_row_tiles * num_pairs
+                                          : p.num_row_tiles * p.num_vocab_tiles;
     const int tile0 = kCluster == 2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
     const int tile_step = kCluster == 2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
     const int nkb = p.leaf_len / (kBK * kSub);   // stages per leaf
@@ -209,13 +224,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer (warp)
         const uint32_t tx_bytes = static_cast<uint32_t>(
-            kSub * ((kCluster == 2 ? kBM : p.x_box_rows) * kBK * 2 + kTileBytes));
+            kSub * ((kCluster == 2 && !kShareW ? kBM : p.x_box_rows) * kBK * 2 + kTileBytes));
         uint32_t stage = 0, phase = 0;
         uint64_t issued = 0;
         bool ok = true;
         for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
             int rt, vt;
-            if (kCluster == 2)
+            if (kShareW)
+                wpair_tile_coords(tile, p, crank, rt, vt);
+            else if (kCluster == 2)
                 pair_tile_coords(tile, p, num_pairs, crank, rt, vt);
             else
                 tile_coords(tile, p, rt, vt);
@@ -234,14 +251,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     for (int u = 0; u < kSub; ++u) {
                         const int k0 = kbase + (kb * kSub + u) * kBK;
                         uint8_t* xdst = sA + stage * kStageBytes + u * kTileBytes;
-                        if (kCluster == 2)  // my 64 rows of the shared X tile, to both CTAs
-                            tma_load_2d_mc_elect(&tmX, &full[stage], xdst + crank * (kTileBytes / 2),
-                                                 k0, row0 + static_cast<int>(crank) * (kBM / 2),
-                                                 kPairMask);
-                        else
+                        uint8_t* wdst = sB + stage * kStageBytes + u * kTileBytes;
+                        if constexpr (kShareW) {
+                            // my own X tile; my 64 vocabulary rows of the shared W tile, to both
                             tma_load_2d_elect(&tmX, &full[stage], xdst, k0, row0);
-                        tma_load_2d_elect(&tmW, &full[stage],
-                                          sB + stage * kStageBytes + u * kTileBytes, k0, v0);
+                            tma_load_2d_mc_elect(&tmW, &full[stage],
+                                                 wdst + crank * (kTileBytes / 2), k0,
+                                                 v0 + static_cast<int>(crank) * (kVT / 2),
+                                                 kPairMask);
+                        } else {
+                            if (kCluster == 2)  // my 64 rows of the shared X tile, to both CTAs
+                                tma_load_2d_mc_elect(&tmX, &full[stage],
+                                                     xdst + crank * (kTileBytes / 2), k0,
+                                                     row0 + static_cast<int>(crank) * (kBM / 2),
+                                                     kPairMask);
+                            else
+                                tma_load_2d_elect(&tmX, &full[stage], xdst, k0, row0);
+                            tma_load_2d_elect(&tmW, &full[stage], wdst, k0, v0);
+                        }
                     }
                     ++issued;
                     if (++stage == kStages) {
@@ -342,7 +369,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         bool ok = true;
         for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
             int rt, vt;
-            if (kCluster == 2)
+            if (kShareW)
+                wpair_tile_coords(tile, p, crank, rt, vt);
+            else if (kCluster == 2)
                 pair_tile_coords(tile, p, num_pairs, crank, rt, vt);
             else
                 tile_coords(tile, p, rt, vt);
@@ -384,15 +413,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (depth == 1) tmem_st64(lane_base + kColS0, R);
                     float b[64];
                     tmem_ld64x2(lane_base + colP, R, lane_base + colB, b);
-#pragma unroll
-                    for (int k = 0; k < 64; ++k) R[k] = __fadd_rn(R[k], b[k]);
+                    add_rn_x2<64>(R, b);
                     ++depth;
                 } else if (npairs == 1) {
                     // single pair: the node is P0 + P1
                     float b[64];
                     tmem_ld64x2(lane_base + colP, R, lane_base + colB, b);
-#pragma unroll
-                    for (int k = 0; k < 64; ++k) R[k] = __fadd_rn(R[k], b[k]);
+                    add_rn_x2<64>(R, b);
                 } else {
                     // odd pair index: close the subtrees that end at this pair
 #pragma unroll
@@ -406,8 +433,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (trailing_ones(i) >= 2) {
                         float b[64];
                         tmem_ld64(lane_base + kColS0, b);
-#pragma unroll
-                        for (int k = 0; k < 64; ++k) R[k] = __fadd_rn(b[k], R[k]);
+                        add_rn_x2<64>(R, b);
                         --depth;
                     }
                 }

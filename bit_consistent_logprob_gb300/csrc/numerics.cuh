@@ -4,8 +4,8 @@
 // tensor-parallel split holds because every path applies exactly these
 // functions, in this order, to exactly the same fp32 values.  Every operation
 // is an explicit IEEE binary32 operation (__fadd_rn / __fsub_rn / __fmul_rn /
-// __fmaf_rn, fmaxf, and CUDA's __expf / expf / expm1f / logf), so no compiler
-// contraction can differ between kernels.
+// __fmaf_rn and the two-lane __fadd2_rn, fmaxf, and CUDA's __expf / expf / expm1f /
+// logf), so no compiler contraction can differ between kernels.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -25,6 +25,21 @@ constexpr int kMaxLeaves = 8;
 // Sticky device status bits (mapped to lp_status by the host).
 constexpr int kStatusBadId = 1;
 constexpr int kStatusTimeout = 2;
+
+// Element-wise r[i] = a[i] + r[i] over n (even) consecutive values, two lanes per
+// instruction.  Each lane of __fadd2_rn is one IEEE binary32 round-to-nearest addition, so
+// every element gets exactly the bits of __fadd_rn; the pairing only halves the additions
+// issued (the leaf-tree adds of the bf16 epilogue).
+template <int n>
+__device__ __forceinline__ void add_rn_x2(float* r, const float* a) {
+    static_assert(n % 2 == 0, "pairs of elements");
+#pragma unroll
+    for (int i = 0; i < n; i += 2) {
+        const float2 t = __fadd2_rn(make_float2(a[i], a[i + 1]), make_float2(r[i], r[i + 1]));
+        r[i] = t.x;
+        r[i + 1] = t.y;
+    }
+}
 
 // Pairwise sum of 32 values, adjacent pairs first, level by level.  Destroys v.
 __device__ __forceinline__ float tree_sum32(float (&v)[32]) {
