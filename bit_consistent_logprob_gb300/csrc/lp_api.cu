@@ -913,10 +913,13 @@ int lp_logprobs_host(lp_handle* h, const void* X, int64_t ldx, const int32_t* id
     // one pass (chunk_rows).  Only the first copy is exposed: the GEMM of a piece takes far
     // longer than the copy of a piece kHostGrowth times its size at large vocabularies.  With
     // max_tokens < 256 the halves are too small and pieces of max_tokens rows run one after
-    // the other in the whole buffer.  Pieces are row ranges: the results do not depend on
-    // the split.
+    // the other in the whole buffer.  A call of at most kHostFirstPiece rows that fits the
+    // buffer is one piece: its copy is exposed either way, and a launch of so few rows streams
+    // all of W, so every extra piece would read W again.  Pieces are row ranges: the results
+    // do not depend on the split.
     const int64_t half = h->cfg.max_tokens / 2 / lp::kBM * lp::kBM;
-    const int nbuf = half > 0 ? 2 : 1;
+    const bool one_piece = T <= kHostFirstPiece && T <= h->chunk_rows && T <= h->cfg.max_tokens;
+    const int nbuf = half > 0 && !one_piece ? 2 : 1;
     const int64_t cap = nbuf == 2 ? (half < h->chunk_rows ? half : h->chunk_rows) : h->chunk_rows;
     const int64_t slot = nbuf == 2 ? half : 0;  // rows between the two halves
     const uint8_t* xb = static_cast<const uint8_t*>(X);

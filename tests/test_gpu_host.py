@@ -6,8 +6,8 @@ on a second stream while the current one computes.
 Rows are independent of the batch around them (vLLM blog "Finish RL training faster",
 section 2: batch independence), so every split must reproduce the device call bit for bit:
 one piece, several pieces, more pieces than halves (each half reused), pieces capped by a small
-workspace, the serial layout of a workspace under 256 rows, strided host rows, the emulated
-TP path and the block-FP8 path.
+workspace, the serial layout of a workspace under 256 rows, a small call as one piece, strided
+host rows, the emulated TP path and the block-FP8 path.
 """
 import pytest
 import torch
@@ -52,11 +52,26 @@ def _compare(eng, X, ids, what):
     (2600, 5000),     # five pieces, both halves reused, several passes through the workspace
     (1000, 2999),     # pieces capped at a 384-row half: eight pieces
     (200, 777),       # workspace under 256 rows: whole-buffer pieces one after the other
+    (256, 256),       # a decode batch filling its workspace: one piece, not two halves
+    (1000, 512),      # the largest call that runs as one piece
+    (600, 513),       # one row more: 256-row pieces in the two halves
 ])
 def test_host_pieces_match_device(data, max_tokens, T):
     X, W, ids = data
     with Engine(W, n_leaves=N, max_tokens=max_tokens) as eng:
         _compare(eng, X[:T], ids[:T], f"max_tokens={max_tokens} T={T}")
+
+
+@pytest.mark.parametrize("max_tokens,T", [(256, 256), (1000, 300), (6000, 7)])
+def test_host_small_call_is_one_launch(data, max_tokens, T):
+    # A call of at most 512 rows that fits the workspace streams W once, like the device call.
+    X, W, ids = data
+    with Engine(W, n_leaves=N, max_tokens=max_tokens) as eng:
+        eng.logprobs(X[:T], ids[:T])
+        dev_launches = eng.last_launch_count
+        eng.logprobs_host(_host(X[:T]), _host(ids[:T]))
+        assert eng.last_launch_count == dev_launches
+        eng.check()
 
 
 def test_host_strided_rows(data):
