@@ -84,6 +84,7 @@ def _bf16_f64(t):
 @pytest.mark.parametrize("T,H,V,N,chunk", [
     (300, 256, 4001, 4, 300),     # 3 row tiles, ragged vocabulary, one chunk
     (300, 256, 4001, 4, 128),     # three backward chunks accumulate into dW
+    (300, 256, 4001, 4, 200),     # a two-row-tile chunk (W-sharing pairs), then a ragged one
     (97, 512, 32001, 8, 97),      # one partial row tile, leaves of 64
 ])
 def test_backward_matches_oracle(dev, T, H, V, N, chunk):

@@ -147,10 +147,10 @@ def test_packed_sequences_vs_each_alone(eng, data):
     eng.check()
 
 
-@pytest.mark.parametrize("s", [2, 4, 8])
-def test_tp_emulated_split(data, eng, s):
+@pytest.mark.parametrize("s,T", [(2, 1500), (4, 1500), (8, 1500), (2, 200), (8, 256)])
+def test_tp_emulated_split(data, eng, s, T):
+    # 1500 rows: a 1024-row and a 476-row pass; 200 and 256 rows: two row tiles, W-sharing pairs
     X, W, ids = data
-    T = 1500
     base, baseZ = eng.logprobs(X[:T], ids[:T], return_logZ=True)
     with Engine(W, n_leaves=N, tp_slices=s, max_tokens=T) as e:
         lp, lz = e.logprobs(X[:T], ids[:T], return_logZ=True)
