@@ -103,6 +103,18 @@ typedef struct lp_handle lp_handle; /* opaque, owned by the library */
  * workspace (device memory sized by max_tokens and V, plus pinned staging for the
  * *_host call).  Returns LP_ERR_UNSUPPORTED for a configuration outside the
  * proven set or a device that is not sm_103.
+ *
+ * Environment variables read here, for this handle's lifetime.  The first group changes only
+ * which CTA computes a tile and how data moves, never a bit of any output (the tests prove
+ * each against the default layout):
+ *   LP_FORCE_SINGLE_CTA=1    one CTA per tile instead of two-CTA clusters;
+ *   LP_FORCE_SHORT_STAGES=1  seven 64-K pipeline stages for every launch;
+ *   LP_FORCE_SHARE_X=1       launches of 129-256 rows pair vocabulary-adjacent tiles that share
+ *                            an X tile, instead of the two row tiles of one W tile;
+ *   LP_BAND=<even n>         vocabulary tiles per scheduling band of bf16 handles (2..1024).
+ *   LP_WAIT_TIMEOUT_MS=<ms>  bound on every in-kernel wait (default 2000); on expiry the
+ *                            sticky status reads LP_ERR_TIMEOUT.
+ *   LP_TEST_FAIL_ALLOC=<name> test hook: the named workspace allocation reports failure.
  */
 LP_API int lp_init(const lp_config* cfg, const void* W, void* stream, lp_handle** out);
 
