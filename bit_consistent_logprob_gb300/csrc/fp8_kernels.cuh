@@ -324,14 +324,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        float P[32];
-                        tmem_ld32(lane_base + buf * kVT + cc * 32, P);
+                    {
+                        // both 32-column halves of the block in one TMEM round trip
+                        float P0[32], P1[32];
+                        tmem_ld32x2(lane_base + buf * kVT, P0, lane_base + buf * kVT + 32, P1);
 #pragma unroll
                         for (int k = 0; k < 32; ++k)
-                            R[cc * 32 + k] = b == 0 ? __fmul_rn(s, P[k])
-                                                    : __fmaf_rn(s, P[k], R[cc * 32 + k]);
+                            R[k] = b == 0 ? __fmul_rn(s, P0[k]) : __fmaf_rn(s, P0[k], R[k]);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            R[32 + k] = b == 0 ? __fmul_rn(s, P1[k])
+                                               : __fmaf_rn(s, P1[k], R[32 + k]);
                     }
                     release_buf(&acc_empty[buf]);
                 }
