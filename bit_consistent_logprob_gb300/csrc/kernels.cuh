@@ -65,7 +65,8 @@ struct GemmParams {
     float* ws_u;              // [num_lse_tiles][ws_ld] entropy partial per tile (kModeLseEnt)
     const float* logZ;        // [T] per-row logZ of the forward pass (kModeGrad)
     const float* gout;        // [T] dLoss/dlogp per row (kModeGrad)
-    uint16_t* dl;             // [T][ldd] bf16 gradient with respect to the logits (kModeGrad)
+    uint16_t* dl;             // [T][ldd] bf16 gradient with respect to the logits (kModeGrad;
+                              // the kernel writes it through the tmD tensor map)
     int64_t ldd;
     const float* sx;          // [T][nkb] activation block scales (block-FP8 kernel)
     const float* sw;          // [num_vocab_tiles][nkb] weight block scales (block-FP8 kernel)
@@ -81,12 +82,22 @@ __host__ __device__ constexpr int kNumBars(int stages) { return 2 * stages + 2 *
 // issuing thread; the MMA sequence of a leaf is the same for every kSub.  kSub = 2: three
 // 128-K stages (192 KB); kSub = 1: seven 64-K stages (224 KB), the deeper ring for launches
 // that stream W from DRAM.
-__host__ __device__ constexpr int gemm_stages(int sub) { return sub == 1 ? 7 : 3; }
-
-__host__ __device__ constexpr int gemm_smem_bytes(int sub) {
-    return 1024 /* alignment slack */ + gemm_stages(sub) * sub * 2 * kTileBytes +
-           kNumBars(gemm_stages(sub)) * 8 + 16 /* TMEM address, abort flag */;
+// The gradient epilogue stages each warp's 32 x 64 bf16 block of dl in shared memory for a TMA
+// store (8 warps: 32 KB), so its 64-K ring has six stages instead of seven.
+constexpr int kGradWarpBytes = 32 * kLT * 2;
+constexpr int kGradStageBytes = kEpiWarps * kGradWarpBytes;
+__host__ __device__ constexpr int gemm_stages(int sub, int mode = kModeLse) {
+    return sub == 1 ? (mode == kModeGrad ? 6 : 7) : 3;
 }
+
+__host__ __device__ constexpr int gemm_smem_bytes(int sub, int mode = kModeLse) {
+    return 1024 /* alignment slack */ + gemm_stages(sub, mode) * sub * 2 * kTileBytes +
+           (mode == kModeGrad ? kGradStageBytes : 0) + kNumBars(gemm_stages(sub, mode)) * 8 +
+           16 /* TMEM address, abort flag */;
+}
+static_assert(gemm_smem_bytes(1, kModeGrad) <= 227 * 1024 &&
+                  gemm_smem_bytes(2, kModeGrad) <= 227 * 1024 && gemm_smem_bytes(1) <= 227 * 1024,
+              "leaf-GEMM shared memory exceeds the per-CTA limit");
 
 // Tile schedule: the vocabulary is cut into bands of `band` tiles; within a band the
 // tiles run row tile by row tile, vocabulary fastest.  Concurrent CTAs therefore share
@@ -158,11 +169,13 @@ __device__ __forceinline__ void release_buf(uint64_t* bar) {
 // (tmX then has 64-row boxes).  kCluster = 2 with kShareW: the pair shares the W tile of two
 // row tiles instead (tmW then has 64-row boxes).  The per-element arithmetic is identical in
 // every mode.
+// tmD (kModeGrad only): dl as bf16 [T][ldd] with 64 x 32 boxes, 128-byte swizzle.
 template <int kMode, int kSub, int kCluster, bool kShareW = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     leaf_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
-                     const __grid_constant__ CUtensorMap tmW, const GemmParams p) {
-    constexpr int kStages = gemm_stages(kSub);
+                     const __grid_constant__ CUtensorMap tmW,
+                     const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
+    constexpr int kStages = gemm_stages(kSub, kMode);
     constexpr int kStageBytes = kSub * kTileBytes;       // one operand, one stage
     static_assert(!kShareW || kCluster == 2, "W is shared within a two-CTA cluster");
     extern __shared__ uint8_t smem_raw[];
@@ -170,7 +183,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;                                  // X  [kStages][kSub][128 x 64] bf16
     uint8_t* sB = smem + kStages * kStageBytes;          // W  [kStages][kSub][128 x 64] bf16
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kStages * kStageBytes);
+    uint8_t* sD = smem + 2 * kStages * kStageBytes;      // dl staging [8 warps][32 x 64] bf16
+    uint64_t* bars = reinterpret_cast<uint64_t*>(
+        sD + (kMode == kModeGrad ? kGradStageBytes : 0));
     uint64_t* full = bars;                               // TMA -> MMA, per stage
     uint64_t* empty = bars + kStages;                    // MMA -> TMA, per stage
     uint64_t* acc_full = bars + 2 * kStages;             // MMA -> epilogue, per TMEM buffer
@@ -464,33 +479,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         if (yc >= 0 && yc < kLT) p.zy[row] = zy;
                     }
                 } else if constexpr (kMode == kModeGrad) {
+                    // The warp's 32 rows x 64 columns of dl go to its shared-memory block in the
+                    // 128-byte swizzled layout (16-byte chunk c of row r at chunk c ^ (r % 8):
+                    // conflict-free), then one TMA store writes them; rows >= T and columns >= V
+                    // fall outside the tensor map and are not written.
                     const int nv = p.V - col0;
-                    if (row_ok && nv > 0) {
-                        const float lz = p.logZ[row], gg = p.gout[row];
-                        const int yc = ycol - h * 64;
+                    const int wrow0 = rt * kBM + q * 32;
+                    if (nv > 0 && wrow0 < p.T) {  // warp-uniform
                         uint32_t pk[32];
+                        if (row_ok) {
+                            const float lz = p.logZ[row], gg = p.gout[row];
+                            const int yc = ycol - h * 64;
 #pragma unroll
-                        for (int i = 0; i < 64; i += 2) {
-                            float d[2];
+                            for (int i = 0; i < 64; i += 2) {
+                                float d[2];
 #pragma unroll
-                            for (int k = 0; k < 2; ++k) {
-                                const float pr = __expf(__fsub_rn(R[i + k], lz));
-                                d[k] = __fmul_rn(gg, __fsub_rn(i + k == yc ? 1.0f : 0.0f, pr));
+                                for (int k = 0; k < 2; ++k) {
+                                    const float pr = __expf(__fsub_rn(R[i + k], lz));
+                                    d[k] = __fmul_rn(gg, __fsub_rn(i + k == yc ? 1.0f : 0.0f, pr));
+                                }
+                                pk[i >> 1] = pack_bf16x2(d[0], d[1]);
                             }
-                            pk[i >> 1] = pack_bf16x2(d[0], d[1]);
-                        }
-                        uint16_t* dst = p.dl + static_cast<int64_t>(row) * p.ldd + col0;
-                        if (nv >= 64) {
-#pragma unroll
-                            for (int i = 0; i < 32; i += 4)
-                                *reinterpret_cast<uint4*>(dst + 2 * i) =
-                                    make_uint4(pk[i], pk[i + 1], pk[i + 2], pk[i + 3]);
                         } else {
 #pragma unroll
-                            for (int i = 0; i < 64; ++i)
-                                if (i < nv)
-                                    dst[i] = static_cast<uint16_t>(
-                                        (i & 1) ? (pk[i >> 1] >> 16) : (pk[i >> 1] & 0xffffu));
+                            for (int i = 0; i < 32; ++i) pk[i] = 0u;
+                        }
+                        uint8_t* blk = sD + (warp - 2) * kGradWarpBytes;
+                        if (lane == 0) bulk_wait_read_all();  // the last store has read blk
+                        __syncwarp();
+                        uint8_t* myrow = blk + lane * (kLT * 2);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<uint4*>(myrow + ((c ^ (lane & 7)) << 4)) =
+                                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmD, blk, col0, wrow0);
+                            bulk_commit_group();
                         }
                     }
                 } else if (row_ok) {
@@ -507,6 +533,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
             }
+        }
+        if constexpr (kMode == kModeGrad) {
+            if (lane == 0) bulk_wait_all();  // this warp's dl stores have completed
         }
     }
 

@@ -206,11 +206,12 @@ int scheduling_band(int H, int bytes_per_weight, int max_tiles) {
 
 template <int kMode, int kSub, int kCluster, bool kShareW = false>
 cudaError_t launch_gemm_variant(int grid, cudaStream_t st, const CUtensorMap& tmX,
-                                const CUtensorMap& tmW, const lp::GemmParams& p) {
+                                const CUtensorMap& tmW, const CUtensorMap& tmD,
+                                const lp::GemmParams& p) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(lp::kGemmThreads);
-    cfg.dynamicSmemBytes = lp::gemm_smem_bytes(kSub);
+    cfg.dynamicSmemBytes = lp::gemm_smem_bytes(kSub, kMode);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     if (kCluster > 1) {
@@ -222,14 +223,14 @@ cudaError_t launch_gemm_variant(int grid, cudaStream_t st, const CUtensorMap& tm
         cfg.numAttrs = 1;
     }
     return cudaLaunchKernelEx(&cfg, lp::leaf_gemm_kernel<kMode, kSub, kCluster, kShareW>, tmX,
-                              tmW, p);
+                              tmW, tmD, p);
 }
 
 template <int kMode>
 int set_gemm_attributes() {
     const auto set = [](auto fn, int sub) {
         return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    lp::gemm_smem_bytes(sub));
+                                    lp::gemm_smem_bytes(sub, kMode));
     };
     cudaError_t e;
     if ((e = set(lp::leaf_gemm_kernel<kMode, 1, 1>, 1)) != cudaSuccess ||
@@ -298,6 +299,12 @@ int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int lea
     int rc = encode_kmajor(&tmX, X, static_cast<uint64_t>(rows), h->cfg.H, ldx,
                            static_cast<uint32_t>(p.x_box_rows));
     if (rc != LP_OK) return rc;
+    // the gradient epilogue's TMA stores: dl [rows][ldd] bf16 in 64-column x 32-row boxes
+    CUtensorMap tmD{};
+    if constexpr (kMode == lp::kModeGrad) {
+        rc = encode_kmajor(&tmD, ga.dl, static_cast<uint64_t>(rows), h->cfg.V, ga.ldd, 32);
+        if (rc != LP_OK) return rc;
+    }
     const int64_t pairs = ceil_div(h->num_vocab_tiles, 2);
     const int64_t tiles =
         share_w ? ceil_div(p.num_row_tiles, 2) * static_cast<int64_t>(h->num_vocab_tiles)
@@ -309,13 +316,13 @@ int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int lea
     if (prof) LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used], st), "profile event");
     cudaError_t e;
     if (share_w)
-        e = launch_gemm_variant<kMode, 1, 2, true>(grid, st, tmX, h->tmW64, p);
+        e = launch_gemm_variant<kMode, 1, 2, true>(grid, st, tmX, h->tmW64, tmD, p);
     else if (cluster)
-        e = sub2 ? launch_gemm_variant<kMode, 2, 2>(grid, st, tmX, h->tmW, p)
-                 : launch_gemm_variant<kMode, 1, 2>(grid, st, tmX, h->tmW, p);
+        e = sub2 ? launch_gemm_variant<kMode, 2, 2>(grid, st, tmX, h->tmW, tmD, p)
+                 : launch_gemm_variant<kMode, 1, 2>(grid, st, tmX, h->tmW, tmD, p);
     else
-        e = sub2 ? launch_gemm_variant<kMode, 2, 1>(grid, st, tmX, h->tmW, p)
-                 : launch_gemm_variant<kMode, 1, 1>(grid, st, tmX, h->tmW, p);
+        e = sub2 ? launch_gemm_variant<kMode, 2, 1>(grid, st, tmX, h->tmW, tmD, p)
+                 : launch_gemm_variant<kMode, 1, 1>(grid, st, tmX, h->tmW, tmD, p);
     LP_CUDA(e, "leaf_gemm_kernel launch");
     LP_CUDA(cudaGetLastError(), "leaf_gemm_kernel launch");
     if (prof) {

@@ -203,9 +203,9 @@ LP_API int lp_logprobs_noalloc(const void* W, int32_t H, int32_t V, int32_t n_le
     const int64_t tiles = static_cast<int64_t>(p.num_row_tiles) * p.num_vocab_tiles;
     const int grid = static_cast<int>(tiles < s.num_sms ? tiles : s.num_sms);
     if (p.leaf_len % (2 * lp::kBK) == 0)
-        lp::leaf_gemm_kernel<lp::kModeLse, 2, 1><<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(2), st>>>(tmX, tmW, p);
+        lp::leaf_gemm_kernel<lp::kModeLse, 2, 1><<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(2), st>>>(tmX, tmW, tmX, p);
     else
-        lp::leaf_gemm_kernel<lp::kModeLse, 1, 1><<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(1), st>>>(tmX, tmW, p);
+        lp::leaf_gemm_kernel<lp::kModeLse, 1, 1><<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(1), st>>>(tmX, tmW, tmX, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return nfail(LP_ERR_CUDA, "leaf_gemm_kernel launch: %s", cudaGetErrorString(e));
 
