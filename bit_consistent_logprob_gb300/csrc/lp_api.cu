@@ -111,6 +111,7 @@ struct lp_handle {
     uint64_t timeout_ns = 0;
     CUtensorMap tmW{};
     CUtensorMap tmW64{};  // the same W with 64-row boxes (W-sharing cluster pairs)
+    double* host_scalars = nullptr;  // pinned host: D3 and n_valid of the host-buffer call
     // workspace (device)
     float2* ws_ms = nullptr;      // [num_lse_tiles][max_tokens]
     float* ws_u = nullptr;        // [num_lse_tiles][max_tokens] entropy partials
@@ -564,6 +565,7 @@ void lp_free(lp_handle* h) {
     cudaFree(h->logz_stage);
     cudaFree(h->is_stage);
     cudaFree(h->is_mask_stage);
+    if (h->host_scalars) cudaFreeHost(h->host_scalars);
     cudaFree(h->scalars);
     delete h;
 }
@@ -661,6 +663,12 @@ int init_impl(const lp_config* cfg, const void* W, void* stream, lp_handle** out
         (rc = alloc(reinterpret_cast<void**>(&h->is_mask_stage), kIsStage, "is_mask_stage")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->scalars), 2 * sizeof(double), "scalars")))
         return cleanup(rc);
+    if (fail_alloc != nullptr && std::strcmp(fail_alloc, "host_scalars") == 0)
+        return cleanup(fail(LP_ERR_OOM, "host_scalars: allocation failed (test hook)"));
+    if (cudaError_t e = cudaMallocHost(reinterpret_cast<void**>(&h->host_scalars),
+                                       2 * sizeof(double));
+        e != cudaSuccess)
+        return cleanup(cuda_fail(e, "host_scalars"));
     h->chunk_rows = mt;
     if (cfg->tp_slices > 1) {
         h->chunk_rows = mt < kTpRows ? mt : kTpRows;
@@ -931,9 +939,14 @@ int lp_logprobs_host(lp_handle* h, const void* X, int64_t ldx, const int32_t* id
     const int64_t slot = nbuf == 2 ? half : 0;  // rows between the two halves
     const uint8_t* xb = static_cast<const uint8_t*>(X);
     uint16_t* xs = static_cast<uint16_t*>(h->x_stage);
-    // the copy stream starts after everything already queued on the caller's stream
-    LP_CUDA(cudaEventRecord(h->host_entry, st), "host entry event");
-    LP_CUDA(cudaStreamWaitEvent(h->copy_stream, h->host_entry, 0), "host entry wait");
+    // Pieces are copied on the handle's copy stream, which starts after everything already
+    // queued on the caller's stream; a single piece has nothing to overlap and is copied on the
+    // caller's stream itself.
+    cudaStream_t cs = one_piece ? st : h->copy_stream;
+    if (!one_piece) {
+        LP_CUDA(cudaEventRecord(h->host_entry, st), "host entry event");
+        LP_CUDA(cudaStreamWaitEvent(h->copy_stream, h->host_entry, 0), "host entry wait");
+    }
     int32_t launches = 0;
     int i = 0;
     int64_t piece = nbuf == 2 && kHostFirstPiece < cap ? kHostFirstPiece : cap;
@@ -943,22 +956,24 @@ int lp_logprobs_host(lp_handle* h, const void* X, int64_t ldx, const int32_t* id
         const int b = i % nbuf;
         const int64_t off = b * slot;
         if (i >= nbuf)
-            LP_CUDA(cudaStreamWaitEvent(h->copy_stream, h->stage_free[b], 0), "stage free wait");
+            LP_CUDA(cudaStreamWaitEvent(cs, h->stage_free[b], 0), "stage free wait");
         LP_CUDA(cudaMemcpy2DAsync(xs + off * H, static_cast<size_t>(H) * 2, xb + r0 * ldx * 2,
                                   static_cast<size_t>(ldx) * 2, static_cast<size_t>(H) * 2, rows,
-                                  cudaMemcpyHostToDevice, h->copy_stream),
+                                  cudaMemcpyHostToDevice, cs),
                 "X host-to-device copy");
         LP_CUDA(cudaMemcpyAsync(h->ids_stage + off, ids + r0, sizeof(int32_t) * rows,
-                                cudaMemcpyHostToDevice, h->copy_stream),
+                                cudaMemcpyHostToDevice, cs),
                 "ids host-to-device copy");
-        LP_CUDA(cudaEventRecord(h->stage_ready[b], h->copy_stream), "stage ready event");
-        LP_CUDA(cudaStreamWaitEvent(st, h->stage_ready[b], 0), "stage ready wait");
+        if (!one_piece) {
+            LP_CUDA(cudaEventRecord(h->stage_ready[b], cs), "stage ready event");
+            LP_CUDA(cudaStreamWaitEvent(st, h->stage_ready[b], 0), "stage ready wait");
+        }
         int rc = logprobs_chunk(h, xs + off * H, H, h->ids_stage + off, rows, h->logp_stage + off,
                                 h->logz_stage + off, nullptr, st);
         if (rc != LP_OK) return rc;
         launches += h->last_launches;
         h->last_launches = 0;
-        LP_CUDA(cudaEventRecord(h->stage_free[b], st), "stage free event");
+        if (!one_piece) LP_CUDA(cudaEventRecord(h->stage_free[b], st), "stage free event");
         // the results of this piece leave on the caller's stream, before any later kernel
         // there can overwrite them
         LP_CUDA(cudaMemcpyAsync(out_logp + r0, h->logp_stage + off, sizeof(float) * rows,
@@ -1185,8 +1200,10 @@ int lp_importance_weights_host(lp_handle* h, const float* logp_pi, const float* 
                                             reinterpret_cast<int64_t*>(d3_dev + 1));
     LP_CUDA(cudaGetLastError(), "is_final_kernel launch");
     ++h->last_launches;
-    double res[2];
-    LP_CUDA(cudaMemcpyAsync(res, d3_dev, sizeof res, cudaMemcpyDeviceToHost, st), "D3 copy");
+    // D3 and n_valid land in pinned memory (a copy to pageable memory would be staged)
+    double* res = h->host_scalars;
+    LP_CUDA(cudaMemcpyAsync(res, d3_dev, 2 * sizeof(double), cudaMemcpyDeviceToHost, st),
+            "D3 copy");
     LP_CUDA(cudaStreamSynchronize(st), "stream synchronize");
     *out_d3 = res[0];
     if (out_nvalid) std::memcpy(out_nvalid, &res[1], sizeof(int64_t));

@@ -62,7 +62,7 @@ def test_bad_id_is_reported_and_isolated():
     assert_bit_equal(lp[keep], good[keep], "rows with valid ids")
 
 
-@pytest.mark.parametrize("buffer", ["ws_ms", "zy", "stat_max", "is_stage", "wq"])
+@pytest.mark.parametrize("buffer", ["ws_ms", "zy", "stat_max", "is_stage", "host_scalars", "wq"])
 def test_allocation_failure_is_reported_and_cleaned_up(buffer, monkeypatch):
     # the test hook fails one named workspace allocation; lp_init must return LP_ERR_OOM,
     # free what it had allocated, and a later init must succeed
