@@ -145,8 +145,10 @@ static __global__ void __launch_bounds__(256) quant_w_kernel(const uint16_t* W, 
     if (threadIdx.x == 0) sw[static_cast<int64_t>(vb) * nkb + kb] = s;
 }
 
-// The block-scaled leaf GEMM with the fused log-sum-exp epilogue (kModeLse outputs).
+// The block-scaled leaf GEMM with the fused log-sum-exp epilogue (kModeLse outputs; with kEnt
+// also the entropy partial per tile, as kModeLseEnt).
 // p.leaf_len is in elements (a multiple of 128); p.sx [T][nkb], p.sw [num_vocab_tiles][nkb].
+template <bool kEnt>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     leaf_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmX,
                          const __grid_constant__ CUtensorMap tmW, const GemmParams p) {
@@ -394,8 +396,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (row_ok && nv > 0) {
                 float zy = 0.0f;
                 const int yc = ycol - h * 64;
-                const float2 ms = tile_lse64(R, min(nv, kLT), yc, zy);
-                p.ws_ms[static_cast<int64_t>(2 * vt + h) * p.ws_ld + row] = ms;
+                const int64_t wi = static_cast<int64_t>(2 * vt + h) * p.ws_ld + row;
+                if constexpr (kEnt) {
+                    float u;
+                    p.ws_ms[wi] = tile_lse64_ent(R, min(nv, kLT), yc, zy, u);
+                    p.ws_u[wi] = u;
+                } else {
+                    p.ws_ms[wi] = tile_lse64(R, min(nv, kLT), yc, zy);
+                }
                 if (yc >= 0 && yc < kLT) p.zy[row] = zy;
             }
         }

@@ -403,7 +403,7 @@ int launch_partials_lse(lp_handle* h, const float* parts, int n_parts, int64_t p
 // Block-FP8 path for one chunk: quantise the rows (1 x 128 blocks), then the block-scaled leaf
 // GEMM with the fused tile log-sum-exp (one CTA per tile, X box cut to the rows when T < 128).
 int launch_fp8_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int rows,
-                     cudaStream_t st) {
+                     bool entropy, cudaStream_t st) {
     const int H = h->cfg.H;
     const int nkb = H / lp::kQBlock;
     const int64_t warps = static_cast<int64_t>(rows) * nkb;
@@ -426,6 +426,7 @@ int launch_fp8_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* id
     p.ws_ms = h->ws_ms;
     p.ws_ld = h->cfg.max_tokens;
     p.zy = h->zy;
+    p.ws_u = h->ws_u;
     p.sx = h->sx;
     p.sw = h->sw;
     p.nkb = nkb;
@@ -440,7 +441,12 @@ int launch_fp8_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* id
     const int grid = static_cast<int>(tiles < h->num_sms ? tiles : h->num_sms);
     const bool prof = h->profiling && h->prof_used < kProfPairs;
     if (prof) LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used], st), "profile event");
-    lp::leaf_gemm_fp8_kernel<<<grid, lp::kGemmThreads, lp::fp8_smem_bytes(), st>>>(tmX, h->tmWq, p);
+    if (entropy)
+        lp::leaf_gemm_fp8_kernel<true><<<grid, lp::kGemmThreads, lp::fp8_smem_bytes(), st>>>(
+            tmX, h->tmWq, p);
+    else
+        lp::leaf_gemm_fp8_kernel<false><<<grid, lp::kGemmThreads, lp::fp8_smem_bytes(), st>>>(
+            tmX, h->tmWq, p);
     LP_CUDA(cudaGetLastError(), "leaf_gemm_fp8_kernel launch");
     if (prof) {
         LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used + 1], st), "profile event");
@@ -466,7 +472,7 @@ int logprobs_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids,
     int rc;
     const int s = h->cfg.tp_slices;
     if (h->fp8) {
-        rc = launch_fp8_chunk(h, X, ldx, ids, rows, st);
+        rc = launch_fp8_chunk(h, X, ldx, ids, rows, out_entropy != nullptr, st);
         if (rc != LP_OK) return rc;
     } else if (s == 1) {
         rc = out_entropy
@@ -710,7 +716,10 @@ int init_impl(const lp_config* cfg, const void* W, void* stream, lp_handle** out
             (rc = alloc(reinterpret_cast<void**>(&h->sx), sizeof(float) * static_cast<size_t>(mt) * nkb,
                         "sx")))
             return cleanup(rc);
-        if ((e = cudaFuncSetAttribute(lp::leaf_gemm_fp8_kernel,
+        if ((e = cudaFuncSetAttribute(lp::leaf_gemm_fp8_kernel<false>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      lp::fp8_smem_bytes())) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(lp::leaf_gemm_fp8_kernel<true>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       lp::fp8_smem_bytes())) != cudaSuccess)
             return cleanup(cuda_fail(e, "cudaFuncSetAttribute(leaf_gemm_fp8_kernel)"));
@@ -809,8 +818,6 @@ int lp_logprobs(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, in
 int lp_logprobs_entropy(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int64_t T,
                         float* out_logp, float* out_logZ, float* out_entropy, int phase,
                         void* stream) {
-    if (h != nullptr && h->fp8)
-        return fail(LP_ERR_UNSUPPORTED, "entropy is not built for block-FP8 handles");
     if (T > 0 && out_entropy == nullptr)
         return fail(LP_ERR_INVALID_ARG, "out_entropy must not be NULL");
     return logprobs_impl(h, X, ldx, ids, T, out_logp, out_logZ, out_entropy, phase, stream);

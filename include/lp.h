@@ -226,8 +226,9 @@ LP_API int lp_importance_weights_host(lp_handle* h, const float* logp_pi, const 
  * a handle-owned e4m3 copy with its scales (synchronises `stream`).  lp_logprobs and
  * lp_logprobs_host on such a handle quantise each chunk of X (1 x 128 blocks) and run the
  * block-scaled GEMM; results obey the same invariance (batch, position, phase, chunking).
- * lp_logprobs_entropy, lp_logits_partial, lp_logprobs_from_partials and lp_logprobs_backward
- * return LP_ERR_UNSUPPORTED on a block-FP8 handle.
+ * lp_logprobs_entropy also runs on such a handle (the same tile entropy partial and merge;
+ * logp and logZ keep the bits of lp_logprobs).  lp_logits_partial, lp_logprobs_from_partials
+ * and lp_logprobs_backward return LP_ERR_UNSUPPORTED on a block-FP8 handle.
  * lp_fp8_requantize re-quantises W after an in-place update (asynchronous on `stream`).
  * lp_fp8_weights exposes the handle's e4m3 weights [V][H] and scales [ceil(V/128)][H/128]
  * (device pointers owned by the handle) for verification.

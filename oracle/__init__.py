@@ -66,6 +66,7 @@ def _load():
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
         lib.oracle_quantize_blocks.argtypes = [p, i64, i64, i64, i64, p, p]
         lib.oracle_logprobs_fp8.argtypes = [p, p, p, p, p, i64, i64, p, i64, p, p]
+        lib.oracle_entropy_fp8.argtypes = [p, p, p, p, i64, i64, p, i64, p]
         lib.oracle_logprobs_f64.argtypes = [p, p, p, i64, i64, i64, p]
         lib.oracle_logprob_grad.argtypes = [p, p, p, p, i64, i64, i64, p, p, p]
         lib.oracle_reinforce_zero.argtypes = [p, p, p, p, i64, p, ctypes.c_int, ctypes.c_int,
@@ -341,3 +342,18 @@ def logprobs_fp8(xq, sx, wq, sw, ids, rows=None):
     _load().oracle_logprobs_fp8(_ptr(xq), _ptr(sx), _ptr(wq), _ptr(sw), _ptr(ids), H, V, _ptr(r),
                                 r.size, _ptr(logp), _ptr(logZ))
     return logp, logZ
+
+
+def entropy_fp8(xq, sx, wq, sw, rows=None) -> np.ndarray:
+    """Softmax entropy (fp64) of the listed rows, logits from block-FP8 operands."""
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    wq = np.ascontiguousarray(wq, dtype=np.uint8)
+    sx = np.ascontiguousarray(sx, dtype=np.float32)
+    sw = np.ascontiguousarray(sw, dtype=np.float32)
+    T, H = xq.shape
+    V = wq.shape[0]
+    r = _rows_arg(rows, T)
+    out = np.empty(r.size, dtype=np.float64)
+    _load().oracle_entropy_fp8(_ptr(xq), _ptr(sx), _ptr(wq), _ptr(sw), H, V, _ptr(r), r.size,
+                               _ptr(out))
+    return out

@@ -59,7 +59,8 @@
  *      E4M3 format: bias 7, 3 mantissa bits, no infinities).  The quantised
  *      bytes are an integer decision, so they are made in the same fp32
  *      arithmetic the GPU uses.  The logits are the plain fp64 dot products
- *      of the dequantised values q * s.
+ *      of the dequantised values q * s.  oracle_entropy_fp8 is oracle_entropy
+ *      over those logits.
  *
  *  - oracle_acceptance_stats: over the valid tokens, the max, mean and
  *      population standard deviation of |a - b| between two logprob vectors,
@@ -476,6 +477,43 @@ void oracle_logprobs_fp8(const uint8_t* xq, const float* sx, const uint8_t* wq, 
             int32_t y = ids[t];
             logZ[r] = lz;
             logp[r] = (y >= 0 && (int64_t)y < V) ? z[y] - lz : NAN;
+        }
+        free(xd);
+        free(z);
+    }
+}
+
+/* Softmax entropy -sum_v p log p of the listed rows, over logits from the dequantised
+ * block-FP8 operands: z[v] = sum_k (qx[k] sx) (qw[v][k] sw), all in fp64. */
+void oracle_entropy_fp8(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
+                        int64_t H, int64_t V, const int64_t* rows, int64_t nrows, double* out) {
+    int64_t nkb = H / 128;
+#pragma omp parallel
+    {
+        double* z = (double*)malloc((size_t)V * sizeof(double));
+        double* xd = (double*)malloc((size_t)H * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < nrows; ++r) {
+            const int64_t t = rows[r];
+            const float* sxrow = sx + t * nkb;
+            for (int64_t k = 0; k < H; ++k)
+                xd[k] = oracle_e4m3_decode(xq[t * H + k]) * (double)sxrow[k / 128];
+            for (int64_t v = 0; v < V; ++v) {
+                const uint8_t* wrow = wq + v * H;
+                const float* swrow = sw + (v / 128) * nkb;
+                double acc = 0.0;
+                for (int64_t k = 0; k < H; ++k)
+                    acc += xd[k] * (oracle_e4m3_decode(wrow[k]) * (double)swrow[k / 128]);
+                z[v] = acc;
+            }
+            const double lz = log_partition(z, V);
+            double h = 0.0;
+            for (int64_t v = 0; v < V; ++v) {
+                const double lpv = z[v] - lz;
+                const double pv = exp(lpv);
+                if (pv > 0.0) h -= pv * lpv;
+            }
+            out[r] = h;
         }
         free(xd);
         free(z);

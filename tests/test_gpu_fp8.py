@@ -7,7 +7,9 @@ RL training faster", section 4.1).  Checks:
 * logp within 2e-3 nats of the oracle's fp64 logprob of the dequantised operands, and within
   1e-4 (fp32 block partials, at most 56 fma promotions and 3 tree adds per logit);
 * the same invariance as the bf16 path (row alone or in a batch, decode versus prefill,
-  chunking, graph replay), and in-place weight updates picked up by re-quantisation.
+  chunking, graph replay), and in-place weight updates picked up by re-quantisation;
+* the row entropy on FP8 handles within 2e-3 of the oracle's entropy of the dequantised
+  operands, logp and logZ bit-equal to the plain call, the same bits for a row alone.
 """
 import numpy as np
 import pytest
@@ -52,6 +54,33 @@ def test_fp8_quantisation_and_logprobs_match_oracle(dev, T, H, V, N):
     errZ = np.abs(lz.cpu().double().numpy()[rows] - wantZ).max()
     assert err <= LOGP_TOL and err <= 1e-4, err
     assert errZ <= 1e-4, errZ
+
+
+@pytest.mark.parametrize("T,H,V,N", [(300, 256, 4001, 2), (130, 1024, 32001, 8)])
+def test_fp8_entropy_matches_oracle_and_keeps_logp_bits(dev, T, H, V, N):
+    X = inputs.hidden_states(T, H, seed=T + 5, device=dev)
+    W = inputs.lm_head(V, H, seed=T + 5, device=dev)
+    ids = inputs.uniform_ids(T, V, seed=T + 5, device=dev)
+    with Engine(W, n_leaves=N, max_tokens=T, fp8=True) as eng:
+        lp0, lz0 = eng.logprobs(X, ids, return_logZ=True)
+        lp, lz, ent = eng.logprobs_entropy(X, ids)
+        wq, sw = eng.fp8_weights()
+        xq, sx = eng.fp8_quantize_x(X)
+        alone = [eng.logprobs_entropy(X[r:r + 1], ids[r:r + 1])[2].clone() for r in (0, T - 1)]
+        dec = eng.logprobs_entropy(X[3:10], ids[3:10])[2].clone()
+        eng.check()
+    assert_bit_equal(lp, lp0, "FP8 logp with entropy")
+    assert_bit_equal(lz, lz0, "FP8 logZ with entropy")
+    assert_bit_equal(alone[0], ent[:1], "row 0 alone")
+    assert_bit_equal(alone[1], ent[T - 1:], "last row alone")
+    assert_bit_equal(dec, ent[3:10], "decode batch of 7")
+    rows = np.unique(np.r_[0, T - 1, np.random.default_rng(T).choice(T, min(T, 32))])
+    want = oracle.entropy_fp8(xq.cpu().numpy(), sx.cpu().numpy(), wq.cpu().numpy(),
+                              sw.cpu().numpy(), rows=rows)
+    got = ent.cpu().double().numpy()[rows]
+    err = np.abs(got - want).max()
+    assert err <= LOGP_TOL, err
+    assert np.all(got >= 0) and np.all(got <= np.log(V) + 1e-4)
 
 
 def test_fp8_invariance(dev):
@@ -106,8 +135,6 @@ def test_fp8_requantize_after_inplace_update_and_unsupported_calls(dev):
         after = eng.logprobs(X, ids)
         assert_bit_equal(after, fresh.logprobs(X, ids), "re-quantised vs fresh")
         assert not torch.equal(before, after)
-        with pytest.raises(LpError):
-            eng.logprobs_entropy(X, ids)
         with pytest.raises(LpError):
             eng.logits_partial(X, 0, 2)
         eng.check()

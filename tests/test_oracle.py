@@ -615,6 +615,38 @@ def test_logprobs_fp8_equals_the_bf16_oracle_on_representable_inputs():
     np.testing.assert_allclose(lz8, lz, rtol=1e-15, atol=0)
 
 
+def test_entropy_fp8_equals_the_bf16_oracle_on_representable_inputs():
+    # the same representable blocks as above: the block-FP8 entropy must equal the (pinned)
+    # bf16 entropy of the same values, with unit scales and with a weight block at 2^-3
+    rng = np.random.default_rng(73)
+    grid = oracle.e4m3_decode(np.arange(1, 0x7F, dtype=np.uint8))
+    grid = np.concatenate([grid, -grid])
+    def rep(shape):
+        v = rng.choice(grid[np.abs(grid) <= 2.0], size=shape)
+        v[:, ::128] = 448.0
+        return v.astype(np.float32)
+    X = f32_to_bf16_bits(rep((4, 256)) / 64.0)   # power-of-two activation scales (7/64)
+    W = f32_to_bf16_bits(np.concatenate([rep((128, 256)), rep((5, 256))]) / 256.0)
+    W[:128, 128:] = f32_to_bf16_bits(np.array([[float(bits_to_fraction(b)) for b in row]
+                                                for row in W[:128, 128:]]) / 8.0)
+    xq, sx = oracle.quantize_blocks(X, 1)
+    wq, sw = oracle.quantize_blocks(W, 128)
+    assert len(set(sw.ravel().tolist())) == 2 and np.all(sx == sx.ravel()[0])
+    np.testing.assert_allclose(oracle.entropy_fp8(xq, sx, wq, sw), oracle.entropy(X, W),
+                               rtol=1e-13, atol=1e-12)
+    # rows subset, in the order given
+    np.testing.assert_allclose(oracle.entropy_fp8(xq, sx, wq, sw, rows=[3, 0]),
+                               oracle.entropy(X, W, rows=[3, 0]), rtol=1e-13, atol=1e-12)
+
+
+def test_entropy_fp8_of_a_zero_lm_head_is_log_v():
+    X = f32_to_bf16_bits(np.random.default_rng(74).standard_normal((3, 128)).astype(np.float32))
+    W = np.zeros((300, 128), dtype=np.uint16)
+    xq, sx = oracle.quantize_blocks(X, 1)
+    wq, sw = oracle.quantize_blocks(W, 128)
+    np.testing.assert_allclose(oracle.entropy_fp8(xq, sx, wq, sw), np.log(300.0), rtol=1e-14)
+
+
 # ----------------------------------------------------------------- planted mistakes
 MUTATIONS = [
     # (description, original text, mutated text)
@@ -637,6 +669,10 @@ MUTATIONS = [
     ("gradient sign", "double coef = n > 0 ? -A /", "double coef = n > 0 ? A /"),
     ("TIS as a floor", "wh > tis_cap) wh = tis_cap;", "wh < tis_cap) wh = tis_cap;"),
     ("entropy sign", "if (p > 0.0) h -= p * lp;", "if (p > 0.0) h += p * lp;"),
+    ("FP8 entropy sign", "if (pv > 0.0) h -= pv * lpv;", "if (pv > 0.0) h += pv * lpv;"),
+    ("FP8 entropy with the activation scale for the weights",
+     "acc += xd[k] * (oracle_e4m3_decode(wrow[k]) * (double)swrow[k / 128]);",
+     "acc += xd[k] * (oracle_e4m3_decode(wrow[k]) * (double)sxrow[k / 128]);"),
     ("gradient without the one-hot term", "dl[t * V + v] = g[t] * (onehot - exp(z[v] - lz));",
      "dl[t * V + v] = g[t] * (-exp(z[v] - lz));"),
     ("gradient with unnormalised probabilities", "dl[t * V + v] = g[t] * (onehot - exp(z[v] - lz));",
@@ -693,7 +729,9 @@ def test_pins_catch_planted_mistake(tmp_path, monkeypatch, golden_dir, desc, ori
             test_logprob_grad_is_the_derivative, test_logprob_grad_identical_rows_give_zero_dx,
             test_e4m3_codes_match_the_library_format,
             test_e4m3_rounding_matches_the_library_and_saturates, test_block_quantisation_rule,
-            test_logprobs_fp8_equals_the_bf16_oracle_on_representable_inputs]
+            test_logprobs_fp8_equals_the_bf16_oracle_on_representable_inputs,
+            test_entropy_fp8_equals_the_bf16_oracle_on_representable_inputs,
+            test_entropy_fp8_of_a_zero_lm_head_is_log_v]
     failed = 0
     for pin in pins:
         try:
