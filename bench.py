@@ -46,7 +46,7 @@ HOST_LAUNCH = ("bit_consistent_logprob_gb300/csrc/lp_api.cu",
                ["encode_kmajor", "scheduling_band", "x_box_rows", "launch_gemm_variant",
                 "launch_leaf_gemm"])
 FP8_SOURCES = ["bit_consistent_logprob_gb300/csrc/fp8_kernels.cuh"]
-FP8_HOST_LAUNCH = ["launch_fp8_chunk", "quantize_weights"]
+FP8_HOST_LAUNCH = ["quantize_x_chunk", "launch_fp8_gemm", "quantize_weights"]
 
 
 def _function_text(src: str, name: str) -> str:

@@ -145,10 +145,11 @@ static __global__ void __launch_bounds__(256) quant_w_kernel(const uint16_t* W, 
     if (threadIdx.x == 0) sw[static_cast<int64_t>(vb) * nkb + kb] = s;
 }
 
-// The block-scaled leaf GEMM with the fused log-sum-exp epilogue (kModeLse outputs; with kEnt
-// also the entropy partial per tile, as kModeLseEnt).
+// The block-scaled leaf GEMM over the leaves [p.leaf_begin, p.leaf_begin + p.leaf_count),
+// finished as in leaf_gemm_kernel: kModeLse (tile log-sum-exp partials and the sampled logit),
+// kModeLseEnt (also the entropy partial) or kModeNode (the tree node z written to p.out).
 // p.leaf_len is in elements (a multiple of 128); p.sx [T][nkb], p.sw [num_vocab_tiles][nkb].
-template <bool kEnt>
+template <int kMode>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     leaf_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmX,
                          const __grid_constant__ CUtensorMap tmW, const GemmParams p) {
@@ -199,6 +200,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int nkb = p.nkb;                      // 128-K blocks over all of H
     const int bpl = p.leaf_len / kQBlock;       // blocks per leaf
     const int n = p.leaf_count;
+    const int kb0 = p.leaf_begin * bpl;         // first block of the leaf range
+    const int nkb_range = n * bpl;              // blocks per tile in the leaf range
     constexpr uint32_t kFull = 0xffffffffu;
 
     if (warp == 0) {
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int rt, vt;
             tile_coords(tile, p, rt, vt);
             const int row0 = rt * kBM, v0 = vt * kVT;
-            for (int kb = 0; kb < nkb; ++kb) {
+            for (int kb = kb0; kb < kb0 + nkb_range; ++kb) {
                 ok = __all_sync(kFull, mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns));
                 if (!ok) {
                     if (lane == 0) raise_timeout(p, abort_flag);
@@ -250,7 +253,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         bool ready = __all_sync(kFull, mbar_test_wait(&full[0], 0));
         bool acc_ready = true;  // the first use of each buffer finds it free
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-            for (int kb = 0; ok && kb < nkb; ++kb) {
+            for (int kb = 0; ok && kb < nkb_range; ++kb) {
                 if (!acc_ready) {
                     ok = __all_sync(kFull, mbar_wait(&acc_empty[buf], bphase ^ 1u, abort_flag,
                                                      p.timeout_ns));
@@ -308,7 +311,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int v0 = vt * kVT;
             const bool row_ok = row < p.T;
             int ycol = -1;
-            if (row_ok) {
+            if (kMode != kModeNode && row_ok) {
                 const int y = p.ids[row];
                 if (y >= 0 && y < p.V) ycol = y - v0;
             }
@@ -318,7 +321,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int j = 0; ok && j < n; ++j) {
                 // leaf j: P_j = sum over its blocks of (sx * sw) * B_kb
                 for (int b = 0; b < bpl; ++b, ++g) {
-                    const int kb = j * bpl + b;
+                    const int kb = kb0 + j * bpl + b;
                     const uint32_t buf = g % kF8Bufs, use = g / kF8Bufs;
                     const float s = __fmul_rn(row_ok ? sxr[kb] : 0.0f, swr[kb]);
                     if (!warp_wait(&acc_full[buf], use & 1u, p, abort_flag)) {
@@ -393,11 +396,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (!ok) break;
             const int col0 = v0 + h * 64;
             const int nv = p.V - col0;
-            if (row_ok && nv > 0) {
+            if constexpr (kMode == kModeNode) {
+                if (row_ok && nv > 0) {
+                    float* dst = p.out + static_cast<int64_t>(row) * p.ldo + col0;
+                    if (nv >= 64) {
+#pragma unroll
+                        for (int i = 0; i < 64; i += 4)
+                            *reinterpret_cast<float4*>(dst + i) =
+                                make_float4(R[i], R[i + 1], R[i + 2], R[i + 3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i)
+                            if (i < nv) dst[i] = R[i];
+                    }
+                }
+            } else if (row_ok && nv > 0) {
                 float zy = 0.0f;
                 const int yc = ycol - h * 64;
                 const int64_t wi = static_cast<int64_t>(2 * vt + h) * p.ws_ld + row;
-                if constexpr (kEnt) {
+                if constexpr (kMode == kModeLseEnt) {
                     float u;
                     p.ws_ms[wi] = tile_lse64_ent(R, min(nv, kLT), yc, zy, u);
                     p.ws_u[wi] = u;

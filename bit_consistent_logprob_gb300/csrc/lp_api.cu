@@ -402,8 +402,9 @@ int launch_partials_lse(lp_handle* h, const float* parts, int n_parts, int64_t p
 
 // Block-FP8 path for one chunk: quantise the rows (1 x 128 blocks), then the block-scaled leaf
 // GEMM with the fused tile log-sum-exp (one CTA per tile, X box cut to the rows when T < 128).
-int launch_fp8_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids, int rows,
-                     bool entropy, cudaStream_t st) {
+// Quantise one chunk of X (rows <= max_tokens) into the handle's e4m3 activations and their
+// 1 x 128 block scales.
+int quantize_x_chunk(lp_handle* h, const void* X, int64_t ldx, int rows, cudaStream_t st) {
     const int H = h->cfg.H;
     const int nkb = H / lp::kQBlock;
     const int64_t warps = static_cast<int64_t>(rows) * nkb;
@@ -411,12 +412,22 @@ int launch_fp8_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* id
         static_cast<const uint16_t*>(X), ldx, rows, H, h->xq, H, h->sx);
     LP_CUDA(cudaGetLastError(), "quant_x_kernel launch");
     ++h->last_launches;
+    return LP_OK;
+}
+
+// The block-FP8 leaf GEMM over the leaves [leaf_begin, leaf_begin + leaf_count) of the chunk
+// quantize_x_chunk left in the handle: tile partials (kModeLse, kModeLseEnt) or the tree node
+// written to out (kModeNode).
+template <int kMode>
+int launch_fp8_gemm(lp_handle* h, int rows, int leaf_begin, int leaf_count, const int32_t* ids,
+                    float* out, int64_t ldo, cudaStream_t st) {
+    const int H = h->cfg.H;
     lp::GemmParams p{};
     p.T = rows;
     p.V = h->cfg.V;
     p.leaf_len = h->leaf_len;
-    p.leaf_begin = 0;
-    p.leaf_count = h->cfg.n_leaves;
+    p.leaf_begin = leaf_begin;
+    p.leaf_count = leaf_count;
     p.num_row_tiles = static_cast<int32_t>(ceil_div(rows, lp::kBM));
     p.num_vocab_tiles = h->num_vocab_tiles;
     p.num_lse_tiles = h->num_lse_tiles;
@@ -427,9 +438,11 @@ int launch_fp8_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* id
     p.ws_ld = h->cfg.max_tokens;
     p.zy = h->zy;
     p.ws_u = h->ws_u;
+    p.out = out;
+    p.ldo = ldo;
     p.sx = h->sx;
     p.sw = h->sw;
-    p.nkb = nkb;
+    p.nkb = H / lp::kQBlock;
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
     CUtensorMap tmX;
@@ -441,12 +454,8 @@ int launch_fp8_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* id
     const int grid = static_cast<int>(tiles < h->num_sms ? tiles : h->num_sms);
     const bool prof = h->profiling && h->prof_used < kProfPairs;
     if (prof) LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used], st), "profile event");
-    if (entropy)
-        lp::leaf_gemm_fp8_kernel<true><<<grid, lp::kGemmThreads, lp::fp8_smem_bytes(), st>>>(
-            tmX, h->tmWq, p);
-    else
-        lp::leaf_gemm_fp8_kernel<false><<<grid, lp::kGemmThreads, lp::fp8_smem_bytes(), st>>>(
-            tmX, h->tmWq, p);
+    lp::leaf_gemm_fp8_kernel<kMode><<<grid, lp::kGemmThreads, lp::fp8_smem_bytes(), st>>>(
+        tmX, h->tmWq, p);
     LP_CUDA(cudaGetLastError(), "leaf_gemm_fp8_kernel launch");
     if (prof) {
         LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used + 1], st), "profile event");
@@ -471,15 +480,16 @@ int logprobs_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids,
                    float* out_logp, float* out_logZ, float* out_entropy, cudaStream_t st) {
     int rc;
     const int s = h->cfg.tp_slices;
-    if (h->fp8) {
-        rc = launch_fp8_chunk(h, X, ldx, ids, rows, out_entropy != nullptr, st);
-        if (rc != LP_OK) return rc;
-    } else if (s == 1) {
-        rc = out_entropy
-                 ? launch_leaf_gemm<lp::kModeLseEnt>(h, X, ldx, rows, 0, h->cfg.n_leaves, ids,
-                                                     nullptr, 0, st)
-                 : launch_leaf_gemm<lp::kModeLse>(h, X, ldx, rows, 0, h->cfg.n_leaves, ids,
-                                                  nullptr, 0, st);
+    const int n = h->cfg.n_leaves;
+    if (h->fp8 && (rc = quantize_x_chunk(h, X, ldx, rows, st)) != LP_OK) return rc;
+    if (s == 1) {
+        if (h->fp8)
+            rc = out_entropy ? launch_fp8_gemm<lp::kModeLseEnt>(h, rows, 0, n, ids, nullptr, 0, st)
+                             : launch_fp8_gemm<lp::kModeLse>(h, rows, 0, n, ids, nullptr, 0, st);
+        else
+            rc = out_entropy
+                     ? launch_leaf_gemm<lp::kModeLseEnt>(h, X, ldx, rows, 0, n, ids, nullptr, 0, st)
+                     : launch_leaf_gemm<lp::kModeLse>(h, X, ldx, rows, 0, n, ids, nullptr, 0, st);
         if (rc != LP_OK) return rc;
     } else {
         // Slice r owns leaves [r*N/s, (r+1)*N/s) and produces that node of the leaf tree;
@@ -488,8 +498,11 @@ int logprobs_chunk(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids,
         const int per = h->cfg.n_leaves / s;
         const int64_t part_stride = h->chunk_rows * h->tp_ldp;
         for (int r = 0; r < s; ++r) {
-            rc = launch_leaf_gemm<lp::kModeNode>(h, X, ldx, rows, r * per, per, nullptr,
-                                         h->tp_parts + r * part_stride, h->tp_ldp, st);
+            float* part = h->tp_parts + r * part_stride;
+            rc = h->fp8 ? launch_fp8_gemm<lp::kModeNode>(h, rows, r * per, per, nullptr, part,
+                                                         h->tp_ldp, st)
+                        : launch_leaf_gemm<lp::kModeNode>(h, X, ldx, rows, r * per, per, nullptr,
+                                                          part, h->tp_ldp, st);
             if (rc != LP_OK) return rc;
         }
         for (int r = 0; r < s; ++r) {
@@ -586,8 +599,6 @@ int init_impl(const lp_config* cfg, const void* W, void* stream, lp_handle** out
         return fail(LP_ERR_UNSUPPORTED,
                     "block FP8 needs H (%d) to be a multiple of 128 * n_leaves (%d)", cfg->H,
                     lp::kQBlock * cfg->n_leaves);
-    if (fp8 && cfg->tp_slices != 1)
-        return fail(LP_ERR_UNSUPPORTED, "block FP8 runs the fused path only (tp_slices = 1)");
     if (W == nullptr) return fail(LP_ERR_INVALID_ARG, "W is NULL");
     if (!aligned16(W)) return fail(LP_ERR_INVALID_ARG, "W must be 16-byte aligned");
 
@@ -716,10 +727,13 @@ int init_impl(const lp_config* cfg, const void* W, void* stream, lp_handle** out
             (rc = alloc(reinterpret_cast<void**>(&h->sx), sizeof(float) * static_cast<size_t>(mt) * nkb,
                         "sx")))
             return cleanup(rc);
-        if ((e = cudaFuncSetAttribute(lp::leaf_gemm_fp8_kernel<false>,
+        if ((e = cudaFuncSetAttribute(lp::leaf_gemm_fp8_kernel<lp::kModeLse>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       lp::fp8_smem_bytes())) != cudaSuccess ||
-            (e = cudaFuncSetAttribute(lp::leaf_gemm_fp8_kernel<true>,
+            (e = cudaFuncSetAttribute(lp::leaf_gemm_fp8_kernel<lp::kModeLseEnt>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      lp::fp8_smem_bytes())) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(lp::leaf_gemm_fp8_kernel<lp::kModeNode>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       lp::fp8_smem_bytes())) != cudaSuccess)
             return cleanup(cuda_fail(e, "cudaFuncSetAttribute(leaf_gemm_fp8_kernel)"));
@@ -999,7 +1013,6 @@ int lp_logprobs_host(lp_handle* h, const void* X, int64_t ldx, const int32_t* id
 int lp_logits_partial(lp_handle* h, const void* X, int64_t ldx, int64_t T, int32_t leaf_begin,
                       int32_t leaf_count, float* out, int64_t ldo, void* stream) {
     if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
-    if (h->fp8) return fail(LP_ERR_UNSUPPORTED, "tree nodes are not exported by block-FP8 handles");
     int rc = check_x(h, X, ldx, T);
     if (rc != LP_OK) return rc;
     if (!is_pow2(leaf_count) || leaf_begin < 0 || leaf_begin % leaf_count != 0 ||
@@ -1017,8 +1030,15 @@ int lp_logits_partial(lp_handle* h, const void* X, int64_t ldx, int64_t T, int32
     const uint8_t* xb = static_cast<const uint8_t*>(X);
     for (int64_t r0 = 0; r0 < T; r0 += chunk) {
         const int rows = static_cast<int>(T - r0 < chunk ? T - r0 : chunk);
-        rc = launch_leaf_gemm<lp::kModeNode>(h, xb + r0 * ldx * 2, ldx, rows, leaf_begin, leaf_count,
-                                     nullptr, out + r0 * ldo, ldo, st);
+        if (h->fp8) {
+            rc = quantize_x_chunk(h, xb + r0 * ldx * 2, ldx, rows, st);
+            if (rc == LP_OK)
+                rc = launch_fp8_gemm<lp::kModeNode>(h, rows, leaf_begin, leaf_count, nullptr,
+                                                    out + r0 * ldo, ldo, st);
+        } else {
+            rc = launch_leaf_gemm<lp::kModeNode>(h, xb + r0 * ldx * 2, ldx, rows, leaf_begin,
+                                                 leaf_count, nullptr, out + r0 * ldo, ldo, st);
+        }
         if (rc != LP_OK) return rc;
     }
     return LP_OK;
@@ -1028,7 +1048,6 @@ int lp_logprobs_from_partials(lp_handle* h, const float* partials, int32_t n_par
                               int64_t part_stride, int64_t ldp, const int32_t* ids, int64_t T,
                               float* out_logp, float* out_logZ, void* stream) {
     if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
-    if (h->fp8) return fail(LP_ERR_UNSUPPORTED, "block-FP8 handles run the fused path only");
     if (!(n_parts == 1 || n_parts == 2 || n_parts == 4 || n_parts == 8) ||
         h->cfg.n_leaves % n_parts != 0)
         return fail(LP_ERR_UNSUPPORTED, "n_parts must be 1, 2, 4 or 8 and divide n_leaves");

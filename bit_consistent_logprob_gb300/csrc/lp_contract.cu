@@ -146,8 +146,7 @@ std::string semantic_json(const lp_config* c) {
 std::string policy_json(const lp_config* c, int precision) {
     const bool fp8 = precision == LP_PRECISION_FP8_BLOCK;
     std::string tp = "[1";
-    if (!fp8)
-        for (int s = 2; s <= c->n_leaves; s *= 2) tp += "," + std::to_string(s);
+    for (int s = 2; s <= c->n_leaves; s *= 2) tp += "," + std::to_string(s);
     tp += "]";
     const char* lm_bf16 =
         "\"impl\":{\"id\":\"leaf_gemm_tcgen05\",\"version\":%d,\"arch\":\"sm_103a\"},"
@@ -204,10 +203,8 @@ int check_args(const lp_config* cfg, int precision) {
     if (rc != LP_OK) return rc;
     if (precision != LP_PRECISION_BF16 && precision != LP_PRECISION_FP8_BLOCK)
         return lp_internal_fail(LP_ERR_INVALID_ARG, "unknown precision %d", precision);
-    if (precision == LP_PRECISION_FP8_BLOCK &&
-        (cfg->H % (128 * cfg->n_leaves) != 0 || cfg->tp_slices != 1))
-        return lp_internal_fail(LP_ERR_UNSUPPORTED,
-                                "block FP8 needs H %% (128 * n_leaves) == 0 and tp_slices == 1");
+    if (precision == LP_PRECISION_FP8_BLOCK && cfg->H % (128 * cfg->n_leaves) != 0)
+        return lp_internal_fail(LP_ERR_UNSUPPORTED, "block FP8 needs H %% (128 * n_leaves) == 0");
     return LP_OK;
 }
 

@@ -222,13 +222,15 @@ LP_API int lp_importance_weights_host(lp_handle* h, const float* logp_pi, const 
  * per block); z = the same fixed pairwise leaf tree, and the same log-sum-exp and combine.
  *
  * lp_init_fp8 takes the same arguments as lp_init (W: the bf16 master lm_head, referenced) and
- * additionally requires H % (128 * n_leaves) == 0 and tp_slices == 1.  It quantises W into
+ * additionally requires H % (128 * n_leaves) == 0.  It quantises W into
  * a handle-owned e4m3 copy with its scales (synchronises `stream`).  lp_logprobs and
  * lp_logprobs_host on such a handle quantise each chunk of X (1 x 128 blocks) and run the
  * block-scaled GEMM; results obey the same invariance (batch, position, phase, chunking).
  * lp_logprobs_entropy also runs on such a handle (the same tile entropy partial and merge;
- * logp and logZ keep the bits of lp_logprobs).  lp_logits_partial, lp_logprobs_from_partials
- * and lp_logprobs_backward return LP_ERR_UNSUPPORTED on a block-FP8 handle.
+ * logp and logZ keep the bits of lp_logprobs), and so does the emulated tensor-parallel split
+ * (tp_slices > 1: each slice's node of the leaf tree from the block-scaled leaves, the same
+ * upper levels) with lp_logits_partial and lp_logprobs_from_partials.  lp_logprobs_backward
+ * returns LP_ERR_UNSUPPORTED on a block-FP8 handle.
  * lp_fp8_requantize re-quantises W after an in-place update (asynchronous on `stream`).
  * lp_fp8_weights exposes the handle's e4m3 weights [V][H] and scales [ceil(V/128)][H/128]
  * (device pointers owned by the handle) for verification.

@@ -64,7 +64,8 @@ def test_block_fp8_policy_differs_and_is_canonical():
     lm = doc["numerical_policy"]["composition"][0]
     assert lm["constants"]["input_dtype"] == "e4m3"
     assert lm["constants"]["quantization"]["weight_block"] == "128x128"
-    assert doc["numerical_policy"]["claims"]["topology"]["tp_slices"] == [1]
+    assert doc["numerical_policy"]["claims"]["topology"]["tp_slices"] == [1, 2, 4, 8]
+    contract.contract(precision=contract.FP8_BLOCK, tp_slices=4, **kw)  # a proven split
     pol = contract.NUMERICAL_POLICY
     assert contract.digest(pol, precision=contract.FP8_BLOCK, **kw) != contract.digest(pol, **kw)
     assert (contract.digest(contract.SEMANTIC, precision=contract.FP8_BLOCK, **kw)

@@ -9,7 +9,9 @@ RL training faster", section 4.1).  Checks:
 * the same invariance as the bf16 path (row alone or in a batch, decode versus prefill,
   chunking, graph replay), and in-place weight updates picked up by re-quantisation;
 * the row entropy on FP8 handles within 2e-3 of the oracle's entropy of the dequantised
-  operands, logp and logZ bit-equal to the plain call, the same bits for a row alone.
+  operands, logp and logZ bit-equal to the plain call, the same bits for a row alone;
+* the exported tree node equals the oracle's fp32 tree over the exported leaves, and the
+  emulated TP split (IsoExec summary, "Parallelism-invariant kernels") gives the fused bits.
 """
 import numpy as np
 import pytest
@@ -83,6 +85,38 @@ def test_fp8_entropy_matches_oracle_and_keeps_logp_bits(dev, T, H, V, N):
     assert np.all(got >= 0) and np.all(got <= np.log(V) + 1e-4)
 
 
+def test_fp8_leaf_tree_partials_and_tp_split(dev):
+    # The node of all leaves equals the oracle's fp32 pairwise tree over the exported
+    # (block-promoted) leaves; finishing from that node, or from the nodes of an emulated TP
+    # split, gives the fused call's bits, entropy included.
+    T, H, V, N = 300, 1024, 4001, 8
+    X = inputs.hidden_states(T, H, seed=31, device=dev)
+    W = inputs.lm_head(V, H, seed=31, device=dev)
+    ids = inputs.uniform_ids(T, V, seed=31, device=dev)
+    with Engine(W, n_leaves=N, max_tokens=T, fp8=True) as eng:
+        base, baseZ = eng.logprobs(X, ids, return_logZ=True)
+        ent = eng.logprobs_entropy(X, ids)[2].clone()
+        parts = torch.stack([eng.logits_partial(X, j, 1).cpu() for j in range(N)], dim=-1)
+        full = eng.logits_partial(X, 0, N)
+        half0 = eng.logits_partial(X, 0, N // 2).cpu()
+        lp_p, lz_p = eng.logprobs_from_partials(full.unsqueeze(0), ids, return_logZ=True)
+        eng.check()
+    assert_bit_equal(full.cpu(), torch.from_numpy(oracle.tree_fp32(parts.numpy())),
+                     "FP8 full tree node vs oracle fp32 tree")
+    assert_bit_equal(half0, torch.from_numpy(oracle.tree_fp32(parts[..., : N // 2].numpy())),
+                     "FP8 left subtree vs oracle fp32 tree")
+    assert_bit_equal(lp_p, base, "FP8 logp from the exported node")
+    assert_bit_equal(lz_p, baseZ, "FP8 logZ from the exported node")
+    for s in (2, 4, 8):
+        with Engine(W, n_leaves=N, tp_slices=s, max_tokens=T, fp8=True) as e:
+            lp, lz = e.logprobs(X, ids, return_logZ=True)
+            ent_s = e.logprobs_entropy(X, ids)[2]
+            e.check()
+        assert_bit_equal(lp, base, f"FP8 tp_slices={s} logp")
+        assert_bit_equal(lz, baseZ, f"FP8 tp_slices={s} logZ")
+        assert_bit_equal(ent_s, ent, f"FP8 tp_slices={s} entropy")
+
+
 def test_fp8_invariance(dev):
     T, H, V, N = 2100, 1024, 32001, 8
     X = inputs.hidden_states(T, H, seed=5, device=dev)
@@ -135,8 +169,9 @@ def test_fp8_requantize_after_inplace_update_and_unsupported_calls(dev):
         after = eng.logprobs(X, ids)
         assert_bit_equal(after, fresh.logprobs(X, ids), "re-quantised vs fresh")
         assert not torch.equal(before, after)
-        with pytest.raises(LpError):
-            eng.logits_partial(X, 0, 2)
+        _, lz = eng.logprobs(X, ids, return_logZ=True)
+        with pytest.raises(LpError):  # the backward is not built for block-FP8 handles
+            eng.logprobs_backward(X, ids, lz, torch.ones(T, device=dev))
         eng.check()
         fresh.check()
     with pytest.raises(LpError):

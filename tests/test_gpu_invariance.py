@@ -171,9 +171,9 @@ def test_run_to_run_and_reinit(data, eng):
         e2.check()
 
 
-def test_cuda_graph_matches_eager(data, dev):
+@pytest.mark.parametrize("T", [1000, 200, 7])  # X-sharing pairs, W-sharing pairs, one CTA per tile
+def test_cuda_graph_matches_eager(data, dev, T):
     X, W, ids = data
-    T = 1000
     with Engine(W, n_leaves=N, max_tokens=T) as e:
         eager = e.logprobs(X[:T], ids[:T])
         out = torch.empty(T, dtype=torch.float32, device=dev)
@@ -192,9 +192,9 @@ def test_cuda_graph_matches_eager(data, dev):
     assert_bit_equal(out, eager, "graph replay vs eager")
 
 
-def test_concurrent_stream_occupying_sms(data, dev, eng):
+@pytest.mark.parametrize("T", [2000, 256])
+def test_concurrent_stream_occupying_sms(data, dev, eng, T):
     X, _, ids = data
-    T = 2000
     ref = eng.logprobs(X[:T], ids[:T])
     side = torch.cuda.Stream()
     a = torch.randn(8192, 8192, device=dev, dtype=torch.bfloat16)
