@@ -65,8 +65,9 @@ struct GemmParams {
     float* ws_u;              // [num_lse_tiles][ws_ld] entropy partial per tile (kModeLseEnt)
     const float* logZ;        // [T] per-row logZ of the forward pass (kModeGrad)
     const float* gout;        // [T] dLoss/dlogp per row (kModeGrad)
-    uint16_t* dl;             // [T][ldd] bf16 gradient with respect to the logits (kModeGrad;
-                              // the kernel writes it through the tmD tensor map)
+    uint16_t* dl;             // [T][ldd] bf16 gradient with respect to the logits (kModeGrad);
+                              // kept for the host's record: the kernel writes dl only through
+                              // the tmD tensor map and reads neither dl nor ldd
     int64_t ldd;
     const float* sx;          // [T][nkb] activation block scales (block-FP8 kernel)
     const float* sw;          // [num_vocab_tiles][nkb] weight block scales (block-FP8 kernel)
