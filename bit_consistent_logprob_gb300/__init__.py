@@ -16,14 +16,16 @@ from ._native import LpError, load as load_library, library_path  # noqa: F401
 
 __all__ = ["Engine", "LpError", "load_library", "library_path", "LP_PHASE_AUTO",
            "LP_PHASE_PREFILL", "LP_PHASE_DECODE", "logprobs_with_grad",
-           "visible_with_graph_gradient"]
+           "visible_with_graph_gradient", "importance_weights_data_parallel",
+           "gather_block_partials", "IS_BLOCK"]
 
 
 def __getattr__(name):
     # Engine imports torch; resolve it lazily so the input generators and the build
     # helper stay importable without touching the GPU stack.
     if name in ("Engine", "LP_PHASE_AUTO", "LP_PHASE_PREFILL", "LP_PHASE_DECODE",
-                "logprobs_with_grad", "visible_with_graph_gradient"):
+                "logprobs_with_grad", "visible_with_graph_gradient",
+                "importance_weights_data_parallel", "gather_block_partials", "IS_BLOCK"):
         from . import engine
 
         return getattr(engine, name)

@@ -1094,6 +1094,50 @@ int lp_importance_weights(lp_handle* h, const float* logp_pi, const float* logp_
     return LP_OK;
 }
 
+static_assert(sizeof(long long) == sizeof(int64_t), "block counts cross the ABI as int64_t");
+
+int lp_importance_weights_partials(lp_handle* h, const float* logp_pi, const float* logp_mu,
+                                   const uint8_t* mask, int64_t T, float* out_w,
+                                   double* out_blk_sum, int64_t* out_blk_cnt, void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    if (T < 0 || T > kMaxIsTokens) return fail(LP_ERR_INVALID_ARG, "T must be in [0, 2^31)");
+    h->last_launches = 0;
+    if (T == 0) return LP_OK;
+    if (logp_pi == nullptr || logp_mu == nullptr || out_w == nullptr || out_blk_sum == nullptr ||
+        out_blk_cnt == nullptr)
+        return fail(LP_ERR_INVALID_ARG,
+                    "logp_pi, logp_mu, out_w, out_blk_sum and out_blk_cnt must not be NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    h->last_stream = st;
+    const int64_t nblk = ceil_div(T, lp::kIsBlock);
+    // the same block kernel as lp_importance_weights, its partials in the caller's arrays
+    lp::IsParams p{logp_pi, logp_mu, mask, T, out_w, out_blk_sum,
+                   reinterpret_cast<long long*>(out_blk_cnt)};
+    lp::is_block_kernel<<<static_cast<unsigned>(nblk), lp::kIsThreads, 0, st>>>(p);
+    LP_CUDA(cudaGetLastError(), "is_block_kernel launch");
+    ++h->last_launches;
+    return LP_OK;
+}
+
+int lp_d3_from_partials(lp_handle* h, const double* blk_sum, const int64_t* blk_cnt,
+                        int64_t num_blocks, double* out_d3, int64_t* out_nvalid, void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    if (num_blocks < 0 || num_blocks > ceil_div(kMaxIsTokens, lp::kIsBlock))
+        return fail(LP_ERR_INVALID_ARG, "num_blocks must be in [0, 2^21]");
+    if (out_d3 == nullptr) return fail(LP_ERR_INVALID_ARG, "out_d3 must not be NULL");
+    if (num_blocks > 0 && (blk_sum == nullptr || blk_cnt == nullptr))
+        return fail(LP_ERR_INVALID_ARG, "blk_sum and blk_cnt must not be NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    h->last_stream = st;
+    h->last_launches = 0;
+    // the fixed fp64 tree over the gathered blocks, as in lp_importance_weights
+    lp::is_final_kernel<<<1, 1024, 0, st>>>(blk_sum, reinterpret_cast<const long long*>(blk_cnt),
+                                            static_cast<int>(num_blocks), out_d3, out_nvalid);
+    LP_CUDA(cudaGetLastError(), "is_final_kernel launch");
+    ++h->last_launches;
+    return LP_OK;
+}
+
 int lp_acceptance_stats(lp_handle* h, const float* logp_a, const float* logp_b,
                         const uint8_t* mask, int64_t T, double* out_stats, void* stream) {
     if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");

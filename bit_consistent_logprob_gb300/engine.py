@@ -9,6 +9,8 @@ import torch
 from . import _native
 from ._native import LP_PHASE_AUTO, LP_PHASE_DECODE, LP_PHASE_PREFILL, LpConfig, LpError
 
+IS_BLOCK = 1024  # tokens per D3 block (LP_IS_BLOCK in include/lp.h)
+
 __all__ = ["Engine", "LpError", "LP_PHASE_AUTO", "LP_PHASE_PREFILL", "LP_PHASE_DECODE"]
 
 
@@ -253,6 +255,44 @@ class Engine:
             _ptr(out_nvalid), _stream_ptr(stream)))
         return out_w, out_d3, out_nvalid
 
+    def importance_weights_partials(self, logp_pi: torch.Tensor, logp_mu: torch.Tensor,
+                                    mask: torch.Tensor = None, stream=None):
+        """(w fp32 [T], block sums fp64 [nb], block counts int64 [nb]), nb = ceil(T / 1024):
+        this rank's share of a data-parallel D3 (see ``d3_from_partials``)."""
+        _require(logp_pi, "logp_pi", torch.float32, 1)
+        _require(logp_mu, "logp_mu", torch.float32, 1)
+        T = int(logp_pi.shape[0])
+        if logp_mu.shape[0] != T:
+            raise ValueError("logp_pi and logp_mu must have the same length")
+        if mask is not None:
+            _require(mask, "mask", torch.uint8, 1)
+            if mask.shape[0] != T:
+                raise ValueError("mask must have length T")
+        dev = logp_pi.device
+        nb = (T + IS_BLOCK - 1) // IS_BLOCK
+        w = torch.empty(T, dtype=torch.float32, device=dev)
+        blk_sum = torch.empty(nb, dtype=torch.float64, device=dev)
+        blk_cnt = torch.empty(nb, dtype=torch.int64, device=dev)
+        _native.check(self._lib.lp_importance_weights_partials(
+            self._h, _ptr(logp_pi), _ptr(logp_mu), _ptr(mask), T, _ptr(w), _ptr(blk_sum),
+            _ptr(blk_cnt), _stream_ptr(stream)))
+        return w, blk_sum, blk_cnt
+
+    def d3_from_partials(self, blk_sum: torch.Tensor, blk_cnt: torch.Tensor, stream=None):
+        """(D3 fp64 [1], n_valid int64 [1]) from gathered 1024-token block partials, in
+        stream order, by the same fixed tree as ``importance_weights``."""
+        _require(blk_sum, "blk_sum", torch.float64, 1)
+        _require(blk_cnt, "blk_cnt", torch.int64, 1)
+        nb = int(blk_sum.shape[0])
+        if blk_cnt.shape[0] != nb or not (blk_sum.is_contiguous() and blk_cnt.is_contiguous()):
+            raise ValueError("blk_sum and blk_cnt must be contiguous and of the same length")
+        out_d3 = torch.empty(1, dtype=torch.float64, device=blk_sum.device)
+        out_nvalid = torch.empty(1, dtype=torch.int64, device=blk_sum.device)
+        _native.check(self._lib.lp_d3_from_partials(
+            self._h, _ptr(blk_sum), _ptr(blk_cnt), nb, _ptr(out_d3), _ptr(out_nvalid),
+            _stream_ptr(stream)))
+        return out_d3, out_nvalid
+
     def acceptance_stats(self, logp_a: torch.Tensor, logp_b: torch.Tensor,
                          mask: torch.Tensor = None, out: torch.Tensor = None, stream=None):
         """fp64 [5] on the device: max, mean and std of |a - b|, k3, n_valid (no sync)."""
@@ -431,3 +471,55 @@ def visible_with_graph_gradient(visible: torch.Tensor, graph: torch.Tensor) -> t
     if visible.shape != graph.shape:
         raise ValueError("visible and graph must have the same shape")
     return visible.detach() + (graph - graph.detach())
+
+
+def gather_block_partials(blk_sum: torch.Tensor, blk_cnt: torch.Tensor, group=None):
+    """All-gather every rank's D3 block partials and concatenate them in rank order.
+
+    The collective only moves the fp64 sums and int64 counts (padded to the longest rank's
+    block count, then trimmed); it never adds them, so the gathered blocks are bit-identical
+    to the ones one rank would have computed for the whole stream.
+    """
+    import torch.distributed as dist
+
+    world = dist.get_world_size(group)
+    n = torch.tensor([blk_sum.shape[0]], dtype=torch.int64, device=blk_sum.device)
+    sizes = [torch.zeros_like(n) for _ in range(world)]
+    dist.all_gather(sizes, n, group=group)
+    sizes = [int(x.item()) for x in sizes]
+    m = max(sizes)
+
+    def padded(t):
+        out = torch.zeros(m, dtype=t.dtype, device=t.device)
+        out[: t.shape[0]] = t
+        return out
+
+    sums = [torch.empty(m, dtype=blk_sum.dtype, device=blk_sum.device) for _ in range(world)]
+    cnts = [torch.empty(m, dtype=blk_cnt.dtype, device=blk_cnt.device) for _ in range(world)]
+    dist.all_gather(sums, padded(blk_sum), group=group)
+    dist.all_gather(cnts, padded(blk_cnt), group=group)
+    return (torch.cat([x[:k] for x, k in zip(sums, sizes)]),
+            torch.cat([x[:k] for x, k in zip(cnts, sizes)]))
+
+
+def importance_weights_data_parallel(engine: "Engine", logp_pi: torch.Tensor,
+                                     logp_mu: torch.Tensor, mask: torch.Tensor = None,
+                                     group=None):
+    """(w [T], D3 [1], n_valid [1]) for a token stream split across data-parallel ranks.
+
+    Each rank passes its own contiguous range of the stream, ranges in rank order and every
+    range but the last a multiple of 1024 tokens.  w is this rank's; D3 and n_valid are the
+    whole stream's, with the bits of one ``importance_weights`` call over it (the block
+    partials are gathered, then every rank runs the same fixed tree).
+    """
+    import torch.distributed as dist
+
+    T = int(logp_pi.shape[0])
+    rank, world = dist.get_rank(group), dist.get_world_size(group)
+    if rank < world - 1 and T % IS_BLOCK != 0:
+        raise ValueError(f"rank {rank} holds {T} tokens: every rank but the last must hold a "
+                         f"multiple of {IS_BLOCK}")
+    w, blk_sum, blk_cnt = engine.importance_weights_partials(logp_pi, logp_mu, mask)
+    all_sum, all_cnt = gather_block_partials(blk_sum, blk_cnt, group)
+    d3, n_valid = engine.d3_from_partials(all_sum, all_cnt)
+    return w, d3, n_valid

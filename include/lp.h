@@ -202,6 +202,32 @@ LP_API int lp_importance_weights(lp_handle* h, const float* logp_pi, const float
                           int64_t* out_nvalid, void* stream);
 
 /*
+ * D3 over a token stream split across data-parallel ranks, with one exchange step.  D3 is a
+ * per-update mean over all valid tokens (REINFORCE Zero summary, section 3), so ranks must
+ * combine their tokens; the pages let the collective only move partials, never reduce them
+ * (IsoExec summary, "Parallelism-invariant kernels": NCCL transports partials).
+ *   lp_importance_weights_partials: out_w as in lp_importance_weights, and per 1024-token
+ *     block (LP_IS_BLOCK) of this rank's range the fp64 sum of the D3 term over its valid
+ *     tokens (out_blk_sum) and their count (out_blk_cnt); both device arrays of
+ *     ceil(T / 1024) entries, caller-owned.
+ *   lp_d3_from_partials: D3 and n_valid from num_blocks gathered blocks (device arrays, in
+ *     stream order; num_blocks <= 2^21), by the same fixed fp64 tree over blocks as
+ *     lp_importance_weights.
+ * When every rank but the last holds a multiple of 1024 tokens and the partials are gathered
+ * in rank order (an all-gather: data movement only), D3 and n_valid are bit-identical to one
+ * lp_importance_weights call over the whole stream, for any number of ranks.  Both calls are
+ * asynchronous on `stream`.
+ */
+#define LP_IS_BLOCK 1024
+LP_API int lp_importance_weights_partials(lp_handle* h, const float* logp_pi,
+                                          const float* logp_mu, const uint8_t* mask, int64_t T,
+                                          float* out_w, double* out_blk_sum, int64_t* out_blk_cnt,
+                                          void* stream);
+LP_API int lp_d3_from_partials(lp_handle* h, const double* blk_sum, const int64_t* blk_cnt,
+                               int64_t num_blocks, double* out_d3, int64_t* out_nvalid,
+                               void* stream);
+
+/*
  * Same as lp_importance_weights with HOST buffers (logp_pi, logp_mu, mask, out_w in
  * host memory; out_d3 and out_nvalid are host scalars).  Tokens are staged through
  * the device workspace in chunks of whole 1024-token blocks, so D3 is the same tree

@@ -7,6 +7,10 @@
   all-gather, no reducing collective) before the upper levels of the same tree are applied
   (IsoExec blog summary, "Parallelism-invariant kernels").  The result must equal the
   single-process tree bit for bit, which is what the GPU's emulated split relies on.
+* D3 over a token stream split across ranks: each rank's fp64 partials over 1024-token
+  blocks are all-gathered in rank order (moved, never added), so every rank holds the whole
+  stream's blocks and the same fixed tree gives one D3 for any number of ranks (REINFORCE
+  Zero summary, section 3: a per-update mean over tokens).
 """
 import os
 import socket
@@ -90,3 +94,74 @@ def test_tp_leaf_split_over_ranks_is_bit_exact(world, n_leaves):
     mp.start_processes(_tp_worker, args=(world, _free_port(), n_leaves, 7 + world, out),
                        nprocs=world, start_method="spawn")
     assert out["split"] == out["whole"]
+
+
+def _stream_blocks(T, seed):
+    """The D3 terms of one synthetic token stream (oracle) and its fp64 sums and valid counts
+    per 1024-token block, by plain numpy."""
+    rng = np.random.default_rng(seed)
+    lp = np.log(rng.uniform(1e-6, 1.0, T)).astype(np.float32)
+    lm = (lp + rng.normal(0.0, 0.05, T)).astype(np.float32)
+    mask = (rng.uniform(size=T) < 0.9).astype(np.uint8)
+    _, term, _, _ = oracle.importance_weights(lp, lm, mask)
+    term = np.where(mask != 0, term, 0.0)
+    nb = (T + 1023) // 1024
+    sums = np.array([term[b * 1024:(b + 1) * 1024].sum() for b in range(nb)])
+    cnts = np.array([int(mask[b * 1024:(b + 1) * 1024].sum()) for b in range(nb)], dtype=np.int64)
+    return sums, cnts
+
+
+def _d3_worker(rank, world, port, bounds, seed, out):
+    import sys
+
+    sys.path.insert(0, ROOT)
+    from bit_consistent_logprob_gb300 import gather_block_partials
+
+    _init(rank, world, port)
+    sums, cnts = _stream_blocks(bounds[-1], seed)
+    b0, b1 = bounds[rank] // 1024, (bounds[rank + 1] + 1023) // 1024   # this rank's blocks
+    s_all, c_all = gather_block_partials(torch.from_numpy(sums[b0:b1].copy()),
+                                         torch.from_numpy(cnts[b0:b1].copy()))
+    out[rank] = (s_all.numpy().view(np.int64).tolist(), c_all.numpy().tolist())
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("bounds", [[0, 3072, 7000], [0, 1024, 9216, 9300]])
+def test_d3_block_partials_gather_in_rank_order(bounds):
+    # Ranks hold consecutive token ranges, all but the last a multiple of 1024 tokens, with
+    # different block counts; every rank must end with the whole stream's blocks, bit for bit,
+    # so the same fixed tree over them gives one D3 for any number of ranks.
+    world = len(bounds) - 1
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    mp.start_processes(_d3_worker, args=(world, _free_port(), bounds, 17, out), nprocs=world,
+                       start_method="spawn")
+    sums, cnts = _stream_blocks(bounds[-1], 17)
+    for r in range(world):
+        assert out[r][0] == sums.view(np.int64).tolist(), f"rank {r} sums"
+        assert out[r][1] == cnts.tolist(), f"rank {r} counts"
+
+
+def _misaligned_worker(rank, world, port, out):
+    import sys
+
+    sys.path.insert(0, ROOT)
+    from bit_consistent_logprob_gb300 import importance_weights_data_parallel
+
+    _init(rank, world, port)
+    if rank == 0:  # not the last rank, and 1000 tokens is not a multiple of 1024
+        x = torch.zeros(1000)
+        try:
+            importance_weights_data_parallel(None, x, x)   # rejected before any collective
+            out[rank] = "accepted"
+        except ValueError:
+            out[rank] = "rejected"
+    dist.destroy_process_group()
+
+
+def test_d3_data_parallel_rejects_a_misaligned_rank():
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    mp.start_processes(_misaligned_worker, args=(2, _free_port(), out), nprocs=2,
+                       start_method="spawn")
+    assert out[0] == "rejected"
