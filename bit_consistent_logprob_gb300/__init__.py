@@ -17,7 +17,7 @@ from ._native import LpError, load as load_library, library_path  # noqa: F401
 __all__ = ["Engine", "LpError", "load_library", "library_path", "LP_PHASE_AUTO",
            "LP_PHASE_PREFILL", "LP_PHASE_DECODE", "logprobs_with_grad",
            "visible_with_graph_gradient", "importance_weights_data_parallel",
-           "gather_block_partials", "IS_BLOCK"]
+           "gather_block_partials", "IS_BLOCK", "acceptance_stats_data_parallel"]
 
 
 def __getattr__(name):
@@ -25,7 +25,8 @@ def __getattr__(name):
     # helper stay importable without touching the GPU stack.
     if name in ("Engine", "LP_PHASE_AUTO", "LP_PHASE_PREFILL", "LP_PHASE_DECODE",
                 "logprobs_with_grad", "visible_with_graph_gradient",
-                "importance_weights_data_parallel", "gather_block_partials", "IS_BLOCK"):
+                "importance_weights_data_parallel", "gather_block_partials", "IS_BLOCK",
+                "acceptance_stats_data_parallel"):
         from . import engine
 
         return getattr(engine, name)

@@ -1162,6 +1162,53 @@ int lp_acceptance_stats(lp_handle* h, const float* logp_a, const float* logp_b,
     return LP_OK;
 }
 
+int lp_acceptance_stats_partials(lp_handle* h, const float* logp_a, const float* logp_b,
+                                 const uint8_t* mask, int64_t T, double* out_blk,
+                                 float* out_blk_max, int64_t* out_blk_cnt, void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    if (T < 0 || T > kMaxIsTokens) return fail(LP_ERR_INVALID_ARG, "T must be in [0, 2^31)");
+    h->last_launches = 0;
+    if (T == 0) return LP_OK;
+    if (logp_a == nullptr || logp_b == nullptr || out_blk == nullptr || out_blk_max == nullptr ||
+        out_blk_cnt == nullptr)
+        return fail(LP_ERR_INVALID_ARG,
+                    "logp_a, logp_b, out_blk, out_blk_max and out_blk_cnt must not be NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    h->last_stream = st;
+    const int64_t nblk = ceil_div(T, lp::kIsBlock);
+    // the block kernel of lp_acceptance_stats, its partials in the caller's arrays
+    lp::StatsParams p{logp_a,          logp_b,          mask,        T,
+                      out_blk,         out_blk + nblk,  out_blk + 2 * nblk, out_blk_max,
+                      reinterpret_cast<long long*>(out_blk_cnt)};
+    lp::stats_block_kernel<<<static_cast<unsigned>(nblk), lp::kIsThreads, 0, st>>>(p);
+    LP_CUDA(cudaGetLastError(), "stats_block_kernel launch");
+    ++h->last_launches;
+    return LP_OK;
+}
+
+int lp_acceptance_stats_from_partials(lp_handle* h, const double* blk, const float* blk_max,
+                                      const int64_t* blk_cnt, int64_t num_blocks,
+                                      double* out_stats, void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    if (num_blocks < 0 || num_blocks > ceil_div(kMaxIsTokens, lp::kIsBlock))
+        return fail(LP_ERR_INVALID_ARG, "num_blocks must be in [0, 2^21]");
+    if (out_stats == nullptr) return fail(LP_ERR_INVALID_ARG, "out_stats must not be NULL");
+    if (num_blocks > 0 && (blk == nullptr || blk_max == nullptr || blk_cnt == nullptr))
+        return fail(LP_ERR_INVALID_ARG, "blk, blk_max and blk_cnt must not be NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    h->last_stream = st;
+    h->last_launches = 0;
+    // the final kernel only reads the block arrays
+    double* b = const_cast<double*>(blk);
+    lp::StatsParams p{nullptr, nullptr, nullptr, 0, b, b + num_blocks, b + 2 * num_blocks,
+                      const_cast<float*>(blk_max),
+                      reinterpret_cast<long long*>(const_cast<int64_t*>(blk_cnt))};
+    lp::stats_final_kernel<<<1, 1024, 0, st>>>(p, static_cast<int>(num_blocks), out_stats);
+    LP_CUDA(cudaGetLastError(), "stats_final_kernel launch");
+    ++h->last_launches;
+    return LP_OK;
+}
+
 int lp_reinforce_zero(lp_handle* h, const float* logp_pi, const float* logp_mu,
                       const uint8_t* mask, int64_t T, const int64_t* seq_offsets, int64_t B,
                       const float* rewards, int32_t group_size, const lp_rz_options* opt,

@@ -311,6 +311,44 @@ class Engine:
             self._h, _ptr(logp_a), _ptr(logp_b), _ptr(mask), T, _ptr(out), _stream_ptr(stream)))
         return out
 
+    def acceptance_stats_partials(self, logp_a: torch.Tensor, logp_b: torch.Tensor,
+                                  mask: torch.Tensor = None, stream=None):
+        """This rank's 1024-token block partials of the acceptance statistics:
+        (sums fp64 [3, nb]: sum |d|, sum d^2, sum k3 term; max fp32 [nb]; counts int64 [nb])."""
+        _require(logp_a, "logp_a", torch.float32, 1)
+        _require(logp_b, "logp_b", torch.float32, 1)
+        T = int(logp_a.shape[0])
+        if logp_b.shape[0] != T:
+            raise ValueError("logp_a and logp_b must have the same length")
+        if mask is not None:
+            _require(mask, "mask", torch.uint8, 1)
+            if mask.shape[0] != T:
+                raise ValueError("mask must have length T")
+        dev = logp_a.device
+        nb = (T + IS_BLOCK - 1) // IS_BLOCK
+        sums = torch.empty(3, nb, dtype=torch.float64, device=dev)
+        bmax = torch.empty(nb, dtype=torch.float32, device=dev)
+        cnts = torch.empty(nb, dtype=torch.int64, device=dev)
+        _native.check(self._lib.lp_acceptance_stats_partials(
+            self._h, _ptr(logp_a), _ptr(logp_b), _ptr(mask), T, _ptr(sums), _ptr(bmax),
+            _ptr(cnts), _stream_ptr(stream)))
+        return sums, bmax, cnts
+
+    def acceptance_stats_from_partials(self, sums: torch.Tensor, bmax: torch.Tensor,
+                                       cnts: torch.Tensor, stream=None):
+        """fp64 [5] as ``acceptance_stats``, from gathered block partials in stream order."""
+        _require(sums, "sums", torch.float64, 2)
+        _require(bmax, "bmax", torch.float32, 1)
+        _require(cnts, "cnts", torch.int64, 1)
+        nb = int(cnts.shape[0])
+        if sums.shape != (3, nb) or bmax.shape[0] != nb or not (
+                sums.is_contiguous() and bmax.is_contiguous() and cnts.is_contiguous()):
+            raise ValueError("sums [3, nb], bmax [nb] and cnts [nb] must be contiguous")
+        out = torch.empty(_native.LP_STAT_COUNT, dtype=torch.float64, device=sums.device)
+        _native.check(self._lib.lp_acceptance_stats_from_partials(
+            self._h, _ptr(sums), _ptr(bmax), _ptr(cnts), nb, _ptr(out), _stream_ptr(stream)))
+        return out
+
     def reinforce_zero(self, logp_pi: torch.Tensor, logp_mu: torch.Tensor,
                        seq_offsets: torch.Tensor, rewards: torch.Tensor, group_size: int,
                        mask: torch.Tensor = None, tis_cap: float = None,
@@ -473,33 +511,34 @@ def visible_with_graph_gradient(visible: torch.Tensor, graph: torch.Tensor) -> t
     return visible.detach() + (graph - graph.detach())
 
 
-def gather_block_partials(blk_sum: torch.Tensor, blk_cnt: torch.Tensor, group=None):
-    """All-gather every rank's D3 block partials and concatenate them in rank order.
+def gather_block_partials(*arrays: torch.Tensor, group=None):
+    """All-gather every rank's per-block partial arrays and concatenate them in rank order.
 
-    The collective only moves the fp64 sums and int64 counts (padded to the longest rank's
+    Each array has the rank's block count as its last dimension (the leading dimensions must
+    agree across ranks).  The collective only moves the values (padded to the longest rank's
     block count, then trimmed); it never adds them, so the gathered blocks are bit-identical
-    to the ones one rank would have computed for the whole stream.
+    to the ones one rank would have computed for the whole stream.  Returns one tensor per
+    array.
     """
     import torch.distributed as dist
 
     world = dist.get_world_size(group)
-    n = torch.tensor([blk_sum.shape[0]], dtype=torch.int64, device=blk_sum.device)
+    nb = arrays[0].shape[-1]
+    n = torch.tensor([nb], dtype=torch.int64, device=arrays[0].device)
     sizes = [torch.zeros_like(n) for _ in range(world)]
     dist.all_gather(sizes, n, group=group)
     sizes = [int(x.item()) for x in sizes]
     m = max(sizes)
-
-    def padded(t):
-        out = torch.zeros(m, dtype=t.dtype, device=t.device)
-        out[: t.shape[0]] = t
-        return out
-
-    sums = [torch.empty(m, dtype=blk_sum.dtype, device=blk_sum.device) for _ in range(world)]
-    cnts = [torch.empty(m, dtype=blk_cnt.dtype, device=blk_cnt.device) for _ in range(world)]
-    dist.all_gather(sums, padded(blk_sum), group=group)
-    dist.all_gather(cnts, padded(blk_cnt), group=group)
-    return (torch.cat([x[:k] for x, k in zip(sums, sizes)]),
-            torch.cat([x[:k] for x, k in zip(cnts, sizes)]))
+    out = []
+    for t in arrays:
+        if t.shape[-1] != nb:
+            raise ValueError("every partial array must have one entry per block")
+        pad = torch.zeros(*t.shape[:-1], m, dtype=t.dtype, device=t.device)
+        pad[..., :nb] = t
+        parts = [torch.empty_like(pad) for _ in range(world)]
+        dist.all_gather(parts, pad.contiguous(), group=group)
+        out.append(torch.cat([x[..., :k] for x, k in zip(parts, sizes)], dim=-1).contiguous())
+    return tuple(out)
 
 
 def importance_weights_data_parallel(engine: "Engine", logp_pi: torch.Tensor,
@@ -520,6 +559,23 @@ def importance_weights_data_parallel(engine: "Engine", logp_pi: torch.Tensor,
         raise ValueError(f"rank {rank} holds {T} tokens: every rank but the last must hold a "
                          f"multiple of {IS_BLOCK}")
     w, blk_sum, blk_cnt = engine.importance_weights_partials(logp_pi, logp_mu, mask)
-    all_sum, all_cnt = gather_block_partials(blk_sum, blk_cnt, group)
+    all_sum, all_cnt = gather_block_partials(blk_sum, blk_cnt, group=group)
     d3, n_valid = engine.d3_from_partials(all_sum, all_cnt)
     return w, d3, n_valid
+
+
+def acceptance_stats_data_parallel(engine: "Engine", logp_a: torch.Tensor, logp_b: torch.Tensor,
+                                   mask: torch.Tensor = None, group=None):
+    """fp64 [5] acceptance statistics of a token stream split across data-parallel ranks,
+    under the same rules as ``importance_weights_data_parallel``; bit-identical to one
+    ``acceptance_stats`` call over the whole stream."""
+    import torch.distributed as dist
+
+    T = int(logp_a.shape[0])
+    rank, world = dist.get_rank(group), dist.get_world_size(group)
+    if rank < world - 1 and T % IS_BLOCK != 0:
+        raise ValueError(f"rank {rank} holds {T} tokens: every rank but the last must hold a "
+                         f"multiple of {IS_BLOCK}")
+    sums, bmax, cnts = engine.acceptance_stats_partials(logp_a, logp_b, mask)
+    all_sums, all_max, all_cnts = gather_block_partials(sums, bmax, cnts, group=group)
+    return engine.acceptance_stats_from_partials(all_sums, all_max, all_cnts)

@@ -316,8 +316,29 @@ LP_API int lp_backward_reserve(lp_handle* h, int64_t max_rows);
  */
 enum { LP_STAT_MAX_ABS = 0, LP_STAT_MEAN_ABS, LP_STAT_STD_ABS, LP_STAT_K3, LP_STAT_N_VALID,
        LP_STAT_COUNT };
+
 LP_API int lp_acceptance_stats(lp_handle* h, const float* logp_a, const float* logp_b,
                                const uint8_t* mask, int64_t T, double* out_stats, void* stream);
+
+/*
+ * The same statistics over a token stream split across data-parallel ranks (acceptance is
+ * over every valid sampled token of the update), with the one exchange step of
+ * lp_importance_weights_partials / lp_d3_from_partials:
+ *   lp_acceptance_stats_partials: per 1024-token block of this rank's range, out_blk
+ *     [3][nb] doubles (sum |d|, sum d^2, sum of e^d - 1 - d), out_blk_max [nb] floats
+ *     (max |d|, NaN kept) and out_blk_cnt [nb] valid counts; nb = ceil(T / 1024), device
+ *     arrays, caller-owned.
+ *   lp_acceptance_stats_from_partials: out_stats as lp_acceptance_stats from num_blocks
+ *     gathered blocks (each of the three rows of blk concatenated in stream order).
+ * With every rank but the last holding a multiple of 1024 tokens and the blocks gathered in
+ * rank order, the statistics are bit-identical to one lp_acceptance_stats call.
+ */
+LP_API int lp_acceptance_stats_partials(lp_handle* h, const float* logp_a, const float* logp_b,
+                                        const uint8_t* mask, int64_t T, double* out_blk,
+                                        float* out_blk_max, int64_t* out_blk_cnt, void* stream);
+LP_API int lp_acceptance_stats_from_partials(lp_handle* h, const double* blk,
+                                             const float* blk_max, const int64_t* blk_cnt,
+                                             int64_t num_blocks, double* out_stats, void* stream);
 
 /*
  * REINFORCE Zero loss (REINFORCE Zero summary, section 4) for B responses packed back to

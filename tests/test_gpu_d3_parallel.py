@@ -1,4 +1,5 @@
-"""D3 of a token stream split across data-parallel ranks, through the C ABI on one GPU.
+"""D3 and the acceptance statistics of a token stream split across data-parallel ranks,
+through the C ABI on one GPU.
 
 D3 is a per-update mean over all valid tokens (REINFORCE Zero summary, section 3), so ranks
 that each hold part of the stream must combine their tokens.  The exchange only moves the
@@ -12,7 +13,8 @@ import socket
 import pytest
 import torch
 
-from bit_consistent_logprob_gb300 import Engine, importance_weights_data_parallel, inputs
+from bit_consistent_logprob_gb300 import (Engine, acceptance_stats_data_parallel,
+                                          importance_weights_data_parallel, inputs)
 
 from gpu_util import assert_bit_equal, require_cuda
 
@@ -57,6 +59,31 @@ def test_split_stream_gives_the_single_call_bits(eng, bounds, masked):
     assert nv_p.item() == nv.item()
 
 
+@pytest.mark.parametrize("bounds,nan_at", [
+    ([0, 1024, 5000], None),
+    ([0, 4096, 2_000_896, 3_000_000], None),
+    ([0, 2048, 9000], 7000),                       # a NaN difference on a later rank
+])
+def test_split_stream_acceptance_statistics(eng, bounds, nan_at):
+    dev = require_cuda()
+    T = bounds[-1]
+    lp, lm, mask = inputs.synthetic_is_inputs(T, seed=T + 1, device=dev)
+    if nan_at is not None:
+        lp[nan_at] = float("nan")
+        mask[nan_at] = 1
+    want = eng.acceptance_stats(lp, lm, mask)
+    parts = [eng.acceptance_stats_partials(lp[a:b], lm[a:b], mask[a:b])
+             for a, b in zip(bounds[:-1], bounds[1:])]
+    got = eng.acceptance_stats_from_partials(torch.cat([p[0] for p in parts], dim=1).contiguous(),
+                                             torch.cat([p[1] for p in parts]),
+                                             torch.cat([p[2] for p in parts]))
+    torch.cuda.synchronize()
+    eng.check()
+    assert_bit_equal(got, want, "statistics from gathered block partials")
+    if nan_at is not None:
+        assert torch.isnan(got[0]).item()
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
@@ -71,11 +98,13 @@ def test_data_parallel_helper_with_nccl(eng):
     dev = require_cuda()
     lp, lm, mask = inputs.synthetic_is_inputs(50_000, seed=5, device=dev)
     w, d3, nv = eng.importance_weights(lp, lm, mask)
+    st = eng.acceptance_stats(lp, lm, mask)
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(_free_port())
     dist.init_process_group("nccl", rank=0, world_size=1)
     try:
         w_p, d3_p, nv_p = importance_weights_data_parallel(eng, lp, lm, mask)
+        st_p = acceptance_stats_data_parallel(eng, lp, lm, mask)
         torch.cuda.synchronize()
     finally:
         dist.destroy_process_group()
@@ -83,3 +112,4 @@ def test_data_parallel_helper_with_nccl(eng):
     assert_bit_equal(w_p, w, "w")
     assert_bit_equal(d3_p, d3, "D3")
     assert nv_p.item() == nv.item()
+    assert_bit_equal(st_p, st, "acceptance statistics")

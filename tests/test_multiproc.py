@@ -122,7 +122,10 @@ def _d3_worker(rank, world, port, bounds, seed, out):
     b0, b1 = bounds[rank] // 1024, (bounds[rank + 1] + 1023) // 1024   # this rank's blocks
     s_all, c_all = gather_block_partials(torch.from_numpy(sums[b0:b1].copy()),
                                          torch.from_numpy(cnts[b0:b1].copy()))
-    out[rank] = (s_all.numpy().view(np.int64).tolist(), c_all.numpy().tolist())
+    rows = np.stack([sums, -sums, 2 * sums])                # a [3, nb] array of partials
+    (r_all,) = gather_block_partials(torch.from_numpy(rows[:, b0:b1].copy()))
+    out[rank] = (s_all.numpy().view(np.int64).tolist(), c_all.numpy().tolist(),
+                 r_all.numpy().view(np.int64).tolist())
     dist.destroy_process_group()
 
 
@@ -137,9 +140,11 @@ def test_d3_block_partials_gather_in_rank_order(bounds):
     mp.start_processes(_d3_worker, args=(world, _free_port(), bounds, 17, out), nprocs=world,
                        start_method="spawn")
     sums, cnts = _stream_blocks(bounds[-1], 17)
+    rows = np.stack([sums, -sums, 2 * sums])
     for r in range(world):
         assert out[r][0] == sums.view(np.int64).tolist(), f"rank {r} sums"
         assert out[r][1] == cnts.tolist(), f"rank {r} counts"
+        assert out[r][2] == rows.view(np.int64).tolist(), f"rank {r} [3, nb] rows"
 
 
 def _misaligned_worker(rank, world, port, out):
