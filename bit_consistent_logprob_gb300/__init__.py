@@ -17,7 +17,8 @@ from ._native import LpError, load as load_library, library_path  # noqa: F401
 __all__ = ["Engine", "LpError", "load_library", "library_path", "LP_PHASE_AUTO",
            "LP_PHASE_PREFILL", "LP_PHASE_DECODE", "logprobs_with_grad",
            "visible_with_graph_gradient", "importance_weights_data_parallel",
-           "gather_block_partials", "IS_BLOCK", "acceptance_stats_data_parallel"]
+           "gather_block_partials", "IS_BLOCK", "acceptance_stats_data_parallel",
+           "logprobs_vocab_parallel", "gather_vocab_partials"]
 
 
 def __getattr__(name):
@@ -26,7 +27,8 @@ def __getattr__(name):
     if name in ("Engine", "LP_PHASE_AUTO", "LP_PHASE_PREFILL", "LP_PHASE_DECODE",
                 "logprobs_with_grad", "visible_with_graph_gradient",
                 "importance_weights_data_parallel", "gather_block_partials", "IS_BLOCK",
-                "acceptance_stats_data_parallel"):
+                "acceptance_stats_data_parallel", "logprobs_vocab_parallel",
+                "gather_vocab_partials"):
         from . import engine
 
         return getattr(engine, name)

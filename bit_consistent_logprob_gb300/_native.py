@@ -53,6 +53,9 @@ SIGNATURES = {
     "lp_importance_weights_host": (ctypes.c_int, [_p, _p, _p, _p, _i64, _p, _p, _p, _p]),
     "lp_importance_weights_partials": (ctypes.c_int, [_p, _p, _p, _p, _i64, _p, _p, _p, _p]),
     "lp_d3_from_partials": (ctypes.c_int, [_p, _p, _p, _i64, _p, _p, _p]),
+    "lp_vocab_partials": (ctypes.c_int, [_p, _p, _i64, _p, _i64, _p, _i64, _p, _p]),
+    "lp_logprobs_from_vocab_partials": (ctypes.c_int, [_p, _i32, _p, _i64, _p, _p, _i64, _p, _p,
+                                                       _p]),
     "lp_acceptance_stats_partials": (ctypes.c_int, [_p, _p, _p, _p, _i64, _p, _p, _p, _p]),
     "lp_acceptance_stats_from_partials": (ctypes.c_int, [_p, _p, _p, _p, _i64, _p, _p]),
     "lp_acceptance_stats": (ctypes.c_int, [_p, _p, _p, _p, _i64, _p, _p]),

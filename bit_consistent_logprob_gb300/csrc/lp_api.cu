@@ -1096,6 +1096,82 @@ int lp_importance_weights(lp_handle* h, const float* logp_pi, const float* logp_
 
 static_assert(sizeof(long long) == sizeof(int64_t), "block counts cross the ABI as int64_t");
 
+int lp_vocab_partials(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids_local,
+                      int64_t T, void* out_ms, int64_t ld_ms, float* out_zy, void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    if (h->fp8 || h->cfg.tp_slices != 1)
+        return fail(LP_ERR_UNSUPPORTED, "vocabulary partials come from a bf16 handle with "
+                                        "tp_slices = 1");
+    int rc = check_x(h, X, ldx, T);
+    if (rc != LP_OK) return rc;
+    if (T > h->cfg.max_tokens) return fail(LP_ERR_INVALID_ARG, "T must be <= max_tokens");
+    h->last_launches = 0;
+    if (T == 0) return LP_OK;
+    if (ids_local == nullptr || out_ms == nullptr || out_zy == nullptr || ld_ms < T ||
+        !aligned16(out_ms))
+        return fail(LP_ERR_INVALID_ARG,
+                    "ids_local, out_ms (16-byte aligned, ld_ms >= T) and out_zy are required");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    h->last_stream = st;
+    const int rows = static_cast<int>(T);
+    // the fused leaf GEMM of this slice; a row whose sampled id lies outside the slice is
+    // simply not captured (its id belongs to another rank)
+    rc = launch_leaf_gemm<lp::kModeLse>(h, X, ldx, rows, 0, h->cfg.n_leaves, ids_local, nullptr,
+                                        0, st);
+    if (rc != LP_OK) return rc;
+    LP_CUDA(cudaMemcpy2DAsync(out_ms, sizeof(float2) * static_cast<size_t>(ld_ms), h->ws_ms,
+                              sizeof(float2) * static_cast<size_t>(h->cfg.max_tokens),
+                              sizeof(float2) * static_cast<size_t>(rows),
+                              static_cast<size_t>(h->num_lse_tiles), cudaMemcpyDeviceToDevice, st),
+            "tile partials copy");
+    LP_CUDA(cudaMemcpyAsync(out_zy, h->zy, sizeof(float) * static_cast<size_t>(rows),
+                            cudaMemcpyDeviceToDevice, st),
+            "sampled logits copy");
+    return LP_OK;
+}
+
+int lp_logprobs_from_vocab_partials(lp_handle* h, int32_t V_full, const void* ms, int64_t ld_ms,
+                                    const float* zy, const int32_t* ids, int64_t T,
+                                    float* out_logp, float* out_logZ, void* stream) {
+    if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
+    if (V_full <= 0) return fail(LP_ERR_INVALID_ARG, "V_full must be positive");
+    const int64_t tiles = ceil_div(static_cast<int64_t>(V_full), lp::kLT);
+    if (tiles > (lp::kCmbMaxThreads << lp::kSegLogMax))
+        return fail(LP_ERR_UNSUPPORTED, "V too large (at most 2^26 columns)");
+    if (T < 0 || T > (int64_t(1) << 31) - 1) return fail(LP_ERR_INVALID_ARG, "T out of range");
+    h->last_launches = 0;
+    if (T == 0) return LP_OK;
+    if (ms == nullptr || zy == nullptr || ids == nullptr || out_logp == nullptr || ld_ms < T ||
+        !aligned16(ms))
+        return fail(LP_ERR_INVALID_ARG, "ms (16-byte aligned, ld_ms >= T), zy, ids and out_logp "
+                                        "are required");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    h->last_stream = st;
+    // the fixed pairwise tree over all tiles of the full vocabulary, as in lp_logprobs
+    const int rows = static_cast<int>(T);
+    lp::CombineParams c{};
+    c.ws_ms = static_cast<const float2*>(ms);
+    c.ws_ld = ld_ms;
+    c.zy = zy;
+    c.ids = ids;
+    c.T = rows;
+    c.V = V_full;
+    c.num_tiles = static_cast<int32_t>(tiles);
+    const lp::CombineLayout lay = lp::combine_layout(rows, c.num_tiles, h->num_sms);
+    c.rows = lay.rows;
+    c.seg_log = lay.seg_log;
+    c.nseg = lay.nseg;
+    c.out_logp = out_logp;
+    c.out_logZ = out_logZ;
+    c.status = h->status;
+    const dim3 grid(static_cast<unsigned>(ceil_div(rows, lay.rows)));
+    const dim3 block(static_cast<unsigned>(lay.rows * lay.nseg));
+    lp::lse_combine_kernel<false><<<grid, block, sizeof(float2) * lay.rows * lay.nseg, st>>>(c);
+    LP_CUDA(cudaGetLastError(), "lse_combine_kernel launch");
+    ++h->last_launches;
+    return LP_OK;
+}
+
 int lp_importance_weights_partials(lp_handle* h, const float* logp_pi, const float* logp_mu,
                                    const uint8_t* mask, int64_t T, float* out_w,
                                    double* out_blk_sum, int64_t* out_blk_cnt, void* stream) {

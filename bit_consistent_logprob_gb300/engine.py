@@ -255,6 +255,42 @@ class Engine:
             _ptr(out_nvalid), _stream_ptr(stream)))
         return out_w, out_d3, out_nvalid
 
+    def vocab_partials(self, X: torch.Tensor, ids_local: torch.Tensor, stream=None):
+        """This vocabulary slice's share of a vocabulary-parallel logprob: (ms fp32
+        [ceil(V/64), T, 2]: per-tile (max, sum-exp); zy fp32 [T]: sampled logit, defined where
+        0 <= ids_local < V).  The handle is opened over the slice; ids_local = id - v0."""
+        _require(X, "X", torch.bfloat16, 2)
+        _require(ids_local, "ids_local", torch.int32, 1)
+        T = int(X.shape[0])
+        if X.shape[1] != self.H or X.stride(1) != 1:
+            raise ValueError("X must be [T, H] with unit column stride")
+        if ids_local.shape[0] != T or not ids_local.is_contiguous():
+            raise ValueError("ids_local must be a contiguous [T] tensor")
+        nt = (self.V + 63) // 64
+        ms = torch.empty(nt, T, 2, dtype=torch.float32, device=X.device)
+        zy = torch.empty(T, dtype=torch.float32, device=X.device)
+        ldx = X.stride(0) if T > 1 else self.H
+        _native.check(self._lib.lp_vocab_partials(self._h, _ptr(X), ldx, _ptr(ids_local), T,
+                                                  _ptr(ms), T, _ptr(zy), _stream_ptr(stream)))
+        return ms, zy
+
+    def logprobs_from_vocab_partials(self, V_full: int, ms: torch.Tensor, zy: torch.Tensor,
+                                     ids: torch.Tensor, return_logZ: bool = False, stream=None):
+        """logp (and logZ) over the full vocabulary from gathered tile partials
+        ms [ceil(V_full/64), T, 2] (vocabulary order) and owner-picked zy [T]."""
+        _require(ms, "ms", torch.float32, 3)
+        _require(zy, "zy", torch.float32, 1)
+        _require(ids, "ids", torch.int32, 1)
+        T = int(zy.shape[0])
+        if ms.shape != ((int(V_full) + 63) // 64, T, 2) or not ms.is_contiguous():
+            raise ValueError("ms must be a contiguous [ceil(V_full/64), T, 2] tensor")
+        out = torch.empty(T, dtype=torch.float32, device=zy.device)
+        out_logZ = torch.empty(T, dtype=torch.float32, device=zy.device) if return_logZ else None
+        _native.check(self._lib.lp_logprobs_from_vocab_partials(
+            self._h, int(V_full), _ptr(ms), T, _ptr(zy), _ptr(ids), T, _ptr(out), _ptr(out_logZ),
+            _stream_ptr(stream)))
+        return (out, out_logZ) if return_logZ else out
+
     def importance_weights_partials(self, logp_pi: torch.Tensor, logp_mu: torch.Tensor,
                                     mask: torch.Tensor = None, stream=None):
         """(w fp32 [T], block sums fp64 [nb], block counts int64 [nb]), nb = ceil(T / 1024):
@@ -579,3 +615,49 @@ def acceptance_stats_data_parallel(engine: "Engine", logp_a: torch.Tensor, logp_
     sums, bmax, cnts = engine.acceptance_stats_partials(logp_a, logp_b, mask)
     all_sums, all_max, all_cnts = gather_block_partials(sums, bmax, cnts, group=group)
     return engine.acceptance_stats_from_partials(all_sums, all_max, all_cnts)
+
+
+def gather_vocab_partials(ms: torch.Tensor, zy: torch.Tensor, ids: torch.Tensor, v0: int,
+                          V_local: int, V_full: int, group=None):
+    """The exchange of a vocabulary-parallel logprob: every rank's tile partials ms
+    [tiles, T, 2] all-gathered in vocabulary order, and each row's sampled logit taken from
+    the rank whose slice [v0, v0 + V_local) holds its (global) id.  Data movement only.
+    Returns (ms_all [ceil(V_full/64), T, 2], zy_all [T])."""
+    import torch.distributed as dist
+
+    if v0 % 128 != 0:
+        raise ValueError(f"a vocabulary slice must start at a multiple of 128 rows (got {v0})")
+    world = dist.get_world_size(group)
+    bounds = torch.tensor([v0, V_local], dtype=torch.int64, device=ms.device)
+    all_bounds = [torch.empty_like(bounds) for _ in range(world)]
+    dist.all_gather(all_bounds, bounds, group=group)
+    starts = [int(b[0]) for b in all_bounds]
+    ends = [int(b[0] + b[1]) for b in all_bounds]
+    if starts[0] != 0 or ends[-1] != V_full or any(e != s for e, s in zip(ends[:-1], starts[1:])):
+        raise ValueError("the slices must cover [0, V_full) in rank order")
+    (ms_t,) = gather_block_partials(ms.permute(1, 2, 0).contiguous(), group=group)
+    ms_all = ms_t.permute(2, 0, 1).contiguous()
+    zys = [torch.empty_like(zy) for _ in range(world)]
+    dist.all_gather(zys, zy.contiguous(), group=group)
+    start_t = torch.tensor(starts, dtype=torch.int64, device=ms.device)
+    owner = (torch.searchsorted(start_t, ids.to(torch.int64), right=True) - 1).clamp_(0, world - 1)
+    zy_all = torch.stack(zys)[owner, torch.arange(zy.shape[0], device=ms.device)].contiguous()
+    return ms_all, zy_all
+
+
+def logprobs_vocab_parallel(engine: "Engine", X: torch.Tensor, ids: torch.Tensor, v0: int,
+                            V_full: int, return_logZ: bool = False, group=None):
+    """Sampled-token logprobs with the lm_head split by vocabulary across ranks.
+
+    ``engine`` is this rank's handle over the rows [v0, v0 + engine.V) of the full lm_head;
+    ranks hold consecutive slices in rank order, each starting at a multiple of 128 rows.
+    Every rank passes the same X and (global) ids and gets the full-vocabulary logp, with the
+    bits of one ``logprobs`` call on the whole lm_head (``gather_vocab_partials`` moves the
+    partials; the fixed tile tree finishes them).
+    """
+    if v0 % 128 != 0:
+        raise ValueError(f"a vocabulary slice must start at a multiple of 128 rows (got {v0})")
+    ms, zy = engine.vocab_partials(X, ids - v0)
+    ms_all, zy_all = gather_vocab_partials(ms, zy, ids, v0, engine.V, V_full, group)
+    return engine.logprobs_from_vocab_partials(V_full, ms_all, zy_all, ids,
+                                               return_logZ=return_logZ)

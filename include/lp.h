@@ -202,6 +202,31 @@ LP_API int lp_importance_weights(lp_handle* h, const float* logp_pi, const float
                           int64_t* out_nvalid, void* stream);
 
 /*
+ * Vocabulary-parallel split of the lm_head (the pages' rule for parallel layouts: ranks only
+ * transport partials, which a fixed schedule then combines; IsoExec summary,
+ * "Parallelism-invariant kernels").  A rank holding the rows [v0, v0 + V) of the full lm_head
+ * opens a bf16 handle over that slice (lp_init with this V and W pointing at row v0).
+ *   lp_vocab_partials: the fused leaf GEMM of the slice for T <= max_tokens rows, writing the
+ *     (max, sum-exp) partial of each of its ceil(V / 64) vocabulary tiles to out_ms (device,
+ *     float pairs [ceil(V / 64)][ld_ms], ld_ms >= T, 16-byte aligned) and the sampled logit
+ *     to out_zy [T].  ids_local[t] = sampled id - v0; out_zy[t] is defined only for rows with
+ *     ids_local[t] in [0, V), whose sampled token this rank owns.
+ *   lp_logprobs_from_vocab_partials: on any handle (it lends its status word), logp and logZ
+ *     for the full vocabulary of V_full tokens from the gathered partials: every rank's tile
+ *     rows concatenated in vocabulary order (ms: float pairs [ceil(V_full / 64)][ld_ms]) and,
+ *     per row, the sampled logit from the rank owning its id (zy [T]); ids are global.
+ * When every slice starts at a multiple of 128 rows, the results are bit-identical to
+ * lp_logprobs on the full lm_head (each tile partial is the same computation, and the tile
+ * tree is the same).  A block-FP8 or TP-split handle returns LP_ERR_UNSUPPORTED.
+ */
+LP_API int lp_vocab_partials(lp_handle* h, const void* X, int64_t ldx, const int32_t* ids_local,
+                             int64_t T, void* out_ms, int64_t ld_ms, float* out_zy, void* stream);
+LP_API int lp_logprobs_from_vocab_partials(lp_handle* h, int32_t V_full, const void* ms,
+                                           int64_t ld_ms, const float* zy, const int32_t* ids,
+                                           int64_t T, float* out_logp, float* out_logZ,
+                                           void* stream);
+
+/*
  * D3 over a token stream split across data-parallel ranks, with one exchange step.  D3 is a
  * per-update mean over all valid tokens (REINFORCE Zero summary, section 3), so ranks must
  * combine their tokens; the pages let the collective only move partials, never reduce them

@@ -170,3 +170,42 @@ def test_d3_data_parallel_rejects_a_misaligned_rank():
     mp.start_processes(_misaligned_worker, args=(2, _free_port(), out), nprocs=2,
                        start_method="spawn")
     assert out[0] == "rejected"
+
+
+def _vocab_worker(rank, world, port, starts, V_full, T, out):
+    import sys
+
+    sys.path.insert(0, ROOT)
+    from bit_consistent_logprob_gb300 import gather_vocab_partials
+
+    _init(rank, world, port)
+    v0, v1 = starts[rank], (starts[rank + 1] if rank + 1 < world else V_full)
+    t0, t1 = v0 // 64, (v1 + 63) // 64                      # this rank's 64-column tiles
+    tiles = torch.arange(t0, t1, dtype=torch.float32)
+    ms = torch.stack([tiles[:, None] * 1000 + torch.arange(T, dtype=torch.float32),
+                      -tiles[:, None].expand(-1, T)], dim=-1)   # [tiles, T, 2], tile-coded
+    zy = torch.full((T,), float(rank)) + torch.arange(T, dtype=torch.float32) / 1000
+    ids = (torch.arange(T, dtype=torch.int64) * 7919 % V_full).to(torch.int32)
+    ms_all, zy_all = gather_vocab_partials(ms, zy, ids, v0, v1 - v0, V_full)
+    out[rank] = (ms_all.numpy().tolist(), zy_all.numpy().tolist())
+    dist.destroy_process_group()
+
+
+def test_vocab_partials_gather_in_vocabulary_order_and_pick_the_owner():
+    # Three ranks own vocabulary slices starting at multiples of 128; every rank must get
+    # all tiles in vocabulary order and, per row, the sampled logit of the rank owning its id.
+    starts, V_full, T = [0, 1280, 2560], 4001, 16
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    mp.start_processes(_vocab_worker, args=(3, _free_port(), starts, V_full, T, out), nprocs=3,
+                       start_method="spawn")
+    nt = (V_full + 63) // 64
+    ids = np.arange(T) * 7919 % V_full
+    owner = np.searchsorted(np.array(starts), ids, side="right") - 1
+    for r in range(3):
+        ms_all = np.array(out[r][0])
+        assert ms_all.shape == (nt, T, 2)
+        assert np.array_equal(ms_all[:, :, 1], -np.arange(nt)[:, None] * np.ones((1, T)))
+        assert np.array_equal(ms_all[:, :, 0], np.arange(nt)[:, None] * 1000 + np.arange(T))
+        want_zy = owner.astype(np.float32) + np.arange(T, dtype=np.float32) / 1000
+        assert np.array_equal(np.array(out[r][1], dtype=np.float32), want_zy), f"rank {r}"
