@@ -86,6 +86,32 @@ def test_null_handle_is_rejected(lib):
     assert LP_OK == 0
 
 
+def test_null_handle_is_rejected_by_the_parallel_exchange_calls(lib):
+    # the partial-export and finish calls of the data- and vocabulary-parallel splits
+    # validate on the host before any CUDA call
+    assert lib.lp_importance_weights_partials(None, None, None, None, 0, None, None, None,
+                                              None) == LP_ERR_INVALID_ARG
+    assert lib.lp_d3_from_partials(None, None, None, 0, None, None, None) == LP_ERR_INVALID_ARG
+    assert lib.lp_acceptance_stats_partials(None, None, None, None, 0, None, None, None,
+                                            None) == LP_ERR_INVALID_ARG
+    assert lib.lp_acceptance_stats_from_partials(None, None, None, None, 0, None,
+                                                 None) == LP_ERR_INVALID_ARG
+    assert lib.lp_vocab_partials(None, None, 256, None, 0, None, 0, None,
+                                 None) == LP_ERR_INVALID_ARG
+    assert lib.lp_logprobs_from_vocab_partials(None, 4096, None, 0, None, None, 0, None, None,
+                                               None) == LP_ERR_INVALID_ARG
+
+
+def test_block_size_of_the_header_and_the_binding_agree():
+    import re
+
+    from bit_consistent_logprob_gb300.engine import IS_BLOCK
+
+    with open(os.path.join(ROOT, "include", "lp.h")) as f:
+        m = re.search(r"#define LP_IS_BLOCK (\d+)", f.read())
+    assert m and int(m.group(1)) == IS_BLOCK
+
+
 def test_engine_requires_the_native_library(monkeypatch, tmp_path):
     # No silent fallback: a missing library is an error that names the build step.
     from bit_consistent_logprob_gb300 import build
