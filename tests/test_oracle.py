@@ -639,6 +639,44 @@ def test_entropy_fp8_equals_the_bf16_oracle_on_representable_inputs():
                                oracle.entropy(X, W, rows=[3, 0]), rtol=1e-13, atol=1e-12)
 
 
+def test_fp8_activation_scales_indexed_by_row_and_block():
+    # Activation blocks (1 x 128, one scale per row and per 128-K block; the DeepSeek block
+    # rule the vLLM blog keeps for block-FP8) whose scales are unequal powers of two that
+    # differ along the row AND along K.  Each block holds e4m3 grid values times its scale, so
+    # it quantises to the grid codes with exactly that scale, and the dequantised operands are
+    # the bf16 values themselves: the block-FP8 logprob and entropy must equal the (pinned)
+    # bf16 oracle's.  A scale read from another row or another block changes the logits.
+    rng = np.random.default_rng(75)
+    grid = oracle.e4m3_decode(np.arange(1, 0x7F, dtype=np.uint8))
+    grid = np.concatenate([grid, -grid])
+    def rep(shape):
+        v = rng.choice(grid[np.abs(grid) <= 2.0], size=shape)
+        v[:, ::128] = 448.0
+        return v.astype(np.float32)
+    expo = np.array([[0, 3], [2, 1], [5, 0], [1, 4], [3, 2]])  # 2^-e per (row, K block)
+    xv = rep((5, 256))
+    for r in range(5):
+        for kb in range(2):
+            xv[r, kb * 128:(kb + 1) * 128] /= np.float32(2.0 ** expo[r, kb])
+    X = f32_to_bf16_bits(xv)
+    W = f32_to_bf16_bits(np.concatenate([rep((128, 256)), rep((6, 256))]) / 16.0)
+    ids = np.array([3, 131, 64, 0, 100], dtype=np.int32)
+    xq, sx = oracle.quantize_blocks(X, 1)
+    wq, sw = oracle.quantize_blocks(W, 128)
+    assert sx.shape == (5, 2)
+    np.testing.assert_array_equal(sx, (2.0 ** -expo).astype(np.float32))
+    assert len(set(sx[:, 0].tolist())) > 1 and np.any(sx[:, 0] != sx[:, 1])
+    lp8, lz8 = oracle.logprobs_fp8(xq, sx, wq, sw, ids)
+    lp, lz = oracle.logprobs(X, W, ids)
+    np.testing.assert_allclose(lp8, lp, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lz8, lz, rtol=1e-15, atol=1e-15)
+    assert np.ptp(lp) > 0.1  # the logits really vary between tokens
+    np.testing.assert_allclose(oracle.entropy_fp8(xq, sx, wq, sw), oracle.entropy(X, W),
+                               rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(oracle.entropy_fp8(xq, sx, wq, sw, rows=[4, 1]),
+                               oracle.entropy(X, W, rows=[4, 1]), rtol=1e-13, atol=1e-13)
+
+
 def test_entropy_fp8_of_a_zero_lm_head_is_log_v():
     X = f32_to_bf16_bits(np.random.default_rng(74).standard_normal((3, 128)).astype(np.float32))
     W = np.zeros((300, 128), dtype=np.uint16)
@@ -686,6 +724,15 @@ MUTATIONS = [
      "float s = amax > 0.0f ? amax / 224.0f : 1.0f;"),
     ("weight scale with a transposed block index", "(double)sw[(v / 128) * nkb + k / 128]",
      "(double)sw[(k / 128) * nkb + v / 128]"),
+    ("FP8 activation scale without the row index",
+     "(double)sx[t * nkb + k / 128];", "(double)sx[k / 128];"),
+    ("FP8 activation scale without the block index",
+     "(double)sx[t * nkb + k / 128];", "(double)sx[t * nkb];"),
+    ("FP8 entropy activation scale without the row index",
+     "const float* sxrow = sx + t * nkb;", "const float* sxrow = sx;"),
+    ("FP8 entropy activation scale without the block index",
+     "xd[k] = oracle_e4m3_decode(xq[t * H + k]) * (double)sxrow[k / 128];",
+     "xd[k] = oracle_e4m3_decode(xq[t * H + k]) * (double)sxrow[0];"),
     ("sequence gate on the last token only", "lr += (double)logp_pi[t] - (double)logp_mu[t];",
      "lr = (double)logp_pi[t] - (double)logp_mu[t];"),
 ]
@@ -731,7 +778,8 @@ def test_pins_catch_planted_mistake(tmp_path, monkeypatch, golden_dir, desc, ori
             test_e4m3_rounding_matches_the_library_and_saturates, test_block_quantisation_rule,
             test_logprobs_fp8_equals_the_bf16_oracle_on_representable_inputs,
             test_entropy_fp8_equals_the_bf16_oracle_on_representable_inputs,
-            test_entropy_fp8_of_a_zero_lm_head_is_log_v]
+            test_entropy_fp8_of_a_zero_lm_head_is_log_v,
+            test_fp8_activation_scales_indexed_by_row_and_block]
     failed = 0
     for pin in pins:
         try:
