@@ -114,33 +114,6 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& 
     vt = vt0 + (r - rt * width);
 }
 
-// Cluster of two CTAs: they take vocabulary-adjacent tiles (2*vp, 2*vp + 1) of one row tile
-// and share its X tile.  Cluster tiles follow the same band schedule with bands of band/2
-// vocabulary pairs.  A CTA whose tile lies past the vocabulary still loads and computes
-// (its partner needs its half of X) but writes nothing.
-__device__ __forceinline__ void pair_tile_coords(int ct, const GemmParams& p, int num_pairs,
-                                                 uint32_t rank, int& rt, int& vt) {
-    const int band = p.band >> 1;
-    const int per_band = p.num_row_tiles * band;
-    const int b = ct / per_band;
-    const int r = ct - b * per_band;
-    const int vp0 = b * band;
-    const int width = min(band, num_pairs - vp0);
-    rt = r / width;
-    vt = 2 * (vp0 + (r - rt * width)) + static_cast<int>(rank);
-}
-
-// W-sharing pair (two-row-tile decode launches): the two CTAs take row tiles 2*rp and
-// 2*rp + 1 of one vocabulary tile and share its W tile, each loading 64 of its 128 vocabulary
-// rows and multicasting them to both; each loads its own X tile.  A CTA whose row tile lies
-// past T still loads and computes (its partner needs its half of W) but writes nothing.
-__device__ __forceinline__ void wpair_tile_coords(int ct, const GemmParams& p, uint32_t rank,
-                                                  int& rt, int& vt) {
-    const int rp = ct / p.num_vocab_tiles;
-    vt = ct - rp * p.num_vocab_tiles;
-    rt = 2 * rp + static_cast<int>(rank);
-}
-
 __device__ __forceinline__ void raise_timeout(const GemmParams& p, volatile int* abort_flag) {
     *abort_flag = 1;
     atomicOr(p.status, kStatusTimeout);
@@ -165,20 +138,15 @@ __device__ __forceinline__ void release_buf(uint64_t* bar) {
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
-// kCluster = 1: one CTA per tile.  kCluster = 2: clusters of two CTAs share the X tile of
-// vocabulary-adjacent tiles; each CTA loads 64 of its 128 rows and multicasts them to both
-// (tmX then has 64-row boxes).  kCluster = 2 with kShareW: the pair shares the W tile of two
-// row tiles instead (tmW then has 64-row boxes).  The per-element arithmetic is identical in
-// every mode.
+// One CTA per 128 x 128 tile; each CTA loads its own X and W boxes.
 // tmD (kModeGrad only): dl as bf16 [T][ldd] with 64 x 32 boxes, 128-byte swizzle.
-template <int kMode, int kSub, int kCluster, bool kShareW = false>
+template <int kMode, int kSub>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     leaf_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
     constexpr int kStages = gemm_stages(kSub, kMode);
     constexpr int kStageBytes = kSub * kTileBytes;       // one operand, one stage
-    static_assert(!kShareW || kCluster == 2, "W is shared within a two-CTA cluster");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -198,12 +166,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    const uint32_t crank = kCluster == 2 ? cluster_ctarank() : 0u;
-    constexpr uint16_t kPairMask = 0x3;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kCluster);  // one MMA commit from each CTA that reads the stage
+            mbar_init(&empty[s], 1);  // the MMA commit that frees the stage
         }
         for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -223,35 +189,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (kCluster == 2) cluster_sync_all();  // the partner's barriers exist before any multicast
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
 
-    const int num_pairs = (p.num_vocab_tiles + 1) >> 1;
-    const int num_tiles = kShareW       ? ((p.num_row_tiles + 1) >> 1) * p.num_vocab_tiles
-                          : kCluster == 2 ? p.num_row_tiles * num_pairs
-                                          : p.num_row_tiles * p.num_vocab_tiles;
-    const int tile0 = kCluster == 2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-    const int tile_step = kCluster == 2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    const int num_tiles = p.num_row_tiles * p.num_vocab_tiles;
+    const int tile0 = static_cast<int>(blockIdx.x);
+    const int tile_step = static_cast<int>(gridDim.x);
     const int nkb = p.leaf_len / (kBK * kSub);   // stages per leaf
     const int n = p.leaf_count;
 
     constexpr uint32_t kFull = 0xffffffffu;
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer (warp)
-        const uint32_t tx_bytes = static_cast<uint32_t>(
-            kSub * ((kCluster == 2 && !kShareW ? kBM : p.x_box_rows) * kBK * 2 + kTileBytes));
+        const uint32_t tx_bytes =
+            static_cast<uint32_t>(kSub * (p.x_box_rows * kBK * 2 + kTileBytes));
         uint32_t stage = 0, phase = 0;
         uint64_t issued = 0;
         bool ok = true;
         for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
             int rt, vt;
-            if (kShareW)
-                wpair_tile_coords(tile, p, crank, rt, vt);
-            else if (kCluster == 2)
-                pair_tile_coords(tile, p, num_pairs, crank, rt, vt);
-            else
-                tile_coords(tile, p, rt, vt);
+            tile_coords(tile, p, rt, vt);
             const int row0 = rt * kBM, v0 = vt * kVT;
             for (int jj = 0; ok && jj < n; ++jj) {
                 const int kbase = (p.leaf_begin + jj) * p.leaf_len;
@@ -268,23 +225,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const int k0 = kbase + (kb * kSub + u) * kBK;
                         uint8_t* xdst = sA + stage * kStageBytes + u * kTileBytes;
                         uint8_t* wdst = sB + stage * kStageBytes + u * kTileBytes;
-                        if constexpr (kShareW) {
-                            // my own X tile; my 64 vocabulary rows of the shared W tile, to both
-                            tma_load_2d_elect(&tmX, &full[stage], xdst, k0, row0);
-                            tma_load_2d_mc_elect(&tmW, &full[stage],
-                                                 wdst + crank * (kTileBytes / 2), k0,
-                                                 v0 + static_cast<int>(crank) * (kVT / 2),
-                                                 kPairMask);
-                        } else {
-                            if (kCluster == 2)  // my 64 rows of the shared X tile, to both CTAs
-                                tma_load_2d_mc_elect(&tmX, &full[stage],
-                                                     xdst + crank * (kTileBytes / 2), k0,
-                                                     row0 + static_cast<int>(crank) * (kBM / 2),
-                                                     kPairMask);
-                            else
-                                tma_load_2d_elect(&tmX, &full[stage], xdst, k0, row0);
-                            tma_load_2d_elect(&tmW, &full[stage], wdst, k0, v0);
-                        }
+                        tma_load_2d_elect(&tmX, &full[stage], xdst, k0, row0);
+                        tma_load_2d_elect(&tmW, &full[stage], wdst, k0, v0);
                     }
                     ++issued;
                     if (++stage == kStages) {
@@ -347,11 +289,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint64_t a = descA + stage * kStageDesc;
                     const uint64_t b = descB + stage * kStageDesc;
                     // +32 bytes (2 descriptor units) per K step of 16 bf16 inside a row;
-                    // only the leaf's very first MMA starts a fresh accumulator; the stage is
-                    // freed for both CTAs of a pair (multicast commit) or for this CTA
+                    // only the leaf's very first MMA starts a fresh accumulator; the commit
+                    // frees the stage
                     static_assert(kSubDesc == 1024, "sub-block stride assumed by the stage issue");
-                    umma_stage_elect<kSub, kCluster == 2>(d_tmem, a, b, kIdesc, kb != 0 ? 1u : 0u,
-                                                          &empty[stage], kPairMask);
+                    umma_stage_elect<kSub>(d_tmem, a, b, kIdesc, kb != 0 ? 1u : 0u,
+                                           &empty[stage]);
                     // probe the next stage (and the next leaf's buffer) while these MMAs run
                     ready = __all_sync(kFull, mbar_test_wait(&full[nstage], nphase));
                     if (kb == nkb - 1)
@@ -385,12 +327,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         bool ok = true;
         for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
             int rt, vt;
-            if (kShareW)
-                wpair_tile_coords(tile, p, crank, rt, vt);
-            else if (kCluster == 2)
-                pair_tile_coords(tile, p, num_pairs, crank, rt, vt);
-            else
-                tile_coords(tile, p, rt, vt);
+            tile_coords(tile, p, rt, vt);
             const int row = rt * kBM + r_in_tile;
             const int v0 = vt * kVT;
             const bool row_ok = row < p.T;
@@ -543,7 +480,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ---------------------------------------------------------------- teardown
     tc_fence_before_sync();
     __syncthreads();
-    if (kCluster == 2) cluster_sync_all();  // no multicast or commit still targets this CTA
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, kTmemCols);

@@ -110,7 +110,6 @@ struct lp_handle {
     int leaf_len = 0;
     uint64_t timeout_ns = 0;
     CUtensorMap tmW{};
-    CUtensorMap tmW64{};  // the same W with 64-row boxes (W-sharing cluster pairs)
     double* host_scalars = nullptr;  // pinned host: D3 and n_valid of the host-buffer call
     // workspace (device)
     float2* ws_ms = nullptr;      // [num_lse_tiles][max_tokens]
@@ -157,12 +156,9 @@ struct lp_handle {
     cudaStream_t last_stream = nullptr;
     int64_t ws_bytes = 0;
     int32_t last_launches = 0;
-    // launch-layout switches read from the environment at init (LP_FORCE_SINGLE_CTA,
-    // LP_FORCE_SHORT_STAGES, LP_FORCE_SHARE_X); they change only the schedule, never the
-    // arithmetic, and let the tests prove that
-    bool force_single_cta = false;
+    // launch-layout switch read from the environment at init (LP_FORCE_SHORT_STAGES); it
+    // changes only the schedule, never the arithmetic, and lets the tests prove that
     bool force_sub1 = false;
-    bool force_share_x = false;
     int band = 0;  // vocabulary tiles per scheduling band (even); schedule only
     // profiling: event pairs around leaf-GEMM launches
     bool profiling = false;
@@ -207,26 +203,13 @@ int scheduling_band(int H, int bytes_per_weight, int max_tiles, int mib) {
     return static_cast<int>(b) & ~1;
 }
 
-template <int kMode, int kSub, int kCluster, bool kShareW = false>
+template <int kMode, int kSub>
 cudaError_t launch_gemm_variant(int grid, cudaStream_t st, const CUtensorMap& tmX,
                                 const CUtensorMap& tmW, const CUtensorMap& tmD,
                                 const lp::GemmParams& p) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(lp::kGemmThreads);
-    cfg.dynamicSmemBytes = lp::gemm_smem_bytes(kSub, kMode);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    if (kCluster > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = kCluster;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
-    return cudaLaunchKernelEx(&cfg, lp::leaf_gemm_kernel<kMode, kSub, kCluster, kShareW>, tmX,
-                              tmW, tmD, p);
+    lp::leaf_gemm_kernel<kMode, kSub>
+        <<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(kSub, kMode), st>>>(tmX, tmW, tmD, p);
+    return cudaGetLastError();
 }
 
 template <int kMode>
@@ -236,11 +219,8 @@ int set_gemm_attributes() {
                                     lp::gemm_smem_bytes(sub, kMode));
     };
     cudaError_t e;
-    if ((e = set(lp::leaf_gemm_kernel<kMode, 1, 1>, 1)) != cudaSuccess ||
-        (e = set(lp::leaf_gemm_kernel<kMode, 2, 1>, 2)) != cudaSuccess ||
-        (e = set(lp::leaf_gemm_kernel<kMode, 1, 2>, 1)) != cudaSuccess ||
-        (e = set(lp::leaf_gemm_kernel<kMode, 2, 2>, 2)) != cudaSuccess ||
-        (e = set(lp::leaf_gemm_kernel<kMode, 1, 2, true>, 1)) != cudaSuccess)
+    if ((e = set(lp::leaf_gemm_kernel<kMode, 1>, 1)) != cudaSuccess ||
+        (e = set(lp::leaf_gemm_kernel<kMode, 2>, 2)) != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute(leaf_gemm_kernel)");
     return LP_OK;
 }
@@ -253,13 +233,9 @@ struct GradArgs {
     int64_t ldd = 0;
 };
 
-// The leaf GEMM over `rows` rows of X starting at `X` (row stride ldx).  Calls with at least
-// one full 128-row tile run in clusters of two CTAs that share each X tile (multicast);
-// smaller (decode) calls run one CTA per tile with an X box cut to their rows.  Decode calls
-// of two row tiles (129-256 rows) pair the two row tiles of one vocabulary tile instead, so
-// each W tile is fetched once into one cluster (measured on GB300: 3 % faster than sharing X
-// at 129, 200 and 256 rows).  Stages are
-// 128 K deep (8 MMAs per barrier synchronisation) when the leaf length allows.  Launches of
+// The leaf GEMM over `rows` rows of X starting at `X` (row stride ldx), one CTA per
+// 128 x 128 tile; calls smaller than one row tile (decode) cut the X box to their rows.
+// Stages are 128 K deep (8 MMAs per barrier synchronisation) when the leaf length allows.  Launches of
 // at most kShortStageRows rows (decode batches) and odd leaf lengths take seven 64-K stages
 // instead: such launches read each W tile from DRAM for one or two row tiles, and the deeper
 // ring keeps 112 KB of W per CTA in flight instead of 96 KB (measured on GB300: decode
@@ -292,12 +268,8 @@ int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int lea
     p.ldd = ga.ldd;
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
-    const bool cluster = rows >= lp::kBM && h->num_vocab_tiles >= 2 && !h->force_single_cta;
     const bool sub2 = h->leaf_len % (2 * lp::kBK) == 0 && rows > kShortStageRows && !h->force_sub1;
-    // two row tiles of a decode batch: the pair shares each W tile instead of each X tile
-    const bool share_w = cluster && !sub2 && rows > lp::kBM && rows <= kShortStageRows &&
-                         !h->force_share_x;
-    p.x_box_rows = static_cast<int32_t>(cluster && !share_w ? lp::kBM / 2 : x_box_rows(rows));
+    p.x_box_rows = static_cast<int32_t>(x_box_rows(rows));
     CUtensorMap tmX;
     int rc = encode_kmajor(&tmX, X, static_cast<uint64_t>(rows), h->cfg.H, ldx,
                            static_cast<uint32_t>(p.x_box_rows));
@@ -308,24 +280,15 @@ int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int lea
         rc = encode_kmajor(&tmD, ga.dl, static_cast<uint64_t>(rows), h->cfg.V, ga.ldd, 32);
         if (rc != LP_OK) return rc;
     }
-    const int64_t pairs = ceil_div(h->num_vocab_tiles, 2);
-    const int64_t tiles =
-        share_w ? ceil_div(p.num_row_tiles, 2) * static_cast<int64_t>(h->num_vocab_tiles)
-                : static_cast<int64_t>(p.num_row_tiles) * (cluster ? pairs : h->num_vocab_tiles);
+    const int64_t tiles = static_cast<int64_t>(p.num_row_tiles) * h->num_vocab_tiles;
     if (tiles > 0x7fffffff) return fail(LP_ERR_UNSUPPORTED, "too many tiles in one launch");
-    const int64_t slots = cluster ? h->num_sms / 2 : h->num_sms;
-    const int grid = static_cast<int>((tiles < slots ? tiles : slots) * (cluster ? 2 : 1));
+    const int64_t slots = h->num_sms;
+    const int grid = static_cast<int>(tiles < slots ? tiles : slots);
     const bool prof = h->profiling && h->prof_used < kProfPairs;
     if (prof) LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used], st), "profile event");
     cudaError_t e;
-    if (share_w)
-        e = launch_gemm_variant<kMode, 1, 2, true>(grid, st, tmX, h->tmW64, tmD, p);
-    else if (cluster)
-        e = sub2 ? launch_gemm_variant<kMode, 2, 2>(grid, st, tmX, h->tmW, tmD, p)
-                 : launch_gemm_variant<kMode, 1, 2>(grid, st, tmX, h->tmW, tmD, p);
-    else
-        e = sub2 ? launch_gemm_variant<kMode, 2, 1>(grid, st, tmX, h->tmW, tmD, p)
-                 : launch_gemm_variant<kMode, 1, 1>(grid, st, tmX, h->tmW, tmD, p);
+    e = sub2 ? launch_gemm_variant<kMode, 2>(grid, st, tmX, h->tmW, tmD, p)
+             : launch_gemm_variant<kMode, 1>(grid, st, tmX, h->tmW, tmD, p);
     LP_CUDA(e, "leaf_gemm_kernel launch");
     LP_CUDA(cudaGetLastError(), "leaf_gemm_kernel launch");
     if (prof) {
@@ -626,9 +589,7 @@ int init_impl(const lp_config* cfg, const void* W, void* stream, lp_handle** out
         if (v > 0) timeout_ms = static_cast<uint64_t>(v);
     }
     h->timeout_ns = timeout_ms * 1000000ull;
-    if (const char* e = std::getenv("LP_FORCE_SINGLE_CTA")) h->force_single_cta = e[0] == '1';
     if (const char* e = std::getenv("LP_FORCE_SHORT_STAGES")) h->force_sub1 = e[0] == '1';
-    if (const char* e = std::getenv("LP_FORCE_SHARE_X")) h->force_share_x = e[0] == '1';
     h->band = scheduling_band(cfg->H, 2, 64, 32);
     if (const char* e = std::getenv("LP_BAND")) {
         const int b = std::atoi(e);
@@ -642,8 +603,6 @@ int init_impl(const lp_config* cfg, const void* W, void* stream, lp_handle** out
         return code;
     };
     rc = encode_kmajor(&h->tmW, W, static_cast<uint64_t>(cfg->V), cfg->H, cfg->H);
-    if (rc != LP_OK) return cleanup(rc);
-    rc = encode_kmajor(&h->tmW64, W, static_cast<uint64_t>(cfg->V), cfg->H, cfg->H, lp::kVT / 2);
     if (rc != LP_OK) return cleanup(rc);
 
     const int64_t mt = cfg->max_tokens;

@@ -177,45 +177,6 @@ __device__ __forceinline__ void tma_load_2d_elect(const CUtensorMap* map, uint64
         : "memory");
 }
 
-// Multicast variant: the box lands at the same shared-memory offset in every CTA of
-// `cta_mask` (this GPU's cluster), and each destination CTA's barrier at the same offset
-// receives the transaction bytes.
-__device__ __forceinline__ void tma_load_2d_mc_elect(const CUtensorMap* map, uint64_t* bar,
-                                                     void* dst, int32_t x, int32_t y,
-                                                     uint16_t cta_mask) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;\n\t}" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask)
-        : "memory");
-}
-
-// Arrive on the barrier at the same offset in every CTA of `cta_mask` when this thread's
-// tcgen05 operations so far complete.
-__device__ __forceinline__ void umma_commit_mc_elect(uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster"
-        ".b64 [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Every thread of every CTA in the cluster arrives, then waits for all of them.
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
-}
-
 __device__ __forceinline__ void umma_bf16_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                 uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -230,8 +191,7 @@ __device__ __forceinline__ void umma_bf16_elect(uint32_t d_tmem, uint64_t a_desc
 // One pipeline stage of MMAs from a single elected lane: 4 * kSub MMAs (kind::f16, K = 16),
 // the descriptors advanced by +32 bytes per K step inside a 64-K sub-block and by 16 KB
 // (1024 descriptor units) per sub-block, the first MMA with the caller's accumulate flag and
-// the rest accumulating, then the commit that frees the stage (multicast to both CTAs of a
-// cluster pair when kMc).  The same instructions as one elected MMA at a time, with one
+// the rest accumulating, then the commit that frees the stage.  The same instructions as one elected MMA at a time, with one
 // election per stage instead of one per instruction.
 #define LP_MMA_F16(A, B, P) "@e tcgen05.mma.cta_group::1.kind::f16 [%0], " A ", " B ", %3, " P ";\n\t"
 #define LP_ADV(OFF) "add.s64 a1, %1, " OFF ";\n\tadd.s64 b1, %2, " OFF ";\n\t"
@@ -245,26 +205,15 @@ __device__ __forceinline__ void umma_bf16_elect(uint32_t d_tmem, uint64_t a_desc
     "{\n\t.reg .pred e, p, t;\n\t.reg .b64 a1, b1;\n\t" \
     "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
 #define LP_COMMIT "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}"
-#define LP_COMMIT_MC                                                                            \
-    "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster" \
-    ".b64 [%5], %6;\n\t}"
 
-template <int kSub, bool kMc>
+template <int kSub>
 __device__ __forceinline__ void umma_stage_elect(uint32_t d_tmem, uint64_t a, uint64_t b,
                                                  uint32_t idesc, uint32_t accumulate,
-                                                 uint64_t* bar, uint16_t mask) {
+                                                 uint64_t* bar) {
     static_assert(kSub == 1 || kSub == 2, "stages hold one or two 64-K sub-blocks");
-    if constexpr (kSub == 2 && kMc) {
-        asm volatile(LP_STAGE_HEAD LP_STAGE_X4 LP_STAGE_X8_TAIL LP_COMMIT_MC ::"r"(d_tmem), "l"(a),
-                     "l"(b), "r"(idesc), "r"(accumulate), "r"(smem_u32(bar)), "h"(mask)
-                     : "memory");
-    } else if constexpr (kSub == 2) {
+    if constexpr (kSub == 2) {
         asm volatile(LP_STAGE_HEAD LP_STAGE_X4 LP_STAGE_X8_TAIL LP_COMMIT ::"r"(d_tmem), "l"(a),
                      "l"(b), "r"(idesc), "r"(accumulate), "r"(smem_u32(bar))
-                     : "memory");
-    } else if constexpr (kMc) {
-        asm volatile(LP_STAGE_HEAD LP_STAGE_X4 LP_COMMIT_MC ::"r"(d_tmem), "l"(a), "l"(b),
-                     "r"(idesc), "r"(accumulate), "r"(smem_u32(bar)), "h"(mask)
                      : "memory");
     } else {
         asm volatile(LP_STAGE_HEAD LP_STAGE_X4 LP_COMMIT ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc),
@@ -278,7 +227,6 @@ __device__ __forceinline__ void umma_stage_elect(uint32_t d_tmem, uint64_t a, ui
 #undef LP_STAGE_X8_TAIL
 #undef LP_STAGE_HEAD
 #undef LP_COMMIT
-#undef LP_COMMIT_MC
 
 __device__ __forceinline__ void umma_commit_elect(uint64_t* bar) {
     asm volatile(
