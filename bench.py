@@ -6,6 +6,9 @@ leaf tree and vocabulary-tile log-sum-exp, the combine and sampled-token gather
 (``lp_logprobs``), then the importance weights and D3 against a rollout logprob from
 a lagged weight copy (``lp_importance_weights``).  Inputs are seeded synthetic data
 already resident in HBM; W alone is larger than L2, so every step streams it from HBM.
+The default workload is the largest single-GPU one: the importance-weight batch of 512
+responses (about 2.07 M tokens, H 4096, V 151936); the same line then carries decode
+sub-records (H 7168, V 129280, batches 1 and 256), each with its own roofline.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -409,9 +412,9 @@ def run_backward(args, world, rank, local, pg):
     grad_ms = gemm_ms / max(1, gemm_n)
     per_launch = 2.0 * T * H * V / (gemm_n / max(1, args.steps))
     achieved = per_launch / (grad_ms / 1000.0) / 1e12
-    peak = float(peaks["bf16_tflops_sustained"])
+    peak, src = tensor_peak(peaks, peak_src, ms * args.steps / 1000.0, False)
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "peak_source": f"{peak_src} bf16_tflops_sustained",
+            "frac": achieved / peak, "peak_source": src,
             "traffic": None, "kernel": "leaf_gemm_kernel<gradient epilogue>",
             "kernel_ms": grad_ms, "algorithmic_per_launch": per_launch}
     cpu = None
@@ -446,6 +449,124 @@ def run_backward(args, world, rank, local, pg):
 
 
 # ----------------------------------------------------------------------------- our arm
+BURST_SECONDS = 1.0  # a timed region shorter than this is a burst: the burst bf16 peak applies
+IS_BYTES_PER_TOKEN = 12  # lp_importance_weights: reads log pi and log mu, writes w (fp32)
+
+
+def tensor_peak(peaks, peak_src, timed_s: float, fp8: bool):
+    """The bf16 (x 2 for fp8) tensor peak that matches the timed region: the burst figure for
+    a region under BURST_SECONDS, the sustained (power-capped) figure for a longer one."""
+    key = "bf16_tflops_sustained" if timed_s >= BURST_SECONDS else "bf16_tflops"
+    peak = float(peaks[key])
+    src = f"{peak_src} {key} (timed region {timed_s:.2f} s)"
+    if fp8:  # dense fp8 = 2 x bf16 (nominal 4.5 / 2.25 PFLOP/s)
+        peak *= 2.0
+        src += " x 2, the nominal fp8/bf16 ratio"
+    return peak, src
+
+
+def forward_roofline(workload, fp8, T, H, V, gemm_avg_ms, launches_per_step, timed_s):
+    """Roofline record of the dominant kernel (the fused leaf GEMM) of one forward step."""
+    peaks, peak_src = load_peaks()
+    if workload == "ds_decode":
+        # HBM-bound: W streamed once per step plus X and the per-tile partials.
+        nb = (V + 63) // 64  # (max, sum-exp) partial per 64-column tile
+        wbytes = H * V + 4 * ((V + 127) // 128) * (H // 128) if fp8 else 2 * H * V
+        xbytes = T * H + 4 * T * (H // 128) if fp8 else 2 * T * H
+        algo = (wbytes + xbytes + 8 * T * nb + 8 * T) / launches_per_step
+        achieved = algo / (gemm_avg_ms / 1000.0) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": f"{peak_src} hbm_gbs",
+                "algorithmic_per_launch": algo, "kernel_ms": gemm_avg_ms}
+    algo = 2.0 * T * H * V / launches_per_step
+    achieved = algo / (gemm_avg_ms / 1000.0) / 1e12
+    peak, src = tensor_peak(peaks, peak_src, timed_s, fp8)
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "peak_source": src, "algorithmic_per_launch": algo,
+            "kernel_ms": gemm_avg_ms}
+
+
+def time_forward(eng, X, ids, mu, phase, steps, warmup, entropy, dev, local, pg):
+    """Warm up, then time `steps` forward steps (logprobs [+ entropy] + importance weights)
+    with CUDA events on the launching stream, the leaf GEMM bracketed by the library's
+    profiling events and the importance-weight call by events of its own."""
+    import torch
+
+    T = X.shape[0]
+    logp = torch.empty(T, dtype=torch.float32, device=dev)
+    w = torch.empty(T, dtype=torch.float32, device=dev)
+    d3 = torch.empty(1, dtype=torch.float64, device=dev)
+    nv = torch.empty(1, dtype=torch.int64, device=dev)
+    ent = torch.empty(T, dtype=torch.float32, device=dev) if entropy else None
+    logz = torch.empty(T, dtype=torch.float32, device=dev) if entropy else None
+    stream = torch.cuda.current_stream()
+    launches = [0]
+    is_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(steps)]
+
+    def step(k=None):
+        if entropy:
+            eng.logprobs_entropy(X, ids, out=logp, out_logZ=logz, out_entropy=ent, phase=phase)
+        else:
+            eng.logprobs(X, ids, out=logp, phase=phase)
+        launches[0] += eng.last_launch_count
+        if k is not None:
+            is_ev[k][0].record(stream)
+        eng.importance_weights(logp, mu, out_w=w, out_d3=d3, out_nvalid=nv)
+        if k is not None:
+            is_ev[k][1].record(stream)
+        launches[0] += eng.last_launch_count
+
+    for _ in range(warmup):
+        step()
+    eng.check()
+    torch.cuda.synchronize()
+    launches[0] = 0
+    eng.profile_enable(True)
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    barrier(pg, dev)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(steps):
+        step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg, dev)
+    clocks = sampler.stop()
+    gemm_ms, gemm_n = eng.profile_read()
+    eng.profile_enable(False)
+    eng.check()
+    ms = e0.elapsed_time(e1) / steps
+    is_ms = sum(a.elapsed_time(b) for a, b in is_ev) / steps
+    return {"ms": ms, "ms_max": max_over_ranks(pg, ms, dev), "gemm_ms": gemm_ms,
+            "gemm_n": gemm_n, "is_ms": is_ms, "launches": launches[0], "clocks": clocks}
+
+
+def decode_subrecord(args, batch, rank, dev, local, pg):
+    """One decode batch of the DeepSeek-like shape (H 7168, V 129280, N 8), timed like the
+    main line: its tokens/s and the leaf GEMM's HBM roofline."""
+    from bit_consistent_logprob_gb300 import Engine, LP_PHASE_DECODE
+
+    wl, _, X, W, ids = make_workload("ds_decode", dev, seed_offset=rank, batch=batch)
+    mu = rollout_logprobs(W, X, ids, wl, wl.seed + rank, batch)
+    steps = max(args.steps, 500)  # a decode step is ~0.3 ms: enough steps for clock samples
+    with Engine(W, n_leaves=wl.n_leaves, max_tokens=batch) as eng:
+        r = time_forward(eng, X, ids, mu, LP_PHASE_DECODE, steps, args.warmup, False, dev,
+                         local, pg)
+    gemm_avg = r["gemm_ms"] / max(1, r["gemm_n"])
+    roof = forward_roofline("ds_decode", False, batch, wl.H, wl.V, gemm_avg,
+                            r["gemm_n"] / steps, r["ms"] * steps / 1000.0)
+    roof["traffic"] = recorded_traffic(f"ds_decode_b{batch}")
+    roof["kernel"] = "leaf_gemm_kernel<fused>"
+    return {"workload": "ds_decode", "batch": batch, "H": wl.H, "V": wl.V,
+            "n_leaves": wl.n_leaves, "steps": steps,
+            "value": batch / (r["ms_max"] / 1000.0), "unit": UNIT, "ms_per_step": r["ms_max"],
+            "roofline": roof, "gpu_launches": r["launches"], "clocks": r["clocks"]}
+
+
 def run_ours(args, world, rank, local, pg):
     import torch
 
@@ -460,49 +581,9 @@ def run_ours(args, world, rank, local, pg):
     mu = rollout_logprobs(W, X, ids, wl, wl.seed + rank, max_tokens)
     eng = Engine(W, n_leaves=N, max_tokens=max_tokens, fp8=args.fp8)
     phase = LP_PHASE_DECODE if args.workload == "ds_decode" else LP_PHASE_PREFILL
-    logp = torch.empty(T, dtype=torch.float32, device=dev)
-    w = torch.empty(T, dtype=torch.float32, device=dev)
-    d3 = torch.empty(1, dtype=torch.float64, device=dev)
-    nv = torch.empty(1, dtype=torch.int64, device=dev)
-    stream = torch.cuda.current_stream()
-    launches = [0]
-
-    ent = torch.empty(T, dtype=torch.float32, device=dev) if args.entropy else None
-    logz = torch.empty(T, dtype=torch.float32, device=dev) if args.entropy else None
-
-    def step():
-        if args.entropy:
-            eng.logprobs_entropy(X, ids, out=logp, out_logZ=logz, out_entropy=ent, phase=phase)
-        else:
-            eng.logprobs(X, ids, out=logp, phase=phase)
-        launches[0] += eng.last_launch_count
-        eng.importance_weights(logp, mu, out_w=w, out_d3=d3, out_nvalid=nv)
-        launches[0] += eng.last_launch_count
-
-    for _ in range(args.warmup):
-        step()
-    eng.check()
-    torch.cuda.synchronize()
-    launches[0] = 0
-    eng.profile_enable(True)
-    sampler = ClockSampler(local)
-    time.sleep(0.3)
-    barrier(pg, dev)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(pg, dev)
-    clocks = sampler.stop()
-    gemm_ms, gemm_n = eng.profile_read()
-    eng.profile_enable(False)
-    eng.check()
-    ms = e0.elapsed_time(e1) / args.steps
-    ms_max = max_over_ranks(pg, ms, dev)
-    gpu_launches = launches[0]
+    r = time_forward(eng, X, ids, mu, phase, args.steps, args.warmup, args.entropy, dev, local,
+                     pg)
+    ms_max = r["ms_max"]
 
     # end to end through the public API with host buffers (pinned), copies in the region
     e2e = None
@@ -531,49 +612,49 @@ def run_ours(args, world, rank, local, pg):
         bo = T * 4 + T * 4 + 16
         e2e = {"value": world * T / (e2e_ms / 1000.0), "unit": UNIT, "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+        del Xh
 
-    peaks, peak_src = load_peaks()
-    gemm_avg_ms = gemm_ms / max(1, gemm_n)
-    launches_per_step = gemm_n / max(1, args.steps)
-    if args.workload == "ds_decode":
-        # HBM-bound: W streamed once per step plus X and the per-tile partials.
-        nb = (V + 63) // 64  # (max, sum-exp) partial per 64-column tile
-        wbytes = H * V + 4 * ((V + 127) // 128) * (H // 128) if args.fp8 else 2 * H * V
-        xbytes = T * H + 4 * T * (H // 128) if args.fp8 else 2 * T * H
-        algo = (wbytes + xbytes + 8 * T * nb + 8 * T) / launches_per_step
-        achieved = algo / (gemm_avg_ms / 1000.0) / 1e9
-        peak = float(peaks["hbm_gbs"])
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "peak_source": f"{peak_src} hbm_gbs"}
-    else:
-        algo = 2.0 * T * H * V / launches_per_step
-        achieved = algo / (gemm_avg_ms / 1000.0) / 1e12
-        peak = float(peaks["bf16_tflops_sustained"])
-        src = (f"{peak_src} bf16_tflops_sustained (kernel timed inside a back-to-back step "
-               f"loop)")
-        if args.fp8:  # dense fp8 = 2 x bf16 (nominal 4.5 / 2.25 PFLOP/s)
-            peak *= 2.0
-            src = f"{src} x 2, the nominal fp8/bf16 ratio"
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "peak_source": src}
+    gemm_avg_ms = r["gemm_ms"] / max(1, r["gemm_n"])
+    timed_s = r["ms"] * args.steps / 1000.0
+    roof = forward_roofline(args.workload, args.fp8, T, H, V, gemm_avg_ms,
+                            r["gemm_n"] / max(1, args.steps), timed_s)
     key = args.workload + ("_fp8" if args.fp8 else "") + ("_entropy" if args.entropy else "")
     if args.workload == "ds_decode":
         key += f"_b{args.batch}"
     roof["traffic"] = recorded_traffic(key)
     roof["kernel"] = ("leaf_gemm_fp8_kernel" if args.fp8 else
                       "leaf_gemm_kernel<fused, entropy>" if args.entropy else "leaf_gemm_kernel<fused>")
-    roof["kernel_ms"] = gemm_avg_ms
-    roof["algorithmic_per_launch"] = algo
+    roof["timed_region_s"] = timed_s
+    roof["launches_per_step"] = r["gemm_n"] / max(1, args.steps)
+
+    # the importance-weight epilogue's own bandwidth: 12 bytes per token against HBM
+    peaks, peak_src = load_peaks()
+    is_algo = IS_BYTES_PER_TOKEN * T + 16
+    is_gbs = is_algo / (r["is_ms"] / 1000.0) / 1e9
+    epilogue = {"kernel": "lp_importance_weights (is_block_kernel + is_final_kernel)",
+                "bound": "hbm", "achieved": is_gbs, "peak": float(peaks["hbm_gbs"]),
+                "unit": "GB/s", "frac": is_gbs / float(peaks["hbm_gbs"]),
+                "peak_source": f"{peak_src} hbm_gbs", "kernel_ms": r["is_ms"],
+                "algorithmic_per_launch": is_algo,
+                "note": f"{is_algo / 1e6:.1f} MB per call; log pi was just written by the "
+                        "combine, so part of the stream may come from L2 (129 MB)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.fp8:
         cpu = cpu_baseline(X, W, ids, mu, wl, rows=args.cpu_rows)
     eng.close()
+    del X, W, ids, mu
+    torch.cuda.empty_cache()
+
+    decode = None
+    if args.decode_batches and not args.fp8 and not args.entropy and args.workload != "ds_decode":
+        decode = [decode_subrecord(args, int(b), rank, dev, local, pg)
+                  for b in args.decode_batches.split(",")]
 
     if rank != 0:
         return None
     value = world * T / (ms_max / 1000.0)
-    return {
+    line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 block-FP8" if args.fp8 else "bf16",
@@ -581,12 +662,16 @@ def run_ours(args, world, rank, local, pg):
         "config": {"workload": wl.name + ("+fp8" if args.fp8 else ""), "T": T, "H": H, "V": V, "n_leaves": N,
                    "n_seqs": len(lengths), "phase": "decode" if phase == LP_PHASE_DECODE else "prefill",
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                   "row_chunk": max_tokens,
                    "l2": f"inputs larger than L2 (W {2 * H * V / 1e6:.0f} MB streamed every step)",
                    "step": ("lp_logprobs_entropy" if args.entropy else "lp_logprobs")
                            + " + lp_importance_weights"},
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
-        "clocks": clocks,
+        "roofline": roof, "epilogue": epilogue, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": r["launches"], "clocks": r["clocks"],
     }
+    if decode is not None:
+        line["decode"] = decode
+    return line
 
 
 def cpu_baseline(X, W, ids, mu, wl, rows: int):
@@ -717,7 +802,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="qwen_prefill",
+    ap.add_argument("--workload", default="is_d3",
                     choices=("tiny", "qwen_prefill", "ds_prefill", "ds_decode", "is_d3",
                              "rl_epilogue"))
     ap.add_argument("--batch", type=int, default=128, help="rows of the decode workload")
@@ -725,6 +810,9 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=128, help="rows of the CPU-baseline sample")
     ap.add_argument("--ref-step-seconds", type=float, default=1.5)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--decode-batches", default="1,256",
+                    help="decode batches (DeepSeek-like shape) timed after a prefill workload "
+                         "and reported in the same line; empty to skip")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--entropy", action="store_true",
                     help="the step also forms each row's softmax entropy (lp_logprobs_entropy)")

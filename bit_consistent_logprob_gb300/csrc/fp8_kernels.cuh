@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
             int rt, vt;
-            tile_coords(tile, p, rt, vt);
+            tile_coords(tile, p.num_row_tiles, p, rt, vt);
             const int row0 = rt * kBM, v0 = vt * kVT;
             for (int kb = kb0; kb < kb0 + nkb_range; ++kb) {
                 ok = __all_sync(kFull, mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns));
@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int npairs = n >> 1;
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
             int rt, vt;
-            tile_coords(tile, p, rt, vt);
+            tile_coords(tile, p.num_row_tiles, p, rt, vt);
             const int row = rt * kBM + r_in_tile;
             const int v0 = vt * kVT;
             const bool row_ok = row < p.T;

@@ -85,27 +85,41 @@ __host__ __device__ constexpr int kNumBars(int stages) { return 2 * stages + 2 *
 // that stream W from DRAM.
 // The gradient epilogue stages each warp's 32 x 64 bf16 block of dl in shared memory for a TMA
 // store (8 warps: 32 KB), so its 64-K ring has six stages instead of seven.
+// A CTA of a pair (cta_group::2, below) loads only 64 of the vocabulary tile's 128 W rows, so
+// its stages are 24 KB per 64-K sub-block instead of 32 KB and its ring holds more of them:
+// four 128-K stages or nine 64-K stages (eight beside the gradient staging).
 constexpr int kGradWarpBytes = 32 * kLT * 2;
 constexpr int kGradStageBytes = kEpiWarps * kGradWarpBytes;
-__host__ __device__ constexpr int gemm_stages(int sub, int mode = kModeLse) {
-    return sub == 1 ? (mode == kModeGrad ? 6 : 7) : 3;
+constexpr int kHalfTileBytes = (kVT / 2) * kBK * 2;  // 8 KB: 64 W rows x 64 K
+__host__ __device__ constexpr int gemm_stages(int sub, int mode = kModeLse, bool pair = false) {
+    return pair ? (sub == 1 ? (mode == kModeGrad ? 8 : 9) : 4)
+                : (sub == 1 ? (mode == kModeGrad ? 6 : 7) : 3);
 }
 
-__host__ __device__ constexpr int gemm_smem_bytes(int sub, int mode = kModeLse) {
-    return 1024 /* alignment slack */ + gemm_stages(sub, mode) * sub * 2 * kTileBytes +
-           (mode == kModeGrad ? kGradStageBytes : 0) + kNumBars(gemm_stages(sub, mode)) * 8 +
+// Bytes of one pipeline stage, both operands.
+__host__ __device__ constexpr int gemm_stage_bytes(int sub, bool pair = false) {
+    return sub * (kTileBytes + (pair ? kHalfTileBytes : kTileBytes));
+}
+
+__host__ __device__ constexpr int gemm_smem_bytes(int sub, int mode = kModeLse, bool pair = false) {
+    return 1024 /* alignment slack */ + gemm_stages(sub, mode, pair) * gemm_stage_bytes(sub, pair) +
+           (mode == kModeGrad ? kGradStageBytes : 0) + kNumBars(gemm_stages(sub, mode, pair)) * 8 +
            16 /* TMEM address, abort flag */;
 }
 static_assert(gemm_smem_bytes(1, kModeGrad) <= 227 * 1024 &&
-                  gemm_smem_bytes(2, kModeGrad) <= 227 * 1024 && gemm_smem_bytes(1) <= 227 * 1024,
+                  gemm_smem_bytes(2, kModeGrad) <= 227 * 1024 && gemm_smem_bytes(1) <= 227 * 1024 &&
+                  gemm_smem_bytes(1, kModeGrad, true) <= 227 * 1024 &&
+                  gemm_smem_bytes(2, kModeGrad, true) <= 227 * 1024 &&
+                  gemm_smem_bytes(1, kModeLse, true) <= 227 * 1024,
               "leaf-GEMM shared memory exceeds the per-CTA limit");
 
 // Tile schedule: the vocabulary is cut into bands of `band` tiles; within a band the
-// tiles run row tile by row tile, vocabulary fastest.  Concurrent CTAs therefore share
-// the band's W tiles and a few X row tiles in L2.  The schedule decides only which
-// CTA computes a tile, never how.
-__device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& rt, int& vt) {
-    const int per_band = p.num_row_tiles * p.band;
+// tiles run row by row (a row tile, or the two row tiles of a CTA pair), vocabulary fastest.
+// Concurrent CTAs therefore share the band's W tiles and a few X row tiles in L2.  The
+// schedule decides only which CTA computes a tile, never how.
+__device__ __forceinline__ void tile_coords(int tile, int num_rows, const GemmParams& p, int& rt,
+                                            int& vt) {
+    const int per_band = num_rows * p.band;
     const int b = tile / per_band;
     const int r = tile - b * per_band;
     const int vt0 = b * p.band;
@@ -114,45 +128,84 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& 
     vt = vt0 + (r - rt * width);
 }
 
+// A wait ran out: stop this CTA's warps (and, in a pair, the partner's) and record it.
+template <bool kPair = false>
 __device__ __forceinline__ void raise_timeout(const GemmParams& p, volatile int* abort_flag) {
     *abort_flag = 1;
+    if constexpr (kPair)
+        st_cluster_u32(cluster_addr(const_cast<int*>(abort_flag), cluster_ctarank() ^ 1u), 1u);
     atomicOr(p.status, kStatusTimeout);
+}
+
+// Bounded wait on a barrier and its non-blocking probe.  A pair's barriers also receive
+// arrivals (and commits) from the partner CTA: the arriving side releases at cluster scope,
+// and the waiting side keeps the CTA-scope acquire of every other wait.
+template <bool kPair>
+__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         uint64_t timeout_ns) {
+    return mbar_wait(bar, parity, abort_flag, timeout_ns);
+}
+
+template <bool kPair>
+__device__ __forceinline__ bool bar_test(uint64_t* bar, uint32_t parity) {
+    return mbar_test_wait(bar, parity);
 }
 
 // Number of trailing one bits of x.
 __device__ __forceinline__ int trailing_ones(int x) { return __ffs(~x) - 1; }
 
 // Warp-uniform bounded wait; on failure raises the abort flag (lane 0) and returns false.
+template <bool kPair = false>
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const GemmParams& p,
                                           volatile int* abort_flag) {
-    bool got = mbar_wait(bar, parity, abort_flag, p.timeout_ns);
+    bool got = bar_wait<kPair>(bar, parity, abort_flag, p.timeout_ns);
     got = __all_sync(0xffffffffu, got);
-    if (!got && (threadIdx.x & 31) == 0) raise_timeout(p, abort_flag);
+    if (!got && (threadIdx.x & 31) == 0) raise_timeout<kPair>(p, abort_flag);
     return got;
 }
 
-// Release a TMEM buffer to the MMA warp: this warp's loads from it have completed.
+// Release a TMEM buffer to the MMA warp: this warp's loads from it have completed.  In a pair
+// the MMA warp is the even CTA's, so both CTAs' warps arrive on its barrier.
+template <bool kPair = false>
 __device__ __forceinline__ void release_buf(uint64_t* bar) {
     tc_fence_before_sync();
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+    if ((threadIdx.x & 31) == 0) {
+        if constexpr (kPair)
+            mbar_arrive_cluster(cluster_addr(bar, 0));
+        else
+            mbar_arrive(bar);
+    }
 }
 
-// One CTA per 128 x 128 tile; each CTA loads its own X and W boxes.
+// kPair = false: one CTA per 128 x 128 tile; each CTA loads its own X and W boxes.
+// kPair = true: clusters of two CTAs (a pair) compute the two row tiles 2*rp and 2*rp + 1 of
+// one vocabulary tile with tcgen05.mma.cta_group::2 (M = 256).  Each CTA loads its own
+// 128-row X box and 64 of the tile's 128 W rows (tmW then has 64-row boxes) into its own
+// shared memory and its own barrier; nothing is multicast.  The even CTA (the leader) issues
+// the MMAs, which read both CTAs' shared memory and write each CTA's 128 rows of the
+// accumulator into that CTA's TMEM; the odd CTA's MMA warp forwards its stage completions to
+// the leader (one remote arrive per stage); the leader's commits free the stages and
+// publish the accumulators in both CTAs (one commit per CTA's barrier), and both CTAs'
+// epilogue warps release the TMEM buffers on the leader's barrier.  A CTA whose row tile lies
+// past T still loads (zero-filled rows) and computes, but writes nothing.  Every element sees
+// the same K = 16 MMA sequence, leaf tree and tile log-sum-exp as with one CTA per tile.
 // tmD (kModeGrad only): dl as bf16 [T][ldd] with 64 x 32 boxes, 128-byte swizzle.
-template <int kMode, int kSub>
+template <int kMode, int kSub, bool kPair = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     leaf_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
-    constexpr int kStages = gemm_stages(kSub, kMode);
-    constexpr int kStageBytes = kSub * kTileBytes;       // one operand, one stage
+    constexpr int kStages = gemm_stages(kSub, kMode, kPair);
+    constexpr int kBTile = kPair ? kHalfTileBytes : kTileBytes;  // W bytes per 64-K sub-block
+    constexpr int kStageA = kSub * kTileBytes;           // X bytes per stage
+    constexpr int kStageB = kSub * kBTile;               // W bytes per stage
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;                                  // X  [kStages][kSub][128 x 64] bf16
-    uint8_t* sB = smem + kStages * kStageBytes;          // W  [kStages][kSub][128 x 64] bf16
-    uint8_t* sD = smem + 2 * kStages * kStageBytes;      // dl staging [8 warps][32 x 64] bf16
+    uint8_t* sB = smem + kStages * kStageA;              // W  [kStages][kSub][128|64 x 64] bf16
+    uint8_t* sD = sB + kStages * kStageB;                // dl staging [8 warps][32 x 64] bf16
     uint64_t* bars = reinterpret_cast<uint64_t*>(
         sD + (kMode == kModeGrad ? kGradStageBytes : 0));
     uint64_t* full = bars;                               // TMA -> MMA, per stage
@@ -165,15 +218,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t crank = kPair ? cluster_ctarank() : 0u;
+    const bool leader = crank == 0u;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
+            // the leader's stage is ready when its own copies landed and the partner forwarded
+            // the completion of its copies
+            mbar_init(&full[s], kPair && leader ? 2 : 1);
             mbar_init(&empty[s], 1);  // the MMA commit that frees the stage
         }
         for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], kEpiWarps);  // every epilogue warp reads every buffer
+            // every epilogue warp (of both CTAs of a pair) reads every buffer
+            mbar_init(&acc_empty[b], kPair ? 2 * kEpiWarps : kEpiWarps);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -184,49 +242,58 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tma_prefetch_desc(&tmW);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_holder, kTmemCols);
-        tmem_relinquish();
+        if constexpr (kPair) {
+            tmem_alloc_pair(tmem_holder, kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_holder, kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (kPair) cluster_sync_all();  // the partner's barriers exist before any signal
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
 
-    const int num_tiles = p.num_row_tiles * p.num_vocab_tiles;
-    const int tile0 = static_cast<int>(blockIdx.x);
-    const int tile_step = static_cast<int>(gridDim.x);
+    // scheduling rows: row tiles, or row-tile pairs
+    const int num_rows = kPair ? (p.num_row_tiles + 1) >> 1 : p.num_row_tiles;
+    const int num_tiles = num_rows * p.num_vocab_tiles;
+    const int tile0 = static_cast<int>(kPair ? blockIdx.x >> 1 : blockIdx.x);
+    const int tile_step = static_cast<int>(kPair ? gridDim.x >> 1 : gridDim.x);
     const int nkb = p.leaf_len / (kBK * kSub);   // stages per leaf
     const int n = p.leaf_count;
 
     constexpr uint32_t kFull = 0xffffffffu;
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer (warp)
-        const uint32_t tx_bytes =
-            static_cast<uint32_t>(kSub * (p.x_box_rows * kBK * 2 + kTileBytes));
+        const uint32_t tx_bytes = static_cast<uint32_t>(kSub * (p.x_box_rows * kBK * 2 + kBTile));
         uint32_t stage = 0, phase = 0;
         uint64_t issued = 0;
         bool ok = true;
         for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
             int rt, vt;
-            tile_coords(tile, p, rt, vt);
-            const int row0 = rt * kBM, v0 = vt * kVT;
+            tile_coords(tile, num_rows, p, rt, vt);
+            if constexpr (kPair) rt = 2 * rt + static_cast<int>(crank);
+            const int row0 = rt * kBM;
+            const int w0 = vt * kVT + static_cast<int>(crank) * (kVT / 2);  // this CTA's W rows
             for (int jj = 0; ok && jj < n; ++jj) {
                 const int kbase = (p.leaf_begin + jj) * p.leaf_len;
                 for (int kb = 0; kb < nkb; ++kb) {
-                    ok = __all_sync(kFull,
-                                    mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns));
+                    ok = __all_sync(kFull, bar_wait<kPair>(&empty[stage], phase ^ 1u, abort_flag,
+                                                           p.timeout_ns));
                     if (!ok) {
-                        if (lane == 0) raise_timeout(p, abort_flag);
+                        if (lane == 0) raise_timeout<kPair>(p, abort_flag);
                         break;
                     }
                     mbar_arrive_expect_tx_elect(&full[stage], tx_bytes);
 #pragma unroll
                     for (int u = 0; u < kSub; ++u) {
                         const int k0 = kbase + (kb * kSub + u) * kBK;
-                        uint8_t* xdst = sA + stage * kStageBytes + u * kTileBytes;
-                        uint8_t* wdst = sB + stage * kStageBytes + u * kTileBytes;
+                        uint8_t* xdst = sA + stage * kStageA + u * kTileBytes;
+                        uint8_t* wdst = sB + stage * kStageB + u * kBTile;
                         tma_load_2d_elect(&tmX, &full[stage], xdst, k0, row0);
-                        tma_load_2d_elect(&tmW, &full[stage], wdst, k0, v0);
+                        tma_load_2d_elect(&tmW, &full[stage], wdst, k0, w0);
                     }
                     ++issued;
                     if (++stage == kStages) {
@@ -237,12 +304,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
         }
         if (!ok) {
-            // Let the copies already in flight land before the CTA exits.
+            // Let the copies already in flight land before the CTA exits.  (A leader's stage
+            // also counts the partner's forwarded arrival; if that never comes the wait runs
+            // to its limit, long after the copies themselves have landed.)
             const uint64_t first = issued > kStages ? issued - kStages : 0;
             for (uint64_t i = first; i < issued; ++i) {
                 volatile int never = 0;
                 mbar_wait(&full[i % kStages], static_cast<uint32_t>((i / kStages) & 1u), &never,
                           p.timeout_ns);
+            }
+        }
+    } else if (kPair && warp == 1 && !leader) {
+        // ------------------------------------------------------------ forwarder (odd CTA)
+        // Each time this CTA's copies of a stage have landed, arrive on the leader's barrier of
+        // that stage (the leader's MMAs read this CTA's shared memory).  The stage sequence is
+        // the producer's.
+        const uint32_t full_leader = cluster_addr(full, 0);
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
+            for (int jj = 0; ok && jj < n; ++jj) {
+                for (int kb = 0; kb < nkb; ++kb) {
+                    ok = __all_sync(kFull, mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns));
+                    if (!ok) {
+                        if (lane == 0) raise_timeout<kPair>(p, abort_flag);
+                        break;
+                    }
+                    if (lane == 0) mbar_arrive_cluster(full_leader + 8u * stage);
+                    __syncwarp();
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
             }
         }
     } else if (warp == 1) {
@@ -253,20 +347,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // of the next leaf's buffer are probed (non-blocking) while this stage's MMAs run.
         const uint64_t descA = sw128_kmajor_desc(smem_u32(sA));
         const uint64_t descB = sw128_kmajor_desc(smem_u32(sB));
-        constexpr uint32_t kStageDesc = kStageBytes >> 4;  // descriptor units per stage
-        constexpr uint32_t kSubDesc = kTileBytes >> 4;     // ... per 64-K sub-block
+        constexpr uint32_t kStageDescA = kStageA >> 4;  // descriptor units per stage
+        constexpr uint32_t kStageDescB = kStageB >> 4;
+        constexpr uint32_t kSubDesc = kTileBytes >> 4;  // ... per 64-K sub-block of X
+        constexpr uint32_t kIdescRun = kPair ? idesc_bf16_f32(2 * kBM, kVT) : kIdesc;
+        // the barriers a pair's commits arrive on: this CTA's and the partner's
+        const uint32_t empty_own = smem_u32(empty), empty_peer = kPair ? cluster_addr(empty, 1) : 0u;
+        const uint32_t accf_own = smem_u32(acc_full),
+                       accf_peer = kPair ? cluster_addr(acc_full, 1) : 0u;
         uint32_t stage = 0, phase = 0;
         uint32_t buf = 0, bphase = 0;  // TMEM buffer of the current leaf, its use parity
         bool ok = true;
-        bool ready = __all_sync(kFull, mbar_test_wait(&full[0], 0));
+        bool ready = __all_sync(kFull, bar_test<kPair>(&full[0], 0));
         bool acc_ready = true;  // the first uses of every buffer find it free
         for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
             for (int jj = 0; ok && jj < n; ++jj) {
                 if (!acc_ready) {
-                    ok = __all_sync(kFull, mbar_wait(&acc_empty[buf], bphase ^ 1u, abort_flag,
-                                                     p.timeout_ns));
+                    ok = __all_sync(kFull, bar_wait<kPair>(&acc_empty[buf], bphase ^ 1u,
+                                                           abort_flag, p.timeout_ns));
                     if (!ok) {
-                        if (lane == 0) raise_timeout(p, abort_flag);
+                        if (lane == 0) raise_timeout<kPair>(p, abort_flag);
                         break;
                     }
                 }
@@ -276,34 +376,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t nbphase = buf + 1 == kAccBufs ? bphase ^ 1u : bphase;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!ready) {
-                        ok = __all_sync(kFull,
-                                        mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns));
+                        ok = __all_sync(kFull, bar_wait<kPair>(&full[stage], phase, abort_flag,
+                                                               p.timeout_ns));
                         if (!ok) {
-                            if (lane == 0) raise_timeout(p, abort_flag);
+                            if (lane == 0) raise_timeout<kPair>(p, abort_flag);
                             break;
                         }
                     }
                     tc_fence_after_sync();
                     const uint32_t nstage = stage + 1 == kStages ? 0u : stage + 1;
                     const uint32_t nphase = stage + 1 == kStages ? phase ^ 1u : phase;
-                    const uint64_t a = descA + stage * kStageDesc;
-                    const uint64_t b = descB + stage * kStageDesc;
+                    const uint64_t a = descA + stage * kStageDescA;
+                    const uint64_t b = descB + stage * kStageDescB;
                     // +32 bytes (2 descriptor units) per K step of 16 bf16 inside a row;
                     // only the leaf's very first MMA starts a fresh accumulator; the commit
-                    // frees the stage
+                    // frees the stage (in a pair: in both CTAs)
                     static_assert(kSubDesc == 1024, "sub-block stride assumed by the stage issue");
-                    umma_stage_elect<kSub>(d_tmem, a, b, kIdesc, kb != 0 ? 1u : 0u,
-                                           &empty[stage]);
+                    if constexpr (kPair)
+                        umma_pair_stage_elect<kSub>(d_tmem, a, b, kIdescRun, kb != 0 ? 1u : 0u,
+                                                    empty_own + 8u * stage,
+                                                    empty_peer + 8u * stage);
+                    else
+                        umma_stage_elect<kSub>(d_tmem, a, b, kIdescRun, kb != 0 ? 1u : 0u,
+                                               &empty[stage]);
                     // probe the next stage (and the next leaf's buffer) while these MMAs run
-                    ready = __all_sync(kFull, mbar_test_wait(&full[nstage], nphase));
+                    ready = __all_sync(kFull, bar_test<kPair>(&full[nstage], nphase));
                     if (kb == nkb - 1)
                         acc_ready =
-                            __all_sync(kFull, mbar_test_wait(&acc_empty[nbuf], nbphase ^ 1u));
+                            __all_sync(kFull, bar_test<kPair>(&acc_empty[nbuf], nbphase ^ 1u));
                     stage = nstage;
                     phase = nphase;
                 }
                 if (!ok) break;
-                umma_commit_elect(&acc_full[buf]);
+                if constexpr (kPair)
+                    umma_commit2_pair_elect(accf_own + 8u * buf, accf_peer + 8u * buf);
+                else
+                    umma_commit_elect(&acc_full[buf]);
                 buf = nbuf;
                 bphase = nbphase;
             }
@@ -311,7 +419,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!ok) {
             // Wait for every MMA already issued before TMEM is released.
             volatile int never = 0;
-            umma_commit_elect(drain);
+            if constexpr (kPair)
+                umma_commit_pair_elect(smem_u32(drain));
+            else
+                umma_commit_elect(drain);
             mbar_wait(drain, 0, &never, p.timeout_ns);
         }
     } else {
@@ -327,7 +438,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         bool ok = true;
         for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
             int rt, vt;
-            tile_coords(tile, p, rt, vt);
+            tile_coords(tile, num_rows, p, rt, vt);
+            if constexpr (kPair) rt = 2 * rt + static_cast<int>(crank);
             const int row = rt * kBM + r_in_tile;
             const int v0 = vt * kVT;
             const bool row_ok = row < p.T;
@@ -345,7 +457,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int npairs = n >> 1;
             for (int jj = 0; jj < n; ++jj, ++g) {
                 const uint32_t buf = g % kAccBufs, use = g / kAccBufs;
-                if (!warp_wait(&acc_full[buf], use & 1u, p, abort_flag)) {
+                if (!warp_wait<kPair>(&acc_full[buf], use & 1u, p, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -353,7 +465,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t colB = buf * kVT;
                 if (n == 1) {
                     tmem_ld64(lane_base + colB, R);
-                    release_buf(&acc_empty[buf]);
+                    release_buf<kPair>(&acc_empty[buf]);
                     continue;
                 }
                 if ((jj & 1) == 0) continue;  // wait for the partner leaf
@@ -390,8 +502,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         --depth;
                     }
                 }
-                release_buf(&acc_empty[pbuf]);
-                release_buf(&acc_empty[buf]);
+                release_buf<kPair>(&acc_empty[pbuf]);
+                release_buf<kPair>(&acc_empty[buf]);
             }
             if (!ok) break;
             {
@@ -480,9 +592,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ---------------------------------------------------------------- teardown
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (kPair) cluster_sync_all();  // no arrive or commit still targets either CTA
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, kTmemCols);
+        if constexpr (kPair)
+            tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 

@@ -110,6 +110,7 @@ struct lp_handle {
     int leaf_len = 0;
     uint64_t timeout_ns = 0;
     CUtensorMap tmW{};
+    CUtensorMap tmW64{};  // the same W with 64-row boxes (a CTA pair's half of a W tile)
     double* host_scalars = nullptr;  // pinned host: D3 and n_valid of the host-buffer call
     // workspace (device)
     float2* ws_ms = nullptr;      // [num_lse_tiles][max_tokens]
@@ -156,8 +157,10 @@ struct lp_handle {
     cudaStream_t last_stream = nullptr;
     int64_t ws_bytes = 0;
     int32_t last_launches = 0;
-    // launch-layout switch read from the environment at init (LP_FORCE_SHORT_STAGES); it
-    // changes only the schedule, never the arithmetic, and lets the tests prove that
+    // launch-layout switches read from the environment at init (LP_FORCE_SINGLE_CTA,
+    // LP_FORCE_SHORT_STAGES); they change only the schedule, never the arithmetic, and let
+    // the tests prove that
+    bool force_single_cta = false;
     bool force_sub1 = false;
     int band = 0;  // vocabulary tiles per scheduling band (even); schedule only
     // profiling: event pairs around leaf-GEMM launches
@@ -203,24 +206,38 @@ int scheduling_band(int H, int bytes_per_weight, int max_tiles, int mib) {
     return static_cast<int>(b) & ~1;
 }
 
-template <int kMode, int kSub>
+template <int kMode, int kSub, bool kPair = false>
 cudaError_t launch_gemm_variant(int grid, cudaStream_t st, const CUtensorMap& tmX,
                                 const CUtensorMap& tmW, const CUtensorMap& tmD,
                                 const lp::GemmParams& p) {
-    lp::leaf_gemm_kernel<kMode, kSub>
-        <<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(kSub, kMode), st>>>(tmX, tmW, tmD, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(lp::kGemmThreads);
+    cfg.dynamicSmemBytes = lp::gemm_smem_bytes(kSub, kMode, kPair);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    if (kPair) {  // clusters of two CTAs: the pair of one cta_group::2 MMA
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, lp::leaf_gemm_kernel<kMode, kSub, kPair>, tmX, tmW, tmD, p);
 }
 
 template <int kMode>
 int set_gemm_attributes() {
-    const auto set = [](auto fn, int sub) {
+    const auto set = [](auto fn, int sub, bool pair) {
         return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    lp::gemm_smem_bytes(sub, kMode));
+                                    lp::gemm_smem_bytes(sub, kMode, pair));
     };
     cudaError_t e;
-    if ((e = set(lp::leaf_gemm_kernel<kMode, 1>, 1)) != cudaSuccess ||
-        (e = set(lp::leaf_gemm_kernel<kMode, 2>, 2)) != cudaSuccess)
+    if ((e = set(lp::leaf_gemm_kernel<kMode, 1>, 1, false)) != cudaSuccess ||
+        (e = set(lp::leaf_gemm_kernel<kMode, 2>, 2, false)) != cudaSuccess ||
+        (e = set(lp::leaf_gemm_kernel<kMode, 1, true>, 1, true)) != cudaSuccess ||
+        (e = set(lp::leaf_gemm_kernel<kMode, 2, true>, 2, true)) != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute(leaf_gemm_kernel)");
     return LP_OK;
 }
@@ -233,9 +250,12 @@ struct GradArgs {
     int64_t ldd = 0;
 };
 
-// The leaf GEMM over `rows` rows of X starting at `X` (row stride ldx), one CTA per
-// 128 x 128 tile; calls smaller than one row tile (decode) cut the X box to their rows.
-// Stages are 128 K deep (8 MMAs per barrier synchronisation) when the leaf length allows.  Launches of
+// The leaf GEMM over `rows` rows of X starting at `X` (row stride ldx).  Calls of more than
+// one row tile run in CTA pairs (cta_group::2: each pair computes two row tiles of one
+// vocabulary tile, each CTA loading half of the W tile, so the tensor core gets 256 rows per
+// MMA instruction and each CTA fills 24 KB of shared memory per 64-K step instead of 32 KB);
+// calls of at most one row tile (decode batches up to 128) run one CTA per 128 x 128 tile with
+// the X box cut to their rows.  Stages are 128 K deep (8 MMAs per barrier synchronisation) when the leaf length allows.  Launches of
 // at most kShortStageRows rows (decode batches) and odd leaf lengths take seven 64-K stages
 // instead: such launches read each W tile from DRAM for one or two row tiles, and the deeper
 // ring keeps 112 KB of W per CTA in flight instead of 96 KB (measured on GB300: decode
@@ -269,6 +289,7 @@ int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int lea
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
     const bool sub2 = h->leaf_len % (2 * lp::kBK) == 0 && rows > kShortStageRows && !h->force_sub1;
+    const bool pair = rows > lp::kBM && !h->force_single_cta;
     p.x_box_rows = static_cast<int32_t>(x_box_rows(rows));
     CUtensorMap tmX;
     int rc = encode_kmajor(&tmX, X, static_cast<uint64_t>(rows), h->cfg.H, ldx,
@@ -280,15 +301,21 @@ int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int lea
         rc = encode_kmajor(&tmD, ga.dl, static_cast<uint64_t>(rows), h->cfg.V, ga.ldd, 32);
         if (rc != LP_OK) return rc;
     }
-    const int64_t tiles = static_cast<int64_t>(p.num_row_tiles) * h->num_vocab_tiles;
+    // scheduling units: tiles, or (pairs) two row tiles of one vocabulary tile
+    const int64_t tiles =
+        (pair ? ceil_div(p.num_row_tiles, 2) : p.num_row_tiles) * int64_t(h->num_vocab_tiles);
     if (tiles > 0x7fffffff) return fail(LP_ERR_UNSUPPORTED, "too many tiles in one launch");
-    const int64_t slots = h->num_sms;
-    const int grid = static_cast<int>(tiles < slots ? tiles : slots);
+    const int64_t slots = pair ? h->num_sms / 2 : h->num_sms;
+    const int grid = static_cast<int>((tiles < slots ? tiles : slots) * (pair ? 2 : 1));
     const bool prof = h->profiling && h->prof_used < kProfPairs;
     if (prof) LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used], st), "profile event");
     cudaError_t e;
-    e = sub2 ? launch_gemm_variant<kMode, 2>(grid, st, tmX, h->tmW, tmD, p)
-             : launch_gemm_variant<kMode, 1>(grid, st, tmX, h->tmW, tmD, p);
+    if (pair)
+        e = sub2 ? launch_gemm_variant<kMode, 2, true>(grid, st, tmX, h->tmW64, tmD, p)
+                 : launch_gemm_variant<kMode, 1, true>(grid, st, tmX, h->tmW64, tmD, p);
+    else
+        e = sub2 ? launch_gemm_variant<kMode, 2>(grid, st, tmX, h->tmW, tmD, p)
+                 : launch_gemm_variant<kMode, 1>(grid, st, tmX, h->tmW, tmD, p);
     LP_CUDA(e, "leaf_gemm_kernel launch");
     LP_CUDA(cudaGetLastError(), "leaf_gemm_kernel launch");
     if (prof) {
@@ -589,6 +616,7 @@ int init_impl(const lp_config* cfg, const void* W, void* stream, lp_handle** out
         if (v > 0) timeout_ms = static_cast<uint64_t>(v);
     }
     h->timeout_ns = timeout_ms * 1000000ull;
+    if (const char* e = std::getenv("LP_FORCE_SINGLE_CTA")) h->force_single_cta = e[0] == '1';
     if (const char* e = std::getenv("LP_FORCE_SHORT_STAGES")) h->force_sub1 = e[0] == '1';
     h->band = scheduling_band(cfg->H, 2, 64, 32);
     if (const char* e = std::getenv("LP_BAND")) {
@@ -603,6 +631,8 @@ int init_impl(const lp_config* cfg, const void* W, void* stream, lp_handle** out
         return code;
     };
     rc = encode_kmajor(&h->tmW, W, static_cast<uint64_t>(cfg->V), cfg->H, cfg->H);
+    if (rc != LP_OK) return cleanup(rc);
+    rc = encode_kmajor(&h->tmW64, W, static_cast<uint64_t>(cfg->V), cfg->H, cfg->H, lp::kVT / 2);
     if (rc != LP_OK) return cleanup(rc);
 
     const int64_t mt = cfg->max_tokens;
@@ -1074,7 +1104,9 @@ int lp_vocab_partials(lp_handle* h, const void* X, int64_t ldx, const int32_t* i
     h->last_stream = st;
     const int rows = static_cast<int>(T);
     // the fused leaf GEMM of this slice; a row whose sampled id lies outside the slice is
-    // simply not captured (its id belongs to another rank)
+    // not captured (its id belongs to another rank) and keeps the NaN written here
+    LP_CUDA(cudaMemsetAsync(h->zy, 0xFF, sizeof(float) * static_cast<size_t>(rows), st),
+            "sampled logits fill");
     rc = launch_leaf_gemm<lp::kModeLse>(h, X, ldx, rows, 0, h->cfg.n_leaves, ids_local, nullptr,
                                         0, st);
     if (rc != LP_OK) return rc;

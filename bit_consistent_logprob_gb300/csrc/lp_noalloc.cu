@@ -1,22 +1,28 @@
 // lp_noalloc.cu -- lp_logprobs_noalloc: the fused sampled-token logprob path for callers
 // that must not allocate device memory.
 //
-// Some callers cannot call cudaMalloc: code that runs while a CUDA graph is being
-// captured, runtimes whose memory is planned ahead by their own allocator (which must not
-// see allocations behind its back), or hosts that forbid allocation after start-up.  For
-// them this entry point needs no handle and no workspace: the per-tile (max, sum-exp)
+// Some callers cannot call cudaMalloc: runtimes whose device memory is planned ahead by
+// their own allocator (which must not see allocations behind its back), and hosts that
+// forbid allocation after start-up (a fixed memory budget checked once).  For them this
+// entry point needs no handle and no workspace: the per-tile (max, sum-exp)
 // partials, the sampled logits and the status word live in one file-scope device array
 // of fixed size, g_lp_noalloc_scratch, which every GPU that loads the library holds until
 // the process exits.  The caller still passes the inputs and the outputs.
 //
 // The kernels are the same templates as the handle-based path (same per-element
 // arithmetic, so the results are bit-identical to lp_logprobs with tp_slices = 1).
+//
+// A bounded in-kernel wait that expires sets the timeout bit of the status word in the
+// scratch; a last small kernel of the same call then turns every row's logp and logZ into
+// NaN, so the caller sees it in the outputs without reading the status word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
 #include <string>
 
@@ -61,13 +67,24 @@ struct DeviceSetup {
     std::string message;
     unsigned char* scratch = nullptr;  // device address of g_lp_noalloc_scratch on this device
     int num_sms = 0;
+    uint64_t timeout_ns = 2000000000ull;  // bound on every in-kernel wait (LP_WAIT_TIMEOUT_MS)
+    int status_init = 0;                  // the status word at the start of each call
 };
 DeviceSetup g_setup[kMaxDevices];
 
 // Once per device, with that device current: resolve the scratch array's device address,
-// check the architecture and raise the kernels' dynamic shared-memory limits.  Nothing here
-// allocates.
+// check the architecture, raise the kernels' dynamic shared-memory limits and read the wait
+// limit from the environment.  Nothing here allocates.
 void setup_device(int dev, DeviceSetup& s) {
+    if (const char* v = std::getenv("LP_WAIT_TIMEOUT_MS")) {
+        const long long ms = std::atoll(v);
+        if (ms > 0) s.timeout_ns = static_cast<uint64_t>(ms) * 1000000ull;
+    }
+    // test hook: every call starts as if one of its waits had expired, so the tests can check
+    // what a caller sees on a timeout without making a GPU wait run out
+    if (const char* v = std::getenv("LP_TEST_NOALLOC_MARK_TIMEOUT")) {
+        if (v[0] == '1') s.status_init = lp::kStatusTimeout;
+    }
     cudaDeviceProp prop;
     cudaError_t e = cudaGetDeviceProperties(&prop, dev);
     if (e == cudaSuccess && !(prop.major == 10 && prop.minor == 3)) {
@@ -79,11 +96,11 @@ void setup_device(int dev, DeviceSetup& s) {
     if (e == cudaSuccess) e = cudaGetSymbolAddress(&ptr, g_lp_noalloc_scratch);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<lp::kModeLse, 1, 1>,
+        e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<lp::kModeLse, 1>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  lp::gemm_smem_bytes(1));
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<lp::kModeLse, 2, 1>,
+        e = cudaFuncSetAttribute(lp::leaf_gemm_kernel<lp::kModeLse, 2>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  lp::gemm_smem_bytes(2));
     if (e != cudaSuccess) {
@@ -125,6 +142,18 @@ int encode(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K, uint64
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The status word's value at the start of a call (0, or the test hook's mark).
+__global__ void noalloc_status_init_kernel(int* status, int value) { *status = value; }
+
+// Last step of a call: if a bounded wait expired (timeout bit), every row's outputs become NaN.
+__global__ void noalloc_timeout_nan_kernel(const int* status, float* logp, float* logZ, int T) {
+    if ((*status & lp::kStatusTimeout) == 0) return;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T; i += gridDim.x * blockDim.x) {
+        logp[i] = NAN;
+        if (logZ != nullptr) logZ[i] = NAN;
+    }
+}
 
 }  // namespace
 
@@ -178,7 +207,8 @@ LP_API int lp_logprobs_noalloc(const void* W, int32_t H, int32_t V, int32_t n_le
     if (rc != LP_OK) return rc;
 
     // the status word starts at zero for every call (the array keeps the last call's data)
-    e = cudaMemsetAsync(status, 0, sizeof(int), st);
+    noalloc_status_init_kernel<<<1, 1, 0, st>>>(status, s.status_init);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return nfail(LP_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
 
     lp::GemmParams p{};
@@ -199,13 +229,13 @@ LP_API int lp_logprobs_noalloc(const void* W, int32_t H, int32_t V, int32_t n_le
     p.out = nullptr;
     p.ldo = 0;
     p.status = status;
-    p.timeout_ns = 2000000000ull;
+    p.timeout_ns = s.timeout_ns;
     const int64_t tiles = static_cast<int64_t>(p.num_row_tiles) * p.num_vocab_tiles;
     const int grid = static_cast<int>(tiles < s.num_sms ? tiles : s.num_sms);
     if (p.leaf_len % (2 * lp::kBK) == 0)
-        lp::leaf_gemm_kernel<lp::kModeLse, 2, 1><<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(2), st>>>(tmX, tmW, tmX, p);
+        lp::leaf_gemm_kernel<lp::kModeLse, 2><<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(2), st>>>(tmX, tmW, tmX, p);
     else
-        lp::leaf_gemm_kernel<lp::kModeLse, 1, 1><<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(1), st>>>(tmX, tmW, tmX, p);
+        lp::leaf_gemm_kernel<lp::kModeLse, 1><<<grid, lp::kGemmThreads, lp::gemm_smem_bytes(1), st>>>(tmX, tmW, tmX, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return nfail(LP_ERR_CUDA, "leaf_gemm_kernel launch: %s", cudaGetErrorString(e));
 
@@ -230,6 +260,11 @@ LP_API int lp_logprobs_noalloc(const void* W, int32_t H, int32_t V, int32_t n_le
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return nfail(LP_ERR_CUDA, "lse_combine_kernel launch: %s", cudaGetErrorString(e));
+    const int nan_blocks = static_cast<int>((rows + 255) / 256 < 64 ? (rows + 255) / 256 : 64);
+    noalloc_timeout_nan_kernel<<<nan_blocks, 256, 0, st>>>(status, out_logp, out_logZ, rows);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return nfail(LP_ERR_CUDA, "timeout check launch: %s", cudaGetErrorString(e));
     return LP_OK;
 }
 

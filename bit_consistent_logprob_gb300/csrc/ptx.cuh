@@ -237,6 +237,130 @@ __device__ __forceinline__ void umma_commit_elect(uint64_t* bar) {
         : "memory");
 }
 
+// ------------------------------------------------------------------ CTA pairs (cta_group::2)
+// Two CTAs of a cluster share one tcgen05.mma of M = 256: each supplies 128 rows of A and
+// half of B from its own shared memory and holds its 128 rows of D in its own TMEM.  Nothing
+// here multicasts: every copy lands in the CTA that issued it, and every cross-CTA signal is
+// one arrive (or one commit) on one barrier at one shared::cluster address.
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of both CTAs arrives, then waits for all of them (release / acquire).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+// The shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+    return r;
+}
+
+// Arrive on a barrier given by its shared::cluster address (this CTA's or the partner's).
+// The release is at CTA scope: what it orders is this thread's completed tcgen05 loads (behind
+// tcgen05.fence::before_thread_sync) or an observed copy completion, not global-memory
+// writes, and a cluster-scope release would make the thread wait for all of its outstanding
+// memory operations first.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+                 : "memory");
+}
+
+// Store one word to a shared::cluster address (the partner CTA's abort flag).
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// TMEM allocation, permit release and de-allocation for a CTA pair: one warp of EACH of the
+// two CTAs executes these together; the same columns are allocated in both CTAs' TMEM.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                 "r"(ncols)
+                 : "memory");
+}
+
+// Arrive on two barriers (shared::cluster addresses: this CTA's and the partner's) when every
+// tcgen05 operation this thread issued so far completes; one elected lane.
+__device__ __forceinline__ void umma_commit2_pair_elect(uint32_t bar_a, uint32_t bar_b) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t}" ::"r"(
+            bar_a),
+        "r"(bar_b)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_pair_elect(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            bar)
+        : "memory");
+}
+
+// One pipeline stage of pair MMAs (M = 256: A rows 0-127 from this CTA's tile, 128-255 from
+// the partner's tile at the same offset; B halves likewise), from one elected lane: 4 * kSub
+// MMAs of K = 16, the A descriptor advanced by 16 KB (1024 units) and the B descriptor by 8 KB
+// (512 units: the 64-row half of W) per 64-K sub-block, +32 bytes per K step inside one; the
+// first MMA with the caller's accumulate flag; then the stage is freed in both CTAs (one
+// commit per CTA's barrier).
+#define LP_PMMA(A, B, P) "@e tcgen05.mma.cta_group::2.kind::f16 [%0], " A ", " B ", %3, " P ";\n\t"
+#define LP_PADV(OA, OB) "add.s64 a1, %1, " OA ";\n\tadd.s64 b1, %2, " OB ";\n\t"
+#define LP_PSTAGE_X4 \
+    LP_PMMA("%1", "%2", "p") LP_PADV("2", "2") LP_PMMA("a1", "b1", "t") \
+    LP_PADV("4", "4") LP_PMMA("a1", "b1", "t") LP_PADV("6", "6") LP_PMMA("a1", "b1", "t")
+#define LP_PSTAGE_X8_TAIL \
+    LP_PADV("1024", "512") LP_PMMA("a1", "b1", "t") LP_PADV("1026", "514") LP_PMMA("a1", "b1", "t") \
+    LP_PADV("1028", "516") LP_PMMA("a1", "b1", "t") LP_PADV("1030", "518") LP_PMMA("a1", "b1", "t")
+#define LP_PSTAGE_HEAD \
+    "{\n\t.reg .pred e, p, t;\n\t.reg .b64 a1, b1;\n\t" \
+    "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+#define LP_PCOMMIT2                                                                       \
+    "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t" \
+    "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}"
+
+template <int kSub>
+__device__ __forceinline__ void umma_pair_stage_elect(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                                      uint32_t idesc, uint32_t accumulate,
+                                                      uint32_t bar_own, uint32_t bar_peer) {
+    static_assert(kSub == 1 || kSub == 2, "stages hold one or two 64-K sub-blocks");
+    if constexpr (kSub == 2) {
+        asm volatile(LP_PSTAGE_HEAD LP_PSTAGE_X4 LP_PSTAGE_X8_TAIL LP_PCOMMIT2 ::"r"(d_tmem),
+                     "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(bar_own), "r"(bar_peer)
+                     : "memory");
+    } else {
+        asm volatile(LP_PSTAGE_HEAD LP_PSTAGE_X4 LP_PCOMMIT2 ::"r"(d_tmem), "l"(a), "l"(b),
+                     "r"(idesc), "r"(accumulate), "r"(bar_own), "r"(bar_peer)
+                     : "memory");
+    }
+}
+#undef LP_PMMA
+#undef LP_PADV
+#undef LP_PSTAGE_X4
+#undef LP_PSTAGE_X8_TAIL
+#undef LP_PSTAGE_HEAD
+#undef LP_PCOMMIT2
+
 // ------------------------------------------------------------------ tcgen05
 // TMEM allocation by one full warp; the base address is written to shared memory.
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {

@@ -33,9 +33,9 @@
  *    synchronisation inside a step, weights updated in place (vLLM blog,
  *    section 4.6).
  *
- * Every call is asynchronous on the caller's CUDA stream (cudaStream_t passed as
- * void*; NULL = legacy default stream), performs no host synchronisation and no
- * allocation (except lp_init, lp_free, lp_check and the *_host variants, which
+ * Every call on a handle is asynchronous on the caller's CUDA stream (cudaStream_t
+ * passed as void*; NULL = legacy default stream), performs no host synchronisation and
+ * no allocation (except lp_init, lp_free, lp_check and the *_host variants, which
  * are documented as synchronous), and can be captured in a CUDA graph.
  *
  * Errors: every function returns an lp_status.  Argument errors are detected on
@@ -107,10 +107,9 @@ typedef struct lp_handle lp_handle; /* opaque, owned by the library */
  * Environment variables read here, for this handle's lifetime.  The first group changes only
  * which CTA computes a tile and how data moves, never a bit of any output (the tests prove
  * each against the default layout):
- *   LP_FORCE_SINGLE_CTA=1    one CTA per tile instead of two-CTA clusters;
- *   LP_FORCE_SHORT_STAGES=1  seven 64-K pipeline stages for every launch;
- *   LP_FORCE_SHARE_X=1       launches of 129-256 rows pair vocabulary-adjacent tiles that share
- *                            an X tile, instead of the two row tiles of one W tile;
+ *   LP_FORCE_SINGLE_CTA=1    one CTA per tile instead of CTA pairs (cta_group::2) for
+ *                            launches of more than 128 rows;
+ *   LP_FORCE_SHORT_STAGES=1  64-K pipeline stages for every launch;
  *   LP_BAND=<even n>         vocabulary tiles per scheduling band of bf16 handles (2..1024).
  *   LP_WAIT_TIMEOUT_MS=<ms>  bound on every in-kernel wait (default 2000); on expiry the
  *                            sticky status reads LP_ERR_TIMEOUT.
@@ -209,8 +208,8 @@ LP_API int lp_importance_weights(lp_handle* h, const float* logp_pi, const float
  *   lp_vocab_partials: the fused leaf GEMM of the slice for T <= max_tokens rows, writing the
  *     (max, sum-exp) partial of each of its ceil(V / 64) vocabulary tiles to out_ms (device,
  *     float pairs [ceil(V / 64)][ld_ms], ld_ms >= T, 16-byte aligned) and the sampled logit
- *     to out_zy [T].  ids_local[t] = sampled id - v0; out_zy[t] is defined only for rows with
- *     ids_local[t] in [0, V), whose sampled token this rank owns.
+ *     to out_zy [T].  ids_local[t] = sampled id - v0; out_zy[t] is the sampled logit for rows
+ *     with ids_local[t] in [0, V), whose sampled token this rank owns, and NaN for the others.
  *   lp_logprobs_from_vocab_partials: on any handle (it lends its status word), logp and logZ
  *     for the full vocabulary of V_full tokens from the gathered partials: every rank's tile
  *     rows concatenated in vocabulary order (ms: float pairs [ceil(V_full / 64)][ld_ms]) and,
@@ -425,20 +424,25 @@ LP_API int lp_profile_read(lp_handle* h, double* gemm_ms_total, int32_t* gemm_la
 /*
  * lp_logprobs without a handle and without any device allocation.  (The pages have no
  * counterpart; this is a deployment entry point.)  For callers that cannot call
- * cudaMalloc -- code running while a CUDA graph is captured, runtimes whose device memory
- * is planned ahead by their own allocator, hosts that forbid allocation after start-up.
- * The scratch (per-tile max/sum-exp pairs, sampled logits, a status word) is a fixed
- * 8.13 MiB file-scope device array that every GPU loading the library holds until exit.
+ * cudaMalloc: runtimes whose device memory is planned ahead by their own allocator (an
+ * allocation behind its back breaks its plan), and hosts that forbid allocation after
+ * start-up.  The scratch (per-tile max/sum-exp pairs, sampled logits, a status word) is a
+ * fixed 8.13 MiB file-scope device array that every GPU loading the library holds until exit.
  *   W, H, V, n_leaves  as in lp_config / lp_init (W referenced, bf16 [V, H]).
  *   X, ldx, ids, T, out_logp, out_logZ  as in lp_logprobs.
  * Limits: T <= 32768 and T * ceil(V / 64) <= 1048576 (e.g. 441 rows at V = 151936);
  * larger calls return LP_ERR_INVALID_ARG and must use lp_logprobs with a handle.
- * The first call on a device resolves the array's device address and sets kernel
- * attributes (no allocation); make that first call before any stream capture.
- * Every call shares the array: calls whose kernels may overlap on the GPU (other streams,
- * other threads) race and must be serialised by the caller.  An id outside [0, V) gives
- * NaN (there is no sticky status for this entry point).  Bit-identical to lp_logprobs
- * with tp_slices = 1.  Errors are described by lp_noalloc_last_error().
+ * The first call on a device resolves the array's device address, sets kernel attributes
+ * and reads LP_WAIT_TIMEOUT_MS (no allocation); make that first call before any stream
+ * capture.  Every call shares the array and overwrites what the last call left there:
+ * calls whose kernels may overlap on the GPU (other streams, other threads) race and must
+ * be serialised by the caller.
+ * Errors found on the GPU are reported in the outputs (this entry point keeps no sticky
+ * status): an id outside [0, V) gives NaN logp on that row; if a bounded in-kernel wait
+ * expires (LP_WAIT_TIMEOUT_MS, default 2000 ms), every row's logp and logZ are NaN.
+ * Bit-identical to lp_logprobs with tp_slices = 1.  Host-side errors are described by
+ * lp_noalloc_last_error().  LP_TEST_NOALLOC_MARK_TIMEOUT=1 (read with the first call) is a
+ * test hook: every call then reports as if a wait had expired.
  */
 LP_API int lp_logprobs_noalloc(const void* W, int32_t H, int32_t V, int32_t n_leaves,
                                const void* X, int64_t ldx, const int32_t* ids, int64_t T,

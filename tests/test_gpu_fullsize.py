@@ -2,7 +2,10 @@
 
 Parity with the fp64 oracle is checked on seeded row samples (the oracle computes
 each sampled row over the whole vocabulary); invariance is checked bit-exactly on
-every row.  Inputs follow the recipes in bit_consistent_logprob_gb300.inputs.
+every row.  Inputs follow the recipes in bit_consistent_logprob_gb300.inputs.  The ids
+of the oracle-checked rows are drawn by seeded Gumbel-max from those rows' oracle
+log-softmax, so the check covers the tokens a sampler actually picks (the other rows
+keep uniform ids).
 """
 import numpy as np
 import pytest
@@ -42,6 +45,21 @@ def sample_rows(T, n, seed, extra=()):
     return list(rng.choice(T, size=min(n, T), replace=False)) + [0, T - 1, *extra]
 
 
+def sampled_ids(X, W, ids, rows, seed):
+    """ids with the listed rows' entries replaced by Gumbel-max draws from those rows'
+    fp64 oracle log-softmax (temperature 1)."""
+    rows = np.asarray(sorted(set(int(r) for r in rows)))
+    idx = torch.as_tensor(rows, device=X.device)
+    ls = oracle.log_softmax(X[idx].cpu(), W.cpu())
+    drawn = inputs.gumbel_max_ids(ls, seed)
+    out = ids.clone()
+    out[idx] = drawn.to(device=ids.device, dtype=ids.dtype)
+    # the drawn tokens are typical draws of each row's softmax, not uniform picks
+    assert len(rows) >= 8
+    assert ls[np.arange(len(rows)), drawn.numpy()].mean() > ls.mean()
+    return out
+
+
 def test_qwen_prefill_packed(dev):
     wl = WORKLOADS["qwen_prefill"]
     lengths = inputs.packed_lengths(wl.n_seqs, wl.len_lo, wl.len_hi, wl.seed)
@@ -49,6 +67,9 @@ def test_qwen_prefill_packed(dev):
     X = inputs.hidden_states(T, wl.H, wl.seed, device=dev)
     W = inputs.lm_head(wl.V, wl.H, wl.seed, device=dev)
     ids = inputs.uniform_ids(T, wl.V, wl.seed, device=dev)
+    starts = np.cumsum([0] + lengths[:-1])
+    rows = sample_rows(T, 24, 1, extra=list(starts[:4]))
+    ids = sampled_ids(X, W, ids, rows, wl.seed)
     with Engine(W, n_leaves=wl.n_leaves, max_tokens=32768) as eng:
         logp, logZ = eng.logprobs(X, ids, return_logZ=True, phase=LP_PHASE_PREFILL)
         # every sequence run alone gives the packed rows bit for bit
@@ -58,8 +79,7 @@ def test_qwen_prefill_packed(dev):
             assert_bit_equal(alone, logp[off:off + L], f"sequence at {off} ({L} tokens)")
             off += L
         eng.check()
-    starts = np.cumsum([0] + lengths[:-1])
-    oracle_check(X, W, ids, logp, logZ, sample_rows(T, 24, 1, extra=list(starts[:4])))
+    oracle_check(X, W, ids, logp, logZ, rows)
 
 
 def test_ds_prefill_chunks_and_tp(dev):
@@ -68,6 +88,8 @@ def test_ds_prefill_chunks_and_tp(dev):
     X = inputs.hidden_states(T, wl.H, wl.seed, device=dev)
     W = inputs.lm_head(wl.V, wl.H, wl.seed, device=dev)
     ids = inputs.uniform_ids(T, wl.V, wl.seed, device=dev)
+    rows = sample_rows(T, 12, 2, extra=[2047, 2048])
+    ids = sampled_ids(X, W, ids, rows, wl.seed)
     with Engine(W, n_leaves=wl.n_leaves, max_tokens=T) as eng:
         one_shot, logZ = eng.logprobs(X, ids, return_logZ=True)
         eng.check()
@@ -84,7 +106,7 @@ def test_ds_prefill_chunks_and_tp(dev):
             tp = eng.logprobs(X[:Tt], ids[:Tt])
             eng.check()
         assert_bit_equal(tp, one_shot[:Tt], f"TP split into {s} slices")
-    oracle_check(X, W, ids, one_shot, logZ, sample_rows(T, 12, 2, extra=[2047, 2048]))
+    oracle_check(X, W, ids, one_shot, logZ, rows)
 
 
 def test_ds_decode_sweep(dev):
@@ -93,9 +115,11 @@ def test_ds_decode_sweep(dev):
     X = inputs.hidden_states(pool, wl.H, wl.seed, device=dev)
     W = inputs.lm_head(wl.V, wl.H, wl.seed, device=dev)
     ids = inputs.uniform_ids(pool, wl.V, wl.seed, device=dev)
+    target = 300
+    rows = sample_rows(pool, 10, 3, extra=[target])
+    ids = sampled_ids(X, W, ids, rows, wl.seed)
     with Engine(W, n_leaves=wl.n_leaves, max_tokens=pool) as eng:
         prefill, logZ = eng.logprobs(X, ids, return_logZ=True, phase=LP_PHASE_PREFILL)
-        target = 300
         for B in wl.batch_sizes:
             # the decode batch: B single-token rows; the target row at several positions
             rng = np.random.default_rng(B)
@@ -106,7 +130,7 @@ def test_ds_decode_sweep(dev):
                 dec = eng.logprobs(X[idx].contiguous(), ids[idx].contiguous(), phase=LP_PHASE_DECODE)
                 assert_bit_equal(dec, prefill[idx], f"decode B={B}, target at {pos}")
         eng.check()
-    oracle_check(X, W, ids, prefill, logZ, sample_rows(pool, 10, 3, extra=[target]))
+    oracle_check(X, W, ids, prefill, logZ, rows)
 
 
 def test_is_d3_at_scale(dev):
@@ -117,6 +141,8 @@ def test_is_d3_at_scale(dev):
     W = inputs.lm_head(wl.V, wl.H, wl.seed, device=dev)
     W_lag = inputs.lagged_lm_head(W, wl.seed)
     ids = inputs.uniform_ids(T, wl.V, wl.seed, device=dev)
+    rows = sample_rows(T, 8, 4)
+    ids = sampled_ids(X, W, ids, rows, wl.seed)
     with Engine(W_lag, n_leaves=wl.n_leaves, max_tokens=32768) as eng:
         mu = eng.logprobs(X, ids)
         eng.check()
@@ -125,7 +151,6 @@ def test_is_d3_at_scale(dev):
         w, d3, nv = eng.importance_weights(logpi, mu)
         eng.check()
     assert nv.item() == T
-    rows = sample_rows(T, 8, 4)
     pi_ref, _ = oracle_check(X, W, ids, logpi, None, rows)
     mu_ref, _ = oracle_check(X, W_lag, ids, mu, None, rows)
     rows = np.asarray(sorted(set(int(r) for r in rows)))

@@ -258,16 +258,35 @@ def test_importance_weights_invariance(eng, dev):
     eng.check()
 
 
-@pytest.mark.parametrize("env", ["LP_FORCE_SHORT_STAGES"])
+@pytest.mark.parametrize("env", ["LP_FORCE_SINGLE_CTA", "LP_FORCE_SHORT_STAGES"])
 def test_launch_layout_changes_no_bits(data, eng, env, monkeypatch):
-    # 128-K versus 64-K pipeline stages change only how data moves, not how a tile is
-    # computed.
+    # CTA pairs (one cta_group::2 MMA over two row tiles) versus one CTA per tile, and 128-K
+    # versus 64-K pipeline stages, change only how data moves and who computes a tile.
     X, W, ids = data
     T = 3000
     base, baseZ = eng.logprobs(X[:T], ids[:T], return_logZ=True)
+    ent = eng.logprobs_entropy(X[:T], ids[:T])
     monkeypatch.setenv(env, "1")
     with Engine(W, n_leaves=N, max_tokens=T) as e2:
         other, otherZ = e2.logprobs(X[:T], ids[:T], return_logZ=True)
+        ent2 = e2.logprobs_entropy(X[:T], ids[:T])
         e2.check()
     assert_bit_equal(other, base, env)
     assert_bit_equal(otherZ, baseZ, env)
+    for a, b in zip(ent2, ent):
+        assert_bit_equal(a, b, env + " entropy step")
+
+
+@pytest.mark.parametrize("T", [129, 200, 256, 383])
+def test_pairs_with_a_ragged_partner_change_no_bits(data, eng, T, monkeypatch):
+    # Calls of 129-256 rows (decode batches of two row tiles) and an odd number of row tiles
+    # (383 rows: the last pair's second CTA has no rows) run in CTA pairs; one CTA per tile
+    # gives the same bits.
+    X, W, ids = data
+    base, baseZ = eng.logprobs(X[:T], ids[:T], return_logZ=True)
+    monkeypatch.setenv("LP_FORCE_SINGLE_CTA", "1")
+    with Engine(W, n_leaves=N, max_tokens=T) as e2:
+        other, otherZ = e2.logprobs(X[:T], ids[:T], return_logZ=True)
+        e2.check()
+    assert_bit_equal(other, base, "LP_FORCE_SINGLE_CTA logp")
+    assert_bit_equal(otherZ, baseZ, "LP_FORCE_SINGLE_CTA logZ")

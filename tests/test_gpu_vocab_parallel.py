@@ -23,7 +23,7 @@ H, N = 1024, 8
 
 @pytest.mark.parametrize("cuts,V,T", [
     ([0, 12800, 25600], 32001, 300),     # three slices, the last one ragged
-    ([0, 16384], 32001, 256),            # two slices; 256 rows: W-sharing cluster pairs
+    ([0, 16384], 32001, 256),            # two slices; 256 rows: two row tiles
     ([0, 128, 4096], 8000, 7),           # a one-tile slice; a decode batch
 ])
 def test_vocab_split_gives_the_full_lm_head_bits(cuts, V, T):
@@ -39,6 +39,9 @@ def test_vocab_split_gives_the_full_lm_head_bits(cuts, V, T):
     for a, b in zip(bounds[:-1], bounds[1:]):
         with Engine(W[a:b], n_leaves=N, max_tokens=T) as part:
             ms, zy = part.vocab_partials(X, ids - a)
+            # the sampled logit of a row this slice owns; NaN for rows owned elsewhere
+            inside = (ids >= a) & (ids < b)
+            assert torch.isfinite(zy[inside]).all() and torch.isnan(zy[~inside]).all()
             ms_parts.append(ms.clone())
             zy_parts.append(zy.clone())
             part.check()

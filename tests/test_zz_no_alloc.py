@@ -1,15 +1,19 @@
 """lp_logprobs_noalloc, called through the C ABI.
 
-This entry point serves callers that cannot call cudaMalloc (code running during CUDA
-graph capture, runtimes that plan device memory with their own allocator, hosts that
-forbid allocation after start-up): it takes no handle and keeps its scratch in a fixed
-file-scope device array.  Two calls in a row must give the same bits as the handle-based
-lp_logprobs on the same inputs, and oversized calls must be refused before any work.
+This entry point serves callers that cannot call cudaMalloc (runtimes that plan device
+memory with their own allocator, hosts that forbid allocation after start-up): it takes no
+handle and keeps its scratch in a fixed file-scope device array.  Two calls in a row must
+give the same bits as the handle-based lp_logprobs on the same inputs, oversized calls must
+be refused before any work, and errors found on the GPU must show in the outputs (NaN),
+since this entry point has no status word a caller can read.
 
 This file is collected last so that a run stopping at the first failure has already
 run every other test; it also passes when run alone in a fresh process.
 """
 import ctypes
+import os
+import subprocess
+import sys
 
 import pytest
 import torch
@@ -83,3 +87,68 @@ def test_noalloc_refuses_calls_beyond_its_scratch():
         eng.check()
     torch.cuda.synchronize()
     assert_bit_equal(out[:441], ref, "largest no-alloc call")
+
+
+def test_noalloc_reports_a_bad_id_on_its_row_only():
+    dev = require_cuda()
+    lib = _native.load()
+    T, H, V, N = 40, 256, 4096, 4
+    W = inputs.lm_head(V, H, seed=5, device=dev)
+    X = inputs.hidden_states(T, H, seed=5, device=dev)
+    ids = inputs.uniform_ids(T, V, seed=5, device=dev)
+    with Engine(W, n_leaves=N, max_tokens=T) as eng:
+        ref, refZ = eng.logprobs(X, ids, return_logZ=True)
+        eng.check()
+    bad = ids.clone()
+    bad[7] = V          # outside [0, V)
+    bad[31] = -1
+    lp = torch.empty(T, device=dev)
+    lz = torch.empty(T, device=dev)
+    assert noalloc(lib, W, X, bad, N, lp, lz) == LP_OK, lib.lp_noalloc_last_error()
+    torch.cuda.synchronize()
+    assert torch.isnan(lp[[7, 31]]).all()
+    keep = torch.ones(T, dtype=torch.bool, device=dev)
+    keep[[7, 31]] = False
+    assert_bit_equal(lp[keep], ref[keep], "no-alloc logp of the good rows")
+    assert_bit_equal(lz, refZ, "no-alloc logZ (it does not depend on the id)")
+    # the next call with good ids is clean again: nothing of the bad call is left over
+    assert noalloc(lib, W, X, ids, N, lp, lz) == LP_OK
+    torch.cuda.synchronize()
+    assert_bit_equal(lp, ref, "no-alloc logp after a bad call")
+
+
+_TIMEOUT_CHILD = r"""
+import ctypes, sys, torch
+sys.path.insert(0, sys.argv[1])
+from bit_consistent_logprob_gb300 import _native, inputs
+lib = _native.load()
+dev = torch.device("cuda:0")
+T, H, V, N = 33, 256, 4096, 4
+W = inputs.lm_head(V, H, seed=3, device=dev)
+X = inputs.hidden_states(T, H, seed=3, device=dev)
+ids = inputs.uniform_ids(T, V, seed=3, device=dev)
+lp = torch.zeros(T, device=dev)
+lz = torch.zeros(T, device=dev)
+s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+for _ in range(2):
+    rc = lib.lp_logprobs_noalloc(ctypes.c_void_p(W.data_ptr()), H, V, N,
+                                 ctypes.c_void_p(X.data_ptr()), H, ctypes.c_void_p(ids.data_ptr()),
+                                 T, ctypes.c_void_p(lp.data_ptr()), ctypes.c_void_p(lz.data_ptr()), s)
+    assert rc == 0, lib.lp_noalloc_last_error()
+    torch.cuda.synchronize()
+    assert torch.isnan(lp).all() and torch.isnan(lz).all(), (lp, lz)
+print("all rows NaN")
+"""
+
+
+def test_noalloc_timeout_turns_every_row_into_nan():
+    # The test hook marks every call of this process as if one of its bounded waits had
+    # expired (no wait is made to run out on the GPU); the caller must then see NaN in
+    # every row of logp and logZ.  The hook is read once per process, so it runs in a child.
+    require_cuda()
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, LP_TEST_NOALLOC_MARK_TIMEOUT="1")
+    out = subprocess.run([sys.executable, "-c", _TIMEOUT_CHILD, root], env=env,
+                         capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert "all rows NaN" in out.stdout
