@@ -72,11 +72,20 @@ struct GemmParams {
     const float* sx;          // [T][nkb] activation block scales (block-FP8 kernel)
     const float* sw;          // [num_vocab_tiles][nkb] weight block scales (block-FP8 kernel)
     int32_t nkb;              // 128-K blocks over H (block-FP8 kernel)
+    int* sched;               // tile counter of a pair launch's dynamic schedule (zero at launch)
     int* status;              // sticky device status word
     uint64_t timeout_ns;      // bound on every mbarrier wait
 };
 
-__host__ __device__ constexpr int kNumBars(int stages) { return 2 * stages + 2 * kAccBufs + 1; }
+// A pair's tile schedule is dynamic: the leader's producer publishes each next tile in a ring
+// of kTileSlots slots that every other warp of both CTAs reads (kTileReaders of them: the
+// leader's MMA warp and 8 epilogue warps, the partner's producer, forwarder and 8 epilogue
+// warps).
+constexpr int kTileSlots = 4;
+constexpr int kTileReaders = 2 * (1 + kEpiWarps) + 1;
+__host__ __device__ constexpr int kNumBars(int stages) {
+    return 2 * stages + 2 * kAccBufs + 1 + 2 * kTileSlots;
+}
 
 // A pipeline stage holds kSub 64-wide K sub-blocks of X and of W (4 MMAs of K = 16 per
 // sub-block).  More MMAs per stage means fewer barrier synchronisations per MMA in the
@@ -104,7 +113,7 @@ __host__ __device__ constexpr int gemm_stage_bytes(int sub, bool pair = false) {
 __host__ __device__ constexpr int gemm_smem_bytes(int sub, int mode = kModeLse, bool pair = false) {
     return 1024 /* alignment slack */ + gemm_stages(sub, mode, pair) * gemm_stage_bytes(sub, pair) +
            (mode == kModeGrad ? kGradStageBytes : 0) + kNumBars(gemm_stages(sub, mode, pair)) * 8 +
-           16 /* TMEM address, abort flag */;
+           8 /* TMEM address, abort flag */ + 4 * kTileSlots /* tile slots */;
 }
 static_assert(gemm_smem_bytes(1, kModeGrad) <= 227 * 1024 &&
                   gemm_smem_bytes(2, kModeGrad) <= 227 * 1024 && gemm_smem_bytes(1) <= 227 * 1024 &&
@@ -178,6 +187,32 @@ __device__ __forceinline__ void release_buf(uint64_t* bar) {
     }
 }
 
+// The k-th tile of this CTA (k = 0, 1, ...).  One CTA per tile: the static round robin
+// tile0 + k * tile_step.  A pair: the tile the leader's producer published in slot
+// k % kTileSlots; the slot is then released on the leader's barrier.  Returns -1 if the wait
+// ran out (the abort flag is then raised).
+template <bool kPair>
+__device__ __forceinline__ int next_tile(uint32_t k, int tile0, int tile_step,
+                                         const volatile int* slots, uint64_t* tile_full,
+                                         uint32_t tile_empty_leader, const GemmParams& p,
+                                         volatile int* abort_flag) {
+    if constexpr (!kPair) {
+        return tile0 + static_cast<int>(k) * tile_step;
+    } else {
+        const uint32_t s = k % kTileSlots;
+        bool got = mbar_wait_cl(&tile_full[s], (k / kTileSlots) & 1u, abort_flag, p.timeout_ns);
+        got = __all_sync(0xffffffffu, got);
+        if (!got) {
+            if ((threadIdx.x & 31) == 0) raise_timeout<true>(p, abort_flag);
+            return -1;
+        }
+        const int t = slots[s];
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(tile_empty_leader + 8u * s);
+        return t;
+    }
+}
+
 // kPair = false: one CTA per 128 x 128 tile; each CTA loads its own X and W boxes.
 // kPair = true: clusters of two CTAs (a pair) compute the two row tiles 2*rp and 2*rp + 1 of
 // one vocabulary tile with tcgen05.mma.cta_group::2 (M = 256).  Each CTA loads its own
@@ -190,6 +225,11 @@ __device__ __forceinline__ void release_buf(uint64_t* bar) {
 // epilogue warps release the TMEM buffers on the leader's barrier.  A CTA whose row tile lies
 // past T still loads (zero-filled rows) and computes, but writes nothing.  Every element sees
 // the same K = 16 MMA sequence, leaf tree and tile log-sum-exp as with one CTA per tile.
+// A pair's tiles are handed out dynamically: the clusters do not all run at the same speed,
+// and with a static round robin the tiles in flight drift apart over a launch (measured at
+// the DS shape: 28 rounds of 76 clusters by the end) until the X rows they share fall out of
+// L2.  The leader's producer takes each next tile from the zeroed counter p.sched (one atomic
+// per tile, fetched a tile ahead) and publishes it to both CTAs (next_tile).
 // tmD (kModeGrad only): dl as bf16 [T][ldd] with 64 x 32 boxes, 128-byte swizzle.
 template <int kMode, int kSub, bool kPair = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -213,8 +253,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* acc_full = bars + 2 * kStages;             // MMA -> epilogue, per TMEM buffer
     uint64_t* acc_empty = acc_full + kAccBufs;           // epilogue -> MMA, per TMEM buffer
     uint64_t* drain = acc_empty + kAccBufs;              // MMA drain on abort
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* tile_full = drain + 1;                     // pair: tile index published, per slot
+    uint64_t* tile_empty = tile_full + kTileSlots;       // pair: slot read by every reader
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tile_empty + kTileSlots);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    volatile int* tile_slot = abort_flag + 1;            // pair: [kTileSlots] tile indices
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -234,6 +277,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&acc_empty[b], kPair ? 2 * kEpiWarps : kEpiWarps);
         }
         mbar_init(drain, 1);
+        for (int s = 0; s < kTileSlots; ++s) {
+            mbar_init(&tile_full[s], 1);
+            mbar_init(&tile_empty[s], kTileReaders);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -261,6 +308,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int num_tiles = num_rows * p.num_vocab_tiles;
     const int tile0 = static_cast<int>(kPair ? blockIdx.x >> 1 : blockIdx.x);
     const int tile_step = static_cast<int>(kPair ? gridDim.x >> 1 : gridDim.x);
+    const uint32_t tile_empty_leader = kPair ? cluster_addr(tile_empty, 0) : 0u;
     const int nkb = p.leaf_len / (kBK * kSub);   // stages per leaf
     const int n = p.leaf_count;
 
@@ -271,7 +319,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t stage = 0, phase = 0;
         uint64_t issued = 0;
         bool ok = true;
-        for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
+        // the leader of a pair publishes the tile sequence: tile0 first, then one counter value
+        // per tile (taken a tile ahead, so the atomic's latency hides behind a tile of loads)
+        const bool publish = kPair && leader;
+        const uint32_t slot_peer = publish ? cluster_addr(const_cast<int*>(tile_slot), 1) : 0u;
+        const uint32_t tfull_peer = publish ? cluster_addr(tile_full, 1) : 0u;
+        int next = tile0;
+        int ahead = 0;
+        if (publish && lane == 0) ahead = atomicAdd(p.sched, 1);
+        for (uint32_t k = 0; ok; ++k) {
+            int tile;
+            if (publish) {
+                tile = next;
+                const uint32_t s = k % kTileSlots;
+                ok = __all_sync(kFull, mbar_wait(&tile_empty[s], ((k / kTileSlots) & 1u) ^ 1u,
+                                                 abort_flag, p.timeout_ns));
+                if (!ok) {
+                    if (lane == 0) raise_timeout<kPair>(p, abort_flag);
+                    break;
+                }
+                if (lane == 0) {
+                    tile_slot[s] = tile;
+                    st_cluster_u32(slot_peer + 4u * s, static_cast<uint32_t>(tile));
+                    mbar_arrive(&tile_full[s]);
+                    mbar_arrive_cluster_release(tfull_peer + 8u * s);
+                }
+                __syncwarp();
+                if (tile >= num_tiles) break;
+                next = tile_step + __shfl_sync(kFull, ahead, 0);
+                if (lane == 0) ahead = atomicAdd(p.sched, 1);
+            } else {
+                tile = next_tile<kPair>(k, tile0, tile_step, tile_slot, tile_full,
+                                        tile_empty_leader, p, abort_flag);
+                if (tile < 0) {
+                    ok = false;
+                    break;
+                }
+                if (tile >= num_tiles) break;
+            }
             int rt, vt;
             tile_coords(tile, num_rows, p, rt, vt);
             if constexpr (kPair) rt = 2 * rt + static_cast<int>(crank);
@@ -322,7 +407,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t full_leader = cluster_addr(full, 0);
         uint32_t stage = 0, phase = 0;
         bool ok = true;
-        for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
+        for (uint32_t k = 0; ok; ++k) {
+            const int tile = next_tile<kPair>(k, tile0, tile_step, tile_slot, tile_full,
+                                              tile_empty_leader, p, abort_flag);
+            if (tile < 0) {
+                ok = false;
+                break;
+            }
+            if (tile >= num_tiles) break;
             for (int jj = 0; ok && jj < n; ++jj) {
                 for (int kb = 0; kb < nkb; ++kb) {
                     ok = __all_sync(kFull, mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns));
@@ -360,7 +452,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         bool ok = true;
         bool ready = __all_sync(kFull, bar_test<kPair>(&full[0], 0));
         bool acc_ready = true;  // the first uses of every buffer find it free
-        for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
+        for (uint32_t k = 0; ok; ++k) {
+            const int tile = next_tile<kPair>(k, tile0, tile_step, tile_slot, tile_full,
+                                              tile_empty_leader, p, abort_flag);
+            if (tile < 0) {
+                ok = false;
+                break;
+            }
+            if (tile >= num_tiles) break;
             for (int jj = 0; ok && jj < n; ++jj) {
                 if (!acc_ready) {
                     ok = __all_sync(kFull, bar_wait<kPair>(&acc_empty[buf], bphase ^ 1u,
@@ -436,7 +535,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * 64);
         uint32_t g = 0;
         bool ok = true;
-        for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
+        for (uint32_t k = 0; ok; ++k) {
+            const int tile = next_tile<kPair>(k, tile0, tile_step, tile_slot, tile_full,
+                                              tile_empty_leader, p, abort_flag);
+            if (tile < 0) {
+                ok = false;
+                break;
+            }
+            if (tile >= num_tiles) break;
             int rt, vt;
             tile_coords(tile, num_rows, p, rt, vt);
             if constexpr (kPair) rt = 2 * rt + static_cast<int>(crank);

@@ -123,6 +123,7 @@ struct lp_handle {
     void* cublas_ws = nullptr;
     float* zy = nullptr;          // [max_tokens]
     int* status = nullptr;        // sticky status word
+    int* sched = nullptr;         // tile counter of the pair launches' dynamic schedule
     double* blk_sum = nullptr;    // [max_is_blocks]
     long long* blk_cnt = nullptr; // [max_is_blocks]
     double* stat_blk = nullptr;   // [2][max_is_blocks]: sum |d|^2 and sum k3 per block
@@ -287,6 +288,7 @@ int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int lea
     p.dl = ga.dl;
     p.ldd = ga.ldd;
     p.status = h->status;
+    p.sched = h->sched;
     p.timeout_ns = h->timeout_ns;
     const bool sub2 = h->leaf_len % (2 * lp::kBK) == 0 && rows > kShortStageRows && !h->force_sub1;
     const bool pair = rows > lp::kBM && !h->force_single_cta;
@@ -307,6 +309,8 @@ int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int lea
     if (tiles > 0x7fffffff) return fail(LP_ERR_UNSUPPORTED, "too many tiles in one launch");
     const int64_t slots = pair ? h->num_sms / 2 : h->num_sms;
     const int grid = static_cast<int>((tiles < slots ? tiles : slots) * (pair ? 2 : 1));
+    // a pair launch hands out its tiles from a counter that starts at zero
+    if (pair) LP_CUDA(cudaMemsetAsync(h->sched, 0, sizeof(int), st), "tile counter reset");
     const bool prof = h->profiling && h->prof_used < kProfPairs;
     if (prof) LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used], st), "profile event");
     cudaError_t e;
@@ -556,6 +560,7 @@ void lp_free(lp_handle* h) {
     cudaFree(h->ws_ms);
     cudaFree(h->zy);
     cudaFree(h->status);
+    cudaFree(h->sched);
     cudaFree(h->ws_u);
     cudaFree(h->wq);
     cudaFree(h->sw);
@@ -654,6 +659,7 @@ int init_impl(const lp_config* cfg, const void* W, void* stream, lp_handle** out
                     sizeof(float) * static_cast<size_t>(h->num_lse_tiles) * mt, "ws_u")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->zy), sizeof(float) * mt, "zy")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->status), sizeof(int), "status")) ||
+        (rc = alloc(reinterpret_cast<void**>(&h->sched), sizeof(int), "sched")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->blk_sum), sizeof(double) * h->max_is_blocks,
                     "blk_sum")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->blk_cnt), sizeof(long long) * h->max_is_blocks,

@@ -272,7 +272,41 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
                  : "memory");
 }
 
-// Store one word to a shared::cluster address (the partner CTA's abort flag).
+// Arrive with a cluster-scope release: also orders this thread's earlier stores to the
+// partner's shared memory (the tile index of a dynamic schedule) before the arrive.  It waits
+// for the thread's outstanding memory operations, so it is kept off per-stage paths.
+__device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+                 : "memory");
+}
+
+// Bounded wait with a cluster-scope acquire (pairs with mbar_arrive_cluster_release).
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity,
+                                             volatile int* abort_flag, uint64_t timeout_ns) {
+    const auto probe = [&]() {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        return done != 0;
+    };
+    if (probe()) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (probe()) return true;
+        if ((it & 15u) == 0u) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) return false;
+        }
+    }
+}
+
+// Store one word to a shared::cluster address (the partner CTA's abort flag, or its copy of a
+// tile index).
 __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
