@@ -46,7 +46,7 @@ KERNEL_SOURCES = ["bit_consistent_logprob_gb300/csrc/kernels.cuh",
                   "bit_consistent_logprob_gb300/csrc/numerics.cuh",
                   "bit_consistent_logprob_gb300/csrc/ptx.cuh"]
 HOST_LAUNCH = ("bit_consistent_logprob_gb300/csrc/lp_api.cu",
-               ["encode_kmajor", "scheduling_band", "x_box_rows", "launch_gemm_variant",
+               ["encode_kmajor", "scheduling_band", "x_box_rows", "pick_band", "launch_gemm_variant",
                 "launch_leaf_gemm"])
 FP8_SOURCES = ["bit_consistent_logprob_gb300/csrc/fp8_kernels.cuh"]
 FP8_HOST_LAUNCH = ["quantize_x_chunk", "launch_fp8_gemm", "quantize_weights"]
@@ -363,7 +363,8 @@ def run_rl_epilogue(args, world, rank, local, pg):
 # ----------------------------------------------------------------------------- backward
 def run_backward(args, world, rank, local, pg):
     """The logprob backward over the workload's batch: dl = g (onehot - p) from the forward's
-    logits (the leaf GEMM's gradient epilogue), then dX = dl W and dW = dl^T X (cuBLAS)."""
+    logits (the leaf GEMM's gradient epilogue), then dX = dl W and dW = dl^T X (the library's
+    own tcgen05 GEMMs)."""
     import torch
 
     from bit_consistent_logprob_gb300 import Engine
@@ -404,6 +405,10 @@ def run_backward(args, world, rank, local, pg):
     torch.cuda.synchronize()
     barrier(pg, dev)
     clocks = sampler.stop()
+    from bit_consistent_logprob_gb300._native import LP_PROFILE_GRAD_DW, LP_PROFILE_GRAD_DX
+
+    dx_ms, dx_n = eng.profile_read_kind(LP_PROFILE_GRAD_DX)
+    dw_ms, dw_n = eng.profile_read_kind(LP_PROFILE_GRAD_DW)
     gemm_ms, gemm_n = eng.profile_read()
     eng.profile_enable(False)
     eng.check()
@@ -413,6 +418,15 @@ def run_backward(args, world, rank, local, pg):
     per_launch = 2.0 * T * H * V / (gemm_n / max(1, args.steps))
     achieved = per_launch / (grad_ms / 1000.0) / 1e12
     peak, src = tensor_peak(peaks, peak_src, ms * args.steps / 1000.0, False)
+    # the two GEMMs of the backward, each 2 * T * H * V flop per step, against the same peak
+    grad_gemms = {}
+    for name, tot, cnt in (("dX = dl W (grad_gemm_kernel, K split summed)", dx_ms, dx_n),
+                           ("dW += dl^T X (grad_gemm_kernel)", dw_ms, dw_n)):
+        step_ms = tot / max(1, args.steps)
+        tf = 2.0 * T * H * V / (step_ms / 1000.0) / 1e12 if step_ms > 0 else None
+        grad_gemms[name] = {"ms_per_step": step_ms, "launches_per_step": cnt / max(1, args.steps),
+                            "achieved": tf, "unit": "TFLOP/s", "peak": peak,
+                            "frac": tf / peak if tf else None}
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "peak_source": src,
             "traffic": None, "kernel": "leaf_gemm_kernel<gradient epilogue>",
@@ -443,8 +457,8 @@ def run_backward(args, world, rank, local, pg):
         "config": {"workload": wl.name + "+backward", "T": T, "H": H, "V": V, "n_leaves": N,
                    "row_chunk": chunk, "step": "lp_logprobs_backward (dX and dW)",
                    "step_tflops": 3 * 2.0 * T * H * V / (ms / 1000.0) / 1e12},
-        "roofline": roof, "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches[0],
-        "clocks": clocks,
+        "roofline": roof, "grad_gemms": grad_gemms, "cpu_baseline": cpu, "e2e": None,
+        "gpu_launches": launches[0], "clocks": clocks,
     }
 
 

@@ -22,6 +22,7 @@ STATUS_NAMES = {
     LP_ERR_OOM: "LP_ERR_OOM", LP_ERR_TIMEOUT: "LP_ERR_TIMEOUT",
 }
 LP_PHASE_AUTO, LP_PHASE_PREFILL, LP_PHASE_DECODE = 0, 1, 2
+LP_PROFILE_LEAF_GEMM, LP_PROFILE_GRAD_DX, LP_PROFILE_GRAD_DW = 0, 1, 2
 
 # Every symbol include/lp.h declares, with its ctypes signature.
 _p = ctypes.c_void_p
@@ -78,6 +79,8 @@ SIGNATURES = {
     "lp_profile_enable": (ctypes.c_int, [_p, ctypes.c_int]),
     "lp_profile_read": (ctypes.c_int, [_p, ctypes.POINTER(ctypes.c_double),
                                        ctypes.POINTER(ctypes.c_int32)]),
+    "lp_profile_read_kind": (ctypes.c_int, [_p, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                            ctypes.POINTER(ctypes.c_int32)]),
     "lp_logprobs_noalloc": (ctypes.c_int, [_p, _i32, _i32, _i32, _p, _i64, _p, _i64, _p, _p, _p]),
     "lp_noalloc_last_error": (ctypes.c_char_p, []),
     "lp_check": (ctypes.c_int, [_p]),

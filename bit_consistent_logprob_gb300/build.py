@@ -3,7 +3,7 @@
 ``csrc/lp_api.cu`` holds the handle-based C ABI and ``csrc/lp_noalloc.cu`` the
 no-allocation entry point; both instantiate the same kernel templates from
 ``csrc/kernels.cuh`` with the same flags, so they share the pinned numerics.  The library links
-the shared CUDA runtime and cuBLAS (for the two plain GEMMs of the logprob backward) and
+only the shared CUDA runtime (every kernel, the backward's GEMMs included, is its own) and
 resolves the driver's tensor-map encoder at run time (no link against libcuda).
 """
 from __future__ import annotations
@@ -23,14 +23,14 @@ SOURCES = [os.path.join(CSRC, "lp_api.cu"), os.path.join(CSRC, "lp_noalloc.cu"),
            os.path.join(CSRC, "lp_contract.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("kernels.cuh", "numerics.cuh", "ptx.cuh",
                                                   "rl_kernels.cuh", "lp_internal.h",
-                                                  "fp8_kernels.cuh")] + [
+                                                  "fp8_kernels.cuh", "grad_gemm.cuh")] + [
     os.path.join(INCLUDE, "lp.h")]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", *ARCH_FLAGS, "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-shared", "-cudart", "shared",
               "-I", INCLUDE, "-I", CSRC]
-LINK_FLAGS = ["-lcublas"]  # the backward's two plain GEMMs (dX = dl W, dW = dl^T X)
+LINK_FLAGS: list = []
 
 
 def nvcc() -> str:

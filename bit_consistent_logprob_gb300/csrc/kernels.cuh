@@ -54,7 +54,8 @@ struct GemmParams {
     int32_t num_row_tiles;    // ceil(T / 128)
     int32_t num_vocab_tiles;  // ceil(V / 128)
     int32_t num_lse_tiles;    // ceil(V / 64)
-    int32_t band;             // vocabulary tiles per scheduling band
+    int32_t band;             // scheduling units per band (along band_axis)
+    int32_t band_axis;        // 0: bands of vocabulary tiles; 1: bands of rows (tiles or pairs)
     int32_t x_box_rows;       // rows per X TMA box (128, or T rounded up to 8 when T < 128)
     const int32_t* ids;       // [T] sampled ids (fused path)
     float2* ws_ms;            // [num_lse_tiles][ws_ld] (max, sum-exp) per 64-column tile (fused)
@@ -122,19 +123,32 @@ static_assert(gemm_smem_bytes(1, kModeGrad) <= 227 * 1024 &&
                   gemm_smem_bytes(1, kModeLse, true) <= 227 * 1024,
               "leaf-GEMM shared memory exceeds the per-CTA limit");
 
-// Tile schedule: the vocabulary is cut into bands of `band` tiles; within a band the
-// tiles run row by row (a row tile, or the two row tiles of a CTA pair), vocabulary fastest.
-// Concurrent CTAs therefore share the band's W tiles and a few X row tiles in L2.  The
-// schedule decides only which CTA computes a tile, never how.
+// Tile schedule.  Vocabulary bands (band_axis 0): the vocabulary is cut into bands of `band`
+// tiles; within a band the tiles run row by row (a row tile, or the two row tiles of a CTA
+// pair), vocabulary fastest, so concurrent CTAs share the band's W tiles (kept in L2) and a
+// few X rows; X is read once per band.  Row bands (band_axis 1): the rows are cut into bands of
+// `band` rows; within a band the tiles run vocabulary tile by vocabulary tile, rows fastest,
+// so the band's X rows stay in L2 and W is read once per band.  The schedule decides only
+// which CTA computes a tile, never how.
 __device__ __forceinline__ void tile_coords(int tile, int num_rows, const GemmParams& p, int& rt,
                                             int& vt) {
-    const int per_band = num_rows * p.band;
-    const int b = tile / per_band;
-    const int r = tile - b * per_band;
-    const int vt0 = b * p.band;
-    const int width = min(p.band, p.num_vocab_tiles - vt0);
-    rt = r / width;
-    vt = vt0 + (r - rt * width);
+    if (p.band_axis == 0) {
+        const int per_band = num_rows * p.band;
+        const int b = tile / per_band;
+        const int r = tile - b * per_band;
+        const int vt0 = b * p.band;
+        const int width = min(p.band, p.num_vocab_tiles - vt0);
+        rt = r / width;
+        vt = vt0 + (r - rt * width);
+    } else {
+        const int per_band = p.num_vocab_tiles * p.band;
+        const int b = tile / per_band;
+        const int r = tile - b * per_band;
+        const int r0 = b * p.band;
+        const int height = min(p.band, num_rows - r0);
+        vt = r / height;
+        rt = r0 + (r - vt * height);
+    }
 }
 
 // A wait ran out: stop this CTA's warps (and, in a pair, the partner's) and record it.

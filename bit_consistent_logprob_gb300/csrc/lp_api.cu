@@ -9,7 +9,6 @@
 // phase, so every row is bit-identical however it is batched.
 #include <cuda.h>
 #include <cudaTypedefs.h>
-#include <cublas_v2.h>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -19,6 +18,7 @@
 #include <string>
 #include <vector>
 
+#include "grad_gemm.cuh"
 #include "kernels.cuh"
 #include "lp.h"
 #include "fp8_kernels.cuh"
@@ -119,8 +119,7 @@ struct lp_handle {
     uint16_t* dl = nullptr;       // [dl_rows][ldd] bf16 gradient with respect to the logits
     int64_t dl_rows = 0;
     int64_t ldd = 0;
-    cublasHandle_t cublas = nullptr;
-    void* cublas_ws = nullptr;
+    float* grad_part = nullptr;   // [kMaxGradSlices][dl_rows][H] fp32: dX partials of a K split
     float* zy = nullptr;          // [max_tokens]
     int* status = nullptr;        // sticky status word
     int* sched = nullptr;         // tile counter of the pair launches' dynamic schedule
@@ -164,9 +163,12 @@ struct lp_handle {
     bool force_single_cta = false;
     bool force_sub1 = false;
     int band = 0;  // vocabulary tiles per scheduling band (even); schedule only
+    int band_axis_env = -1;  // LP_BAND_AXIS: -1 = chosen per launch, 0 = vocabulary, 1 = rows
+    int band_rows_env = 0;   // LP_BAND_ROWS: scheduling rows per row band (0 = from the budget)
     // profiling: event pairs around leaf-GEMM launches
     bool profiling = false;
     std::vector<cudaEvent_t> prof_events;  // 2 * kProfPairs, created on enable
+    std::vector<int> prof_kind;            // what each pair brackets (LP_PROFILE_*)
     int prof_used = 0;                     // pairs recorded since the last read
 };
 
@@ -205,6 +207,42 @@ int scheduling_band(int H, int bytes_per_weight, int max_tiles, int mib) {
     int64_t b = (static_cast<int64_t>(mib) << 20) / per_tile;
     b = b < 8 ? 8 : (b > max_tiles ? max_tiles : b);
     return static_cast<int>(b) & ~1;
+}
+
+// Profiling: a pair of events on the launch stream around one timed kernel (or group).
+bool prof_begin(lp_handle* h, cudaStream_t st, int kind) {
+    if (!h->profiling || h->prof_used >= kProfPairs) return false;
+    h->prof_kind[h->prof_used] = kind;
+    return cudaEventRecord(h->prof_events[2 * h->prof_used], st) == cudaSuccess;
+}
+
+cudaError_t prof_end(lp_handle* h, cudaStream_t st) {
+    const cudaError_t e = cudaEventRecord(h->prof_events[2 * h->prof_used + 1], st);
+    ++h->prof_used;
+    return e;
+}
+
+// The band of one bf16 leaf-GEMM launch (see tile_coords).  Vocabulary bands of h->band
+// tiles (32 MiB of W) by default; LP_BAND_AXIS=rows switches to row bands of LP_BAND_ROWS
+// scheduling rows (default: 32 MiB of X).  Measured on GB300 (DRAM reads per launch, time):
+// at the 32 MiB budget row bands read less (H 2048, V 151936, 17627 rows: 1.3 GB against
+// 2.0 GB; H 4096, V 151936, 32768 rows: 10.2 GB against 11.5 GB) but run 1-1.5 % slower at
+// the larger shapes; resident bands beyond ~32 MiB, on either axis, thrash L2 (H 7168,
+// V 129280, 16384 rows: 28 GB with 36 vocabulary tiles, 71 GB with 22 row pairs, against
+// 15.8 GB).  The band moves data, never arithmetic.
+constexpr int kBandMiB = 32;
+void pick_band(const lp_handle* h, int rows, bool pair, int32_t& axis, int32_t& band) {
+    (void)rows;
+    axis = h->band_axis_env == 1 ? 1 : 0;
+    if (axis == 0) {
+        band = h->band;
+        return;
+    }
+    const int64_t unit_rows = pair ? 2 * lp::kBM : lp::kBM;  // rows per scheduling row
+    int64_t rband = h->band_rows_env > 0
+                        ? h->band_rows_env
+                        : (int64_t(kBandMiB) << 20) / (unit_rows * int64_t(h->cfg.H) * 2);
+    band = static_cast<int32_t>(rband < 1 ? 1 : rband);
 }
 
 template <int kMode, int kSub, bool kPair = false>
@@ -275,7 +313,6 @@ int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int lea
     p.num_row_tiles = static_cast<int32_t>(ceil_div(rows, lp::kBM));
     p.num_vocab_tiles = h->num_vocab_tiles;
     p.num_lse_tiles = h->num_lse_tiles;
-    p.band = h->band;
     p.ids = ids;
     p.ws_ms = h->ws_ms;
     p.ws_ld = h->cfg.max_tokens;
@@ -292,6 +329,7 @@ int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int lea
     p.timeout_ns = h->timeout_ns;
     const bool sub2 = h->leaf_len % (2 * lp::kBK) == 0 && rows > kShortStageRows && !h->force_sub1;
     const bool pair = rows > lp::kBM && !h->force_single_cta;
+    pick_band(h, rows, pair, p.band_axis, p.band);
     p.x_box_rows = static_cast<int32_t>(x_box_rows(rows));
     CUtensorMap tmX;
     int rc = encode_kmajor(&tmX, X, static_cast<uint64_t>(rows), h->cfg.H, ldx,
@@ -311,8 +349,7 @@ int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int lea
     const int grid = static_cast<int>((tiles < slots ? tiles : slots) * (pair ? 2 : 1));
     // a pair launch hands out its tiles from a counter that starts at zero
     if (pair) LP_CUDA(cudaMemsetAsync(h->sched, 0, sizeof(int), st), "tile counter reset");
-    const bool prof = h->profiling && h->prof_used < kProfPairs;
-    if (prof) LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used], st), "profile event");
+    const bool prof = prof_begin(h, st, LP_PROFILE_LEAF_GEMM);
     cudaError_t e;
     if (pair)
         e = sub2 ? launch_gemm_variant<kMode, 2, true>(grid, st, tmX, h->tmW64, tmD, p)
@@ -322,10 +359,7 @@ int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int lea
                  : launch_gemm_variant<kMode, 1>(grid, st, tmX, h->tmW, tmD, p);
     LP_CUDA(e, "leaf_gemm_kernel launch");
     LP_CUDA(cudaGetLastError(), "leaf_gemm_kernel launch");
-    if (prof) {
-        LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used + 1], st), "profile event");
-        ++h->prof_used;
-    }
+    if (prof) LP_CUDA(prof_end(h, st), "profile event");
     ++h->last_launches;
     return LP_OK;
 }
@@ -448,15 +482,11 @@ int launch_fp8_gemm(lp_handle* h, int rows, int leaf_begin, int leaf_count, cons
     const int64_t tiles = static_cast<int64_t>(p.num_row_tiles) * h->num_vocab_tiles;
     if (tiles > 0x7fffffff) return fail(LP_ERR_UNSUPPORTED, "too many tiles in one launch");
     const int grid = static_cast<int>(tiles < h->num_sms ? tiles : h->num_sms);
-    const bool prof = h->profiling && h->prof_used < kProfPairs;
-    if (prof) LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used], st), "profile event");
+    const bool prof = prof_begin(h, st, LP_PROFILE_LEAF_GEMM);
     lp::leaf_gemm_fp8_kernel<kMode><<<grid, lp::kGemmThreads, lp::fp8_smem_bytes(), st>>>(
         tmX, h->tmWq, p);
     LP_CUDA(cudaGetLastError(), "leaf_gemm_fp8_kernel launch");
-    if (prof) {
-        LP_CUDA(cudaEventRecord(h->prof_events[2 * h->prof_used + 1], st), "profile event");
-        ++h->prof_used;
-    }
+    if (prof) LP_CUDA(prof_end(h, st), "profile event");
     ++h->last_launches;
     return LP_OK;
 }
@@ -567,8 +597,7 @@ void lp_free(lp_handle* h) {
     cudaFree(h->xq);
     cudaFree(h->sx);
     cudaFree(h->dl);
-    cudaFree(h->cublas_ws);
-    if (h->cublas) cublasDestroy(h->cublas);
+    cudaFree(h->grad_part);
     cudaFree(h->blk_sum);
     cudaFree(h->blk_cnt);
     cudaFree(h->stat_blk);
@@ -627,6 +656,14 @@ int init_impl(const lp_config* cfg, const void* W, void* stream, lp_handle** out
     if (const char* e = std::getenv("LP_BAND")) {
         const int b = std::atoi(e);
         if (b >= 2 && b <= 1024) h->band = b & ~1;
+    }
+    if (const char* e = std::getenv("LP_BAND_AXIS")) {
+        if (std::strcmp(e, "vocab") == 0) h->band_axis_env = 0;
+        if (std::strcmp(e, "rows") == 0) h->band_axis_env = 1;
+    }
+    if (const char* e = std::getenv("LP_BAND_ROWS")) {
+        const int b = std::atoi(e);
+        if (b >= 1 && b <= 1 << 20) h->band_rows_env = b;
     }
     h->band_fp8 = scheduling_band(cfg->H, 1, 128, 28);  // e4m3 weights: twice the tiles per byte
     h->fp8 = fp8;
@@ -835,11 +872,70 @@ int lp_logprobs_entropy(lp_handle* h, const void* X, int64_t ldx, const int32_t*
 }
 
 namespace {
-constexpr size_t kCublasWorkspace = size_t(32) << 20;
+// K splits of the dX GEMM: at most kMaxGradSlices fp32 partials of [rows][H].
+constexpr int kMaxGradSlices = 4;
 
-int cublas_fail(cublasStatus_t s, const char* what) {
-    return fail(LP_ERR_CUDA, "%s: cuBLAS status %d", what, static_cast<int>(s));
+// Slices of K for a launch of `units` pair tiles on `clusters` SM pairs: the count that fills
+// the most of its last wave (each slice costs one fp32 partial and its share of the sum); a
+// larger count must win by 3 % of the cluster-waves.
+int grad_slices(int64_t units, int64_t clusters, int64_t kblocks) {
+    int best = 1;
+    double best_eff = 0.0;
+    for (int sl = 1; sl <= kMaxGradSlices && sl <= kblocks; ++sl) {
+        const int64_t w = units * sl;
+        const double eff = double(w) / double((w + clusters - 1) / clusters * clusters);
+        if (eff > best_eff + 0.03) {
+            best = sl;
+            best_eff = eff;
+        }
+    }
+    return best;
 }
+
+// One backward GEMM, D (+)= A . B over `slices` K slices (slice s writes D + s * slice_stride).
+// tmA: K-major (a_mn = false) or MN-major A; tmB: MN-major B.  Returns the slice count used.
+int launch_grad_gemm(lp_handle* h, bool a_mn, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                     int M, int N, int K, int slices, float* D, int64_t ldd, int64_t slice_stride,
+                     int accumulate, cudaStream_t st, int* used) {
+    lp::GradGemmParams g{};
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.num_m = static_cast<int32_t>(ceil_div(M, lp::kGgTileM));
+    g.num_n = static_cast<int32_t>(ceil_div(N, lp::kGgTileN));
+    const int64_t kblocks = ceil_div(K, lp::kBK);
+    const int64_t per = ceil_div(kblocks, slices);
+    g.num_slices = static_cast<int32_t>(ceil_div(kblocks, per));  // no empty slice
+    g.k_slice = static_cast<int32_t>(per * lp::kBK);
+    g.D = D;
+    g.ldd = ldd;
+    g.slice_stride = slice_stride;
+    g.accumulate = accumulate;
+    g.status = h->status;
+    g.timeout_ns = h->timeout_ns;
+    const int64_t units = int64_t(g.num_slices) * g.num_m * g.num_n;
+    if (units > 0x7fffffff) return fail(LP_ERR_UNSUPPORTED, "too many tiles in one launch");
+    const int64_t clusters = units < h->num_sms / 2 ? units : h->num_sms / 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+    cfg.blockDim = dim3(lp::kGgThreads);
+    cfg.dynamicSmemBytes = lp::kGgSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = a_mn ? cudaLaunchKernelEx(&cfg, lp::grad_gemm_kernel<true>, tmA, tmB, g)
+                               : cudaLaunchKernelEx(&cfg, lp::grad_gemm_kernel<false>, tmA, tmB, g);
+    LP_CUDA(e, "grad_gemm_kernel launch");
+    ++h->last_launches;
+    if (used) *used = g.num_slices;
+    return LP_OK;
+}
+
 }  // namespace
 
 int lp_backward_reserve(lp_handle* h, int64_t max_rows) {
@@ -849,30 +945,37 @@ int lp_backward_reserve(lp_handle* h, int64_t max_rows) {
     if (max_rows <= h->dl_rows) return LP_OK;
     const int64_t ldd = ceil_div(h->cfg.V, 8) * 8;
     void* p = nullptr;
+    void* q = nullptr;
     const size_t bytes = sizeof(uint16_t) * static_cast<size_t>(max_rows) * ldd;
+    const size_t pbytes =
+        sizeof(float) * static_cast<size_t>(kMaxGradSlices) * max_rows * h->cfg.H;
     cudaError_t e = cudaMalloc(&p, bytes);
+    if (e == cudaSuccess) {
+        e = cudaMalloc(&q, pbytes);
+        if (e != cudaSuccess) cudaFree(p);
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
-        return fail(LP_ERR_OOM, "backward workspace (%zu bytes): %s", bytes, cudaGetErrorString(e));
+        return fail(LP_ERR_OOM, "backward workspace (%zu + %zu bytes): %s", bytes, pbytes,
+                    cudaGetErrorString(e));
     }
     if (h->dl) {
         LP_CUDA(cudaDeviceSynchronize(), "device synchronize");
         cudaFree(h->dl);
-        h->ws_bytes -= static_cast<int64_t>(sizeof(uint16_t)) * h->dl_rows * h->ldd;
+        cudaFree(h->grad_part);
+        h->ws_bytes -= static_cast<int64_t>(sizeof(uint16_t)) * h->dl_rows * h->ldd +
+                       int64_t(sizeof(float)) * kMaxGradSlices * h->dl_rows * h->cfg.H;
     }
     h->dl = static_cast<uint16_t*>(p);
+    h->grad_part = static_cast<float*>(q);
     h->dl_rows = max_rows;
     h->ldd = ldd;
-    h->ws_bytes += static_cast<int64_t>(bytes);
-    if (h->cublas == nullptr) {
-        cublasStatus_t cs = cublasCreate(&h->cublas);
-        if (cs != CUBLAS_STATUS_SUCCESS) {
-            h->cublas = nullptr;
-            return cublas_fail(cs, "cublasCreate");
-        }
-        LP_CUDA(cudaMalloc(&h->cublas_ws, kCublasWorkspace), "cuBLAS workspace");
-        h->ws_bytes += static_cast<int64_t>(kCublasWorkspace);
-    }
+    h->ws_bytes += static_cast<int64_t>(bytes + pbytes);
+    for (const void* fn : {reinterpret_cast<const void*>(lp::grad_gemm_kernel<false>),
+                           reinterpret_cast<const void*>(lp::grad_gemm_kernel<true>)})
+        LP_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     lp::kGgSmemBytes),
+                "cudaFuncSetAttribute(grad_gemm_kernel)");
     return LP_OK;
 }
 
@@ -887,6 +990,8 @@ int lp_logprobs_backward(lp_handle* h, const void* X, int64_t ldx, const int32_t
         return fail(LP_ERR_INVALID_ARG, "call lp_backward_reserve before lp_logprobs_backward");
     if (T > 0 && (ids == nullptr || logZ == nullptr || grad_logp == nullptr))
         return fail(LP_ERR_INVALID_ARG, "ids, logZ and grad_logp must not be NULL");
+    if ((dX != nullptr && !aligned16(dX)) || (dW != nullptr && !aligned16(dW)))
+        return fail(LP_ERR_INVALID_ARG, "dX and dW must be 16-byte aligned");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     h->last_stream = st;
     h->last_launches = 0;
@@ -894,12 +999,12 @@ int lp_logprobs_backward(lp_handle* h, const void* X, int64_t ldx, const int32_t
     if (dW != nullptr && !accumulate)
         LP_CUDA(cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * H, st), "dW clear");
     if (T == 0 || (dX == nullptr && dW == nullptr)) return LP_OK;
-    cublasStatus_t cs;
-    if ((cs = cublasSetStream(h->cublas, st)) != CUBLAS_STATUS_SUCCESS ||
-        (cs = cublasSetWorkspace(h->cublas, h->cublas_ws, kCublasWorkspace)) != CUBLAS_STATUS_SUCCESS)
-        return cublas_fail(cs, "cublasSetStream/cublasSetWorkspace");
-    const float one = 1.0f, zero = 0.0f;
     const uint8_t* xb = static_cast<const uint8_t*>(X);
+    // W as the B operand of dX: [K = V][N = H], MN-major 64 x 64 boxes (one tensor map for all
+    // chunks)
+    CUtensorMap tmWB;
+    rc = encode_kmajor(&tmWB, h->W, static_cast<uint64_t>(V), H, H, 64);
+    if (rc != LP_OK) return rc;
     for (int64_t r0 = 0; r0 < T; r0 += h->dl_rows) {
         const int rows = static_cast<int>(T - r0 < h->dl_rows ? T - r0 : h->dl_rows);
         const void* Xc = xb + r0 * ldx * 2;
@@ -911,19 +1016,42 @@ int lp_logprobs_backward(lp_handle* h, const void* X, int64_t ldx, const int32_t
         rc = launch_leaf_gemm<lp::kModeGrad>(h, Xc, ldx, rows, 0, h->cfg.n_leaves, ids + r0,
                                              nullptr, 0, st, ga);
         if (rc != LP_OK) return rc;
-        // row-major [r][c] buffers seen column-major: dX^T = W^T dl^T, dW^T = X^T dl
         if (dX != nullptr) {
-            cs = cublasGemmEx(h->cublas, CUBLAS_OP_N, CUBLAS_OP_N, H, rows, V, &one, h->W,
-                              CUDA_R_16BF, H, h->dl, CUDA_R_16BF, static_cast<int>(h->ldd), &zero,
-                              dX + r0 * H, CUDA_R_32F, H, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-            if (cs != CUBLAS_STATUS_SUCCESS) return cublas_fail(cs, "dX GEMM");
+            // dX = dl W: A = dl [rows][V] K-major (64 x 128 boxes), split over K = V when the
+            // tiles alone leave most of the last wave empty
+            CUtensorMap tmA;
+            rc = encode_kmajor(&tmA, h->dl, static_cast<uint64_t>(rows), V, h->ldd);
+            if (rc != LP_OK) return rc;
+            const int64_t units = ceil_div(rows, lp::kGgTileM) * ceil_div(H, lp::kGgTileN);
+            const int slices = grad_slices(units, h->num_sms / 2, ceil_div(V, lp::kBK));
+            float* dXc = dX + r0 * H;
+            const bool prof = prof_begin(h, st, LP_PROFILE_GRAD_DX);
+            int used = 1;
+            rc = launch_grad_gemm(h, false, tmA, tmWB, rows, H, V, slices,
+                                  slices == 1 ? dXc : h->grad_part, H, int64_t(rows) * H, 0, st,
+                                  &used);
+            if (rc != LP_OK) return rc;
+            if (used > 1) {
+                const int64_t n = int64_t(rows) * H;
+                const int64_t blocks = ceil_div(n / 4, 256);
+                lp::splitk_sum_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0,
+                                        st>>>(h->grad_part, used, n, n, dXc);
+                LP_CUDA(cudaGetLastError(), "splitk_sum_kernel launch");
+                ++h->last_launches;
+            }
+            if (prof) LP_CUDA(prof_end(h, st), "profile event");
         }
         if (dW != nullptr) {
-            cs = cublasGemmEx(h->cublas, CUBLAS_OP_N, CUBLAS_OP_T, H, V, rows, &one, Xc,
-                              CUDA_R_16BF, static_cast<int>(ldx), h->dl, CUDA_R_16BF,
-                              static_cast<int>(h->ldd), &one, dW, CUDA_R_32F, H,
-                              CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-            if (cs != CUBLAS_STATUS_SUCCESS) return cublas_fail(cs, "dW GEMM");
+            // dW += dl^T X: A = dl seen as [K = rows][M = V], B = X as [K = rows][N = H], both
+            // MN-major 64 x 64 boxes; one K slice, so each dW element has one writer per chunk
+            CUtensorMap tmA, tmB;
+            rc = encode_kmajor(&tmA, h->dl, static_cast<uint64_t>(rows), V, h->ldd, 64);
+            if (rc == LP_OK) rc = encode_kmajor(&tmB, Xc, static_cast<uint64_t>(rows), H, ldx, 64);
+            if (rc != LP_OK) return rc;
+            const bool prof = prof_begin(h, st, LP_PROFILE_GRAD_DW);
+            rc = launch_grad_gemm(h, true, tmA, tmB, V, H, rows, 1, dW, H, 0, 1, st, nullptr);
+            if (rc != LP_OK) return rc;
+            if (prof) LP_CUDA(prof_end(h, st), "profile event");
         }
     }
     return LP_OK;
@@ -1406,6 +1534,7 @@ int lp_profile_enable(lp_handle* h, int enable) {
     if (h == nullptr) return fail(LP_ERR_INVALID_ARG, "handle is NULL");
     if (enable && h->prof_events.empty()) {
         h->prof_events.resize(2 * kProfPairs);
+        h->prof_kind.assign(kProfPairs, 0);
         for (auto& e : h->prof_events) LP_CUDA(cudaEventCreate(&e), "cudaEventCreate");
     }
     h->profiling = enable != 0;
@@ -1413,21 +1542,31 @@ int lp_profile_enable(lp_handle* h, int enable) {
     return LP_OK;
 }
 
-int lp_profile_read(lp_handle* h, double* gemm_ms_total, int32_t* gemm_launches) {
-    if (h == nullptr || gemm_ms_total == nullptr)
-        return fail(LP_ERR_INVALID_ARG, "handle and gemm_ms_total must not be NULL");
+int lp_profile_read_kind(lp_handle* h, int kind, double* ms_total, int32_t* count) {
+    if (h == nullptr || ms_total == nullptr)
+        return fail(LP_ERR_INVALID_ARG, "handle and ms_total must not be NULL");
     double total = 0.0;
+    int32_t n = 0;
     for (int i = 0; i < h->prof_used; ++i) {
+        if (h->prof_kind[i] != kind) continue;
         LP_CUDA(cudaEventSynchronize(h->prof_events[2 * i + 1]), "cudaEventSynchronize");
         float ms = 0.0f;
         LP_CUDA(cudaEventElapsedTime(&ms, h->prof_events[2 * i], h->prof_events[2 * i + 1]),
                 "cudaEventElapsedTime");
         total += ms;
+        ++n;
     }
-    *gemm_ms_total = total;
-    if (gemm_launches) *gemm_launches = h->prof_used;
-    h->prof_used = 0;
+    *ms_total = total;
+    if (count) *count = n;
     return LP_OK;
+}
+
+int lp_profile_read(lp_handle* h, double* gemm_ms_total, int32_t* gemm_launches) {
+    if (h == nullptr || gemm_ms_total == nullptr)
+        return fail(LP_ERR_INVALID_ARG, "handle and gemm_ms_total must not be NULL");
+    const int rc = lp_profile_read_kind(h, LP_PROFILE_LEAF_GEMM, gemm_ms_total, gemm_launches);
+    h->prof_used = 0;
+    return rc;
 }
 
 int lp_selftest_wait_timeout(lp_handle* h, int64_t timeout_us, void* stream) {

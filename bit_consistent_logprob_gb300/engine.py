@@ -458,6 +458,15 @@ class Engine:
         """Bracket every leaf-GEMM launch with CUDA events on its stream."""
         _native.check(self._lib.lp_profile_enable(self._h, int(bool(enable))))
 
+    def profile_read_kind(self, kind: int):
+        """(total milliseconds, count) of one timed kind (_native.LP_PROFILE_*) since the last
+        profile_read, without clearing; synchronises."""
+        ms = ctypes.c_double()
+        n = ctypes.c_int32()
+        _native.check(self._lib.lp_profile_read_kind(self._h, int(kind), ctypes.byref(ms),
+                                                     ctypes.byref(n)))
+        return ms.value, n.value
+
     def profile_read(self):
         """(total leaf-GEMM milliseconds, launches) since the last read; synchronises."""
         ms = ctypes.c_double()

@@ -110,6 +110,9 @@ typedef struct lp_handle lp_handle; /* opaque, owned by the library */
  *   LP_FORCE_SINGLE_CTA=1    one CTA per tile instead of CTA pairs (cta_group::2) for
  *                            launches of more than 128 rows;
  *   LP_FORCE_SHORT_STAGES=1  64-K pipeline stages for every launch;
+ *   LP_BAND_AXIS=rows        schedule bf16 launches in bands of rows (X kept in L2, W read
+ *                            once per band) instead of bands of vocabulary tiles;
+ *   LP_BAND_ROWS=<n>         scheduling rows (row tiles, or row-tile pairs) per row band;
  *   LP_BAND=<even n>         vocabulary tiles per scheduling band of bf16 handles (2..1024).
  *   LP_WAIT_TIMEOUT_MS=<ms>  bound on every in-kernel wait (default 2000); on expiry the
  *                            sticky status reads LP_ERR_TIMEOUT.
@@ -300,8 +303,10 @@ LP_API int lp_fp8_quantize_x(lp_handle* h, const void* X, int64_t ldx, int64_t T
  *   dX[t,:] = sum_v dl[t,v] W[v,:]                            fp32 [T][H] (row stride H)
  *   dW[v,:] = sum_t dl[t,v] X[t,:]  (added to dW if accumulate) fp32 [V][H]
  * z is recomputed by the forward's leaf GEMM and tree (the same kernel, a third epilogue),
- * so dl uses exactly the forward's logits.  The two products are plain GEMMs (cuBLAS, fp32
- * accumulation).  The pages' recipe keeps forward values from the inference kernel and
+ * so dl uses exactly the forward's logits.  The two products are the library's own tcgen05
+ * GEMMs (bf16 operands, fp32 accumulation in TMEM); dX may be split over K = V into at most 4
+ * fp32 partials that are added in slice order, and every dW element has one writer per row
+ * chunk.  The pages' recipe keeps forward values from the inference kernel and
  * differentiates a separate training graph, whose backward need only be correct, not
  * deterministic (vLLM blog "Finish RL training faster", section 3.1); this backward is
  * deterministic for a given T and chunking but is not covered by the invariance guarantees.
@@ -314,8 +319,8 @@ LP_API int lp_logprobs_backward(lp_handle* h, const void* X, int64_t ldx, const 
 
 /*
  * Reserve the backward's workspace for row chunks of max_rows rows: a bf16 buffer
- * [max_rows][ceil(V/8)*8] (e.g. 4096 rows at V = 151936: 1.24 GB) and a cuBLAS handle with
- * a 32 MiB workspace.  Allocates and may synchronise the device: call it before any graph
+ * [max_rows][ceil(V/8)*8] (e.g. 4096 rows at V = 151936: 1.24 GB) and fp32 K-split partials
+ * of dX [4][max_rows][H] (e.g. 134 MB at H = 2048).  Allocates and may synchronise the device: call it before any graph
  * capture.  A smaller request than the current reservation is a no-op.
  */
 LP_API int lp_backward_reserve(lp_handle* h, int64_t max_rows);
@@ -413,13 +418,17 @@ LP_API int lp_reinforce_zero(lp_handle* h, const float* logp_pi, const float* lo
 
 /*
  * Kernel timing for profiling.  While enabled, every leaf-GEMM launch (the dominant
- * kernel) is bracketed by a pair of CUDA events recorded on the launch stream (at
- * most 4096 pairs are kept).  lp_profile_read synchronises, returns the summed
- * duration in milliseconds and the number of launches recorded since the last
- * read, and clears the record.  Enabling creates the events (not graph-capturable).
+ * kernel), and each of the backward's two GEMMs (dX with its K-split sum; dW), is bracketed
+ * by a pair of CUDA events recorded on the launch stream (at most 4096 pairs are kept).
+ * lp_profile_read_kind synchronises and returns the summed duration in milliseconds and the
+ * number of pairs of one kind (LP_PROFILE_*) recorded since the last lp_profile_read;
+ * lp_profile_read does the same for the leaf GEMM and clears the record.  Enabling creates
+ * the events (not graph-capturable).
  */
+enum { LP_PROFILE_LEAF_GEMM = 0, LP_PROFILE_GRAD_DX = 1, LP_PROFILE_GRAD_DW = 2 };
 LP_API int lp_profile_enable(lp_handle* h, int enable);
 LP_API int lp_profile_read(lp_handle* h, double* gemm_ms_total, int32_t* gemm_launches);
+LP_API int lp_profile_read_kind(lp_handle* h, int kind, double* ms_total, int32_t* count);
 
 /*
  * lp_logprobs without a handle and without any device allocation.  (The pages have no

@@ -84,8 +84,9 @@ def _bf16_f64(t):
 @pytest.mark.parametrize("T,H,V,N,chunk", [
     (300, 256, 4001, 4, 300),     # 3 row tiles, ragged vocabulary, one chunk
     (300, 256, 4001, 4, 128),     # three backward chunks accumulate into dW
-    (300, 256, 4001, 4, 200),     # a two-row-tile chunk (W-sharing pairs), then a ragged one
+    (300, 256, 4001, 4, 200),     # a two-row-tile chunk (a CTA pair), then a ragged one
     (97, 512, 32001, 8, 97),      # one partial row tile, leaves of 64
+    (130, 384, 1000, 2, 130),     # H not a multiple of the 256-column GEMM tile
 ])
 def test_backward_matches_oracle(dev, T, H, V, N, chunk):
     X = inputs.hidden_states(T, H, seed=T + V, device=dev)
@@ -180,3 +181,32 @@ def test_entropy_qwen_shape_rows(dev):
     want = oracle.entropy(X.cpu(), W.cpu(), rows=rows)
     err = np.abs(ent.cpu().double().numpy()[rows] - want).max()
     assert err <= 1e-4, err
+
+
+def test_backward_qwen_shape_dw_rows(dev):
+    # Qwen-shape lm_head (H = 2048, V = 151936), 600 rows in chunks of 256: selected rows of dW
+    # (tile edges, the last vocabulary row, and rows that are sampled ids) against an fp64
+    # reference dW[v] = sum_t dl[t, v] X[t], with dl[t, v] = g_t (1[v = y_t] - e^(z - logZ_t))
+    # from the exact logits and the forward's logZ; the bound allows the bf16 rounding of dl.
+    T, H, V, N = 600, 2048, 151936, 8
+    X = inputs.hidden_states(T, H, seed=1002, device=dev)
+    W = inputs.lm_head(V, H, seed=1002, device=dev)
+    ids = inputs.uniform_ids(T, V, seed=1002, device=dev)
+    g = torch.randn(T, generator=torch.Generator().manual_seed(6), dtype=torch.float32).to(dev)
+    with Engine(W, n_leaves=N, max_tokens=T) as eng:
+        _, lz = eng.logprobs(X, ids, return_logZ=True)
+        eng.backward_reserve(256)
+        _, dW = eng.logprobs_backward(X, ids, lz, g, need_dX=False)
+        eng.check()
+    ids_h = ids.cpu().numpy()
+    vs = np.array(sorted({0, 1, 127, 128, 255, 256, 75000, V - 1, *ids_h[[0, 299, 599]].tolist()}))
+    Xd = _bf16_f64(X)                               # [T, H]
+    Wd = _bf16_f64(W[torch.as_tensor(vs, device=dev)])  # [S, H]
+    z = Xd @ Wd.T                                   # exact-ish fp64 logits [T, S]
+    onehot = (ids_h[:, None] == vs[None, :]).astype(np.float64)
+    dl = g.cpu().double().numpy()[:, None] * (onehot - np.exp(z - lz.cpu().double().numpy()[:, None]))
+    want = dl.T @ Xd                                # [S, H]
+    got = dW[torch.as_tensor(vs, device=dev)].cpu().double().numpy()
+    bound = (2.0 ** -8) * (np.abs(dl).T @ np.abs(Xd)) + 1e-6 * np.abs(want).max()
+    err = np.abs(got - want)
+    assert np.all(err <= bound), (err / np.maximum(bound, 1e-30)).max()

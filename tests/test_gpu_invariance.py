@@ -277,6 +277,22 @@ def test_launch_layout_changes_no_bits(data, eng, env, monkeypatch):
         assert_bit_equal(a, b, env + " entropy step")
 
 
+@pytest.mark.parametrize("band", ["1", "3", "7"])
+def test_row_bands_change_no_bits(data, eng, band, monkeypatch):
+    # Row bands (X rows kept in L2 while the vocabulary sweeps past them) instead of
+    # vocabulary bands: only the order in which tiles are handed out changes.
+    X, W, ids = data
+    T = 3000
+    base, baseZ = eng.logprobs(X[:T], ids[:T], return_logZ=True)
+    monkeypatch.setenv("LP_BAND_AXIS", "rows")
+    monkeypatch.setenv("LP_BAND_ROWS", band)
+    with Engine(W, n_leaves=N, max_tokens=T) as e2:
+        other, otherZ = e2.logprobs(X[:T], ids[:T], return_logZ=True)
+        e2.check()
+    assert_bit_equal(other, base, f"row bands of {band}")
+    assert_bit_equal(otherZ, baseZ, f"row bands of {band} logZ")
+
+
 @pytest.mark.parametrize("T", [129, 200, 256, 383])
 def test_pairs_with_a_ragged_partner_change_no_bits(data, eng, T, monkeypatch):
     # Calls of 129-256 rows (decode batches of two row tiles) and an odd number of row tiles
