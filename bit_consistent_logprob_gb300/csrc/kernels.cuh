@@ -74,6 +74,7 @@ struct GemmParams {
     const float* sw;          // [num_vocab_tiles][nkb] weight block scales (block-FP8 kernel)
     int32_t nkb;              // 128-K blocks over H (block-FP8 kernel)
     int* sched;               // tile counter of a pair launch's dynamic schedule (zero at launch)
+    int32_t test_stop_after;  // test hook: the producer stops after this many stages (0 = off)
     int* status;              // sticky device status word
     uint64_t timeout_ns;      // bound on every mbarrier wait
 };
@@ -395,6 +396,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         tma_load_2d_elect(&tmW, &full[stage], wdst, k0, w0);
                     }
                     ++issued;
+                    // test hook: stop as if this warp's own wait had run out (the consumers'
+                    // bounded waits then expire and the abort path runs)
+                    if (p.test_stop_after > 0 && issued >= uint64_t(p.test_stop_after)) {
+                        ok = false;
+                        break;
+                    }
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;

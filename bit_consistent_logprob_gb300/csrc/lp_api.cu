@@ -162,6 +162,7 @@ struct lp_handle {
     // the tests prove that
     bool force_single_cta = false;
     bool force_sub1 = false;
+    int test_stop_after = 0;  // LP_TEST_STOP_AFTER_STAGES: test hook of the abort path
     int band = 0;  // vocabulary tiles per scheduling band (even); schedule only
     int band_axis_env = -1;  // LP_BAND_AXIS: -1 = chosen per launch, 0 = vocabulary, 1 = rows
     int band_rows_env = 0;   // LP_BAND_ROWS: scheduling rows per row band (0 = from the budget)
@@ -326,6 +327,7 @@ int launch_leaf_gemm(lp_handle* h, const void* X, int64_t ldx, int rows, int lea
     p.ldd = ga.ldd;
     p.status = h->status;
     p.sched = h->sched;
+    p.test_stop_after = h->test_stop_after;
     p.timeout_ns = h->timeout_ns;
     const bool sub2 = h->leaf_len % (2 * lp::kBK) == 0 && rows > kShortStageRows && !h->force_sub1;
     const bool pair = rows > lp::kBM && !h->force_single_cta;
@@ -652,6 +654,10 @@ int init_impl(const lp_config* cfg, const void* W, void* stream, lp_handle** out
     h->timeout_ns = timeout_ms * 1000000ull;
     if (const char* e = std::getenv("LP_FORCE_SINGLE_CTA")) h->force_single_cta = e[0] == '1';
     if (const char* e = std::getenv("LP_FORCE_SHORT_STAGES")) h->force_sub1 = e[0] == '1';
+    if (const char* e = std::getenv("LP_TEST_STOP_AFTER_STAGES")) {
+        const int v = std::atoi(e);
+        if (v > 0) h->test_stop_after = v;
+    }
     h->band = scheduling_band(cfg->H, 2, 64, 32);
     if (const char* e = std::getenv("LP_BAND")) {
         const int b = std::atoi(e);

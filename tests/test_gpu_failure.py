@@ -2,7 +2,9 @@
 
 Every pipeline wait in the kernels is bounded (a %globaltimer budget).  The self-test kernel
 waits on an mbarrier that nothing ever arrives on -- a flag that nothing sets -- with that
-same bounded wait; it must give up, raise the sticky timeout status and return.  The host
+same bounded wait; it must give up, raise the sticky timeout status and return.  A test hook
+makes the leaf GEMM's own abort path run: its copy producer stops early, and the kernel must
+drain and return with a timeout status.  The host
 reads the status (LP_ERR_TIMEOUT), clears it, and the context keeps working bit-exactly.
 Bad sampled ids are the other device-side failure: NaN for that row and LP_ERR_INVALID_ARG.
 """
@@ -39,6 +41,41 @@ def test_bounded_wait_reports_timeout_and_context_survives():
         after = eng.logprobs(X, ids)
         eng.check()
     assert_bit_equal(after, before, "after a reported timeout")
+
+
+@pytest.mark.parametrize("T", [100, 300])   # one CTA per tile; CTA pairs (two row-tile pairs)
+def test_leaf_gemm_abort_path_reports_timeout_and_recovers(T, monkeypatch):
+    # The test hook stops the leaf GEMM's copy producer after its first pipeline stage, as if
+    # its own wait had run out.  That stage's copies land and are consumed; the MMA warp's wait
+    # for the next stage then runs out, it raises the abort flag (in a pair, the partner's too)
+    # and drains its MMAs; the epilogue warps see the flag and stop; the producer's drain finds
+    # its one stage complete; TMEM is freed and the kernel returns with nothing in flight.  The
+    # host reads LP_ERR_TIMEOUT, and afterwards the context gives the reference bits.
+    dev = require_cuda()
+    X = inputs.hidden_states(T, 256, seed=5, device=dev)
+    W = inputs.lm_head(4096, 256, seed=5, device=dev)
+    ids = inputs.uniform_ids(T, 4096, seed=5, device=dev)
+    with Engine(W, n_leaves=4, max_tokens=T) as eng:
+        ref = eng.logprobs(X, ids).clone()
+        eng.check()
+    monkeypatch.setenv("LP_WAIT_TIMEOUT_MS", "50")
+    monkeypatch.setenv("LP_TEST_STOP_AFTER_STAGES", "1")
+    with Engine(W, n_leaves=4, max_tokens=T) as hooked:
+        t0 = time.perf_counter()
+        hooked.logprobs(X, ids)
+        with pytest.raises(LpError) as err:
+            hooked.check()
+        elapsed = time.perf_counter() - t0
+        assert err.value.code == LP_ERR_TIMEOUT
+        assert 0.04 < elapsed < 10.0, elapsed
+        hooked.clear_status()
+        hooked.check()
+    monkeypatch.delenv("LP_TEST_STOP_AFTER_STAGES")
+    monkeypatch.delenv("LP_WAIT_TIMEOUT_MS")
+    with Engine(W, n_leaves=4, max_tokens=T) as eng:
+        again = eng.logprobs(X, ids)
+        eng.check()
+    assert_bit_equal(again, ref, "after the abort path ran")
 
 
 def test_bad_id_is_reported_and_isolated():
