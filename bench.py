@@ -602,7 +602,9 @@ def run_ours(args, world, rank, local, pg):
     # end to end through the public API with host buffers (pinned), copies in the region
     e2e = None
     if not args.no_e2e and not args.entropy:
-        Xh = X.cpu().pin_memory()
+        # pinned host copies made directly (no pageable intermediate: 17 GB per rank at is_d3)
+        Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+        Xh.copy_(X)
         idsh = ids.cpu().pin_memory()
         muh = mu.cpu().pin_memory()
         logph = torch.empty(T, dtype=torch.float32).pin_memory()
@@ -698,12 +700,13 @@ def cpu_baseline(X, W, ids, mu, wl, rows: int):
     T = X.shape[0]
     rng = np.random.default_rng(wl.seed)
     sample = np.sort(rng.choice(T, size=min(rows, T), replace=False))
-    Xh, Wh = X.cpu(), W.cpu()
-    idsh = ids.cpu().numpy()
+    idx = torch.as_tensor(sample, device=X.device)
+    Xh, Wh = X[idx].cpu(), W.cpu()        # only the sampled rows travel to the host
+    idsh = ids[idx].cpu().numpy()
     oracle.build()
     t0 = time.perf_counter()
-    logp, _ = oracle.logprobs(Xh, Wh, idsh, rows=sample)
-    oracle.importance_weights(logp.astype(np.float32), mu.cpu().numpy()[sample])
+    logp, _ = oracle.logprobs(Xh, Wh, idsh)
+    oracle.importance_weights(logp.astype(np.float32), mu[idx].cpu().numpy())
     dt = time.perf_counter() - t0
     del torch
     return {"value": len(sample) / dt, "unit": UNIT, "cores": oracle.num_threads(),

@@ -11,7 +11,8 @@
 // The GEMM keeps the K leaves and the fixed leaf tree:
 //   B_kb[t,v] = sum_{k in block kb} qx[t,k] qw[v,k]           tcgen05.mma kind::f8f6f4, fp32
 //   P_j       = sum_{kb in leaf j, ascending} (sx[t,kb] sw[v/128,kb]) B_kb
-//               (first term a product, then one fma per block)
+//               (first term a product, then one fma per block; computed as one fma per
+//               block from -0, which gives the product's bits for the first term)
 //   z         = fixed pairwise tree over P_0..P_{N-1}
 // and the same 64-column tile log-sum-exp and vocabulary combine as the bf16 path.
 //
@@ -319,7 +320,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const float* swr = p.sw + static_cast<int64_t>(vt) * nkb;
             float R[64];
             for (int j = 0; ok && j < n; ++j) {
-                // leaf j: P_j = sum over its blocks of (sx * sw) * B_kb
+                // leaf j: P_j = sum over its blocks of (sx * sw) * B_kb.  The sum starts at -0:
+                // fma(s, B, -0) rounds s * B + (-0) = s * B once, which is exactly the product
+                // (a signed zero included), so every block is one fma and the first block gets
+                // the bits of a plain product.
+#pragma unroll
+                for (int k = 0; k < 64; ++k) R[k] = -0.0f;
                 for (int b = 0; b < bpl; ++b, ++g) {
                     const int kb = kb0 + j * bpl + b;
                     const uint32_t buf = g % kF8Bufs, use = g / kF8Bufs;
@@ -330,16 +336,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     tc_fence_after_sync();
                     {
-                        // both 32-column halves of the block in one TMEM round trip
-                        float P0[32], P1[32];
-                        tmem_ld32x2(lane_base + buf * kVT, P0, lane_base + buf * kVT + 32, P1);
+                        // the block's 64 columns in one TMEM load (one instruction, one wait)
+                        float P[64];
+                        tmem_ld64(lane_base + buf * kVT, P);
+                        const float* P0 = P;
+                        const float* P1 = P + 32;
+                        // two lanes per instruction: each lane of __ffma2_rn is one IEEE
+                        // binary32 fma, so every element gets exactly the bits of __fmaf_rn
+                        const float2 s2 = make_float2(s, s);
 #pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            R[k] = b == 0 ? __fmul_rn(s, P0[k]) : __fmaf_rn(s, P0[k], R[k]);
+                        for (int k = 0; k < 32; k += 2) {
+                            const float2 t = __ffma2_rn(s2, make_float2(P0[k], P0[k + 1]),
+                                                        make_float2(R[k], R[k + 1]));
+                            R[k] = t.x;
+                            R[k + 1] = t.y;
+                        }
 #pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            R[32 + k] = b == 0 ? __fmul_rn(s, P1[k])
-                                               : __fmaf_rn(s, P1[k], R[32 + k]);
+                        for (int k = 0; k < 32; k += 2) {
+                            const float2 t = __ffma2_rn(s2, make_float2(P1[k], P1[k + 1]),
+                                                        make_float2(R[32 + k], R[33 + k]));
+                            R[32 + k] = t.x;
+                            R[33 + k] = t.y;
+                        }
                     }
                     release_buf(&acc_empty[buf]);
                 }
