@@ -328,7 +328,7 @@ def run_rl_epilogue(args, world, rank, local, pg):
     peak = float(peaks["hbm_gbs"])
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "peak_source": f"{peak_src} hbm_gbs",
-            "traffic": None, "kernel": "lp_reinforce_zero (rz_seq_kernel + rz_final_kernel)",
+            "traffic": None, "kernel": "lp_reinforce_zero (rz_seq_kernel)",
             "kernel_ms": rz_ms, "algorithmic_per_launch": algo}
 
     cpu = None
@@ -647,7 +647,7 @@ def run_ours(args, world, rank, local, pg):
     peaks, peak_src = load_peaks()
     is_algo = IS_BYTES_PER_TOKEN * T + 16
     is_gbs = is_algo / (r["is_ms"] / 1000.0) / 1e9
-    epilogue = {"kernel": "lp_importance_weights (is_block_kernel + is_final_kernel)",
+    epilogue = {"kernel": "lp_importance_weights (is_fused_kernel)",
                 "bound": "hbm", "achieved": is_gbs, "peak": float(peaks["hbm_gbs"]),
                 "unit": "GB/s", "frac": is_gbs / float(peaks["hbm_gbs"]),
                 "peak_source": f"{peak_src} hbm_gbs", "kernel_ms": r["is_ms"],

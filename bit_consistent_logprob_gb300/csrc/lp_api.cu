@@ -125,6 +125,7 @@ struct lp_handle {
     int* sched = nullptr;         // tile counter of the pair launches' dynamic schedule
     double* blk_sum = nullptr;    // [max_is_blocks]
     long long* blk_cnt = nullptr; // [max_is_blocks]
+    unsigned* is_done = nullptr;  // blocks done in a one-launch epilogue (IS, statistics, loss); 0 between calls
     double* stat_blk = nullptr;   // [2][max_is_blocks]: sum |d|^2 and sum k3 per block
     float* stat_max = nullptr;    // [max_is_blocks]: max |d| per block
     int64_t max_is_blocks = 0;
@@ -602,6 +603,7 @@ void lp_free(lp_handle* h) {
     cudaFree(h->grad_part);
     cudaFree(h->blk_sum);
     cudaFree(h->blk_cnt);
+    cudaFree(h->is_done);
     cudaFree(h->stat_blk);
     cudaFree(h->stat_max);
     cudaFree(h->tp_parts);
@@ -707,6 +709,7 @@ int init_impl(const lp_config* cfg, const void* W, void* stream, lp_handle** out
                     "blk_sum")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->blk_cnt), sizeof(long long) * h->max_is_blocks,
                     "blk_cnt")) ||
+        (rc = alloc(reinterpret_cast<void**>(&h->is_done), sizeof(unsigned), "is_done")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->stat_blk), 2 * sizeof(double) * h->max_is_blocks,
                     "stat_blk")) ||
         (rc = alloc(reinterpret_cast<void**>(&h->stat_max), sizeof(float) * h->max_is_blocks,
@@ -755,6 +758,7 @@ int init_impl(const lp_config* cfg, const void* W, void* stream, lp_handle** out
         return cleanup(fail(LP_ERR_UNSUPPORTED, "V too large (at most 2^26 columns)"));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if ((e = cudaMemsetAsync(h->status, 0, sizeof(int), st)) != cudaSuccess ||
+        (e = cudaMemsetAsync(h->is_done, 0, sizeof(unsigned), st)) != cudaSuccess ||
         (e = cudaStreamSynchronize(st)) != cudaSuccess)
         return cleanup(cuda_fail(e, "status init"));
     if (fp8) {
@@ -1211,14 +1215,15 @@ int lp_importance_weights(lp_handle* h, const float* logp_pi, const float* logp_
     h->last_launches = 0;
     const int64_t nblk = ceil_div(T, lp::kIsBlock);
     if (nblk > 0) {
-        lp::IsParams p{logp_pi, logp_mu, mask, T, out_w, h->blk_sum, h->blk_cnt};
-        lp::is_block_kernel<<<static_cast<unsigned>(nblk), lp::kIsThreads, 0, st>>>(p);
-        LP_CUDA(cudaGetLastError(), "is_block_kernel launch");
-        ++h->last_launches;
+        // one launch: weights, block partials and (in the last block to finish) the fixed tree
+        lp::IsFusedParams q{{logp_pi, logp_mu, mask, T, out_w, h->blk_sum, h->blk_cnt},
+                            static_cast<int>(nblk), h->is_done, out_d3, out_nvalid};
+        lp::is_fused_kernel<<<static_cast<unsigned>(nblk), lp::kIsThreads, 0, st>>>(q);
+        LP_CUDA(cudaGetLastError(), "is_fused_kernel launch");
+    } else {
+        lp::is_final_kernel<<<1, 1024, 0, st>>>(h->blk_sum, h->blk_cnt, 0, out_d3, out_nvalid);
+        LP_CUDA(cudaGetLastError(), "is_final_kernel launch");
     }
-    lp::is_final_kernel<<<1, 1024, 0, st>>>(h->blk_sum, h->blk_cnt, static_cast<int>(nblk),
-                                            out_d3, out_nvalid);
-    LP_CUDA(cudaGetLastError(), "is_final_kernel launch");
     ++h->last_launches;
     return LP_OK;
 }
@@ -1359,12 +1364,14 @@ int lp_acceptance_stats(lp_handle* h, const float* logp_a, const float* logp_b,
     lp::StatsParams p{logp_a, logp_b, mask, T, h->blk_sum, h->stat_blk,
                       h->stat_blk + h->max_is_blocks, h->stat_max, h->blk_cnt};
     if (nblk > 0) {
-        lp::stats_block_kernel<<<static_cast<unsigned>(nblk), lp::kIsThreads, 0, st>>>(p);
-        LP_CUDA(cudaGetLastError(), "stats_block_kernel launch");
-        ++h->last_launches;
+        // one launch: block partials, the statistics in the last block to finish
+        lp::stats_fused_kernel<<<static_cast<unsigned>(nblk), lp::kIsThreads, 0, st>>>(
+            p, static_cast<int>(nblk), h->is_done, out_stats);
+        LP_CUDA(cudaGetLastError(), "stats_fused_kernel launch");
+    } else {
+        lp::stats_final_kernel<<<1, 1024, 0, st>>>(p, 0, out_stats);
+        LP_CUDA(cudaGetLastError(), "stats_final_kernel launch");
     }
-    lp::stats_final_kernel<<<1, 1024, 0, st>>>(p, static_cast<int>(nblk), out_stats);
-    LP_CUDA(cudaGetLastError(), "stats_final_kernel launch");
     ++h->last_launches;
     return LP_OK;
 }
@@ -1469,17 +1476,20 @@ int lp_reinforce_zero(lp_handle* h, const float* logp_pi, const float* logp_mu,
     p.seq_term = h->blk_sum;
     p.seq_kept = h->blk_cnt;
     p.status = h->status;
+    p.done = h->is_done;
+    p.out_loss = out_loss;
+    p.out_kept = out_n_kept;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     h->last_stream = st;
     h->last_launches = 0;
     if (B > 0) {
+        // one launch: a block per response, the loss's tree in the last block to finish
         lp::rz_seq_kernel<<<static_cast<unsigned>(B), lp::kRzThreads, 0, st>>>(p);
         LP_CUDA(cudaGetLastError(), "rz_seq_kernel launch");
-        ++h->last_launches;
+    } else {
+        lp::rz_final_kernel<<<1, 1024, 0, st>>>(h->blk_sum, h->blk_cnt, 0, out_loss, out_n_kept);
+        LP_CUDA(cudaGetLastError(), "rz_final_kernel launch");
     }
-    lp::rz_final_kernel<<<1, 1024, 0, st>>>(h->blk_sum, h->blk_cnt, static_cast<int>(B), out_loss,
-                                            out_n_kept);
-    LP_CUDA(cudaGetLastError(), "rz_final_kernel launch");
     ++h->last_launches;
     return LP_OK;
 }

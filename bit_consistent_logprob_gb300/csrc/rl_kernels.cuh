@@ -1,16 +1,20 @@
 // Epilogues of the RL step that consume per-token logprobs.
 //
-//  stats_block_kernel /
-//  stats_final_kernel   acceptance statistics between two logprob vectors: max, mean and
+//  stats_fused_kernel   acceptance statistics between two logprob vectors: max, mean and
 //                       population std of |a - b| and the k3 estimate mean(r - 1 - log r),
 //                       r = e^(a - b), over valid tokens (vLLM blog "Finish RL training
 //                       faster", section 2: acceptance asks max, mean and std of the
-//                       per-token difference to be 0; section 3.2: the k3 estimator).
-//  rz_seq_kernel /
-//  rz_final_kernel      the REINFORCE Zero loss L = -(1/B) sum_i (1/T_i) sum_t A_i w_it with
+//                       per-token difference to be 0; section 3.2: the k3 estimator).  Its
+//                       block partials (stats_block_kernel) and its finish (stats_final_kernel)
+//                       also run separately for the data-parallel path.
+//  is_fused_kernel      importance weights and D3 in one launch: the per-token weights and
+//                       block partials of is_block_kernel, then the last block to finish runs
+//                       is_final_kernel's fixed tree over every block partial (same bits).
+//  rz_seq_kernel        the REINFORCE Zero loss L = -(1/B) sum_i (1/T_i) sum_t A_i w_it with
 //                       group-mean advantages, its gradient with respect to log pi, and the
 //                       TIS / token-gate / sequence-gate options (REINFORCE Zero summary,
-//                       section 4 and results table; vLLM blog, section 1).
+//                       section 4 and results table; vLLM blog, section 1); one block per
+//                       response, the loss's fixed tree in the last block to finish.
 //
 // Per-token sums are double-float (fp32 pairs, error-free additions) within a thread and a
 // warp and fp64 above, in a fixed order that depends only on token positions (1024-token
@@ -25,6 +29,109 @@
 namespace lp {
 
 constexpr int kStatusBadOffsets = 4;  // a response's [offs[i], offs[i+1]) is not inside [0, T)
+
+// ---------------------------------------------------------------------- one-launch finishing
+// A kernel whose blocks each publish a partial can finish in its last block: every block
+// fences and counts itself done, and the block that finds it was the last runs the fixed tree
+// over all partials (reading them past L1), then zeroes the counter for the next launch.  The
+// tree and its operands are those of the separate finishing kernels, so the bits are too.
+
+// Thread 0 publishes this block's partials before the call; returns, to every thread, whether
+// this block was the last of num_blocks to finish.
+__device__ __forceinline__ bool finished_last(unsigned* done, int num_blocks, int* flag) {
+    if (threadIdx.x == 0) {
+        __threadfence();
+        *flag = atomicAdd(done, 1u) == static_cast<unsigned>(num_blocks - 1);
+    }
+    __syncthreads();
+    const bool last = *flag != 0;
+    if (last) __threadfence();
+    return last;
+}
+
+// The aligned-chunk, level-wise pairwise fp64 tree of tree_over_partials over n values,
+// computed by one block of kIsThreads threads, each reading its kIsChunk / kIsThreads values of
+// a chunk with all loads in flight.  `chunk` holds kIsChunk and `chunk_res` 1024 doubles of
+// shared memory.  Every thread gets the result.
+__device__ __forceinline__ double last_block_tree(const double* src, int n, double* chunk,
+                                                  double* chunk_res) {
+    constexpr int kPer = kIsChunk / kIsThreads;
+    const int num_chunks = (n + kIsChunk - 1) / kIsChunk;
+    for (int ch = 0; ch < num_chunks; ++ch) {
+        const int lo = ch * kIsChunk;
+        const int len = min(kIsChunk, n - lo);
+        double v[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = static_cast<int>(threadIdx.x) + k * kIsThreads;
+            v[k] = i < len ? __ldcg(src + lo + i) : 0.0;
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = static_cast<int>(threadIdx.x) + k * kIsThreads;
+            if (i < len) chunk[i] = v[k];
+        }
+        __syncthreads();
+        block_tree_f64(chunk, len);
+        if (threadIdx.x == 0) chunk_res[ch] = chunk[0];
+        __syncthreads();
+    }
+    if (num_chunks > 0) block_tree_f64(chunk_res, num_chunks);
+    __syncthreads();
+    const double r = num_chunks > 0 ? chunk_res[0] : 0.0;
+    __syncthreads();
+    return r;
+}
+
+// Sum of n counts (integer adds, any order) by one block of kIsThreads threads.
+__device__ __forceinline__ long long last_block_count(const long long* src, int n,
+                                                      long long* part) {
+    long long c = 0;
+    for (int i = threadIdx.x; i < n; i += kIsThreads) c += __ldcg(src + i);
+    part[threadIdx.x] = c;
+    __syncthreads();
+    for (int k = kIsThreads >> 1; k >= 1; k >>= 1) {
+        if (threadIdx.x < k) part[threadIdx.x] += part[threadIdx.x + k];
+        __syncthreads();
+    }
+    const long long r = part[0];
+    __syncthreads();
+    return r;
+}
+
+// Whether four consecutive elements starting at p can move as one 16-byte (or, for bytes,
+// 4-byte) access.
+template <typename T>
+__device__ __forceinline__ bool aligned_x4(const T* p) {
+    return (reinterpret_cast<uintptr_t>(p) & (4 * sizeof(T) - 1)) == 0;
+}
+
+// Thread j of a 1024-token block reads tokens t0 .. t0 + 3 (t0 = block * 1024 + 4 j): a = log pi
+// (or the first logprob), b = log mu (or the second), valid = inside [0, T) and unmasked.  One
+// vector load per input when the four are inside T and the pointers are aligned.
+__device__ __forceinline__ void load_token_quad(const float* pa, const float* pb,
+                                                const uint8_t* mask, int64_t T, int64_t t0,
+                                                float (&a)[4], float (&b)[4], bool (&valid)[4],
+                                                bool& vec) {
+    vec = t0 + 3 < T && aligned_x4(pa) && aligned_x4(pb) && (mask == nullptr || aligned_x4(mask));
+    if (vec) {
+        const float4 va = *reinterpret_cast<const float4*>(pa + t0);
+        const float4 vb = *reinterpret_cast<const float4*>(pb + t0);
+        a[0] = va.x; a[1] = va.y; a[2] = va.z; a[3] = va.w;
+        b[0] = vb.x; b[1] = vb.y; b[2] = vb.z; b[3] = vb.w;
+        const uint32_t m = mask ? *reinterpret_cast<const uint32_t*>(mask + t0) : 0x01010101u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) valid[i] = ((m >> (8 * i)) & 0xffu) != 0;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t t = t0 + i;
+            a[i] = t < T ? pa[t] : 0.0f;
+            b[i] = t < T ? pb[t] : 0.0f;
+            valid[i] = t < T && (mask == nullptr || mask[t] != 0);
+        }
+    }
+}
 
 // ---------------------------------------------------------------------- acceptance statistics
 struct StatsParams {
@@ -45,20 +152,20 @@ __device__ __forceinline__ float nan_max(float m, float x) { return (x > m || x 
 // Per block of 1024 tokens (4 per thread, in order): three double-float sums reduced exactly
 // like the D3 block sum (is_block_kernel), so the k3 partials are bit-equal to the D3 partials
 // of the same tokens; |d|^2 enters exactly (an fma recovers the product's rounding error);
-// max and count are exact in any order.
-static __global__ void __launch_bounds__(kIsThreads) stats_block_kernel(const StatsParams p) {
-    __shared__ double s_w[8];
-    __shared__ float s_max[8];
-    __shared__ long long s_cnt[8];
+// max and count are exact in any order.  Thread 0 writes the block's partials.
+__device__ __forceinline__ void stats_block_body(const StatsParams& p, double* s_w, float* s_max,
+                                                 long long* s_cnt) {
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kIsBlock + threadIdx.x * 4;
+    float a[4], b[4];
+    bool valid[4], vec;
+    load_token_quad(p.a, p.b, p.mask, p.T, t0, a, b, valid, vec);
     df32 acc_abs{0.0f, 0.0f}, acc_sq{0.0f, 0.0f}, acc_k3{0.0f, 0.0f};
     float mx = 0.0f;
     long long cnt = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int64_t t = t0 + i;
-        if (t < p.T && (p.mask == nullptr || p.mask[t] != 0)) {
-            const float d = __fsub_rn(p.a[t], p.b[t]);
+        if (valid[i]) {
+            const float d = __fsub_rn(a[i], b[i]);
             const float x = fabsf(d);
             acc_abs = df_add(acc_abs, x);
             acc_sq = df_add(acc_sq, square_exact(x));
@@ -96,6 +203,64 @@ static __global__ void __launch_bounds__(kIsThreads) stats_block_kernel(const St
     }
 }
 
+static __global__ void __launch_bounds__(kIsThreads) stats_block_kernel(const StatsParams p) {
+    __shared__ double s_w[8];
+    __shared__ float s_max[8];
+    __shared__ long long s_cnt[8];
+    stats_block_body(p, s_w, s_max, s_cnt);
+}
+
+// The statistics of stats_final_kernel from n_valid and the three sums.
+__device__ __forceinline__ void stats_finish(double mx, long long n, double s_abs, double s_sq,
+                                             double s_k3, double* out) {
+    if (n == 0) {
+        for (int i = 0; i < 5; ++i) out[i] = 0.0;
+    } else {
+        const double nd = static_cast<double>(n);
+        const double mean = __ddiv_rn(s_abs, nd);
+        const double var = __dsub_rn(__ddiv_rn(s_sq, nd), __dmul_rn(mean, mean));
+        out[0] = mx;
+        out[1] = mean;
+        out[2] = var > 0.0 ? __dsqrt_rn(var) : (var == var ? 0.0 : var);
+        out[3] = __ddiv_rn(s_k3, nd);
+        out[4] = nd;
+    }
+}
+
+// stats_block_kernel and stats_final_kernel in one launch: every block writes its partials,
+// the last block to finish forms the statistics from all of them (same trees, same bits).
+static __global__ void __launch_bounds__(kIsThreads) stats_fused_kernel(const StatsParams p,
+                                                                       int num_blocks,
+                                                                       unsigned* done,
+                                                                       double* out) {
+    __shared__ double s_w[8];
+    __shared__ float s_max[8];
+    __shared__ long long s_cnt[8];
+    __shared__ int last;
+    stats_block_body(p, s_w, s_max, s_cnt);
+    if (!finished_last(done, num_blocks, &last)) return;
+    __shared__ double chunk[kIsChunk];
+    __shared__ double chunk_res[1024];
+    __shared__ long long cpart[kIsThreads];
+    __shared__ float mpart[kIsThreads];
+    float m = 0.0f;
+    for (int i = threadIdx.x; i < num_blocks; i += kIsThreads) m = nan_max(m, __ldcg(p.blk_max + i));
+    mpart[threadIdx.x] = m;
+    __syncthreads();
+    for (int k = kIsThreads >> 1; k >= 1; k >>= 1) {
+        if (threadIdx.x < k) mpart[threadIdx.x] = nan_max(mpart[threadIdx.x], mpart[threadIdx.x + k]);
+        __syncthreads();
+    }
+    const long long n = last_block_count(p.blk_cnt, num_blocks, cpart);
+    const double s_abs = last_block_tree(p.blk_abs, num_blocks, chunk, chunk_res);
+    const double s_sq = last_block_tree(p.blk_sq, num_blocks, chunk, chunk_res);
+    const double s_k3 = last_block_tree(p.blk_k3, num_blocks, chunk, chunk_res);
+    if (threadIdx.x == 0) {
+        stats_finish(static_cast<double>(mpart[0]), n, s_abs, s_sq, s_k3, out);
+        *done = 0u;
+    }
+}
+
 // One block of 1024: the fixed trees over the block sums, then
 // out[0] = max |d|, out[1] = mean |d|, out[2] = sqrt(max(0, mean d^2 - mean^2)),
 // out[3] = k3, out[4] = n_valid; all zero when n_valid == 0.
@@ -117,19 +282,72 @@ static __global__ void __launch_bounds__(1024) stats_final_kernel(const StatsPar
     const double s_abs = tree_over_partials(p.blk_abs, num_blocks, a, chunk_res);
     const double s_sq = tree_over_partials(p.blk_sq, num_blocks, a, chunk_res);
     const double s_k3 = tree_over_partials(p.blk_k3, num_blocks, a, chunk_res);
-    if (threadIdx.x == 0) {
-        if (n == 0) {
-            for (int i = 0; i < 5; ++i) out[i] = 0.0;
-        } else {
-            const double nd = static_cast<double>(n);
-            const double mean = __ddiv_rn(s_abs, nd);
-            const double var = __dsub_rn(__ddiv_rn(s_sq, nd), __dmul_rn(mean, mean));
-            out[0] = static_cast<double>(max_part[0]);
-            out[1] = mean;
-            out[2] = var > 0.0 ? __dsqrt_rn(var) : (var == var ? 0.0 : var);
-            out[3] = __ddiv_rn(s_k3, nd);
-            out[4] = nd;
+    if (threadIdx.x == 0) stats_finish(static_cast<double>(max_part[0]), n, s_abs, s_sq, s_k3, out);
+}
+
+// ---------------------------------------------------------------------- IS / D3, one launch
+struct IsFusedParams {
+    IsParams is;
+    int num_blocks;          // ceil(T / kIsBlock) >= 1
+    unsigned* done;          // blocks finished; zero at launch, zeroed again by the last block
+    double* out_d3;
+    int64_t* out_nvalid;     // may be null
+};
+
+// Per block of 1024 tokens (thread j takes tokens 4j .. 4j + 3 of the block, in order): w = e^d
+// and the double-float sum of the valid tokens' D3 terms, reduced to the block partial by the
+// lane butterfly and the 8-warp fp64 tree, with the valid count: the arithmetic of
+// is_block_kernel, operation for operation (full groups of four move as one vector load of
+// each input and one vector store of w).  The last block to finish then sums every block
+// partial with is_final_kernel's tree and writes D3 = sum / n_valid.
+static __global__ void __launch_bounds__(kIsThreads) is_fused_kernel(const IsFusedParams q) {
+    const IsParams& p = q.is;
+    __shared__ double wsum[kIsThreads / 32];
+    __shared__ long long wcnt[kIsThreads / 32];
+    __shared__ int last;
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kIsBlock + threadIdx.x * 4;
+    float a[4], b[4];
+    bool valid[4], vec;
+    load_token_quad(p.logp_pi, p.logp_mu, p.mask, p.T, t0, a, b, valid, vec);
+    df32 acc{0.0f, 0.0f};
+    long long cnt = 0;
+    float w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float d = __fsub_rn(a[i], b[i]);
+        w[i] = expf(d);
+        if (valid[i]) {
+            acc = df_add(acc, d3_term(d));
+            ++cnt;
         }
+    }
+    if (vec && aligned_x4(p.out_w)) {
+        *reinterpret_cast<float4*>(p.out_w + t0) = make_float4(w[0], w[1], w[2], w[3]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (t0 + i < p.T) p.out_w[t0 + i] = w[i];
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+    if ((threadIdx.x & 31) == 0) wcnt[threadIdx.x >> 5] = cnt;
+    const double total = block_sum_8warps(acc, wsum);
+    if (threadIdx.x == 0) {
+        long long c = 0;
+        for (int k = 0; k < kIsThreads / 32; ++k) c += wcnt[k];
+        p.blk_sum[blockIdx.x] = total;
+        p.blk_cnt[blockIdx.x] = c;
+    }
+    if (!finished_last(q.done, q.num_blocks, &last)) return;
+    __shared__ double chunk[kIsChunk];
+    __shared__ double chunk_res[1024];
+    __shared__ long long cpart[kIsThreads];
+    const long long n = last_block_count(p.blk_cnt, q.num_blocks, cpart);
+    const double sum = last_block_tree(p.blk_sum, q.num_blocks, chunk, chunk_res);
+    if (threadIdx.x == 0) {
+        *q.out_d3 = n > 0 ? __ddiv_rn(sum, static_cast<double>(n)) : 0.0;
+        if (q.out_nvalid) *q.out_nvalid = n;
+        *q.done = 0u;  // ready for the next call (kernels on the stream run in order)
     }
 }
 
@@ -158,6 +376,9 @@ struct RzParams {
     double* seq_term;        // [B] workspace: A_i * sum_t w_hat / T_i (0 if empty or gated)
     long long* seq_kept;     // [B] workspace: 1 if the response passed the sequence gate
     int* status;
+    unsigned* done;          // responses finished; zero at launch, zeroed again by the last block
+    double* out_loss;
+    int64_t* out_kept;       // may be null
 };
 
 // The token weight before the sequence gate: w = e^d (fp32), the token gate decided on the
@@ -169,16 +390,20 @@ __device__ __forceinline__ float rz_token_weight(const RzParams& p, float d) {
     return w;
 }
 
-// One block per response i.  Pass 1 (thread j takes tokens j, j + 256, ... in order, four
+// One block per response i.  Pass 1 (thread j takes tokens j, j + 256, ... in order, eight
 // loads in flight): the
 // valid-token count, the sequence log-ratio sum d (d exact as a double-float difference of the
 // two fp32 inputs) and sum w_hat, each a double-float sum per thread, reduced by the lane
 // butterfly and the 8-warp fp64 tree.  Then the gate, A_i = R_i - mean of the group's rewards
 // (fp64, in order), and pass 2 writes w_hat and dL/dlog pi = -(A_i / (B T_i)) w_hat per token
-// (the coefficient rounded to fp32 once, then one fp32 product).
+// (the coefficient rounded to fp32 once, then one fp32 product).  The last response block to
+// finish forms the loss L = -(fixed tree over the response terms) / B and the number of
+// responses that passed the sequence gate, as rz_final_kernel does.
 static __global__ void __launch_bounds__(kRzThreads) rz_seq_kernel(const RzParams p) {
+    static_assert(kRzThreads == kIsThreads, "the last-block finish runs on kIsThreads threads");
     __shared__ double s_w[8];
     __shared__ long long s_n[8];
+    __shared__ int last;
     const int64_t i = blockIdx.x;
     int64_t t_begin = p.offs[i], t_end = p.offs[i + 1];
     if (t_begin < 0 || t_end < t_begin || t_end > p.T) {
@@ -187,8 +412,8 @@ static __global__ void __launch_bounds__(kRzThreads) rz_seq_kernel(const RzParam
     }
     df32 lr{0.0f, 0.0f}, ws{0.0f, 0.0f};
     long long n = 0;
-    // four tokens per round: their loads are issued together, then folded in token order
-    constexpr int kU = 4;
+    // eight tokens per round: their loads are issued together, then folded in token order
+    constexpr int kU = 8;
     for (int64_t t0 = t_begin + threadIdx.x; t0 < t_end; t0 += kU * kRzThreads) {
         float a[kU], b[kU];
         bool valid[kU];
@@ -248,10 +473,21 @@ static __global__ void __launch_bounds__(kRzThreads) rz_seq_kernel(const RzParam
         p.seq_kept[i] = keep ? 1 : 0;
         if (p.out_adv) p.out_adv[i] = A;
     }
+    if (!finished_last(p.done, static_cast<int>(p.B), &last)) return;
+    __shared__ double chunk[kIsChunk];
+    __shared__ double chunk_res[1024];
+    __shared__ long long cpart[kIsThreads];
+    const long long kept = last_block_count(p.seq_kept, static_cast<int>(p.B), cpart);
+    const double sum = last_block_tree(p.seq_term, static_cast<int>(p.B), chunk, chunk_res);
+    if (threadIdx.x == 0) {
+        *p.out_loss = __ddiv_rn(-sum, static_cast<double>(p.B));
+        if (p.out_kept) *p.out_kept = kept;
+        *p.done = 0u;
+    }
 }
 
 // One block of 1024: L = -(fixed tree over the response terms) / B, and the number of
-// responses that passed the sequence gate.
+// responses that passed the sequence gate (used for B = 0; rz_seq_kernel finishes B > 0).
 static __global__ void __launch_bounds__(1024) rz_final_kernel(const double* seq_term,
                                                         const long long* seq_kept, int B,
                                                         double* out_loss, int64_t* out_kept) {

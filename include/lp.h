@@ -36,7 +36,10 @@
  * Every call on a handle is asynchronous on the caller's CUDA stream (cudaStream_t
  * passed as void*; NULL = legacy default stream), performs no host synchronisation and
  * no allocation (except lp_init, lp_free, lp_check and the *_host variants, which
- * are documented as synchronous), and can be captured in a CUDA graph.
+ * are documented as synchronous), and can be captured in a CUDA graph.  The calls on one
+ * handle share its device workspace (tile partials, block sums, the block counter of the
+ * one-launch epilogues), so the kernels of two calls on the same handle must not overlap on
+ * the GPU: issue them on one stream, or order their streams.
  *
  * Errors: every function returns an lp_status.  Argument errors are detected on
  * the host and returned before anything is enqueued; lp_last_error() gives a
