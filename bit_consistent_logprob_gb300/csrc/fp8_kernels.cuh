@@ -18,10 +18,12 @@
 //
 //  quant_x_kernel        bf16 rows -> e4m3 rows + per-(row, block) scales
 //  quant_w_kernel        bf16 lm_head -> e4m3 + per-(128 x 128 block) scales
-//  leaf_gemm_fp8_kernel  persistent, warp-specialised: TMA producer warp, MMA warp (one
-//                        128-K block per TMEM buffer, two buffers), 8 epilogue warps that apply
-//                        the block scales, fold the leaves through the tree (TMEM slots L and
-//                        S0, a shared-memory slot S1 for N = 8) and form the tile partials.
+//  leaf_gemm_fp8_kernel  persistent, warp-specialised: TMA producer warp, two MMA warps (one
+//                        128-K block per TMEM buffer, two buffers: one warp issues the even
+//                        blocks into buffer 0, the other the odd blocks into buffer 1), 8
+//                        epilogue warps that apply the block scales, fold the leaves through
+//                        the tree (TMEM slots L and S0, a shared-memory slot S1 for N = 8) and
+//                        form the tile partials.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -41,7 +43,16 @@ constexpr int kF8S1Bytes = kBM * kVT * 4; // shared-memory slot: the second stac
 constexpr uint32_t kIdescF8 = (1u << 4) | ((static_cast<uint32_t>(kVT) >> 3) << 17) |
                               ((static_cast<uint32_t>(kBM) >> 4) << 24);
 
-__host__ __device__ constexpr int kF8NumBars() { return 2 * kF8Stages + 2 * kF8Bufs + 1; }
+// Warp 0 copies, warps 1 and 2 issue the MMAs (block g by warp 1 + g % 2), warps 3-10 are the
+// epilogue.  A block is only 256 tensor cycles; with one issuing warp its waits and commits
+// left the tensor pipe idle between blocks, while two warps cover each other's gaps.
+constexpr int kF8MmaWarps = 2;
+constexpr int kF8FirstEpiWarp = 1 + kF8MmaWarps;
+constexpr int kF8Threads = 32 * (kF8FirstEpiWarp + kEpiWarps);
+static_assert(kF8Bufs == kF8MmaWarps, "each MMA warp owns one TMEM block buffer");
+static_assert(kF8Stages % kF8MmaWarps == 0, "each stage is always used by the same MMA warp");
+
+__host__ __device__ constexpr int kF8NumBars() { return 2 * kF8Stages + 2 * kF8Bufs + kF8MmaWarps; }
 __host__ __device__ constexpr int fp8_smem_bytes() {
     return 1024 + kF8Stages * 2 * kTileBytes + kF8S1Bytes + kF8NumBars() * 8 + 16;
 }
@@ -151,7 +162,7 @@ static __global__ void __launch_bounds__(256) quant_w_kernel(const uint16_t* W, 
 // kModeLseEnt (also the entropy partial) or kModeNode (the tree node z written to p.out).
 // p.leaf_len is in elements (a multiple of 128); p.sx [T][nkb], p.sw [num_vocab_tiles][nkb].
 template <int kMode>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kF8Threads, 1)
     leaf_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmX,
                          const __grid_constant__ CUtensorMap tmW, const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -165,8 +176,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* empty = bars + kF8Stages;
     uint64_t* acc_full = bars + 2 * kF8Stages;
     uint64_t* acc_empty = acc_full + kF8Bufs;
-    uint64_t* drain = acc_empty + kF8Bufs;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* drain = acc_empty + kF8Bufs;  // [kF8MmaWarps]
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + kF8MmaWarps);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -180,7 +191,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], kEpiWarps);
         }
-        mbar_init(drain, 1);
+        for (int m = 0; m < kF8MmaWarps; ++m) mbar_init(&drain[m], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -239,65 +250,50 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                           p.timeout_ns);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer (warp)
-        // One 128-K block per stage: 4 MMAs of K = 32 (32 bytes of each 128-byte row), a fresh
-        // accumulator at the block's first MMA, the block's TMEM buffer handed to the epilogue.
+    } else if (warp < kF8FirstEpiWarp) {
+        // ------------------------------------------------------------ MMA issuers (2 warps)
+        // Block g of this CTA's sequence (tiles in order, 128-K blocks in order within a tile)
+        // is issued by MMA warp g % 2 into TMEM buffer g % 2 from stage g % kF8Stages: 4 MMAs
+        // of K = 32 (32 bytes of each 128-byte row), a fresh accumulator at the block's first
+        // MMA, then the commits that free the stage and hand the buffer to the epilogue.  The
+        // epilogue reads the blocks in order, so nothing about a block depends on which warp
+        // issued it.
+        const uint32_t me = static_cast<uint32_t>(warp - 1);
         const uint64_t descA = sw128_kmajor_desc(smem_u32(sA));
         const uint64_t descB = sw128_kmajor_desc(smem_u32(sB));
         constexpr uint32_t kStageDesc = kTileBytes >> 4;
-        // the next stage's and next buffer's barriers are probed while this block's MMAs run
-        uint32_t stage = 0, phase = 0;
-        uint32_t buf = 0, bphase = 0;
-        uint64_t used = 0;
+        const uint32_t d_tmem = tmem_base + me * kVT;
+        uint64_t g = 0;     // block index in the CTA's sequence
+        uint32_t use = 0;   // blocks this warp has issued (uses of its buffer)
         bool ok = true;
-        bool ready = __all_sync(kFull, mbar_test_wait(&full[0], 0));
-        bool acc_ready = true;  // the first use of each buffer finds it free
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-            for (int kb = 0; ok && kb < nkb_range; ++kb) {
-                if (!acc_ready) {
-                    ok = __all_sync(kFull, mbar_wait(&acc_empty[buf], bphase ^ 1u, abort_flag,
-                                                     p.timeout_ns));
-                    if (!ok) {
-                        if (lane == 0) raise_timeout(p, abort_flag);
-                        break;
-                    }
-                }
-                if (!ready) {
-                    ok = __all_sync(kFull, mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns));
-                    if (!ok) {
-                        if (lane == 0) raise_timeout(p, abort_flag);
-                        break;
-                    }
+            for (int kb = 0; ok && kb < nkb_range; ++kb, ++g) {
+                if ((g % kF8MmaWarps) != me) continue;
+                const uint32_t stage = static_cast<uint32_t>(g % kF8Stages);
+                const uint32_t phase = static_cast<uint32_t>((g / kF8Stages) & 1u);
+                // the buffer's previous block has been read (a fresh barrier passes at once)
+                ok = __all_sync(kFull, mbar_wait(&acc_empty[me], (use & 1u) ^ 1u, abort_flag,
+                                                 p.timeout_ns)) &&
+                     __all_sync(kFull, mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns));
+                if (!ok) {
+                    if (lane == 0) raise_timeout(p, abort_flag);
+                    break;
                 }
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + buf * kVT;
-                const uint64_t a = descA + stage * kStageDesc;
-                const uint64_t b = descB + stage * kStageDesc;
-                umma_f8_block_elect(d_tmem, a, b, kIdescF8, &empty[stage], &acc_full[buf]);
-                ++used;
-                if (++stage == kF8Stages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-                if (++buf == kF8Bufs) {
-                    buf = 0;
-                    bphase ^= 1u;
-                }
-                ready = __all_sync(kFull, mbar_test_wait(&full[stage], phase));
-                acc_ready = used < kF8Bufs ||
-                            __all_sync(kFull, mbar_test_wait(&acc_empty[buf], bphase ^ 1u));
+                umma_f8_block_elect(d_tmem, descA + stage * kStageDesc, descB + stage * kStageDesc,
+                                    kIdescF8, &empty[stage], &acc_full[me]);
+                ++use;
             }
         }
         if (!ok) {
             volatile int never = 0;
-            umma_commit_elect(drain);
-            mbar_wait(drain, 0, &never, p.timeout_ns);
+            umma_commit_elect(&drain[me]);
+            mbar_wait(&drain[me], 0, &never, p.timeout_ns);
         }
     } else {
         // ------------------------------------------------------------ epilogue (8 warps)
-        const int q = warp & 3;
-        const int h = (warp - 2) >> 2;
+        const int q = warp & 3;  // TMEM lane quarter: warp w reaches lanes 32 (w % 4) ..
+        const int h = (warp - kF8FirstEpiWarp) >> 2;
         const int r_in_tile = q * 32 + lane;
         const uint32_t lane_base =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * 64);
@@ -316,8 +312,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int y = p.ids[row];
                 if (y >= 0 && y < p.V) ycol = y - v0;
             }
-            const float* sxr = p.sx + static_cast<int64_t>(row_ok ? row : 0) * nkb;
-            const float* swr = p.sw + static_cast<int64_t>(vt) * nkb;
+            const float* sxr = p.sx + static_cast<int64_t>(row_ok ? row : 0) * nkb + kb0;
+            const float* swr = p.sw + static_cast<int64_t>(vt) * nkb + kb0;
+            // The block scales (this row's activation scale and the tile's weight scale) are
+            // read kSxAhead blocks before they are used: with ~200 KB of shared memory per SM
+            // they do not stay in L1, and a load issued at use would put an L2 round trip into
+            // every block.
+            constexpr int kSxAhead = 3;
+            float sxq[kSxAhead], swq[kSxAhead];
+#pragma unroll
+            for (int i = 0; i < kSxAhead; ++i) {
+                sxq[i] = i < nkb_range ? sxr[i] : 0.0f;
+                swq[i] = i < nkb_range ? swr[i] : 0.0f;
+            }
+            int bi = 0;  // block index within the tile
             float R[64];
             for (int j = 0; ok && j < n; ++j) {
                 // leaf j: P_j = sum over its blocks of (sx * sw) * B_kb.  The sum starts at -0:
@@ -326,10 +334,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 // the bits of a plain product.
 #pragma unroll
                 for (int k = 0; k < 64; ++k) R[k] = -0.0f;
-                for (int b = 0; b < bpl; ++b, ++g) {
-                    const int kb = kb0 + j * bpl + b;
+                for (int b = 0; b < bpl; ++b, ++g, ++bi) {
                     const uint32_t buf = g % kF8Bufs, use = g / kF8Bufs;
-                    const float s = __fmul_rn(row_ok ? sxr[kb] : 0.0f, swr[kb]);
+                    const float s = __fmul_rn(row_ok ? sxq[0] : 0.0f, swq[0]);
+#pragma unroll
+                    for (int i = 0; i + 1 < kSxAhead; ++i) {
+                        sxq[i] = sxq[i + 1];
+                        swq[i] = swq[i + 1];
+                    }
+                    const bool more = bi + kSxAhead < nkb_range;
+                    sxq[kSxAhead - 1] = more ? sxr[bi + kSxAhead] : 0.0f;
+                    swq[kSxAhead - 1] = more ? swr[bi + kSxAhead] : 0.0f;
                     if (!warp_wait(&acc_full[buf], use & 1u, p, abort_flag)) {
                         ok = false;
                         break;

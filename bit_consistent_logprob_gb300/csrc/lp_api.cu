@@ -486,7 +486,7 @@ int launch_fp8_gemm(lp_handle* h, int rows, int leaf_begin, int leaf_count, cons
     if (tiles > 0x7fffffff) return fail(LP_ERR_UNSUPPORTED, "too many tiles in one launch");
     const int grid = static_cast<int>(tiles < h->num_sms ? tiles : h->num_sms);
     const bool prof = prof_begin(h, st, LP_PROFILE_LEAF_GEMM);
-    lp::leaf_gemm_fp8_kernel<kMode><<<grid, lp::kGemmThreads, lp::fp8_smem_bytes(), st>>>(
+    lp::leaf_gemm_fp8_kernel<kMode><<<grid, lp::kF8Threads, lp::fp8_smem_bytes(), st>>>(
         tmX, h->tmWq, p);
     LP_CUDA(cudaGetLastError(), "leaf_gemm_fp8_kernel launch");
     if (prof) LP_CUDA(prof_end(h, st), "profile event");
