@@ -187,7 +187,9 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- workloads
-def make_workload(name: str, device, seed_offset: int = 0, batch: int = 128):
+def make_workload(name: str, device, seed_offset: int = 0, batch: int = 128, rows: int = 0):
+    """The named workload's inputs; rows > 0 keeps only its first `rows` tokens (a small case
+    of the same shapes, for profiler captures)."""
     import torch
 
     from bit_consistent_logprob_gb300 import inputs
@@ -203,6 +205,14 @@ def make_workload(name: str, device, seed_offset: int = 0, batch: int = 128):
     else:
         T = wl.T
         lengths = [T]
+    if 0 < rows < T:
+        kept, left = [], rows
+        for L in lengths:
+            if left == 0:
+                break
+            kept.append(min(L, left))
+            left -= kept[-1]
+        lengths, T = kept, rows
     X = inputs.hidden_states(T, wl.H, seed, device=device)
     W = inputs.lm_head(wl.V, wl.H, seed, device=device)
     ids = inputs.uniform_ids(T, wl.V, seed, device=device)
@@ -371,7 +381,8 @@ def run_backward(args, world, rank, local, pg):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl, lengths, X, W, ids = make_workload(args.workload, dev, seed_offset=rank, batch=args.batch)
+    wl, lengths, X, W, ids = make_workload(args.workload, dev, seed_offset=rank, batch=args.batch,
+                                           rows=args.rows)
     T, H, V, N = X.shape[0], wl.H, wl.V, wl.n_leaves
     eng = Engine(W, n_leaves=N, max_tokens=min(T, args.max_tokens))
     _, logZ = eng.logprobs(X, ids, return_logZ=True)
@@ -589,7 +600,8 @@ def run_ours(args, world, rank, local, pg):
     assert torch.cuda.is_available(), "bench.py needs a CUDA device"
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl, lengths, X, W, ids = make_workload(args.workload, dev, seed_offset=rank, batch=args.batch)
+    wl, lengths, X, W, ids = make_workload(args.workload, dev, seed_offset=rank, batch=args.batch,
+                                           rows=args.rows)
     T, H, V, N = X.shape[0], wl.H, wl.V, wl.n_leaves
     max_tokens = min(T, args.max_tokens)
     mu = rollout_logprobs(W, X, ids, wl, wl.seed + rank, max_tokens)
@@ -637,7 +649,8 @@ def run_ours(args, world, rank, local, pg):
     key = args.workload + ("_fp8" if args.fp8 else "") + ("_entropy" if args.entropy else "")
     if args.workload == "ds_decode":
         key += f"_b{args.batch}"
-    roof["traffic"] = recorded_traffic(key)
+    # the recorded traffic is for a full-size launch; a --rows case has none
+    roof["traffic"] = recorded_traffic(key) if not args.rows else None
     roof["kernel"] = ("leaf_gemm_fp8_kernel" if args.fp8 else
                       "leaf_gemm_kernel<fused, entropy>" if args.entropy else "leaf_gemm_kernel<fused>")
     roof["timed_region_s"] = timed_s
@@ -679,6 +692,7 @@ def run_ours(args, world, rank, local, pg):
                    "n_seqs": len(lengths), "phase": "decode" if phase == LP_PHASE_DECODE else "prefill",
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
                    "row_chunk": max_tokens,
+                   **({"rows_kept": args.rows} if args.rows else {}),
                    "l2": f"inputs larger than L2 (W {2 * H * V / 1e6:.0f} MB streamed every step)",
                    "step": ("lp_logprobs_entropy" if args.entropy else "lp_logprobs")
                            + " + lp_importance_weights"},
@@ -823,6 +837,9 @@ def parse_args(argv=None):
                     choices=("tiny", "qwen_prefill", "ds_prefill", "ds_decode", "is_d3",
                              "rl_epilogue"))
     ap.add_argument("--batch", type=int, default=128, help="rows of the decode workload")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="keep only the workload's first ROWS tokens (a small case for profiler "
+                         "captures; 0 = the whole workload)")
     ap.add_argument("--max-tokens", type=int, default=32768, help="row chunk of the engine")
     ap.add_argument("--cpu-rows", type=int, default=128, help="rows of the CPU-baseline sample")
     ap.add_argument("--ref-step-seconds", type=float, default=1.5)
