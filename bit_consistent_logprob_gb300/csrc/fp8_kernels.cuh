@@ -236,6 +236,12 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 tma_load_2d_elect(&tmX, &full[stage], sA + stage * kTileBytes, kb * kQBlock, row0);
                 tma_load_2d_elect(&tmW, &full[stage], sB + stage * kTileBytes, kb * kQBlock, v0);
                 ++issued;
+                // test hook: stop as if this warp's own wait had run out (the consumers'
+                // bounded waits then expire and the abort path runs)
+                if (p.test_stop_after > 0 && issued >= uint64_t(p.test_stop_after)) {
+                    ok = false;
+                    break;
+                }
                 if (++stage == kF8Stages) {
                     stage = 0;
                     phase ^= 1u;

@@ -465,6 +465,7 @@ int launch_fp8_gemm(lp_handle* h, int rows, int leaf_begin, int leaf_count, cons
     p.num_vocab_tiles = h->num_vocab_tiles;
     p.num_lse_tiles = h->num_lse_tiles;
     p.band = h->band_fp8;
+    p.test_stop_after = h->test_stop_after;
     p.x_box_rows = static_cast<int32_t>(x_box_rows(rows));
     p.ids = ids;
     p.ws_ms = h->ws_ms;

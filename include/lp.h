@@ -120,7 +120,8 @@ typedef struct lp_handle lp_handle; /* opaque, owned by the library */
  *   LP_WAIT_TIMEOUT_MS=<ms>  bound on every in-kernel wait (default 2000); on expiry the
  *                            sticky status reads LP_ERR_TIMEOUT.
  *   LP_TEST_FAIL_ALLOC=<name> test hook: the named workspace allocation reports failure.
- *   LP_TEST_STOP_AFTER_STAGES=<n> test hook: the bf16 leaf GEMM's copy producer stops after n
+ *   LP_TEST_STOP_AFTER_STAGES=<n> test hook: the leaf GEMM's copy producer (bf16 or
+ *                            block-FP8) stops after n
  *                            pipeline stages, as if its own wait had run out; the other warps'
  *                            bounded waits then expire, the kernel drains and returns, and the
  *                            sticky status reads LP_ERR_TIMEOUT.

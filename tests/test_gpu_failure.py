@@ -78,6 +78,42 @@ def test_leaf_gemm_abort_path_reports_timeout_and_recovers(T, monkeypatch):
     assert_bit_equal(again, ref, "after the abort path ran")
 
 
+def test_fp8_leaf_gemm_abort_path_reports_timeout_and_recovers(monkeypatch):
+    # The block-FP8 kernel issues its MMAs from two warps (alternate 128-K blocks, each with its
+    # own TMEM buffer), and each drains only the MMAs it issued.  With the copy producer stopped
+    # after its first block: that block lands, the first MMA warp issues it and the epilogue
+    # reads it; both MMA warps' waits for their next blocks run out, they raise the abort flag
+    # and drain; the epilogue stops on the flag; the producer's drain finds its copy complete;
+    # TMEM is freed with nothing in flight.  The host reads LP_ERR_TIMEOUT, and afterwards the
+    # context gives the reference bits.
+    dev = require_cuda()
+    T, H, V = 200, 512, 4096
+    X = inputs.hidden_states(T, H, seed=6, device=dev)
+    W = inputs.lm_head(V, H, seed=6, device=dev)
+    ids = inputs.uniform_ids(T, V, seed=6, device=dev)
+    with Engine(W, n_leaves=4, max_tokens=T, fp8=True) as eng:
+        ref = eng.logprobs(X, ids).clone()
+        eng.check()
+    monkeypatch.setenv("LP_WAIT_TIMEOUT_MS", "50")
+    monkeypatch.setenv("LP_TEST_STOP_AFTER_STAGES", "1")
+    with Engine(W, n_leaves=4, max_tokens=T, fp8=True) as hooked:
+        t0 = time.perf_counter()
+        hooked.logprobs(X, ids)
+        with pytest.raises(LpError) as err:
+            hooked.check()
+        elapsed = time.perf_counter() - t0
+        assert err.value.code == LP_ERR_TIMEOUT
+        assert 0.04 < elapsed < 10.0, elapsed
+        hooked.clear_status()
+        hooked.check()
+    monkeypatch.delenv("LP_TEST_STOP_AFTER_STAGES")
+    monkeypatch.delenv("LP_WAIT_TIMEOUT_MS")
+    with Engine(W, n_leaves=4, max_tokens=T, fp8=True) as eng:
+        again = eng.logprobs(X, ids)
+        eng.check()
+    assert_bit_equal(again, ref, "after the FP8 abort path ran")
+
+
 def test_bad_id_is_reported_and_isolated():
     dev = require_cuda()
     X = inputs.hidden_states(200, 256, seed=3, device=dev)
