@@ -187,6 +187,17 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- workloads
+def first_rows(lengths, rows: int):
+    """The sequence lengths of the first `rows` tokens of a packed batch (the last one cut)."""
+    kept, left = [], rows
+    for L in lengths:
+        if left == 0:
+            break
+        kept.append(min(L, left))
+        left -= kept[-1]
+    return kept
+
+
 def make_workload(name: str, device, seed_offset: int = 0, batch: int = 128, rows: int = 0):
     """The named workload's inputs; rows > 0 keeps only its first `rows` tokens (a small case
     of the same shapes, for profiler captures)."""
@@ -206,13 +217,7 @@ def make_workload(name: str, device, seed_offset: int = 0, batch: int = 128, row
         T = wl.T
         lengths = [T]
     if 0 < rows < T:
-        kept, left = [], rows
-        for L in lengths:
-            if left == 0:
-                break
-            kept.append(min(L, left))
-            left -= kept[-1]
-        lengths, T = kept, rows
+        lengths, T = first_rows(lengths, rows), rows
     X = inputs.hidden_states(T, wl.H, seed, device=device)
     W = inputs.lm_head(wl.V, wl.H, seed, device=device)
     ids = inputs.uniform_ids(T, wl.V, seed, device=device)

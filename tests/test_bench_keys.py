@@ -57,3 +57,12 @@ def test_traffic_records_are_well_formed(bench):
         assert re.fullmatch(r"[0-9a-f]{16}", rec["kernel_source_sha"]), key
         assert rec["dram_bytes_per_launch"] > 0, key
         assert os.path.exists(os.path.join(ROOT, rec["source"].split(" ")[0])), key
+
+
+def test_first_rows_keeps_a_prefix_of_the_packed_batch(bench):
+    lengths = [300, 500, 200]
+    assert bench.first_rows(lengths, 1000) == [300, 500, 200]
+    assert bench.first_rows(lengths, 800) == [300, 500]
+    assert bench.first_rows(lengths, 650) == [300, 350]
+    assert bench.first_rows(lengths, 1) == [1]
+    assert sum(bench.first_rows(lengths, 777)) == 777
