@@ -49,52 +49,103 @@ __device__ __forceinline__ bool finished_last(unsigned* done, int num_blocks, in
     return last;
 }
 
-// The aligned-chunk, level-wise pairwise fp64 tree of tree_over_partials over n values,
-// computed by one block of kIsThreads threads, each reading its kIsChunk / kIsThreads values of
-// a chunk with all loads in flight.  `chunk` holds kIsChunk and `chunk_res` 1024 doubles of
-// shared memory.  Every thread gets the result.
-__device__ __forceinline__ double last_block_tree(const double* src, int n, double* chunk,
-                                                  double* chunk_res) {
-    constexpr int kPer = kIsChunk / kIsThreads;
+// The level-wise pairwise tree of block_tree_f64 (pairs (2i, 2i + 1), an odd last value
+// carried up a level) is the aligned binary tree over the value indices: node (L, j) is the sum
+// of the values [j 2^L, (j + 1) 2^L) that exist, formed as node (L - 1, 2j) + node (L - 1, 2j + 1),
+// or as node (L - 1, 2j) alone when no value falls in the right half.  The last block of a
+// launch (kIsThreads threads) evaluates each aligned chunk of kIsChunk values in that form:
+// every thread its 8 consecutive values (levels 1-3) in registers, every warp levels 4-8 by a
+// lane butterfly, thread 0 levels 9-11 over the 8 warp results; block_tree_f64 then joins the
+// chunks.  The additions, their operands and their order are those of tree_over_partials, so
+// are the bits, with one barrier per chunk instead of two per level.
+static_assert(kIsChunk == 8 * kIsThreads, "a thread holds 8 consecutive values of a chunk");
+
+// Node (3, t) of a chunk: v[k] is the chunk's value first + k (first = 8 t); `len` values exist.
+__device__ __forceinline__ double tree_levels_1_3(const double (&v)[8], int first, int len) {
+    double n1[4], n2[2];
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+        n1[m] = first + 2 * m + 1 < len ? __dadd_rn(v[2 * m], v[2 * m + 1]) : v[2 * m];
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+        n2[m] = first + 4 * m + 2 < len ? __dadd_rn(n1[2 * m], n1[2 * m + 1]) : n1[2 * m];
+    return first + 4 < len ? __dadd_rn(n2[0], n2[1]) : n2[0];
+}
+
+// Levels 4-8: lane l of warp w enters with node (3, 32 w + l) and every lane leaves with node
+// (8, w).  At distance `off` the lower lane of a pair of groups holds the left child and the
+// upper lane the right one; both form left + right, or take the left child when the right
+// half holds no value.
+__device__ __forceinline__ double tree_levels_4_8(double v, int len) {
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    const int warp_first = static_cast<int>(threadIdx.x >> 5) * 256;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const double o = __shfl_xor_sync(0xffffffffu, v, off);
+        const bool low = (lane & off) == 0;
+        const int right_first = warp_first + 8 * ((lane & ~(2 * off - 1)) + off);
+        if (right_first < len) v = low ? __dadd_rn(v, o) : __dadd_rn(o, v);
+        else if (!low) v = o;
+    }
+    return v;
+}
+
+// Levels 9-11 from r[w] = node (8, w), w < 8.
+__device__ __forceinline__ double tree_levels_9_11(const double* r, int len) {
+    double a[4], b[2];
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+        a[m] = 256 * (2 * m + 1) < len ? __dadd_rn(r[2 * m], r[2 * m + 1]) : r[2 * m];
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+        b[m] = 512 * (2 * m + 1) < len ? __dadd_rn(a[2 * m], a[2 * m + 1]) : a[2 * m];
+    return 1024 < len ? __dadd_rn(b[0], b[1]) : b[0];
+}
+
+// The tree over n <= 2^21 partials (0 for n = 0), by the whole block; `chunk_res` holds 1024
+// and `wres` 8 doubles of shared memory.  Every thread gets the result.
+__device__ __forceinline__ double last_block_tree(const double* src, int n, double* chunk_res,
+                                                  double* wres) {
     const int num_chunks = (n + kIsChunk - 1) / kIsChunk;
+    const int first = 8 * static_cast<int>(threadIdx.x);
     for (int ch = 0; ch < num_chunks; ++ch) {
-        const int lo = ch * kIsChunk;
-        const int len = min(kIsChunk, n - lo);
-        double v[kPer];
+        const double* c = src + static_cast<int64_t>(ch) * kIsChunk;
+        const int len = min(kIsChunk, n - ch * kIsChunk);
+        double v[8];
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int i = static_cast<int>(threadIdx.x) + k * kIsThreads;
-            v[k] = i < len ? __ldcg(src + lo + i) : 0.0;
-        }
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int i = static_cast<int>(threadIdx.x) + k * kIsThreads;
-            if (i < len) chunk[i] = v[k];
-        }
+        for (int k = 0; k < 8; ++k) v[k] = first + k < len ? __ldcg(c + first + k) : 0.0;
+        const double node = tree_levels_4_8(tree_levels_1_3(v, first, len), len);
+        if ((threadIdx.x & 31) == 0) wres[threadIdx.x >> 5] = node;
         __syncthreads();
-        block_tree_f64(chunk, len);
-        if (threadIdx.x == 0) chunk_res[ch] = chunk[0];
+        if (threadIdx.x == 0) chunk_res[ch] = tree_levels_9_11(wres, len);
         __syncthreads();
     }
-    if (num_chunks > 0) block_tree_f64(chunk_res, num_chunks);
-    __syncthreads();
+    if (num_chunks > 1) block_tree_f64(chunk_res, num_chunks);
     const double r = num_chunks > 0 ? chunk_res[0] : 0.0;
     __syncthreads();
     return r;
 }
 
-// Sum of n counts (integer adds, any order) by one block of kIsThreads threads.
+// Sum of n counts (integer adds, any order) by the whole block, each thread reading 8 at a
+// time; `wcnt` holds 8 long longs of shared memory.  Every thread gets the result.
 __device__ __forceinline__ long long last_block_count(const long long* src, int n,
-                                                      long long* part) {
+                                                      long long* wcnt) {
+    const int first = 8 * static_cast<int>(threadIdx.x);
     long long c = 0;
-    for (int i = threadIdx.x; i < n; i += kIsThreads) c += __ldcg(src + i);
-    part[threadIdx.x] = c;
-    __syncthreads();
-    for (int k = kIsThreads >> 1; k >= 1; k >>= 1) {
-        if (threadIdx.x < k) part[threadIdx.x] += part[threadIdx.x + k];
-        __syncthreads();
+    for (int lo = 0; lo < n; lo += kIsChunk) {
+        long long v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = lo + first + k < n ? __ldcg(src + lo + first + k) : 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) c += v[k];
     }
-    const long long r = part[0];
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+    if ((threadIdx.x & 31) == 0) wcnt[threadIdx.x >> 5] = c;
+    __syncthreads();
+    long long r = 0;
+#pragma unroll
+    for (int w = 0; w < kIsThreads / 32; ++w) r += wcnt[w];
     __syncthreads();
     return r;
 }
@@ -149,6 +200,57 @@ struct StatsParams {
 // max that keeps a NaN once seen (fmaxf would drop it); commutative for every input pair
 __device__ __forceinline__ float nan_max(float m, float x) { return (x > m || x != x) ? x : m; }
 
+// Max of n block maxima by the whole block, each thread reading 8 at a time; `wmax` holds 8
+// floats of shared memory.  Every GPU-computed NaN has the same bits, so any order gives the
+// same result.  Every thread gets it.
+__device__ __forceinline__ float last_block_max(const float* src, int n, float* wmax) {
+    const int first = 8 * static_cast<int>(threadIdx.x);
+    float m = 0.0f;
+    for (int lo = 0; lo < n; lo += kIsChunk) {
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = lo + first + k < n ? __ldcg(src + lo + first + k) : 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m = nan_max(m, v[k]);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) m = nan_max(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+    __syncthreads();
+    float r = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kIsThreads / 32; ++w) r = nan_max(r, wmax[w]);
+    __syncthreads();
+    return r;
+}
+
+// The pairwise fp64 tree of block_sum_8warps over 8 warp results.
+__device__ __forceinline__ double sum8_f64(const double* s) {
+    const double s01 = __dadd_rn(s[0], s[1]), s23 = __dadd_rn(s[2], s[3]);
+    const double s45 = __dadd_rn(s[4], s[5]), s67 = __dadd_rn(s[6], s[7]);
+    return __dadd_rn(__dadd_rn(s01, s23), __dadd_rn(s45, s67));
+}
+
+// Three block sums at once, each with block_sum_8warps' arithmetic: the lane butterfly of
+// each (warp_sum_df), one barrier for all three, then the 8-warp tree of each.  `s_w` holds
+// 24 doubles.
+__device__ __forceinline__ void block_sum3_8warps(df32 a, df32 b, df32 c, double* s_w,
+                                                  double& ra, double& rb, double& rc) {
+    a = warp_sum_df(a);
+    b = warp_sum_df(b);
+    c = warp_sum_df(c);
+    const int w = static_cast<int>(threadIdx.x >> 5);
+    if ((threadIdx.x & 31) == 0) {
+        s_w[w] = df_to_f64(a);
+        s_w[8 + w] = df_to_f64(b);
+        s_w[16 + w] = df_to_f64(c);
+    }
+    __syncthreads();
+    ra = sum8_f64(s_w);
+    rb = sum8_f64(s_w + 8);
+    rc = sum8_f64(s_w + 16);
+}
+
 // Per block of 1024 tokens (4 per thread, in order): three double-float sums reduced exactly
 // like the D3 block sum (is_block_kernel), so the k3 partials are bit-equal to the D3 partials
 // of the same tokens; |d|^2 enters exactly (an fma recovers the product's rounding error);
@@ -183,11 +285,8 @@ __device__ __forceinline__ void stats_block_body(const StatsParams& p, double* s
         s_max[threadIdx.x >> 5] = mx;
         s_cnt[threadIdx.x >> 5] = cnt;
     }
-    const double sum_abs = block_sum_8warps(acc_abs, s_w);
-    __syncthreads();
-    const double sum_sq = block_sum_8warps(acc_sq, s_w);
-    __syncthreads();
-    const double sum_k3 = block_sum_8warps(acc_k3, s_w);
+    double sum_abs, sum_sq, sum_k3;
+    block_sum3_8warps(acc_abs, acc_sq, acc_k3, s_w, sum_abs, sum_sq, sum_k3);
     if (threadIdx.x == 0) {
         p.blk_abs[blockIdx.x] = sum_abs;
         p.blk_sq[blockIdx.x] = sum_sq;
@@ -204,7 +303,7 @@ __device__ __forceinline__ void stats_block_body(const StatsParams& p, double* s
 }
 
 static __global__ void __launch_bounds__(kIsThreads) stats_block_kernel(const StatsParams p) {
-    __shared__ double s_w[8];
+    __shared__ double s_w[24];
     __shared__ float s_max[8];
     __shared__ long long s_cnt[8];
     stats_block_body(p, s_w, s_max, s_cnt);
@@ -229,34 +328,25 @@ __device__ __forceinline__ void stats_finish(double mx, long long n, double s_ab
 
 // stats_block_kernel and stats_final_kernel in one launch: every block writes its partials,
 // the last block to finish forms the statistics from all of them (same trees, same bits).
-static __global__ void __launch_bounds__(kIsThreads) stats_fused_kernel(const StatsParams p,
+static __global__ void __launch_bounds__(kIsThreads, 8) stats_fused_kernel(const StatsParams p,
                                                                        int num_blocks,
                                                                        unsigned* done,
                                                                        double* out) {
-    __shared__ double s_w[8];
+    __shared__ double s_w[24];
     __shared__ float s_max[8];
     __shared__ long long s_cnt[8];
     __shared__ int last;
     stats_block_body(p, s_w, s_max, s_cnt);
     if (!finished_last(done, num_blocks, &last)) return;
-    __shared__ double chunk[kIsChunk];
+    // the block's own scratch is free again (finished_last synchronised the block)
     __shared__ double chunk_res[1024];
-    __shared__ long long cpart[kIsThreads];
-    __shared__ float mpart[kIsThreads];
-    float m = 0.0f;
-    for (int i = threadIdx.x; i < num_blocks; i += kIsThreads) m = nan_max(m, __ldcg(p.blk_max + i));
-    mpart[threadIdx.x] = m;
-    __syncthreads();
-    for (int k = kIsThreads >> 1; k >= 1; k >>= 1) {
-        if (threadIdx.x < k) mpart[threadIdx.x] = nan_max(mpart[threadIdx.x], mpart[threadIdx.x + k]);
-        __syncthreads();
-    }
-    const long long n = last_block_count(p.blk_cnt, num_blocks, cpart);
-    const double s_abs = last_block_tree(p.blk_abs, num_blocks, chunk, chunk_res);
-    const double s_sq = last_block_tree(p.blk_sq, num_blocks, chunk, chunk_res);
-    const double s_k3 = last_block_tree(p.blk_k3, num_blocks, chunk, chunk_res);
+    const float mx = last_block_max(p.blk_max, num_blocks, s_max);
+    const long long n = last_block_count(p.blk_cnt, num_blocks, s_cnt);
+    const double s_abs = last_block_tree(p.blk_abs, num_blocks, chunk_res, s_w);
+    const double s_sq = last_block_tree(p.blk_sq, num_blocks, chunk_res, s_w);
+    const double s_k3 = last_block_tree(p.blk_k3, num_blocks, chunk_res, s_w);
     if (threadIdx.x == 0) {
-        stats_finish(static_cast<double>(mpart[0]), n, s_abs, s_sq, s_k3, out);
+        stats_finish(static_cast<double>(mx), n, s_abs, s_sq, s_k3, out);
         *done = 0u;
     }
 }
@@ -300,7 +390,7 @@ struct IsFusedParams {
 // is_block_kernel, operation for operation (full groups of four move as one vector load of
 // each input and one vector store of w).  The last block to finish then sums every block
 // partial with is_final_kernel's tree and writes D3 = sum / n_valid.
-static __global__ void __launch_bounds__(kIsThreads) is_fused_kernel(const IsFusedParams q) {
+static __global__ void __launch_bounds__(kIsThreads, 8) is_fused_kernel(const IsFusedParams q) {
     const IsParams& p = q.is;
     __shared__ double wsum[kIsThreads / 32];
     __shared__ long long wcnt[kIsThreads / 32];
@@ -339,11 +429,10 @@ static __global__ void __launch_bounds__(kIsThreads) is_fused_kernel(const IsFus
         p.blk_cnt[blockIdx.x] = c;
     }
     if (!finished_last(q.done, q.num_blocks, &last)) return;
-    __shared__ double chunk[kIsChunk];
+    // the block's own scratch is free again (finished_last synchronised the block)
     __shared__ double chunk_res[1024];
-    __shared__ long long cpart[kIsThreads];
-    const long long n = last_block_count(p.blk_cnt, q.num_blocks, cpart);
-    const double sum = last_block_tree(p.blk_sum, q.num_blocks, chunk, chunk_res);
+    const long long n = last_block_count(p.blk_cnt, q.num_blocks, wcnt);
+    const double sum = last_block_tree(p.blk_sum, q.num_blocks, chunk_res, wsum);
     if (threadIdx.x == 0) {
         *q.out_d3 = n > 0 ? __ddiv_rn(sum, static_cast<double>(n)) : 0.0;
         if (q.out_nvalid) *q.out_nvalid = n;
@@ -474,11 +563,11 @@ static __global__ void __launch_bounds__(kRzThreads) rz_seq_kernel(const RzParam
         if (p.out_adv) p.out_adv[i] = A;
     }
     if (!finished_last(p.done, static_cast<int>(p.B), &last)) return;
-    __shared__ double chunk[kIsChunk];
     __shared__ double chunk_res[1024];
-    __shared__ long long cpart[kIsThreads];
-    const long long kept = last_block_count(p.seq_kept, static_cast<int>(p.B), cpart);
-    const double sum = last_block_tree(p.seq_term, static_cast<int>(p.B), chunk, chunk_res);
+    __shared__ double wres[kIsThreads / 32];
+    __shared__ long long wkept[kIsThreads / 32];
+    const long long kept = last_block_count(p.seq_kept, static_cast<int>(p.B), wkept);
+    const double sum = last_block_tree(p.seq_term, static_cast<int>(p.B), chunk_res, wres);
     if (threadIdx.x == 0) {
         *p.out_loss = __ddiv_rn(-sum, static_cast<double>(p.B));
         if (p.out_kept) *p.out_kept = kept;
