@@ -479,7 +479,7 @@ __device__ __forceinline__ float rz_token_weight(const RzParams& p, float d) {
     return w;
 }
 
-// One block per response i.  Pass 1 (thread j takes tokens j, j + 256, ... in order, eight
+// One block per response i.  Pass 1 (thread j takes tokens j, j + 256, ... in order, sixteen
 // loads in flight): the
 // valid-token count, the sequence log-ratio sum d (d exact as a double-float difference of the
 // two fp32 inputs) and sum w_hat, each a double-float sum per thread, reduced by the lane
@@ -488,7 +488,7 @@ __device__ __forceinline__ float rz_token_weight(const RzParams& p, float d) {
 // (the coefficient rounded to fp32 once, then one fp32 product).  The last response block to
 // finish forms the loss L = -(fixed tree over the response terms) / B and the number of
 // responses that passed the sequence gate, as rz_final_kernel does.
-static __global__ void __launch_bounds__(kRzThreads) rz_seq_kernel(const RzParams p) {
+static __global__ void __launch_bounds__(kRzThreads, 4) rz_seq_kernel(const RzParams p) {
     static_assert(kRzThreads == kIsThreads, "the last-block finish runs on kIsThreads threads");
     __shared__ double s_w[8];
     __shared__ long long s_n[8];
@@ -501,8 +501,9 @@ static __global__ void __launch_bounds__(kRzThreads) rz_seq_kernel(const RzParam
     }
     df32 lr{0.0f, 0.0f}, ws{0.0f, 0.0f};
     long long n = 0;
-    // eight tokens per round: their loads are issued together, then folded in token order
-    constexpr int kU = 8;
+    // sixteen tokens per round: their loads are issued together, then folded in token order
+    // (64 registers: four blocks per SM, so all 512 responses of a 2 M-token batch are resident)
+    constexpr int kU = 16;
     for (int64_t t0 = t_begin + threadIdx.x; t0 < t_end; t0 += kU * kRzThreads) {
         float a[kU], b[kU];
         bool valid[kU];
