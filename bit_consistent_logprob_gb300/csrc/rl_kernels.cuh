@@ -231,24 +231,13 @@ __device__ __forceinline__ double sum8_f64(const double* s) {
     return __dadd_rn(__dadd_rn(s01, s23), __dadd_rn(s45, s67));
 }
 
-// Three block sums at once, each with block_sum_8warps' arithmetic: the lane butterfly of
-// each (warp_sum_df), one barrier for all three, then the 8-warp tree of each.  `s_w` holds
-// 24 doubles.
-__device__ __forceinline__ void block_sum3_8warps(df32 a, df32 b, df32 c, double* s_w,
-                                                  double& ra, double& rb, double& rc) {
-    a = warp_sum_df(a);
-    b = warp_sum_df(b);
-    c = warp_sum_df(c);
-    const int w = static_cast<int>(threadIdx.x >> 5);
-    if ((threadIdx.x & 31) == 0) {
-        s_w[w] = df_to_f64(a);
-        s_w[8 + w] = df_to_f64(b);
-        s_w[16 + w] = df_to_f64(c);
-    }
-    __syncthreads();
-    ra = sum8_f64(s_w);
-    rb = sum8_f64(s_w + 8);
-    rc = sum8_f64(s_w + 16);
+// The fp64 pipe of a GB300 SM completes only a few operations per clock, so the 8-warp fp64
+// trees of the block sums (block_sum_8warps' arithmetic) run in thread 0 alone, the only
+// thread that uses them: every warp runs its lane butterflies (fp32 pairs) and lane 0 widens
+// the warp's sum to fp64 into shared memory, then one barrier.
+__device__ __forceinline__ void warp_sums_to_shared(df32 v, double* s_w) {
+    v = warp_sum_df(v);
+    if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = df_to_f64(v);
 }
 
 // Per block of 1024 tokens (4 per thread, in order): three double-float sums reduced exactly
@@ -285,12 +274,14 @@ __device__ __forceinline__ void stats_block_body(const StatsParams& p, double* s
         s_max[threadIdx.x >> 5] = mx;
         s_cnt[threadIdx.x >> 5] = cnt;
     }
-    double sum_abs, sum_sq, sum_k3;
-    block_sum3_8warps(acc_abs, acc_sq, acc_k3, s_w, sum_abs, sum_sq, sum_k3);
+    warp_sums_to_shared(acc_abs, s_w);
+    warp_sums_to_shared(acc_sq, s_w + 8);
+    warp_sums_to_shared(acc_k3, s_w + 16);
+    __syncthreads();
     if (threadIdx.x == 0) {
-        p.blk_abs[blockIdx.x] = sum_abs;
-        p.blk_sq[blockIdx.x] = sum_sq;
-        p.blk_k3[blockIdx.x] = sum_k3;
+        p.blk_abs[blockIdx.x] = sum8_f64(s_w);
+        p.blk_sq[blockIdx.x] = sum8_f64(s_w + 8);
+        p.blk_k3[blockIdx.x] = sum8_f64(s_w + 16);
         float m = 0.0f;
         long long c = 0;
         for (int w = 0; w < 8; ++w) {
@@ -421,11 +412,12 @@ static __global__ void __launch_bounds__(kIsThreads, 8) is_fused_kernel(const Is
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
     if ((threadIdx.x & 31) == 0) wcnt[threadIdx.x >> 5] = cnt;
-    const double total = block_sum_8warps(acc, wsum);
+    warp_sums_to_shared(acc, wsum);
+    __syncthreads();
     if (threadIdx.x == 0) {
         long long c = 0;
         for (int k = 0; k < kIsThreads / 32; ++k) c += wcnt[k];
-        p.blk_sum[blockIdx.x] = total;
+        p.blk_sum[blockIdx.x] = sum8_f64(wsum);
         p.blk_cnt[blockIdx.x] = c;
     }
     if (!finished_last(q.done, q.num_blocks, &last)) return;
@@ -490,8 +482,10 @@ __device__ __forceinline__ float rz_token_weight(const RzParams& p, float d) {
 // responses that passed the sequence gate, as rz_final_kernel does.
 static __global__ void __launch_bounds__(kRzThreads, 4) rz_seq_kernel(const RzParams p) {
     static_assert(kRzThreads == kIsThreads, "the last-block finish runs on kIsThreads threads");
-    __shared__ double s_w[8];
+    __shared__ double s_w[16];
     __shared__ long long s_n[8];
+    __shared__ float s_coef;
+    __shared__ int s_keep;
     __shared__ int last;
     const int64_t i = blockIdx.x;
     int64_t t_begin = p.offs[i], t_end = p.offs[i + 1];
@@ -525,20 +519,33 @@ static __global__ void __launch_bounds__(kRzThreads, 4) rz_seq_kernel(const RzPa
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
     if ((threadIdx.x & 31) == 0) s_n[threadIdx.x >> 5] = n;
-    const double lrd = block_sum_8warps(lr, s_w);
+    warp_sums_to_shared(lr, s_w);
+    warp_sums_to_shared(ws, s_w + 8);
     __syncthreads();
-    const double wsd = block_sum_8warps(ws, s_w);
-    n = 0;
-    for (int w = 0; w < 8; ++w) n += s_n[w];
-    const bool keep = !(p.flags & kRzFlagSeqGate) || (lrd >= p.seq_lo && lrd <= p.seq_hi);
-
-    const int64_t g0 = (i / p.G) * p.G;
-    double gsum = 0.0;
-    for (int64_t j = g0; j < g0 + p.G; ++j) gsum = __dadd_rn(gsum, static_cast<double>(p.rewards[j]));
-    const double A = __dsub_rn(static_cast<double>(p.rewards[i]),
-                               __ddiv_rn(gsum, static_cast<double>(p.G)));
-    const double bn = __dmul_rn(static_cast<double>(p.B), static_cast<double>(n));
-    const float coef = (n > 0 && keep) ? __double2float_rn(__ddiv_rn(-A, bn)) : 0.0f;
+    // the response's fp64 scalars in thread 0 alone (the fp64 pipe is narrow): the two sums,
+    // the gate, the advantage, the response term; the gate and the coefficient are broadcast
+    if (threadIdx.x == 0) {
+        const double lrd = sum8_f64(s_w);
+        const double wsd = sum8_f64(s_w + 8);
+        long long nt = 0;
+        for (int w = 0; w < 8; ++w) nt += s_n[w];
+        const bool kp = !(p.flags & kRzFlagSeqGate) || (lrd >= p.seq_lo && lrd <= p.seq_hi);
+        const int64_t g0 = (i / p.G) * p.G;
+        double gsum = 0.0;
+        for (int64_t j = g0; j < g0 + p.G; ++j)
+            gsum = __dadd_rn(gsum, static_cast<double>(p.rewards[j]));
+        const double A = __dsub_rn(static_cast<double>(p.rewards[i]),
+                                   __ddiv_rn(gsum, static_cast<double>(p.G)));
+        const double bn = __dmul_rn(static_cast<double>(p.B), static_cast<double>(nt));
+        s_coef = (nt > 0 && kp) ? __double2float_rn(__ddiv_rn(-A, bn)) : 0.0f;
+        s_keep = kp ? 1 : 0;
+        p.seq_term[i] = (nt > 0 && kp) ? __ddiv_rn(__dmul_rn(A, wsd), static_cast<double>(nt)) : 0.0;
+        p.seq_kept[i] = kp ? 1 : 0;
+        if (p.out_adv) p.out_adv[i] = A;
+    }
+    __syncthreads();
+    const bool keep = s_keep != 0;
+    const float coef = s_coef;
 
     for (int64_t t0 = t_begin + threadIdx.x; t0 < t_end; t0 += kU * kRzThreads) {
         float d[kU];
@@ -557,11 +564,6 @@ static __global__ void __launch_bounds__(kRzThreads, 4) rz_seq_kernel(const RzPa
             if (p.out_w_hat) p.out_w_hat[t] = wh;
             p.out_grad[t] = valid[u] ? __fmul_rn(coef, wh) : 0.0f;
         }
-    }
-    if (threadIdx.x == 0) {
-        p.seq_term[i] = (n > 0 && keep) ? __ddiv_rn(__dmul_rn(A, wsd), static_cast<double>(n)) : 0.0;
-        p.seq_kept[i] = keep ? 1 : 0;
-        if (p.out_adv) p.out_adv[i] = A;
     }
     if (!finished_last(p.done, static_cast<int>(p.B), &last)) return;
     __shared__ double chunk_res[1024];
