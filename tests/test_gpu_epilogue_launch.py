@@ -38,11 +38,14 @@ def responses(T, B, seed, device):
 
 
 def test_sizes_in_a_row_match_the_two_step_path(eng):
-    # 1 and 1024 tokens are one block; 1025 a full block and a one-token block; 2.1 M tokens
-    # are 2051 blocks (more than one chunk of the final tree); the counter must start from
-    # zero in each call whatever the previous call's block count was.
+    # 1 and 1024 tokens are one block; 1025 a full block and a one-token block; 257 blocks
+    # put one value past a warp's 256; 2048 blocks fill one chunk of the final tree exactly,
+    # 2049 and 2051 blocks add a second chunk of one and of three, 4097 blocks make three
+    # chunks (an odd carry among the chunk results); the counter must start from zero in each
+    # call whatever the previous call's block count was.
     dev = require_cuda()
-    for T in (5000, 2_100_000, 1, 1024, 1025, 77_777):
+    for T in (5000, 2_100_000, 1, 1024, 1025, 77_777, 262_145, 2_097_152, 2_097_153,
+              4_194_305):
         lp, lm, mask = inputs.synthetic_is_inputs(T, seed=T, device=dev)
         w, d3, nv = eng.importance_weights(lp, lm, mask)
         w_p, s, c = eng.importance_weights_partials(lp, lm, mask)

@@ -169,6 +169,16 @@ def test_reinforce_zero_at_importance_weight_workload_scale(eng, dev):
     _check_rz(eng, lp, lm, mask, offs, rewards, 8, MODES["all"])
 
 
+@pytest.mark.parametrize("n_groups", [512, 513, 1025])
+def test_reinforce_zero_over_several_chunks_of_responses(eng, dev, n_groups):
+    # 2048, 2052 and 4100 short responses: the last block's tree over the response terms
+    # takes one full chunk of 2048, a second chunk of four, and three chunks
+    lp, lm, mask, offs, rewards = _rz_inputs(n_groups, 4, 1, 40, seed=31 + n_groups, dev=dev)
+    assert rewards.shape[0] == 4 * n_groups
+    _check_rz(eng, lp, lm, mask, offs, rewards, 4, {})
+    _check_rz(eng, lp, lm, mask, offs, rewards, 4, MODES["seq_gate"])
+
+
 def test_reinforce_zero_degenerate_cases(eng, dev):
     # equal policies: w = 1 and group-centred advantages cancel
     lp, _, mask, offs, rewards = _rz_inputs(4, 4, 1, 50, seed=22, dev=dev)
