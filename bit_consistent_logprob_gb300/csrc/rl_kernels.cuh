@@ -224,28 +224,49 @@ __device__ __forceinline__ float last_block_max(const float* src, int n, float* 
     return r;
 }
 
-// The pairwise fp64 tree of block_sum_8warps over 8 warp results.
-__device__ __forceinline__ double sum8_f64(const double* s) {
-    const double s01 = __dadd_rn(s[0], s[1]), s23 = __dadd_rn(s[2], s[3]);
-    const double s45 = __dadd_rn(s[4], s[5]), s67 = __dadd_rn(s[6], s[7]);
-    return __dadd_rn(__dadd_rn(s01, s23), __dadd_rn(s45, s67));
+// Block sums with block_sum_8warps' arithmetic (each warp's lane butterfly of fp32 pairs,
+// the pair widened to fp64, the 8-warp tree ((w0 + w1) + (w2 + w3)) + ((w4 + w5) + (w6 + w7))),
+// for NS sums at once.  The fp64 pipe of a GB300 SM is narrow, and a warp instruction holds it
+// for as long whatever its active lanes, so the fp64 steps run in warp 0 with lane 8s + w
+// holding warp w's value of sum s: one instruction per step for every warp and sum (six in
+// all) instead of a widening in each warp and a tree in one thread.
+template <int NS>
+struct BlockSums {
+    static_assert(NS >= 1 && NS <= 4, "lane 8s + w of one warp per sum s and warp w");
+    float hi[8 * NS], lo[8 * NS];
+};
+
+// Sum s of the calling warp: its lane butterfly, then lane 0 stores the warp's pair.
+template <int NS>
+__device__ __forceinline__ void stage_warp_sum(df32 v, int s, BlockSums<NS>& sh) {
+    v = warp_sum_df(v);
+    if ((threadIdx.x & 31) == 0) {
+        sh.hi[8 * s + (threadIdx.x >> 5)] = v.hi;
+        sh.lo[8 * s + (threadIdx.x >> 5)] = v.lo;
+    }
 }
 
-// The fp64 pipe of a GB300 SM completes only a few operations per clock, so the 8-warp fp64
-// trees of the block sums (block_sum_8warps' arithmetic) run in thread 0 alone, the only
-// thread that uses them: every warp runs its lane butterflies (fp32 pairs) and lane 0 widens
-// the warp's sum to fp64 into shared memory, then one barrier.
-__device__ __forceinline__ void warp_sums_to_shared(df32 v, double* s_w) {
-    v = warp_sum_df(v);
-    if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = df_to_f64(v);
+// After a barrier that follows every stage_warp_sum, called by all lanes of warp 0: sum s ends
+// in lane 8s (other lanes hold partial or unused values).
+template <int NS>
+__device__ __forceinline__ double finish_block_sums(const BlockSums<NS>& sh) {
+    const int l = static_cast<int>(threadIdx.x & 31);
+    double x = 0.0;
+    if (l < 8 * NS) x = __dadd_rn(static_cast<double>(sh.hi[l]), static_cast<double>(sh.lo[l]));
+#pragma unroll
+    for (int off = 1; off <= 4; off <<= 1) {
+        const double y = __shfl_down_sync(0xffffffffu, x, off);
+        if ((l & (2 * off - 1)) == 0 && l < 8 * NS) x = __dadd_rn(x, y);
+    }
+    return x;
 }
 
 // Per block of 1024 tokens (4 per thread, in order): three double-float sums reduced exactly
 // like the D3 block sum (is_block_kernel), so the k3 partials are bit-equal to the D3 partials
 // of the same tokens; |d|^2 enters exactly (an fma recovers the product's rounding error);
 // max and count are exact in any order.  Thread 0 writes the block's partials.
-__device__ __forceinline__ void stats_block_body(const StatsParams& p, double* s_w, float* s_max,
-                                                 long long* s_cnt) {
+__device__ __forceinline__ void stats_block_body(const StatsParams& p, BlockSums<3>& s_w,
+                                                 float* s_max, long long* s_cnt) {
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kIsBlock + threadIdx.x * 4;
     float a[4], b[4];
     bool valid[4], vec;
@@ -274,14 +295,18 @@ __device__ __forceinline__ void stats_block_body(const StatsParams& p, double* s
         s_max[threadIdx.x >> 5] = mx;
         s_cnt[threadIdx.x >> 5] = cnt;
     }
-    warp_sums_to_shared(acc_abs, s_w);
-    warp_sums_to_shared(acc_sq, s_w + 8);
-    warp_sums_to_shared(acc_k3, s_w + 16);
+    stage_warp_sum(acc_abs, 0, s_w);
+    stage_warp_sum(acc_sq, 1, s_w);
+    stage_warp_sum(acc_k3, 2, s_w);
     __syncthreads();
+    if (threadIdx.x >= 32) return;
+    const double x = finish_block_sums(s_w);
+    const double sum_sq = __shfl_sync(0xffffffffu, x, 8);
+    const double sum_k3 = __shfl_sync(0xffffffffu, x, 16);
     if (threadIdx.x == 0) {
-        p.blk_abs[blockIdx.x] = sum8_f64(s_w);
-        p.blk_sq[blockIdx.x] = sum8_f64(s_w + 8);
-        p.blk_k3[blockIdx.x] = sum8_f64(s_w + 16);
+        p.blk_abs[blockIdx.x] = x;
+        p.blk_sq[blockIdx.x] = sum_sq;
+        p.blk_k3[blockIdx.x] = sum_k3;
         float m = 0.0f;
         long long c = 0;
         for (int w = 0; w < 8; ++w) {
@@ -294,7 +319,7 @@ __device__ __forceinline__ void stats_block_body(const StatsParams& p, double* s
 }
 
 static __global__ void __launch_bounds__(kIsThreads) stats_block_kernel(const StatsParams p) {
-    __shared__ double s_w[24];
+    __shared__ BlockSums<3> s_w;
     __shared__ float s_max[8];
     __shared__ long long s_cnt[8];
     stats_block_body(p, s_w, s_max, s_cnt);
@@ -323,7 +348,7 @@ static __global__ void __launch_bounds__(kIsThreads, 8) stats_fused_kernel(const
                                                                        int num_blocks,
                                                                        unsigned* done,
                                                                        double* out) {
-    __shared__ double s_w[24];
+    __shared__ BlockSums<3> s_w;
     __shared__ float s_max[8];
     __shared__ long long s_cnt[8];
     __shared__ int last;
@@ -333,9 +358,10 @@ static __global__ void __launch_bounds__(kIsThreads, 8) stats_fused_kernel(const
     __shared__ double chunk_res[1024];
     const float mx = last_block_max(p.blk_max, num_blocks, s_max);
     const long long n = last_block_count(p.blk_cnt, num_blocks, s_cnt);
-    const double s_abs = last_block_tree(p.blk_abs, num_blocks, chunk_res, s_w);
-    const double s_sq = last_block_tree(p.blk_sq, num_blocks, chunk_res, s_w);
-    const double s_k3 = last_block_tree(p.blk_k3, num_blocks, chunk_res, s_w);
+    __shared__ double wres[kIsThreads / 32];
+    const double s_abs = last_block_tree(p.blk_abs, num_blocks, chunk_res, wres);
+    const double s_sq = last_block_tree(p.blk_sq, num_blocks, chunk_res, wres);
+    const double s_k3 = last_block_tree(p.blk_k3, num_blocks, chunk_res, wres);
     if (threadIdx.x == 0) {
         stats_finish(static_cast<double>(mx), n, s_abs, s_sq, s_k3, out);
         *done = 0u;
@@ -383,6 +409,7 @@ struct IsFusedParams {
 // partial with is_final_kernel's tree and writes D3 = sum / n_valid.
 static __global__ void __launch_bounds__(kIsThreads, 8) is_fused_kernel(const IsFusedParams q) {
     const IsParams& p = q.is;
+    __shared__ BlockSums<1> bsum;
     __shared__ double wsum[kIsThreads / 32];
     __shared__ long long wcnt[kIsThreads / 32];
     __shared__ int last;
@@ -412,12 +439,13 @@ static __global__ void __launch_bounds__(kIsThreads, 8) is_fused_kernel(const Is
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
     if ((threadIdx.x & 31) == 0) wcnt[threadIdx.x >> 5] = cnt;
-    warp_sums_to_shared(acc, wsum);
+    stage_warp_sum(acc, 0, bsum);
     __syncthreads();
+    const double total = threadIdx.x < 32 ? finish_block_sums(bsum) : 0.0;
     if (threadIdx.x == 0) {
         long long c = 0;
         for (int k = 0; k < kIsThreads / 32; ++k) c += wcnt[k];
-        p.blk_sum[blockIdx.x] = sum8_f64(wsum);
+        p.blk_sum[blockIdx.x] = total;
         p.blk_cnt[blockIdx.x] = c;
     }
     if (!finished_last(q.done, q.num_blocks, &last)) return;
@@ -482,7 +510,7 @@ __device__ __forceinline__ float rz_token_weight(const RzParams& p, float d) {
 // responses that passed the sequence gate, as rz_final_kernel does.
 static __global__ void __launch_bounds__(kRzThreads, 4) rz_seq_kernel(const RzParams p) {
     static_assert(kRzThreads == kIsThreads, "the last-block finish runs on kIsThreads threads");
-    __shared__ double s_w[16];
+    __shared__ BlockSums<2> s_w;
     __shared__ long long s_n[8];
     __shared__ float s_coef;
     __shared__ int s_keep;
@@ -519,14 +547,16 @@ static __global__ void __launch_bounds__(kRzThreads, 4) rz_seq_kernel(const RzPa
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
     if ((threadIdx.x & 31) == 0) s_n[threadIdx.x >> 5] = n;
-    warp_sums_to_shared(lr, s_w);
-    warp_sums_to_shared(ws, s_w + 8);
+    stage_warp_sum(lr, 0, s_w);
+    stage_warp_sum(ws, 1, s_w);
     __syncthreads();
+    const double lr_ws = threadIdx.x < 32 ? finish_block_sums(s_w) : 0.0;
+    const double ws_sum = __shfl_sync(0xffffffffu, lr_ws, 8);  // warp 0's lane 8
     // the response's fp64 scalars in thread 0 alone (the fp64 pipe is narrow): the two sums,
     // the gate, the advantage, the response term; the gate and the coefficient are broadcast
     if (threadIdx.x == 0) {
-        const double lrd = sum8_f64(s_w);
-        const double wsd = sum8_f64(s_w + 8);
+        const double lrd = lr_ws;
+        const double wsd = ws_sum;
         long long nt = 0;
         for (int w = 0; w < 8; ++w) nt += s_n[w];
         const bool kp = !(p.flags & kRzFlagSeqGate) || (lrd >= p.seq_lo && lrd <= p.seq_hi);
