@@ -264,7 +264,8 @@ __device__ __forceinline__ double finish_block_sums(const BlockSums<NS>& sh) {
 // Per block of 1024 tokens (4 per thread, in order): three double-float sums reduced exactly
 // like the D3 block sum (is_block_kernel), so the k3 partials are bit-equal to the D3 partials
 // of the same tokens; |d|^2 enters exactly (an fma recovers the product's rounding error);
-// max and count are exact in any order.  Thread 0 writes the block's partials.
+// max and count are exact in any order.  Thread 0 writes the block's partials.  Warps 1-7
+// return after the block barrier; warp 0 returns once it has formed the fp64 sums.
 __device__ __forceinline__ void stats_block_body(const StatsParams& p, BlockSums<3>& s_w,
                                                  float* s_max, long long* s_cnt) {
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kIsBlock + threadIdx.x * 4;
