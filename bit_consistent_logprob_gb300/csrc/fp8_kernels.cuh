@@ -33,7 +33,7 @@
 namespace lp {
 
 constexpr int kQBlock = 128;              // quantisation block along K (and along V for W)
-constexpr int kF8Stages = 4;              // 128-K pipeline stages: X 16 KB + W 16 KB each
+constexpr int kF8Stages = 5;              // 128-K pipeline stages: X 16 KB + W 16 KB each
 constexpr int kF8Bufs = 2;                // TMEM block accumulators
 constexpr uint32_t kF8ColL = 256;         // TMEM slot: the even leaf waiting for its pair
 constexpr uint32_t kF8ColS0 = 384;        // TMEM slot: the first stack level of the tree
@@ -50,7 +50,13 @@ constexpr int kF8MmaWarps = 2;
 constexpr int kF8FirstEpiWarp = 1 + kF8MmaWarps;
 constexpr int kF8Threads = 32 * (kF8FirstEpiWarp + kEpiWarps);
 static_assert(kF8Bufs == kF8MmaWarps, "each MMA warp owns one TMEM block buffer");
-static_assert(kF8Stages % kF8MmaWarps == 0, "each stage is always used by the same MMA warp");
+// A stage is used by both MMA warps in turn (5 stages, 2 warps).  A warp waits on the stage of
+// block g only after its buffer's previous block g - 2 was released, and the epilogue releases
+// blocks in order, so block g - 5 (the stage's previous use) has been issued and its phase has
+// completed: the parity wait cannot match a stale phase.  Five stages keep 80 KB of W in flight
+// per SM, which a weight stream (decode) needs; 230.5 KB of shared memory in all.
+static_assert(kF8Stages >= kF8MmaWarps,
+              "a stage's previous use must not follow the buffer's previous block");
 
 __host__ __device__ constexpr int kF8NumBars() { return 2 * kF8Stages + 2 * kF8Bufs + kF8MmaWarps; }
 __host__ __device__ constexpr int fp8_smem_bytes() {
